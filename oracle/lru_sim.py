@@ -1,0 +1,148 @@
+"""Independent simulator of the GPU adapter slot table (test infrastructure only).
+
+Semantics, as read from the "Multi-LoRA 适配器缓存生产实战" page:
+
+* section 核心原理 (parameter table): ``max_loras`` bounds how many adapters one
+  batch can use at once, i.e. the number of GPU slots.
+* section 核心原理 (last paragraph): on a hit the adapter is touched (moved to
+  most recent); when capacity is short the new adapter is validated first and
+  then the oldest adapter by LRU is removed; an adapter in use by an executing
+  task is never evicted.
+* section 数据面: per-adapter residency fields (load_count, hit_count,
+  eviction_count, inflight_requests).
+* section 需要重点监控哪些指标, item 3: thrash ratio = reloads within a short
+  window after eviction / total evictions.
+
+Readings where the page is silent: the LRU clock is a counter that advances by
+one on every touch or bind, so no two slots tie; a free slot (lowest index
+first) is used before anything is evicted; the rank is validated before any
+eviction, so a rejected adapter never costs a resident one its slot; the
+thrash window is counted in caller-declared epochs (steps).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+OK = 0
+RANK_ERR = -2
+NO_SLOT = -3
+STATE_ERR = -5
+
+
+@dataclass
+class AdapterRecord:
+    load_count: int = 0
+    hit_count: int = 0
+    eviction_count: int = 0
+    last_evict_epoch: int | None = None
+
+
+class LruSlotSim:
+    def __init__(self, max_loras: int, max_lora_rank: int, thrash_window: int = 10):
+        self.S = max_loras
+        self.R = max_lora_rank
+        self.window = thrash_window
+        self.slot_id: list[int | None] = [None] * max_loras
+        self.last_use = [0] * max_loras
+        self.refs = [0] * max_loras
+        self.clock = 0
+        self.epoch = 0
+        self.where: dict[int, int] = {}
+        self.records: dict[int, AdapterRecord] = {}
+        self.hits = self.misses = self.evictions = self.reloads = self.rejected = 0
+        self.log: list[tuple] = []
+
+    def _touch(self, s: int) -> None:
+        self.clock += 1
+        self.last_use[s] = self.clock
+
+    def _victim(self) -> int | None:
+        best = None
+        for s in range(self.S):
+            if self.slot_id[s] is None or self.refs[s] > 0:
+                continue
+            if best is None or self.last_use[s] < self.last_use[best]:
+                best = s
+        return best
+
+    def _evict(self, s: int) -> int:
+        aid = self.slot_id[s]
+        self.slot_id[s] = None
+        del self.where[aid]
+        self.evictions += 1
+        rec = self.records[aid]
+        rec.eviction_count += 1
+        rec.last_evict_epoch = self.epoch
+        return aid
+
+    def lookup(self, aid: int) -> int:
+        s = self.where.get(aid, -1)
+        if s >= 0:
+            self._touch(s)
+            self.hits += 1
+            self.records[aid].hit_count += 1
+        self.log.append(("lookup", aid, s))
+        return s
+
+    def assign(self, aid: int, rank: int):
+        """Returns (status, slot, needs_load, evicted_id or -1)."""
+        if aid in self.where:
+            s = self.lookup(aid)
+            self.log[-1] = ("assign", aid, OK, s, 0, -1)
+            return OK, s, 0, -1
+        if rank < 1 or rank > self.R:
+            self.rejected += 1
+            self.log.append(("assign", aid, RANK_ERR, -1, 0, -1))
+            return RANK_ERR, -1, 0, -1
+        free = [s for s in range(self.S) if self.slot_id[s] is None]
+        evicted = -1
+        if free:
+            s = free[0]
+        else:
+            s = self._victim()
+            if s is None:
+                self.log.append(("assign", aid, NO_SLOT, -1, 0, -1))
+                return NO_SLOT, -1, 0, -1
+            evicted = self._evict(s)
+        rec = self.records.setdefault(aid, AdapterRecord())
+        if rec.last_evict_epoch is not None and self.epoch - rec.last_evict_epoch <= self.window:
+            self.reloads += 1
+        rec.load_count += 1
+        self.slot_id[s] = aid
+        self.where[aid] = s
+        self.refs[s] = 0
+        self._touch(s)
+        self.misses += 1
+        self.log.append(("assign", aid, OK, s, 1, evicted))
+        return OK, s, 1, evicted
+
+    def acquire(self, s: int) -> int:
+        if not (0 <= s < self.S) or self.slot_id[s] is None:
+            return STATE_ERR
+        self.refs[s] += 1
+        return OK
+
+    def release(self, s: int) -> int:
+        if not (0 <= s < self.S) or self.refs[s] <= 0:
+            return STATE_ERR
+        self.refs[s] -= 1
+        return OK
+
+    def evict_lru(self):
+        """Returns (status, slot or -1, evicted id or -1)."""
+        if all(a is None for a in self.slot_id):
+            self.log.append(("evict", OK, -1, -1))
+            return OK, -1, -1
+        s = self._victim()
+        if s is None:
+            self.log.append(("evict", NO_SLOT, -1, -1))
+            return NO_SLOT, -1, -1
+        aid = self._evict(s)
+        self.log.append(("evict", OK, s, aid))
+        return OK, s, aid
+
+    def tick(self) -> None:
+        self.epoch += 1
+
+    def thrash_ratio(self) -> float:
+        return self.reloads / self.evictions if self.evictions else 0.0

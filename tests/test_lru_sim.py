@@ -1,0 +1,97 @@
+"""Pins for the independent LRU slot-table simulator: scripted sequences whose
+victims are derived by hand from the "Multi-LoRA 适配器缓存生产实战" page
+(section 核心原理: touch on hit, oldest evicted, in-flight adapters never
+evicted; section 为什么纯 LRU 在多租户场景下容易失效: the 4-slot / 20-adapter
+burst)."""
+from oracle.lru_sim import LruSlotSim, OK, NO_SLOT, RANK_ERR, STATE_ERR
+
+
+def test_touch_changes_victim():
+    s = LruSlotSim(2, 16)
+    assert s.assign(10, 4) == (OK, 0, 1, -1)        # free slot 0
+    assert s.assign(11, 4) == (OK, 1, 1, -1)        # free slot 1
+    assert s.lookup(10) == 0                        # hit: 10 becomes most recent
+    assert s.assign(12, 4) == (OK, 1, 1, 11)        # 11 is oldest
+    assert s.assign(13, 4) == (OK, 0, 1, 10)        # 10 (touched before 12 loaded)
+    assert s.hits == 1 and s.misses == 4 and s.evictions == 2
+
+
+def test_hit_does_not_reload():
+    s = LruSlotSim(3, 16)
+    s.assign(1, 8)
+    assert s.assign(1, 8) == (OK, 0, 0, -1)
+    assert s.misses == 1 and s.hits == 1
+
+
+def test_lowest_free_slot_first_after_explicit_evict():
+    s = LruSlotSim(3, 16)
+    for a in (5, 6, 7):
+        s.assign(a, 8)
+    assert s.evict_lru() == (OK, 0, 5)
+    s.lookup(6)
+    assert s.assign(8, 8) == (OK, 0, 1, -1)         # reuses the free slot, evicts nothing
+
+
+def test_in_flight_is_never_evicted():
+    s = LruSlotSim(2, 16)
+    s.assign(1, 4)
+    s.assign(2, 4)
+    assert s.acquire(0) == OK                       # adapter 1 is in flight
+    assert s.assign(3, 4) == (OK, 1, 1, 2)          # 2 evicted although 1 is older
+    assert s.acquire(1) == OK
+    assert s.assign(4, 4) == (NO_SLOT, -1, 0, -1)   # both in flight
+    assert s.evict_lru() == (NO_SLOT, -1, -1)
+    assert s.release(0) == OK
+    assert s.assign(4, 4) == (OK, 0, 1, 1)
+    assert s.release(0) == STATE_ERR                # refcount already zero
+
+
+def test_rank_validated_before_eviction():
+    s = LruSlotSim(2, 16)
+    s.assign(1, 16)
+    s.assign(2, 16)
+    assert s.assign(3, 17) == (RANK_ERR, -1, 0, -1)
+    assert s.assign(3, 0) == (RANK_ERR, -1, 0, -1)
+    assert s.slot_id == [1, 2] and s.evictions == 0 and s.rejected == 2
+
+
+def test_evict_on_empty_table():
+    s = LruSlotSim(4, 16)
+    assert s.evict_lru() == (OK, -1, -1)
+
+
+def test_burst_of_cold_adapters_flushes_hot_set():
+    """4 GPU slots, hot adapters 0..3 in use; a batch tenant then touches 20
+    low-frequency adapters in a row; pure LRU evicts every hot adapter, and the
+    hot set reloads afterwards (4 reloads inside the window)."""
+    s = LruSlotSim(4, 16, thrash_window=10)
+    for rnd in range(3):
+        for a in range(4):
+            s.assign(a, 16)
+        s.tick()
+    assert s.misses == 4 and s.hits == 8
+    evicted = []
+    for a in range(100, 120):
+        st, slot, load, ev = s.assign(a, 16)
+        assert st == OK and load == 1
+        evicted.append(ev)
+    assert evicted[:4] == [0, 1, 2, 3]
+    assert evicted[4:] == list(range(100, 116))
+    s.tick()
+    again = [s.assign(a, 16) for a in range(4)]
+    assert [g[3] for g in again] == [116, 117, 118, 119]
+    assert all(g[2] == 1 for g in again)
+    assert s.evictions == 24 and s.reloads == 4
+    assert abs(s.thrash_ratio() - 4 / 24) < 1e-15
+
+
+def test_reload_outside_window_is_not_thrash():
+    s = LruSlotSim(1, 16, thrash_window=2)
+    s.assign(1, 8)
+    s.assign(2, 8)          # evicts 1 at epoch 0
+    for _ in range(3):
+        s.tick()
+    s.assign(1, 8)          # epoch 3: 3 > window
+    assert s.reloads == 0
+    s.assign(2, 8)          # 2 evicted at epoch 3, reloaded at epoch 3
+    assert s.reloads == 1
