@@ -1,0 +1,223 @@
+/*
+ * rank_adapter_apply -- multi-LoRA delta and GPU adapter slot table, GB300.
+ *
+ * For every token t of a batch and every injected linear layer l:
+ *
+ *     y_l[t] += (lora_alpha_s / r_s) * B_{l,s} * (A_{l,s} * x_l[t]),
+ *     s = token_slot_idx[t];  s == -1 means base model only (y untouched).
+ *
+ * r_s and lora_alpha_s are the adapter's "r" and "lora_alpha" (the PEFT
+ * adapter_config.json example on the "vLLM LoRA Resolver 插件详解" page, section
+ * 3.2, with use_rslora and use_dora false). The slot table follows the
+ * "Multi-LoRA 适配器缓存生产实战" page: max_loras GPU slots, ranks padded to
+ * max_lora_rank (section 核心原理, parameter table); CPU-resident adapters are
+ * uploaded host-to-device on a miss (section 冷加载延迟, tier L1); eviction is
+ * LRU with touch on hit and never removes an adapter in use (section 核心原理,
+ * last paragraph; section 数据面).
+ *
+ * Conventions for every call:
+ *  - All functions return LORA_OK (0) or a negative lora_status; none throws,
+ *    aborts or exits. lora_last_error() gives a message for the calling thread.
+ *  - Device memory (slot pools, scale/rank arrays, workspace, activations) is
+ *    allocated and owned by the caller. The library owns host bookkeeping and
+ *    CUDA events only.
+ *  - Streams are passed as cudaStream_t cast to void*. Kernels run on the
+ *    compute stream; slot uploads on the upload stream. No call synchronises
+ *    the host except lora_sync_uploads and lora_stats.
+ *  - Layouts are row-major. A pool of layer l: [max_loras][max_lora_rank][d_in];
+ *    B pool: [max_loras][d_out][max_lora_rank]; element type = the context's
+ *    dtype. Activations x: [n_tokens][d_in]; outputs y: [n_tokens][d_out].
+ *  - A context is not thread-safe: one host thread at a time.
+ */
+#ifndef RANK_ADAPTER_APPLY_H
+#define RANK_ADAPTER_APPLY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct lora_ctx lora_ctx;
+
+enum lora_status {
+    LORA_OK = 0,
+    LORA_ERR_ARG = -1,      /* bad pointer, size, index or layout */
+    LORA_ERR_RANK = -2,     /* r > max_lora_rank ("LoRA rank exceeds maximum",
+                               "vLLM LoRA Resolver 插件详解" page, section 6.1 item 4) */
+    LORA_ERR_NO_SLOT = -3,  /* every occupied slot is in flight, nothing evictable */
+    LORA_ERR_CUDA = -4,     /* a CUDA runtime call failed (message has the detail) */
+    LORA_ERR_STATE = -5,    /* call not valid in the current state */
+};
+
+enum lora_dtype {
+    LORA_DTYPE_F32 = 0,     /* fp32 activations, weights and fp32 arithmetic */
+    LORA_DTYPE_BF16 = 1,    /* bf16 storage, fp32 accumulation, one final rounding */
+};
+
+/* One injected linear layer: its shapes and its caller-owned device slot pools. */
+typedef struct {
+    int d_in;
+    int d_out;
+    void *A_pool;           /* device, [max_loras][max_lora_rank][d_in] */
+    void *B_pool;           /* device, [max_loras][d_out][max_lora_rank] */
+} lora_layer_desc;
+
+typedef struct {
+    uint64_t hits;                  /* lookups/assigns that found the adapter resident */
+    uint64_t misses;                /* assigns that bound a new adapter to a slot */
+    uint64_t evictions;             /* adapters removed from a slot */
+    uint64_t reloads_after_eviction;/* misses within thrash_window epochs of that adapter's eviction */
+    uint64_t rejected;              /* assigns refused before any eviction (bad rank) */
+    uint64_t uploads;               /* lora_load_slot calls that queued copies */
+    uint64_t upload_bytes;          /* sum of (d_in + d_out) * r * bytes_per_param per upload */
+    uint64_t invalid_token_index;   /* tokens with index < -1 or >= max_loras (skipped) */
+    double upload_seconds;          /* device time of completed uploads */
+    int64_t epoch;                  /* current epoch (lora_tick) */
+} lora_stats_t;
+
+/*
+ * Bytes of device workspace a context needs. The workspace holds the token
+ * grouping, the fp32 rank-r intermediates and the split reduction partials.
+ * max_tokens bounds n_tokens of every apply call; max_layers_per_call bounds n
+ * of lora_apply_multi (1..8).
+ */
+size_t lora_workspace_bytes(int max_loras, int max_lora_rank, int max_tokens,
+                            int max_layers_per_call);
+
+/*
+ * Create a context. max_loras: 1..256 slots. max_lora_rank: 8..256, a
+ * multiple of 8. dtype: lora_dtype. layers[n_layers]: shapes and pools (d_in,
+ * d_out >= 1). scale_dev / rank_dev: device arrays [max_loras] (fp32 / int32)
+ * that the library writes on every upload or eviction. workspace: device,
+ * lora_workspace_bytes(...) bytes, 256-byte aligned; it is zeroed here (on the
+ * compute stream). compute_stream / upload_stream: caller-owned cudaStream_t.
+ *
+ * n_layers == 0 creates a host-only slot table: no CUDA call is made, and only
+ * lora_lookup/assign/acquire/release/evict_lru/tick/stats may be used. That is
+ * how the slot-table decisions are tested without a GPU.
+ *
+ * On success *out owns host state and CUDA events; free it with lora_destroy.
+ */
+int lora_slots_init(lora_ctx **out, int max_loras, int max_lora_rank, int max_tokens,
+                    int max_layers_per_call, int dtype,
+                    int n_layers, const lora_layer_desc *layers,
+                    float *scale_dev, int32_t *rank_dev,
+                    void *workspace, size_t workspace_bytes,
+                    void *compute_stream, void *upload_stream);
+
+/* Release events and host state. Waits for work the library queued. NULL ok. */
+void lora_destroy(lora_ctx *ctx);
+
+/*
+ * Upload one adapter into slot `slot` (tier L1 of the "Multi-LoRA
+ * 适配器缓存生产实战" page, section 冷加载延迟: CPU hit -> H2D upload).
+ * A_host[l] is [rank][d_in] and B_host[l] is [d_out][rank] for every layer l,
+ * host memory (pinned for a truly asynchronous copy) that the caller keeps
+ * alive and unchanged until the upload completes (lora_sync_uploads, or any
+ * later host sync on the upload stream). Ranks below max_lora_rank are padded
+ * with zeros; scale_dev[slot] = alpha / rank, rank_dev[slot] = rank.
+ * Validation (slot range, 1 <= rank <= max_lora_rank, non-NULL pointers,
+ * finite alpha) happens before anything is queued: a rejected call changes
+ * nothing. The copies wait for compute work already queued (so a slot being
+ * read is never overwritten) and the next apply waits for the copies.
+ */
+int lora_load_slot(lora_ctx *ctx, int slot, const void *const *A_host,
+                   const void *const *B_host, int rank, float alpha);
+
+/*
+ * Apply the delta of one layer: y[t] += scale_s * B_s (A_s x[t]) for the
+ * n_tokens rows of x / y (device). token_slot_idx: device int32 [n_tokens].
+ * Index -1, an index >= max_loras or < -1 (counted in invalid_token_index), or
+ * an empty slot (rank 0) leaves y[t] bit-for-bit unchanged. Stream-ordered on
+ * the compute stream; no host synchronisation. 0 <= n_tokens <= max_tokens.
+ * Rows of x must not alias rows of y.
+ */
+int lora_apply(lora_ctx *ctx, int layer, const void *x, void *y,
+               const int32_t *token_slot_idx, int n_tokens);
+
+/*
+ * Apply n layers (a layer set: q/k/v/o, gate/up/down) that share one token
+ * batch and one token_slot_idx. xs[i] / ys[i] are the device input / output of
+ * layer layers[i]. Layers may share an input pointer (q, k, v read the same
+ * hidden state). The grouping of tokens by slot is computed once for the set.
+ */
+int lora_apply_multi(lora_ctx *ctx, int n, const int *layers, const void *const *xs,
+                     void *const *ys, const int32_t *token_slot_idx, int n_tokens);
+
+/*
+ * The same as lora_apply_multi with HOST buffers: copies the inputs (distinct
+ * xs_host once each, ys_host, idx_host) to the caller's device staging buffers
+ * xs_dev / ys_dev / idx_dev, applies, and copies every y back to ys_host, all
+ * on the compute stream. Returns after queuing; synchronise the compute stream
+ * before reading ys_host. Host buffers should be pinned.
+ */
+int lora_apply_multi_host(lora_ctx *ctx, int n, const int *layers,
+                          const void *const *xs_host, void *const *ys_host,
+                          const int32_t *idx_host, int n_tokens,
+                          void *const *xs_dev, void *const *ys_dev, int32_t *idx_dev);
+
+/*
+ * Host slot table (the LRU of the "Multi-LoRA 适配器缓存生产实战" page, section
+ * 核心原理). adapter ids are opaque 64-bit keys. The LRU clock advances by one
+ * on every touch or bind, so no two slots tie.
+ */
+
+/* Hit: touch and return the slot in *slot. Miss: *slot = -1 (no state change). */
+int lora_lookup(lora_ctx *ctx, uint64_t adapter_id, int *slot);
+
+/*
+ * Hit: touch, *slot = its slot, *needs_load = 0. Miss: validate rank first
+ * (LORA_ERR_RANK, nothing evicted), then take the lowest free slot, else evict
+ * the least recently used slot that is not in flight (LORA_ERR_NO_SLOT if
+ * none); bind the id, *needs_load = 1, *evicted_id = the removed id or
+ * UINT64_MAX. The caller then uploads with lora_load_slot.
+ */
+int lora_assign(lora_ctx *ctx, uint64_t adapter_id, int rank, int *slot,
+                int *needs_load, uint64_t *evicted_id);
+
+/* In-flight reference count of an occupied slot (never evicted while > 0). */
+int lora_acquire(lora_ctx *ctx, int slot);
+int lora_release(lora_ctx *ctx, int slot);
+
+/*
+ * Evict the least recently used occupied slot that is not in flight.
+ * *evicted_slot = -1 when no slot is occupied (LORA_OK). LORA_ERR_NO_SLOT when
+ * every occupied slot is in flight. With a device context the slot's rank is
+ * set to 0 on the device, after compute work already queued.
+ */
+int lora_evict_lru(lora_ctx *ctx, int *evicted_slot, uint64_t *evicted_id);
+
+/* Advance the epoch used by the thrash window (call once per step). */
+int lora_tick(lora_ctx *ctx);
+
+/* Set the thrash window in epochs (default 10). */
+int lora_set_thrash_window(lora_ctx *ctx, int epochs);
+
+/*
+ * Segment-length threshold for the tensor-core prefill path: contiguous runs
+ * of tokens on one slot at least this long use it; shorter runs and decode
+ * tokens use the grouped decode kernels. 0 disables the prefill path.
+ * Values 1..63 are raised to 64. Default 64.
+ */
+int lora_set_prefill_min_tokens(lora_ctx *ctx, int n);
+
+/* Block until every queued upload finished; accumulates upload_seconds. */
+int lora_sync_uploads(lora_ctx *ctx);
+
+/* Counters; synchronises the compute stream to read the device error count. */
+int lora_stats(lora_ctx *ctx, lora_stats_t *out);
+
+/* Bytes one adapter upload moves: sum over layers of (d_in + d_out) * rank * bytes_per_param. */
+uint64_t lora_adapter_bytes(int n_layers, const int *d_in, const int *d_out, int rank,
+                            int bytes_per_param);
+
+/* Message for the last failed call on this thread ("" if none). */
+const char *lora_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RANK_ADAPTER_APPLY_H */

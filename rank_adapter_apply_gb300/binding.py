@@ -1,0 +1,220 @@
+"""Thin ctypes binding of the C ABI (include/rank_adapter_apply.h).
+
+Functions keep the C names and only marshal arguments; every step of the path
+runs in the compiled library. ``LoraSlots`` is a convenience owner of the
+device memory the ABI asks the caller for (slot pools, scale/rank arrays,
+workspace) and of the two streams, all allocated through PyTorch.
+
+Loading raises ``RuntimeError`` when the library has not been built: there is
+no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "librank_adapter_apply.so")
+
+LORA_OK = 0
+LORA_ERR_ARG = -1
+LORA_ERR_RANK = -2
+LORA_ERR_NO_SLOT = -3
+LORA_ERR_CUDA = -4
+LORA_ERR_STATE = -5
+LORA_DTYPE_F32 = 0
+LORA_DTYPE_BF16 = 1
+NO_ID = (1 << 64) - 1
+
+EXPORTED = [
+    "lora_workspace_bytes", "lora_slots_init", "lora_destroy", "lora_load_slot", "lora_apply",
+    "lora_apply_multi", "lora_apply_multi_host", "lora_lookup", "lora_assign", "lora_acquire",
+    "lora_release", "lora_evict_lru", "lora_tick", "lora_set_thrash_window",
+    "lora_set_prefill_min_tokens", "lora_sync_uploads", "lora_stats", "lora_adapter_bytes",
+    "lora_last_error",
+]
+
+
+class LoraLayerDesc(ctypes.Structure):
+    _fields_ = [("d_in", ctypes.c_int), ("d_out", ctypes.c_int),
+                ("A_pool", ctypes.c_void_p), ("B_pool", ctypes.c_void_p)]
+
+
+class LoraStats(ctypes.Structure):
+    _fields_ = [("hits", ctypes.c_uint64), ("misses", ctypes.c_uint64),
+                ("evictions", ctypes.c_uint64), ("reloads_after_eviction", ctypes.c_uint64),
+                ("rejected", ctypes.c_uint64), ("uploads", ctypes.c_uint64),
+                ("upload_bytes", ctypes.c_uint64), ("invalid_token_index", ctypes.c_uint64),
+                ("upload_seconds", ctypes.c_double), ("epoch", ctypes.c_int64)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+class LoraError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"[{code}] {msg}")
+        self.code = code
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load the compiled library (raises if it is missing)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"rank_adapter_apply library not built: {path} is missing "
+                           "(run `python -m rank_adapter_apply_gb300.build`)")
+    lib = ctypes.CDLL(path)
+    vp, i32, u64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_size_t
+    P = ctypes.POINTER
+    sig = {
+        "lora_workspace_bytes": (sz, [i32, i32, i32, i32]),
+        "lora_slots_init": (i32, [P(vp), i32, i32, i32, i32, i32, i32, P(LoraLayerDesc), vp, vp,
+                                  vp, sz, vp, vp]),
+        "lora_destroy": (None, [vp]),
+        "lora_load_slot": (i32, [vp, i32, P(vp), P(vp), i32, ctypes.c_float]),
+        "lora_apply": (i32, [vp, i32, vp, vp, vp, i32]),
+        "lora_apply_multi": (i32, [vp, i32, P(i32), P(vp), P(vp), vp, i32]),
+        "lora_apply_multi_host": (i32, [vp, i32, P(i32), P(vp), P(vp), vp, i32, P(vp), P(vp), vp]),
+        "lora_lookup": (i32, [vp, u64, P(i32)]),
+        "lora_assign": (i32, [vp, u64, i32, P(i32), P(i32), P(u64)]),
+        "lora_acquire": (i32, [vp, i32]),
+        "lora_release": (i32, [vp, i32]),
+        "lora_evict_lru": (i32, [vp, P(i32), P(u64)]),
+        "lora_tick": (i32, [vp]),
+        "lora_set_thrash_window": (i32, [vp, i32]),
+        "lora_set_prefill_min_tokens": (i32, [vp, i32]),
+        "lora_sync_uploads": (i32, [vp]),
+        "lora_stats": (i32, [vp, P(LoraStats)]),
+        "lora_adapter_bytes": (u64, [i32, P(i32), P(i32), i32, i32]),
+        "lora_last_error": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def last_error() -> str:
+    return load().lora_last_error().decode()
+
+
+def check(rc: int) -> int:
+    if rc != LORA_OK:
+        raise LoraError(rc, last_error())
+    return rc
+
+
+def _vp_array(ptrs):
+    return (ctypes.c_void_p * len(ptrs))(*[ctypes.c_void_p(p) for p in ptrs])
+
+
+def _i32_array(vals):
+    return (ctypes.c_int * len(vals))(*vals)
+
+
+# --- C-named wrappers (argument marshalling only) --------------------------------
+
+def lora_workspace_bytes(max_loras, max_lora_rank, max_tokens, max_layers_per_call):
+    return int(load().lora_workspace_bytes(max_loras, max_lora_rank, max_tokens, max_layers_per_call))
+
+
+def lora_slots_init(max_loras, max_lora_rank, max_tokens, max_layers_per_call, dtype, layers,
+                    scale_dev, rank_dev, workspace, workspace_bytes, compute_stream, upload_stream):
+    """layers: list of (d_in, d_out, A_pool_ptr, B_pool_ptr). Returns the context handle."""
+    descs = (LoraLayerDesc * max(1, len(layers)))(
+        *[LoraLayerDesc(di, do, a, b) for di, do, a, b in layers])
+    h = ctypes.c_void_p()
+    check(load().lora_slots_init(ctypes.byref(h), max_loras, max_lora_rank, max_tokens,
+                                 max_layers_per_call, dtype, len(layers), descs, scale_dev,
+                                 rank_dev, workspace, workspace_bytes, compute_stream,
+                                 upload_stream))
+    return h
+
+
+def lora_destroy(ctx):
+    load().lora_destroy(ctx)
+
+
+def lora_load_slot(ctx, slot, A_ptrs, B_ptrs, rank, alpha):
+    return check(load().lora_load_slot(ctx, slot, _vp_array(A_ptrs), _vp_array(B_ptrs), rank,
+                                       float(alpha)))
+
+
+def lora_apply(ctx, layer, x_ptr, y_ptr, idx_ptr, n_tokens):
+    return check(load().lora_apply(ctx, layer, x_ptr, y_ptr, idx_ptr, n_tokens))
+
+
+def lora_apply_multi(ctx, layers, x_ptrs, y_ptrs, idx_ptr, n_tokens):
+    return check(load().lora_apply_multi(ctx, len(layers), _i32_array(layers), _vp_array(x_ptrs),
+                                         _vp_array(y_ptrs), idx_ptr, n_tokens))
+
+
+def lora_apply_multi_host(ctx, layers, xs_host, ys_host, idx_host, n_tokens, xs_dev, ys_dev,
+                          idx_dev):
+    return check(load().lora_apply_multi_host(
+        ctx, len(layers), _i32_array(layers), _vp_array(xs_host), _vp_array(ys_host), idx_host,
+        n_tokens, _vp_array(xs_dev), _vp_array(ys_dev), idx_dev))
+
+
+def lora_lookup(ctx, adapter_id):
+    s = ctypes.c_int()
+    check(load().lora_lookup(ctx, adapter_id, ctypes.byref(s)))
+    return s.value
+
+
+def lora_assign(ctx, adapter_id, rank):
+    """Returns (status, slot, needs_load, evicted_id or -1); status is not raised."""
+    s, nl, ev = ctypes.c_int(-1), ctypes.c_int(0), ctypes.c_uint64(NO_ID)
+    rc = load().lora_assign(ctx, adapter_id, rank, ctypes.byref(s), ctypes.byref(nl),
+                            ctypes.byref(ev))
+    return rc, s.value, nl.value, (-1 if ev.value == NO_ID else ev.value)
+
+
+def lora_acquire(ctx, slot):
+    return load().lora_acquire(ctx, slot)
+
+
+def lora_release(ctx, slot):
+    return load().lora_release(ctx, slot)
+
+
+def lora_evict_lru(ctx):
+    """Returns (status, slot or -1, evicted id or -1)."""
+    s, ev = ctypes.c_int(-1), ctypes.c_uint64(NO_ID)
+    rc = load().lora_evict_lru(ctx, ctypes.byref(s), ctypes.byref(ev))
+    return rc, s.value, (-1 if ev.value == NO_ID else ev.value)
+
+
+def lora_tick(ctx):
+    return check(load().lora_tick(ctx))
+
+
+def lora_set_thrash_window(ctx, epochs):
+    return check(load().lora_set_thrash_window(ctx, epochs))
+
+
+def lora_set_prefill_min_tokens(ctx, n):
+    return check(load().lora_set_prefill_min_tokens(ctx, n))
+
+
+def lora_sync_uploads(ctx):
+    return check(load().lora_sync_uploads(ctx))
+
+
+def lora_stats(ctx) -> dict:
+    st = LoraStats()
+    check(load().lora_stats(ctx, ctypes.byref(st)))
+    return st.as_dict()
+
+
+def lora_adapter_bytes(layers, rank, bytes_per_param):
+    di = _i32_array([a for a, _ in layers])
+    do = _i32_array([b for _, b in layers])
+    return int(load().lora_adapter_bytes(len(layers), di, do, rank, bytes_per_param))

@@ -1,0 +1,374 @@
+// Decode path: grouped shrink and expand-add over tiles of <= 16 tokens that
+// share one slot.
+//
+//   shrink:  v[t][k] = sum_j A_s[k][j] x[t][j]           (k < r_s, fp32)
+//   expand:  y[t][i] = round(y[t][i] + scale_s * sum_k B_s[i][k] v[t][k])
+//
+// The delta itself is the LoRA update written with the PEFT adapter fields r
+// and lora_alpha (the adapter_config.json example on the "vLLM LoRA Resolver
+// 插件详解" page, section 3.2); scale_s = lora_alpha / r_s with the adapter's own
+// rank, ranks zero-padded to max_lora_rank in the slot pools (the
+// "Multi-LoRA 适配器缓存生产实战" page, section 核心原理, parameter table).
+//
+// bf16: both contractions run on the tensor cores with mma.m16n8k16 (bf16
+// operands, fp32 accumulation). Operands go straight from global memory to
+// registers with 128-bit loads: the order of the k index inside one MMA is a
+// free choice as long as both operands use the same one, so every lane loads
+// eight consecutive elements of a row at once. The expand splits v into a bf16
+// high part and a bf16 remainder (two MMAs) so v keeps ~16 significant bits.
+// fp32: plain CUDA-core loops (exact fp32 FMAs).
+//
+// The shrink splits d_in into n_chunks column chunks (one CTA each) so a
+// decode batch fills the GPU; each CTA writes its partial sums, and the last
+// CTA to arrive for a tile adds them in chunk order (deterministic) and writes v.
+#include "kernels.cuh"
+
+#include <cuda_bf16.h>
+
+namespace lora {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kWarps = kThreads / 32;
+constexpr int kExpandCols = 256;          // output columns per expand CTA (bf16 and fp32)
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t p) { return __uint_as_float(p << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t p) { return __uint_as_float(p & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Eight consecutive bf16 of a row starting at column c (zero past d or when !ok).
+__device__ __forceinline__ uint4 load8_bf16(const uint16_t *row, int c, int d, bool ok, int vec) {
+    uint4 r = make_uint4(0, 0, 0, 0);
+    if (!ok) return r;
+    if (vec && c + 8 <= d) return __ldg(reinterpret_cast<const uint4 *>(row + c));
+    uint16_t e[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) e[i] = (c + i < d) ? row[c + i] : (uint16_t)0;
+    r.x = e[0] | ((uint32_t)e[1] << 16);
+    r.y = e[2] | ((uint32_t)e[3] << 16);
+    r.z = e[4] | ((uint32_t)e[5] << 16);
+    r.w = e[6] | ((uint32_t)e[7] << 16);
+    return r;
+}
+
+// Sum the chunk partials of one tile in chunk order and write v (last CTA only).
+__device__ void finish_split(const LayerArgs &L, const GroupView &g, int tile_i, int p0, int cnt,
+                             int r) {
+    __shared__ int last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int prev = atomicAdd(&L.counters[tile_i], 1);
+        last = (prev == L.n_chunks - 1);
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    const int R = g.R, T = g.T;
+    for (int e = threadIdx.x; e < cnt * r; e += kThreads) {
+        int pos = p0 + e / r, k = e % r;
+        float s = 0.f;
+        for (int ch = 0; ch < L.n_chunks; ++ch)
+            s += __ldcg(&L.part[((size_t)ch * T + pos) * R + k]);
+        L.v[(size_t)pos * R + k] = s;
+    }
+    if (threadIdx.x == 0) L.counters[tile_i] = 0;
+}
+
+// ---------------------------------------------------------------------------
+// bf16 shrink. CTA = (d_in chunk, tile, layer); 4 warps stride the chunk in
+// 32-column steps. Per warp and step: m16n8k16 with M = 16 ranks (per 16-rank
+// block), N = 8 tokens (two token blocks), K = 16 (two MMAs per 32 columns).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads)
+shrink_bf16_kernel(MultiArgs ma, GroupView g) {
+    const LayerArgs &L = ma.l[blockIdx.z];
+    const int chunk = blockIdx.x, tile_i = blockIdx.y;
+    if (chunk >= L.n_chunks || tile_i >= g.hdr[kHdrTiles]) return;
+    const int4 tile = g.tiles[tile_i];
+    const int s = tile.x, p0 = tile.y, cnt = tile.z;
+    const int r = g.rank[s];
+    const int nmb = (r + 15) >> 4;
+    const int R = g.R, d_in = L.d_in;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
+
+    const int tok0 = gq < cnt ? g.perm[p0 + gq] : -1;
+    const int tok1 = gq + 8 < cnt ? g.perm[p0 + 8 + gq] : -1;
+    const uint16_t *x = static_cast<const uint16_t *>(L.x);
+    const uint16_t *xr0 = x + (size_t)(tok0 < 0 ? 0 : tok0) * d_in;
+    const uint16_t *xr1 = x + (size_t)(tok1 < 0 ? 0 : tok1) * d_in;
+    const uint16_t *As = static_cast<const uint16_t *>(L.A) + (size_t)s * R * d_in;
+
+    float acc[4][2][4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[m][n][j] = 0.f;
+
+    const int c0 = chunk * L.chunk_cols;
+    const int c1 = min(d_in, c0 + L.chunk_cols);
+#pragma unroll 2
+    for (int col = c0 + warp * 32; col < c1; col += kWarps * 32) {
+        const int cc = col + 8 * tq;
+        const uint4 xa = load8_bf16(xr0, cc, d_in, tok0 >= 0, L.vec);
+        const uint4 xb = load8_bf16(xr1, cc, d_in, tok1 >= 0, L.vec);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            if (m < nmb) {
+                const int k0 = m * 16 + gq, k1 = k0 + 8;
+                const uint4 a0 = load8_bf16(As + (size_t)k0 * d_in, cc, d_in, k0 < r, L.vec);
+                const uint4 a1 = load8_bf16(As + (size_t)k1 * d_in, cc, d_in, k1 < r, L.vec);
+                mma_bf16(acc[m][0], a0.x, a1.x, a0.y, a1.y, xa.x, xa.y);
+                mma_bf16(acc[m][0], a0.z, a1.z, a0.w, a1.w, xa.z, xa.w);
+                mma_bf16(acc[m][1], a0.x, a1.x, a0.y, a1.y, xb.x, xb.y);
+                mma_bf16(acc[m][1], a0.z, a1.z, a0.w, a1.w, xb.z, xb.w);
+            }
+        }
+    }
+
+    // Cross-warp sum through shared memory.
+    __shared__ float red[kWarps][4 * 2 * 4][32];
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) red[warp][(m * 2 + n) * 4 + j][lane] = acc[m][n][j];
+    __syncthreads();
+    float *dst_base = L.n_chunks == 1 ? L.v : L.part + (size_t)chunk * g.T * R;
+    for (int e = threadIdx.x; e < nmb * 256; e += kThreads) {
+        const int ln = e & 31, slot_j = e >> 5;          // slot_j = (m*2+n)*4 + j
+        const int j = slot_j & 3, n = (slot_j >> 2) & 1, m = slot_j >> 3;
+        float v = red[0][slot_j][ln] + red[1][slot_j][ln] + red[2][slot_j][ln] + red[3][slot_j][ln];
+        const int k = m * 16 + (ln >> 2) + ((j & 2) ? 8 : 0);
+        const int tk = n * 8 + 2 * (ln & 3) + (j & 1);
+        if (tk < cnt && k < r) dst_base[(size_t)(p0 + tk) * R + k] = v;
+    }
+    if (L.n_chunks > 1) finish_split(L, g, tile_i, p0, cnt, r);
+}
+
+// ---------------------------------------------------------------------------
+// bf16 expand-add. CTA = (256-column block of d_out, tile, layer); each warp
+// owns 64 columns (two 32-column groups). Per group: 4 MMAs with M = 16 tokens,
+// N = 8 columns, K = 16 ranks, columns permuted so that each lane ends with 8
+// consecutive outputs of two token rows (one 128-bit y access per row).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads)
+expand_bf16_kernel(MultiArgs ma, GroupView g) {
+    const LayerArgs &L = ma.l[blockIdx.z];
+    const int tile_i = blockIdx.y;
+    const int d_out = L.d_out;
+    if (blockIdx.x * kExpandCols >= d_out || tile_i >= g.hdr[kHdrTiles]) return;
+    const int4 tile = g.tiles[tile_i];
+    const int s = tile.x, p0 = tile.y, cnt = tile.z;
+    const int r = g.rank[s];
+    const int nkb = (r + 15) >> 4;
+    const float scale = g.scale[s];
+    const int R = g.R;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
+
+    const int tok0 = gq < cnt ? g.perm[p0 + gq] : -1;
+    const int tok1 = gq + 8 < cnt ? g.perm[p0 + 8 + gq] : -1;
+
+    // A fragments of V (rows = tokens gq, gq+8; k = 4tq..4tq+3 of each 16-rank block).
+    uint32_t ahi[4][4], alo[4][4];
+#pragma unroll
+    for (int kb = 0; kb < 4; ++kb) {
+        float f0[4], f1[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int k = kb * 16 + 4 * tq + i;
+            const bool kin = kb < nkb && k < r;
+            f0[i] = (kin && gq < cnt) ? L.v[(size_t)(p0 + gq) * R + k] : 0.f;
+            f1[i] = (kin && gq + 8 < cnt) ? L.v[(size_t)(p0 + gq + 8) * R + k] : 0.f;
+        }
+        float h0[4], h1[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            h0[i] = __bfloat162float(__float2bfloat16_rn(f0[i]));
+            h1[i] = __bfloat162float(__float2bfloat16_rn(f1[i]));
+        }
+        ahi[kb][0] = pack_bf16(h0[0], h0[1]);
+        ahi[kb][1] = pack_bf16(h1[0], h1[1]);
+        ahi[kb][2] = pack_bf16(h0[2], h0[3]);
+        ahi[kb][3] = pack_bf16(h1[2], h1[3]);
+        alo[kb][0] = pack_bf16(f0[0] - h0[0], f0[1] - h0[1]);
+        alo[kb][1] = pack_bf16(f1[0] - h1[0], f1[1] - h1[1]);
+        alo[kb][2] = pack_bf16(f0[2] - h0[2], f0[3] - h0[3]);
+        alo[kb][3] = pack_bf16(f1[2] - h1[2], f1[3] - h1[3]);
+    }
+
+    const uint16_t *Bs = static_cast<const uint16_t *>(L.B) + (size_t)s * d_out * R;
+    uint16_t *y = static_cast<uint16_t *>(L.y);
+    const int vec = L.vec;
+
+#pragma unroll
+    for (int grp = 0; grp < 2; ++grp) {
+        const int c = blockIdx.x * kExpandCols + warp * 64 + grp * 32;
+        if (c >= d_out) break;
+        float acc[4][4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+            const int P = c + 8 * (gq >> 1) + 2 * j + (gq & 1);
+#pragma unroll
+            for (int kb = 0; kb < 4; ++kb) {
+                if (kb < nkb) {
+                    const int k = kb * 16 + 4 * tq;
+                    uint2 bb = make_uint2(0, 0);
+                    if (P < d_out && k < R)
+                        bb = __ldg(reinterpret_cast<const uint2 *>(Bs + (size_t)P * R + k));
+                    if (k + 4 > r) {
+                        if (k + 0 >= r) bb.x &= 0xffff0000u;
+                        if (k + 1 >= r) bb.x &= 0x0000ffffu;
+                        if (k + 2 >= r) bb.y &= 0xffff0000u;
+                        if (k + 3 >= r) bb.y &= 0x0000ffffu;
+                    }
+                    mma_bf16(acc[j], ahi[kb][0], ahi[kb][1], ahi[kb][2], ahi[kb][3], bb.x, bb.y);
+                    mma_bf16(acc[j], alo[kb][0], alo[kb][1], alo[kb][2], alo[kb][3], bb.x, bb.y);
+                }
+            }
+        }
+        // Lane owns columns c + 8tq .. c + 8tq + 7 of rows tok0 (acc[.][0..1]) and tok1 (acc[.][2..3]).
+        const int cc = c + 8 * tq;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int tok = h ? tok1 : tok0;
+            if (tok < 0) continue;
+            uint16_t *row = y + (size_t)tok * d_out;
+            float dlt[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                dlt[2 * j] = acc[j][2 * h];
+                dlt[2 * j + 1] = acc[j][2 * h + 1];
+            }
+            if (vec && cc + 8 <= d_out) {
+                uint4 yv = *reinterpret_cast<const uint4 *>(row + cc);
+                uint32_t w[4] = {yv.x, yv.y, yv.z, yv.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    w[q] = pack_bf16(fmaf(scale, dlt[2 * q], bf_lo(w[q])),
+                                     fmaf(scale, dlt[2 * q + 1], bf_hi(w[q])));
+                *reinterpret_cast<uint4 *>(row + cc) = make_uint4(w[0], w[1], w[2], w[3]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (cc + i < d_out) {
+                        float yo = __uint_as_float((uint32_t)row[cc + i] << 16);
+                        __nv_bfloat16 o = __float2bfloat16_rn(fmaf(scale, dlt[i], yo));
+                        row[cc + i] = *reinterpret_cast<uint16_t *>(&o);
+                    }
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// fp32 shrink: one warp per token of the tile, lanes stride the chunk, one
+// warp-shuffle reduction per rank.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads)
+shrink_f32_kernel(MultiArgs ma, GroupView g) {
+    const LayerArgs &L = ma.l[blockIdx.z];
+    const int chunk = blockIdx.x, tile_i = blockIdx.y;
+    if (chunk >= L.n_chunks || tile_i >= g.hdr[kHdrTiles]) return;
+    const int4 tile = g.tiles[tile_i];
+    const int s = tile.x, p0 = tile.y, cnt = tile.z;
+    const int r = g.rank[s];
+    const int R = g.R, d_in = L.d_in;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float *x = static_cast<const float *>(L.x);
+    const float *As = static_cast<const float *>(L.A) + (size_t)s * R * d_in;
+    const int c0 = chunk * L.chunk_cols;
+    const int c1 = min(d_in, c0 + L.chunk_cols);
+    float *dst_base = L.n_chunks == 1 ? L.v : L.part + (size_t)chunk * g.T * R;
+    for (int i = warp; i < cnt; i += kWarps) {
+        const float *xr = x + (size_t)g.perm[p0 + i] * d_in;
+        for (int k = 0; k < r; ++k) {
+            const float *ar = As + (size_t)k * d_in;
+            float a = 0.f;
+            for (int c = c0 + lane; c < c1; c += 32) a = fmaf(ar[c], xr[c], a);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+            if (lane == 0) dst_base[(size_t)(p0 + i) * R + k] = a;
+        }
+    }
+    if (L.n_chunks > 1) finish_split(L, g, tile_i, p0, cnt, r);
+}
+
+// fp32 expand-add: each thread owns two columns of the 256-column block.
+__global__ void __launch_bounds__(kThreads)
+expand_f32_kernel(MultiArgs ma, GroupView g) {
+    const LayerArgs &L = ma.l[blockIdx.z];
+    const int tile_i = blockIdx.y;
+    const int d_out = L.d_out;
+    if (blockIdx.x * kExpandCols >= d_out || tile_i >= g.hdr[kHdrTiles]) return;
+    const int4 tile = g.tiles[tile_i];
+    const int s = tile.x, p0 = tile.y, cnt = tile.z;
+    const int r = g.rank[s];
+    const float scale = g.scale[s];
+    const int R = g.R;
+    extern __shared__ float sv[];                     // [kTileTokens][r]
+    for (int e = threadIdx.x; e < cnt * r; e += kThreads)
+        sv[e] = L.v[(size_t)(p0 + e / r) * R + e % r];
+    __syncthreads();
+    const float *Bs = static_cast<const float *>(L.B) + (size_t)s * d_out * R;
+    float *y = static_cast<float *>(L.y);
+    for (int h = 0; h < 2; ++h) {
+        const int col = blockIdx.x * kExpandCols + h * kThreads + threadIdx.x;
+        if (col >= d_out) continue;
+        const float *br = Bs + (size_t)col * R;
+        for (int i = 0; i < cnt; ++i) {
+            float a = 0.f;
+            for (int k = 0; k < r; ++k) a = fmaf(br[k], sv[i * r + k], a);
+            float *yp = y + (size_t)g.perm[p0 + i] * d_out + col;
+            *yp = fmaf(scale, a, *yp);
+        }
+    }
+}
+
+__global__ void set_slot_kernel(float *scale_dev, int *rank_dev, int slot, float scale, int rank) {
+    scale_dev[slot] = scale;
+    rank_dev[slot] = rank;
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const MultiArgs &ma, const GroupView &gv, int dtype, int grid_tiles,
+                          int max_chunks, int max_dblocks, cudaStream_t st) {
+    if (grid_tiles <= 0) return cudaSuccess;
+    dim3 gs(max_chunks, grid_tiles, ma.n), ge(max_dblocks, grid_tiles, ma.n);
+    if (dtype == 1) {
+        shrink_bf16_kernel<<<gs, kThreads, 0, st>>>(ma, gv);
+        expand_bf16_kernel<<<ge, kThreads, 0, st>>>(ma, gv);
+    } else {
+        shrink_f32_kernel<<<gs, kThreads, 0, st>>>(ma, gv);
+        size_t smem = (size_t)kTileTokens * gv.R * sizeof(float);
+        expand_f32_kernel<<<ge, kThreads, smem, st>>>(ma, gv);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_set_slot(float *scale_dev, int *rank_dev, int slot, float scale, int rank,
+                            cudaStream_t st) {
+    set_slot_kernel<<<1, 1, 0, st>>>(scale_dev, rank_dev, slot, scale, rank);
+    return cudaGetLastError();
+}
+
+}  // namespace lora

@@ -1,0 +1,90 @@
+// Internal declarations shared by the C-ABI layer and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace lora {
+
+constexpr int kTileTokens = 16;      // decode tile: tokens of one slot per CTA row
+constexpr int kPrefillRows = 128;    // prefill tile: rows of one same-slot segment
+constexpr int kMinPrefillRun = 64;   // shortest run routed to the prefill path
+constexpr int kMaxLayersPerCall = 8;
+constexpr int kMaxChunks = 16;       // split of d_in in the decode shrink
+constexpr int kPartialRowCap = 65536;
+constexpr int kMaxSlots = 256;
+
+// Header words at the start of the workspace.
+enum HdrWord { kHdrTiles = 0, kHdrPrefillTiles = 1, kHdrInvalid = 2, kHdrDecodeTokens = 3 };
+
+struct WsLayout {
+    size_t hdr, perm, run_start, run_of, tiles, ptiles, counters, v, part, total;
+    int max_tiles, max_ptiles, part_rows, max_tokens, R, max_layers;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline WsLayout ws_layout(int S, int R, int max_tokens, int max_layers) {
+    WsLayout w{};
+    int T = max_tokens > 0 ? max_tokens : 1;
+    w.max_tokens = T;
+    w.R = R;
+    w.max_layers = max_layers;
+    w.max_tiles = (T + kTileTokens - 1) / kTileTokens + (S < T ? S : T) + 1;
+    w.max_ptiles = T / kPrefillRows + T / kMinPrefillRun + 2;
+    long long pr = (long long)kMaxChunks * T;
+    w.part_rows = (int)(pr < kPartialRowCap ? pr : (kPartialRowCap > T ? kPartialRowCap : T));
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
+    w.hdr = take(64 * sizeof(int));
+    w.perm = take((size_t)T * sizeof(int));
+    w.run_start = take((size_t)(T + 1) * sizeof(int));
+    w.run_of = take((size_t)T * sizeof(int));
+    w.tiles = take((size_t)w.max_tiles * sizeof(int4));
+    w.ptiles = take((size_t)w.max_ptiles * sizeof(int4));
+    w.counters = take((size_t)max_layers * w.max_tiles * sizeof(int));
+    w.v = take((size_t)max_layers * T * R * sizeof(float));
+    w.part = take((size_t)max_layers * w.part_rows * R * sizeof(float));
+    w.total = o;
+    return w;
+}
+
+// Per-layer arguments of one decode launch (blockIdx.z selects the layer).
+struct LayerArgs {
+    const void *x;
+    void *y;
+    const void *A;       // pool base [S][R][d_in]
+    const void *B;       // pool base [S][d_out][R]
+    float *v;            // [T][R] fp32 rank-r intermediates, by grouped position
+    float *part;         // [n_chunks * T][R] split partials
+    int *counters;       // [max_tiles] arrival counters (self-resetting)
+    int d_in, d_out;
+    int n_chunks, chunk_cols;
+    int vec;             // 1: rows are 16-byte aligned, 128-bit accesses allowed
+};
+
+struct MultiArgs {
+    LayerArgs l[kMaxLayersPerCall];
+    int n;
+};
+
+// Grouping results shared by every layer of a call.
+struct GroupView {
+    const int *hdr;
+    const int *perm;
+    const int4 *tiles;
+    const float *scale;
+    const int *rank;
+    int R;
+    int T;
+};
+
+cudaError_t launch_group_tokens(const int32_t *idx, int T, const int *rank_dev, int S,
+                                int min_run, char *ws, const WsLayout &lay, cudaStream_t st);
+cudaError_t launch_decode(const MultiArgs &ma, const GroupView &gv, int dtype, int grid_tiles,
+                          int max_chunks, int max_dblocks, cudaStream_t st);
+cudaError_t launch_set_slot(float *scale_dev, int *rank_dev, int slot, float scale, int rank,
+                            cudaStream_t st);
+
+}  // namespace lora

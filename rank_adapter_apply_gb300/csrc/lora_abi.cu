@@ -1,0 +1,489 @@
+// C ABI of the multi-LoRA delta library: context, slot uploads, apply calls
+// and the host slot table. Every declaration lives in include/rank_adapter_apply.h.
+#include "../../include/rank_adapter_apply.h"
+#include "kernels.cuh"
+#include "slot_table.h"
+
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+using namespace lora;
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+#define CUDA_TRY(call)                                                                   \
+    do {                                                                                 \
+        cudaError_t e_ = (call);                                                         \
+        if (e_ != cudaSuccess)                                                           \
+            return fail(LORA_ERR_CUDA, "%s: %s (%s:%d)", #call, cudaGetErrorString(e_),   \
+                        __FILE__, __LINE__);                                             \
+    } while (0)
+
+struct UploadTiming {
+    cudaEvent_t start, end;
+};
+
+}  // namespace
+
+struct lora_ctx {
+    int S = 0, R = 0, max_tokens = 0, max_layers = 0, dtype = 0, n_layers = 0;
+    bool device = false;
+    std::vector<lora_layer_desc> layers;
+    float *scale_dev = nullptr;
+    int32_t *rank_dev = nullptr;
+    char *ws = nullptr;
+    size_t ws_bytes = 0;
+    WsLayout lay{};
+    cudaStream_t compute = nullptr, upload = nullptr;
+    SlotTable table;
+    std::vector<cudaEvent_t> slot_ev;
+    std::vector<char> slot_pending;
+    cudaEvent_t compute_done = nullptr;
+    bool compute_recorded = false;
+    std::vector<UploadTiming> timing;
+    double upload_seconds = 0.0;
+    uint64_t uploads = 0, upload_bytes = 0, invalid_seen = 0;
+    int prefill_min = 0;
+    int num_sms = 148;
+
+    lora_ctx(int S_, int R_) : table(S_, R_) {}
+};
+
+namespace {
+
+int elem_bytes(int dtype) { return dtype == LORA_DTYPE_F32 ? 4 : 2; }
+
+// Move finished upload timings into upload_seconds (blocking when `wait`).
+int harvest_timings(lora_ctx *c, bool wait) {
+    std::vector<UploadTiming> keep;
+    for (auto &t : c->timing) {
+        cudaError_t q = wait ? cudaEventSynchronize(t.end) : cudaEventQuery(t.end);
+        if (q == cudaErrorNotReady) {
+            keep.push_back(t);
+            continue;
+        }
+        if (q != cudaSuccess) return fail(LORA_ERR_CUDA, "upload event: %s", cudaGetErrorString(q));
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, t.start, t.end) == cudaSuccess) c->upload_seconds += ms * 1e-3;
+        cudaEventDestroy(t.start);
+        cudaEventDestroy(t.end);
+    }
+    c->timing.swap(keep);
+    return LORA_OK;
+}
+
+bool capturing(cudaStream_t s) {
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &st) != cudaSuccess) return false;
+    return st != cudaStreamCaptureStatusNone;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *lora_last_error(void) { return g_err.c_str(); }
+
+size_t lora_workspace_bytes(int max_loras, int max_lora_rank, int max_tokens,
+                            int max_layers_per_call) {
+    if (max_loras < 1 || max_lora_rank < 1 || max_tokens < 0 || max_layers_per_call < 1 ||
+        max_layers_per_call > kMaxLayersPerCall)
+        return 0;
+    return ws_layout(max_loras, max_lora_rank, max_tokens, max_layers_per_call).total;
+}
+
+uint64_t lora_adapter_bytes(int n_layers, const int *d_in, const int *d_out, int rank,
+                            int bytes_per_param) {
+    if (n_layers < 0 || (n_layers > 0 && (!d_in || !d_out)) || rank < 0 || bytes_per_param < 0)
+        return 0;
+    uint64_t b = 0;
+    for (int l = 0; l < n_layers; ++l)
+        b += ((uint64_t)d_in[l] + (uint64_t)d_out[l]) * (uint64_t)rank * (uint64_t)bytes_per_param;
+    return b;
+}
+
+int lora_slots_init(lora_ctx **out, int max_loras, int max_lora_rank, int max_tokens,
+                    int max_layers_per_call, int dtype, int n_layers,
+                    const lora_layer_desc *layers, float *scale_dev, int32_t *rank_dev,
+                    void *workspace, size_t workspace_bytes, void *compute_stream,
+                    void *upload_stream) {
+    if (!out) return fail(LORA_ERR_ARG, "out is NULL");
+    *out = nullptr;
+    if (max_loras < 1 || max_loras > kMaxSlots)
+        return fail(LORA_ERR_ARG, "max_loras must be in 1..%d", kMaxSlots);
+    if (dtype != LORA_DTYPE_F32 && dtype != LORA_DTYPE_BF16)
+        return fail(LORA_ERR_ARG, "unknown dtype %d", dtype);
+    const int rmax = dtype == LORA_DTYPE_BF16 ? 64 : 256;
+    if (max_lora_rank < 8 || max_lora_rank > rmax || max_lora_rank % 8 != 0)
+        return fail(LORA_ERR_ARG, "max_lora_rank must be a multiple of 8 in 8..%d", rmax);
+    if (n_layers < 0) return fail(LORA_ERR_ARG, "n_layers < 0");
+    auto *c = new lora_ctx(max_loras, max_lora_rank);
+    c->S = max_loras;
+    c->R = max_lora_rank;
+    c->dtype = dtype;
+    c->n_layers = n_layers;
+    if (n_layers == 0) {          // host-only slot table: no CUDA call at all
+        *out = c;
+        return LORA_OK;
+    }
+    auto reject = [&](int code, const char *msg) {
+        delete c;
+        return fail(code, "%s", msg);
+    };
+    if (!layers || !scale_dev || !rank_dev || !workspace)
+        return reject(LORA_ERR_ARG, "layers, scale_dev, rank_dev and workspace are required");
+    if (max_tokens < 1) return reject(LORA_ERR_ARG, "max_tokens must be >= 1");
+    if (max_layers_per_call < 1 || max_layers_per_call > kMaxLayersPerCall)
+        return reject(LORA_ERR_ARG, "max_layers_per_call must be in 1..8");
+    for (int l = 0; l < n_layers; ++l)
+        if (layers[l].d_in < 1 || layers[l].d_out < 1 || !layers[l].A_pool || !layers[l].B_pool)
+            return reject(LORA_ERR_ARG, "layer with bad shape or NULL pool");
+    for (int l = 0; l < n_layers; ++l)
+        if (reinterpret_cast<uintptr_t>(layers[l].A_pool) % 16 != 0 ||
+            reinterpret_cast<uintptr_t>(layers[l].B_pool) % 16 != 0)
+            return reject(LORA_ERR_ARG, "slot pools must be 16-byte aligned");
+    c->lay = ws_layout(max_loras, max_lora_rank, max_tokens, max_layers_per_call);
+    if (workspace_bytes < c->lay.total) return reject(LORA_ERR_ARG, "workspace too small");
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+        return reject(LORA_ERR_ARG, "workspace must be 256-byte aligned");
+    c->device = true;
+    c->max_tokens = max_tokens;
+    c->max_layers = max_layers_per_call;
+    c->layers.assign(layers, layers + n_layers);
+    c->scale_dev = scale_dev;
+    c->rank_dev = rank_dev;
+    c->ws = static_cast<char *>(workspace);
+    c->ws_bytes = workspace_bytes;
+    c->compute = static_cast<cudaStream_t>(compute_stream);
+    c->upload = static_cast<cudaStream_t>(upload_stream);
+    c->slot_ev.assign(max_loras, nullptr);
+    c->slot_pending.assign(max_loras, 0);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
+    for (int s = 0; s < max_loras && e == cudaSuccess; ++s)
+        e = cudaEventCreateWithFlags(&c->slot_ev[s], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->compute_done, cudaEventDisableTiming);
+    // Empty table: every slot rank 0; workspace zeroed (arrival counters start at 0).
+    if (e == cudaSuccess) e = cudaMemsetAsync(rank_dev, 0, sizeof(int32_t) * max_loras, c->compute);
+    if (e == cudaSuccess) e = cudaMemsetAsync(scale_dev, 0, sizeof(float) * max_loras, c->compute);
+    if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, c->lay.total, c->compute);
+    if (e == cudaSuccess) e = cudaEventRecord(c->compute_done, c->compute);
+    if (e != cudaSuccess) {
+        lora_destroy(c);
+        return fail(LORA_ERR_CUDA, "lora_slots_init: %s", cudaGetErrorString(e));
+    }
+    c->compute_recorded = true;
+    *out = c;
+    return LORA_OK;
+}
+
+void lora_destroy(lora_ctx *c) {
+    if (!c) return;
+    if (c->device) {
+        if (c->upload) cudaStreamSynchronize(c->upload);
+        if (c->compute) cudaStreamSynchronize(c->compute);
+        harvest_timings(c, true);
+        for (auto ev : c->slot_ev)
+            if (ev) cudaEventDestroy(ev);
+        if (c->compute_done) cudaEventDestroy(c->compute_done);
+    }
+    delete c;
+}
+
+int lora_load_slot(lora_ctx *c, int slot, const void *const *A_host, const void *const *B_host,
+                   int rank, float alpha) {
+    if (!c) return fail(LORA_ERR_ARG, "ctx is NULL");
+    if (!c->device) return fail(LORA_ERR_STATE, "host-only context has no slot pools");
+    if (slot < 0 || slot >= c->S) return fail(LORA_ERR_ARG, "slot %d out of range", slot);
+    if (rank < 1 || rank > c->R)
+        return fail(LORA_ERR_RANK, "LoRA rank %d exceeds maximum %d (or is < 1)", rank, c->R);
+    if (!std::isfinite(alpha)) return fail(LORA_ERR_ARG, "alpha is not finite");
+    if (!A_host || !B_host) return fail(LORA_ERR_ARG, "A_host / B_host is NULL");
+    for (int l = 0; l < c->n_layers; ++l)
+        if (!A_host[l] || !B_host[l]) return fail(LORA_ERR_ARG, "layer %d weights are NULL", l);
+
+    const size_t e = elem_bytes(c->dtype);
+    const size_t R = c->R, r = rank;
+    UploadTiming tm{};
+    CUDA_TRY(cudaEventCreate(&tm.start));
+    CUDA_TRY(cudaEventCreate(&tm.end));
+    // Never overwrite a slot that queued compute work may still read.
+    if (c->compute_recorded) CUDA_TRY(cudaStreamWaitEvent(c->upload, c->compute_done, 0));
+    CUDA_TRY(cudaEventRecord(tm.start, c->upload));
+    uint64_t bytes = 0;
+    for (int l = 0; l < c->n_layers; ++l) {
+        const lora_layer_desc &L = c->layers[l];
+        const size_t din = L.d_in, dout = L.d_out;
+        char *A = static_cast<char *>(L.A_pool) + (size_t)slot * R * din * e;
+        char *B = static_cast<char *>(L.B_pool) + (size_t)slot * dout * R * e;
+        CUDA_TRY(cudaMemcpyAsync(A, A_host[l], r * din * e, cudaMemcpyHostToDevice, c->upload));
+        if (r < R) CUDA_TRY(cudaMemsetAsync(A + r * din * e, 0, (R - r) * din * e, c->upload));
+        if (r == R) {
+            CUDA_TRY(cudaMemcpyAsync(B, B_host[l], dout * R * e, cudaMemcpyHostToDevice, c->upload));
+        } else {
+            CUDA_TRY(cudaMemcpy2DAsync(B, R * e, B_host[l], r * e, r * e, dout,
+                                       cudaMemcpyHostToDevice, c->upload));
+            CUDA_TRY(cudaMemset2DAsync(B + r * e, R * e, 0, (R - r) * e, dout, c->upload));
+        }
+        bytes += (din + dout) * r * e;
+    }
+    CUDA_TRY(launch_set_slot(c->scale_dev, c->rank_dev, slot, alpha / (float)rank, rank, c->upload));
+    CUDA_TRY(cudaEventRecord(tm.end, c->upload));
+    CUDA_TRY(cudaEventRecord(c->slot_ev[slot], c->upload));
+    c->slot_pending[slot] = 1;
+    c->timing.push_back(tm);
+    c->uploads += 1;
+    c->upload_bytes += bytes;
+    if (c->timing.size() > 256) harvest_timings(c, false);
+    return LORA_OK;
+}
+
+namespace {
+
+int apply_impl(lora_ctx *c, int n, const int *layers, const void *const *xs, void *const *ys,
+               const int32_t *idx, int T) {
+    if (!c) return fail(LORA_ERR_ARG, "ctx is NULL");
+    if (!c->device) return fail(LORA_ERR_STATE, "host-only context cannot apply");
+    if (n < 1 || n > c->max_layers) return fail(LORA_ERR_ARG, "n must be in 1..%d", c->max_layers);
+    if (T < 0 || T > c->max_tokens) return fail(LORA_ERR_ARG, "n_tokens %d out of 0..%d", T, c->max_tokens);
+    if (!layers || !xs || !ys) return fail(LORA_ERR_ARG, "layers / xs / ys is NULL");
+    for (int i = 0; i < n; ++i) {
+        if (layers[i] < 0 || layers[i] >= c->n_layers) return fail(LORA_ERR_ARG, "bad layer %d", layers[i]);
+        if (T > 0 && (!xs[i] || !ys[i])) return fail(LORA_ERR_ARG, "NULL x or y for entry %d", i);
+    }
+    if (T == 0) return LORA_OK;
+    if (!idx) return fail(LORA_ERR_ARG, "token_slot_idx is NULL");
+
+    // Uploads queued since the last apply must land before any kernel reads a slot.
+    if (!capturing(c->compute)) {
+        for (int s = 0; s < c->S; ++s)
+            if (c->slot_pending[s]) {
+                CUDA_TRY(cudaStreamWaitEvent(c->compute, c->slot_ev[s], 0));
+                c->slot_pending[s] = 0;
+            }
+    } else {
+        for (int s = 0; s < c->S; ++s)
+            if (c->slot_pending[s])
+                return fail(LORA_ERR_STATE, "slot %d upload pending during stream capture; "
+                                            "call lora_sync_uploads before capturing", s);
+    }
+
+    CUDA_TRY(launch_group_tokens(idx, T, c->rank_dev, c->S, c->prefill_min, c->ws, c->lay, c->compute));
+
+    const size_t e = elem_bytes(c->dtype);
+    const int est_tiles = (T + kTileTokens - 1) / kTileTokens + (c->S < T ? c->S : T);
+    MultiArgs ma{};
+    ma.n = n;
+    int max_chunks = 1, max_dblocks = 1;
+    for (int i = 0; i < n; ++i) {
+        const lora_layer_desc &L = c->layers[layers[i]];
+        LayerArgs &a = ma.l[i];
+        a.x = xs[i];
+        a.y = ys[i];
+        a.A = L.A_pool;
+        a.B = L.B_pool;
+        a.d_in = L.d_in;
+        a.d_out = L.d_out;
+        a.v = reinterpret_cast<float *>(c->ws + c->lay.v) + (size_t)i * c->lay.max_tokens * c->R;
+        a.part = reinterpret_cast<float *>(c->ws + c->lay.part) + (size_t)i * c->lay.part_rows * c->R;
+        a.counters = reinterpret_cast<int *>(c->ws + c->lay.counters) + (size_t)i * c->lay.max_tiles;
+        // Split d_in so that the shrink launches about two CTAs per SM.
+        int want = (2 * c->num_sms + est_tiles * n - 1) / (est_tiles * n);
+        int cap = c->lay.part_rows / T;
+        int chunks = want < 1 ? 1 : want;
+        if (chunks > kMaxChunks) chunks = kMaxChunks;
+        if (chunks > cap) chunks = cap < 1 ? 1 : cap;
+        int cols = (L.d_in + chunks - 1) / chunks;
+        cols = (cols + 127) / 128 * 128;
+        a.chunk_cols = cols;
+        a.n_chunks = (L.d_in + cols - 1) / cols;
+        const bool al = (reinterpret_cast<uintptr_t>(xs[i]) % 16 == 0) &&
+                        (reinterpret_cast<uintptr_t>(ys[i]) % 16 == 0) &&
+                        (reinterpret_cast<uintptr_t>(L.A_pool) % 16 == 0) &&
+                        ((size_t)L.d_in * e % 16 == 0) && ((size_t)L.d_out * e % 16 == 0);
+        a.vec = al ? 1 : 0;
+        if (a.n_chunks > max_chunks) max_chunks = a.n_chunks;
+        int db = (L.d_out + 255) / 256;
+        if (db > max_dblocks) max_dblocks = db;
+    }
+    GroupView gv{};
+    gv.hdr = reinterpret_cast<const int *>(c->ws + c->lay.hdr);
+    gv.perm = reinterpret_cast<const int *>(c->ws + c->lay.perm);
+    gv.tiles = reinterpret_cast<const int4 *>(c->ws + c->lay.tiles);
+    gv.scale = c->scale_dev;
+    gv.rank = c->rank_dev;
+    gv.R = c->R;
+    gv.T = T;
+    int grid_tiles = est_tiles < c->lay.max_tiles ? est_tiles : c->lay.max_tiles;
+    CUDA_TRY(launch_decode(ma, gv, c->dtype, grid_tiles, max_chunks, max_dblocks, c->compute));
+    if (!capturing(c->compute)) {
+        CUDA_TRY(cudaEventRecord(c->compute_done, c->compute));
+        c->compute_recorded = true;
+    }
+    return LORA_OK;
+}
+
+}  // namespace
+
+int lora_apply(lora_ctx *c, int layer, const void *x, void *y, const int32_t *idx, int n_tokens) {
+    const void *xs[1] = {x};
+    void *ys[1] = {y};
+    return apply_impl(c, 1, &layer, xs, ys, idx, n_tokens);
+}
+
+int lora_apply_multi(lora_ctx *c, int n, const int *layers, const void *const *xs, void *const *ys,
+                     const int32_t *idx, int n_tokens) {
+    return apply_impl(c, n, layers, xs, ys, idx, n_tokens);
+}
+
+int lora_apply_multi_host(lora_ctx *c, int n, const int *layers, const void *const *xs_host,
+                          void *const *ys_host, const int32_t *idx_host, int T,
+                          void *const *xs_dev, void *const *ys_dev, int32_t *idx_dev) {
+    if (!c || !c->device) return fail(LORA_ERR_STATE, "needs a device context");
+    if (n < 1 || n > c->max_layers || !layers || !xs_host || !ys_host || !xs_dev || !ys_dev)
+        return fail(LORA_ERR_ARG, "bad arguments");
+    if (T < 0 || T > c->max_tokens) return fail(LORA_ERR_ARG, "n_tokens out of range");
+    if (T == 0) return LORA_OK;
+    if (!idx_host || !idx_dev) return fail(LORA_ERR_ARG, "token_slot_idx is NULL");
+    for (int i = 0; i < n; ++i)
+        if (layers[i] < 0 || layers[i] >= c->n_layers) return fail(LORA_ERR_ARG, "bad layer");
+    const size_t e = elem_bytes(c->dtype);
+    CUDA_TRY(cudaMemcpyAsync(idx_dev, idx_host, sizeof(int32_t) * T, cudaMemcpyHostToDevice, c->compute));
+    for (int i = 0; i < n; ++i) {
+        const lora_layer_desc &L = c->layers[layers[i]];
+        bool dup = false;                          // layers sharing one input copy it once
+        for (int j = 0; j < i; ++j) dup = dup || (xs_host[j] == xs_host[i] && xs_dev[j] == xs_dev[i]);
+        if (!dup)
+            CUDA_TRY(cudaMemcpyAsync(xs_dev[i], xs_host[i], (size_t)T * L.d_in * e,
+                                     cudaMemcpyHostToDevice, c->compute));
+        CUDA_TRY(cudaMemcpyAsync(ys_dev[i], ys_host[i], (size_t)T * L.d_out * e,
+                                 cudaMemcpyHostToDevice, c->compute));
+    }
+    int rc = apply_impl(c, n, layers, xs_dev, ys_dev, idx_dev, T);
+    if (rc != LORA_OK) return rc;
+    for (int i = 0; i < n; ++i) {
+        const lora_layer_desc &L = c->layers[layers[i]];
+        CUDA_TRY(cudaMemcpyAsync(ys_host[i], ys_dev[i], (size_t)T * L.d_out * e,
+                                 cudaMemcpyDeviceToHost, c->compute));
+    }
+    return LORA_OK;
+}
+
+int lora_lookup(lora_ctx *c, uint64_t id, int *slot) {
+    if (!c || !slot) return fail(LORA_ERR_ARG, "NULL argument");
+    *slot = c->table.lookup(id);
+    return LORA_OK;
+}
+
+int lora_assign(lora_ctx *c, uint64_t id, int rank, int *slot, int *needs_load, uint64_t *evicted_id) {
+    if (!c || !slot || !needs_load || !evicted_id) return fail(LORA_ERR_ARG, "NULL argument");
+    *needs_load = 0;
+    switch (c->table.assign(id, rank, slot, evicted_id)) {
+    case AssignResult::Hit:
+        return LORA_OK;
+    case AssignResult::Loaded:
+        *needs_load = 1;
+        return LORA_OK;
+    case AssignResult::BadRank:
+        return fail(LORA_ERR_RANK, "LoRA rank %d exceeds maximum %d (or is < 1)", rank, c->R);
+    case AssignResult::NoSlot:
+    default:
+        return fail(LORA_ERR_NO_SLOT, "every occupied slot is in flight");
+    }
+}
+
+int lora_acquire(lora_ctx *c, int slot) {
+    if (!c) return fail(LORA_ERR_ARG, "ctx is NULL");
+    return c->table.acquire(slot) ? LORA_OK : fail(LORA_ERR_STATE, "slot %d is not occupied", slot);
+}
+
+int lora_release(lora_ctx *c, int slot) {
+    if (!c) return fail(LORA_ERR_ARG, "ctx is NULL");
+    return c->table.release(slot) ? LORA_OK : fail(LORA_ERR_STATE, "slot %d is not in flight", slot);
+}
+
+int lora_evict_lru(lora_ctx *c, int *evicted_slot, uint64_t *evicted_id) {
+    if (!c || !evicted_slot || !evicted_id) return fail(LORA_ERR_ARG, "NULL argument");
+    if (!c->table.evict_lru(evicted_slot, evicted_id))
+        return fail(LORA_ERR_NO_SLOT, "every occupied slot is in flight");
+    if (c->device && *evicted_slot >= 0) {
+        // The slot reads as empty for work queued after this call.
+        if (c->compute_recorded) CUDA_TRY(cudaStreamWaitEvent(c->upload, c->compute_done, 0));
+        CUDA_TRY(launch_set_slot(c->scale_dev, c->rank_dev, *evicted_slot, 0.f, 0, c->upload));
+        CUDA_TRY(cudaEventRecord(c->slot_ev[*evicted_slot], c->upload));
+        c->slot_pending[*evicted_slot] = 1;
+    }
+    return LORA_OK;
+}
+
+int lora_tick(lora_ctx *c) {
+    if (!c) return fail(LORA_ERR_ARG, "ctx is NULL");
+    c->table.tick();
+    return LORA_OK;
+}
+
+int lora_set_thrash_window(lora_ctx *c, int epochs) {
+    if (!c || epochs < 0) return fail(LORA_ERR_ARG, "bad arguments");
+    c->table.set_window(epochs);
+    return LORA_OK;
+}
+
+int lora_set_prefill_min_tokens(lora_ctx *c, int n) {
+    if (!c || n < 0) return fail(LORA_ERR_ARG, "bad arguments");
+    c->prefill_min = 0;   // the tensor-core prefill path is not built in this version
+    (void)n;
+    return LORA_OK;
+}
+
+int lora_sync_uploads(lora_ctx *c) {
+    if (!c) return fail(LORA_ERR_ARG, "ctx is NULL");
+    if (!c->device) return LORA_OK;
+    CUDA_TRY(cudaStreamSynchronize(c->upload));
+    return harvest_timings(c, true);
+}
+
+int lora_stats(lora_ctx *c, lora_stats_t *o) {
+    if (!c || !o) return fail(LORA_ERR_ARG, "NULL argument");
+    memset(o, 0, sizeof *o);
+    if (c->device) {
+        CUDA_TRY(cudaStreamSynchronize(c->compute));
+        int inv = 0;
+        CUDA_TRY(cudaMemcpy(&inv, c->ws + c->lay.hdr + kHdrInvalid * sizeof(int), sizeof(int),
+                            cudaMemcpyDeviceToHost));
+        c->invalid_seen = (uint64_t)inv;
+        int rc = harvest_timings(c, false);
+        if (rc != LORA_OK) return rc;
+    }
+    o->hits = c->table.hits;
+    o->misses = c->table.misses;
+    o->evictions = c->table.evictions;
+    o->reloads_after_eviction = c->table.reloads;
+    o->rejected = c->table.rejected;
+    o->uploads = c->uploads;
+    o->upload_bytes = c->upload_bytes;
+    o->invalid_token_index = c->invalid_seen;
+    o->upload_seconds = c->upload_seconds;
+    o->epoch = c->table.epoch();
+    return LORA_OK;
+}
+
+}  // extern "C"

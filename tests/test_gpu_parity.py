@@ -1,0 +1,149 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle."""
+import numpy as np
+import pytest
+
+from rank_adapter_apply_gb300 import workloads as wl
+from tests.parity_util import check_layer
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from rank_adapter_apply_gb300 import build
+    build.build()
+
+
+def _run(w, multi=True, layers=None, **kw):
+    from rank_adapter_apply_gb300.harness import DeviceWorkload
+    dw = DeviceWorkload(w, **kw)
+    try:
+        out = dw.run(layers, multi=multi)
+        stats = dw.slots.stats()
+    finally:
+        dw.close()
+    return out, stats
+
+
+def _custom(T, d_in, d_out, S, R, ranks, idx, dtype=wl.DTYPE_BF16, seed=0, empty=()):
+    rng = np.random.default_rng(seed)
+    layers = [wl.Layer("l0", d_in, d_out, "x")]
+    adapters = []
+    for s in range(S):
+        if s in empty:
+            adapters.append(None)
+            continue
+        adapters.append(wl._adapter(rng, layers, int(ranks[s]), dtype))
+    x = wl._mat(rng, (T, d_in), "normal", 1.0, dtype)
+    y = wl._mat(rng, (T, d_out), "normal", 1.0, dtype)
+    rk = np.array([0 if s in empty else ranks[s] for s in range(S)], np.int32)
+    return wl.Workload("custom", dtype, S, R, layers, np.asarray(idx, np.int32), {"x": x},
+                       {"l0": y}, adapters, rk, 2.0 * np.maximum(rk, 1))
+
+
+def test_tiny_fp32_full():
+    w = wl.tiny_fp32(0)
+    out, _ = _run(w)
+    check_layer(w, "proj", out["proj"])
+
+
+@pytest.mark.parametrize("multi", [True, False])
+def test_decode_qv_4096_full(multi):
+    w = wl.decode_qv_4096(0)
+    out, st = _run(w, multi=multi)
+    for ly in w.layers:
+        check_layer(w, ly.name, out[ly.name])
+    assert st["invalid_token_index"] == 0
+    assert st["upload_bytes"] == 8 * 524_288
+
+
+@pytest.mark.parametrize("T", [1, 2, 15, 16, 17, 37])
+def test_small_and_ragged_token_counts(T):
+    rng = np.random.default_rng(T)
+    idx = rng.integers(-1, 4, size=T)
+    w = _custom(T, 256, 128, 4, 16, [16, 16, 16, 16], idx)
+    out, _ = _run(w)
+    check_layer(w, "l0", out["l0"])
+
+
+def test_all_base_only_is_bitwise_noop():
+    T = 64
+    w = _custom(T, 512, 256, 4, 16, [16] * 4, np.full(T, -1))
+    w.ys["l0"][0, :8] = 0x8000          # -0.0 in bf16
+    out, _ = _run(w)
+    assert np.array_equal(out["l0"], w.ys["l0"])
+
+
+def test_unaligned_dims_and_small_ranks():
+    """d_in, d_out not multiples of 8 (scalar tails), ranks below 8 and odd."""
+    T = 45
+    rng = np.random.default_rng(7)
+    idx = rng.integers(-1, 3, size=T)
+    w = _custom(T, 203, 37, 3, 16, [3, 1, 13], idx)
+    out, _ = _run(w)
+    check_layer(w, "l0", out["l0"])
+
+
+def test_fp32_unaligned():
+    T = 23
+    rng = np.random.default_rng(8)
+    idx = rng.integers(-1, 3, size=T)
+    w = _custom(T, 77, 53, 3, 24, [24, 5, 17], idx, dtype=wl.DTYPE_F32)
+    out, _ = _run(w)
+    check_layer(w, "l0", out["l0"])
+
+
+def test_empty_slot_and_invalid_indices():
+    T = 40
+    idx = np.array(([0, 1, 2, 3, 7, -5, -1, 1] * 5)[:T])   # slot 2 empty; 7 and -5 invalid
+    w = _custom(T, 256, 256, 4, 16, [16, 8, 16, 16], idx, empty=(2,))
+    out, st = _run(w)
+    check_layer(w, "l0", out["l0"])
+    assert st["invalid_token_index"] == 10
+
+
+def test_max_rank_64_mixed():
+    T = 96
+    rng = np.random.default_rng(9)
+    ranks = [8, 16, 32, 64, 48, 24]
+    idx = rng.integers(0, 6, size=T)
+    w = _custom(T, 1024, 512, 6, 64, ranks, idx)
+    out, _ = _run(w)
+    check_layer(w, "l0", out["l0"])
+
+
+def test_prefill_small_full():
+    w = wl.prefill_5120(0, n_seqs=4, len_range=(5, 150))
+    out, _ = _run(w)
+    for ly in w.layers:
+        check_layer(w, ly.name, out[ly.name])
+
+
+def test_mixed_ranks_small_full():
+    w = wl.mixed_ranks_8b(0, n_segments=2, seg_len=70, n_decode=40)
+    out, _ = _run(w)
+    for ly in w.layers:
+        check_layer(w, ly.name, out[ly.name])
+
+
+def _sample(w, n, seed=0):
+    rng = np.random.default_rng(seed)
+    tok = rng.choice(w.n_tokens, size=min(n, w.n_tokens), replace=False)
+    # always include both ends and some segment boundaries
+    return np.unique(np.concatenate([tok, [0, w.n_tokens - 1]]))
+
+
+def test_prefill_full_size_sampled():
+    w = wl.prefill_5120(0)
+    out, _ = _run(w)
+    tok = _sample(w, 160)
+    for ly in w.layers:
+        check_layer(w, ly.name, out[ly.name], tokens=tok)
+
+
+def test_mixed_ranks_full_size_sampled():
+    w = wl.mixed_ranks_8b(0)
+    out, _ = _run(w)
+    tok = _sample(w, 120)
+    for ly in w.layers:
+        check_layer(w, ly.name, out[ly.name], tokens=tok)
