@@ -1,0 +1,457 @@
+#!/usr/bin/env python
+"""Benchmark of the multi-LoRA delta path on one GB300 (or N replicas).
+
+Workload: the decode batch of Llama-7B-shaped q_proj and v_proj (4096 -> 4096,
+bf16), max_loras = 8 slots of rank 16 (alpha 32), 256 tokens per batch with
+Zipf(1.1) slot ids and 10% base-only tokens.
+
+One step = one batch through the whole path: slot lookup (every adapter is
+resident after warm-up, so no upload is queued), token grouping, shrink and
+expand-add for both layers.
+
+* value: delta tokens per second per layer set with inputs resident in HBM,
+  from CUDA-graph replays on CUDA events. Every step uses its own x, y, slot
+  ids and its own copy of the slot pools, cycling over enough sets to exceed
+  twice the L2 size, so no step finds its operands in L2.
+* e2e: the same metric through lora_apply_multi_host with pinned HOST buffers:
+  H2D of x, y and slot ids, apply, D2H of y, plus host slot admission
+  (assign/acquire/release), wall clock.
+* cpu_baseline / --impl reference: the fp64 CPU oracle on host cores.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from rank_adapter_apply_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "LoRA-delta tokens/s per layer set; achieved HBM GB/s and % roofline (1xGB300)"
+UNIT = "delta-tokens/s"
+WORKLOAD = "decode_qv_4096"
+T_TOKENS, N_SLOTS, RANK, ALPHA, D = 256, 8, 16, 32.0, 4096
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def algorithmic_bytes(idx: np.ndarray, ranks, layers, e=2) -> int:
+    """Per layer call: x rows of adapter tokens read, y rows read and written,
+    each used slot's true-rank A and B read once, the slot ids read."""
+    T = idx.shape[0]
+    act = idx[idx >= 0]
+    used = np.unique(act)
+    total = 0
+    for ly in layers:
+        total += act.size * (ly.d_in + 2 * ly.d_out) * e
+        total += sum((ly.d_in + ly.d_out) * int(ranks[s]) * e for s in used)
+        total += T * 4
+    return total
+
+
+def algorithmic_flops(idx, ranks, layers) -> int:
+    act = idx[idx >= 0]
+    return sum(2 * int(ranks[s]) * (ly.d_in + ly.d_out) for ly in layers for s in act)
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        self.t0 = time.time()
+
+    def stop(self):
+        rows = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.file.flush()
+            self.file.seek(0)
+            for line in self.file:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        try:
+            os.unlink(self.file.name)
+        except Exception:
+            pass
+        return rows
+
+    @staticmethod
+    def summary(rows):
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def make_batches(n_sets: int, seed0: int = 0):
+    """Set 0 is the decode workload itself; sets 1.. draw new x, base outputs
+    and slot ids with the same recipe (base output drawn directly)."""
+    w = wl.decode_qv_4096(seed0)
+    batches = [(w.xs["x"], w.ys, w.token_slot_idx)]
+    for i in range(1, n_sets):
+        rng = np.random.default_rng(seed0 + 7919 * i)
+        batches.append(wl.decode_batch(rng, T_TOKENS, N_SLOTS, True))
+    return w, batches
+
+
+def cpu_oracle_run(w, batches, budget_s: float = 10.0, max_batches=None):
+    """Time the fp64 oracle over whole batches (both layers) until the budget
+    is spent. Returns (delta tokens/s, batches done, threads)."""
+    import oracle
+    pools = {ly.name: w.padded_pools(ly.name) for ly in w.layers}
+    oracle.lora_apply_ref(batches[0][0][:1], batches[0][1]["q_proj"][:1], *pools["q_proj"],
+                          w.ranks, w.alphas, batches[0][2][:1])        # build + load outside timing
+    tokens, done = 0, 0
+    t0 = time.perf_counter()
+    while True:
+        x, ys, idx = batches[done % len(batches)]
+        for ly in w.layers:
+            oracle.lora_apply_ref(x, ys[ly.name], *pools[ly.name], w.ranks, w.alphas, idx)
+        tokens += int((idx >= 0).sum())
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_batches and done >= max_batches):
+            break
+    return tokens / el, done, oracle.threads(), el
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    w, batches = make_batches(4)
+    import oracle
+    pools = {ly.name: w.padded_pools(ly.name) for ly in w.layers}
+    n_tok = [T_TOKENS]
+
+    # each step: the oracle over a bounded sample of one batch (the first n_tok
+    # tokens, both layers), sized so that the K timed steps take about a minute
+    def step(i):
+        x, ys, idx = batches[i % len(batches)]
+        tok = np.arange(n_tok[0])
+        for ly in w.layers:
+            oracle.lora_apply_ref(x, ys[ly.name], *pools[ly.name], w.ranks, w.alphas, idx, tokens=tok)
+        return int((idx[tok] >= 0).sum())
+    n_tok[0] = 16
+    t0 = time.perf_counter()
+    step(0)
+    per_tok = (time.perf_counter() - t0) / 16
+    n_tok[0] = int(max(1, min(T_TOKENS, 60.0 / max(1, args.steps) / max(per_tok, 1e-9))))
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    toks = sum(step(i) for i in range(args.steps))
+    el = time.perf_counter() - t0
+    v = toks / el
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "tokens_per_batch": T_TOKENS, "layers": ["q_proj", "v_proj"],
+                       "d": D, "max_loras": N_SLOTS, "rank": RANK, "alpha": ALPHA},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+                             "sample": f"first {n_tok[0]} tokens of a 256-token batch, q_proj and v_proj, per step"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from rank_adapter_apply_gb300 import binding as B
+    from rank_adapter_apply_gb300 import build as build_mod
+    from rank_adapter_apply_gb300.harness import to_torch
+    from rank_adapter_apply_gb300.slots import LoraSlots
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or not os.path.exists(B.LIB_PATH):
+        build_mod.build()
+    if world > 1:
+        dist.barrier()
+    B.load()
+
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 129 * 2 ** 20) or 129 * 2 ** 20
+    per_set = T_TOKENS * D * 2 * 3 + 2 * N_SLOTS * RANK * D * 2 * 2 + T_TOKENS * 4
+    n_sets = int(max(8, -(-2.5 * l2 // per_set)))
+    w, batches = make_batches(n_sets)
+    layers = [(ly.d_in, ly.d_out) for ly in w.layers]
+    stream = torch.cuda.Stream(device=dev)
+    upload = torch.cuda.Stream(device=dev)
+    host_ad = []
+    for s in range(N_SLOTS):
+        A = [to_torch(w.adapters[s][ly.name][0], w.dtype).pin_memory() for ly in w.layers]
+        Bm = [to_torch(w.adapters[s][ly.name][1], w.dtype).pin_memory() for ly in w.layers]
+        host_ad.append((A, Bm))
+
+    class DevSet:
+        pass
+
+    sets = []
+    for i, (x, ys, idx) in enumerate(batches):
+        d = DevSet()
+        d.slots = LoraSlots(layers, N_SLOTS, RANK, T_TOKENS, dtype=torch.bfloat16, device=dev,
+                            compute_stream=stream, upload_stream=upload)
+        for s in range(N_SLOTS):
+            # admission: adapter id s -> slot (all misses on first sight), then upload
+            rc, slot, need, _ = d.slots.assign(s, RANK)
+            assert rc == 0 and need == 1
+            d.slots.load_slot(slot, host_ad[s][0], host_ad[s][1], RANK, ALPHA)
+        d.x = to_torch(x, w.dtype).to(dev)
+        d.ys = [to_torch(ys[ly.name], w.dtype).to(dev) for ly in w.layers]
+        d.idx = torch.from_numpy(idx).to(dev)
+        d.t_act = int((idx >= 0).sum())
+        d.bytes = algorithmic_bytes(idx, w.ranks, w.layers)
+        d.flops = algorithmic_flops(idx, w.ranks, w.layers)
+        sets.append(d)
+    torch.cuda.synchronize(dev)
+    for d in sets:
+        d.slots.sync_uploads()
+
+    def step_apply(d):
+        d.slots.apply_multi([0, 1], [d.x, d.x], d.ys, d.idx)
+
+    # eager warm-up (clears pending-upload waits; sets kernel attributes)
+    with torch.cuda.stream(stream):
+        for d in sets:
+            step_apply(d)
+    torch.cuda.synchronize(dev)
+
+    # graphs: one over all sets, and one per set for the remainder of K
+    g_all = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_all, stream=stream):
+        for d in sets:
+            step_apply(d)
+    g_one = []
+    for d in sets:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step_apply(d)
+        g_one.append(g)
+    torch.cuda.synchronize(dev)
+
+    def run_steps(k):
+        full, rem = divmod(k, len(sets))
+        with torch.cuda.stream(stream):
+            for _ in range(full):
+                g_all.replay()
+            for i in range(rem):
+                g_one[i].replay()
+        return full, rem
+
+    run_steps(max(3, args.warmup))
+    torch.cuda.synchronize(dev)
+    # keep the GPU busy ~1 s before timing so the clocks settle (untimed)
+    t_probe = time.perf_counter()
+    while not args.quick and time.perf_counter() - t_probe < 1.0:
+        run_steps(len(sets) * 20)
+        torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.12)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    full, rem = run_steps(args.steps)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1)
+    clock_rows = sampler.stop()
+    if world > 1:
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    order = [i % len(sets) for i in range(full * len(sets))] + list(range(rem))
+    tokens = sum(sets[i].t_act for i in order)
+    bytes_ = sum(sets[i].bytes for i in order)
+    flops = sum(sets[i].flops for i in order)
+    value = tokens * world / (ms * 1e-3)
+    hbm, peak_kind = peaks()
+    achieved = bytes_ / (ms * 1e-3) / 1e9
+
+    # --- end to end through the C ABI with host buffers --------------------
+    e2e = None if args.quick else run_e2e(args, w, batches, sets[0], stream, dev, world)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded numpy: x~N(0,1), A~U(+-1/64), B~N(0,0.02), Zipf(1.1) slots, 10% base-only)",
+        "config": {"workload": WORKLOAD, "tokens_per_batch": T_TOKENS, "layers": ["q_proj", "v_proj"],
+                   "d": D, "max_loras": N_SLOTS, "rank": RANK, "alpha": ALPHA,
+                   "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2: {len(sets)} distinct x/y/idx/pool sets, "
+                         f"{len(sets) * per_set / 2**20:.0f} MiB per cycle vs L2 {l2 / 2**20:.0f} MiB",
+                   "timing": "CUDA-graph replay, CUDA events on the launch stream"},
+        "roofline": {"bound": "hbm", "kernel": "decode step: group_tokens + shrink_bf16 + expand_bf16 (3 launches)",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "peak_kind": peak_kind, "traffic": None,
+                     "algorithmic_bytes_per_step": bytes_ / max(1, args.steps),
+                     "tflops": flops / (ms * 1e-3) / 1e12},
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": ClockSampler.summary(clock_rows),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quick:
+        v, n, cores, el = cpu_oracle_run(w, batches, budget_s=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": f"{n} whole batches (256 tokens, q_proj+v_proj) in {el:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    for d in sets:
+        d.slots.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, w, batches, d0, stream, dev, world):
+    """Whole-job throughput through lora_apply_multi_host with pinned host
+    buffers: per step host admission of every adapter in the batch (lookup hit,
+    acquire), H2D of x / y / slot ids, apply, D2H of both y, release."""
+    import torch
+    from rank_adapter_apply_gb300 import binding as B
+    from rank_adapter_apply_gb300.harness import to_torch
+
+    ctx = d0.slots.ctx
+    nh = min(4, len(batches))
+    hx = [to_torch(batches[i][0], w.dtype).pin_memory() for i in range(nh)]
+    hy = [[to_torch(batches[i][1][ly.name], w.dtype).pin_memory() for ly in w.layers] for i in range(nh)]
+    hid = [batches[i][2] for i in range(nh)]                       # adapter id per token (-1: base)
+    hidx = [torch.empty(T_TOKENS, dtype=torch.int32).pin_memory() for _ in range(nh)]
+    xd = torch.empty((T_TOKENS, D), dtype=torch.bfloat16, device=dev)
+    yd = [torch.empty((T_TOKENS, D), dtype=torch.bfloat16, device=dev) for _ in w.layers]
+    idd = torch.empty(T_TOKENS, dtype=torch.int32, device=dev)
+    lib = B.load()
+    import ctypes
+    lay = (ctypes.c_int * 2)(0, 1)
+    xs_dev = B._vp_array([xd.data_ptr(), xd.data_ptr()])
+    ys_dev = B._vp_array([t.data_ptr() for t in yd])
+    host_x = [B._vp_array([h.data_ptr(), h.data_ptr()]) for h in hx]
+    host_y = [B._vp_array([t.data_ptr() for t in hy[i]]) for i in range(nh)]
+    slot_of = np.full(N_SLOTS, -1, np.int32)
+    distinct = [np.unique(h[h >= 0]) for h in hid]
+
+    def step(i):
+        j = i % nh
+        held = []
+        for a in distinct[j]:
+            rc, slot, need, _ = B.lora_assign(ctx, int(a), RANK)
+            if rc != 0 or need:
+                raise RuntimeError("adapter unexpectedly not resident")
+            lib.lora_acquire(ctx, slot)
+            slot_of[a] = slot
+            held.append(slot)
+        ids = hid[j]
+        hidx[j].numpy()[:] = np.where(ids >= 0, slot_of[np.maximum(ids, 0)], -1)
+        B.check(lib.lora_apply_multi_host(ctx, 2, lay, host_x[j], host_y[j], hidx[j].data_ptr(),
+                                          T_TOKENS, xs_dev, ys_dev, idd.data_ptr()))
+        for s in held:
+            lib.lora_release(ctx, s)
+        return int((ids >= 0).sum())
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    stream.synchronize()
+    k = min(args.steps, 20000)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    toks = 0
+    for i in range(k):
+        if i % nh == 0 and i > 0:
+            stream.synchronize()          # host buffers of a set are reused every nh steps
+        toks += step(i)
+    stream.synchronize()
+    el = time.perf_counter() - t0
+    h2d = T_TOKENS * D * 2 + 2 * T_TOKENS * D * 2 + T_TOKENS * 4
+    d2h = 2 * T_TOKENS * D * 2
+    return {"value": toks * world / el, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": k,
+            "timing": "wall clock, host admission + H2D + apply + D2H per step"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--quick", action="store_true",
+                    help="profiling runs: no clock settling, no e2e, no CPU baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

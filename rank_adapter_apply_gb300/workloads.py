@@ -149,19 +149,31 @@ def tiny_fp32(seed: int = 0) -> Workload:
                     adapters, np.full(S, r, np.int32), np.full(S, alpha))
 
 
-def decode_qv_4096(seed: int = 0, direct_base: bool = False, n_tokens: int = 256) -> Workload:
-    rng = np.random.default_rng(seed)
-    S, R, r, alpha, T, d = 8, 16, 16, 32.0, n_tokens, 4096
-    layers = [Layer("q_proj", d, d, "x"), Layer("v_proj", d, d, "x")]
-    adapters = [_adapter(rng, layers, r, DTYPE_BF16) for _ in range(S)]
+DECODE_LAYERS = [Layer("q_proj", 4096, 4096, "x"), Layer("v_proj", 4096, 4096, "x")]
+
+
+def decode_batch(rng, T: int, S: int, direct_base: bool, layers=DECODE_LAYERS,
+                 base_only_p: float = 0.1, zipf_s: float = 1.1):
+    """One decode batch: x ~ N(0,1) bf16, base outputs, slot ids (-1 with
+    probability base_only_p, else Zipf(zipf_s) over S slots)."""
+    d = layers[0].d_in
     x = _mat(rng, (T, d), "normal", 1.0, DTYPE_BF16)
     ys = {}
     for ly in layers:
         ys[ly.name] = (_base_out_direct(rng, T, ly, DTYPE_BF16) if direct_base
                        else _base_out_matmul(rng, x, ly, DTYPE_BF16))
-    base_only = rng.random(T) < 0.1
-    slots = rng.choice(S, size=T, p=zipf_probs(S, 1.1)).astype(np.int32)
+    base_only = rng.random(T) < base_only_p
+    slots = rng.choice(S, size=T, p=zipf_probs(S, zipf_s)).astype(np.int32)
     idx = np.where(base_only, -1, slots).astype(np.int32)
+    return x, ys, idx
+
+
+def decode_qv_4096(seed: int = 0, direct_base: bool = False, n_tokens: int = 256) -> Workload:
+    rng = np.random.default_rng(seed)
+    S, R, r, alpha, T = 8, 16, 16, 32.0, n_tokens
+    layers = list(DECODE_LAYERS)
+    adapters = [_adapter(rng, layers, r, DTYPE_BF16) for _ in range(S)]
+    x, ys, idx = decode_batch(rng, T, S, direct_base, layers)
     return Workload("decode_qv_4096", DTYPE_BF16, S, R, layers, idx, {"x": x}, ys,
                     adapters, np.full(S, r, np.int32), np.full(S, alpha))
 
