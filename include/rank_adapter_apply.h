@@ -75,6 +75,8 @@ typedef struct {
     uint64_t invalid_token_index;   /* tokens with index < -1 or >= max_loras (skipped) */
     double upload_seconds;          /* device time of completed uploads */
     int64_t epoch;                  /* current epoch (lora_tick) */
+    uint64_t device_wait_timeouts;  /* non-zero: a bounded device-side wait gave up and the
+                                       rows it guarded were left unchanged (never expected) */
 } lora_stats_t;
 
 /*

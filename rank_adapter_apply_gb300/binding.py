@@ -45,7 +45,8 @@ class LoraStats(ctypes.Structure):
                 ("evictions", ctypes.c_uint64), ("reloads_after_eviction", ctypes.c_uint64),
                 ("rejected", ctypes.c_uint64), ("uploads", ctypes.c_uint64),
                 ("upload_bytes", ctypes.c_uint64), ("invalid_token_index", ctypes.c_uint64),
-                ("upload_seconds", ctypes.c_double), ("epoch", ctypes.c_int64)]
+                ("upload_seconds", ctypes.c_double), ("epoch", ctypes.c_int64),
+                ("device_wait_timeouts", ctypes.c_uint64)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}

@@ -22,6 +22,7 @@
 // decode batch fills the GPU; each CTA writes its partial sums, and the last
 // CTA to arrive for a tile adds them in chunk order (deterministic) and writes v.
 #include "kernels.cuh"
+#include "device_util.cuh"
 
 #include <cuda_bf16.h>
 
@@ -31,38 +32,6 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kWarps = kThreads / 32;
 constexpr int kExpandCols = 256;          // output columns per expand CTA (bf16 and fp32)
-
-__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ float bf_lo(uint32_t p) { return __uint_as_float(p << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t p) { return __uint_as_float(p & 0xffff0000u); }
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&h);
-}
-
-// Eight consecutive bf16 of a row starting at column c (zero past d or when !ok).
-__device__ __forceinline__ uint4 load8_bf16(const uint16_t *row, int c, int d, bool ok, int vec) {
-    uint4 r = make_uint4(0, 0, 0, 0);
-    if (!ok) return r;
-    if (vec && c + 8 <= d) return __ldg(reinterpret_cast<const uint4 *>(row + c));
-    uint16_t e[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) e[i] = (c + i < d) ? row[c + i] : (uint16_t)0;
-    r.x = e[0] | ((uint32_t)e[1] << 16);
-    r.y = e[2] | ((uint32_t)e[3] << 16);
-    r.z = e[4] | ((uint32_t)e[5] << 16);
-    r.w = e[6] | ((uint32_t)e[7] << 16);
-    return r;
-}
 
 // Sum the chunk partials of one tile in chunk order and write v (last CTA only).
 __device__ void finish_split(const LayerArgs &L, const GroupView &g, int tile_i, int p0, int cnt,

@@ -16,10 +16,16 @@ constexpr int kPartialRowCap = 65536;
 constexpr int kMaxSlots = 256;
 
 // Header words at the start of the workspace.
-enum HdrWord { kHdrTiles = 0, kHdrPrefillTiles = 1, kHdrInvalid = 2, kHdrDecodeTokens = 3 };
+enum HdrWord {
+    kHdrTiles = 0, kHdrPrefillTiles = 1, kHdrInvalid = 2, kHdrDecodeTokens = 3,
+    kHdrEpoch = 4,      // launches of the fused decode kernel so far (flag target = epoch + 1)
+    kHdrExit = 5,       // CTAs of the running fused launch that have finished
+    kHdrError = 6,      // non-zero: a bounded wait gave up (the affected rows were skipped)
+};
+constexpr int kFusedMaxTokens = 1024;   // batches up to this size take the fused decode kernel
 
 struct WsLayout {
-    size_t hdr, perm, run_start, run_of, tiles, ptiles, counters, v, part, total;
+    size_t hdr, perm, run_start, run_of, tiles, ptiles, counters, flags, v, part, total;
     int max_tiles, max_ptiles, part_rows, max_tokens, R, max_layers;
 };
 
@@ -44,6 +50,7 @@ inline WsLayout ws_layout(int S, int R, int max_tokens, int max_layers) {
     w.tiles = take((size_t)w.max_tiles * sizeof(int4));
     w.ptiles = take((size_t)w.max_ptiles * sizeof(int4));
     w.counters = take((size_t)max_layers * w.max_tiles * sizeof(int));
+    w.flags = take((size_t)max_layers * w.max_tiles * kMaxChunks * sizeof(unsigned));
     w.v = take((size_t)max_layers * T * R * sizeof(float));
     w.part = take((size_t)max_layers * w.part_rows * R * sizeof(float));
     w.total = o;
@@ -84,6 +91,23 @@ cudaError_t launch_group_tokens(const int32_t *idx, int T, const int *rank_dev, 
                                 int min_run, char *ws, const WsLayout &lay, cudaStream_t st);
 cudaError_t launch_decode(const MultiArgs &ma, const GroupView &gv, int dtype, int grid_tiles,
                           int max_chunks, int max_dblocks, cudaStream_t st);
+// Fused decode step for batches of at most kFusedMaxTokens tokens (bf16 only).
+struct FusedArgs {
+    LayerArgs l[kMaxLayersPerCall];   // x, y, A, B, d_in, d_out, n_chunks, chunk_cols
+    int n;
+    const int32_t *idx;
+    int T, S, R;
+    const int *rank;
+    const float *scale;
+    float *part;                      // layer l at part + l * part_layer_stride
+    size_t part_layer_stride;         // floats
+    unsigned *flags;                  // [n][max_tiles][kMaxChunks]
+    int max_tiles;
+    int *hdr;
+};
+int fused_decode_ctas_per_sm(int max_lora_rank);
+cudaError_t launch_fused_decode(const FusedArgs &fa, int grid, cudaStream_t st);
+
 cudaError_t launch_set_slot(float *scale_dev, int *rank_dev, int slot, float scale, int rank,
                             cudaStream_t st);
 

@@ -54,6 +54,7 @@ def test_decode_qv_4096_full(multi):
     for ly in w.layers:
         check_layer(w, ly.name, out[ly.name])
     assert st["invalid_token_index"] == 0
+    assert st["device_wait_timeouts"] == 0
     assert st["upload_bytes"] == 8 * 524_288
 
 
@@ -147,3 +148,21 @@ def test_mixed_ranks_full_size_sampled():
     tok = _sample(w, 120)
     for ly in w.layers:
         check_layer(w, ly.name, out[ly.name], tokens=tok)
+
+
+def test_fused_repeated_calls_and_layer_subsets():
+    """Many launches on one context (epoch-tagged flags), single layers and the
+    pair, each checked against the oracle after applying once more."""
+    from rank_adapter_apply_gb300.harness import DeviceWorkload
+    w = wl.decode_qv_4096(3, n_tokens=200)
+    dw = DeviceWorkload(w)
+    try:
+        for rep in range(5):
+            dw.reset()
+            out = dw.run(["v_proj"] if rep % 2 else None, multi=rep < 3)
+            for name, y in out.items():
+                check_layer(w, name, y)
+        st = dw.slots.stats()
+        assert st["device_wait_timeouts"] == 0
+    finally:
+        dw.close()
