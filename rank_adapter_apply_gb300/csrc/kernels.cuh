@@ -18,14 +18,12 @@ constexpr int kMaxSlots = 256;
 // Header words at the start of the workspace.
 enum HdrWord {
     kHdrTiles = 0, kHdrPrefillTiles = 1, kHdrInvalid = 2, kHdrDecodeTokens = 3,
-    kHdrEpoch = 4,      // launches of the fused decode kernel so far (flag target = epoch + 1)
-    kHdrExit = 5,       // CTAs of the running fused launch that have finished
     kHdrError = 6,      // non-zero: a bounded wait gave up (the affected rows were skipped)
 };
-constexpr int kFusedMaxTokens = 1024;   // batches up to this size take the fused decode kernel
+constexpr int kFusedMaxTokens = 1024;   // batches up to this size take the cluster decode kernel
 
 struct WsLayout {
-    size_t hdr, perm, run_start, run_of, tiles, ptiles, counters, flags, v, part, total;
+    size_t hdr, perm, run_start, run_of, tiles, ptiles, counters, v, part, total;
     int max_tiles, max_ptiles, part_rows, max_tokens, R, max_layers;
 };
 
@@ -50,7 +48,6 @@ inline WsLayout ws_layout(int S, int R, int max_tokens, int max_layers) {
     w.tiles = take((size_t)w.max_tiles * sizeof(int4));
     w.ptiles = take((size_t)w.max_ptiles * sizeof(int4));
     w.counters = take((size_t)max_layers * w.max_tiles * sizeof(int));
-    w.flags = take((size_t)max_layers * w.max_tiles * kMaxChunks * sizeof(unsigned));
     w.v = take((size_t)max_layers * T * R * sizeof(float));
     w.part = take((size_t)max_layers * w.part_rows * R * sizeof(float));
     w.total = o;
@@ -68,6 +65,7 @@ struct LayerArgs {
     int *counters;       // [max_tiles] arrival counters (self-resetting)
     int d_in, d_out;
     int n_chunks, chunk_cols;
+    int out_cols;        // cluster decode: output columns per CTA of a cluster
     int vec;             // 1: rows are 16-byte aligned, 128-bit accesses allowed
 };
 
@@ -91,22 +89,23 @@ cudaError_t launch_group_tokens(const int32_t *idx, int T, const int *rank_dev, 
                                 int min_run, char *ws, const WsLayout &lay, cudaStream_t st);
 cudaError_t launch_decode(const MultiArgs &ma, const GroupView &gv, int dtype, int grid_tiles,
                           int max_chunks, int max_dblocks, cudaStream_t st);
-// Fused decode step for batches of at most kFusedMaxTokens tokens (bf16 only).
+// Single-launch decode step on 8-CTA clusters, batches of at most
+// kFusedMaxTokens bf16 tokens: one cluster per (layer, tile of <= 16 tokens),
+// CTA c of a cluster owns columns [c*chunk_cols, ...) of d_in and
+// [c*out_cols, ...) of d_out.
 struct FusedArgs {
-    LayerArgs l[kMaxLayersPerCall];   // x, y, A, B, d_in, d_out, n_chunks, chunk_cols
+    LayerArgs l[kMaxLayersPerCall];   // x, y, A, B, d_in, d_out, chunk_cols, out_cols
     int n;
     const int32_t *idx;
     int T, S, R;
     const int *rank;
     const float *scale;
-    float *part;                      // layer l at part + l * part_layer_stride
-    size_t part_layer_stride;         // floats
-    unsigned *flags;                  // [n][max_tiles][kMaxChunks]
-    int max_tiles;
-    int *hdr;
+    int *hdr;                         // workspace header: invalid-index count, error word
 };
-int fused_decode_ctas_per_sm(int max_lora_rank);
-cudaError_t launch_fused_decode(const FusedArgs &fa, int grid, cudaStream_t st);
+constexpr int kClusterSize = 8;
+int cluster_decode_kb(int R);
+size_t cluster_decode_smem(int R);
+cudaError_t launch_cluster_decode(const FusedArgs &fa, int tiles, cudaStream_t st, bool pdl);
 
 cudaError_t launch_set_slot(float *scale_dev, int *rank_dev, int slot, float scale, int rank,
                             cudaStream_t st);

@@ -1,6 +1,6 @@
 // C ABI of the multi-LoRA delta library: context, slot uploads, apply calls
 // and the host slot table. Every declaration lives in include/rank_adapter_apply.h.
-#include "../../include/rank_adapter_apply.h"
+#include "rank_adapter_apply.h"
 #include "kernels.cuh"
 #include "slot_table.h"
 
@@ -63,7 +63,6 @@ struct lora_ctx {
     uint64_t uploads = 0, upload_bytes = 0, invalid_seen = 0;
     int prefill_min = 0;
     int num_sms = 148;
-    int fused_grid_cap = 0;       // resident CTAs of the fused decode kernel (0: not queried yet)
 
     lora_ctx(int S_, int R_) : table(S_, R_) {}
 };
@@ -260,26 +259,20 @@ int lora_load_slot(lora_ctx *c, int slot, const void *const *A_host, const void 
 
 namespace {
 
-// Fused single-launch decode step. Returns LORA_OK, an error, or 1 when the
-// shapes or alignment do not allow it.
+// Single-launch decode step on 8-CTA clusters. Returns LORA_OK, an error, or 1
+// when the shapes or alignment do not allow it.
 int fused_apply(lora_ctx *c, int n, const int *layers, const void *const *xs, void *const *ys,
                 const int32_t *idx, int T) {
+    if (c->S > 255) return 1;
     for (int i = 0; i < n; ++i) {
         const lora_layer_desc &L = c->layers[layers[i]];
         if (L.d_in % 8 || L.d_out % 8 || reinterpret_cast<uintptr_t>(xs[i]) % 16 ||
             reinterpret_cast<uintptr_t>(ys[i]) % 16)
             return 1;
     }
-    if (c->fused_grid_cap == 0) {
-        int per_sm = fused_decode_ctas_per_sm(c->R);
-        if (per_sm > 4) per_sm = 4;
-        c->fused_grid_cap = c->num_sms * per_sm;
-    }
-    const int G_cap = c->fused_grid_cap;
     const int est_tiles = (T + kTileTokens - 1) / kTileTokens + (c->S < T ? c->S : T);
     FusedArgs fa{};
     fa.n = n;
-    int ns_est = 0, ne_est = 0;
     for (int i = 0; i < n; ++i) {
         const lora_layer_desc &L = c->layers[layers[i]];
         LayerArgs &a = fa.l[i];
@@ -290,18 +283,9 @@ int fused_apply(lora_ctx *c, int n, const int *layers, const void *const *xs, vo
         a.d_in = L.d_in;
         a.d_out = L.d_out;
         a.vec = 1;
-        // d_in chunks: about one shrink item per resident CTA over the whole set.
-        int want = (G_cap + est_tiles * n - 1) / (est_tiles * n);
-        int cap = c->lay.part_rows / T;
-        int chunks = want < 1 ? 1 : want;
-        if (chunks > kMaxChunks) chunks = kMaxChunks;
-        if (chunks > cap) chunks = cap < 1 ? 1 : cap;
-        int cols = (L.d_in + chunks - 1) / chunks;
-        cols = (cols + 127) / 128 * 128;
-        a.chunk_cols = cols;
-        a.n_chunks = (L.d_in + cols - 1) / cols;
-        ns_est += est_tiles * a.n_chunks;
-        ne_est += est_tiles * ((L.d_out + 255) / 256);
+        a.chunk_cols = ((L.d_in + kClusterSize - 1) / kClusterSize + 31) / 32 * 32;
+        a.out_cols = ((L.d_out + kClusterSize - 1) / kClusterSize + 31) / 32 * 32;
+        a.n_chunks = kClusterSize;
     }
     fa.idx = idx;
     fa.T = T;
@@ -309,15 +293,8 @@ int fused_apply(lora_ctx *c, int n, const int *layers, const void *const *xs, vo
     fa.R = c->R;
     fa.rank = c->rank_dev;
     fa.scale = c->scale_dev;
-    fa.part = reinterpret_cast<float *>(c->ws + c->lay.part);
-    fa.part_layer_stride = (size_t)c->lay.part_rows * c->R;
-    fa.flags = reinterpret_cast<unsigned *>(c->ws + c->lay.flags);
-    fa.max_tiles = c->lay.max_tiles;
     fa.hdr = reinterpret_cast<int *>(c->ws + c->lay.hdr);
-    int G = ns_est > ne_est ? ns_est : ne_est;
-    if (G > G_cap) G = G_cap;
-    if (G < 1) G = 1;
-    CUDA_TRY(launch_fused_decode(fa, G, c->compute));
+    CUDA_TRY(launch_cluster_decode(fa, est_tiles, c->compute, true));
     if (!capturing(c->compute)) {
         CUDA_TRY(cudaEventRecord(c->compute_done, c->compute));
         c->compute_recorded = true;
