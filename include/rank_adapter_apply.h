@@ -215,6 +215,37 @@ int lora_stats(lora_ctx *ctx, lora_stats_t *out);
 uint64_t lora_adapter_bytes(int n_layers, const int *d_in, const int *d_out, int rank,
                             int bytes_per_param);
 
+/*
+ * One layer of the delta with no workspace and no allocation. The source pages
+ * have no counterpart to this call: it exists for callers that cannot allocate
+ * device memory for a context workspace -- a plugin whose host application
+ * owns every device allocation through its own pool, a process that reserved
+ * all device memory up front, or a latency-critical path that must not call
+ * the allocator (cudaMalloc can synchronise the device and fail at run time).
+ *
+ * The result is the one lora_apply computes for the same layer (grouped
+ * decode kernels; every token, long segments included, takes that path). The
+ * caller passes inputs and outputs exactly as described for lora_apply and
+ * lora_slots_init: x [n_tokens][d_in], y [n_tokens][d_out] updated in place,
+ * device token_slot_idx, the layer's slot pools A_pool [max_loras]
+ * [max_lora_rank][d_in] and B_pool [max_loras][d_out][max_lora_rank] (16-byte
+ * aligned), scale_dev / rank_dev [max_loras] as lora_load_slot fills them,
+ * and the stream the work is queued on (cudaStream_t as void*).
+ *
+ * Scratch comes from a file-scope device array of 4 MiB that every GPU loading
+ * this library holds until the process exits. Calls needing more (large
+ * n_tokens at large max_lora_rank) return LORA_ERR_ARG with a message. The
+ * first call on each device looks up that array's address while the device is
+ * current: make it before any stream capture. All calls share the array:
+ * calls whose work overlaps on the GPU race and must be serialised. The call
+ * calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+int lora_apply_static_scratch(const void *x, void *y, const int32_t *token_slot_idx,
+                              int n_tokens, int d_in, int d_out, int max_loras,
+                              int max_lora_rank, int dtype, const void *A_pool,
+                              const void *B_pool, const float *scale_dev,
+                              const int32_t *rank_dev, void *stream);
+
 /* Message for the last failed call on this thread ("" if none). */
 const char *lora_last_error(void);
 

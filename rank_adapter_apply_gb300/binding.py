@@ -31,7 +31,7 @@ EXPORTED = [
     "lora_apply_multi", "lora_apply_multi_host", "lora_lookup", "lora_assign", "lora_acquire",
     "lora_release", "lora_evict_lru", "lora_tick", "lora_set_thrash_window",
     "lora_set_prefill_min_tokens", "lora_sync_uploads", "lora_stats", "lora_adapter_bytes",
-    "lora_last_error",
+    "lora_last_error", "lora_apply_static_scratch",
 ]
 
 
@@ -93,6 +93,8 @@ def load(path: str = LIB_PATH):
         "lora_stats": (i32, [vp, P(LoraStats)]),
         "lora_adapter_bytes": (u64, [i32, P(i32), P(i32), i32, i32]),
         "lora_last_error": (ctypes.c_char_p, []),
+        "lora_apply_static_scratch": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp,
+                                            vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -219,3 +221,11 @@ def lora_adapter_bytes(layers, rank, bytes_per_param):
     di = _i32_array([a for a, _ in layers])
     do = _i32_array([b for _, b in layers])
     return int(load().lora_adapter_bytes(len(layers), di, do, rank, bytes_per_param))
+
+
+def lora_apply_static_scratch(x_ptr, y_ptr, idx_ptr, n_tokens, d_in, d_out, max_loras,
+                              max_lora_rank, dtype, A_pool, B_pool, scale_dev, rank_dev, stream):
+    """One layer without a context or workspace (scratch in the library's static array)."""
+    return check(load().lora_apply_static_scratch(x_ptr, y_ptr, idx_ptr, n_tokens, d_in, d_out,
+                                                  max_loras, max_lora_rank, dtype, A_pool, B_pool,
+                                                  scale_dev, rank_dev, stream))

@@ -18,7 +18,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "librank_adapter_apply.so")
-SOURCES = ["lora_abi.cu", "group.cu", "decode.cu", "decode_cluster.cu", "slot_table.cpp"]
+SOURCES = ["lora_abi.cu", "group.cu", "decode.cu", "decode_cluster.cu", "static_scratch.cu",
+           "slot_table.cpp"]
 HEADERS = ["kernels.cuh", "slot_table.h", "device_util.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

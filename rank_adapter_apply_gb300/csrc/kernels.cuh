@@ -107,6 +107,9 @@ int cluster_decode_kb(int R);
 size_t cluster_decode_smem(int R);
 cudaError_t launch_cluster_decode(const FusedArgs &fa, int tiles, cudaStream_t st, bool pdl);
 
+// Record the message returned by lora_last_error() for this thread; returns code.
+int set_last_error(int code, const char *msg);
+
 cudaError_t launch_set_slot(float *scale_dev, int *rank_dev, int slot, float scale, int rank,
                             cudaStream_t st);
 

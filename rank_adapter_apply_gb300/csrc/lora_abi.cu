@@ -37,6 +37,15 @@ int fail(int code, const char *fmt, ...) {
                         __FILE__, __LINE__);                                             \
     } while (0)
 
+}  // namespace
+
+int lora::set_last_error(int code, const char *msg) {
+    g_err = msg;
+    return code;
+}
+
+namespace {
+
 struct UploadTiming {
     cudaEvent_t start, end;
 };
