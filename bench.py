@@ -56,6 +56,22 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def kernel_traffic(kernel_file: str):
+    """DRAM bytes per launch of the decode kernel from the committed ncu summary,
+    if that summary was taken on the current kernel source (else None)."""
+    import hashlib
+    src = os.path.join(ROOT, "rank_adapter_apply_gb300", "csrc", kernel_file)
+    summ = os.path.join(ROOT, "profiles", "decode_cluster_qv4096_traffic.json")
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        rec = json.load(open(summ))
+        if rec.get("kernel_source_sha256") == sha:
+            return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
 def algorithmic_bytes(idx: np.ndarray, ranks, layers, e=2) -> int:
     """Per layer call: x rows of adapter tokens read, y rows read and written,
     each used slot's true-rank A and B read once, the slot ids read."""
@@ -348,13 +364,15 @@ def run_ours(args):
                    "l2": f"inputs larger than L2: {len(sets)} distinct x/y/idx/pool sets, "
                          f"{len(sets) * per_set / 2**20:.0f} MiB per cycle vs L2 {l2 / 2**20:.0f} MiB",
                    "timing": "CUDA-graph replay, CUDA events on the launch stream"},
-        "roofline": {"bound": "hbm", "kernel": "decode step: group_tokens + shrink_bf16 + expand_bf16 (3 launches)",
+        "roofline": {"bound": "hbm",
+                     "kernel": "decode_cluster_kernel (one launch per step: grouping, shrink and "
+                               "expand of q_proj and v_proj)",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "peak_kind": peak_kind, "traffic": None,
+                     "peak_kind": peak_kind, "traffic": kernel_traffic("decode_cluster.cu"),
                      "algorithmic_bytes_per_step": bytes_ / max(1, args.steps),
                      "tflops": flops / (ms * 1e-3) / 1e12},
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": args.steps,
         "clocks": ClockSampler.summary(clock_rows),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quick:

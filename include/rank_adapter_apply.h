@@ -198,12 +198,21 @@ int lora_tick(lora_ctx *ctx);
 int lora_set_thrash_window(lora_ctx *ctx, int epochs);
 
 /*
- * Segment-length threshold for the tensor-core prefill path: contiguous runs
- * of tokens on one slot at least this long use it; shorter runs and decode
- * tokens use the grouped decode kernels. 0 disables the prefill path.
- * Values 1..63 are raised to 64. Default 64.
+ * Segment-length threshold for the tensor-core prefill path (bf16 contexts
+ * with max_lora_rank 16, 32 or 64; layers with d_out a multiple of 64):
+ * contiguous runs of tokens on one slot at least this long use it; shorter
+ * runs and decode tokens use the grouped decode kernels. 0 disables the
+ * prefill path. Values 1..63 are raised to 64. Default 64.
  */
 int lora_set_prefill_min_tokens(lora_ctx *ctx, int n);
+
+/*
+ * Batches of at most n tokens (0..1024, default 1024) take the single-launch
+ * decode kernel (thread-block clusters), which treats every token as a decode
+ * token; larger batches take the grouping + tensor-core prefill + decode
+ * kernels. 0 always takes the latter.
+ */
+int lora_set_small_batch_tokens(lora_ctx *ctx, int n);
 
 /* Block until every queued upload finished; accumulates upload_seconds. */
 int lora_sync_uploads(lora_ctx *ctx);

@@ -1,6 +1,7 @@
 // Internal declarations shared by the C-ABI layer and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
@@ -106,6 +107,21 @@ constexpr int kClusterSize = 8;
 int cluster_decode_kb(int R);
 size_t cluster_decode_smem(int R);
 cudaError_t launch_cluster_decode(const FusedArgs &fa, int tiles, cudaStream_t st, bool pdl);
+
+// Tensor-core prefill of one layer over the prefill tiles of the workspace.
+struct PrefillArgs {
+    CUtensorMap mx, ma, mb, my;   // x [T][d_in], A pool [S*R][d_in], B pool [S*d_out][R], y [T][d_out]
+    uint16_t *y;
+    int d_in, d_out;
+    const float *scale;
+    int *hdr;
+    const int4 *ptiles;
+    int cols_per_split;           // d_out columns per CTA (multiple of 64)
+};
+bool prefill_tc_supported(int R);
+cudaError_t launch_prefill_tc(const void *x, void *y, int T, int d_in, int d_out, const void *A_pool,
+                              const void *B_pool, int S, int R, const float *scale, const int *hdr,
+                              const int4 *ptiles, int grid_tiles, int nsplit, cudaStream_t st);
 
 // Record the message returned by lora_last_error() for this thread; returns code.
 int set_last_error(int code, const char *msg);

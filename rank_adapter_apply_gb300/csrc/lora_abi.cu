@@ -70,7 +70,8 @@ struct lora_ctx {
     std::vector<UploadTiming> timing;
     double upload_seconds = 0.0;
     uint64_t uploads = 0, upload_bytes = 0, invalid_seen = 0;
-    int prefill_min = 0;
+    int prefill_min = 0;          // shortest same-slot run sent to the tensor-core prefill kernel
+    int small_batch = kFusedMaxTokens;   // batches up to this size take the cluster decode kernel
     int num_sms = 148;
 
     lora_ctx(int S_, int R_) : table(S_, R_) {}
@@ -174,6 +175,7 @@ int lora_slots_init(lora_ctx **out, int max_loras, int max_lora_rank, int max_to
     if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
         return reject(LORA_ERR_ARG, "workspace must be 256-byte aligned");
     c->device = true;
+    c->prefill_min = kMinPrefillRun;
     c->max_tokens = max_tokens;
     c->max_layers = max_layers_per_call;
     c->layers.assign(layers, layers + n_layers);
@@ -339,12 +341,42 @@ int apply_impl(lora_ctx *c, int n, const int *layers, const void *const *xs, voi
                                             "call lora_sync_uploads before capturing", s);
     }
 
-    if (c->dtype == LORA_DTYPE_BF16 && T <= kFusedMaxTokens) {
+    if (c->dtype == LORA_DTYPE_BF16 && T <= c->small_batch) {
         int rc = fused_apply(c, n, layers, xs, ys, idx, T);
         if (rc != 1) return rc;          // 1: shapes not eligible, take the general path
     }
 
-    CUDA_TRY(launch_group_tokens(idx, T, c->rank_dev, c->S, c->prefill_min, c->ws, c->lay, c->compute));
+    // Long same-slot runs go to the tensor-core prefill kernel when every layer allows it.
+    bool prefill = c->prefill_min > 0 && c->dtype == LORA_DTYPE_BF16 && prefill_tc_supported(c->R) &&
+                   T >= c->prefill_min;
+    for (int i = 0; i < n && prefill; ++i) {
+        const lora_layer_desc &L = c->layers[layers[i]];
+        prefill = L.d_in % 8 == 0 && L.d_out % 64 == 0 && reinterpret_cast<uintptr_t>(xs[i]) % 16 == 0 &&
+                  reinterpret_cast<uintptr_t>(ys[i]) % 16 == 0;
+    }
+    CUDA_TRY(launch_group_tokens(idx, T, c->rank_dev, c->S, prefill ? c->prefill_min : 0, c->ws, c->lay,
+                                 c->compute));
+    if (prefill) {
+        // upper bound on prefill tiles: T/128 full tiles plus one ragged tile per run
+        int grid_tiles = T / kPrefillRows + T / c->prefill_min + 2;
+        if (grid_tiles > c->lay.max_ptiles) grid_tiles = c->lay.max_ptiles;
+        const int est = T / kPrefillRows + 1;
+        for (int i = 0; i < n; ++i) {
+            const lora_layer_desc &L = c->layers[layers[i]];
+            // about three waves of resident CTAs (two per SM) across the d_out splits
+            int nsplit = (3 * 2 * c->num_sms + est - 1) / est;
+            const int max_split = L.d_out / 64;
+            if (nsplit > max_split) nsplit = max_split;
+            if (nsplit > 16) nsplit = 16;
+            if (nsplit < 1) nsplit = 1;
+            cudaError_t e = launch_prefill_tc(
+                xs[i], ys[i], T, L.d_in, L.d_out, L.A_pool, L.B_pool, c->S, c->R, c->scale_dev,
+                reinterpret_cast<const int *>(c->ws + c->lay.hdr),
+                reinterpret_cast<const int4 *>(c->ws + c->lay.ptiles), grid_tiles, nsplit, c->compute);
+            if (e != cudaSuccess)
+                return fail(LORA_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
+        }
+    }
 
     const size_t e = elem_bytes(c->dtype);
     const int est_tiles = (T + kTileTokens - 1) / kTileTokens + (c->S < T ? c->S : T);
@@ -506,8 +538,13 @@ int lora_set_thrash_window(lora_ctx *c, int epochs) {
 
 int lora_set_prefill_min_tokens(lora_ctx *c, int n) {
     if (!c || n < 0) return fail(LORA_ERR_ARG, "bad arguments");
-    c->prefill_min = 0;   // the tensor-core prefill path is not built in this version
-    (void)n;
+    c->prefill_min = n == 0 ? 0 : (n < kMinPrefillRun ? kMinPrefillRun : n);
+    return LORA_OK;
+}
+
+int lora_set_small_batch_tokens(lora_ctx *c, int n) {
+    if (!c || n < 0 || n > kFusedMaxTokens) return fail(LORA_ERR_ARG, "n must be in 0..%d", kFusedMaxTokens);
+    c->small_batch = n;
     return LORA_OK;
 }
 

@@ -30,7 +30,7 @@ class DeviceWorkload:
     """A Workload resident on the GPU with every adapter uploaded to its slot."""
 
     def __init__(self, w: wl.Workload, device="cuda:0", max_tokens=None, pin=True,
-                 prefill_min_tokens=None):
+                 prefill_min_tokens=None, small_batch_tokens=None):
         self.w = w
         self.device = torch.device(device)
         tdt = torch.bfloat16 if w.dtype == wl.DTYPE_BF16 else torch.float32
@@ -38,9 +38,11 @@ class DeviceWorkload:
         self.slots = LoraSlots([(ly.d_in, ly.d_out) for ly in w.layers], w.max_loras,
                                w.max_lora_rank, max_tokens or max(1, w.n_tokens), dtype=tdt,
                                max_layers_per_call=min(8, len(w.layers)), device=device)
+        from . import binding as B
         if prefill_min_tokens is not None:
-            from . import binding as B
             B.lora_set_prefill_min_tokens(self.slots.ctx, prefill_min_tokens)
+        if small_batch_tokens is not None:
+            B.lora_set_small_batch_tokens(self.slots.ctx, small_batch_tokens)
         self.host_adapters = []
         for s, ad in enumerate(w.adapters):
             if ad is None:

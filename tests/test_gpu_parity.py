@@ -166,3 +166,32 @@ def test_fused_repeated_calls_and_layer_subsets():
         assert st["device_wait_timeouts"] == 0
     finally:
         dw.close()
+
+
+@pytest.mark.parametrize("R", [16, 32, 64])
+def test_tensor_core_prefill_small(R):
+    """Runs of >= 64 same-slot tokens through the tcgen05 prefill kernel (general
+    path forced), ragged run ends, decode tokens mixed in, ranks below R."""
+    rng = np.random.default_rng(R)
+    runs = [(0, 200), (2, 64), (1, 63), (3, 130), (-1, 40), (2, 129), (0, 7), (1, 300)]
+    idx = np.concatenate([np.full(n, s) for s, n in runs]).astype(np.int32)
+    ranks = [R, max(1, R // 2), R, 8 if R > 8 else R]
+    w = _custom(idx.shape[0], 512, 384, 4, R, ranks, idx, seed=R)
+    out, st = _run(w, small_batch_tokens=0)
+    check_layer(w, "l0", out["l0"])
+    assert st["device_wait_timeouts"] == 0
+
+
+def test_prefill_small_general_path_matches_oracle():
+    w = wl.prefill_5120(1, n_seqs=5, len_range=(60, 300))
+    out, st = _run(w, small_batch_tokens=0)
+    for ly in w.layers:
+        check_layer(w, ly.name, out[ly.name])
+    assert st["device_wait_timeouts"] == 0
+
+
+def test_prefill_disabled_matches_oracle():
+    w = wl.prefill_5120(2, n_seqs=3, len_range=(100, 200))
+    out, _ = _run(w, small_batch_tokens=0, prefill_min_tokens=0)
+    for ly in w.layers:
+        check_layer(w, ly.name, out[ly.name])
