@@ -453,6 +453,98 @@ def run_e2e(args, w, batches, d0, stream, dev, world):
             "timing": "wall clock, host admission + H2D + apply + D2H per step"}
 
 
+def run_big(args, name):
+    """Prefill-style workloads (one large batch per step, every layer of the set)."""
+    import torch
+    from rank_adapter_apply_gb300 import build as build_mod
+    from rank_adapter_apply_gb300.harness import DeviceWorkload
+    build_mod.build()
+    w = wl.BY_NAME[name](0)
+    dw = DeviceWorkload(w, max_tokens=w.n_tokens)
+    lys = list(range(len(w.layers)))
+    xs = [dw.xs[ly.x_key] for ly in w.layers]
+    ys = [dw.ys[ly.name] for ly in w.layers]
+    st = dw.slots.compute
+    with torch.cuda.stream(st):
+        for _ in range(max(3, args.warmup)):
+            dw.slots.apply_multi(lys, xs, ys, dw.idx)
+    st.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        dw.slots.apply_multi(lys, xs, ys, dw.idx)
+    with torch.cuda.stream(st):
+        for _ in range(3):
+            g.replay()
+    st.synchronize()
+    sampler = ClockSampler(0)
+    sampler.start()
+    time.sleep(0.12)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    with torch.cuda.stream(st):
+        for _ in range(args.steps):
+            g.replay()
+    e1.record(st)
+    st.synchronize()
+    ms = e0.elapsed_time(e1)
+    clocks = ClockSampler.summary(sampler.stop())
+    act = int((w.token_slot_idx >= 0).sum())
+    bytes_ = algorithmic_bytes(w.token_slot_idx, w.ranks, w.layers)
+    flops = algorithmic_flops(w.token_slot_idx, w.ranks, w.layers)
+    hbm, kind = peaks()
+    ach = bytes_ * args.steps / (ms * 1e-3) / 1e9
+    line = {"metric": METRIC, "value": act * args.steps / (ms * 1e-3), "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded numpy, shapes and slot structure of the workload)",
+            "config": {"workload": name, "tokens": w.n_tokens, "layers": [l.name for l in w.layers],
+                       "max_loras": w.max_loras, "max_lora_rank": w.max_lora_rank,
+                       "l2": f"inputs larger than L2 ({bytes_ / 2**20:.0f} MiB per step)",
+                       "timing": "CUDA-graph replay, CUDA events on the launch stream"},
+            "roofline": {"bound": "hbm", "kernel": "prefill_tc_kernel per layer + grouping + decode kernels",
+                         "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "peak_kind": kind,
+                         "traffic": None, "algorithmic_bytes_per_step": bytes_,
+                         "tflops": flops * args.steps / (ms * 1e-3) / 1e12},
+            "gpu_launches": (len(w.layers) + 3) * args.steps, "clocks": clocks}
+    print(json.dumps(line), flush=True)
+    dw.close()
+    return 0
+
+
+def run_churn(args):
+    """Slot churn: 64 GPU slots, 512 rank-16 adapters in pinned host memory,
+    Zipf(1.2) adapter ids with a burst of 20 cold adapters every 50 steps."""
+    from rank_adapter_apply_gb300 import build as build_mod
+    from rank_adapter_apply_gb300.churn import ChurnRunner
+    build_mod.build()
+    steps = args.steps if args.steps <= 1000 else 200
+    trace = wl.churn_trace(0, n_steps=steps)
+    warm = wl.churn_trace(99, n_steps=max(3, min(args.warmup, 20)))
+    r = ChurnRunner()
+    r.run(warm)
+    base = r.slots.stats()
+    res = r.run(trace)
+    st = res.stats
+    d = {k: st[k] - base[k] for k in ("hits", "misses", "evictions", "reloads_after_eviction",
+                                      "uploads", "upload_bytes")}
+    up_s = st["upload_seconds"] - base["upload_seconds"]
+    line = {"metric": "slot-churn decode steps/s (LRU lookup, H2D uploads, q_proj+v_proj delta)",
+            "value": res.steps / res.wall_s, "unit": "steps/s", "n_gpus": 1, "steps": res.steps,
+            "warmup": len(warm.steps), "ms_per_step": res.wall_s * 1e3 / res.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded Zipf(1.2) adapter ids over 512 with cold bursts)",
+            "config": {"workload": "churn_4096", "max_loras": 64, "host_adapters": 512, "rank": 16,
+                       "tokens_per_step": 256, "timing": "wall clock, host bookkeeping included"},
+            "churn": {**d, "thrash_ratio": (d["reloads_after_eviction"] / d["evictions"]) if d["evictions"] else 0.0,
+                      "hit_rate": d["hits"] / max(1, d["hits"] + d["misses"]),
+                      "h2d_GBps": d["upload_bytes"] / up_s / 1e9 if up_s > 0 else None,
+                      "delta_tokens_per_s": res.tokens / res.wall_s},
+            "gpu_launches": None}
+    print(json.dumps(line), flush=True)
+    r.close()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -461,6 +553,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--workload", default=WORKLOAD,
+                    choices=[WORKLOAD, "prefill_5120", "mixed_ranks_8b", "churn_4096"])
     ap.add_argument("--quick", action="store_true",
                     help="profiling runs: no clock settling, no e2e, no CPU baseline")
     args = ap.parse_args()
@@ -468,6 +562,10 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload in ("prefill_5120", "mixed_ranks_8b"):
+        return run_big(args, args.workload)
+    if args.workload == "churn_4096":
+        return run_churn(args)
     return run_ours(args)
 
 

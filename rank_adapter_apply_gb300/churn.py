@@ -1,0 +1,124 @@
+"""Slot-churn driver: decode steps whose adapters come and go.
+
+Each step takes a batch of tokens with adapter ids, and for every group of at
+most max_loras distinct adapters (first-appearance order; max_loras bounds the
+adapters one batch may use, "Multi-LoRA 适配器缓存生产实战" page, section
+核心原理, parameter table):
+  1. assigns each adapter a slot (hit: touch; miss: free slot or LRU victim
+     that is not in flight) and takes an in-flight reference,
+  2. uploads the missing adapters from pinned host memory (tier L1, CPU hit ->
+     H2D upload, section 冷加载延迟),
+  3. applies the delta to q_proj and v_proj for the group's tokens,
+  4. releases the references.
+The epoch advances once per step (the thrash window counts epochs). Every
+decision goes through the C ABI; this module only moves data.
+"""
+from __future__ import annotations
+
+import time
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+from . import binding as B
+from . import workloads as wl
+from .harness import to_torch
+from .slots import LoraSlots
+
+
+@dataclass
+class ChurnResult:
+    steps: int
+    wall_s: float
+    stats: dict
+    decisions: list = field(default_factory=list)   # (step, adapter, status, slot, needs_load, evicted)
+    tokens: int = 0
+
+
+class ChurnRunner:
+    def __init__(self, n_adapters=512, max_loras=64, rank=16, d=4096, tokens=256, seed=0,
+                 device="cuda:0", alpha=32.0):
+        self.dev = torch.device(device)
+        self.S, self.R, self.d, self.T = max_loras, rank, d, tokens
+        self.alpha = alpha
+        host = wl.churn_adapters(seed, n_adapters, d, rank)
+        # pinned host adapter store: per adapter, per layer A [r, d], B [d, r]
+        self.A = {k: to_torch(v[0], wl.DTYPE_BF16).pin_memory() for k, v in host.items()}
+        self.B = {k: to_torch(v[1], wl.DTYPE_BF16).pin_memory() for k, v in host.items()}
+        self.host_np = host
+        self.layers = ["q_proj", "v_proj"]
+        self.slots = LoraSlots([(d, d), (d, d)], max_loras, rank, tokens, dtype=torch.bfloat16,
+                               device=self.dev)
+        rng = np.random.default_rng(seed + 7)
+        xf = rng.standard_normal((tokens, d), dtype=np.float32)
+        self.x_np = wl.f32_to_bf16_bits(xf)
+        self.y_np = [wl.f32_to_bf16_bits(rng.standard_normal((tokens, d), dtype=np.float32)
+                                         * np.float32(0.02 * np.sqrt(d))) for _ in self.layers]
+        self.x = to_torch(self.x_np, wl.DTYPE_BF16).to(self.dev)
+        self.y0 = [to_torch(v, wl.DTYPE_BF16).to(self.dev) for v in self.y_np]
+        self.y = [t.clone() for t in self.y0]
+        # one slot-id buffer per adapter group of a step (a step has at most
+        # ceil(tokens / max_loras) groups); reused only after the step's sync
+        self.max_groups = (tokens + max_loras - 1) // max_loras
+        self.idx_host = torch.empty((self.max_groups, tokens), dtype=torch.int32).pin_memory()
+        self.idx = torch.empty((self.max_groups, tokens), dtype=torch.int32, device=self.dev)
+
+    def upload(self, slot, adapter):
+        a = [self.A[l][adapter] for l in self.layers]
+        b = [self.B[l][adapter] for l in self.layers]
+        self.slots.load_slot(slot, a, b, self.R, self.alpha)
+
+    def run(self, trace: wl.ChurnTrace, record=False, reset_y=True, check_step=None):
+        """Run every step of the trace; returns ChurnResult. With check_step=k
+        the outputs of step k (y after that step's groups, starting from the
+        base outputs) are kept in self.checked = (ids, slot_of_token, y_q, y_v)."""
+        decisions = []
+        tokens = 0
+        ctx = self.slots.ctx
+        lib = B.load()
+        torch.cuda.synchronize(self.dev)
+        t0 = time.perf_counter()
+        for k, ids in enumerate(trace.steps):
+            if reset_y or k == check_step:
+                with torch.cuda.stream(self.slots.compute):
+                    for y, y0 in zip(self.y, self.y0):
+                        y.copy_(y0)
+            order = list(dict.fromkeys(int(a) for a in ids))   # distinct, first appearance
+            slot_tok = np.full(self.T, -1, np.int32)
+            for gi, g0 in enumerate(range(0, len(order), self.S)):
+                group = order[g0:g0 + self.S]
+                held, where = [], {}
+                for a in group:
+                    st, slot, need, ev = B.lora_assign(ctx, a, self.R)
+                    if record:
+                        decisions.append((k, a, st, slot, need, ev))
+                    if st != 0:
+                        raise RuntimeError(f"assign failed for adapter {a}: {st}")
+                    if need:
+                        self.upload(slot, a)
+                    lib.lora_acquire(ctx, slot)
+                    held.append(slot)
+                    where[a] = slot
+                sel = np.isin(ids, group)
+                idx = np.where(sel, [where.get(int(a), -1) for a in ids], -1).astype(np.int32)
+                slot_tok[sel] = idx[sel]
+                self.idx_host[gi].numpy()[:] = idx
+                with torch.cuda.stream(self.slots.compute):
+                    self.idx[gi].copy_(self.idx_host[gi], non_blocking=True)
+                    self.slots.apply_multi([0, 1], [self.x, self.x], self.y, self.idx[gi])
+                for s in held:
+                    lib.lora_release(ctx, s)
+                tokens += int(sel.sum())
+            self.slots.compute.synchronize()       # slot-id buffers are reused next step
+            if k == check_step:
+                self.checked = (ids.copy(), slot_tok, [y.clone().cpu() for y in self.y])
+            B.lora_tick(ctx)
+        self.slots.compute.synchronize()
+        self.slots.sync_uploads()
+        wall = time.perf_counter() - t0
+        st = self.slots.stats()
+        return ChurnResult(len(trace.steps), wall, st, decisions, tokens)
+
+    def close(self):
+        self.slots.close()
