@@ -459,7 +459,8 @@ def run_big(args, name):
     from rank_adapter_apply_gb300 import build as build_mod
     from rank_adapter_apply_gb300.harness import DeviceWorkload
     build_mod.build()
-    w = wl.BY_NAME[name](0)
+    w = (wl.prefill_5120(0, n_seqs=args.prefill_seqs) if name == "prefill_5120"
+         else wl.BY_NAME[name](0))
     dw = DeviceWorkload(w, max_tokens=w.n_tokens)
     lys = list(range(len(w.layers)))
     xs = [dw.xs[ly.x_key] for ly in w.layers]
@@ -555,6 +556,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=[WORKLOAD, "prefill_5120", "mixed_ranks_8b", "churn_4096"])
+    ap.add_argument("--prefill-seqs", type=int, default=32,
+                    help="sequences in the prefill workload (32 = the full workload)")
     ap.add_argument("--quick", action="store_true",
                     help="profiling runs: no clock settling, no e2e, no CPU baseline")
     args = ap.parse_args()
