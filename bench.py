@@ -267,6 +267,8 @@ def run_ours(args):
         d = DevSet()
         d.slots = LoraSlots(layers, N_SLOTS, RANK, T_TOKENS, dtype=torch.bfloat16, device=dev,
                             compute_stream=stream, upload_stream=upload)
+        # every step's x, slot ids and pools are its own: the kernel before never writes them
+        B.lora_set_inputs_ready(d.slots.ctx, not args.no_early)
         for s in range(N_SLOTS):
             # admission: adapter id s -> slot (all misses on first sight), then upload
             rc, slot, need, _ = d.slots.assign(s, RANK)
@@ -363,7 +365,8 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2: {len(sets)} distinct x/y/idx/pool sets, "
                          f"{len(sets) * per_set / 2**20:.0f} MiB per cycle vs L2 {l2 / 2**20:.0f} MiB",
-                   "timing": "CUDA-graph replay, CUDA events on the launch stream"},
+                   "timing": "CUDA-graph replay, CUDA events on the launch stream",
+                   "inputs_ready": not args.no_early},
         "roofline": {"bound": "hbm",
                      "kernel": "decode_cluster_kernel (one launch per step: grouping, shrink and "
                                "expand of q_proj and v_proj)",
@@ -556,6 +559,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=[WORKLOAD, "prefill_5120", "mixed_ranks_8b", "churn_4096"])
+    ap.add_argument("--no-early", action="store_true",
+                    help="decode: do not declare inputs independent of the preceding kernel")
     ap.add_argument("--prefill-seqs", type=int, default=32,
                     help="sequences in the prefill workload (32 = the full workload)")
     ap.add_argument("--quick", action="store_true",

@@ -214,6 +214,18 @@ int lora_set_prefill_min_tokens(lora_ctx *ctx, int n);
  */
 int lora_set_small_batch_tokens(lora_ctx *ctx, int n);
 
+/*
+ * on != 0 declares that, for every following apply call on this context, x,
+ * token_slot_idx, the slot pools and scale_dev / rank_dev are not written by
+ * the kernel launched immediately before that call on the compute stream (y
+ * may be: the usual case of a base-model GEMM writing y right before the
+ * delta is added). The single-launch decode kernel then starts while that
+ * kernel finishes (programmatic dependent launch), groups the tokens and
+ * loads x and the slot weights early, and waits for it only before reading y.
+ * Default 0: everything waits for the preceding kernel.
+ */
+int lora_set_inputs_ready(lora_ctx *ctx, int on);
+
 /* Block until every queued upload finished; accumulates upload_seconds. */
 int lora_sync_uploads(lora_ctx *ctx);
 

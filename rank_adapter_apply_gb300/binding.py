@@ -30,7 +30,7 @@ EXPORTED = [
     "lora_workspace_bytes", "lora_slots_init", "lora_destroy", "lora_load_slot", "lora_apply",
     "lora_apply_multi", "lora_apply_multi_host", "lora_lookup", "lora_assign", "lora_acquire",
     "lora_release", "lora_evict_lru", "lora_tick", "lora_set_thrash_window",
-    "lora_set_prefill_min_tokens", "lora_set_small_batch_tokens", "lora_sync_uploads", "lora_stats", "lora_adapter_bytes",
+    "lora_set_prefill_min_tokens", "lora_set_small_batch_tokens", "lora_set_inputs_ready", "lora_sync_uploads", "lora_stats", "lora_adapter_bytes",
     "lora_last_error", "lora_apply_static_scratch",
 ]
 
@@ -90,6 +90,7 @@ def load(path: str = LIB_PATH):
         "lora_set_thrash_window": (i32, [vp, i32]),
         "lora_set_prefill_min_tokens": (i32, [vp, i32]),
         "lora_set_small_batch_tokens": (i32, [vp, i32]),
+        "lora_set_inputs_ready": (i32, [vp, i32]),
         "lora_sync_uploads": (i32, [vp]),
         "lora_stats": (i32, [vp, P(LoraStats)]),
         "lora_adapter_bytes": (u64, [i32, P(i32), P(i32), i32, i32]),
@@ -210,6 +211,10 @@ def lora_set_prefill_min_tokens(ctx, n):
 
 def lora_set_small_batch_tokens(ctx, n):
     return check(load().lora_set_small_batch_tokens(ctx, n))
+
+
+def lora_set_inputs_ready(ctx, on):
+    return check(load().lora_set_inputs_ready(ctx, 1 if on else 0))
 
 
 def lora_sync_uploads(ctx):

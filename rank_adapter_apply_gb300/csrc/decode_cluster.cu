@@ -142,9 +142,11 @@ __device__ void issue_shrink(const LayerArgs &L, const ClusterSmem &sm, Dyn<KB> 
 }
 
 // Expand stage j: y rows of the tile and B rows [os, os + w) of the slot.
+// parts: 1 = B rows only (no arrival yet), 2 = y rows and the stage arrival,
+// 3 = both. Splitting lets B be fetched before the wait on the previous kernel.
 template <int KB>
 __device__ void issue_expand(const LayerArgs &L, const ClusterSmem &sm, Dyn<KB> &d, const Tile &t,
-                             int R, int o0, int o1, int j, uint64_t *bar) {
+                             int R, int o0, int o1, int j, uint64_t *bar, int parts = 3) {
     const int b = j & 1;
     const int os = o0 + j * kSW, w = min(kSW, o1 - os);
     const int cpr = w >> 3;
@@ -152,18 +154,20 @@ __device__ void issue_expand(const LayerArgs &L, const ClusterSmem &sm, Dyn<KB> 
     const uint16_t *B = static_cast<const uint16_t *>(L.B) + ((size_t)t.s * L.d_out + os) * R;
     uint16_t *ys = d.ys + b * kTileTokens * kSW;
     uint16_t *bs = d.bs + (size_t)b * kSW * KB * 16;
-    const int ny = t.cnt * cpr, nb = (w * R) >> 3;
-    for (int e = threadIdx.x; e < ny + nb; e += kCT) {
-        if (e < ny) {
-            const int row = e / cpr, col = (e - row * cpr) * 8;
-            cp_async16(ys + swz(row, col), y + (size_t)sm.tok[row] * L.d_out + os + col);
-        } else {
-            const int q = (e - ny) * 8;             // element offset in the contiguous block
+    if (parts & 1) {
+        for (int e = threadIdx.x; e < (w * R) >> 3; e += kCT) {
+            const int q = e * 8;                  // element offset in the contiguous block
             const int P = q / R;
             cp_async16(bs + bsw(P, q - P * R, R), B + q);
         }
     }
-    cp_async_arrive_noinc(bar);
+    if (parts & 2) {
+        for (int e = threadIdx.x; e < t.cnt * cpr; e += kCT) {
+            const int row = e / cpr, col = (e - row * cpr) * 8;
+            cp_async16(ys + swz(row, col), y + (size_t)sm.tok[row] * L.d_out + os + col);
+        }
+        cp_async_arrive_noinc(bar);
+    }
 }
 
 template <int KB>
@@ -179,8 +183,10 @@ decode_cluster_kernel(const __grid_constant__ FusedArgs fa) {
     const LayerArgs &L = fa.l[blockIdx.y];
 
     // Inputs may come from the previous kernel in the stream: wait for it, then
-    // let the next launch start filling free SMs.
-    grid_dependency_wait();
+    // let the next launch start filling free SMs. With fa.early the caller has
+    // declared that only y can be written by that kernel: everything else is
+    // read before the wait, y after it.
+    if (!fa.early) grid_dependency_wait();
     grid_launch_dependents();
 
     // ---- group the batch by slot (every CTA, from shared memory) ----------
@@ -290,7 +296,13 @@ decode_cluster_kernel(const __grid_constant__ FusedArgs fa) {
 
     // ---- issue everything that fits in the stage rings --------------------
     for (int j = 0; j < nks && j < 2; ++j) issue_shrink<KB>(L, sm, d, t, R, k0, k1, j, &sm.sbar[j]);
-    for (int j = 0; j < nes && j < 2; ++j) issue_expand<KB>(L, sm, d, t, R, o0, o1, j, &sm.ebar[j]);
+    if (fa.early) {
+        for (int j = 0; j < nes && j < 2; ++j) issue_expand<KB>(L, sm, d, t, R, o0, o1, j, &sm.ebar[j], 1);
+        grid_dependency_wait();
+        for (int j = 0; j < nes && j < 2; ++j) issue_expand<KB>(L, sm, d, t, R, o0, o1, j, &sm.ebar[j], 2);
+    } else {
+        for (int j = 0; j < nes && j < 2; ++j) issue_expand<KB>(L, sm, d, t, R, o0, o1, j, &sm.ebar[j]);
+    }
     bool ok = true;
 
     // ---- shrink over this CTA's d_in slice ---------------------------------

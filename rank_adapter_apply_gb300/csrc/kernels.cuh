@@ -102,6 +102,7 @@ struct FusedArgs {
     const int *rank;
     const float *scale;
     int *hdr;                         // workspace header: invalid-index count, error word
+    int early;                        // read all but y before waiting on the previous kernel
 };
 constexpr int kClusterSize = 8;
 int cluster_decode_kb(int R);

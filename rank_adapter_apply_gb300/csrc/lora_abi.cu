@@ -72,6 +72,7 @@ struct lora_ctx {
     uint64_t uploads = 0, upload_bytes = 0, invalid_seen = 0;
     int prefill_min = 0;          // shortest same-slot run sent to the tensor-core prefill kernel
     int small_batch = kFusedMaxTokens;   // batches up to this size take the cluster decode kernel
+    int inputs_ready = 0;         // caller: x, slot ids, pools not written by the preceding kernel
     int num_sms = 148;
 
     lora_ctx(int S_, int R_) : table(S_, R_) {}
@@ -305,6 +306,7 @@ int fused_apply(lora_ctx *c, int n, const int *layers, const void *const *xs, vo
     fa.rank = c->rank_dev;
     fa.scale = c->scale_dev;
     fa.hdr = reinterpret_cast<int *>(c->ws + c->lay.hdr);
+    fa.early = c->inputs_ready;
     CUDA_TRY(launch_cluster_decode(fa, est_tiles, c->compute, true));
     if (!capturing(c->compute)) {
         CUDA_TRY(cudaEventRecord(c->compute_done, c->compute));
@@ -545,6 +547,12 @@ int lora_set_prefill_min_tokens(lora_ctx *c, int n) {
 int lora_set_small_batch_tokens(lora_ctx *c, int n) {
     if (!c || n < 0 || n > kFusedMaxTokens) return fail(LORA_ERR_ARG, "n must be in 0..%d", kFusedMaxTokens);
     c->small_batch = n;
+    return LORA_OK;
+}
+
+int lora_set_inputs_ready(lora_ctx *c, int on) {
+    if (!c) return fail(LORA_ERR_ARG, "ctx is NULL");
+    c->inputs_ready = on ? 1 : 0;
     return LORA_OK;
 }
 

@@ -195,3 +195,23 @@ def test_prefill_disabled_matches_oracle():
     out, _ = _run(w, small_batch_tokens=0, prefill_min_tokens=0)
     for ly in w.layers:
         check_layer(w, ly.name, out[ly.name])
+
+
+def test_inputs_ready_back_to_back():
+    """Early input loads: several applies in a row on one context with
+    lora_set_inputs_ready, the second layer's y depending on nothing else."""
+    from rank_adapter_apply_gb300 import binding as B
+    from rank_adapter_apply_gb300.harness import DeviceWorkload
+    w = wl.decode_qv_4096(5)
+    dw = DeviceWorkload(w)
+    try:
+        B.lora_set_inputs_ready(dw.slots.ctx, True)
+        for rep in range(3):
+            dw.reset()
+            out = dw.run(["q_proj"], multi=False)
+            out.update(dw.run(["v_proj"], multi=False))
+            for name, y in out.items():
+                check_layer(w, name, y)
+        assert dw.slots.stats()["device_wait_timeouts"] == 0
+    finally:
+        dw.close()
