@@ -66,12 +66,16 @@ struct ClusterSmem {
 };
 
 // Dynamic shared memory of one CTA for a given number of 16-rank blocks.
+// Region 1 holds the two shrink stages (x rows, A rows) and, once the shrink
+// has consumed them, the two expand stages (y rows, B rows) in the same bytes.
+__host__ __device__ constexpr size_t region1_bytes(int KB) {
+    return 2 * (size_t)kTileTokens * kSW * 2 + 2 * (size_t)KB * 16 * kSW * 2;
+}
 __host__ __device__ constexpr size_t dyn_bytes(int KB) {
-    return 2 * (size_t)kTileTokens * kSW * 2          // x stages
-           + 2 * (size_t)KB * 16 * kSW * 2            // A stages
-           + 2 * (size_t)kTileTokens * kSW * 2        // y stages
-           + 2 * (size_t)kSW * KB * 16 * 2            // B stages
-           + (size_t)kCl * kTileTokens * KB * 16 * 4;   // partials pushed by the 8 ranks
+    return region1_bytes(KB)
+           + (size_t)kCl * kTileTokens * KB * 16 * 4   // partials pushed by the 8 ranks
+           + (size_t)kCW * KB * 8 * 32 * 4              // cross-warp sums of the shrink
+           + (size_t)kTileTokens * KB * 16 * 4;         // v = sum of the partials
 }
 static_assert(sizeof(GroupScratch) <= (size_t)kCl * kTileTokens * 16 * 4, "grouping scratch fits");
 
@@ -79,15 +83,17 @@ template <int KB>
 struct Dyn {
     uint16_t *xs, *as, *ys, *bs;
     float *vpart;                            // [kCl][16][KB*16] partials pushed by each rank
-    float *vsum;                             // [16][KB*16], in the idle x stages
+    float *red;                              // [kCW][KB*8][32]
+    float *vsum;                             // [16][KB*16]
     GroupScratch *g;                         // prologue only, aliases vpart
     __device__ Dyn(uint8_t *base) {
         xs = reinterpret_cast<uint16_t *>(base);
         as = xs + 2 * kTileTokens * kSW;
-        ys = as + 2 * KB * 16 * kSW;
-        bs = ys + 2 * kTileTokens * kSW;
-        vpart = reinterpret_cast<float *>(bs + 2 * kSW * KB * 16);
-        vsum = reinterpret_cast<float *>(xs) + KB * 1024; // past the cross-warp scratch (x/A stages idle)
+        ys = xs;                                             // after the shrink
+        bs = xs + 2 * kTileTokens * kSW;                     // after the shrink
+        vpart = reinterpret_cast<float *>(base + region1_bytes(KB));
+        red = vpart + kCl * kTileTokens * KB * 16;
+        vsum = red + kCW * KB * 8 * 32;
         g = reinterpret_cast<GroupScratch *>(vpart);
     }
 };
@@ -296,13 +302,6 @@ decode_cluster_kernel(const __grid_constant__ FusedArgs fa) {
 
     // ---- issue everything that fits in the stage rings --------------------
     for (int j = 0; j < nks && j < 2; ++j) issue_shrink<KB>(L, sm, d, t, R, k0, k1, j, &sm.sbar[j]);
-    if (fa.early) {
-        for (int j = 0; j < nes && j < 2; ++j) issue_expand<KB>(L, sm, d, t, R, o0, o1, j, &sm.ebar[j], 1);
-        grid_dependency_wait();
-        for (int j = 0; j < nes && j < 2; ++j) issue_expand<KB>(L, sm, d, t, R, o0, o1, j, &sm.ebar[j], 2);
-    } else {
-        for (int j = 0; j < nes && j < 2; ++j) issue_expand<KB>(L, sm, d, t, R, o0, o1, j, &sm.ebar[j]);
-    }
     bool ok = true;
 
     // ---- shrink over this CTA's d_in slice ---------------------------------
@@ -342,8 +341,15 @@ decode_cluster_kernel(const __grid_constant__ FusedArgs fa) {
         if (j + 2 < nks) issue_shrink<KB>(L, sm, d, t, R, k0, k1, j + 2, &sm.sbar[b]);
     }
 
-    // Cross-warp sum into this CTA's partial v[token][k] (the x stages are idle now).
-    float *red = reinterpret_cast<float *>(d.xs);        // [kCW][KB*8][32]
+    // The shrink stages are consumed: the same bytes now receive the expand
+    // stages. B never depends on the previous kernel; y may (fa.early waits here).
+    __syncthreads();
+    for (int j = 0; j < nes && j < 2; ++j) issue_expand<KB>(L, sm, d, t, R, o0, o1, j, &sm.ebar[j], 1);
+    if (fa.early) grid_dependency_wait();
+    for (int j = 0; j < nes && j < 2; ++j) issue_expand<KB>(L, sm, d, t, R, o0, o1, j, &sm.ebar[j], 2);
+
+    // Cross-warp sum into this CTA's partial v[token][k].
+    float *red = d.red;
 #pragma unroll
     for (int m = 0; m < KB; ++m)
 #pragma unroll
