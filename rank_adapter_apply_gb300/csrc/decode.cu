@@ -62,11 +62,7 @@ __device__ void finish_split(const LayerArgs &L, const GroupView &g, int tile_i,
 // 32-column steps. Per warp and step: m16n8k16 with M = 16 ranks (per 16-rank
 // block), N = 8 tokens (two token blocks), K = 16 (two MMAs per 32 columns).
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads)
-shrink_bf16_kernel(MultiArgs ma, GroupView g) {
-    const LayerArgs &L = ma.l[blockIdx.z];
-    const int chunk = blockIdx.x, tile_i = blockIdx.y;
-    if (chunk >= L.n_chunks || tile_i >= g.hdr[kHdrTiles]) return;
+__device__ __forceinline__ void shrink_bf16_tile(const LayerArgs &L, const GroupView &g, int chunk, int tile_i) {
     const int4 tile = g.tiles[tile_i];
     const int s = tile.x, p0 = tile.y, cnt = tile.z;
     const int r = g.rank[s];
@@ -137,12 +133,8 @@ shrink_bf16_kernel(MultiArgs ma, GroupView g) {
 // N = 8 columns, K = 16 ranks, columns permuted so that each lane ends with 8
 // consecutive outputs of two token rows (one 128-bit y access per row).
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads)
-expand_bf16_kernel(MultiArgs ma, GroupView g) {
-    const LayerArgs &L = ma.l[blockIdx.z];
-    const int tile_i = blockIdx.y;
+__device__ __forceinline__ void expand_bf16_tile(const LayerArgs &L, const GroupView &g, int tile_i) {
     const int d_out = L.d_out;
-    if (blockIdx.x * kExpandCols >= d_out || tile_i >= g.hdr[kHdrTiles]) return;
     const int4 tile = g.tiles[tile_i];
     const int s = tile.x, p0 = tile.y, cnt = tile.z;
     const int r = g.rank[s];
@@ -252,11 +244,7 @@ expand_bf16_kernel(MultiArgs ma, GroupView g) {
 // fp32 shrink: one warp per token of the tile, lanes stride the chunk, one
 // warp-shuffle reduction per rank.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads)
-shrink_f32_kernel(MultiArgs ma, GroupView g) {
-    const LayerArgs &L = ma.l[blockIdx.z];
-    const int chunk = blockIdx.x, tile_i = blockIdx.y;
-    if (chunk >= L.n_chunks || tile_i >= g.hdr[kHdrTiles]) return;
+__device__ __forceinline__ void shrink_f32_tile(const LayerArgs &L, const GroupView &g, int chunk, int tile_i) {
     const int4 tile = g.tiles[tile_i];
     const int s = tile.x, p0 = tile.y, cnt = tile.z;
     const int r = g.rank[s];
@@ -282,12 +270,8 @@ shrink_f32_kernel(MultiArgs ma, GroupView g) {
 }
 
 // fp32 expand-add: each thread owns two columns of the 256-column block.
-__global__ void __launch_bounds__(kThreads)
-expand_f32_kernel(MultiArgs ma, GroupView g) {
-    const LayerArgs &L = ma.l[blockIdx.z];
-    const int tile_i = blockIdx.y;
+__device__ __forceinline__ void expand_f32_tile(const LayerArgs &L, const GroupView &g, int tile_i) {
     const int d_out = L.d_out;
-    if (blockIdx.x * kExpandCols >= d_out || tile_i >= g.hdr[kHdrTiles]) return;
     const int4 tile = g.tiles[tile_i];
     const int s = tile.x, p0 = tile.y, cnt = tile.z;
     const int r = g.rank[s];
@@ -312,6 +296,51 @@ expand_f32_kernel(MultiArgs ma, GroupView g) {
     }
 }
 
+// The kernels: CTA = (chunk or column block, tile slot, layer). Tiles are
+// taken with a stride of gridDim.y, so the grid stays a few waves deep even
+// when the host can only bound the tile count (a prefill batch leaves few or
+// no decode tiles, and the count is known on the device only).
+__global__ void __launch_bounds__(kThreads)
+shrink_bf16_kernel(MultiArgs ma, GroupView g) {
+    const LayerArgs &L = ma.l[blockIdx.z];
+    if ((int)blockIdx.x >= L.n_chunks) return;
+    const int nt = g.hdr[kHdrTiles];
+    for (int t = blockIdx.y; t < nt; t += gridDim.y) {
+        shrink_bf16_tile(L, g, blockIdx.x, t);
+        __syncthreads();
+    }
+}
+
+__global__ void __launch_bounds__(kThreads)
+expand_bf16_kernel(MultiArgs ma, GroupView g) {
+    const LayerArgs &L = ma.l[blockIdx.z];
+    if ((int)blockIdx.x * kExpandCols >= L.d_out) return;
+    const int nt = g.hdr[kHdrTiles];
+    for (int t = blockIdx.y; t < nt; t += gridDim.y) expand_bf16_tile(L, g, t);
+}
+
+__global__ void __launch_bounds__(kThreads)
+shrink_f32_kernel(MultiArgs ma, GroupView g) {
+    const LayerArgs &L = ma.l[blockIdx.z];
+    if ((int)blockIdx.x >= L.n_chunks) return;
+    const int nt = g.hdr[kHdrTiles];
+    for (int t = blockIdx.y; t < nt; t += gridDim.y) {
+        shrink_f32_tile(L, g, blockIdx.x, t);
+        __syncthreads();
+    }
+}
+
+__global__ void __launch_bounds__(kThreads)
+expand_f32_kernel(MultiArgs ma, GroupView g) {
+    const LayerArgs &L = ma.l[blockIdx.z];
+    if ((int)blockIdx.x * kExpandCols >= L.d_out) return;
+    const int nt = g.hdr[kHdrTiles];
+    for (int t = blockIdx.y; t < nt; t += gridDim.y) {
+        expand_f32_tile(L, g, t);
+        __syncthreads();
+    }
+}
+
 __global__ void set_slot_kernel(float *scale_dev, int *rank_dev, int slot, float scale, int rank) {
     scale_dev[slot] = scale;
     rank_dev[slot] = rank;
@@ -320,9 +349,16 @@ __global__ void set_slot_kernel(float *scale_dev, int *rank_dev, int slot, float
 }  // namespace
 
 cudaError_t launch_decode(const MultiArgs &ma, const GroupView &gv, int dtype, int grid_tiles,
-                          int max_chunks, int max_dblocks, cudaStream_t st) {
+                          int max_chunks, int max_dblocks, int num_sms, cudaStream_t st) {
     if (grid_tiles <= 0) return cudaSuccess;
-    dim3 gs(max_chunks, grid_tiles, ma.n), ge(max_dblocks, grid_tiles, ma.n);
+    // At most ~16 CTAs per SM per launch; the tile loop covers the rest.
+    const long long cap = 16LL * (num_sms > 0 ? num_sms : 1);
+    auto rows = [&](int gx) {
+        long long y = cap / ((long long)gx * ma.n);
+        if (y < 1) y = 1;
+        return (int)(y < grid_tiles ? y : grid_tiles);
+    };
+    dim3 gs(max_chunks, rows(max_chunks), ma.n), ge(max_dblocks, rows(max_dblocks), ma.n);
     if (dtype == 1) {
         shrink_bf16_kernel<<<gs, kThreads, 0, st>>>(ma, gv);
         expand_bf16_kernel<<<ge, kThreads, 0, st>>>(ma, gv);

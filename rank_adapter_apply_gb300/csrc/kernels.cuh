@@ -89,7 +89,7 @@ struct GroupView {
 cudaError_t launch_group_tokens(const int32_t *idx, int T, const int *rank_dev, int S,
                                 int min_run, char *ws, const WsLayout &lay, cudaStream_t st);
 cudaError_t launch_decode(const MultiArgs &ma, const GroupView &gv, int dtype, int grid_tiles,
-                          int max_chunks, int max_dblocks, cudaStream_t st);
+                          int max_chunks, int max_dblocks, int num_sms, cudaStream_t st);
 // Single-launch decode step on 8-CTA clusters, batches of at most
 // kFusedMaxTokens bf16 tokens: one cluster per (layer, tile of <= 16 tokens),
 // CTA c of a cluster owns columns [c*chunk_cols, ...) of d_in and
@@ -109,20 +109,22 @@ int cluster_decode_kb(int R);
 size_t cluster_decode_smem(int R);
 cudaError_t launch_cluster_decode(const FusedArgs &fa, int tiles, cudaStream_t st, bool pdl);
 
-// Tensor-core prefill of one layer over the prefill tiles of the workspace.
-struct PrefillArgs {
-    CUtensorMap mx, ma, mb, my;   // x [T][d_in], A pool [S*R][d_in], B pool [S*d_out][R], y [T][d_out]
-    uint16_t *y;
+// Tensor-core prefill over the prefill tiles of the workspace, every layer of
+// one call: a shrink kernel that reads each x tile once for all the layers
+// sharing that input and writes fp32 partials of V = x A^T, then a persistent
+// expand kernel that streams y through a TMA ring and adds scale * V B^T.
+struct PrefillLayer {
+    const void *x;        // [T][d_in] bf16
+    void *y;              // [T][d_out] bf16, updated in place
+    const void *A;        // pool [S][R][d_in]
+    const void *B;        // pool [S][d_out][R]
+    float *part;          // [part_rows][R] fp32 partials of V (chunk c at row c*T)
     int d_in, d_out;
-    const float *scale;
-    int *hdr;
-    const int4 *ptiles;
-    int cols_per_split;           // d_out columns per CTA (multiple of 64)
 };
 bool prefill_tc_supported(int R);
-cudaError_t launch_prefill_tc(const void *x, void *y, int T, int d_in, int d_out, const void *A_pool,
-                              const void *B_pool, int S, int R, const float *scale, const int *hdr,
-                              const int4 *ptiles, int grid_tiles, int nsplit, cudaStream_t st);
+cudaError_t launch_prefill_tc(const PrefillLayer *layers, int n, int T, int S, int R, const float *scale,
+                              int *hdr, const int4 *ptiles, int grid_tiles, int part_rows, int num_sms,
+                              cudaStream_t st);
 
 // Record the message returned by lora_last_error() for this thread; returns code.
 int set_last_error(int code, const char *msg);

@@ -362,22 +362,21 @@ int apply_impl(lora_ctx *c, int n, const int *layers, const void *const *xs, voi
         // upper bound on prefill tiles: T/128 full tiles plus one ragged tile per run
         int grid_tiles = T / kPrefillRows + T / c->prefill_min + 2;
         if (grid_tiles > c->lay.max_ptiles) grid_tiles = c->lay.max_ptiles;
-        const int est = T / kPrefillRows + 1;
+        PrefillLayer pl[kMaxLayersPerCall];
         for (int i = 0; i < n; ++i) {
             const lora_layer_desc &L = c->layers[layers[i]];
-            // about three waves of resident CTAs (two per SM) across the d_out splits
-            int nsplit = (3 * 2 * c->num_sms + est - 1) / est;
-            const int max_split = L.d_out / 64;
-            if (nsplit > max_split) nsplit = max_split;
-            if (nsplit > 16) nsplit = 16;
-            if (nsplit < 1) nsplit = 1;
-            cudaError_t e = launch_prefill_tc(
-                xs[i], ys[i], T, L.d_in, L.d_out, L.A_pool, L.B_pool, c->S, c->R, c->scale_dev,
-                reinterpret_cast<const int *>(c->ws + c->lay.hdr),
-                reinterpret_cast<const int4 *>(c->ws + c->lay.ptiles), grid_tiles, nsplit, c->compute);
-            if (e != cudaSuccess)
-                return fail(LORA_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
+            pl[i].x = xs[i];
+            pl[i].y = ys[i];
+            pl[i].A = L.A_pool;
+            pl[i].B = L.B_pool;
+            pl[i].part = reinterpret_cast<float *>(c->ws + c->lay.part) + (size_t)i * c->lay.part_rows * c->R;
+            pl[i].d_in = L.d_in;
+            pl[i].d_out = L.d_out;
         }
+        cudaError_t e = launch_prefill_tc(pl, n, T, c->S, c->R, c->scale_dev, reinterpret_cast<int *>(c->ws + c->lay.hdr),
+                                          reinterpret_cast<const int4 *>(c->ws + c->lay.ptiles), grid_tiles,
+                                          c->lay.part_rows, c->num_sms, c->compute);
+        if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
     }
 
     const size_t e = elem_bytes(c->dtype);
@@ -425,7 +424,7 @@ int apply_impl(lora_ctx *c, int n, const int *layers, const void *const *xs, voi
     gv.R = c->R;
     gv.T = T;
     int grid_tiles = est_tiles < c->lay.max_tiles ? est_tiles : c->lay.max_tiles;
-    CUDA_TRY(launch_decode(ma, gv, c->dtype, grid_tiles, max_chunks, max_dblocks, c->compute));
+    CUDA_TRY(launch_decode(ma, gv, c->dtype, grid_tiles, max_chunks, max_dblocks, c->num_sms, c->compute));
     if (!capturing(c->compute)) {
         CUDA_TRY(cudaEventRecord(c->compute_done, c->compute));
         c->compute_recorded = true;

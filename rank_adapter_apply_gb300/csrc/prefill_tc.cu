@@ -12,17 +12,30 @@
 // LoRA Resolver 插件详解" page, section 3.2). Slot pools are zero-padded to
 // R = max_lora_rank, so the padded ranks contribute exact zeros.
 //
-// One CTA owns one tile (<= 128 rows of one run) and one range of d_out
-// columns. Warp roles:
-//   warp 0      TMA producer: X / A_s k-blocks (64 columns), then y / B_s
-//               n-blocks (64 columns), through one 3-stage shared-memory ring;
-//   warp 1      allocates TMEM and issues every tcgen05.mma from one thread;
-//   warps 4..7  epilogue, one TMEM lane (= one tile row) per thread:
-//               V (fp32 in TMEM) -> bf16 high + low parts in swizzled shared
-//               memory (the A operand of the expand, so V keeps ~16
-//               significant bits); then per n-block y = round(y + scale * D).
-// TMEM columns: [0, R) shrink accumulator, [64, 128) and [128, 192) the two
-// expand accumulators. Every mbarrier wait is bounded.
+// Two kernels per call, both HBM-bound:
+//
+// prefill_shrink_kernel  one CTA per (tile, input group, d_in chunk). An input
+//   group is the set of layers of the call that read the same x (q/k/v, or
+//   gate/up), so each x tile crosses HBM once for all of them. A TMA producer
+//   warp streams 64-column k-blocks of x and of every A_s of the group through
+//   a shared-memory ring; one thread issues tcgen05.mma (M 128, N R, K 16) into
+//   one TMEM accumulator per layer; four epilogue warps write the fp32 partial
+//   V of their rows to the workspace (chunk c of layer l at rows c*T + t).
+//
+// prefill_expand_kernel  persistent, one CTA per SM. The work items are
+//   (layer, tile, 256-column block of d_out), split into contiguous ranges.
+//   The epilogue warps sum the partials of V in a fixed order, split V into
+//   bf16 high + low parts in swizzled shared memory (double-buffered across
+//   tiles), the producer streams y and B_s n-blocks (64 columns) through the
+//   ring, one thread issues the expand MMAs (M 128, N 64, K R, twice: high
+//   and low parts) into rotating TMEM accumulators, and the epilogue computes
+//   y = round(y + scale * D) in place in the ring and stores full tiles back
+//   with a TMA store (ragged tiles with plain row stores, so that no row of a
+//   neighbouring run is touched).
+//
+// Every mbarrier wait is bounded; a wait that gives up sets the workspace
+// error word, the CTA stops issuing work, drains the copies and MMAs it has in
+// flight, frees its TMEM and returns.
 #include "device_util.cuh"
 #include "kernels.cuh"
 #include "tc_util.cuh"
@@ -35,243 +48,486 @@
 namespace lora {
 namespace {
 
-constexpr int kPT = 256;                   // 8 warps
-constexpr int kStages = 3;
-constexpr int kStageBytes = 24576;         // 16 KB (X or y tile) + 8 KB (A or B tile)
-constexpr int kTileBytes = 16384;          // 128 rows x 64 bf16
-constexpr int kTmemCols = 256;
-constexpr uint32_t kAcc2Col = 64;
-constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr int kThreads = 192;              // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kTileBytes = 16384;          // 128 rows x 64 bf16: one x k-block or one y n-block
+constexpr int kColBlock = 256;             // d_out columns per expand work item
+constexpr int kAcc = 4;                    // expand accumulators (64 TMEM columns each)
+constexpr int kMaxStages = 8;
+constexpr int kMaxJobs = 64;
+constexpr uint32_t kWaitLimit = 1u << 22;
 
-struct PrefillSmem {
-    uint64_t full[kStages], empty[kStages];
-    uint64_t acc1_full, v_ready;
-    uint64_t acc2_full[2], acc2_empty[2];
-    uint32_t tmem_base;
-    int error;
-};
-
-__host__ __device__ constexpr size_t prefill_smem_bytes(int R) {
-    return 1024 /* alignment slack */ + (size_t)kStages * kStageBytes + 2 * 128 * (size_t)R * 2 +
-           sizeof(PrefillSmem);
-}
-
-__device__ __forceinline__ bool wait(uint64_t *bar, uint32_t parity, int *err) {
+// Wait for a phase unless an earlier wait of this CTA already gave up.
+__device__ __forceinline__ bool wait_ok(uint64_t *bar, uint32_t parity, volatile int *flag) {
+    if (*flag) return false;
     if (mbar_wait_bounded(bar, parity, kWaitLimit)) return true;
-    *err = 1;
+    *flag = 1;
     return false;
 }
 
+__host__ __device__ inline uint32_t tmem_cols_for(int cols) {
+    uint32_t c = 32;
+    while ((int)c < cols) c <<= 1;
+    return c;
+}
+
+// Row i of a K-major operand of R bf16 per row, in the swizzle the TMA and
+// the MMA descriptors use for that row width: 16-byte chunk c of the row goes
+// to chunk c ^ f(i).
 template <int R>
-__global__ void __launch_bounds__(kPT, 2)
-prefill_tc_kernel(const __grid_constant__ PrefillArgs pa) {
+__device__ __forceinline__ int swz_chunk(int c, int i) {
+    if constexpr (R == 64) return c ^ (i & 7);
+    else if constexpr (R == 32) return c ^ ((i >> 1) & 3);
+    else return c ^ ((i >> 2) & 1);
+}
+
+template <int R>
+__device__ __forceinline__ void tmem_ld_row(uint32_t taddr, float (&v)[R]) {
+    if constexpr (R == 16) {
+        uint32_t r[16];
+        tc::tmem_ld16_sync(taddr, r);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[k] = __uint_as_float(r[k]);
+    } else {
+#pragma unroll
+        for (int c = 0; c < R / 32; ++c) {
+            uint32_t r[32];
+            tc::tmem_ld32_sync(taddr + 32 * c, r);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[32 * c + k] = __uint_as_float(r[k]);
+        }
+    }
+}
+
+// ============================================================================
+// Shrink
+// ============================================================================
+
+struct ShrinkJob {
+    int group, chunk, kb0, kb1;               // k-blocks [kb0, kb1) of d_in
+};
+
+struct ShrinkArgs {
+    CUtensorMap mx[kMaxLayersPerCall];        // per group: x [T][d_in], box 64 x 128
+    CUtensorMap ma[kMaxLayersPerCall];        // per member (group order): A pool [S*R][d_in], box 64 x R
+    float *part[kMaxLayersPerCall];           // per member
+    int g_first[kMaxLayersPerCall], g_count[kMaxLayersPerCall];
+    ShrinkJob jobs[kMaxJobs];
+    const int4 *ptiles;
+    int *hdr;
+    int T, stages, tmem_cols;
+};
+
+template <int R>
+__global__ void __launch_bounds__(kThreads, 2)
+prefill_shrink_kernel(const __grid_constant__ ShrinkArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *ring = base;
-    uint8_t *v_hi = base + kStages * kStageBytes;
-    uint8_t *v_lo = v_hi + 128 * R * 2;
-    PrefillSmem &sm = *reinterpret_cast<PrefillSmem *>(v_lo + 128 * R * 2);
-    constexpr int W = R * 2;                                   // bytes per V / B row
-    constexpr uint32_t kSwzRank = R == 64 ? tc::kSwz128 : (R == 32 ? tc::kSwz64 : tc::kSwz32);
+    __shared__ uint64_t full[kMaxStages], empty[kMaxStages], acc_full, drained;
+    __shared__ uint32_t tmem_base;
+    __shared__ int error;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n_tiles = pa.hdr[kHdrPrefillTiles];
-    if ((int)blockIdx.x >= n_tiles) return;
-    const int4 pt = pa.ptiles[blockIdx.x];
+    if ((int)blockIdx.x >= a.hdr[kHdrPrefillTiles]) return;
+    const int4 pt = a.ptiles[blockIdx.x];
     const int s = pt.x, row0 = pt.y, rows = pt.z;
-    const int o_begin = blockIdx.y * pa.cols_per_split;
-    const int o_end = min(pa.d_out, o_begin + pa.cols_per_split);
-    if (o_begin >= o_end) return;
-    const int nk = (pa.d_in + 63) / 64;
-    const int nn = (o_end - o_begin + 63) / 64;
+    const ShrinkJob job = a.jobs[blockIdx.y];
+    const int g = job.group, nl = a.g_count[g], m0 = a.g_first[g];
+    const int stages = a.stages;
+    const uint32_t stage_bytes = kTileBytes + (uint32_t)nl * R * 128;
 
     if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) {
-            mbar_init(&sm.full[i], 1);
-            mbar_init(&sm.empty[i], 2);          // MMA completion + epilogue (n-blocks) or MMA again
+        for (int i = 0; i < stages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
         }
-        mbar_init(&sm.acc1_full, 1);
-        mbar_init(&sm.v_ready, 128);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&sm.acc2_full[i], 1);
-            mbar_init(&sm.acc2_empty[i], 128);
-        }
-        sm.error = 0;
+        mbar_init(&acc_full, 1);
+        mbar_init(&drained, 1);
+        error = 0;
         fence_mbar_init();
-        tc::prefetch_tensormap(&pa.mx);
-        tc::prefetch_tensormap(&pa.ma);
-        tc::prefetch_tensormap(&pa.mb);
-        tc::prefetch_tensormap(&pa.my);
+        tc::prefetch_tensormap(&a.mx[g]);
+        for (int l = 0; l < nl; ++l) tc::prefetch_tensormap(&a.ma[m0 + l]);
     }
     if (warp == 1) {
-        tc::tmem_alloc(&sm.tmem_base, kTmemCols);
+        tc::tmem_alloc(&tmem_base, (uint32_t)a.tmem_cols);
         tc::tmem_relinquish();
     }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    const uint32_t tmem = sm.tmem_base;
-    int err = 0;
+    const uint32_t tmem = tmem_base;
+    volatile int *err = &error;
+    const int nkb = job.kb1 - job.kb0;
 
     if (warp == 0) {
         if (lane == 0) {
             // ---------------- producer ----------------
-            for (int i = 0; i < nk + nn; ++i) {
-                const int st = i % kStages;
-                const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-                wait(&sm.empty[st], ph ^ 1u, &err);
-                uint8_t *tile = ring + st * kStageBytes;
-                if (i < nk) {
-                    mbar_arrive_expect_tx(&sm.full[st], kTileBytes + R * 128);
-                    tc::tma_load_2d(tile, &pa.mx, i * 64, row0, &sm.full[st]);
-                    tc::tma_load_2d(tile + kTileBytes, &pa.ma, i * 64, s * R, &sm.full[st]);
-                } else {
-                    const int col = o_begin + (i - nk) * 64;
-                    mbar_arrive_expect_tx(&sm.full[st], kTileBytes + 64 * W);
-                    tc::tma_load_2d(tile, &pa.my, col, row0, &sm.full[st]);
-                    tc::tma_load_2d(tile + kTileBytes, &pa.mb, 0, s * pa.d_out + col, &sm.full[st]);
-                }
+            int issued = 0;
+            for (int j = 0; j < nkb; ++j) {
+                const int st = j % stages;
+                if (!wait_ok(&empty[st], ((uint32_t)(j / stages) & 1u) ^ 1u, err)) break;
+                uint8_t *tile = base + (size_t)st * stage_bytes;
+                const int col = (job.kb0 + j) * 64;
+                mbar_arrive_expect_tx(&full[st], stage_bytes);
+                tc::tma_load_2d(tile, &a.mx[g], col, row0, &full[st]);
+                for (int l = 0; l < nl; ++l)
+                    tc::tma_load_2d(tile + kTileBytes + l * R * 128, &a.ma[m0 + l], col, s * R, &full[st]);
+                issued = j + 1;
             }
+            // Drain: the last loads issued must have landed before the CTA exits.
+            for (int j = issued - stages < 0 ? 0 : issued - stages; j < issued; ++j)
+                mbar_wait_bounded(&full[j % stages], (uint32_t)(j / stages) & 1u, kWaitLimit);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------- MMA issuer ----------------
-            constexpr uint32_t id1 = tc::idesc_bf16(128, R);
-            constexpr uint32_t id2 = tc::idesc_bf16(128, 64);
-            for (int kb = 0; kb < nk; ++kb) {
-                const int st = kb % kStages;
-                wait(&sm.full[st], (uint32_t)(kb / kStages) & 1u, &err);
+            constexpr uint32_t idesc = tc::idesc_bf16(128, R);
+            for (int j = 0; j < nkb; ++j) {
+                const int st = j % stages;
+                if (!wait_ok(&full[st], (uint32_t)(j / stages) & 1u, err)) break;
                 tc::fence_after_sync();
-                const uint32_t xa = smem_u32(ring + st * kStageBytes);
-                const uint32_t aa = xa + kTileBytes;
+                const uint32_t xa = smem_u32(base + (size_t)st * stage_bytes);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    tc::mma_bf16(tmem, tc::smem_desc(xa + k * 32, 128, tc::kSwz128),
-                                 tc::smem_desc(aa + k * 32, 128, tc::kSwz128), id1, (kb | k) != 0);
-                tc::mma_commit(&sm.empty[st]);
-                tc::mbar_arrive(&sm.empty[st]);
+                    for (int l = 0; l < nl; ++l)
+                        tc::mma_bf16(tmem + (uint32_t)(l * R),
+                                     tc::smem_desc(xa + k * 32, 128, tc::kSwz128),
+                                     tc::smem_desc(xa + kTileBytes + l * R * 128 + k * 32, 128, tc::kSwz128),
+                                     idesc, (j | k) != 0);
+                tc::mma_commit(&empty[st]);
             }
-            tc::mma_commit(&sm.acc1_full);
-            wait(&sm.v_ready, 0, &err);
-            tc::fence_after_sync();
-            const uint32_t vh = smem_u32(v_hi), vl = smem_u32(v_lo);
-            for (int j = 0; j < nn; ++j) {
-                const int i = nk + j, st = i % kStages, b = j & 1;
-                wait(&sm.full[st], (uint32_t)(i / kStages) & 1u, &err);
-                wait(&sm.acc2_empty[b], ((uint32_t)(j >> 1) & 1u) ^ 1u, &err);
-                tc::fence_after_sync();
-                const uint32_t ba = smem_u32(ring + st * kStageBytes + kTileBytes);
-                const uint32_t d = tmem + kAcc2Col + 64u * b;
-#pragma unroll
-                for (int k = 0; k < R / 16; ++k)
-                    tc::mma_bf16(d, tc::smem_desc(vh + k * 32, W, kSwzRank),
-                                 tc::smem_desc(ba + k * 32, W, kSwzRank), id2, k != 0);
-#pragma unroll
-                for (int k = 0; k < R / 16; ++k)
-                    tc::mma_bf16(d, tc::smem_desc(vl + k * 32, W, kSwzRank),
-                                 tc::smem_desc(ba + k * 32, W, kSwzRank), id2, 1);
-                tc::mma_commit(&sm.acc2_full[b]);
-                tc::mma_commit(&sm.empty[st]);
-            }
+            tc::mma_commit(&acc_full);
+            tc::mma_commit(&drained);
+            mbar_wait_bounded(&drained, 0, kWaitLimit);      // every MMA done before TMEM is freed
         }
-    } else if (warp >= 4) {
+    } else {
         // ---------------- epilogue: row i of the tile ----------------
-        const int q = warp & 3;                        // TMEM lane quarter of this warp
+        const int q = warp & 3;
         const int i = q * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-        wait(&sm.acc1_full, 0, &err);
+        const bool ok = wait_ok(&acc_full, 0, err);
         __syncwarp();
         tc::fence_after_sync();
-        float v[R];
-        if constexpr (R == 16) {
-            uint32_t r[16];
-            tc::tmem_ld16_sync(tmem + lane_addr, r);
+        if (__all_sync(0xffffffffu, ok)) {
+            for (int l = 0; l < nl; ++l) {
+                float v[R];
+                tmem_ld_row<R>(tmem + lane_addr + (uint32_t)(l * R), v);
+                if (i < rows) {
+                    float4 *dst = reinterpret_cast<float4 *>(a.part[m0 + l] +
+                                                             ((size_t)job.chunk * a.T + row0 + i) * R);
 #pragma unroll
-            for (int k = 0; k < 16; ++k) v[k] = __uint_as_float(r[k]);
-        } else {
-#pragma unroll
-            for (int c = 0; c < R / 32; ++c) {
-                uint32_t r[32];
-                tc::tmem_ld32_sync(tmem + lane_addr + 32 * c, r);
-#pragma unroll
-                for (int k = 0; k < 32; ++k) v[32 * c + k] = __uint_as_float(r[k]);
-            }
-        }
-        // V row i -> bf16 high and low parts, K-major with the rank swizzle.
-#pragma unroll
-        for (int c = 0; c < R / 8; ++c) {
-            uint32_t hw[4], lw[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float a = v[8 * c + 2 * e], b2 = v[8 * c + 2 * e + 1];
-                const float ha = round_bf16(a), hb = round_bf16(b2);
-                hw[e] = pack_bf16(ha, hb);
-                lw[e] = pack_bf16(a - ha, b2 - hb);
-            }
-            int pc = c;
-            if constexpr (R == 64) pc ^= (i & 7);
-            else if constexpr (R == 32) pc ^= (i >> 1) & 3;
-            else pc ^= (i >> 2) & 1;
-            *reinterpret_cast<uint4 *>(v_hi + i * W + pc * 16) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4 *>(v_lo + i * W + pc * 16) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-        }
-        tc::fence_proxy_async_smem();
-        tc::fence_before_sync();
-        tc::mbar_arrive(&sm.v_ready);
-
-        const float scale = pa.scale[s];
-        uint16_t *yg = pa.y;
-        for (int j = 0; j < nn; ++j) {
-            const int ii = nk + j, st = ii % kStages, b = j & 1;
-            wait(&sm.acc2_full[b], (uint32_t)(j >> 1) & 1u, &err);
-            wait(&sm.full[st], (uint32_t)(ii / kStages) & 1u, &err);
-            __syncwarp();
-            tc::fence_after_sync();
-            uint32_t d0[32], d1[32];
-            tc::tmem_ld32_sync(tmem + lane_addr + kAcc2Col + 64u * b, d0);
-            tc::tmem_ld32_sync(tmem + lane_addr + kAcc2Col + 64u * b + 32, d1);
-            tc::fence_before_sync();
-            tc::mbar_arrive(&sm.acc2_empty[b]);
-            const uint8_t *yt = ring + st * kStageBytes + i * 128;     // row i, 128B swizzle
-            const int col0 = o_begin + j * 64;
-            uint4 out[8];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint4 yv = *reinterpret_cast<const uint4 *>(yt + ((c ^ (i & 7)) * 16));
-                uint32_t w[4] = {yv.x, yv.y, yv.z, yv.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int n = 8 * c + 2 * e;
-                    const float da = __uint_as_float(n < 32 ? d0[n] : d1[n - 32]);
-                    const float db = __uint_as_float(n + 1 < 32 ? d0[n + 1] : d1[n + 1 - 32]);
-                    w[e] = pack_bf16(fmaf(scale, da, bf_lo(w[e])), fmaf(scale, db, bf_hi(w[e])));
+                    for (int k = 0; k < R / 4; ++k)
+                        dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
                 }
-                out[c] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-            // The stage goes back to the TMA (async proxy) after these generic
-            // reads: order them before the release, or a refill can land first.
-            tc::fence_proxy_async_smem();
-            tc::named_bar(1, 128);                     // every row read from this stage
-            if (i == 0) tc::mbar_arrive(&sm.empty[st]);
-            if (i < rows && !err) {
-                uint16_t *dst = yg + (size_t)(row0 + i) * pa.d_out + col0;
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    if (col0 + 8 * c < o_end) *reinterpret_cast<uint4 *>(dst + 8 * c) = out[c];
             }
         }
     }
 
-    if (err) atomicExch(&sm.error, 1);
     tc::fence_before_sync();
     __syncthreads();
-    if (sm.error && tid == 0) atomicExch(pa.hdr + kHdrError, 1);
+    if (error && tid == 0) atomicExch(a.hdr + kHdrError, 1);
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, (uint32_t)a.tmem_cols);
+    }
+}
+
+// ============================================================================
+// Expand
+// ============================================================================
+
+struct ExpandArgs {
+    CUtensorMap my[kMaxLayersPerCall];        // y [T][d_out], box 64 x 128, 128-byte swizzle
+    CUtensorMap mb[kMaxLayersPerCall];        // B pool [S*d_out][R], box R x 64, rank swizzle
+    const float *part[kMaxLayersPerCall];
+    uint16_t *y[kMaxLayersPerCall];
+    int d_out[kMaxLayersPerCall], ncb[kMaxLayersPerCall], nch[kMaxLayersPerCall];
+    const int4 *ptiles;
+    int *hdr;
+    const float *scale;
+    int n, T, stages, sum_ncb;
+};
+
+struct Item {
+    int l, p, cb;
+};
+
+// Work item k: layers one after another, within a layer tiles, within a tile
+// column blocks (so consecutive items of one CTA share the tile's V).
+__device__ __forceinline__ Item item_at(const ExpandArgs &a, int k, int np) {
+    int l = 0;
+    while (l < a.n - 1 && k >= np * a.ncb[l]) {
+        k -= np * a.ncb[l];
+        ++l;
+    }
+    return Item{l, k / a.ncb[l], k % a.ncb[l]};
+}
+
+__device__ __forceinline__ int n_blocks(const ExpandArgs &a, const Item &it) {
+    const int left = (a.d_out[it.l] - it.cb * kColBlock) / 64;
+    return left < kColBlock / 64 ? left : kColBlock / 64;
+}
+
+template <int R>
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ uint64_t full[kMaxStages], empty[kMaxStages];
+    __shared__ uint64_t acc_full[kAcc], acc_empty[kAcc], v_full[2], v_empty[2], drained;
+    __shared__ uint32_t tmem_base;
+    __shared__ int error;
+
+    constexpr int W = R * 2;                                   // bytes per V / B row
+    constexpr uint32_t kSwzRank = R == 64 ? tc::kSwz128 : (R == 32 ? tc::kSwz64 : tc::kSwz32);
+    constexpr uint32_t kStage = kTileBytes + 64 * W;
+    constexpr uint32_t kVBytes = 128 * W;
+    const int stages = a.stages;
+    uint8_t *ring = base;
+    uint8_t *vbuf = base + (size_t)stages * kStage;            // [2][hi, lo]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int np = a.hdr[kHdrPrefillTiles];
+    const long long total = (long long)np * a.sum_ncb;
+    const int k0 = (int)(total * blockIdx.x / gridDim.x);
+    const int k1 = (int)(total * (blockIdx.x + 1) / gridDim.x);
+    if (k0 >= k1) return;
+
+    if (tid == 0) {
+        for (int i = 0; i < stages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < kAcc; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], 128);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&v_full[i], 128);
+            mbar_init(&v_empty[i], 1);
+        }
+        mbar_init(&drained, 1);
+        error = 0;
+        fence_mbar_init();
+        for (int l = 0; l < a.n; ++l) {
+            tc::prefetch_tensormap(&a.my[l]);
+            tc::prefetch_tensormap(&a.mb[l]);
+        }
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(&tmem_base, 64 * kAcc);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = tmem_base;
+    volatile int *err = &error;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- producer: y and B n-blocks ----------------
+            int j = 0;
+            for (int k = k0; k < k1 && !*err; ++k) {
+                const Item it = item_at(a, k, np);
+                const int4 pt = a.ptiles[it.p];
+                const int nb = n_blocks(a, it), d_out = a.d_out[it.l];
+                for (int b = 0; b < nb; ++b) {
+                    const int st = j % stages;
+                    if (!wait_ok(&empty[st], ((uint32_t)(j / stages) & 1u) ^ 1u, err)) break;
+                    uint8_t *tile = ring + (size_t)st * kStage;
+                    const int col = it.cb * kColBlock + b * 64;
+                    mbar_arrive_expect_tx(&full[st], kStage);
+                    tc::tma_load_2d(tile, &a.my[it.l], col, pt.y, &full[st]);
+                    tc::tma_load_2d(tile + kTileBytes, &a.mb[it.l], 0, pt.x * d_out + col, &full[st]);
+                    ++j;
+                }
+            }
+            for (int i = j - stages < 0 ? 0 : j - stages; i < j; ++i)
+                mbar_wait_bounded(&full[i % stages], (uint32_t)(i / stages) & 1u, kWaitLimit);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer ----------------
+            constexpr uint32_t idesc = tc::idesc_bf16(128, 64);
+            int j = 0, gen = -1, pl = -1, pp = -1;
+            for (int k = k0; k < k1 && !*err; ++k) {
+                const Item it = item_at(a, k, np);
+                if (it.l != pl || it.p != pp) {
+                    ++gen;
+                    pl = it.l;
+                    pp = it.p;
+                    if (!wait_ok(&v_full[gen & 1], (uint32_t)(gen >> 1) & 1u, err)) break;
+                    tc::fence_after_sync();
+                }
+                const uint32_t vh = smem_u32(vbuf + (size_t)(gen & 1) * 2 * kVBytes);
+                const uint32_t vl = vh + kVBytes;
+                const int nb = n_blocks(a, it);
+                for (int b = 0; b < nb; ++b) {
+                    const int st = j % stages, ac = j % kAcc;
+                    if (!wait_ok(&full[st], (uint32_t)(j / stages) & 1u, err)) break;
+                    if (!wait_ok(&acc_empty[ac], ((uint32_t)(j / kAcc) & 1u) ^ 1u, err)) break;
+                    tc::fence_after_sync();
+                    const uint32_t ba = smem_u32(ring + (size_t)st * kStage + kTileBytes);
+                    const uint32_t d = tmem + 64u * ac;
+#pragma unroll
+                    for (int kk = 0; kk < R / 16; ++kk)
+                        tc::mma_bf16(d, tc::smem_desc(vh + kk * 32, W, kSwzRank),
+                                     tc::smem_desc(ba + kk * 32, W, kSwzRank), idesc, kk != 0);
+#pragma unroll
+                    for (int kk = 0; kk < R / 16; ++kk)
+                        tc::mma_bf16(d, tc::smem_desc(vl + kk * 32, W, kSwzRank),
+                                     tc::smem_desc(ba + kk * 32, W, kSwzRank), idesc, 1);
+                    tc::mma_commit(&acc_full[ac]);
+                    ++j;
+                }
+                bool last_use = k + 1 >= k1;
+                if (!last_use) {
+                    const Item nx = item_at(a, k + 1, np);
+                    last_use = nx.l != it.l || nx.p != it.p;
+                }
+                if (last_use) tc::mma_commit(&v_empty[gen & 1]);
+            }
+            tc::mma_commit(&drained);
+            mbar_wait_bounded(&drained, 0, kWaitLimit);
+        }
+    } else {
+        // ---------------- epilogue: row i of the tile ----------------
+        const int q = warp & 3;
+        const int i = q * 32 + lane;
+        const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+        const bool leader = tid == 64;
+        int j = 0, gen = -1, pl = -1, pp = -1, pend = -1;
+        for (int k = k0; k < k1; ++k) {
+            const Item it = item_at(a, k, np);
+            const int4 pt = a.ptiles[it.p];
+            const int s = pt.x, row0 = pt.y, rows = pt.z;
+            if (it.l != pl || it.p != pp) {
+                ++gen;
+                pl = it.l;
+                pp = it.p;
+                const int vb = gen & 1;
+                if (wait_ok(&v_empty[vb], ((uint32_t)(gen >> 1) & 1u) ^ 1u, err)) {
+                    float v[R];
+#pragma unroll
+                    for (int r = 0; r < R; ++r) v[r] = 0.f;
+                    if (i < rows) {
+                        for (int c = 0; c < a.nch[it.l]; ++c) {
+                            const float4 *src = reinterpret_cast<const float4 *>(
+                                a.part[it.l] + ((size_t)c * a.T + row0 + i) * R);
+#pragma unroll
+                            for (int r = 0; r < R / 4; ++r) {
+                                const float4 f = src[r];
+                                v[4 * r] += f.x;
+                                v[4 * r + 1] += f.y;
+                                v[4 * r + 2] += f.z;
+                                v[4 * r + 3] += f.w;
+                            }
+                        }
+                    }
+                    uint8_t *vh = vbuf + (size_t)vb * 2 * kVBytes;
+                    uint8_t *vl = vh + kVBytes;
+#pragma unroll
+                    for (int c = 0; c < R / 8; ++c) {
+                        uint32_t hw[4], lw[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float x0 = v[8 * c + 2 * e], x1 = v[8 * c + 2 * e + 1];
+                            const float h0 = round_bf16(x0), h1 = round_bf16(x1);
+                            hw[e] = pack_bf16(h0, h1);
+                            lw[e] = pack_bf16(x0 - h0, x1 - h1);
+                        }
+                        const int pc = swz_chunk<R>(c, i);
+                        *reinterpret_cast<uint4 *>(vh + i * W + pc * 16) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        *reinterpret_cast<uint4 *>(vl + i * W + pc * 16) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    }
+                    tc::fence_proxy_async_smem();
+                    tc::mbar_arrive(&v_full[vb]);
+                }
+            }
+            const float scale = a.scale[s];
+            const int nb = n_blocks(a, it), d_out = a.d_out[it.l];
+            for (int b = 0; b < nb; ++b) {
+                const int st = j % stages, ac = j % kAcc;
+                const int col = it.cb * kColBlock + b * 64;
+                bool ok = wait_ok(&acc_full[ac], (uint32_t)(j / kAcc) & 1u, err);
+                ok = ok && wait_ok(&full[st], (uint32_t)(j / stages) & 1u, err);
+                ok = __all_sync(0xffffffffu, ok);
+                uint8_t *yt = ring + (size_t)st * kStage + i * 128;    // row i, 128-byte swizzle
+                if (ok) {
+                    tc::fence_after_sync();
+                    uint32_t d0[32], d1[32];
+                    tc::tmem_ld32_sync(tmem + lane_addr + 64u * ac, d0);
+                    tc::tmem_ld32_sync(tmem + lane_addr + 64u * ac + 32, d1);
+                    tc::fence_before_sync();
+                    tc::mbar_arrive(&acc_empty[ac]);
+                    uint4 out[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        uint4 *p = reinterpret_cast<uint4 *>(yt + ((c ^ (i & 7)) * 16));
+                        const uint4 yv = *p;
+                        uint32_t w[4] = {yv.x, yv.y, yv.z, yv.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int n = 8 * c + 2 * e;
+                            const float da = __uint_as_float(n < 32 ? d0[n] : d1[n - 32]);
+                            const float db = __uint_as_float(n + 1 < 32 ? d0[n + 1] : d1[n + 1 - 32]);
+                            w[e] = pack_bf16(fmaf(scale, da, bf_lo(w[e])), fmaf(scale, db, bf_hi(w[e])));
+                        }
+                        out[c] = make_uint4(w[0], w[1], w[2], w[3]);
+                        *p = out[c];
+                    }
+                    if (rows < 128 && i < rows) {
+                        uint16_t *dst = a.y[it.l] + (size_t)(row0 + i) * d_out + col;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) reinterpret_cast<uint4 *>(dst)[c] = out[c];
+                    }
+                }
+                // Generic writes to the stage become visible to the TMA store.
+                tc::fence_proxy_async_smem();
+                tc::named_bar(1, 128);
+                if (leader) {
+                    if (rows == 128 && !*err) {
+                        tc::tma_store_2d(&a.my[it.l], ring + (size_t)st * kStage, col, row0);
+                        tc::bulk_commit_group();
+                        tc::bulk_wait_group_read<1>();
+                        if (pend >= 0) tc::mbar_arrive(&empty[pend]);
+                        pend = st;
+                    } else {
+                        // No store of this block: hand back the one still pending too,
+                        // so that the producer never waits on a stage nobody releases.
+                        if (pend >= 0) {
+                            tc::bulk_wait_group_read<0>();
+                            tc::mbar_arrive(&empty[pend]);
+                            pend = -1;
+                        }
+                        tc::mbar_arrive(&empty[st]);
+                    }
+                }
+                ++j;
+            }
+        }
+        if (leader) {
+            tc::bulk_wait_group_all();
+            if (pend >= 0) tc::mbar_arrive(&empty[pend]);
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (error && tid == 0) atomicExch(a.hdr + kHdrError, 1);
     if (warp == 1) {
         __syncwarp();
         tc::fence_after_sync();
-        tc::tmem_dealloc(tmem, kTmemCols);
+        tc::tmem_dealloc(tmem, 64 * kAcc);
     }
 }
+
+// ============================================================================
+// Host side
+// ============================================================================
+
+constexpr size_t kShrinkRingBudget = 108 * 1024;   // two shrink CTAs per SM
+constexpr size_t kExpandSmemBudget = 216 * 1024;   // one expand CTA per SM
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -288,16 +544,27 @@ bool encode_2d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, ui
 }
 
 template <int R>
-cudaError_t launch_r(const PrefillArgs &pa, int grid_tiles, int nsplit, cudaStream_t st) {
+size_t expand_smem(int stages) {
+    return 1024 + (size_t)stages * (kTileBytes + 64 * R * 2) + 4 * (size_t)128 * R * 2;
+}
+
+template <int R>
+cudaError_t launch_r(const ShrinkArgs &sa, int grid_tiles, int n_jobs, size_t shrink_smem,
+                     const ExpandArgs &ea, int expand_grid, cudaStream_t st) {
     static bool attr = false;
-    const size_t smem = prefill_smem_bytes(R);
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
+        cudaError_t e = cudaFuncSetAttribute(prefill_shrink_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)(1024 + kShrinkRingBudget));
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(prefill_expand_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kExpandSmemBudget);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    prefill_tc_kernel<R><<<dim3(grid_tiles, nsplit, 1), kPT, smem, st>>>(pa);
+    prefill_shrink_kernel<R><<<dim3(grid_tiles, n_jobs, 1), kThreads, shrink_smem, st>>>(sa);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    prefill_expand_kernel<R><<<expand_grid, kThreads, expand_smem<R>(ea.stages), st>>>(ea);
     return cudaGetLastError();
 }
 
@@ -305,9 +572,10 @@ cudaError_t launch_r(const PrefillArgs &pa, int grid_tiles, int nsplit, cudaStre
 
 bool prefill_tc_supported(int R) { return R == 16 || R == 32 || R == 64; }
 
-cudaError_t launch_prefill_tc(const void *x, void *y, int T, int d_in, int d_out, const void *A_pool,
-                              const void *B_pool, int S, int R, const float *scale, const int *hdr,
-                              const int4 *ptiles, int grid_tiles, int nsplit, cudaStream_t st) {
+cudaError_t launch_prefill_tc(const PrefillLayer *L, int n, int T, int S, int R, const float *scale,
+                              int *hdr, const int4 *ptiles, int grid_tiles, int part_rows, int num_sms,
+                              cudaStream_t st) {
+    if (!prefill_tc_supported(R) || n < 1 || n > kMaxLayersPerCall || T < 1) return cudaErrorInvalidValue;
     if (!g_encode) {
         cudaDriverEntryPointQueryResult q;
         void *fn = nullptr;
@@ -316,26 +584,126 @@ cudaError_t launch_prefill_tc(const void *x, void *y, int T, int d_in, int d_out
         if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
         g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
-    PrefillArgs pa{};
+
+    // Input groups: layers reading the same x, at most 256 TMEM columns each.
+    const int max_members = 256 / R;
+    int grp[kMaxLayersPerCall], ng = 0, gcount[kMaxLayersPerCall] = {0};
+    int glead[kMaxLayersPerCall];
+    for (int i = 0; i < n; ++i) {
+        int g = -1;
+        for (int h = 0; h < ng && g < 0; ++h)
+            if (L[glead[h]].x == L[i].x && L[glead[h]].d_in == L[i].d_in && gcount[h] < max_members) g = h;
+        if (g < 0) {
+            g = ng++;
+            glead[g] = i;
+        }
+        grp[i] = g;
+        ++gcount[g];
+    }
+
+    ShrinkArgs sa{};
+    ExpandArgs ea{};
+    int m = 0;
+    for (int g = 0; g < ng; ++g) {
+        sa.g_first[g] = m;
+        sa.g_count[g] = gcount[g];
+        const PrefillLayer &x = L[glead[g]];
+        if (!encode_2d(&sa.mx[g], x.x, (uint64_t)x.d_in, (uint64_t)T, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+        for (int i = 0; i < n; ++i) {
+            if (grp[i] != g) continue;
+            if (!encode_2d(&sa.ma[m], L[i].A, (uint64_t)L[i].d_in, (uint64_t)S * R, 64, (uint32_t)R,
+                           CU_TENSOR_MAP_SWIZZLE_128B))
+                return cudaErrorInvalidValue;
+            sa.part[m] = L[i].part;
+            ++m;
+        }
+    }
+
+    // d_in chunks: about two waves of shrink CTAs (two per SM), each group's
+    // share proportional to its d_in; partial rows bound the chunk count.
+    int max_ch = part_rows / T;
+    if (max_ch > 16) max_ch = 16;
+    if (max_ch < 1) return cudaErrorInvalidValue;
+    const int est_tiles = T / kPrefillRows + 1;
+    int kb[kMaxLayersPerCall], nch[kMaxLayersPerCall], kb_total = 0;
+    for (int g = 0; g < ng; ++g) {
+        kb[g] = (L[glead[g]].d_in + 63) / 64;
+        kb_total += kb[g];
+    }
+    const int want = (4 * num_sms + est_tiles - 1) / est_tiles;    // jobs per tile
+    int n_jobs = 0;
+    for (int g = 0; g < ng; ++g) {
+        int c = (int)(((long long)want * kb[g] + kb_total - 1) / kb_total);
+        if (c < 1) c = 1;
+        if (c > max_ch) c = max_ch;
+        if (c > kb[g]) c = kb[g];
+        nch[g] = c;
+        n_jobs += c;
+    }
+    while (n_jobs > kMaxJobs) {
+        int gm = 0;
+        for (int g = 1; g < ng; ++g)
+            if (nch[g] > nch[gm]) gm = g;
+        --nch[gm];
+        --n_jobs;
+    }
+    int jb = 0;
+    size_t max_stage = 0;
+    for (int g = 0; g < ng; ++g) {
+        const size_t sb = kTileBytes + (size_t)gcount[g] * R * 128;
+        if (sb > max_stage) max_stage = sb;
+        for (int c = 0; c < nch[g]; ++c) {
+            sa.jobs[jb].group = g;
+            sa.jobs[jb].chunk = c;
+            sa.jobs[jb].kb0 = (int)((long long)kb[g] * c / nch[g]);
+            sa.jobs[jb].kb1 = (int)((long long)kb[g] * (c + 1) / nch[g]);
+            ++jb;
+        }
+    }
+    // One ring depth for the launch: the deepest that the largest stage fits.
+    sa.stages = (int)(kShrinkRingBudget / max_stage);
+    if (sa.stages > kMaxStages) sa.stages = kMaxStages;
+    if (sa.stages < 2) return cudaErrorInvalidValue;
+    const size_t shrink_smem = 1024 + (size_t)sa.stages * max_stage;
+    int max_cols = 0;
+    for (int g = 0; g < ng; ++g)
+        if (gcount[g] * R > max_cols) max_cols = gcount[g] * R;
+    sa.tmem_cols = (int)tmem_cols_for(max_cols);
+    sa.ptiles = ptiles;
+    sa.hdr = hdr;
+    sa.T = T;
+
     const CUtensorMapSwizzle swz_rank = R == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
                                       : (R == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
-    bool ok = encode_2d(&pa.mx, x, (uint64_t)d_in, (uint64_t)T, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
-              encode_2d(&pa.ma, A_pool, (uint64_t)d_in, (uint64_t)S * R, 64, (uint32_t)R,
-                        CU_TENSOR_MAP_SWIZZLE_128B) &&
-              encode_2d(&pa.my, y, (uint64_t)d_out, (uint64_t)T, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
-              encode_2d(&pa.mb, B_pool, (uint64_t)R, (uint64_t)S * d_out, (uint32_t)R, 64, swz_rank);
-    if (!ok) return cudaErrorInvalidValue;
-    pa.y = static_cast<uint16_t *>(y);
-    pa.d_in = d_in;
-    pa.d_out = d_out;
-    pa.scale = scale;
-    pa.hdr = const_cast<int *>(hdr);
-    pa.ptiles = ptiles;
-    pa.cols_per_split = ((d_out + nsplit - 1) / nsplit + 63) / 64 * 64;
+    ea.n = n;
+    ea.sum_ncb = 0;
+    for (int i = 0; i < n; ++i) {
+        if (L[i].d_out % 64 != 0) return cudaErrorInvalidValue;
+        if (!encode_2d(&ea.my[i], L[i].y, (uint64_t)L[i].d_out, (uint64_t)T, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_2d(&ea.mb[i], L[i].B, (uint64_t)R, (uint64_t)S * L[i].d_out, (uint32_t)R, 64, swz_rank))
+            return cudaErrorInvalidValue;
+        ea.part[i] = L[i].part;
+        ea.y[i] = static_cast<uint16_t *>(L[i].y);
+        ea.d_out[i] = L[i].d_out;
+        ea.ncb[i] = (L[i].d_out + kColBlock - 1) / kColBlock;
+        ea.nch[i] = nch[grp[i]];
+        ea.sum_ncb += ea.ncb[i];
+    }
+    const size_t vbytes = 4 * (size_t)128 * R * 2, stage = kTileBytes + 64 * (size_t)R * 2;
+    ea.stages = (int)((kExpandSmemBudget - 1024 - vbytes) / stage);
+    if (ea.stages > kMaxStages) ea.stages = kMaxStages;
+    ea.ptiles = ptiles;
+    ea.hdr = hdr;
+    ea.scale = scale;
+    ea.T = T;
+    long long items = (long long)grid_tiles * ea.sum_ncb;
+    const int expand_grid = (int)(items < num_sms ? items : num_sms);
+
     switch (R) {
-    case 16: return launch_r<16>(pa, grid_tiles, nsplit, st);
-    case 32: return launch_r<32>(pa, grid_tiles, nsplit, st);
-    case 64: return launch_r<64>(pa, grid_tiles, nsplit, st);
+    case 16: return launch_r<16>(sa, grid_tiles, n_jobs, shrink_smem, ea, expand_grid, st);
+    case 32: return launch_r<32>(sa, grid_tiles, n_jobs, shrink_smem, ea, expand_grid, st);
+    case 64: return launch_r<64>(sa, grid_tiles, n_jobs, shrink_smem, ea, expand_grid, st);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -158,7 +158,7 @@ extern "C" int lora_apply_static_scratch(const void *x, void *y, const int32_t *
     gv.R = max_lora_rank;
     gv.T = T;
     const int grid_tiles = est_tiles < lay.max_tiles ? est_tiles : lay.max_tiles;
-    e = launch_decode(ma, gv, dtype, grid_tiles, a.n_chunks, (d_out + 255) / 256, st);
+    e = launch_decode(ma, gv, dtype, grid_tiles, a.n_chunks, (d_out + 255) / 256, num_sms, st);
     if (e != cudaSuccess)
         return fail_static(LORA_ERR_CUDA, (std::string("launch: ") + cudaGetErrorString(e)).c_str());
     return LORA_OK;

@@ -215,3 +215,24 @@ def test_inputs_ready_back_to_back():
         assert dw.slots.stats()["device_wait_timeouts"] == 0
     finally:
         dw.close()
+
+
+def test_mixed_ranks_small_general_path():
+    """Five layers reading one input at max_lora_rank 64: the shrink splits
+    them into input groups of at most four, each x tile read once per group."""
+    w = wl.mixed_ranks_8b(1, n_segments=3, seg_len=150, n_decode=50)
+    out, st = _run(w, small_batch_tokens=0)
+    for ly in w.layers:
+        check_layer(w, ly.name, out[ly.name])
+    assert st["device_wait_timeouts"] == 0
+
+
+@pytest.mark.parametrize("T,run", [(100, 100), (90, 70), (129, 129)])
+def test_prefill_batch_shorter_than_a_tile(T, run):
+    """Fewer tokens than one 128-row tile (the TMA boxes reach past the last
+    row), and a run ending one row into a second tile."""
+    idx = np.concatenate([np.full(run, 1), np.full(T - run, 0)]).astype(np.int32)
+    w = _custom(T, 320, 192, 2, 32, [32, 16], idx, seed=T)
+    out, st = _run(w, small_batch_tokens=0)
+    check_layer(w, "l0", out["l0"])
+    assert st["device_wait_timeouts"] == 0
