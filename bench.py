@@ -73,16 +73,21 @@ def kernel_traffic(kernel_file: str):
 
 
 def algorithmic_bytes(idx: np.ndarray, ranks, layers, e=2) -> int:
-    """Per layer call: x rows of adapter tokens read, y rows read and written,
-    each used slot's true-rank A and B read once, the slot ids read."""
+    """Per layer set: the x rows of adapter tokens read once per distinct input
+    (q/k/v, or gate/up, read the same activations), y rows read and written per
+    layer, each used slot's true-rank A and B read once per layer, the slot ids
+    read once."""
     T = idx.shape[0]
     act = idx[idx >= 0]
     used = np.unique(act)
-    total = 0
+    total = T * 4
+    seen = set()
     for ly in layers:
-        total += act.size * (ly.d_in + 2 * ly.d_out) * e
+        if ly.x_key not in seen:
+            seen.add(ly.x_key)
+            total += act.size * ly.d_in * e
+        total += act.size * 2 * ly.d_out * e
         total += sum((ly.d_in + ly.d_out) * int(ranks[s]) * e for s in used)
-        total += T * 4
     return total
 
 
@@ -505,11 +510,11 @@ def run_big(args, name):
                        "max_loras": w.max_loras, "max_lora_rank": w.max_lora_rank,
                        "l2": f"inputs larger than L2 ({bytes_ / 2**20:.0f} MiB per step)",
                        "timing": "CUDA-graph replay, CUDA events on the launch stream"},
-            "roofline": {"bound": "hbm", "kernel": "prefill_tc_kernel per layer + grouping + decode kernels",
+            "roofline": {"bound": "hbm", "kernel": "whole step: group_tokens, prefill_shrink, prefill_expand, decode shrink + expand (5 launches, every layer)",
                          "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "peak_kind": kind,
                          "traffic": None, "algorithmic_bytes_per_step": bytes_,
                          "tflops": flops * args.steps / (ms * 1e-3) / 1e12},
-            "gpu_launches": (len(w.layers) + 3) * args.steps, "clocks": clocks}
+            "gpu_launches": 5 * args.steps, "clocks": clocks}
     print(json.dumps(line), flush=True)
     dw.close()
     return 0

@@ -133,7 +133,7 @@ __device__ __forceinline__ void shrink_bf16_tile(const LayerArgs &L, const Group
 // N = 8 columns, K = 16 ranks, columns permuted so that each lane ends with 8
 // consecutive outputs of two token rows (one 128-bit y access per row).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void expand_bf16_tile(const LayerArgs &L, const GroupView &g, int tile_i) {
+__device__ __forceinline__ void expand_bf16_tile(const LayerArgs &L, const GroupView &g, int dblock, int tile_i) {
     const int d_out = L.d_out;
     const int4 tile = g.tiles[tile_i];
     const int s = tile.x, p0 = tile.y, cnt = tile.z;
@@ -180,7 +180,7 @@ __device__ __forceinline__ void expand_bf16_tile(const LayerArgs &L, const Group
 
 #pragma unroll
     for (int grp = 0; grp < 2; ++grp) {
-        const int c = blockIdx.x * kExpandCols + warp * 64 + grp * 32;
+        const int c = dblock * kExpandCols + warp * 64 + grp * 32;
         if (c >= d_out) break;
         float acc[4][4];
 #pragma unroll
@@ -270,7 +270,7 @@ __device__ __forceinline__ void shrink_f32_tile(const LayerArgs &L, const GroupV
 }
 
 // fp32 expand-add: each thread owns two columns of the 256-column block.
-__device__ __forceinline__ void expand_f32_tile(const LayerArgs &L, const GroupView &g, int tile_i) {
+__device__ __forceinline__ void expand_f32_tile(const LayerArgs &L, const GroupView &g, int dblock, int tile_i) {
     const int d_out = L.d_out;
     const int4 tile = g.tiles[tile_i];
     const int s = tile.x, p0 = tile.y, cnt = tile.z;
@@ -284,7 +284,7 @@ __device__ __forceinline__ void expand_f32_tile(const LayerArgs &L, const GroupV
     const float *Bs = static_cast<const float *>(L.B) + (size_t)s * d_out * R;
     float *y = static_cast<float *>(L.y);
     for (int h = 0; h < 2; ++h) {
-        const int col = blockIdx.x * kExpandCols + h * kThreads + threadIdx.x;
+        const int col = dblock * kExpandCols + h * kThreads + threadIdx.x;
         if (col >= d_out) continue;
         const float *br = Bs + (size_t)col * R;
         for (int i = 0; i < cnt; ++i) {
@@ -296,47 +296,58 @@ __device__ __forceinline__ void expand_f32_tile(const LayerArgs &L, const GroupV
     }
 }
 
-// The kernels: CTA = (chunk or column block, tile slot, layer). Tiles are
-// taken with a stride of gridDim.y, so the grid stays a few waves deep even
-// when the host can only bound the tile count (a prefill batch leaves few or
-// no decode tiles, and the count is known on the device only).
+// The kernels are persistent: work items are (tile, layer, chunk) for the
+// shrink and (tile, layer, 256-column block) for the expand, taken with a
+// stride of gridDim.x. The tile count is known on the device only (a prefill
+// batch may leave few or no decode tiles), so the grid is sized from the SM
+// count and items past the count cost nothing.
 __global__ void __launch_bounds__(kThreads)
-shrink_bf16_kernel(MultiArgs ma, GroupView g) {
-    const LayerArgs &L = ma.l[blockIdx.z];
-    if ((int)blockIdx.x >= L.n_chunks) return;
-    const int nt = g.hdr[kHdrTiles];
-    for (int t = blockIdx.y; t < nt; t += gridDim.y) {
-        shrink_bf16_tile(L, g, blockIdx.x, t);
+shrink_bf16_kernel(MultiArgs ma, GroupView g, int max_chunks) {
+    const int per_tile = max_chunks * ma.n;
+    const int items = g.hdr[kHdrTiles] * per_tile;
+    for (int w = blockIdx.x; w < items; w += gridDim.x) {
+        const int chunk = w % max_chunks, l = (w / max_chunks) % ma.n, t = w / per_tile;
+        const LayerArgs &L = ma.l[l];
+        if (chunk >= L.n_chunks) continue;
+        shrink_bf16_tile(L, g, chunk, t);
         __syncthreads();
     }
 }
 
 __global__ void __launch_bounds__(kThreads)
-expand_bf16_kernel(MultiArgs ma, GroupView g) {
-    const LayerArgs &L = ma.l[blockIdx.z];
-    if ((int)blockIdx.x * kExpandCols >= L.d_out) return;
-    const int nt = g.hdr[kHdrTiles];
-    for (int t = blockIdx.y; t < nt; t += gridDim.y) expand_bf16_tile(L, g, t);
+expand_bf16_kernel(MultiArgs ma, GroupView g, int max_dblocks) {
+    const int per_tile = max_dblocks * ma.n;
+    const int items = g.hdr[kHdrTiles] * per_tile;
+    for (int w = blockIdx.x; w < items; w += gridDim.x) {
+        const int db = w % max_dblocks, l = (w / max_dblocks) % ma.n, t = w / per_tile;
+        const LayerArgs &L = ma.l[l];
+        if (db * kExpandCols >= L.d_out) continue;
+        expand_bf16_tile(L, g, db, t);
+    }
 }
 
 __global__ void __launch_bounds__(kThreads)
-shrink_f32_kernel(MultiArgs ma, GroupView g) {
-    const LayerArgs &L = ma.l[blockIdx.z];
-    if ((int)blockIdx.x >= L.n_chunks) return;
-    const int nt = g.hdr[kHdrTiles];
-    for (int t = blockIdx.y; t < nt; t += gridDim.y) {
-        shrink_f32_tile(L, g, blockIdx.x, t);
+shrink_f32_kernel(MultiArgs ma, GroupView g, int max_chunks) {
+    const int per_tile = max_chunks * ma.n;
+    const int items = g.hdr[kHdrTiles] * per_tile;
+    for (int w = blockIdx.x; w < items; w += gridDim.x) {
+        const int chunk = w % max_chunks, l = (w / max_chunks) % ma.n, t = w / per_tile;
+        const LayerArgs &L = ma.l[l];
+        if (chunk >= L.n_chunks) continue;
+        shrink_f32_tile(L, g, chunk, t);
         __syncthreads();
     }
 }
 
 __global__ void __launch_bounds__(kThreads)
-expand_f32_kernel(MultiArgs ma, GroupView g) {
-    const LayerArgs &L = ma.l[blockIdx.z];
-    if ((int)blockIdx.x * kExpandCols >= L.d_out) return;
-    const int nt = g.hdr[kHdrTiles];
-    for (int t = blockIdx.y; t < nt; t += gridDim.y) {
-        expand_f32_tile(L, g, t);
+expand_f32_kernel(MultiArgs ma, GroupView g, int max_dblocks) {
+    const int per_tile = max_dblocks * ma.n;
+    const int items = g.hdr[kHdrTiles] * per_tile;
+    for (int w = blockIdx.x; w < items; w += gridDim.x) {
+        const int db = w % max_dblocks, l = (w / max_dblocks) % ma.n, t = w / per_tile;
+        const LayerArgs &L = ma.l[l];
+        if (db * kExpandCols >= L.d_out) continue;
+        expand_f32_tile(L, g, db, t);
         __syncthreads();
     }
 }
@@ -351,21 +362,19 @@ __global__ void set_slot_kernel(float *scale_dev, int *rank_dev, int slot, float
 cudaError_t launch_decode(const MultiArgs &ma, const GroupView &gv, int dtype, int grid_tiles,
                           int max_chunks, int max_dblocks, int num_sms, cudaStream_t st) {
     if (grid_tiles <= 0) return cudaSuccess;
-    // At most ~16 CTAs per SM per launch; the tile loop covers the rest.
-    const long long cap = 16LL * (num_sms > 0 ? num_sms : 1);
-    auto rows = [&](int gx) {
-        long long y = cap / ((long long)gx * ma.n);
-        if (y < 1) y = 1;
-        return (int)(y < grid_tiles ? y : grid_tiles);
+    // Persistent grids: at most 8 resident-sized waves of CTAs per SM.
+    const long long cap = 8LL * (num_sms > 0 ? num_sms : 1);
+    auto grid = [&](int per_tile) {
+        long long items = (long long)grid_tiles * per_tile * ma.n;
+        return (int)(items < cap ? items : cap);
     };
-    dim3 gs(max_chunks, rows(max_chunks), ma.n), ge(max_dblocks, rows(max_dblocks), ma.n);
     if (dtype == 1) {
-        shrink_bf16_kernel<<<gs, kThreads, 0, st>>>(ma, gv);
-        expand_bf16_kernel<<<ge, kThreads, 0, st>>>(ma, gv);
+        shrink_bf16_kernel<<<grid(max_chunks), kThreads, 0, st>>>(ma, gv, max_chunks);
+        expand_bf16_kernel<<<grid(max_dblocks), kThreads, 0, st>>>(ma, gv, max_dblocks);
     } else {
-        shrink_f32_kernel<<<gs, kThreads, 0, st>>>(ma, gv);
+        shrink_f32_kernel<<<grid(max_chunks), kThreads, 0, st>>>(ma, gv, max_chunks);
         size_t smem = (size_t)kTileTokens * gv.R * sizeof(float);
-        expand_f32_kernel<<<ge, kThreads, smem, st>>>(ma, gv);
+        expand_f32_kernel<<<grid(max_dblocks), kThreads, smem, st>>>(ma, gv, max_dblocks);
     }
     return cudaGetLastError();
 }

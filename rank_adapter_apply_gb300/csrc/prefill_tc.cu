@@ -48,7 +48,10 @@
 namespace lora {
 namespace {
 
-constexpr int kThreads = 192;              // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kThreads = 192;              // shrink: warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kExpandThreads = 384;        // expand: warp 0 TMA, 1 MMA, 2..3 V loaders, 4..11 epilogue
+constexpr int kEpiThreads = 256;
+constexpr int kVThreads = 64;
 constexpr int kTileBytes = 16384;          // 128 rows x 64 bf16: one x k-block or one y n-block
 constexpr int kColBlock = 256;             // d_out columns per expand work item
 constexpr int kAcc = 4;                    // expand accumulators (64 TMEM columns each)
@@ -268,7 +271,7 @@ __device__ __forceinline__ int n_blocks(const ExpandArgs &a, const Item &it) {
 }
 
 template <int R>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kExpandThreads, 1)
 prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -299,10 +302,10 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
         }
         for (int i = 0; i < kAcc; ++i) {
             mbar_init(&acc_full[i], 1);
-            mbar_init(&acc_empty[i], 128);
+            mbar_init(&acc_empty[i], kEpiThreads);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&v_full[i], 128);
+            mbar_init(&v_full[i], kVThreads);
             mbar_init(&v_empty[i], 1);
         }
         mbar_init(&drained, 1);
@@ -390,61 +393,71 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
             tc::mma_commit(&drained);
             mbar_wait_bounded(&drained, 0, kWaitLimit);
         }
+    } else if (warp < 4) {
+        // ---------------- V loaders: rows vt and vt + 64 ----------------
+        const int vt = tid - 64;
+        int gen = -1, pl = -1, pp = -1;
+        for (int k = k0; k < k1; ++k) {
+            const Item it = item_at(a, k, np);
+            if (it.l == pl && it.p == pp) continue;
+            ++gen;
+            pl = it.l;
+            pp = it.p;
+            const int vb = gen & 1;
+            if (!wait_ok(&v_empty[vb], ((uint32_t)(gen >> 1) & 1u) ^ 1u, err)) break;
+            const int4 pt = a.ptiles[it.p];
+            uint8_t *vh = vbuf + (size_t)vb * 2 * kVBytes;
+            uint8_t *vl = vh + kVBytes;
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                const int i = vt + 64 * h;
+                float v[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) v[r] = 0.f;
+                if (i < pt.z) {
+                    for (int c = 0; c < a.nch[it.l]; ++c) {
+                        const float4 *src = reinterpret_cast<const float4 *>(
+                            a.part[it.l] + ((size_t)c * a.T + pt.y + i) * R);
+#pragma unroll
+                        for (int r = 0; r < R / 4; ++r) {
+                            const float4 f = src[r];
+                            v[4 * r] += f.x;
+                            v[4 * r + 1] += f.y;
+                            v[4 * r + 2] += f.z;
+                            v[4 * r + 3] += f.w;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < R / 8; ++c) {
+                    uint32_t hw[4], lw[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float x0 = v[8 * c + 2 * e], x1 = v[8 * c + 2 * e + 1];
+                        const float h0 = round_bf16(x0), h1 = round_bf16(x1);
+                        hw[e] = pack_bf16(h0, h1);
+                        lw[e] = pack_bf16(x0 - h0, x1 - h1);
+                    }
+                    const int pc = swz_chunk<R>(c, i);
+                    *reinterpret_cast<uint4 *>(vh + i * W + pc * 16) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    *reinterpret_cast<uint4 *>(vl + i * W + pc * 16) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                }
+            }
+            tc::fence_proxy_async_smem();
+            tc::mbar_arrive(&v_full[vb]);
+        }
     } else {
-        // ---------------- epilogue: row i of the tile ----------------
-        const int q = warp & 3;
+        // ---------------- epilogue: row i, columns 32h .. 32h + 31 of each n-block ----------------
+        const int q = warp & 3, h = (warp - 4) >> 2;
         const int i = q * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-        const bool leader = tid == 64;
-        int j = 0, gen = -1, pl = -1, pp = -1, pend = -1;
+        const bool leader = tid == 128;
+        int j = 0, pend = -1;
         for (int k = k0; k < k1; ++k) {
             const Item it = item_at(a, k, np);
             const int4 pt = a.ptiles[it.p];
-            const int s = pt.x, row0 = pt.y, rows = pt.z;
-            if (it.l != pl || it.p != pp) {
-                ++gen;
-                pl = it.l;
-                pp = it.p;
-                const int vb = gen & 1;
-                if (wait_ok(&v_empty[vb], ((uint32_t)(gen >> 1) & 1u) ^ 1u, err)) {
-                    float v[R];
-#pragma unroll
-                    for (int r = 0; r < R; ++r) v[r] = 0.f;
-                    if (i < rows) {
-                        for (int c = 0; c < a.nch[it.l]; ++c) {
-                            const float4 *src = reinterpret_cast<const float4 *>(
-                                a.part[it.l] + ((size_t)c * a.T + row0 + i) * R);
-#pragma unroll
-                            for (int r = 0; r < R / 4; ++r) {
-                                const float4 f = src[r];
-                                v[4 * r] += f.x;
-                                v[4 * r + 1] += f.y;
-                                v[4 * r + 2] += f.z;
-                                v[4 * r + 3] += f.w;
-                            }
-                        }
-                    }
-                    uint8_t *vh = vbuf + (size_t)vb * 2 * kVBytes;
-                    uint8_t *vl = vh + kVBytes;
-#pragma unroll
-                    for (int c = 0; c < R / 8; ++c) {
-                        uint32_t hw[4], lw[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float x0 = v[8 * c + 2 * e], x1 = v[8 * c + 2 * e + 1];
-                            const float h0 = round_bf16(x0), h1 = round_bf16(x1);
-                            hw[e] = pack_bf16(h0, h1);
-                            lw[e] = pack_bf16(x0 - h0, x1 - h1);
-                        }
-                        const int pc = swz_chunk<R>(c, i);
-                        *reinterpret_cast<uint4 *>(vh + i * W + pc * 16) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                        *reinterpret_cast<uint4 *>(vl + i * W + pc * 16) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-                    }
-                    tc::fence_proxy_async_smem();
-                    tc::mbar_arrive(&v_full[vb]);
-                }
-            }
-            const float scale = a.scale[s];
+            const int row0 = pt.y, rows = pt.z;
+            const float scale = a.scale[pt.x];
             const int nb = n_blocks(a, it), d_out = a.d_out[it.l];
             for (int b = 0; b < nb; ++b) {
                 const int st = j % stages, ac = j % kAcc;
@@ -455,36 +468,32 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
                 uint8_t *yt = ring + (size_t)st * kStage + i * 128;    // row i, 128-byte swizzle
                 if (ok) {
                     tc::fence_after_sync();
-                    uint32_t d0[32], d1[32];
-                    tc::tmem_ld32_sync(tmem + lane_addr + 64u * ac, d0);
-                    tc::tmem_ld32_sync(tmem + lane_addr + 64u * ac + 32, d1);
+                    uint32_t d[32];
+                    tc::tmem_ld32_sync(tmem + lane_addr + 64u * ac + 32u * h, d);
                     tc::fence_before_sync();
                     tc::mbar_arrive(&acc_empty[ac]);
-                    uint4 out[8];
+                    uint4 out[4];
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        uint4 *p = reinterpret_cast<uint4 *>(yt + ((c ^ (i & 7)) * 16));
+                    for (int c = 0; c < 4; ++c) {
+                        uint4 *p = reinterpret_cast<uint4 *>(yt + (((4 * h + c) ^ (i & 7)) * 16));
                         const uint4 yv = *p;
                         uint32_t w[4] = {yv.x, yv.y, yv.z, yv.w};
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int n = 8 * c + 2 * e;
-                            const float da = __uint_as_float(n < 32 ? d0[n] : d1[n - 32]);
-                            const float db = __uint_as_float(n + 1 < 32 ? d0[n + 1] : d1[n + 1 - 32]);
-                            w[e] = pack_bf16(fmaf(scale, da, bf_lo(w[e])), fmaf(scale, db, bf_hi(w[e])));
-                        }
+                        for (int e = 0; e < 4; ++e)
+                            w[e] = pack_bf16(fmaf(scale, __uint_as_float(d[8 * c + 2 * e]), bf_lo(w[e])),
+                                             fmaf(scale, __uint_as_float(d[8 * c + 2 * e + 1]), bf_hi(w[e])));
                         out[c] = make_uint4(w[0], w[1], w[2], w[3]);
                         *p = out[c];
                     }
                     if (rows < 128 && i < rows) {
-                        uint16_t *dst = a.y[it.l] + (size_t)(row0 + i) * d_out + col;
+                        uint4 *dst = reinterpret_cast<uint4 *>(a.y[it.l] + (size_t)(row0 + i) * d_out + col + 32 * h);
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) reinterpret_cast<uint4 *>(dst)[c] = out[c];
+                        for (int c = 0; c < 4; ++c) dst[c] = out[c];
                     }
                 }
                 // Generic writes to the stage become visible to the TMA store.
                 tc::fence_proxy_async_smem();
-                tc::named_bar(1, 128);
+                tc::named_bar(1, kEpiThreads);
                 if (leader) {
                     if (rows == 128 && !*err) {
                         tc::tma_store_2d(&a.my[it.l], ring + (size_t)st * kStage, col, row0);
@@ -564,7 +573,7 @@ cudaError_t launch_r(const ShrinkArgs &sa, int grid_tiles, int n_jobs, size_t sh
     prefill_shrink_kernel<R><<<dim3(grid_tiles, n_jobs, 1), kThreads, shrink_smem, st>>>(sa);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    prefill_expand_kernel<R><<<expand_grid, kThreads, expand_smem<R>(ea.stages), st>>>(ea);
+    prefill_expand_kernel<R><<<expand_grid, kExpandThreads, expand_smem<R>(ea.stages), st>>>(ea);
     return cudaGetLastError();
 }
 
