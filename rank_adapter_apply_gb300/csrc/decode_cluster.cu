@@ -74,8 +74,7 @@ __host__ __device__ constexpr size_t region1_bytes(int KB) {
 __host__ __device__ constexpr size_t dyn_bytes(int KB) {
     return region1_bytes(KB)
            + (size_t)kCl * kTileTokens * KB * 16 * 4   // partials pushed by the 8 ranks
-           + (size_t)kCW * KB * 8 * 32 * 4              // cross-warp sums of the shrink
-           + (size_t)kTileTokens * KB * 16 * 4;         // v = sum of the partials
+           + (size_t)kCW * KB * 8 * 32 * 4;             // cross-warp sums of the shrink, then v
 }
 static_assert(sizeof(GroupScratch) <= (size_t)kCl * kTileTokens * 16 * 4, "grouping scratch fits");
 
@@ -84,7 +83,7 @@ struct Dyn {
     uint16_t *xs, *as, *ys, *bs;
     float *vpart;                            // [kCl][16][KB*16] partials pushed by each rank
     float *red;                              // [kCW][KB*8][32]
-    float *vsum;                             // [16][KB*16]
+    float *vsum;                             // [16][KB*16], in `red` once the partials are pushed
     GroupScratch *g;                         // prologue only, aliases vpart
     __device__ Dyn(uint8_t *base) {
         xs = reinterpret_cast<uint16_t *>(base);
@@ -93,7 +92,7 @@ struct Dyn {
         bs = xs + 2 * kTileTokens * kSW;                     // after the shrink
         vpart = reinterpret_cast<float *>(base + region1_bytes(KB));
         red = vpart + kCl * kTileTokens * KB * 16;
-        vsum = red + kCW * KB * 8 * 32;
+        vsum = red;
         g = reinterpret_cast<GroupScratch *>(vpart);
     }
 };
@@ -176,8 +175,13 @@ __device__ void issue_expand(const LayerArgs &L, const ClusterSmem &sm, Dyn<KB> 
     }
 }
 
+// Resident CTAs per SM the register budget must allow (the shared memory of
+// one CTA permits that many): rank 16 fits five, so two consecutive decode
+// steps' CTAs can be resident together under programmatic dependent launch.
+constexpr int min_blocks(int KB) { return KB == 1 ? 5 : (KB == 2 ? 3 : 1); }
+
 template <int KB>
-__global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kCT)
+__global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kCT, min_blocks(KB))
 decode_cluster_kernel(const __grid_constant__ FusedArgs fa) {
     __shared__ ClusterSmem sm;
     extern __shared__ __align__(128) uint8_t dyn_raw[];
@@ -342,11 +346,10 @@ decode_cluster_kernel(const __grid_constant__ FusedArgs fa) {
     }
 
     // The shrink stages are consumed: the same bytes now receive the expand
-    // stages. B never depends on the previous kernel; y may (fa.early waits here).
+    // stages. B never depends on the previous kernel; y may (fa.early waits
+    // for it once the partials of v have been exchanged).
     __syncthreads();
     for (int j = 0; j < nes && j < 2; ++j) issue_expand<KB>(L, sm, d, t, R, o0, o1, j, &sm.ebar[j], 1);
-    if (fa.early) grid_dependency_wait();
-    for (int j = 0; j < nes && j < 2; ++j) issue_expand<KB>(L, sm, d, t, R, o0, o1, j, &sm.ebar[j], 2);
 
     // Cross-warp sum into this CTA's partial v[token][k].
     float *red = d.red;
@@ -434,6 +437,12 @@ decode_cluster_kernel(const __grid_constant__ FusedArgs fa) {
             alo[kb][3] = pack_bf16(f[1][2] - hi[1][2], f[1][3] - hi[1][3]);
         }
     }
+
+    // Everything so far depends only on inputs the caller declared ready
+    // (fa.early): the partial exchange ran before the wait, so after it only
+    // the y rows are fetched, updated and written.
+    if (fa.early) grid_dependency_wait();
+    for (int j = 0; j < nes && j < 2; ++j) issue_expand<KB>(L, sm, d, t, R, o0, o1, j, &sm.ebar[j], 2);
 
     // ---- expand over this CTA's d_out slice --------------------------------
     const float scale = sm.scale;

@@ -17,6 +17,15 @@ using namespace lora;
 
 namespace {
 
+// Tiles of <= kTileTokens tokens over the slots a batch uses: each used slot
+// adds at most kTileTokens - 1 padding places, so
+// sum_s ceil(n_s / 16) <= (T + 15 * min(S, T)) / 16.
+int max_decode_tiles(int T, int S) {
+    const long long used = S < T ? S : T;
+    return (int)(((long long)T + (kTileTokens - 1) * used) / kTileTokens);
+}
+
+
 thread_local std::string g_err;
 
 int fail(int code, const char *fmt, ...) {
@@ -282,7 +291,7 @@ int fused_apply(lora_ctx *c, int n, const int *layers, const void *const *xs, vo
             reinterpret_cast<uintptr_t>(ys[i]) % 16)
             return 1;
     }
-    const int est_tiles = (T + kTileTokens - 1) / kTileTokens + (c->S < T ? c->S : T);
+    const int est_tiles = max_decode_tiles(T, c->S);
     FusedArgs fa{};
     fa.n = n;
     for (int i = 0; i < n; ++i) {
@@ -380,7 +389,7 @@ int apply_impl(lora_ctx *c, int n, const int *layers, const void *const *xs, voi
     }
 
     const size_t e = elem_bytes(c->dtype);
-    const int est_tiles = (T + kTileTokens - 1) / kTileTokens + (c->S < T ? c->S : T);
+    const int est_tiles = max_decode_tiles(T, c->S);
     MultiArgs ma{};
     ma.n = n;
     int max_chunks = 1, max_dblocks = 1;
