@@ -49,9 +49,10 @@ namespace lora {
 namespace {
 
 constexpr int kThreads = 192;              // shrink: warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
-constexpr int kExpandThreads = 384;        // expand: warp 0 TMA, 1 MMA, 2..3 V loaders, 4..11 epilogue
-constexpr int kEpiThreads = 256;
-constexpr int kVThreads = 64;
+constexpr int kExpandThreads = 448;        // expand: warp 0 TMA, 1 MMA, 2..5 V loaders, 6..13 epilogue
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kVThreads = 128;
 constexpr int kTileBytes = 16384;          // 128 rows x 64 bf16: one x k-block or one y n-block
 constexpr int kColBlock = 256;             // d_out columns per expand work item
 constexpr int kAcc = 4;                    // expand accumulators (64 TMEM columns each)
@@ -239,7 +240,8 @@ prefill_shrink_kernel(const __grid_constant__ ShrinkArgs a) {
 // ============================================================================
 
 struct ExpandArgs {
-    CUtensorMap my[kMaxLayersPerCall];        // y [T][d_out], box 64 x 128, 128-byte swizzle
+    CUtensorMap my[kMaxLayersPerCall];        // y [T][d_out], box 64 x 128, 128-byte swizzle (loads)
+    CUtensorMap ms[kMaxLayersPerCall];        // the same y, box 64 x 32 (one row quarter's store)
     CUtensorMap mb[kMaxLayersPerCall];        // B pool [S*d_out][R], box R x 64, rank swizzle
     const float *part[kMaxLayersPerCall];
     uint16_t *y[kMaxLayersPerCall];
@@ -298,7 +300,7 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
     if (tid == 0) {
         for (int i = 0; i < stages; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
+            mbar_init(&empty[i], 4);             // the four row quarters, once their rows are stored
         }
         for (int i = 0; i < kAcc; ++i) {
             mbar_init(&acc_full[i], 1);
@@ -313,6 +315,7 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
         fence_mbar_init();
         for (int l = 0; l < a.n; ++l) {
             tc::prefetch_tensormap(&a.my[l]);
+            tc::prefetch_tensormap(&a.ms[l]);
             tc::prefetch_tensormap(&a.mb[l]);
         }
     }
@@ -393,9 +396,9 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
             tc::mma_commit(&drained);
             mbar_wait_bounded(&drained, 0, kWaitLimit);
         }
-    } else if (warp < 4) {
-        // ---------------- V loaders: rows vt and vt + 64 ----------------
-        const int vt = tid - 64;
+    } else if (warp < 6) {
+        // ---------------- V loaders: row i of the tile ----------------
+        const int i = tid - 64;
         int gen = -1, pl = -1, pp = -1;
         for (int k = k0; k < k1; ++k) {
             const Item it = item_at(a, k, np);
@@ -408,50 +411,70 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
             const int4 pt = a.ptiles[it.p];
             uint8_t *vh = vbuf + (size_t)vb * 2 * kVBytes;
             uint8_t *vl = vh + kVBytes;
-#pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
-                const int i = vt + 64 * h;
-                float v[R];
+            float v[R];
 #pragma unroll
-                for (int r = 0; r < R; ++r) v[r] = 0.f;
-                if (i < pt.z) {
-                    for (int c = 0; c < a.nch[it.l]; ++c) {
-                        const float4 *src = reinterpret_cast<const float4 *>(
-                            a.part[it.l] + ((size_t)c * a.T + pt.y + i) * R);
+            for (int r = 0; r < R; ++r) v[r] = 0.f;
+            if (i < pt.z) {
+                // Partials in chunk order (fixed summation order); two chunks'
+                // loads are in flight together where registers allow.
+                constexpr int kPair = R <= 32 ? 2 : 1;
+                const int nch = a.nch[it.l];
+                const float4 *src = reinterpret_cast<const float4 *>(a.part[it.l] + ((size_t)pt.y + i) * R);
+                const size_t cstride = (size_t)a.T * R / 4;
+                int c = 0;
+                for (; c + kPair <= nch; c += kPair) {
+                    float4 f[kPair][R / 4];
+#pragma unroll
+                    for (int u = 0; u < kPair; ++u)
+#pragma unroll
+                        for (int r = 0; r < R / 4; ++r) f[u][r] = src[(c + u) * cstride + r];
+#pragma unroll
+                    for (int u = 0; u < kPair; ++u)
 #pragma unroll
                         for (int r = 0; r < R / 4; ++r) {
-                            const float4 f = src[r];
-                            v[4 * r] += f.x;
-                            v[4 * r + 1] += f.y;
-                            v[4 * r + 2] += f.z;
-                            v[4 * r + 3] += f.w;
+                            v[4 * r] += f[u][r].x;
+                            v[4 * r + 1] += f[u][r].y;
+                            v[4 * r + 2] += f[u][r].z;
+                            v[4 * r + 3] += f[u][r].w;
                         }
+                }
+                for (; c < nch; ++c) {
+#pragma unroll
+                    for (int r = 0; r < R / 4; ++r) {
+                        const float4 f = src[c * cstride + r];
+                        v[4 * r] += f.x;
+                        v[4 * r + 1] += f.y;
+                        v[4 * r + 2] += f.z;
+                        v[4 * r + 3] += f.w;
                     }
                 }
+            }
 #pragma unroll
-                for (int c = 0; c < R / 8; ++c) {
-                    uint32_t hw[4], lw[4];
+            for (int c = 0; c < R / 8; ++c) {
+                uint32_t hw[4], lw[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float x0 = v[8 * c + 2 * e], x1 = v[8 * c + 2 * e + 1];
-                        const float h0 = round_bf16(x0), h1 = round_bf16(x1);
-                        hw[e] = pack_bf16(h0, h1);
-                        lw[e] = pack_bf16(x0 - h0, x1 - h1);
-                    }
-                    const int pc = swz_chunk<R>(c, i);
-                    *reinterpret_cast<uint4 *>(vh + i * W + pc * 16) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                    *reinterpret_cast<uint4 *>(vl + i * W + pc * 16) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                for (int e = 0; e < 4; ++e) {
+                    const float x0 = v[8 * c + 2 * e], x1 = v[8 * c + 2 * e + 1];
+                    const float h0 = round_bf16(x0), h1 = round_bf16(x1);
+                    hw[e] = pack_bf16(h0, h1);
+                    lw[e] = pack_bf16(x0 - h0, x1 - h1);
                 }
+                const int pc = swz_chunk<R>(c, i);
+                *reinterpret_cast<uint4 *>(vh + i * W + pc * 16) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4 *>(vl + i * W + pc * 16) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
             }
             tc::fence_proxy_async_smem();
             tc::mbar_arrive(&v_full[vb]);
         }
     } else {
         // ---------------- epilogue: row i, columns 32h .. 32h + 31 of each n-block ----------------
-        const int q = warp & 3, h = (warp - 4) >> 2;
+        // The two warps of a TMEM row quarter update their rows of the stage in
+        // place; one of them stores the quarter's 32 rows with a TMA store
+        // (full tiles) and hands the stage back once the store has read it.
+        const int q = warp & 3, h = (warp - 6) >> 2;
         const int i = q * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-        const bool leader = tid == 128;
+        const bool leader = h == 0 && lane == 0;
         int j = 0, pend = -1;
         for (int k = k0; k < k1; ++k) {
             const Item it = item_at(a, k, np);
@@ -491,12 +514,13 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
                         for (int c = 0; c < 4; ++c) dst[c] = out[c];
                     }
                 }
-                // Generic writes to the stage become visible to the TMA store.
+                // Generic writes to the stage become visible to the TMA store; the
+                // two warps of this row quarter meet, one stores its 32 rows.
                 tc::fence_proxy_async_smem();
-                tc::named_bar(1, kEpiThreads);
+                tc::named_bar(1 + q, 64);
                 if (leader) {
                     if (rows == 128 && !*err) {
-                        tc::tma_store_2d(&a.my[it.l], ring + (size_t)st * kStage, col, row0);
+                        tc::tma_store_2d(&a.ms[it.l], ring + (size_t)st * kStage + q * 32 * 128, col, row0 + 32 * q);
                         tc::bulk_commit_group();
                         tc::bulk_wait_group_read<1>();
                         if (pend >= 0) tc::mbar_arrive(&empty[pend]);
@@ -690,6 +714,7 @@ cudaError_t launch_prefill_tc(const PrefillLayer *L, int n, int T, int S, int R,
     for (int i = 0; i < n; ++i) {
         if (L[i].d_out % 64 != 0) return cudaErrorInvalidValue;
         if (!encode_2d(&ea.my[i], L[i].y, (uint64_t)L[i].d_out, (uint64_t)T, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_2d(&ea.ms[i], L[i].y, (uint64_t)L[i].d_out, (uint64_t)T, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B) ||
             !encode_2d(&ea.mb[i], L[i].B, (uint64_t)R, (uint64_t)S * L[i].d_out, (uint32_t)R, 64, swz_rank))
             return cudaErrorInvalidValue;
         ea.part[i] = L[i].part;
