@@ -55,7 +55,8 @@ constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kVThreads = 128;
 constexpr int kTileBytes = 16384;          // 128 rows x 64 bf16: one x k-block or one y n-block
 constexpr int kColBlock = 256;             // d_out columns per expand work item
-constexpr int kAcc = 4;                    // expand accumulators (64 TMEM columns each)
+constexpr int kNB = 128;                   // d_out columns per expand n-block (two 64-column y boxes)
+constexpr int kAcc = 2;                    // expand accumulators (kNB TMEM columns each)
 constexpr int kMaxStages = 8;
 constexpr int kMaxJobs = 64;
 constexpr uint32_t kWaitLimit = 1u << 22;
@@ -242,7 +243,7 @@ prefill_shrink_kernel(const __grid_constant__ ShrinkArgs a) {
 struct ExpandArgs {
     CUtensorMap my[kMaxLayersPerCall];        // y [T][d_out], box 64 x 128, 128-byte swizzle (loads)
     CUtensorMap ms[kMaxLayersPerCall];        // the same y, box 64 x 32 (one row quarter's store)
-    CUtensorMap mb[kMaxLayersPerCall];        // B pool [S*d_out][R], box R x 64, rank swizzle
+    CUtensorMap mb[kMaxLayersPerCall];        // B pool [S*d_out][R], box R x 128, rank swizzle
     const float *part[kMaxLayersPerCall];
     uint16_t *y[kMaxLayersPerCall];
     int d_out[kMaxLayersPerCall], ncb[kMaxLayersPerCall], nch[kMaxLayersPerCall];
@@ -268,8 +269,8 @@ __device__ __forceinline__ Item item_at(const ExpandArgs &a, int k, int np) {
 }
 
 __device__ __forceinline__ int n_blocks(const ExpandArgs &a, const Item &it) {
-    const int left = (a.d_out[it.l] - it.cb * kColBlock) / 64;
-    return left < kColBlock / 64 ? left : kColBlock / 64;
+    const int left = (a.d_out[it.l] - it.cb * kColBlock + kNB - 1) / kNB;
+    return left < kColBlock / kNB ? left : kColBlock / kNB;
 }
 
 template <int R>
@@ -284,7 +285,7 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
 
     constexpr int W = R * 2;                                   // bytes per V / B row
     constexpr uint32_t kSwzRank = R == 64 ? tc::kSwz128 : (R == 32 ? tc::kSwz64 : tc::kSwz32);
-    constexpr uint32_t kStage = kTileBytes + 64 * W;
+    constexpr uint32_t kStage = 2 * kTileBytes + kNB * W;       // y boxes [2][128][64], B [128][R]
     constexpr uint32_t kVBytes = 128 * W;
     const int stages = a.stages;
     uint8_t *ring = base;
@@ -300,7 +301,7 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
     if (tid == 0) {
         for (int i = 0; i < stages; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 4);             // the four row quarters, once their rows are stored
+            mbar_init(&empty[i], kEpiWarps);     // every epilogue warp, once its rows are stored
         }
         for (int i = 0; i < kAcc; ++i) {
             mbar_init(&acc_full[i], 1);
@@ -320,7 +321,7 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
         }
     }
     if (warp == 1) {
-        tc::tmem_alloc(&tmem_base, 64 * kAcc);
+        tc::tmem_alloc(&tmem_base, kNB * kAcc);
         tc::tmem_relinquish();
     }
     tc::fence_before_sync();
@@ -341,10 +342,11 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
                     const int st = j % stages;
                     if (!wait_ok(&empty[st], ((uint32_t)(j / stages) & 1u) ^ 1u, err)) break;
                     uint8_t *tile = ring + (size_t)st * kStage;
-                    const int col = it.cb * kColBlock + b * 64;
+                    const int col = it.cb * kColBlock + b * kNB;
                     mbar_arrive_expect_tx(&full[st], kStage);
                     tc::tma_load_2d(tile, &a.my[it.l], col, pt.y, &full[st]);
-                    tc::tma_load_2d(tile + kTileBytes, &a.mb[it.l], 0, pt.x * d_out + col, &full[st]);
+                    tc::tma_load_2d(tile + kTileBytes, &a.my[it.l], col + 64, pt.y, &full[st]);
+                    tc::tma_load_2d(tile + 2 * kTileBytes, &a.mb[it.l], 0, pt.x * d_out + col, &full[st]);
                     ++j;
                 }
             }
@@ -354,7 +356,7 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------- MMA issuer ----------------
-            constexpr uint32_t idesc = tc::idesc_bf16(128, 64);
+            constexpr uint32_t idesc = tc::idesc_bf16(128, kNB);
             int j = 0, gen = -1, pl = -1, pp = -1;
             for (int k = k0; k < k1 && !*err; ++k) {
                 const Item it = item_at(a, k, np);
@@ -373,8 +375,8 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
                     if (!wait_ok(&full[st], (uint32_t)(j / stages) & 1u, err)) break;
                     if (!wait_ok(&acc_empty[ac], ((uint32_t)(j / kAcc) & 1u) ^ 1u, err)) break;
                     tc::fence_after_sync();
-                    const uint32_t ba = smem_u32(ring + (size_t)st * kStage + kTileBytes);
-                    const uint32_t d = tmem + 64u * ac;
+                    const uint32_t ba = smem_u32(ring + (size_t)st * kStage + 2 * kTileBytes);
+                    const uint32_t d = tmem + (uint32_t)kNB * ac;
 #pragma unroll
                     for (int kk = 0; kk < R / 16; ++kk)
                         tc::mma_bf16(d, tc::smem_desc(vh + kk * 32, W, kSwzRank),
@@ -467,14 +469,14 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
             tc::mbar_arrive(&v_full[vb]);
         }
     } else {
-        // ---------------- epilogue: row i, columns 32h .. 32h + 31 of each n-block ----------------
-        // The two warps of a TMEM row quarter update their rows of the stage in
-        // place; one of them stores the quarter's 32 rows with a TMA store
-        // (full tiles) and hands the stage back once the store has read it.
+        // ---------------- epilogue: row i, columns 64h .. 64h + 63 of each n-block ----------------
+        // Each warp updates its 32 rows x 64 columns of the stage in place and
+        // stores them with its own TMA store (full tiles) or row stores
+        // (ragged tiles); the stage goes back to the producer once all eight
+        // warps' stores have read it.
         const int q = warp & 3, h = (warp - 6) >> 2;
         const int i = q * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-        const bool leader = h == 0 && lane == 0;
         int j = 0, pend = -1;
         for (int k = k0; k < k1; ++k) {
             const Item it = item_at(a, k, np);
@@ -484,43 +486,47 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
             const int nb = n_blocks(a, it), d_out = a.d_out[it.l];
             for (int b = 0; b < nb; ++b) {
                 const int st = j % stages, ac = j % kAcc;
-                const int col = it.cb * kColBlock + b * 64;
+                const int col = it.cb * kColBlock + b * kNB + 64 * h;    // this warp's first column
+                const bool live = col < d_out;
                 bool ok = wait_ok(&acc_full[ac], (uint32_t)(j / kAcc) & 1u, err);
                 ok = ok && wait_ok(&full[st], (uint32_t)(j / stages) & 1u, err);
                 ok = __all_sync(0xffffffffu, ok);
-                uint8_t *yt = ring + (size_t)st * kStage + i * 128;    // row i, 128-byte swizzle
+                uint8_t *ybox = ring + (size_t)st * kStage + h * kTileBytes;
+                uint8_t *yt = ybox + i * 128;                             // row i, 128-byte swizzle
                 if (ok) {
                     tc::fence_after_sync();
-                    uint32_t d[32];
-                    tc::tmem_ld32_sync(tmem + lane_addr + 64u * ac + 32u * h, d);
+                    uint32_t d[64];
+                    {
+                        uint32_t (&d0)[32] = *reinterpret_cast<uint32_t (*)[32]>(d);
+                        uint32_t (&d1)[32] = *reinterpret_cast<uint32_t (*)[32]>(d + 32);
+                        tc::tmem_ld32_sync(tmem + lane_addr + (uint32_t)kNB * ac + 64u * h, d0);
+                        tc::tmem_ld32_sync(tmem + lane_addr + (uint32_t)kNB * ac + 64u * h + 32, d1);
+                    }
                     tc::fence_before_sync();
                     tc::mbar_arrive(&acc_empty[ac]);
-                    uint4 out[4];
+                    if (live) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint4 *p = reinterpret_cast<uint4 *>(yt + (((4 * h + c) ^ (i & 7)) * 16));
-                        const uint4 yv = *p;
-                        uint32_t w[4] = {yv.x, yv.y, yv.z, yv.w};
+                        for (int c = 0; c < 8; ++c) {
+                            uint4 *p = reinterpret_cast<uint4 *>(yt + ((c ^ (i & 7)) * 16));
+                            const uint4 yv = *p;
+                            uint32_t w[4] = {yv.x, yv.y, yv.z, yv.w};
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            w[e] = pack_bf16(fmaf(scale, __uint_as_float(d[8 * c + 2 * e]), bf_lo(w[e])),
-                                             fmaf(scale, __uint_as_float(d[8 * c + 2 * e + 1]), bf_hi(w[e])));
-                        out[c] = make_uint4(w[0], w[1], w[2], w[3]);
-                        *p = out[c];
-                    }
-                    if (rows < 128 && i < rows) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(a.y[it.l] + (size_t)(row0 + i) * d_out + col + 32 * h);
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) dst[c] = out[c];
+                            for (int e = 0; e < 4; ++e)
+                                w[e] = pack_bf16(fmaf(scale, __uint_as_float(d[8 * c + 2 * e]), bf_lo(w[e])),
+                                                 fmaf(scale, __uint_as_float(d[8 * c + 2 * e + 1]), bf_hi(w[e])));
+                            const uint4 o = make_uint4(w[0], w[1], w[2], w[3]);
+                            *p = o;
+                            if (rows < 128 && i < rows)
+                                reinterpret_cast<uint4 *>(a.y[it.l] + (size_t)(row0 + i) * d_out + col)[c] = o;
+                        }
                     }
                 }
-                // Generic writes to the stage become visible to the TMA store; the
-                // two warps of this row quarter meet, one stores its 32 rows.
+                // Generic writes to the stage become visible to the TMA store.
                 tc::fence_proxy_async_smem();
-                tc::named_bar(1 + q, 64);
-                if (leader) {
-                    if (rows == 128 && !*err) {
-                        tc::tma_store_2d(&a.ms[it.l], ring + (size_t)st * kStage + q * 32 * 128, col, row0 + 32 * q);
+                __syncwarp();
+                if (lane == 0) {
+                    if (rows == 128 && live && !*err) {
+                        tc::tma_store_2d(&a.ms[it.l], ybox + q * 32 * 128, col, row0 + 32 * q);
                         tc::bulk_commit_group();
                         tc::bulk_wait_group_read<1>();
                         if (pend >= 0) tc::mbar_arrive(&empty[pend]);
@@ -539,7 +545,7 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
                 ++j;
             }
         }
-        if (leader) {
+        if (lane == 0) {
             tc::bulk_wait_group_all();
             if (pend >= 0) tc::mbar_arrive(&empty[pend]);
         }
@@ -551,7 +557,7 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
     if (warp == 1) {
         __syncwarp();
         tc::fence_after_sync();
-        tc::tmem_dealloc(tmem, 64 * kAcc);
+        tc::tmem_dealloc(tmem, kNB * kAcc);
     }
 }
 
@@ -578,7 +584,7 @@ bool encode_2d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, ui
 
 template <int R>
 size_t expand_smem(int stages) {
-    return 1024 + (size_t)stages * (kTileBytes + 64 * R * 2) + 4 * (size_t)128 * R * 2;
+    return 1024 + (size_t)stages * (2 * kTileBytes + kNB * R * 2) + 4 * (size_t)128 * R * 2;
 }
 
 template <int R>
@@ -715,7 +721,7 @@ cudaError_t launch_prefill_tc(const PrefillLayer *L, int n, int T, int S, int R,
         if (L[i].d_out % 64 != 0) return cudaErrorInvalidValue;
         if (!encode_2d(&ea.my[i], L[i].y, (uint64_t)L[i].d_out, (uint64_t)T, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
             !encode_2d(&ea.ms[i], L[i].y, (uint64_t)L[i].d_out, (uint64_t)T, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_2d(&ea.mb[i], L[i].B, (uint64_t)R, (uint64_t)S * L[i].d_out, (uint32_t)R, 64, swz_rank))
+            !encode_2d(&ea.mb[i], L[i].B, (uint64_t)R, (uint64_t)S * L[i].d_out, (uint32_t)R, kNB, swz_rank))
             return cudaErrorInvalidValue;
         ea.part[i] = L[i].part;
         ea.y[i] = static_cast<uint16_t *>(L[i].y);
@@ -724,7 +730,7 @@ cudaError_t launch_prefill_tc(const PrefillLayer *L, int n, int T, int S, int R,
         ea.nch[i] = nch[grp[i]];
         ea.sum_ncb += ea.ncb[i];
     }
-    const size_t vbytes = 4 * (size_t)128 * R * 2, stage = kTileBytes + 64 * (size_t)R * 2;
+    const size_t vbytes = 4 * (size_t)128 * R * 2, stage = 2 * kTileBytes + kNB * (size_t)R * 2;
     ea.stages = (int)((kExpandSmemBudget - 1024 - vbytes) / stage);
     if (ea.stages > kMaxStages) ea.stages = kMaxStages;
     ea.ptiles = ptiles;
