@@ -34,6 +34,8 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kExpandCols = 256;          // output columns per expand CTA (bf16 and fp32)
 
 // Sum the chunk partials of one tile in chunk order and write v (last CTA only).
+// Loads of eight chunks are issued before they are added (the sum keeps the
+// chunk order), so a 14-way split costs two L2 round trips, not fourteen.
 __device__ void finish_split(const LayerArgs &L, const GroupView &g, int tile_i, int p0, int cnt,
                              int r) {
     __shared__ int last;
@@ -47,11 +49,20 @@ __device__ void finish_split(const LayerArgs &L, const GroupView &g, int tile_i,
     if (!last) return;
     __threadfence();
     const int R = g.R, T = g.T;
+    const size_t cs = (size_t)T * R;
     for (int e = threadIdx.x; e < cnt * r; e += kThreads) {
-        int pos = p0 + e / r, k = e % r;
+        const int pos = p0 + e / r, k = e % r;
+        const float *src = L.part + (size_t)pos * R + k;
         float s = 0.f;
-        for (int ch = 0; ch < L.n_chunks; ++ch)
-            s += __ldcg(&L.part[((size_t)ch * T + pos) * R + k]);
+        int ch = 0;
+        for (; ch + 8 <= L.n_chunks; ch += 8) {
+            float a[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) a[u] = __ldcg(src + (size_t)(ch + u) * cs);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) s += a[u];
+        }
+        for (; ch < L.n_chunks; ++ch) s += __ldcg(src + (size_t)ch * cs);
         L.v[(size_t)pos * R + k] = s;
     }
     if (threadIdx.x == 0) L.counters[tile_i] = 0;
@@ -178,6 +189,21 @@ __device__ __forceinline__ void expand_bf16_tile(const LayerArgs &L, const Group
     uint16_t *y = static_cast<uint16_t *>(L.y);
     const int vec = L.vec;
 
+    // y of both column groups and both token rows, fetched before the MMAs so
+    // that their latency overlaps the B loads.
+    uint4 ypre[2][2];
+#pragma unroll
+    for (int grp = 0; grp < 2; ++grp) {
+        const int cc = dblock * kExpandCols + warp * 64 + grp * 32 + 8 * tq;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int tok = h ? tok1 : tok0;
+            ypre[grp][h] = (vec && tok >= 0 && cc + 8 <= d_out)
+                               ? *reinterpret_cast<const uint4 *>(y + (size_t)tok * d_out + cc)
+                               : make_uint4(0, 0, 0, 0);
+        }
+    }
+
 #pragma unroll
     for (int grp = 0; grp < 2; ++grp) {
         const int c = dblock * kExpandCols + warp * 64 + grp * 32;
@@ -219,7 +245,7 @@ __device__ __forceinline__ void expand_bf16_tile(const LayerArgs &L, const Group
                 dlt[2 * j + 1] = acc[j][2 * h + 1];
             }
             if (vec && cc + 8 <= d_out) {
-                uint4 yv = *reinterpret_cast<const uint4 *>(row + cc);
+                const uint4 yv = ypre[grp][h];
                 uint32_t w[4] = {yv.x, yv.y, yv.z, yv.w};
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
