@@ -46,7 +46,7 @@ enum lora_status {
     LORA_ERR_ARG = -1,      /* bad pointer, size, index or layout */
     LORA_ERR_RANK = -2,     /* r > max_lora_rank ("LoRA rank exceeds maximum",
                                "vLLM LoRA Resolver 插件详解" page, section 6.1 item 4) */
-    LORA_ERR_NO_SLOT = -3,  /* every occupied slot is in flight, nothing evictable */
+    LORA_ERR_NO_SLOT = -3,  /* no occupied slot may be evicted (in flight, pinned or cooling) */
     LORA_ERR_CUDA = -4,     /* a CUDA runtime call failed (message has the detail) */
     LORA_ERR_STATE = -5,    /* call not valid in the current state */
 };
@@ -172,9 +172,10 @@ int lora_lookup(lora_ctx *ctx, uint64_t adapter_id, int *slot);
 /*
  * Hit: touch, *slot = its slot, *needs_load = 0. Miss: validate rank first
  * (LORA_ERR_RANK, nothing evicted), then take the lowest free slot, else evict
- * the least recently used slot that is not in flight (LORA_ERR_NO_SLOT if
- * none); bind the id, *needs_load = 1, *evicted_id = the removed id or
- * UINT64_MAX. The caller then uploads with lora_load_slot.
+ * the slot the eviction policy picks among those not in flight, not pinned and
+ * not cooling (least recently used by default; LORA_ERR_NO_SLOT if none);
+ * bind the id, *needs_load = 1, *evicted_id = the removed id or UINT64_MAX.
+ * The caller then uploads with lora_load_slot.
  */
 int lora_assign(lora_ctx *ctx, uint64_t adapter_id, int rank, int *slot,
                 int *needs_load, uint64_t *evicted_id);
@@ -184,9 +185,10 @@ int lora_acquire(lora_ctx *ctx, int slot);
 int lora_release(lora_ctx *ctx, int slot);
 
 /*
- * Evict the least recently used occupied slot that is not in flight.
+ * Evict the occupied slot the eviction policy picks (least recently used by
+ * default) among those not in flight, not pinned and not cooling.
  * *evicted_slot = -1 when no slot is occupied (LORA_OK). LORA_ERR_NO_SLOT when
- * every occupied slot is in flight. With a device context the slot's rank is
+ * no occupied slot may be evicted. With a device context the slot's rank is
  * set to 0 on the device, after compute work already queued.
  */
 int lora_evict_lru(lora_ctx *ctx, int *evicted_slot, uint64_t *evicted_id);
@@ -196,6 +198,55 @@ int lora_tick(lora_ctx *ctx);
 
 /* Set the thrash window in epochs (default 10). */
 int lora_set_thrash_window(lora_ctx *ctx, int epochs);
+
+/*
+ * Eviction policies on top of LRU, from the "Multi-LoRA 适配器缓存生产实战" page,
+ * section 为什么纯 LRU 在多租户场景下容易失效 (warm set / pin, a cooling window
+ * against short bursts, a recency + frequency keep_score), and the `pinned`
+ * field of section 数据面. Every policy still never evicts a slot in flight,
+ * still uses the lowest free slot first and still validates the rank before
+ * anything is evicted. They apply to lora_assign and lora_evict_lru alike.
+ */
+
+/*
+ * Pin (pinned != 0) or unpin the adapter in an occupied slot: a pinned slot
+ * is never chosen for eviction (the warm set). LORA_ERR_STATE if the slot is
+ * empty, LORA_ERR_ARG if out of range. The pin ends when the slot is unpinned;
+ * a pinned adapter can still be replaced only by first unpinning it.
+ */
+int lora_pin(lora_ctx *ctx, int slot, int pinned);
+
+/*
+ * Cooling window: an adapter accessed (hit or bound) within the last `epochs`
+ * epochs (current epoch - last access epoch < epochs) is not evicted; an
+ * assign that finds nothing else evictable returns LORA_ERR_NO_SLOT, and the
+ * caller defers that adapter. 0 (default) turns the window off; < 0 is
+ * LORA_ERR_ARG.
+ */
+int lora_set_min_residency(lora_ctx *ctx, int epochs);
+
+enum lora_policy {
+    LORA_POLICY_LRU = 0,         /* least recently used (default) */
+    LORA_POLICY_KEEP_SCORE = 1,  /* lowest keep_score, ties to the least recently used */
+};
+
+/*
+ * Select the eviction policy. keep_score of a resident adapter at epoch E:
+ *   recent     = 1 / (1 + (E - last access epoch))
+ *   frequency  = hits and binds in the last W epochs (epoch > E - W), W the
+ *                thrash window of lora_set_thrash_window
+ *   priority   = the value set with lora_set_adapter_priority (default 0)
+ *   reload_cost = size = rank / max_lora_rank  (relative H2D and slot bytes)
+ *   keep = w1 recent + w2 frequency + w3 priority + w4 reload_cost - w5 size
+ * evaluated in double precision in that order. LORA_ERR_ARG for an unknown policy.
+ */
+int lora_set_policy(lora_ctx *ctx, int policy);
+
+/* keep_score weights w1..w5 (host array of 5 doubles; default 1, 1, 1, 0, 0). */
+int lora_set_keep_score_weights(lora_ctx *ctx, const double *w);
+
+/* The tenant / SLO priority term of keep_score for one adapter id (default 0). */
+int lora_set_adapter_priority(lora_ctx *ctx, uint64_t adapter_id, double priority);
 
 /*
  * Segment-length threshold for the tensor-core prefill path (bf16 contexts

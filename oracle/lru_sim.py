@@ -13,20 +13,35 @@ Semantics, as read from the "Multi-LoRA 适配器缓存生产实战" page:
 * section 需要重点监控哪些指标, item 3: thrash ratio = reloads within a short
   window after eviction / total evictions.
 
+* section 为什么纯 LRU 在多租户场景下容易失效: platform policies on top of
+  LRU — a pinned warm set that low-priority traffic cannot push out, a cooling
+  window (minimum residency) against short bursts, and a recency + frequency
+  keep_score  w1 recent + w2 frequency + w3 priority + w4 reload_cost - w5 size.
+
 Readings where the page is silent: the LRU clock is a counter that advances by
 one on every touch or bind, so no two slots tie; a free slot (lowest index
 first) is used before anything is evicted; the rank is validated before any
 eviction, so a rejected adapter never costs a resident one its slot; the
-thrash window is counted in caller-declared epochs (steps).
+thrash window is counted in caller-declared epochs (steps). For the policies:
+a pinned slot is never a victim; the cooling window protects adapters whose
+last access (hit or bind) is fewer than `min_residency` epochs old; keep_score
+takes recent = 1 / (1 + epochs since the last access), frequency = accesses
+(hits and binds) in the last `thrash_window` epochs, priority as set by the caller,
+reload_cost = size = rank / max_lora_rank, and the lowest score is evicted,
+ties going to the least recently used.
 """
 from __future__ import annotations
 
-from dataclasses import dataclass
+from dataclasses import dataclass, field
 
 OK = 0
+ARG_ERR = -1
 RANK_ERR = -2
 NO_SLOT = -3
 STATE_ERR = -5
+
+
+LRU, KEEP_SCORE = 0, 1
 
 
 @dataclass
@@ -35,6 +50,10 @@ class AdapterRecord:
     hit_count: int = 0
     eviction_count: int = 0
     last_evict_epoch: int | None = None
+    last_access: int | None = None
+    access_epochs: list = field(default_factory=list)   # one entry per access
+    rank: int = 0
+    priority: float = 0.0
 
 
 class LruSlotSim:
@@ -51,23 +70,65 @@ class LruSlotSim:
         self.records: dict[int, AdapterRecord] = {}
         self.hits = self.misses = self.evictions = self.reloads = self.rejected = 0
         self.log: list[tuple] = []
+        self.pinned = [False] * max_loras
+        self.min_residency = 0
+        self.policy = LRU
+        self.weights = (1.0, 1.0, 1.0, 0.0, 0.0)
 
     def _touch(self, s: int) -> None:
         self.clock += 1
         self.last_use[s] = self.clock
+        rec = self.records[self.slot_id[s]]
+        rec.last_access = self.epoch
+        # history older than the window is dropped at each access (a window
+        # changed later applies to what is left)
+        rec.access_epochs = [e for e in rec.access_epochs if e > self.epoch - self.window]
+        rec.access_epochs.append(self.epoch)
+
+    def _may_evict(self, s: int) -> bool:
+        aid = self.slot_id[s]
+        if aid is None or self.refs[s] > 0 or self.pinned[s]:
+            return False
+        if self.min_residency > 0 and self.epoch - self.records[aid].last_access < self.min_residency:
+            return False
+        return True
+
+    def keep_score(self, s: int) -> float:
+        rec = self.records[self.slot_id[s]]
+        w1, w2, w3, w4, w5 = self.weights
+        recent = 1.0 / (1.0 + float(self.epoch - rec.last_access))
+        freq = float(sum(1 for e in rec.access_epochs if e > self.epoch - self.window))
+        rel = float(rec.rank) / float(self.R)
+        k = w1 * recent
+        k += w2 * freq
+        k += w3 * rec.priority
+        k += w4 * rel
+        k -= w5 * rel
+        return k
 
     def _victim(self) -> int | None:
-        best = None
-        for s in range(self.S):
-            if self.slot_id[s] is None or self.refs[s] > 0:
-                continue
-            if best is None or self.last_use[s] < self.last_use[best]:
-                best = s
-        return best
+        cands = [s for s in range(self.S) if self._may_evict(s)]
+        if not cands:
+            return None
+        if self.policy == LRU:
+            return min(cands, key=lambda s: self.last_use[s])
+        return min(cands, key=lambda s: (self.keep_score(s), self.last_use[s]))
+
+    def pin(self, s: int, on: bool = True) -> int:
+        if not 0 <= s < self.S:
+            return ARG_ERR
+        if self.slot_id[s] is None:
+            return STATE_ERR
+        self.pinned[s] = bool(on)
+        return OK
+
+    def set_priority(self, aid: int, p: float) -> None:
+        self.records.setdefault(aid, AdapterRecord()).priority = float(p)
 
     def _evict(self, s: int) -> int:
         aid = self.slot_id[s]
         self.slot_id[s] = None
+        self.pinned[s] = False
         del self.where[aid]
         self.evictions += 1
         rec = self.records[aid]
@@ -108,9 +169,11 @@ class LruSlotSim:
         if rec.last_evict_epoch is not None and self.epoch - rec.last_evict_epoch <= self.window:
             self.reloads += 1
         rec.load_count += 1
+        rec.rank = rank
         self.slot_id[s] = aid
         self.where[aid] = s
         self.refs[s] = 0
+        self.pinned[s] = False
         self._touch(s)
         self.misses += 1
         self.log.append(("assign", aid, OK, s, 1, evicted))

@@ -31,7 +31,8 @@ EXPORTED = [
     "lora_apply_multi", "lora_apply_multi_host", "lora_lookup", "lora_assign", "lora_acquire",
     "lora_release", "lora_evict_lru", "lora_tick", "lora_set_thrash_window",
     "lora_set_prefill_min_tokens", "lora_set_small_batch_tokens", "lora_set_inputs_ready", "lora_sync_uploads", "lora_stats", "lora_adapter_bytes",
-    "lora_last_error", "lora_apply_static_scratch",
+    "lora_last_error", "lora_apply_static_scratch", "lora_pin", "lora_set_min_residency",
+    "lora_set_policy", "lora_set_keep_score_weights", "lora_set_adapter_priority",
 ]
 
 
@@ -88,6 +89,11 @@ def load(path: str = LIB_PATH):
         "lora_evict_lru": (i32, [vp, P(i32), P(u64)]),
         "lora_tick": (i32, [vp]),
         "lora_set_thrash_window": (i32, [vp, i32]),
+        "lora_pin": (i32, [vp, i32, i32]),
+        "lora_set_min_residency": (i32, [vp, i32]),
+        "lora_set_policy": (i32, [vp, i32]),
+        "lora_set_keep_score_weights": (i32, [vp, P(ctypes.c_double)]),
+        "lora_set_adapter_priority": (i32, [vp, u64, ctypes.c_double]),
         "lora_set_prefill_min_tokens": (i32, [vp, i32]),
         "lora_set_small_batch_tokens": (i32, [vp, i32]),
         "lora_set_inputs_ready": (i32, [vp, i32]),
@@ -203,6 +209,31 @@ def lora_tick(ctx):
 
 def lora_set_thrash_window(ctx, epochs):
     return check(load().lora_set_thrash_window(ctx, epochs))
+
+
+LORA_POLICY_LRU, LORA_POLICY_KEEP_SCORE = 0, 1
+
+
+def lora_pin(ctx, slot, pinned=True):
+    """Returns the status (LORA_ERR_STATE for an empty slot)."""
+    return load().lora_pin(ctx, slot, 1 if pinned else 0)
+
+
+def lora_set_min_residency(ctx, epochs):
+    return check(load().lora_set_min_residency(ctx, epochs))
+
+
+def lora_set_policy(ctx, policy):
+    return check(load().lora_set_policy(ctx, policy))
+
+
+def lora_set_keep_score_weights(ctx, w):
+    arr = (ctypes.c_double * 5)(*[float(v) for v in w])
+    return check(load().lora_set_keep_score_weights(ctx, arr))
+
+
+def lora_set_adapter_priority(ctx, adapter_id, priority):
+    return check(load().lora_set_adapter_priority(ctx, int(adapter_id), float(priority)))
 
 
 def lora_set_prefill_min_tokens(ctx, n):

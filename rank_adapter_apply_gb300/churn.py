@@ -12,6 +12,10 @@ adapters one batch may use, "Multi-LoRA 适配器缓存生产实战" page, secti
   4. releases the references.
 The epoch advances once per step (the thrash window counts epochs). Every
 decision goes through the C ABI; this module only moves data.
+
+`admission_stats` replays the same admission on a host-only context (no GPU)
+to compare the eviction policies of the section 为什么纯 LRU 在多租户场景下容易
+失效: pure LRU, a pinned warm set of the most popular adapters, and keep_score.
 """
 from __future__ import annotations
 
@@ -27,6 +31,69 @@ from .harness import to_torch
 from .slots import LoraSlots
 
 
+def plan_groups(order, pinned_resident, capacity):
+    """Split a step's distinct adapters (first-appearance order) into groups:
+    every adapter not already resident in a pinned slot needs one of
+    `capacity` evictable slots (max_loras minus the pinned ones)."""
+    groups, cur, cost = [], [], 0
+    for a in order:
+        c = 0 if a in pinned_resident else 1
+        if cur and cost + c > capacity:
+            groups.append(cur)
+            cur, cost = [], 0
+        cur.append(a)
+        cost += c
+    if cur:
+        groups.append(cur)
+    return groups
+
+
+def admission_stats(trace, max_loras=64, rank=16, policy=0, weights=None, pin_top=0,
+                    min_residency=0, window=10, record=False):
+    """Host-only replay of the churn admission: per step, groups of adapters are
+    assigned (hit: touch; miss: free slot or policy victim), acquired, then
+    released; adapters with id < pin_top are pinned when first bound (the warm
+    set). Returns the slot-table statistics (and the decision log if record)."""
+    ctx = B.lora_slots_init(max_loras, rank, 0, 1, B.LORA_DTYPE_BF16, [], None, None, None, 0,
+                            None, None)
+    lib = B.load()
+    log = []
+    try:
+        B.lora_set_thrash_window(ctx, window)
+        B.lora_set_policy(ctx, policy)
+        if weights is not None:
+            B.lora_set_keep_score_weights(ctx, weights)
+        B.lora_set_min_residency(ctx, min_residency)
+        pinned = {}
+        for k, ids in enumerate(trace.steps):
+            order = list(dict.fromkeys(int(a) for a in ids))
+            for group in plan_groups(order, pinned, max_loras - len(pinned)):
+                held = []
+                for a in group:
+                    st, slot, need, ev = B.lora_assign(ctx, a, rank)
+                    if record:
+                        log.append((k, a, st, slot, need, ev))
+                    if st != 0:
+                        raise RuntimeError(f"assign failed for adapter {a}: {st}")
+                    if a < pin_top and a not in pinned:
+                        B.check(B.lora_pin(ctx, slot, True))
+                        pinned[a] = slot
+                    lib.lora_acquire(ctx, slot)
+                    held.append(slot)
+                for sl in held:
+                    lib.lora_release(ctx, sl)
+            B.lora_tick(ctx)
+        st = B.lora_stats(ctx)
+    finally:
+        B.lora_destroy(ctx)
+    st["hit_rate"] = st["hits"] / max(1, st["hits"] + st["misses"])
+    st["thrash_ratio"] = st["reloads_after_eviction"] / st["evictions"] if st["evictions"] else 0.0
+    st["pinned"] = len(pinned)
+    if record:
+        st["log"] = log
+    return st
+
+
 @dataclass
 class ChurnResult:
     steps: int
@@ -38,7 +105,7 @@ class ChurnResult:
 
 class ChurnRunner:
     def __init__(self, n_adapters=512, max_loras=64, rank=16, d=4096, tokens=256, seed=0,
-                 device="cuda:0", alpha=32.0):
+                 device="cuda:0", alpha=32.0, policy=0, weights=None, pin_top=0):
         self.dev = torch.device(device)
         self.S, self.R, self.d, self.T = max_loras, rank, d, tokens
         self.alpha = alpha
@@ -50,6 +117,11 @@ class ChurnRunner:
         self.layers = ["q_proj", "v_proj"]
         self.slots = LoraSlots([(d, d), (d, d)], max_loras, rank, tokens, dtype=torch.bfloat16,
                                device=self.dev)
+        B.lora_set_policy(self.slots.ctx, policy)
+        if weights is not None:
+            B.lora_set_keep_score_weights(self.slots.ctx, weights)
+        self.pin_top = pin_top
+        self.pinned = {}
         rng = np.random.default_rng(seed + 7)
         xf = rng.standard_normal((tokens, d), dtype=np.float32)
         self.x_np = wl.f32_to_bf16_bits(xf)
@@ -59,8 +131,8 @@ class ChurnRunner:
         self.y0 = [to_torch(v, wl.DTYPE_BF16).to(self.dev) for v in self.y_np]
         self.y = [t.clone() for t in self.y0]
         # one slot-id buffer per adapter group of a step (a step has at most
-        # ceil(tokens / max_loras) groups); reused only after the step's sync
-        self.max_groups = (tokens + max_loras - 1) // max_loras
+        # ceil(tokens / evictable slots) groups); reused only after the step's sync
+        self.max_groups = (tokens + max(1, max_loras - pin_top) - 1) // max(1, max_loras - pin_top)
         self.idx_host = torch.empty((self.max_groups, tokens), dtype=torch.int32).pin_memory()
         self.idx = torch.empty((self.max_groups, tokens), dtype=torch.int32, device=self.dev)
 
@@ -86,8 +158,7 @@ class ChurnRunner:
                         y.copy_(y0)
             order = list(dict.fromkeys(int(a) for a in ids))   # distinct, first appearance
             slot_tok = np.full(self.T, -1, np.int32)
-            for gi, g0 in enumerate(range(0, len(order), self.S)):
-                group = order[g0:g0 + self.S]
+            for gi, group in enumerate(plan_groups(order, self.pinned, self.S - len(self.pinned))):
                 held, where = [], {}
                 for a in group:
                     st, slot, need, ev = B.lora_assign(ctx, a, self.R)
@@ -97,6 +168,9 @@ class ChurnRunner:
                         raise RuntimeError(f"assign failed for adapter {a}: {st}")
                     if need:
                         self.upload(slot, a)
+                    if a < self.pin_top and a not in self.pinned:
+                        B.check(B.lora_pin(ctx, slot, True))
+                        self.pinned[a] = slot
                     lib.lora_acquire(ctx, slot)
                     held.append(slot)
                     where[a] = slot

@@ -510,7 +510,7 @@ int lora_assign(lora_ctx *c, uint64_t id, int rank, int *slot, int *needs_load, 
         return fail(LORA_ERR_RANK, "LoRA rank %d exceeds maximum %d (or is < 1)", rank, c->R);
     case AssignResult::NoSlot:
     default:
-        return fail(LORA_ERR_NO_SLOT, "every occupied slot is in flight");
+        return fail(LORA_ERR_NO_SLOT, "no occupied slot may be evicted (in flight, pinned or cooling)");
     }
 }
 
@@ -524,10 +524,46 @@ int lora_release(lora_ctx *c, int slot) {
     return c->table.release(slot) ? LORA_OK : fail(LORA_ERR_STATE, "slot %d is not in flight", slot);
 }
 
+int lora_pin(lora_ctx *c, int slot, int pinned) {
+    if (!c) return fail(LORA_ERR_ARG, "ctx is NULL");
+    if (slot < 0 || slot >= c->S) return fail(LORA_ERR_ARG, "slot %d out of range", slot);
+    return c->table.pin(slot, pinned != 0) ? LORA_OK : fail(LORA_ERR_STATE, "slot %d is empty", slot);
+}
+
+int lora_set_min_residency(lora_ctx *c, int epochs) {
+    if (!c) return fail(LORA_ERR_ARG, "ctx is NULL");
+    if (epochs < 0) return fail(LORA_ERR_ARG, "epochs must be >= 0");
+    c->table.set_min_residency(epochs);
+    return LORA_OK;
+}
+
+int lora_set_policy(lora_ctx *c, int policy) {
+    if (!c) return fail(LORA_ERR_ARG, "ctx is NULL");
+    if (policy != LORA_POLICY_LRU && policy != LORA_POLICY_KEEP_SCORE)
+        return fail(LORA_ERR_ARG, "unknown policy %d", policy);
+    c->table.set_policy(policy == LORA_POLICY_LRU ? EvictPolicy::Lru : EvictPolicy::KeepScore);
+    return LORA_OK;
+}
+
+int lora_set_keep_score_weights(lora_ctx *c, const double *w) {
+    if (!c || !w) return fail(LORA_ERR_ARG, "NULL argument");
+    for (int i = 0; i < 5; ++i)
+        if (!std::isfinite(w[i])) return fail(LORA_ERR_ARG, "weight %d is not finite", i);
+    c->table.set_weights(w);
+    return LORA_OK;
+}
+
+int lora_set_adapter_priority(lora_ctx *c, uint64_t adapter_id, double priority) {
+    if (!c) return fail(LORA_ERR_ARG, "ctx is NULL");
+    if (!std::isfinite(priority)) return fail(LORA_ERR_ARG, "priority is not finite");
+    c->table.set_priority(adapter_id, priority);
+    return LORA_OK;
+}
+
 int lora_evict_lru(lora_ctx *c, int *evicted_slot, uint64_t *evicted_id) {
     if (!c || !evicted_slot || !evicted_id) return fail(LORA_ERR_ARG, "NULL argument");
     if (!c->table.evict_lru(evicted_slot, evicted_id))
-        return fail(LORA_ERR_NO_SLOT, "every occupied slot is in flight");
+        return fail(LORA_ERR_NO_SLOT, "no occupied slot may be evicted (in flight, pinned or cooling)");
     if (c->device && *evicted_slot >= 0) {
         // The slot reads as empty for work queued after this call.
         if (c->compute_recorded) CUDA_TRY(cudaStreamWaitEvent(c->upload, c->compute_done, 0));

@@ -3,8 +3,20 @@
 namespace lora {
 
 SlotTable::SlotTable(int max_loras, int max_lora_rank)
-    : S_(max_loras), R_(max_lora_rank), id_(max_loras, 0), occ_(max_loras, 0),
+    : S_(max_loras), R_(max_lora_rank), id_(max_loras, 0), occ_(max_loras, 0), pin_(max_loras, 0),
       last_use_(max_loras, 0), refs_(max_loras, 0) {}
+
+void SlotTable::touch(int slot) {
+    last_use_[slot] = ++clock_;
+    AdapterResidency &r = rec_[id_[slot]];
+    r.last_access_epoch = epoch_;
+    if (!r.accesses.empty() && r.accesses.back().first == epoch_) ++r.accesses.back().second;
+    else r.accesses.emplace_back(epoch_, 1u);
+    // Entries older than the window no longer count; keep the list short.
+    size_t drop = 0;
+    while (drop < r.accesses.size() && r.accesses[drop].first <= epoch_ - window_) ++drop;
+    if (drop) r.accesses.erase(r.accesses.begin(), r.accesses.begin() + (long)drop);
+}
 
 int SlotTable::lookup(uint64_t id) {
     auto it = where_.find(id);
@@ -15,12 +27,47 @@ int SlotTable::lookup(uint64_t id) {
     return it->second;
 }
 
-// Least recently used occupied slot with no in-flight reference; -1 if none.
+bool SlotTable::evictable(int s) const {
+    if (!occ_[s] || refs_[s] > 0 || pin_[s]) return false;
+    if (min_res_ > 0) {
+        const AdapterResidency &r = rec_.at(id_[s]);
+        if (epoch_ - r.last_access_epoch < min_res_) return false;
+    }
+    return true;
+}
+
+// Evaluated in this order in double precision (the simulator does the same).
+double SlotTable::keep_score(int s) const {
+    const AdapterResidency &r = rec_.at(id_[s]);
+    const double recent = 1.0 / (1.0 + (double)(epoch_ - r.last_access_epoch));
+    uint64_t n = 0;
+    for (const auto &a : r.accesses)
+        if (a.first > epoch_ - window_) n += a.second;
+    const double freq = (double)n;
+    const double rel = (double)r.rank / (double)R_;
+    double k = w_[0] * recent;
+    k += w_[1] * freq;
+    k += w_[2] * r.priority;
+    k += w_[3] * rel;
+    k -= w_[4] * rel;
+    return k;
+}
+
+// The evictable slot chosen by the policy; -1 if none.
 int SlotTable::victim() const {
     int best = -1;
+    double best_k = 0.0;
     for (int s = 0; s < S_; ++s) {
-        if (!occ_[s] || refs_[s] > 0) continue;
-        if (best < 0 || last_use_[s] < last_use_[best]) best = s;
+        if (!evictable(s)) continue;
+        if (policy_ == EvictPolicy::Lru) {
+            if (best < 0 || last_use_[s] < last_use_[best]) best = s;
+        } else {
+            const double k = keep_score(s);
+            if (best < 0 || k < best_k || (k == best_k && last_use_[s] < last_use_[best])) {
+                best = s;
+                best_k = k;
+            }
+        }
     }
     return best;
 }
@@ -28,6 +75,7 @@ int SlotTable::victim() const {
 uint64_t SlotTable::evict(int slot) {
     uint64_t id = id_[slot];
     occ_[slot] = 0;
+    pin_[slot] = 0;
     refs_[slot] = 0;
     where_.erase(id);
     ++evictions;
@@ -65,8 +113,10 @@ AssignResult SlotTable::assign(uint64_t id, int rank, int *slot, uint64_t *evict
     AdapterResidency &r = rec_[id];
     if (r.last_evict_epoch >= 0 && epoch_ - r.last_evict_epoch <= window_) ++reloads;
     ++r.load_count;
+    r.rank = rank;
     id_[s] = id;
     occ_[s] = 1;
+    pin_[s] = 0;
     refs_[s] = 0;
     where_[id] = s;
     touch(s);
@@ -84,6 +134,12 @@ bool SlotTable::acquire(int slot) {
 bool SlotTable::release(int slot) {
     if (slot < 0 || slot >= S_ || refs_[slot] <= 0) return false;
     --refs_[slot];
+    return true;
+}
+
+bool SlotTable::pin(int slot, bool on) {
+    if (slot < 0 || slot >= S_ || !occ_[slot]) return false;
+    pin_[slot] = on ? 1 : 0;
     return true;
 }
 

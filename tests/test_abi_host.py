@@ -141,3 +141,95 @@ def test_thrash_burst_through_abi(lib):
         assert B.lora_stats(ctx)["reloads_after_eviction"] == 4
     finally:
         B.lora_destroy(ctx)
+
+
+def _policy_stream(ctx, sim, rng, steps, S, pin_p, set_prio):
+    p = np.arange(1, 97, dtype=float) ** -1.1
+    p /= p.sum()
+    for step in range(steps):
+        ids = list(dict.fromkeys(int(a) for a in rng.choice(96, size=14, p=p)))[:S]
+        held = []
+        for a in ids:
+            if set_prio and rng.random() < 0.05:
+                pr = float(rng.integers(0, 4))
+                B.lora_set_adapter_priority(ctx, a, pr)
+                sim.set_priority(a, pr)
+            rank = int(rng.choice([8, 16, 32]))
+            got = B.lora_assign(ctx, a, rank)
+            assert got == sim.assign(a, rank), (step, a, got)
+            if got[0] == 0 and rng.random() < 0.6:
+                assert B.lora_acquire(ctx, got[1]) == sim.acquire(got[1])
+                held.append(got[1])
+        if rng.random() < pin_p:
+            s = int(rng.integers(0, S))
+            on = bool(rng.random() < 0.6)
+            assert B.lora_pin(ctx, s, on) == sim.pin(s, on)
+        if rng.random() < 0.1:
+            assert B.lora_evict_lru(ctx) == sim.evict_lru()
+        for s in held:
+            assert B.lora_release(ctx, s) == sim.release(s)
+        B.lora_tick(ctx)
+        sim.tick()
+    st = B.lora_stats(ctx)
+    assert (st["hits"], st["misses"], st["evictions"], st["reloads_after_eviction"]) == \
+        (sim.hits, sim.misses, sim.evictions, sim.reloads)
+
+
+@pytest.mark.parametrize("policy", [0, 1])
+@pytest.mark.parametrize("min_res", [0, 2])
+def test_policy_decision_log_matches_simulator(lib, policy, min_res):
+    """Pins, the cooling window and both eviction policies: every decision of
+    the library equals the independent simulator's."""
+    from oracle.lru_sim import LruSlotSim
+    rng = np.random.default_rng(10 * policy + min_res)
+    S, R = 8, 32
+    ctx = _host_ctx(S, R)
+    sim = LruSlotSim(S, R, thrash_window=6)
+    try:
+        B.lora_set_thrash_window(ctx, 6)
+        B.lora_set_policy(ctx, policy)
+        sim.policy = policy
+        w = (1.0, 0.5, 2.0, 0.25, 0.75)
+        B.lora_set_keep_score_weights(ctx, w)
+        sim.weights = w
+        B.lora_set_min_residency(ctx, min_res)
+        sim.min_residency = min_res
+        _policy_stream(ctx, sim, rng, 250, S, pin_p=0.2, set_prio=True)
+    finally:
+        B.lora_destroy(ctx)
+
+
+def test_policy_argument_errors(lib):
+    ctx = _host_ctx(2, 16)
+    try:
+        assert B.lora_pin(ctx, 0) == B.LORA_ERR_STATE          # empty slot
+        assert B.lora_pin(ctx, 7) == B.LORA_ERR_ARG
+        with pytest.raises(B.LoraError):
+            B.lora_set_policy(ctx, 9)
+        with pytest.raises(B.LoraError):
+            B.lora_set_min_residency(ctx, -1)
+        with pytest.raises(B.LoraError):
+            B.lora_set_keep_score_weights(ctx, [1, float("nan"), 0, 0, 0])
+        with pytest.raises(B.LoraError):
+            B.lora_set_adapter_priority(ctx, 3, float("inf"))
+    finally:
+        B.lora_destroy(ctx)
+
+
+def test_pinned_burst_through_abi(lib):
+    from oracle.lru_sim import LruSlotSim
+    ctx = _host_ctx(4, 16)
+    sim = LruSlotSim(4, 16)
+    try:
+        ops = []
+        for _ in range(3):
+            ops += [("assign", a, 16) for a in range(4)] + [("tick",)]
+        _run_script(ctx, sim, ops)
+        for s in (0, 1):
+            assert B.lora_pin(ctx, s) == sim.pin(s) == 0
+        ops = [("assign", a, 16) for a in range(100, 120)] + [("tick",)]
+        ops += [("assign", a, 16) for a in range(4)]
+        _run_script(ctx, sim, ops)
+        assert sim.reloads == 2                      # only the unpinned 2 and 3
+    finally:
+        B.lora_destroy(ctx)

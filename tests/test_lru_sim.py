@@ -95,3 +95,107 @@ def test_reload_outside_window_is_not_thrash():
     assert s.reloads == 0
     s.assign(2, 8)          # 2 evicted at epoch 3, reloaded at epoch 3
     assert s.reloads == 1
+
+
+# ---- platform policies (section 为什么纯 LRU 在多租户场景下容易失效) ----------
+
+from oracle.lru_sim import ARG_ERR, KEEP_SCORE  # noqa: E402
+
+
+def _hot_rounds(s, rounds=3):
+    for _ in range(rounds):
+        for a in range(4):
+            s.assign(a, 16)
+        s.tick()
+
+
+def test_pinned_warm_set_survives_burst():
+    """Slots of adapters 0 and 1 pinned: the 20-adapter burst cycles through the
+    two unpinned slots only (2 and 3 go first, then the burst evicts itself)."""
+    s = LruSlotSim(4, 16, thrash_window=10)
+    _hot_rounds(s)
+    assert s.pin(0) == OK and s.pin(1) == OK
+    evicted = [s.assign(a, 16)[3] for a in range(100, 120)]
+    assert evicted[:2] == [2, 3]
+    assert evicted[2:] == list(range(100, 118))
+    s.tick()
+    assert s.assign(0, 16) == (OK, 0, 0, -1) and s.assign(1, 16) == (OK, 1, 0, -1)
+
+
+def test_pin_errors_and_unpin():
+    s = LruSlotSim(2, 16)
+    assert s.pin(0) == STATE_ERR                     # empty slot
+    assert s.pin(5) == ARG_ERR
+    s.assign(1, 8)
+    s.assign(2, 8)
+    s.pin(0)
+    s.pin(1)
+    assert s.assign(3, 8) == (NO_SLOT, -1, 0, -1)    # everything pinned
+    assert s.evict_lru() == (NO_SLOT, -1, -1)
+    s.pin(1, False)
+    assert s.assign(3, 8) == (OK, 1, 1, 2)
+
+
+def test_cooling_window_defers_until_old_enough():
+    s = LruSlotSim(2, 16)
+    s.min_residency = 2
+    s.assign(1, 8)
+    s.assign(2, 8)
+    assert s.assign(3, 8) == (NO_SLOT, -1, 0, -1)    # both accessed this epoch
+    s.tick()
+    assert s.assign(3, 8) == (NO_SLOT, -1, 0, -1)    # 1 epoch old < 2
+    s.lookup(2)                                      # 2 accessed again at epoch 1
+    s.tick()
+    assert s.assign(3, 8) == (OK, 0, 1, 1)           # 1 is 2 epochs old, 2 only 1
+
+
+def test_keep_score_hand_example_differs_from_lru():
+    """w = (1, 1, 0, 0, 0). A: bound at epoch 0 and hit twice; B bound at
+    epoch 1; C bound at epoch 2; at epoch 3:
+      A: recent 1/(1+3) = 0.25, frequency 3  -> 3.25
+      B: recent 1/(1+2),        frequency 1  -> 1.333...
+      C: recent 1/(1+1) = 0.5,  frequency 1  -> 1.5
+    keep_score evicts B; LRU would evict A (oldest last use)."""
+    def build(policy):
+        s = LruSlotSim(3, 16)
+        s.policy = policy
+        s.weights = (1.0, 1.0, 0.0, 0.0, 0.0)
+        s.assign(10, 16); s.lookup(10); s.lookup(10); s.tick()
+        s.assign(11, 16); s.tick()
+        s.assign(12, 16); s.tick()
+        return s
+    k = build(KEEP_SCORE)
+    assert [k.keep_score(i) for i in range(3)] == [3.25, 1.0 + 1.0 / 3.0, 1.5]
+    assert k.assign(13, 16) == (OK, 1, 1, 11)
+    assert build(0).assign(13, 16) == (OK, 0, 1, 10)
+
+
+def test_keep_score_priority_and_size_terms():
+    s = LruSlotSim(2, 64)
+    s.policy = KEEP_SCORE
+    s.weights = (1.0, 1.0, 1.0, 0.0, 1.0)
+    s.assign(1, 64)                                  # size term 1.0
+    s.assign(2, 16)                                  # size term 0.25
+    # both: recent 1, frequency 1 -> 2 - size: 1 -> 1.0, 2 -> 1.75
+    assert s.assign(3, 16) == (OK, 0, 1, 1)
+    s.set_priority(3, 5.0)
+    # 3: 2 + 5 - 0.25 = 6.75 ; 2: 1.75 -> 2 goes
+    assert s.assign(4, 16) == (OK, 1, 1, 2)
+
+
+def test_keep_score_burst_keeps_hot_set():
+    """The page's scenario under keep_score (1, 1, 0, 0, 0): at the burst epoch
+    the hot adapters score 1/2 + 3 = 3.5 and each newcomer 1 + 1 = 2, so the
+    first burst adapter costs one hot adapter (the LRU tie-break) and every
+    later one evicts the previous newcomer."""
+    s = LruSlotSim(4, 16, thrash_window=10)
+    s.policy = KEEP_SCORE
+    s.weights = (1.0, 1.0, 0.0, 0.0, 0.0)
+    _hot_rounds(s)
+    evicted = [s.assign(a, 16)[3] for a in range(100, 120)]
+    assert evicted[0] == 0
+    assert evicted[1:] == list(range(100, 119))
+    s.tick()
+    hot = [s.assign(a, 16) for a in range(4)]
+    assert [h[2] for h in hot] == [1, 0, 0, 0]       # only adapter 0 reloads
+    assert s.reloads == 1
