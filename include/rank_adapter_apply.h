@@ -200,6 +200,19 @@ int lora_tick(lora_ctx *ctx);
 int lora_set_thrash_window(lora_ctx *ctx, int epochs);
 
 /*
+ * Per-slot ordering of uploads (copy/compute overlap; the adapter_h2d term of
+ * the TTFT decomposition and the H2D metric of the "Multi-LoRA 适配器缓存生产实战"
+ * page, sections 冷加载延迟 and 需要重点监控哪些指标). By default an upload or an
+ * eviction waits for every apply queued before it. With tracking on, the
+ * caller promises that each apply's token_slot_idx names only slots it holds
+ * in flight (lora_acquire) when it calls apply; an upload into slot s then
+ * waits only for the last apply issued while s was in flight, so the next
+ * step's adapters can be copied while the current step computes. Device
+ * contexts only (LORA_ERR_STATE otherwise).
+ */
+int lora_set_slot_tracking(lora_ctx *ctx, int on);
+
+/*
  * Eviction policies on top of LRU, from the "Multi-LoRA 适配器缓存生产实战" page,
  * section 为什么纯 LRU 在多租户场景下容易失效 (warm set / pin, a cooling window
  * against short bursts, a recency + frequency keep_score), and the `pinned`

@@ -33,6 +33,7 @@ EXPORTED = [
     "lora_set_prefill_min_tokens", "lora_set_small_batch_tokens", "lora_set_inputs_ready", "lora_sync_uploads", "lora_stats", "lora_adapter_bytes",
     "lora_last_error", "lora_apply_static_scratch", "lora_pin", "lora_set_min_residency",
     "lora_set_policy", "lora_set_keep_score_weights", "lora_set_adapter_priority",
+    "lora_set_slot_tracking",
 ]
 
 
@@ -90,6 +91,7 @@ def load(path: str = LIB_PATH):
         "lora_tick": (i32, [vp]),
         "lora_set_thrash_window": (i32, [vp, i32]),
         "lora_pin": (i32, [vp, i32, i32]),
+        "lora_set_slot_tracking": (i32, [vp, i32]),
         "lora_set_min_residency": (i32, [vp, i32]),
         "lora_set_policy": (i32, [vp, i32]),
         "lora_set_keep_score_weights": (i32, [vp, P(ctypes.c_double)]),
@@ -212,6 +214,10 @@ def lora_set_thrash_window(ctx, epochs):
 
 
 LORA_POLICY_LRU, LORA_POLICY_KEEP_SCORE = 0, 1
+
+
+def lora_set_slot_tracking(ctx, on=True):
+    return check(load().lora_set_slot_tracking(ctx, 1 if on else 0))
 
 
 def lora_pin(ctx, slot, pinned=True):

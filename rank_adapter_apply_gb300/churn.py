@@ -105,7 +105,7 @@ class ChurnResult:
 
 class ChurnRunner:
     def __init__(self, n_adapters=512, max_loras=64, rank=16, d=4096, tokens=256, seed=0,
-                 device="cuda:0", alpha=32.0, policy=0, weights=None, pin_top=0):
+                 device="cuda:0", alpha=32.0, policy=0, weights=None, pin_top=0, overlap=False):
         self.dev = torch.device(device)
         self.S, self.R, self.d, self.T = max_loras, rank, d, tokens
         self.alpha = alpha
@@ -122,6 +122,12 @@ class ChurnRunner:
             B.lora_set_keep_score_weights(self.slots.ctx, weights)
         self.pin_top = pin_top
         self.pinned = {}
+        # overlap: uploads wait only for the applies that used their slot, and
+        # the host runs ahead of the GPU (slot-id buffers rotate over 4 steps)
+        self.overlap = overlap
+        if overlap:
+            B.lora_set_slot_tracking(self.slots.ctx, True)
+        self.ring = 4 if overlap else 1
         rng = np.random.default_rng(seed + 7)
         xf = rng.standard_normal((tokens, d), dtype=np.float32)
         self.x_np = wl.f32_to_bf16_bits(xf)
@@ -133,8 +139,9 @@ class ChurnRunner:
         # one slot-id buffer per adapter group of a step (a step has at most
         # ceil(tokens / evictable slots) groups); reused only after the step's sync
         self.max_groups = (tokens + max(1, max_loras - pin_top) - 1) // max(1, max_loras - pin_top)
-        self.idx_host = torch.empty((self.max_groups, tokens), dtype=torch.int32).pin_memory()
-        self.idx = torch.empty((self.max_groups, tokens), dtype=torch.int32, device=self.dev)
+        self.idx_host = torch.empty((self.ring, self.max_groups, tokens), dtype=torch.int32).pin_memory()
+        self.idx = torch.empty((self.ring, self.max_groups, tokens), dtype=torch.int32, device=self.dev)
+        self.step_done = [None] * self.ring
 
     def upload(self, slot, adapter):
         a = [self.A[l][adapter] for l in self.layers]
@@ -152,6 +159,9 @@ class ChurnRunner:
         torch.cuda.synchronize(self.dev)
         t0 = time.perf_counter()
         for k, ids in enumerate(trace.steps):
+            rb = k % self.ring
+            if self.step_done[rb] is not None:
+                self.step_done[rb].synchronize()          # this step's slot-id buffers are free
             if reset_y or k == check_step:
                 with torch.cuda.stream(self.slots.compute):
                     for y, y0 in zip(self.y, self.y0):
@@ -177,14 +187,18 @@ class ChurnRunner:
                 sel = np.isin(ids, group)
                 idx = np.where(sel, [where.get(int(a), -1) for a in ids], -1).astype(np.int32)
                 slot_tok[sel] = idx[sel]
-                self.idx_host[gi].numpy()[:] = idx
+                self.idx_host[rb, gi].numpy()[:] = idx
                 with torch.cuda.stream(self.slots.compute):
-                    self.idx[gi].copy_(self.idx_host[gi], non_blocking=True)
-                    self.slots.apply_multi([0, 1], [self.x, self.x], self.y, self.idx[gi])
+                    self.idx[rb, gi].copy_(self.idx_host[rb, gi], non_blocking=True)
+                    self.slots.apply_multi([0, 1], [self.x, self.x], self.y, self.idx[rb, gi])
                 for s in held:
                     lib.lora_release(ctx, s)
                 tokens += int(sel.sum())
-            self.slots.compute.synchronize()       # slot-id buffers are reused next step
+            ev = torch.cuda.Event()
+            ev.record(self.slots.compute)
+            self.step_done[rb] = ev
+            if not self.overlap or k == check_step:
+                ev.synchronize()                    # slot-id buffers are reused next step
             if k == check_step:
                 self.checked = (ids.copy(), slot_tok, [y.clone().cpu() for y in self.y])
             B.lora_tick(ctx)

@@ -83,6 +83,12 @@ struct lora_ctx {
     int small_batch = kFusedMaxTokens;   // batches up to this size take the cluster decode kernel
     int inputs_ready = 0;         // caller: x, slot ids, pools not written by the preceding kernel
     int num_sms = 148;
+    // Per-slot tracking (lora_set_slot_tracking): apply i records ring[i % kRing];
+    // slot_gen[s] is the last apply issued while slot s was in flight.
+    int track = 0;
+    std::vector<cudaEvent_t> ring;
+    std::vector<int64_t> slot_gen;
+    int64_t n_apply = 0;
 
     lora_ctx(int S_, int R_) : table(S_, R_) {}
 };
@@ -90,6 +96,35 @@ struct lora_ctx {
 namespace {
 
 int elem_bytes(int dtype) { return dtype == LORA_DTYPE_F32 ? 4 : 2; }
+
+constexpr int kRing = 64;
+
+// After the launches of one apply: the stream-wide event, and with slot
+// tracking the ring event of this apply for every slot in flight.
+cudaError_t note_apply(lora_ctx *c) {
+    cudaError_t e = cudaEventRecord(c->compute_done, c->compute);
+    if (e != cudaSuccess) return e;
+    c->compute_recorded = true;
+    if (!c->track) return cudaSuccess;
+    e = cudaEventRecord(c->ring[c->n_apply % kRing], c->compute);
+    if (e != cudaSuccess) return e;
+    for (int s = 0; s < c->S; ++s)
+        if (c->table.refs(s) > 0) c->slot_gen[s] = c->n_apply;
+    ++c->n_apply;
+    return cudaSuccess;
+}
+
+// Order the upload stream after every queued apply that may read `slot`:
+// all of them by default; with slot tracking only the last apply issued while
+// the slot was in flight (a ring event reused by a later apply only makes the
+// wait longer, never too short).
+cudaError_t wait_slot_reads(lora_ctx *c, int slot) {
+    if (c->track) {
+        const int64_t g = c->slot_gen[slot];
+        return g >= 0 ? cudaStreamWaitEvent(c->upload, c->ring[g % kRing], 0) : cudaSuccess;
+    }
+    return c->compute_recorded ? cudaStreamWaitEvent(c->upload, c->compute_done, 0) : cudaSuccess;
+}
 
 // Move finished upload timings into upload_seconds (blocking when `wait`).
 int harvest_timings(lora_ctx *c, bool wait) {
@@ -226,6 +261,8 @@ void lora_destroy(lora_ctx *c) {
         for (auto ev : c->slot_ev)
             if (ev) cudaEventDestroy(ev);
         if (c->compute_done) cudaEventDestroy(c->compute_done);
+        for (auto ev : c->ring)
+            if (ev) cudaEventDestroy(ev);
     }
     delete c;
 }
@@ -248,7 +285,7 @@ int lora_load_slot(lora_ctx *c, int slot, const void *const *A_host, const void 
     CUDA_TRY(cudaEventCreate(&tm.start));
     CUDA_TRY(cudaEventCreate(&tm.end));
     // Never overwrite a slot that queued compute work may still read.
-    if (c->compute_recorded) CUDA_TRY(cudaStreamWaitEvent(c->upload, c->compute_done, 0));
+    CUDA_TRY(wait_slot_reads(c, slot));
     CUDA_TRY(cudaEventRecord(tm.start, c->upload));
     uint64_t bytes = 0;
     for (int l = 0; l < c->n_layers; ++l) {
@@ -317,10 +354,7 @@ int fused_apply(lora_ctx *c, int n, const int *layers, const void *const *xs, vo
     fa.hdr = reinterpret_cast<int *>(c->ws + c->lay.hdr);
     fa.early = c->inputs_ready;
     CUDA_TRY(launch_cluster_decode(fa, est_tiles, c->compute, true));
-    if (!capturing(c->compute)) {
-        CUDA_TRY(cudaEventRecord(c->compute_done, c->compute));
-        c->compute_recorded = true;
-    }
+    if (!capturing(c->compute)) CUDA_TRY(note_apply(c));
     return LORA_OK;
 }
 
@@ -438,10 +472,7 @@ int apply_impl(lora_ctx *c, int n, const int *layers, const void *const *xs, voi
     gv.T = T;
     int grid_tiles = est_tiles < c->lay.max_tiles ? est_tiles : c->lay.max_tiles;
     CUDA_TRY(launch_decode(ma, gv, c->dtype, grid_tiles, max_chunks, max_dblocks, c->num_sms, c->compute));
-    if (!capturing(c->compute)) {
-        CUDA_TRY(cudaEventRecord(c->compute_done, c->compute));
-        c->compute_recorded = true;
-    }
+    if (!capturing(c->compute)) CUDA_TRY(note_apply(c));
     return LORA_OK;
 }
 
@@ -524,6 +555,23 @@ int lora_release(lora_ctx *c, int slot) {
     return c->table.release(slot) ? LORA_OK : fail(LORA_ERR_STATE, "slot %d is not in flight", slot);
 }
 
+int lora_set_slot_tracking(lora_ctx *c, int on) {
+    if (!c) return fail(LORA_ERR_ARG, "ctx is NULL");
+    if (!c->device) return fail(LORA_ERR_STATE, "host-only context has no uploads");
+    if (on && c->ring.empty()) {
+        c->ring.assign(kRing, nullptr);
+        for (auto &ev : c->ring) CUDA_TRY(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+    }
+    if (on && !c->track) {
+        // Everything queued so far may read any slot: start from the stream-wide event.
+        CUDA_TRY(cudaEventRecord(c->ring[c->n_apply % kRing], c->compute));
+        c->slot_gen.assign(c->S, c->n_apply);
+        ++c->n_apply;
+    }
+    c->track = on ? 1 : 0;
+    return LORA_OK;
+}
+
 int lora_pin(lora_ctx *c, int slot, int pinned) {
     if (!c) return fail(LORA_ERR_ARG, "ctx is NULL");
     if (slot < 0 || slot >= c->S) return fail(LORA_ERR_ARG, "slot %d out of range", slot);
@@ -566,7 +614,7 @@ int lora_evict_lru(lora_ctx *c, int *evicted_slot, uint64_t *evicted_id) {
         return fail(LORA_ERR_NO_SLOT, "no occupied slot may be evicted (in flight, pinned or cooling)");
     if (c->device && *evicted_slot >= 0) {
         // The slot reads as empty for work queued after this call.
-        if (c->compute_recorded) CUDA_TRY(cudaStreamWaitEvent(c->upload, c->compute_done, 0));
+        CUDA_TRY(wait_slot_reads(c, *evicted_slot));
         CUDA_TRY(launch_set_slot(c->scale_dev, c->rank_dev, *evicted_slot, 0.f, 0, c->upload));
         CUDA_TRY(cudaEventRecord(c->slot_ev[*evicted_slot], c->upload));
         c->slot_pending[*evicted_slot] = 1;

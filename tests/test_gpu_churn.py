@@ -71,3 +71,48 @@ def test_churn_decisions_and_outputs():
         _check_step(r, n_adapters, R, 32.0)
     finally:
         r.close()
+
+
+def test_churn_overlap_tracking_outputs_and_decisions():
+    """Uploads ordered per slot (slot tracking) with the host running ahead of
+    the GPU: the same decisions, and a checked step still matches the oracle."""
+    import torch
+    from rank_adapter_apply_gb300 import build
+    from rank_adapter_apply_gb300.churn import ChurnRunner
+    build.build()
+    n_adapters, S, R, steps = 512, 64, 16, 45
+    trace = wl.churn_trace(1, n_adapters=n_adapters, n_steps=steps, burst_every=15)
+    r = ChurnRunner(n_adapters=n_adapters, max_loras=S, rank=R, overlap=True)
+    try:
+        res = r.run(trace, record=True, check_step=31)
+        exp, sim = _sim_decisions(trace, S, R)
+        assert res.decisions == exp
+        st = res.stats
+        assert st["device_wait_timeouts"] == 0 and st["uploads"] == sim.misses
+        ids, slot_tok, ys = r.checked
+        r.checked = (ids, slot_tok, [y.view(torch.int16).numpy().view(np.uint16) for y in ys])
+        _check_step(r, n_adapters, R, 32.0)
+    finally:
+        r.close()
+
+
+def test_churn_pinned_warm_set_and_keep_score_outputs():
+    """Policies on the GPU path: decisions equal the simulator's replay and the
+    checked step matches the oracle."""
+    import torch
+    from rank_adapter_apply_gb300 import build
+    from rank_adapter_apply_gb300 import churn
+    build.build()
+    n_adapters, S, R, steps = 512, 64, 16, 40
+    trace = wl.churn_trace(2, n_adapters=n_adapters, n_steps=steps, burst_every=20)
+    for kw in ({"pin_top": 16}, {"policy": 1, "weights": (1.0, 1.0, 0.0, 0.0, 0.0)}):
+        r = churn.ChurnRunner(n_adapters=n_adapters, max_loras=S, rank=R, **kw)
+        try:
+            res = r.run(trace, record=True, check_step=25)
+            host = churn.admission_stats(trace, max_loras=S, rank=R, record=True, **kw)
+            assert res.decisions == host["log"]
+            ids, slot_tok, ys = r.checked
+            r.checked = (ids, slot_tok, [y.view(torch.int16).numpy().view(np.uint16) for y in ys])
+            _check_step(r, n_adapters, R, 32.0)
+        finally:
+            r.close()
