@@ -531,7 +531,7 @@ def run_churn(args):
     warm = wl.churn_trace(99, n_steps=max(3, min(args.warmup, 20)))
     pol = {"lru": {}, "pin16": {"pin_top": 16},
            "keep": {"policy": 1, "weights": (1.0, 1.0, 0.0, 0.0, 0.0)}}[args.churn_policy]
-    r = ChurnRunner(overlap=args.churn_overlap, **pol)
+    r = ChurnRunner(overlap=args.churn_overlap, batched_upload=args.churn_upload == "batched", **pol)
     r.run(warm)
     base = r.slots.stats()
     res = r.run(trace)
@@ -546,6 +546,7 @@ def run_churn(args):
             "data": "synthetic (seeded Zipf(1.2) adapter ids over 512 with cold bursts)",
             "config": {"workload": "churn_4096", "max_loras": 64, "host_adapters": 512, "rank": 16,
                        "eviction_policy": args.churn_policy, "upload_overlap": args.churn_overlap,
+                       "upload": args.churn_upload,
                        "tokens_per_step": 256, "timing": "wall clock, host bookkeeping included"},
             "churn": {**d, "thrash_ratio": (d["reloads_after_eviction"] / d["evictions"]) if d["evictions"] else 0.0,
                       "hit_rate": d["hits"] / max(1, d["hits"] + d["misses"]),
@@ -573,6 +574,8 @@ def main():
                     help="sequences in the prefill workload (32 = the full workload)")
     ap.add_argument("--churn-policy", choices=["lru", "pin16", "keep"], default="lru",
                     help="churn: pure LRU, LRU with the 16 most popular adapters pinned, or keep_score")
+    ap.add_argument("--churn-upload", choices=["batched", "copy"], default="batched",
+                    help="churn: one upload kernel per group (default) or copy-engine copies per adapter")
     ap.add_argument("--churn-overlap", action="store_true",
                     help="churn: per-slot upload ordering, host runs ahead of the GPU")
     ap.add_argument("--quick", action="store_true",

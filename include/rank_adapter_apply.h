@@ -200,6 +200,25 @@ int lora_tick(lora_ctx *ctx);
 int lora_set_thrash_window(lora_ctx *ctx, int epochs);
 
 /*
+ * Upload several adapters at once (the CPU-hit tier, L1 of section 冷加载延迟 of
+ * the "Multi-LoRA 适配器缓存生产实战" page; its cost is the adapter_h2d term of
+ * the TTFT decomposition there). slots[n], ranks[n], alphas[n]; A_host and
+ * B_host hold n * n_layers host pointers, adapter-major (entry i * n_layers +
+ * l is layer l of adapter i), each laid out as for lora_load_slot. Adapters
+ * whose buffers are page-locked and device-mapped (cudaHostAlloc, torch
+ * pin_memory) with 16-byte aligned rows (r * bytes_per_param and d_in *
+ * bytes_per_param multiples of 16) are copied by one kernel that reads host
+ * memory directly and also zero-fills the padding and sets scale = alpha / r
+ * and the rank; any other adapter takes the copy-engine path of
+ * lora_load_slot. Same ordering, events and statistics as n calls of
+ * lora_load_slot. Everything is validated before anything is queued
+ * (LORA_ERR_ARG: bad slot, a slot twice, NULL; LORA_ERR_RANK). The host
+ * buffers must stay alive and unchanged until lora_sync_uploads returns.
+ */
+int lora_load_slots(lora_ctx *ctx, int n, const int *slots, const void *const *A_host,
+                    const void *const *B_host, const int *ranks, const float *alphas);
+
+/*
  * Per-slot ordering of uploads (copy/compute overlap; the adapter_h2d term of
  * the TTFT decomposition and the H2D metric of the "Multi-LoRA 适配器缓存生产实战"
  * page, sections 冷加载延迟 and 需要重点监控哪些指标). By default an upload or an

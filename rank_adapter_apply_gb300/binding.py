@@ -33,7 +33,7 @@ EXPORTED = [
     "lora_set_prefill_min_tokens", "lora_set_small_batch_tokens", "lora_set_inputs_ready", "lora_sync_uploads", "lora_stats", "lora_adapter_bytes",
     "lora_last_error", "lora_apply_static_scratch", "lora_pin", "lora_set_min_residency",
     "lora_set_policy", "lora_set_keep_score_weights", "lora_set_adapter_priority",
-    "lora_set_slot_tracking",
+    "lora_set_slot_tracking", "lora_load_slots",
 ]
 
 
@@ -92,6 +92,7 @@ def load(path: str = LIB_PATH):
         "lora_set_thrash_window": (i32, [vp, i32]),
         "lora_pin": (i32, [vp, i32, i32]),
         "lora_set_slot_tracking": (i32, [vp, i32]),
+        "lora_load_slots": (i32, [vp, i32, P(i32), P(vp), P(vp), P(i32), P(ctypes.c_float)]),
         "lora_set_min_residency": (i32, [vp, i32]),
         "lora_set_policy": (i32, [vp, i32]),
         "lora_set_keep_score_weights": (i32, [vp, P(ctypes.c_double)]),
@@ -158,6 +159,14 @@ def lora_destroy(ctx):
 def lora_load_slot(ctx, slot, A_ptrs, B_ptrs, rank, alpha):
     return check(load().lora_load_slot(ctx, slot, _vp_array(A_ptrs), _vp_array(B_ptrs), rank,
                                        float(alpha)))
+
+
+def lora_load_slots(ctx, slots, A_ptrs, B_ptrs, ranks, alphas):
+    """A_ptrs / B_ptrs: n * n_layers host pointers, adapter-major."""
+    n = len(slots)
+    return check(load().lora_load_slots(ctx, n, _i32_array(list(slots)), _vp_array(A_ptrs),
+                                        _vp_array(B_ptrs), _i32_array(list(ranks)),
+                                        (ctypes.c_float * n)(*[float(a) for a in alphas])))
 
 
 def lora_apply(ctx, layer, x_ptr, y_ptr, idx_ptr, n_tokens):

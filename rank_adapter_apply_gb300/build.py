@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "librank_adapter_apply.so")
 SOURCES = ["lora_abi.cu", "group.cu", "decode.cu", "decode_cluster.cu", "static_scratch.cu",
-           "prefill_tc.cu", "slot_table.cpp"]
+           "prefill_tc.cu", "upload.cu", "slot_table.cpp"]
 HEADERS = ["kernels.cuh", "slot_table.h", "device_util.cuh", "tc_util.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

@@ -105,7 +105,8 @@ class ChurnResult:
 
 class ChurnRunner:
     def __init__(self, n_adapters=512, max_loras=64, rank=16, d=4096, tokens=256, seed=0,
-                 device="cuda:0", alpha=32.0, policy=0, weights=None, pin_top=0, overlap=False):
+                 device="cuda:0", alpha=32.0, policy=0, weights=None, pin_top=0, overlap=False,
+                 batched_upload=True):
         self.dev = torch.device(device)
         self.S, self.R, self.d, self.T = max_loras, rank, d, tokens
         self.alpha = alpha
@@ -125,6 +126,9 @@ class ChurnRunner:
         # overlap: uploads wait only for the applies that used their slot, and
         # the host runs ahead of the GPU (slot-id buffers rotate over 4 steps)
         self.overlap = overlap
+        # batched: one lora_load_slots per group (one kernel reads the host
+        # adapters); otherwise one lora_load_slot (copy engine) per adapter
+        self.batched_upload = batched_upload
         if overlap:
             B.lora_set_slot_tracking(self.slots.ctx, True)
         self.ring = 4 if overlap else 1
@@ -169,14 +173,16 @@ class ChurnRunner:
             order = list(dict.fromkeys(int(a) for a in ids))   # distinct, first appearance
             slot_tok = np.full(self.T, -1, np.int32)
             for gi, group in enumerate(plan_groups(order, self.pinned, self.S - len(self.pinned))):
-                held, where = [], {}
+                held, where, pending = [], {}, []
                 for a in group:
                     st, slot, need, ev = B.lora_assign(ctx, a, self.R)
                     if record:
                         decisions.append((k, a, st, slot, need, ev))
                     if st != 0:
                         raise RuntimeError(f"assign failed for adapter {a}: {st}")
-                    if need:
+                    if need and self.batched_upload:
+                        pending.append((slot, a))
+                    elif need:
                         self.upload(slot, a)
                     if a < self.pin_top and a not in self.pinned:
                         B.check(B.lora_pin(ctx, slot, True))
@@ -184,6 +190,11 @@ class ChurnRunner:
                     lib.lora_acquire(ctx, slot)
                     held.append(slot)
                     where[a] = slot
+                if pending:
+                    self.slots.load_slots([sl for sl, _ in pending],
+                                          [([self.A[l][a] for l in self.layers], [self.B[l][a] for l in self.layers])
+                                           for _, a in pending],
+                                          [self.R] * len(pending), [self.alpha] * len(pending))
                 sel = np.isin(ids, group)
                 idx = np.where(sel, [where.get(int(a), -1) for a in ids], -1).astype(np.int32)
                 slot_tok[sel] = idx[sel]

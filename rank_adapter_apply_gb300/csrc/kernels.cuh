@@ -126,6 +126,30 @@ cudaError_t launch_prefill_tc(const PrefillLayer *layers, int n, int T, int S, i
                               int *hdr, const int4 *ptiles, int grid_tiles, int part_rows, int num_sms,
                               cudaStream_t st);
 
+// Batched slot upload (upload.cu): one kernel reads every adapter of a call
+// from page-locked host memory (device-mapped) into its slot rows.
+constexpr int kMaxUploadSlots = 128;
+constexpr int kMaxUploadEntries = 256;     // adapters x layers per launch
+struct UploadEntry {
+    const void *A_src;      // host, device-mapped: [r][d_in]
+    const void *B_src;      // host, device-mapped: [d_out][r]
+    void *A_dst;            // slot rows of the A pool: [R][d_in]
+    void *B_dst;            // slot rows of the B pool: [d_out][R]
+    int d_in, d_out, r, pad;
+};
+struct UploadArgs {
+    UploadEntry e[kMaxUploadEntries];
+    int unit_start[kMaxUploadEntries];
+    int slots[kMaxUploadSlots];
+    float scale[kMaxUploadSlots];
+    int rank[kMaxUploadSlots];
+    float *scale_dev;
+    int *rank_dev;
+    int n, n_slots, R, esize;
+};
+int upload_units(const UploadEntry &e, int R, int esize);
+cudaError_t launch_upload_slots(const UploadArgs &a, int total_units, cudaStream_t st);
+
 // Record the message returned by lora_last_error() for this thread; returns code.
 int set_last_error(int code, const char *msg);
 

@@ -6,6 +6,7 @@
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -311,6 +312,100 @@ int lora_load_slot(lora_ctx *c, int slot, const void *const *A_host, const void 
     c->timing.push_back(tm);
     c->uploads += 1;
     c->upload_bytes += bytes;
+    if (c->timing.size() > 256) harvest_timings(c, false);
+    return LORA_OK;
+}
+
+int lora_load_slots(lora_ctx *c, int n, const int *slots, const void *const *A_host,
+                    const void *const *B_host, const int *ranks, const float *alphas) {
+    if (!c) return fail(LORA_ERR_ARG, "ctx is NULL");
+    if (!c->device) return fail(LORA_ERR_STATE, "host-only context has no slot pools");
+    if (n < 0) return fail(LORA_ERR_ARG, "n must be >= 0");
+    if (n == 0) return LORA_OK;
+    if (!slots || !A_host || !B_host || !ranks || !alphas) return fail(LORA_ERR_ARG, "NULL argument");
+    const int L = c->n_layers;
+    const size_t e = elem_bytes(c->dtype);
+    // Validate everything before anything is queued.
+    std::vector<char> seen(c->S, 0);
+    for (int i = 0; i < n; ++i) {
+        if (slots[i] < 0 || slots[i] >= c->S) return fail(LORA_ERR_ARG, "slot %d out of range", slots[i]);
+        if (seen[slots[i]]) return fail(LORA_ERR_ARG, "slot %d appears twice", slots[i]);
+        seen[slots[i]] = 1;
+        if (ranks[i] < 1 || ranks[i] > c->R)
+            return fail(LORA_ERR_RANK, "LoRA rank %d exceeds maximum %d (or is < 1)", ranks[i], c->R);
+        if (!std::isfinite(alphas[i])) return fail(LORA_ERR_ARG, "alpha %d is not finite", i);
+        for (int l = 0; l < L; ++l)
+            if (!A_host[(size_t)i * L + l] || !B_host[(size_t)i * L + l])
+                return fail(LORA_ERR_ARG, "adapter %d layer %d weights are NULL", i, l);
+    }
+    // Adapters the kernel can read: device-mapped host pointers, 16-byte
+    // aligned rows. The others take the copy-engine path of lora_load_slot.
+    std::vector<int> direct, copies;
+    for (int i = 0; i < n; ++i) {
+        bool ok = ((size_t)ranks[i] * e) % 16 == 0;
+        for (int l = 0; l < L && ok; ++l) {
+            const void *p[2] = {A_host[(size_t)i * L + l], B_host[(size_t)i * L + l]};
+            for (int q = 0; q < 2 && ok; ++q) {
+                void *dp = nullptr;
+                ok = cudaHostGetDevicePointer(&dp, const_cast<void *>(p[q]), 0) == cudaSuccess && dp == p[q] &&
+                     reinterpret_cast<uintptr_t>(p[q]) % 16 == 0;
+            }
+            ok = ok && ((size_t)c->layers[l].d_in * e) % 16 == 0;
+        }
+        cudaGetLastError();                    // clear a lookup failure of an unmapped pointer
+        (ok ? direct : copies).push_back(i);
+    }
+    for (int i : copies) {
+        int rc = lora_load_slot(c, slots[i], A_host + (size_t)i * L, B_host + (size_t)i * L, ranks[i], alphas[i]);
+        if (rc != LORA_OK) return rc;
+    }
+    const int per_launch = std::min(kMaxUploadSlots, kMaxUploadEntries / (L > 0 ? L : 1));
+    for (size_t b0 = 0; b0 < direct.size(); b0 += per_launch) {
+        const size_t b1 = std::min(direct.size(), b0 + (size_t)per_launch);
+        UploadArgs ua{};
+        ua.R = c->R;
+        ua.esize = (int)e;
+        ua.scale_dev = c->scale_dev;
+        ua.rank_dev = c->rank_dev;
+        int units = 0;
+        uint64_t bytes = 0;
+        for (size_t k = b0; k < b1; ++k) {
+            const int i = direct[k], s = slots[i];
+            CUDA_TRY(wait_slot_reads(c, s));
+            for (int l = 0; l < L; ++l) {
+                const lora_layer_desc &D = c->layers[l];
+                UploadEntry &u = ua.e[ua.n];
+                u.A_src = A_host[(size_t)i * L + l];
+                u.B_src = B_host[(size_t)i * L + l];
+                u.A_dst = static_cast<char *>(D.A_pool) + (size_t)s * c->R * D.d_in * e;
+                u.B_dst = static_cast<char *>(D.B_pool) + (size_t)s * D.d_out * c->R * e;
+                u.d_in = D.d_in;
+                u.d_out = D.d_out;
+                u.r = ranks[i];
+                ua.unit_start[ua.n] = units;
+                units += upload_units(u, c->R, (int)e);
+                bytes += ((uint64_t)D.d_in + D.d_out) * ranks[i] * e;
+                ++ua.n;
+            }
+            ua.slots[ua.n_slots] = s;
+            ua.scale[ua.n_slots] = alphas[i] / (float)ranks[i];
+            ua.rank[ua.n_slots] = ranks[i];
+            ++ua.n_slots;
+        }
+        UploadTiming tm{};
+        CUDA_TRY(cudaEventCreate(&tm.start));
+        CUDA_TRY(cudaEventCreate(&tm.end));
+        CUDA_TRY(cudaEventRecord(tm.start, c->upload));
+        CUDA_TRY(launch_upload_slots(ua, units, c->upload));
+        CUDA_TRY(cudaEventRecord(tm.end, c->upload));
+        for (int k = 0; k < ua.n_slots; ++k) {
+            CUDA_TRY(cudaEventRecord(c->slot_ev[ua.slots[k]], c->upload));
+            c->slot_pending[ua.slots[k]] = 1;
+        }
+        c->timing.push_back(tm);
+        c->uploads += (uint64_t)ua.n_slots;
+        c->upload_bytes += bytes;
+    }
     if (c->timing.size() > 256) harvest_timings(c, false);
     return LORA_OK;
 }

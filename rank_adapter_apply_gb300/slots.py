@@ -54,6 +54,17 @@ class LoraSlots:
         B.lora_load_slot(self.ctx, slot, [a.data_ptr() for a in A_host],
                          [b.data_ptr() for b in B_host], rank, alpha)
 
+    def load_slots(self, slots, adapters, ranks, alphas):
+        """Several adapters in one call: adapters[i] = (A_host list, B_host list)
+        per layer, as for load_slot."""
+        self._keep = getattr(self, "_keep", {})
+        A_ptrs, B_ptrs = [], []
+        for s, (A_host, B_host) in zip(slots, adapters):
+            self._keep[s] = (A_host, B_host)
+            A_ptrs += [a.data_ptr() for a in A_host]
+            B_ptrs += [b.data_ptr() for b in B_host]
+        B.lora_load_slots(self.ctx, slots, A_ptrs, B_ptrs, ranks, alphas)
+
     def assign(self, adapter_id, rank):
         return B.lora_assign(self.ctx, adapter_id, rank)
 

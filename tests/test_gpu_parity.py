@@ -236,3 +236,55 @@ def test_prefill_batch_shorter_than_a_tile(T, run):
     out, st = _run(w, small_batch_tokens=0)
     check_layer(w, "l0", out["l0"])
     assert st["device_wait_timeouts"] == 0
+
+
+@pytest.mark.parametrize("dtype", [wl.DTYPE_BF16, wl.DTYPE_F32])
+def test_batched_upload_matches_oracle(dtype):
+    """lora_load_slots: adapters of several ranks (zero padding up to R) in one
+    call, pinned buffers read by the upload kernel plus one pageable adapter on
+    the copy-engine path; then the delta equals the oracle's, and padding rows
+    of a slot that held a larger rank before are zero again."""
+    import torch
+    from rank_adapter_apply_gb300.harness import to_torch, from_torch
+    from rank_adapter_apply_gb300.slots import LoraSlots
+    rng = np.random.default_rng(11)
+    T, d_in, d_out, S, R = 96, 512, 384, 5, 32
+    ranks = [32, 8, 16, 24, 32]
+    layers = [wl.Layer("l0", d_in, d_out, "x")]
+    ads = [wl._adapter(rng, layers, r, dtype) for r in ranks]
+    idx = rng.integers(-1, S, size=T).astype(np.int32)
+    x = wl._mat(rng, (T, d_in), "normal", 1.0, dtype)
+    y = wl._mat(rng, (T, d_out), "normal", 1.0, dtype)
+    w = wl.Workload("custom", dtype, S, R, layers, idx, {"x": x}, {"l0": y}, ads,
+                    np.array(ranks, np.int32), 2.0 * np.array(ranks, np.float64))
+    tdt = torch.bfloat16 if dtype == wl.DTYPE_BF16 else torch.float32
+    sl = LoraSlots([(d_in, d_out)], S, R, T, dtype=tdt, device="cuda:0")
+    try:
+        # slot 1 first holds a rank-32 adapter, so its padding must be cleared later
+        big = wl._adapter(rng, layers, 32, dtype)
+        sl.load_slot(1, [to_torch(big["l0"][0], dtype).pin_memory()],
+                     [to_torch(big["l0"][1], dtype).pin_memory()], 32, 64.0)
+        sl.sync_uploads()
+        host = []
+        for s in range(S):
+            A = to_torch(ads[s]["l0"][0], dtype)
+            Bm = to_torch(ads[s]["l0"][1], dtype)
+            if s != 3:                                   # slot 3: pageable, copy-engine path
+                A, Bm = A.pin_memory(), Bm.pin_memory()
+            host.append(([A], [Bm]))
+        sl.load_slots(list(range(S)), host, ranks, [2.0 * r for r in ranks])
+        sl.sync_uploads()
+        st = sl.stats()
+        assert st["uploads"] == S + 1
+        assert st["upload_bytes"] == sum((d_in + d_out) * r for r in [32] + ranks) * (2 if dtype == wl.DTYPE_BF16 else 4)
+        xd = to_torch(x, dtype).to("cuda:0")
+        yd = to_torch(y, dtype).to("cuda:0")
+        sl.apply(0, xd, yd, torch.from_numpy(idx).to("cuda:0"))
+        torch.cuda.synchronize()
+        check_layer(w, "l0", from_torch(yd))
+        A_pool = from_torch(sl.A[0])
+        B_pool = from_torch(sl.B[0])
+        assert not A_pool[1, 8:].any()                   # rank 8 now: rows 8..31 zero again
+        assert not B_pool[1, :, 8:].any()
+    finally:
+        sl.close()
