@@ -422,24 +422,22 @@ def run_e2e(args, w, batches, d0, stream, dev, world):
     host_y = [B._vp_array([t.data_ptr() for t in hy[i]]) for i in range(nh)]
     slot_of = np.full(N_SLOTS, -1, np.int32)
     distinct = [np.unique(h[h >= 0]) for h in hid]
+    act = [int((h >= 0).sum()) for h in hid]
 
     def step(i):
         j = i % nh
-        held = []
-        for a in distinct[j]:
-            rc, slot, need, _ = B.lora_assign(ctx, int(a), RANK)
-            if rc != 0 or need:
-                raise RuntimeError("adapter unexpectedly not resident")
-            lib.lora_acquire(ctx, slot)
-            slot_of[a] = slot
-            held.append(slot)
+        # admission of the batch's adapters in one call (all hits here), then
+        # the slot id of every token from a lookup table
+        rc, done, slots, need, _ = B.lora_assign_batch(ctx, distinct[j], [RANK] * len(distinct[j]))
+        if rc != 0 or need.any():
+            raise RuntimeError("adapter unexpectedly not resident")
+        slot_of[distinct[j]] = slots
         ids = hid[j]
         hidx[j].numpy()[:] = np.where(ids >= 0, slot_of[np.maximum(ids, 0)], -1)
         B.check(lib.lora_apply_multi_host(ctx, 2, lay, host_x[j], host_y[j], hidx[j].data_ptr(),
                                           T_TOKENS, xs_dev, ys_dev, idd.data_ptr()))
-        for s in held:
-            lib.lora_release(ctx, s)
-        return int((ids >= 0).sum())
+        B.check(B.lora_release_batch(ctx, slots))
+        return act[j]
 
     for i in range(max(3, args.warmup)):
         step(i)

@@ -180,6 +180,18 @@ int lora_lookup(lora_ctx *ctx, uint64_t adapter_id, int *slot);
 int lora_assign(lora_ctx *ctx, uint64_t adapter_id, int rank, int *slot,
                 int *needs_load, uint64_t *evicted_id);
 
+/*
+ * n lora_assign calls in order (and, if acquire != 0, lora_acquire on each
+ * resulting slot), for serving loops that admit a batch's adapters at once.
+ * Outputs per entry as for lora_assign. Stops at the first failure and returns
+ * its status; *n_done = entries completed (their effects stay).
+ */
+int lora_assign_batch(lora_ctx *ctx, int n, const uint64_t *adapter_ids, const int *ranks, int acquire,
+                      int *slots, int *needs_load, uint64_t *evicted_ids, int *n_done);
+
+/* lora_release on each of slots[n] in order; stops at the first slot not in flight (LORA_ERR_STATE). */
+int lora_release_batch(lora_ctx *ctx, int n, const int *slots);
+
 /* In-flight reference count of an occupied slot (never evicted while > 0). */
 int lora_acquire(lora_ctx *ctx, int slot);
 int lora_release(lora_ctx *ctx, int slot);

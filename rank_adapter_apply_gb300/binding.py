@@ -33,7 +33,7 @@ EXPORTED = [
     "lora_set_prefill_min_tokens", "lora_set_small_batch_tokens", "lora_set_inputs_ready", "lora_sync_uploads", "lora_stats", "lora_adapter_bytes",
     "lora_last_error", "lora_apply_static_scratch", "lora_pin", "lora_set_min_residency",
     "lora_set_policy", "lora_set_keep_score_weights", "lora_set_adapter_priority",
-    "lora_set_slot_tracking", "lora_load_slots",
+    "lora_set_slot_tracking", "lora_load_slots", "lora_assign_batch", "lora_release_batch",
 ]
 
 
@@ -92,6 +92,8 @@ def load(path: str = LIB_PATH):
         "lora_set_thrash_window": (i32, [vp, i32]),
         "lora_pin": (i32, [vp, i32, i32]),
         "lora_set_slot_tracking": (i32, [vp, i32]),
+        "lora_assign_batch": (i32, [vp, i32, P(u64), P(i32), i32, P(i32), P(i32), P(u64), P(i32)]),
+        "lora_release_batch": (i32, [vp, i32, P(i32)]),
         "lora_load_slots": (i32, [vp, i32, P(i32), P(vp), P(vp), P(i32), P(ctypes.c_float)]),
         "lora_set_min_residency": (i32, [vp, i32]),
         "lora_set_policy": (i32, [vp, i32]),
@@ -197,6 +199,31 @@ def lora_assign(ctx, adapter_id, rank):
     rc = load().lora_assign(ctx, adapter_id, rank, ctypes.byref(s), ctypes.byref(nl),
                             ctypes.byref(ev))
     return rc, s.value, nl.value, (-1 if ev.value == NO_ID else ev.value)
+
+
+def lora_assign_batch(ctx, ids, ranks, acquire=True):
+    """Returns (status, n_done, slots, needs_load, evicted ids (-1: none)) as numpy arrays."""
+    import numpy as np
+    n = len(ids)
+    ida = np.ascontiguousarray(np.asarray(ids, dtype=np.uint64))
+    rka = np.ascontiguousarray(np.asarray(ranks, dtype=np.int32))
+    slots = np.full(n, -1, np.int32)
+    need = np.zeros(n, np.int32)
+    ev = np.zeros(n, np.uint64)
+    done = ctypes.c_int(0)
+    P = ctypes.POINTER
+    rc = load().lora_assign_batch(ctx, n, ida.ctypes.data_as(P(ctypes.c_uint64)),
+                                  rka.ctypes.data_as(P(ctypes.c_int)), 1 if acquire else 0,
+                                  slots.ctypes.data_as(P(ctypes.c_int)), need.ctypes.data_as(P(ctypes.c_int)),
+                                  ev.ctypes.data_as(P(ctypes.c_uint64)), ctypes.byref(done))
+    evi = np.where(ev == np.uint64(NO_ID), -1, ev.astype(np.int64))
+    return rc, done.value, slots, need, evi
+
+
+def lora_release_batch(ctx, slots):
+    import numpy as np
+    sa = np.ascontiguousarray(np.asarray(slots, dtype=np.int32))
+    return load().lora_release_batch(ctx, len(sa), sa.ctypes.data_as(ctypes.POINTER(ctypes.c_int)))
 
 
 def lora_acquire(ctx, slot):

@@ -109,6 +109,7 @@ class ChurnRunner:
                  batched_upload=True):
         self.dev = torch.device(device)
         self.S, self.R, self.d, self.T = max_loras, rank, d, tokens
+        self.n_adapters = n_adapters
         self.alpha = alpha
         host = wl.churn_adapters(seed, n_adapters, d, rank)
         # pinned host adapter store: per adapter, per layer A [r, d], B [d, r]
@@ -159,7 +160,6 @@ class ChurnRunner:
         decisions = []
         tokens = 0
         ctx = self.slots.ctx
-        lib = B.load()
         torch.cuda.synchronize(self.dev)
         t0 = time.perf_counter()
         for k, ids in enumerate(trace.steps):
@@ -170,40 +170,41 @@ class ChurnRunner:
                 with torch.cuda.stream(self.slots.compute):
                     for y, y0 in zip(self.y, self.y0):
                         y.copy_(y0)
-            order = list(dict.fromkeys(int(a) for a in ids))   # distinct, first appearance
+            _, first = np.unique(ids, return_index=True)        # distinct, first appearance
+            order = [int(a) for a in ids[np.sort(first)]]
             slot_tok = np.full(self.T, -1, np.int32)
             for gi, group in enumerate(plan_groups(order, self.pinned, self.S - len(self.pinned))):
-                held, where, pending = [], {}, []
-                for a in group:
-                    st, slot, need, ev = B.lora_assign(ctx, a, self.R)
-                    if record:
-                        decisions.append((k, a, st, slot, need, ev))
-                    if st != 0:
-                        raise RuntimeError(f"assign failed for adapter {a}: {st}")
-                    if need and self.batched_upload:
-                        pending.append((slot, a))
-                    elif need:
-                        self.upload(slot, a)
+                # admit the group in one call: assign (hit: touch; miss: free
+                # slot or policy victim) and take an in-flight reference
+                rc, done, slots, need, evicted = B.lora_assign_batch(ctx, group, [self.R] * len(group))
+                if rc != 0:
+                    raise RuntimeError(f"assign failed for adapter {group[done]}: {rc}")
+                if record:
+                    decisions += [(k, a, 0, int(sl), int(nd), int(ev_))
+                                  for a, sl, nd, ev_ in zip(group, slots, need, evicted)]
+                pending = [(int(sl), a) for a, sl, nd in zip(group, slots, need) if nd]
+                for a, sl in zip(group, slots):
                     if a < self.pin_top and a not in self.pinned:
-                        B.check(B.lora_pin(ctx, slot, True))
-                        self.pinned[a] = slot
-                    lib.lora_acquire(ctx, slot)
-                    held.append(slot)
-                    where[a] = slot
-                if pending:
+                        B.check(B.lora_pin(ctx, int(sl), True))
+                        self.pinned[a] = int(sl)
+                if pending and self.batched_upload:
                     self.slots.load_slots([sl for sl, _ in pending],
                                           [([self.A[l][a] for l in self.layers], [self.B[l][a] for l in self.layers])
                                            for _, a in pending],
                                           [self.R] * len(pending), [self.alpha] * len(pending))
-                sel = np.isin(ids, group)
-                idx = np.where(sel, [where.get(int(a), -1) for a in ids], -1).astype(np.int32)
+                else:
+                    for sl, a in pending:
+                        self.upload(sl, a)
+                slot_of = np.full(self.n_adapters, -1, np.int32)
+                slot_of[np.asarray(group)] = slots
+                idx = slot_of[ids]
+                sel = idx >= 0
                 slot_tok[sel] = idx[sel]
                 self.idx_host[rb, gi].numpy()[:] = idx
                 with torch.cuda.stream(self.slots.compute):
                     self.idx[rb, gi].copy_(self.idx_host[rb, gi], non_blocking=True)
                     self.slots.apply_multi([0, 1], [self.x, self.x], self.y, self.idx[rb, gi])
-                for s in held:
-                    lib.lora_release(ctx, s)
+                B.check(B.lora_release_batch(ctx, slots))
                 tokens += int(sel.sum())
             ev = torch.cuda.Event()
             ev.record(self.slots.compute)

@@ -640,6 +640,30 @@ int lora_assign(lora_ctx *c, uint64_t id, int rank, int *slot, int *needs_load, 
     }
 }
 
+int lora_assign_batch(lora_ctx *c, int n, const uint64_t *ids, const int *ranks, int acquire, int *slots,
+                      int *needs_load, uint64_t *evicted_ids, int *n_done) {
+    if (!c || n_done == nullptr) return fail(LORA_ERR_ARG, "NULL argument");
+    *n_done = 0;
+    if (n < 0) return fail(LORA_ERR_ARG, "n must be >= 0");
+    if (n > 0 && (!ids || !ranks || !slots || !needs_load || !evicted_ids))
+        return fail(LORA_ERR_ARG, "NULL argument");
+    for (int i = 0; i < n; ++i) {
+        int rc = lora_assign(c, ids[i], ranks[i], &slots[i], &needs_load[i], &evicted_ids[i]);
+        if (rc != LORA_OK) return rc;
+        if (acquire) c->table.acquire(slots[i]);
+        *n_done = i + 1;
+    }
+    return LORA_OK;
+}
+
+int lora_release_batch(lora_ctx *c, int n, const int *slots) {
+    if (!c) return fail(LORA_ERR_ARG, "ctx is NULL");
+    if (n < 0 || (n > 0 && !slots)) return fail(LORA_ERR_ARG, "bad arguments");
+    for (int i = 0; i < n; ++i)
+        if (!c->table.release(slots[i])) return fail(LORA_ERR_STATE, "slot %d is not in flight", slots[i]);
+    return LORA_OK;
+}
+
 int lora_acquire(lora_ctx *c, int slot) {
     if (!c) return fail(LORA_ERR_ARG, "ctx is NULL");
     return c->table.acquire(slot) ? LORA_OK : fail(LORA_ERR_STATE, "slot %d is not occupied", slot);

@@ -233,3 +233,34 @@ def test_pinned_burst_through_abi(lib):
         assert sim.reloads == 2                      # only the unpinned 2 and 3
     finally:
         B.lora_destroy(ctx)
+
+
+def test_assign_batch_equals_sequential_calls(lib):
+    """lora_assign_batch / lora_release_batch take the decisions of the
+    equivalent lora_assign + lora_acquire / lora_release sequence."""
+    from oracle.lru_sim import LruSlotSim
+    rng = np.random.default_rng(5)
+    S, R = 6, 16
+    ctx = _host_ctx(S, R)
+    sim = LruSlotSim(S, R)
+    try:
+        for step in range(120):
+            ids = list(dict.fromkeys(int(a) for a in rng.integers(0, 20, size=8)))[:S]
+            ranks = [int(rng.choice([8, 16])) for _ in ids]
+            rc, done, slots, need, ev = B.lora_assign_batch(ctx, ids, ranks)
+            assert rc == 0 and done == len(ids)
+            for a, r, s_, n_, e_ in zip(ids, ranks, slots, need, ev):
+                assert sim.assign(a, r) == (0, int(s_), int(n_), int(e_))
+                assert sim.acquire(int(s_)) == 0
+            assert B.lora_release_batch(ctx, slots) == 0
+            for s_ in slots:
+                sim.release(int(s_))
+            B.lora_tick(ctx)
+            sim.tick()
+        # a failing entry stops the batch: rank too large after two good ones
+        rc, done, slots, need, ev = B.lora_assign_batch(ctx, [1001, 1002, 1003], [8, 8, 99])
+        assert rc == B.LORA_ERR_RANK and done == 2
+        assert B.lora_release_batch(ctx, slots[:2]) == 0
+        assert B.lora_release_batch(ctx, slots[:1]) == B.LORA_ERR_STATE
+    finally:
+        B.lora_destroy(ctx)
