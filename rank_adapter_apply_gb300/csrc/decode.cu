@@ -157,6 +157,21 @@ __device__ __forceinline__ void expand_bf16_tile(const LayerArgs &L, const Group
     const int tok0 = gq < cnt ? g.perm[p0 + gq] : -1;
     const int tok1 = gq + 8 < cnt ? g.perm[p0 + 8 + gq] : -1;
 
+    // This block's B rows (the slot's first 16 * nkb ranks) go to shared memory
+    // in one burst of 16-byte cp.async: row P of the block at bs + 64 P, chunk
+    // c of the row at chunk c ^ (P & 7) so the fragment reads spread over banks.
+    __shared__ __align__(16) uint16_t bs[kExpandCols * 64];
+    const uint16_t *Bs = static_cast<const uint16_t *>(L.B) + (size_t)s * d_out * R;
+    const int c0 = dblock * kExpandCols;
+    {
+        const int cpr = 2 * nkb;
+        for (int i = threadIdx.x; i < kExpandCols * cpr; i += kThreads) {
+            const int P = i / cpr, ch = i - P * cpr;
+            if (c0 + P < d_out) cp_async16(bs + P * 64 + ((ch ^ (P & 7)) << 3), Bs + (size_t)(c0 + P) * R + ch * 8);
+        }
+        cp_async_commit();
+    }
+
     // A fragments of V (rows = tokens gq, gq+8; k = 4tq..4tq+3 of each 16-rank block).
     uint32_t ahi[4][4], alo[4][4];
 #pragma unroll
@@ -185,7 +200,6 @@ __device__ __forceinline__ void expand_bf16_tile(const LayerArgs &L, const Group
         alo[kb][3] = pack_bf16(f1[2] - h1[2], f1[3] - h1[3]);
     }
 
-    const uint16_t *Bs = static_cast<const uint16_t *>(L.B) + (size_t)s * d_out * R;
     uint16_t *y = static_cast<uint16_t *>(L.y);
     const int vec = L.vec;
 
@@ -204,6 +218,9 @@ __device__ __forceinline__ void expand_bf16_tile(const LayerArgs &L, const Group
         }
     }
 
+    cp_async_wait_all();                 // this thread's B chunks have landed
+    __syncthreads();                     // and every other thread's
+
 #pragma unroll
     for (int grp = 0; grp < 2; ++grp) {
         const int c = dblock * kExpandCols + warp * 64 + grp * 32;
@@ -218,8 +235,10 @@ __device__ __forceinline__ void expand_bf16_tile(const LayerArgs &L, const Group
                 if (kb < nkb) {
                     const int k = kb * 16 + 4 * tq;
                     uint2 bb = make_uint2(0, 0);
-                    if (P < d_out && k < R)
-                        bb = __ldg(reinterpret_cast<const uint2 *>(Bs + (size_t)P * R + k));
+                    if (P < d_out && k < R) {
+                        const int Pl = P - c0;
+                        bb = *reinterpret_cast<const uint2 *>(bs + Pl * 64 + ((((k >> 3) ^ (Pl & 7))) << 3) + (k & 7));
+                    }
                     if (k + 4 > r) {
                         if (k + 0 >= r) bb.x &= 0xffff0000u;
                         if (k + 1 >= r) bb.x &= 0x0000ffffu;
@@ -349,6 +368,7 @@ expand_bf16_kernel(MultiArgs ma, GroupView g, int max_dblocks) {
         const LayerArgs &L = ma.l[l];
         if (db * kExpandCols >= L.d_out) continue;
         expand_bf16_tile(L, g, db, t);
+        __syncthreads();                     // the staged B rows are free for the next item
     }
 }
 

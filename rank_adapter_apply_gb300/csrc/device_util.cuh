@@ -154,6 +154,9 @@ __device__ __forceinline__ void cp_async16(void *dst_smem, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
 }
 
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 // Arrive on `bar` once every cp.async this thread issued so far has landed
 // (the barrier's expected count includes this arrival).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {

@@ -534,12 +534,12 @@ int apply_impl(lora_ctx *c, int n, const int *layers, const void *const *xs, voi
         a.v = reinterpret_cast<float *>(c->ws + c->lay.v) + (size_t)i * c->lay.max_tokens * c->R;
         a.part = reinterpret_cast<float *>(c->ws + c->lay.part) + (size_t)i * c->lay.part_rows * c->R;
         a.counters = reinterpret_cast<int *>(c->ws + c->lay.counters) + (size_t)i * c->lay.max_tiles;
-        // Split d_in into chunks of ~512 columns so that a tile's shrink is
+        // Split d_in into chunks of ~256 columns so that a tile's shrink is
         // spread over many CTAs (the host cannot tell how many decode tiles a
-        // batch has), as long as the fp32 partials stay under 1/8 of the x
-        // bytes they replace.
-        int chunks = (L.d_in + 511) / 512;
-        const int by_bytes = (int)((size_t)L.d_in * e / (32 * (size_t)c->R));
+        // batch has), as long as a tile's fp32 partials (written and read,
+        // 16 tokens x R) stay under 1/8 of the x and A bytes the tile reads.
+        int chunks = (L.d_in + 255) / 256;
+        const int by_bytes = (int)((size_t)(kTileTokens + c->R) * L.d_in * e / (8 * 2 * kTileTokens * 4 * (size_t)c->R));
         if (chunks > by_bytes) chunks = by_bytes;
         if (chunks > kMaxChunks) chunks = kMaxChunks;
         if (chunks > c->lay.part_rows / T) chunks = c->lay.part_rows / T;
