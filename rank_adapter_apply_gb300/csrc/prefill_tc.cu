@@ -250,7 +250,7 @@ struct ExpandArgs {
     const int4 *ptiles;
     int *hdr;
     const float *scale;
-    int n, T, stages, sum_ncb;
+    int n, T, stages, sum_ncb, S;
 };
 
 struct Item {
@@ -280,6 +280,7 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ uint64_t full[kMaxStages], empty[kMaxStages];
     __shared__ uint64_t acc_full[kAcc], acc_empty[kAcc], v_full[2], v_empty[2], drained;
+    __shared__ float sscale[kMaxSlots];
     __shared__ uint32_t tmem_base;
     __shared__ int error;
 
@@ -320,6 +321,7 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
             tc::prefetch_tensormap(&a.mb[l]);
         }
     }
+    for (int x = tid; x < a.S; x += kExpandThreads) sscale[x] = a.scale[x];
     if (warp == 1) {
         tc::tmem_alloc(&tmem_base, kNB * kAcc);
         tc::tmem_relinquish();
@@ -478,11 +480,18 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
         const int i = q * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
         int j = 0, pend = -1;
+        // item metadata one item ahead, so its global load leaves the chain
+        Item it = item_at(a, k0, np);
+        int4 pt = a.ptiles[it.p];
         for (int k = k0; k < k1; ++k) {
-            const Item it = item_at(a, k, np);
-            const int4 pt = a.ptiles[it.p];
+            Item nit = it;
+            int4 npt = pt;
+            if (k + 1 < k1) {
+                nit = item_at(a, k + 1, np);
+                npt = a.ptiles[nit.p];
+            }
             const int row0 = pt.y, rows = pt.z;
-            const float scale = a.scale[pt.x];
+            const float scale = sscale[pt.x];
             const int nb = n_blocks(a, it), d_out = a.d_out[it.l];
             for (int b = 0; b < nb; ++b) {
                 const int st = j % stages, ac = j % kAcc;
@@ -544,6 +553,8 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
                 }
                 ++j;
             }
+            it = nit;
+            pt = npt;
         }
         if (lane == 0) {
             tc::bulk_wait_group_all();
@@ -736,6 +747,7 @@ cudaError_t launch_prefill_tc(const PrefillLayer *L, int n, int T, int S, int R,
     ea.ptiles = ptiles;
     ea.hdr = hdr;
     ea.scale = scale;
+    ea.S = S;
     ea.T = T;
     long long items = (long long)grid_tiles * ea.sum_ncb;
     const int expand_grid = (int)(items < num_sms ? items : num_sms);
