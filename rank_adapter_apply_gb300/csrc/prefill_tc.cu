@@ -505,12 +505,7 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
                 if (ok) {
                     tc::fence_after_sync();
                     uint32_t d[64];
-                    {
-                        uint32_t (&d0)[32] = *reinterpret_cast<uint32_t (*)[32]>(d);
-                        uint32_t (&d1)[32] = *reinterpret_cast<uint32_t (*)[32]>(d + 32);
-                        tc::tmem_ld32_sync(tmem + lane_addr + (uint32_t)kNB * ac + 64u * h, d0);
-                        tc::tmem_ld32_sync(tmem + lane_addr + (uint32_t)kNB * ac + 64u * h + 32, d1);
-                    }
+                    tc::tmem_ld64_sync(tmem + lane_addr + (uint32_t)kNB * ac + 64u * h, d);
                     tc::fence_before_sync();
                     tc::mbar_arrive(&acc_empty[ac]);
                     if (live) {
