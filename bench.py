@@ -156,6 +156,21 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
+def reduce_over_ranks(ms: float, tokens: int, device=None):
+    """Job-wide figures of a weak-scaled run (one replica per rank, no data
+    exchange between ranks): the slowest rank's time and every rank's tokens.
+    Returns (ms, tokens) unchanged when no process group is running."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms, tokens
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    n = torch.tensor([float(tokens)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(round(n.item()))
+
+
 def make_batches(n_sets: int, seed0: int = 0):
     """Set 0 is the decode workload itself; sets 1.. draw new x, base outputs
     and slot ids with the same recipe (base output drawn directly)."""
@@ -344,16 +359,13 @@ def run_ours(args):
         dist.barrier()
     ms = ev0.elapsed_time(ev1)
     clock_rows = sampler.stop()
-    if world > 1:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
 
     order = [i % len(sets) for i in range(full * len(sets))] + list(range(rem))
     tokens = sum(sets[i].t_act for i in order)
     bytes_ = sum(sets[i].bytes for i in order)
     flops = sum(sets[i].flops for i in order)
-    value = tokens * world / (ms * 1e-3)
+    ms, job_tokens = reduce_over_ranks(ms, tokens, dev)
+    value = job_tokens / (ms * 1e-3)
     hbm, peak_kind = peaks()
     achieved = bytes_ / (ms * 1e-3) / 1e9
 
@@ -452,9 +464,11 @@ def run_e2e(args, w, batches, d0, stream, dev, world):
         toks += step(i)
     stream.synchronize()
     el = time.perf_counter() - t0
+    el_ms, job_toks = reduce_over_ranks(el * 1e3, toks, dev)
+    el = el_ms * 1e-3
     h2d = T_TOKENS * D * 2 + 2 * T_TOKENS * D * 2 + T_TOKENS * 4
     d2h = 2 * T_TOKENS * D * 2
-    return {"value": toks * world / el, "unit": UNIT, "h2d_bytes_per_step": h2d,
+    return {"value": job_toks / el, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": k,
             "timing": "wall clock, host admission + H2D + apply + D2H per step"}
 
