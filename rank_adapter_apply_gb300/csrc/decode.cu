@@ -76,7 +76,7 @@ __device__ void finish_split(const LayerArgs &L, const GroupView &g, int tile_i,
 __device__ __forceinline__ void shrink_bf16_tile(const LayerArgs &L, const GroupView &g, int chunk, int tile_i) {
     const int4 tile = g.tiles[tile_i];
     const int s = tile.x, p0 = tile.y, cnt = tile.z;
-    const int r = g.rank[s];
+    const int r = tile.w;                      // the slot's rank, from the grouping
     const int nmb = (r + 15) >> 4;
     const int R = g.R, d_in = L.d_in;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
@@ -148,7 +148,7 @@ __device__ __forceinline__ void expand_bf16_tile(const LayerArgs &L, const Group
     const int d_out = L.d_out;
     const int4 tile = g.tiles[tile_i];
     const int s = tile.x, p0 = tile.y, cnt = tile.z;
-    const int r = g.rank[s];
+    const int r = tile.w;                      // the slot's rank, from the grouping
     const int nkb = (r + 15) >> 4;
     const float scale = g.scale[s];
     const int R = g.R;
@@ -292,7 +292,7 @@ __device__ __forceinline__ void expand_bf16_tile(const LayerArgs &L, const Group
 __device__ __forceinline__ void shrink_f32_tile(const LayerArgs &L, const GroupView &g, int chunk, int tile_i) {
     const int4 tile = g.tiles[tile_i];
     const int s = tile.x, p0 = tile.y, cnt = tile.z;
-    const int r = g.rank[s];
+    const int r = tile.w;                      // the slot's rank, from the grouping
     const int R = g.R, d_in = L.d_in;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float *x = static_cast<const float *>(L.x);
@@ -319,7 +319,7 @@ __device__ __forceinline__ void expand_f32_tile(const LayerArgs &L, const GroupV
     const int d_out = L.d_out;
     const int4 tile = g.tiles[tile_i];
     const int s = tile.x, p0 = tile.y, cnt = tile.z;
-    const int r = g.rank[s];
+    const int r = tile.w;                      // the slot's rank, from the grouping
     const float scale = g.scale[s];
     const int R = g.R;
     extern __shared__ float sv[];                     // [kTileTokens][r]

@@ -4,7 +4,7 @@
 //    kPrefillRows rows (slot, first row, rows);
 //  * decode tiles: every other adapter token, grouped by slot (counting sort
 //    into `perm`, one run at a time), cut into tiles of kTileTokens (slot, perm
-//    offset, count).
+//    offset, count, the slot's rank).
 // Each thread owns a contiguous block of tokens and then a contiguous block of
 // runs, so the whole batch takes a handful of block-wide scans. The order of
 // tokens inside one slot's decode list is not fixed (runs claim their places
@@ -137,7 +137,7 @@ group_tokens_kernel(const int32_t *__restrict__ idx, int T, const int *__restric
     const int tpos = block_excl_scan(nt, sm, &n_tiles);
     for (int i = 0; i < nt; ++i) {
         const int c = cnt - i * kTileTokens;
-        tiles[tpos + i] = make_int4(tid, off + i * kTileTokens, c < kTileTokens ? c : kTileTokens, 0);
+        tiles[tpos + i] = make_int4(tid, off + i * kTileTokens, c < kTileTokens ? c : kTileTokens, sm.rank[tid]);
     }
     __syncthreads();
 
