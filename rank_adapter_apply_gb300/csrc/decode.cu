@@ -73,6 +73,35 @@ __device__ void finish_split(const LayerArgs &L, const GroupView &g, int tile_i,
 // 32-column steps. Per warp and step: m16n8k16 with M = 16 ranks (per 16-rank
 // block), N = 8 tokens (two token blocks), K = 16 (two MMAs per 32 columns).
 // ---------------------------------------------------------------------------
+// The column loop of one shrink item for NMB 16-rank blocks, UNROLL steps
+// of 32 columns per warp in flight.
+template <int NMB, int UNROLL>
+__device__ __forceinline__ void shrink_steps(float (&acc)[4][2][4], const uint16_t *xr0, const uint16_t *xr1,
+                                             const uint16_t *As, int tok0, int tok1, int r, int d_in, int c0,
+                                             int c1, int vec) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
+#pragma unroll UNROLL
+    for (int col = c0 + warp * 32; col < c1; col += kWarps * 32) {
+        const int cc = col + 8 * tq;
+        const uint4 xa = load8_bf16(xr0, cc, d_in, tok0 >= 0, vec);
+        const uint4 xb = load8_bf16(xr1, cc, d_in, tok1 >= 0, vec);
+        uint4 a0[NMB], a1[NMB];
+#pragma unroll
+        for (int m = 0; m < NMB; ++m) {
+            const int k0 = m * 16 + gq, k1 = k0 + 8;
+            a0[m] = load8_bf16(As + (size_t)k0 * d_in, cc, d_in, k0 < r, vec);
+            a1[m] = load8_bf16(As + (size_t)k1 * d_in, cc, d_in, k1 < r, vec);
+        }
+#pragma unroll
+        for (int m = 0; m < NMB; ++m) {
+            mma_bf16(acc[m][0], a0[m].x, a1[m].x, a0[m].y, a1[m].y, xa.x, xa.y);
+            mma_bf16(acc[m][0], a0[m].z, a1[m].z, a0[m].w, a1[m].w, xa.z, xa.w);
+            mma_bf16(acc[m][1], a0[m].x, a1[m].x, a0[m].y, a1[m].y, xb.x, xb.y);
+            mma_bf16(acc[m][1], a0[m].z, a1[m].z, a0[m].w, a1[m].w, xb.z, xb.w);
+        }
+    }
+}
+
 __device__ __forceinline__ void shrink_bf16_tile(const LayerArgs &L, const GroupView &g, int chunk, int tile_i) {
     const int4 tile = g.tiles[tile_i];
     const int s = tile.x, p0 = tile.y, cnt = tile.z;
@@ -98,24 +127,11 @@ __device__ __forceinline__ void shrink_bf16_tile(const LayerArgs &L, const Group
 
     const int c0 = chunk * L.chunk_cols;
     const int c1 = min(d_in, c0 + L.chunk_cols);
-#pragma unroll 2
-    for (int col = c0 + warp * 32; col < c1; col += kWarps * 32) {
-        const int cc = col + 8 * tq;
-        const uint4 xa = load8_bf16(xr0, cc, d_in, tok0 >= 0, L.vec);
-        const uint4 xb = load8_bf16(xr1, cc, d_in, tok1 >= 0, L.vec);
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            if (m < nmb) {
-                const int k0 = m * 16 + gq, k1 = k0 + 8;
-                const uint4 a0 = load8_bf16(As + (size_t)k0 * d_in, cc, d_in, k0 < r, L.vec);
-                const uint4 a1 = load8_bf16(As + (size_t)k1 * d_in, cc, d_in, k1 < r, L.vec);
-                mma_bf16(acc[m][0], a0.x, a1.x, a0.y, a1.y, xa.x, xa.y);
-                mma_bf16(acc[m][0], a0.z, a1.z, a0.w, a1.w, xa.z, xa.w);
-                mma_bf16(acc[m][1], a0.x, a1.x, a0.y, a1.y, xb.x, xb.y);
-                mma_bf16(acc[m][1], a0.z, a1.z, a0.w, a1.w, xb.z, xb.w);
-            }
-        }
-    }
+    // The rank-block count is a template argument of the loop, so that no
+    // runtime condition stands between the loads of several steps.
+    if (nmb <= 1) shrink_steps<1, 4>(acc, xr0, xr1, As, tok0, tok1, r, d_in, c0, c1, L.vec);
+    else if (nmb == 2) shrink_steps<2, 2>(acc, xr0, xr1, As, tok0, tok1, r, d_in, c0, c1, L.vec);
+    else shrink_steps<4, 2>(acc, xr0, xr1, As, tok0, tok1, r, d_in, c0, c1, L.vec);
 
     // Cross-warp sum through shared memory.
     __shared__ float red[kWarps][4 * 2 * 4][32];
