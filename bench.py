@@ -522,11 +522,12 @@ def run_big(args, name):
                        "max_loras": w.max_loras, "max_lora_rank": w.max_lora_rank,
                        "l2": f"inputs larger than L2 ({bytes_ / 2**20:.0f} MiB per step)",
                        "timing": "CUDA-graph replay, CUDA events on the launch stream"},
-            "roofline": {"bound": "hbm", "kernel": "whole step: group_tokens, prefill_shrink, prefill_expand, decode shrink + expand (5 launches, every layer)",
+            "roofline": {"bound": "hbm", "kernel": "whole step: group_tokens, prefill_shrink, [prefill_reduce], prefill_expand, decode shrink + expand (every layer)",
                          "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "peak_kind": kind,
                          "traffic": None, "algorithmic_bytes_per_step": bytes_,
                          "tflops": flops * args.steps / (ms * 1e-3) / 1e12},
-            "gpu_launches": 5 * args.steps, "clocks": clocks}
+            # grouping, prefill shrink, [chunk sums at rank 64], prefill expand, decode shrink + expand
+            "gpu_launches": (6 if name == "mixed_ranks_8b" else 5) * args.steps, "clocks": clocks}
     print(json.dumps(line), flush=True)
     dw.close()
     return 0

@@ -122,6 +122,53 @@ struct ShrinkArgs {
     int T, stages, tmem_cols;
 };
 
+// Sum of the d_in chunks of V, in chunk order, left in chunk 0: one CTA per
+// (layer of the call, block of 256 / (R/4) rows of a tile), one 16-byte column
+// of one row per thread.
+struct ReduceArgs {
+    float *part[kMaxLayersPerCall];
+    int nch[kMaxLayersPerCall];
+    const int4 *ptiles;
+    const int *hdr;
+    int T, R;
+};
+
+__global__ void __launch_bounds__(256)
+prefill_reduce_kernel(const __grid_constant__ ReduceArgs a) {
+    const int R4 = a.R / 4, rows_per_cta = 256 / R4, blocks = kPrefillRows / rows_per_cta;
+    const int p = blockIdx.x / blocks, rb = blockIdx.x % blocks, l = blockIdx.y;
+    if (p >= a.hdr[kHdrPrefillTiles] || a.nch[l] < 2) return;
+    const int4 pt = a.ptiles[p];
+    const int nch = a.nch[l];
+    float4 *base = reinterpret_cast<float4 *>(a.part[l]) + (size_t)pt.y * R4;
+    const size_t cs = (size_t)a.T * R4;
+    const int e = rb * rows_per_cta * R4 + threadIdx.x;
+    if (e < pt.z * R4) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        int c = 0;
+        for (; c + 4 <= nch; c += 4) {
+            float4 f[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) f[u] = __ldcg(base + (c + u) * cs + e);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                acc.x += f[u].x;
+                acc.y += f[u].y;
+                acc.z += f[u].z;
+                acc.w += f[u].w;
+            }
+        }
+        for (; c < nch; ++c) {
+            const float4 f = __ldcg(base + c * cs + e);
+            acc.x += f.x;
+            acc.y += f.y;
+            acc.z += f.z;
+            acc.w += f.w;
+        }
+        base[e] = acc;
+    }
+}
+
 template <int R>
 __global__ void __launch_bounds__(kThreads, 2)
 prefill_shrink_kernel(const __grid_constant__ ShrinkArgs a) {
@@ -595,7 +642,7 @@ size_t expand_smem(int stages) {
 
 template <int R>
 cudaError_t launch_r(const ShrinkArgs &sa, int grid_tiles, int n_jobs, size_t shrink_smem,
-                     const ExpandArgs &ea, int expand_grid, cudaStream_t st) {
+                     const ReduceArgs *ra, const ExpandArgs &ea, int expand_grid, cudaStream_t st) {
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(prefill_shrink_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -609,6 +656,11 @@ cudaError_t launch_r(const ShrinkArgs &sa, int grid_tiles, int n_jobs, size_t sh
     prefill_shrink_kernel<R><<<dim3(grid_tiles, n_jobs, 1), kThreads, shrink_smem, st>>>(sa);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (ra) {
+        prefill_reduce_kernel<<<dim3(grid_tiles * (kPrefillRows / (256 / (R / 4))), ea.n, 1), 256, 0, st>>>(*ra);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     prefill_expand_kernel<R><<<expand_grid, kExpandThreads, expand_smem<R>(ea.stages), st>>>(ea);
     return cudaGetLastError();
 }
@@ -718,6 +770,19 @@ cudaError_t launch_prefill_tc(const PrefillLayer *L, int n, int T, int S, int R,
     sa.ptiles = ptiles;
     sa.hdr = hdr;
     sa.T = T;
+    // The expand's V loaders add the chunks themselves when that takes them
+    // at most two rounds of loads (two chunks per round up to rank 32, one at
+    // rank 64); otherwise a separate pass adds them once per (layer, tile)
+    // with thousands of loads in flight.
+    int max_nch = 1;
+    for (int g = 0; g < ng; ++g) max_nch = nch[g] > max_nch ? nch[g] : max_nch;
+    const int per_round = R <= 32 ? 2 : 1;
+    const bool reduce_pass = (max_nch + per_round - 1) / per_round > 2;
+    ReduceArgs ra{};
+    ra.ptiles = ptiles;
+    ra.hdr = hdr;
+    ra.T = T;
+    ra.R = R;
 
     const CUtensorMapSwizzle swz_rank = R == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
                                       : (R == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
@@ -733,7 +798,9 @@ cudaError_t launch_prefill_tc(const PrefillLayer *L, int n, int T, int S, int R,
         ea.y[i] = static_cast<uint16_t *>(L[i].y);
         ea.d_out[i] = L[i].d_out;
         ea.ncb[i] = (L[i].d_out + kColBlock - 1) / kColBlock;
-        ea.nch[i] = nch[grp[i]];
+        ea.nch[i] = reduce_pass ? 1 : nch[grp[i]];
+        ra.part[i] = L[i].part;
+        ra.nch[i] = nch[grp[i]];
         ea.sum_ncb += ea.ncb[i];
     }
     const size_t vbytes = 4 * (size_t)128 * R * 2, stage = 2 * kTileBytes + kNB * (size_t)R * 2;
@@ -748,9 +815,9 @@ cudaError_t launch_prefill_tc(const PrefillLayer *L, int n, int T, int S, int R,
     const int expand_grid = (int)(items < num_sms ? items : num_sms);
 
     switch (R) {
-    case 16: return launch_r<16>(sa, grid_tiles, n_jobs, shrink_smem, ea, expand_grid, st);
-    case 32: return launch_r<32>(sa, grid_tiles, n_jobs, shrink_smem, ea, expand_grid, st);
-    case 64: return launch_r<64>(sa, grid_tiles, n_jobs, shrink_smem, ea, expand_grid, st);
+    case 16: return launch_r<16>(sa, grid_tiles, n_jobs, shrink_smem, reduce_pass ? &ra : nullptr, ea, expand_grid, st);
+    case 32: return launch_r<32>(sa, grid_tiles, n_jobs, shrink_smem, reduce_pass ? &ra : nullptr, ea, expand_grid, st);
+    case 64: return launch_r<64>(sa, grid_tiles, n_jobs, shrink_smem, reduce_pass ? &ra : nullptr, ea, expand_grid, st);
     default: return cudaErrorInvalidValue;
     }
 }
