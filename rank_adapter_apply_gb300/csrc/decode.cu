@@ -160,6 +160,8 @@ __device__ __forceinline__ void shrink_bf16_tile(const LayerArgs &L, const Group
 // N = 8 columns, K = 16 ranks, columns permuted so that each lane ends with 8
 // consecutive outputs of two token rows (one 128-bit y access per row).
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ int bkey(int P) { return (((P >> 3) & 3) << 1) | (P & 1); }
+
 __device__ __forceinline__ void expand_bf16_tile(const LayerArgs &L, const GroupView &g, int dblock, int tile_i) {
     const int d_out = L.d_out;
     const int4 tile = g.tiles[tile_i];
@@ -175,7 +177,9 @@ __device__ __forceinline__ void expand_bf16_tile(const LayerArgs &L, const Group
 
     // This block's B rows (the slot's first 16 * nkb ranks) go to shared memory
     // in one burst of 16-byte cp.async: row P of the block at bs + 64 P, chunk
-    // c of the row at chunk c ^ (P & 7) so the fragment reads spread over banks.
+    // c of the row at chunk c ^ key(P). One fragment read touches rows
+    // P0 + 8a + b (a < 4, b < 2), so the key takes bits 3..4 and 0 of P and
+    // those eight rows land in distinct bank groups.
     __shared__ __align__(16) uint16_t bs[kExpandCols * 64];
     const uint16_t *Bs = static_cast<const uint16_t *>(L.B) + (size_t)s * d_out * R;
     const int c0 = dblock * kExpandCols;
@@ -183,7 +187,7 @@ __device__ __forceinline__ void expand_bf16_tile(const LayerArgs &L, const Group
         const int cpr = 2 * nkb;
         for (int i = threadIdx.x; i < kExpandCols * cpr; i += kThreads) {
             const int P = i / cpr, ch = i - P * cpr;
-            if (c0 + P < d_out) cp_async16(bs + P * 64 + ((ch ^ (P & 7)) << 3), Bs + (size_t)(c0 + P) * R + ch * 8);
+            if (c0 + P < d_out) cp_async16(bs + P * 64 + ((ch ^ bkey(P)) << 3), Bs + (size_t)(c0 + P) * R + ch * 8);
         }
         cp_async_commit();
     }
@@ -250,16 +254,11 @@ __device__ __forceinline__ void expand_bf16_tile(const LayerArgs &L, const Group
             for (int kb = 0; kb < 4; ++kb) {
                 if (kb < nkb) {
                     const int k = kb * 16 + 4 * tq;
+                    // ranks >= r: zero in the pool and in v, so no mask is needed
                     uint2 bb = make_uint2(0, 0);
-                    if (P < d_out && k < R) {
+                    if (P < d_out) {
                         const int Pl = P - c0;
-                        bb = *reinterpret_cast<const uint2 *>(bs + Pl * 64 + ((((k >> 3) ^ (Pl & 7))) << 3) + (k & 7));
-                    }
-                    if (k + 4 > r) {
-                        if (k + 0 >= r) bb.x &= 0xffff0000u;
-                        if (k + 1 >= r) bb.x &= 0x0000ffffu;
-                        if (k + 2 >= r) bb.y &= 0xffff0000u;
-                        if (k + 3 >= r) bb.y &= 0x0000ffffu;
+                        bb = *reinterpret_cast<const uint2 *>(bs + Pl * 64 + (((k >> 3) ^ bkey(Pl)) << 3) + (k & 7));
                     }
                     mma_bf16(acc[j], ahi[kb][0], ahi[kb][1], ahi[kb][2], ahi[kb][3], bb.x, bb.y);
                     mma_bf16(acc[j], alo[kb][0], alo[kb][1], alo[kb][2], alo[kb][3], bb.x, bb.y);
