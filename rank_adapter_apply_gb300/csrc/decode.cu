@@ -196,13 +196,20 @@ __device__ __forceinline__ void expand_bf16_tile(const LayerArgs &L, const Group
     uint32_t ahi[4][4], alo[4][4];
 #pragma unroll
     for (int kb = 0; kb < 4; ++kb) {
-        float f0[4], f1[4];
+        float f0[4] = {0.f, 0.f, 0.f, 0.f}, f1[4] = {0.f, 0.f, 0.f, 0.f};
+        const int kq = kb * 16 + 4 * tq;                 // ranks kq .. kq + 3, one 16-byte load per row
+        if (kb < nkb) {
+            if (gq < cnt) {
+                const float4 q = *reinterpret_cast<const float4 *>(L.v + (size_t)(p0 + gq) * R + kq);
+                f0[0] = q.x; f0[1] = q.y; f0[2] = q.z; f0[3] = q.w;
+            }
+            if (gq + 8 < cnt) {
+                const float4 q = *reinterpret_cast<const float4 *>(L.v + (size_t)(p0 + gq + 8) * R + kq);
+                f1[0] = q.x; f1[1] = q.y; f1[2] = q.z; f1[3] = q.w;
+            }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int k = kb * 16 + 4 * tq + i;
-            const bool kin = kb < nkb && k < r;
-            f0[i] = (kin && gq < cnt) ? L.v[(size_t)(p0 + gq) * R + k] : 0.f;
-            f1[i] = (kin && gq + 8 < cnt) ? L.v[(size_t)(p0 + gq + 8) * R + k] : 0.f;
+            for (int i = 0; i < 4; ++i)
+                if (kq + i >= r) f0[i] = f1[i] = 0.f;
         }
         float h0[4], h1[4];
 #pragma unroll
