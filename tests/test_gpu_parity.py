@@ -288,3 +288,41 @@ def test_batched_upload_matches_oracle(dtype):
         assert not B_pool[1, :, 8:].any()
     finally:
         sl.close()
+
+
+@pytest.mark.parametrize("name", ["decode", "prefill", "mixed"])
+def test_repeated_runs_are_bitwise_identical(name):
+    """Every reduction (d_in chunks, cluster partials, prefill chunk sums) adds in
+    a fixed order, so the same inputs give the same bits on every run."""
+    from rank_adapter_apply_gb300.harness import DeviceWorkload
+    w = {"decode": lambda: wl.decode_qv_4096(4),
+         "prefill": lambda: wl.prefill_5120(3, n_seqs=6, len_range=(100, 700)),
+         "mixed": lambda: wl.mixed_ranks_8b(2, n_segments=3, seg_len=300, n_decode=200)}[name]()
+    dw = DeviceWorkload(w, small_batch_tokens=None if name == "decode" else 0)
+    try:
+        outs = []
+        for _ in range(3):
+            dw.reset()
+            outs.append(dw.run())
+        for ly in w.layers:
+            for o in outs[1:]:
+                assert np.array_equal(o[ly.name], outs[0][ly.name]), ly.name
+        check_layer(w, w.layers[0].name, outs[0][w.layers[0].name])
+    finally:
+        dw.close()
+
+
+def test_batched_upload_rejects_bad_arguments():
+    import torch
+    from rank_adapter_apply_gb300 import binding as B
+    from rank_adapter_apply_gb300.slots import LoraSlots
+    sl = LoraSlots([(64, 64)], 4, 16, 8, dtype=torch.bfloat16, device="cuda:0")
+    try:
+        a = torch.zeros((16, 64), dtype=torch.bfloat16).pin_memory()
+        b = torch.zeros((64, 16), dtype=torch.bfloat16).pin_memory()
+        for slots, ranks in (([0, 0], [16, 16]), ([4], [16]), ([1], [32]), ([1], [0])):
+            with pytest.raises(B.LoraError):
+                sl.load_slots(slots, [([a], [b])] * len(slots), ranks, [32.0] * len(slots))
+        assert sl.stats()["uploads"] == 0          # nothing was queued
+    finally:
+        sl.close()
