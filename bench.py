@@ -369,6 +369,9 @@ def run_ours(args):
     hbm, peak_kind = peaks()
     achieved = bytes_ / (ms * 1e-3) / 1e9
 
+    # --- context: a plain copy of the same bytes per graph-replayed launch ---
+    floor = None if args.quick else copy_floor(bytes_ / max(1, args.steps), stream, dev, l2)
+
     # --- end to end through the C ABI with host buffers --------------------
     e2e = None if args.quick else run_e2e(args, w, batches, sets[0], stream, dev, world)
 
@@ -389,6 +392,7 @@ def run_ours(args):
                                "expand of q_proj and v_proj)",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "peak_kind": peak_kind, "traffic": kernel_traffic("decode_cluster.cu"),
+                     "copy_floor": floor,
                      "algorithmic_bytes_per_step": bytes_ / max(1, args.steps),
                      "tflops": flops / (ms * 1e-3) / 1e12},
         "e2e": e2e,
@@ -406,6 +410,38 @@ def run_ours(args):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def copy_floor(step_bytes, stream, dev, l2):
+    """GB/s of a plain device-to-device copy that moves as many bytes per
+    launch as one step (half read, half written), graph-replayed over buffers
+    larger than L2 in total: what a single launch of this size reaches on this
+    GPU, for comparison with the step's achieved GB/s."""
+    import torch
+    n = max(1, int(step_bytes // 4))                     # bf16 elements per buffer (bytes/2 each)
+    sets = int(max(8, -(-2.5 * l2 // (2 * n * 2))))
+    bufs = [(torch.empty(n, dtype=torch.bfloat16, device=dev), torch.empty(n, dtype=torch.bfloat16, device=dev))
+            for _ in range(sets)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for a, b in bufs:
+            b.copy_(a)
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            g.replay()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 50
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            g.replay()
+    e1.record(stream)
+    stream.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (reps * sets)
+    del bufs
+    return {"GBps": 4.0 * n / us / 1e3, "us_per_launch": us, "bytes_per_launch": 4 * n,
+            "note": "torch device-to-device copy of the step's byte count per launch, CUDA-graph replayed"}
 
 
 def run_e2e(args, w, batches, d0, stream, dev, world):
