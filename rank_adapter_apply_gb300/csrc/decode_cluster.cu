@@ -532,13 +532,13 @@ size_t cluster_decode_smem(int R) { return dyn_bytes(cluster_decode_kb(R)); }
 
 template <int KB>
 static cudaError_t launch_cluster_kb(const FusedArgs &fa, int tiles, cudaStream_t st, bool pdl) {
-    static bool attr_done = false;
+    static std::atomic<uint64_t> attr_done{0};
     const size_t smem = dyn_bytes(KB);
-    if (!attr_done) {
+    if (!device_bit(attr_done)) {
         cudaError_t e = cudaFuncSetAttribute(decode_cluster_kernel<KB>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        attr_done = true;
+        set_device_bit(attr_done);
     }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)(tiles * kCl), (unsigned)fa.n, 1);

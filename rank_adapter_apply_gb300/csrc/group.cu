@@ -162,13 +162,13 @@ group_tokens_kernel(const int32_t *__restrict__ idx, int T, const int *__restric
 
 cudaError_t launch_group_tokens(const int32_t *idx, int T, const int *rank_dev, int S,
                                 int min_run, char *ws, const WsLayout &lay, cudaStream_t st) {
-    static bool attr_set = false;
+    static std::atomic<uint64_t> attr_set{0};
     size_t smem = sizeof(GroupSmem);
-    if (!attr_set) {
+    if (!device_bit(attr_set)) {
         cudaError_t e = cudaFuncSetAttribute(group_tokens_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        set_device_bit(attr_set);
     }
     group_tokens_kernel<<<1, kGroupThreads, smem, st>>>(
         idx, T, rank_dev, S, min_run, reinterpret_cast<int *>(ws + lay.hdr),

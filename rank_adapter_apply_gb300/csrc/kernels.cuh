@@ -3,6 +3,7 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 
@@ -29,6 +30,19 @@ struct WsLayout {
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Kernel attributes (e.g. the dynamic shared-memory limit) are per device:
+// one bit per device (ids 0..63) records that the current device has them.
+inline bool device_bit(const std::atomic<uint64_t> &f) {
+    int d = 0;
+    cudaGetDevice(&d);
+    return (f.load(std::memory_order_acquire) >> (d & 63)) & 1u;
+}
+inline void set_device_bit(std::atomic<uint64_t> &f) {
+    int d = 0;
+    cudaGetDevice(&d);
+    f.fetch_or(uint64_t(1) << (d & 63), std::memory_order_release);
+}
 
 inline WsLayout ws_layout(int S, int R, int max_tokens, int max_layers) {
     WsLayout w{};

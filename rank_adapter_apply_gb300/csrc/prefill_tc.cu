@@ -643,15 +643,15 @@ size_t expand_smem(int stages) {
 template <int R>
 cudaError_t launch_r(const ShrinkArgs &sa, int grid_tiles, int n_jobs, size_t shrink_smem,
                      const ReduceArgs *ra, const ExpandArgs &ea, int expand_grid, cudaStream_t st) {
-    static bool attr = false;
-    if (!attr) {
+    static std::atomic<uint64_t> attr{0};
+    if (!device_bit(attr)) {
         cudaError_t e = cudaFuncSetAttribute(prefill_shrink_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)(1024 + kShrinkRingBudget));
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(prefill_expand_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kExpandSmemBudget);
         if (e != cudaSuccess) return e;
-        attr = true;
+        set_device_bit(attr);
     }
     prefill_shrink_kernel<R><<<dim3(grid_tiles, n_jobs, 1), kThreads, shrink_smem, st>>>(sa);
     cudaError_t e = cudaGetLastError();
