@@ -327,6 +327,17 @@ int lora_sync_uploads(lora_ctx *ctx);
 /* Counters; synchronises the compute stream to read the device error count. */
 int lora_stats(lora_ctx *ctx, lora_stats_t *out);
 
+/*
+ * Failure-path self test (no counterpart on the source pages): launches, on
+ * the compute stream, a one-CTA kernel that waits on a barrier nothing
+ * completes, with the same bounded wait every kernel of the library uses. The
+ * wait gives up after 2^14 probes, the kernel sets the device error word and
+ * returns; *gave_up = 1 once it has. The word stays set, as after a real
+ * timeout, and lora_stats reports it (device_wait_timeouts). Nothing faults
+ * or hangs and the context stays usable. Synchronises the compute stream.
+ */
+int lora_selftest_wait_timeout(lora_ctx *ctx, int *gave_up);
+
 /* Bytes one adapter upload moves: sum over layers of (d_in + d_out) * rank * bytes_per_param. */
 uint64_t lora_adapter_bytes(int n_layers, const int *d_in, const int *d_out, int rank,
                             int bytes_per_param);

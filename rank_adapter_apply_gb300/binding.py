@@ -34,6 +34,7 @@ EXPORTED = [
     "lora_last_error", "lora_apply_static_scratch", "lora_pin", "lora_set_min_residency",
     "lora_set_policy", "lora_set_keep_score_weights", "lora_set_adapter_priority",
     "lora_set_slot_tracking", "lora_load_slots", "lora_assign_batch", "lora_release_batch",
+    "lora_selftest_wait_timeout",
 ]
 
 
@@ -92,6 +93,7 @@ def load(path: str = LIB_PATH):
         "lora_set_thrash_window": (i32, [vp, i32]),
         "lora_pin": (i32, [vp, i32, i32]),
         "lora_set_slot_tracking": (i32, [vp, i32]),
+        "lora_selftest_wait_timeout": (i32, [vp, P(i32)]),
         "lora_assign_batch": (i32, [vp, i32, P(u64), P(i32), i32, P(i32), P(i32), P(u64), P(i32)]),
         "lora_release_batch": (i32, [vp, i32, P(i32)]),
         "lora_load_slots": (i32, [vp, i32, P(i32), P(vp), P(vp), P(i32), P(ctypes.c_float)]),
@@ -250,6 +252,13 @@ def lora_set_thrash_window(ctx, epochs):
 
 
 LORA_POLICY_LRU, LORA_POLICY_KEEP_SCORE = 0, 1
+
+
+def lora_selftest_wait_timeout(ctx):
+    """Returns 1 when the bounded wait gave up and set the device error word."""
+    g = ctypes.c_int(0)
+    check(load().lora_selftest_wait_timeout(ctx, ctypes.byref(g)))
+    return g.value
 
 
 def lora_set_slot_tracking(ctx, on=True):

@@ -420,6 +420,19 @@ expand_f32_kernel(MultiArgs ma, GroupView g, int max_dblocks) {
     }
 }
 
+// A wait that nothing completes, bounded like every wait of the kernels: it
+// gives up after `limit` probes and records that in the error word.
+__global__ void selftest_wait_kernel(int *err_word, uint32_t limit) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const bool done = mbar_wait_bounded(&bar, 0, limit);
+    if (!done && threadIdx.x == 0) atomicExch(err_word, 1);
+}
+
 __global__ void set_slot_kernel(float *scale_dev, int *rank_dev, int slot, float scale, int rank) {
     scale_dev[slot] = scale;
     rank_dev[slot] = rank;
@@ -444,6 +457,11 @@ cudaError_t launch_decode(const MultiArgs &ma, const GroupView &gv, int dtype, i
         size_t smem = (size_t)kTileTokens * gv.R * sizeof(float);
         expand_f32_kernel<<<grid(max_dblocks), kThreads, smem, st>>>(ma, gv, max_dblocks);
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_selftest_wait(int *err_word, uint32_t limit, cudaStream_t st) {
+    selftest_wait_kernel<<<1, 32, 0, st>>>(err_word, limit);
     return cudaGetLastError();
 }
 

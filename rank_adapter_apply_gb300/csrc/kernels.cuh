@@ -169,5 +169,6 @@ int set_last_error(int code, const char *msg);
 
 cudaError_t launch_set_slot(float *scale_dev, int *rank_dev, int slot, float scale, int rank,
                             cudaStream_t st);
+cudaError_t launch_selftest_wait(int *err_word, uint32_t limit, cudaStream_t st);
 
 }  // namespace lora

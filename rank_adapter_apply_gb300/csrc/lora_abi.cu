@@ -778,6 +778,19 @@ int lora_sync_uploads(lora_ctx *c) {
     return harvest_timings(c, true);
 }
 
+int lora_selftest_wait_timeout(lora_ctx *c, int *gave_up) {
+    if (!c || !gave_up) return fail(LORA_ERR_ARG, "NULL argument");
+    if (!c->device) return fail(LORA_ERR_STATE, "host-only context has no device");
+    *gave_up = 0;
+    int *word = reinterpret_cast<int *>(c->ws + c->lay.hdr) + kHdrError;
+    CUDA_TRY(launch_selftest_wait(word, 1u << 14, c->compute));
+    CUDA_TRY(cudaStreamSynchronize(c->compute));
+    int v = 0;
+    CUDA_TRY(cudaMemcpy(&v, word, sizeof v, cudaMemcpyDeviceToHost));
+    *gave_up = v != 0;
+    return LORA_OK;
+}
+
 int lora_stats(lora_ctx *c, lora_stats_t *o) {
     if (!c || !o) return fail(LORA_ERR_ARG, "NULL argument");
     memset(o, 0, sizeof *o);

@@ -264,3 +264,13 @@ def test_assign_batch_equals_sequential_calls(lib):
         assert B.lora_release_batch(ctx, slots[:1]) == B.LORA_ERR_STATE
     finally:
         B.lora_destroy(ctx)
+
+
+def test_selftest_needs_a_device_context(lib):
+    ctx = _host_ctx(2, 16)
+    try:
+        import ctypes
+        g = ctypes.c_int(0)
+        assert lib.lora_selftest_wait_timeout(ctx, ctypes.byref(g)) == B.LORA_ERR_STATE
+    finally:
+        B.lora_destroy(ctx)
