@@ -151,9 +151,15 @@ int lora_apply_multi(lora_ctx *ctx, int n, const int *layers, const void *const 
 /*
  * The same as lora_apply_multi with HOST buffers: copies the inputs (distinct
  * xs_host once each, ys_host, idx_host) to the caller's device staging buffers
- * xs_dev / ys_dev / idx_dev, applies, and copies every y back to ys_host, all
- * on the compute stream. Returns after queuing; synchronise the compute stream
- * before reading ys_host. Host buffers should be pinned.
+ * xs_dev / ys_dev / idx_dev, applies, and copies every y back to ys_host.
+ * The copies in run on the upload stream, each device buffer after the copies
+ * back of the last call that used it; the apply and the copies back run on the
+ * compute stream. A caller that alternates two sets of device buffers thus
+ * overlaps one call's copies in with the previous call's work; reusing one set
+ * is also correct (the calls then serialise). Under stream capture, or with
+ * more than 64 distinct device buffers seen, everything runs on the compute
+ * stream. Returns after queuing; synchronise the compute stream before reading
+ * ys_host or reusing a host buffer. Host buffers should be pinned.
  */
 int lora_apply_multi_host(lora_ctx *ctx, int n, const int *layers,
                           const void *const *xs_host, void *const *ys_host,

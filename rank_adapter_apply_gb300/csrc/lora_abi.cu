@@ -90,6 +90,11 @@ struct lora_ctx {
     std::vector<cudaEvent_t> ring;
     std::vector<int64_t> slot_gen;
     int64_t n_apply = 0;
+    // Host-buffer path: the last use of each device staging buffer (recorded on
+    // the compute stream after that call's copies back), and this call's
+    // host-to-device copies (on the upload stream).
+    std::vector<std::pair<const void *, cudaEvent_t>> buf_ev;
+    cudaEvent_t h2d_done = nullptr;
 
     lora_ctx(int S_, int R_) : table(S_, R_) {}
 };
@@ -264,6 +269,9 @@ void lora_destroy(lora_ctx *c) {
         if (c->compute_done) cudaEventDestroy(c->compute_done);
         for (auto ev : c->ring)
             if (ev) cudaEventDestroy(ev);
+        for (auto &be : c->buf_ev)
+            if (be.second) cudaEventDestroy(be.second);
+        if (c->h2d_done) cudaEventDestroy(c->h2d_done);
     }
     delete c;
 }
@@ -596,16 +604,47 @@ int lora_apply_multi_host(lora_ctx *c, int n, const int *layers, const void *con
     for (int i = 0; i < n; ++i)
         if (layers[i] < 0 || layers[i] >= c->n_layers) return fail(LORA_ERR_ARG, "bad layer");
     const size_t e = elem_bytes(c->dtype);
-    CUDA_TRY(cudaMemcpyAsync(idx_dev, idx_host, sizeof(int32_t) * T, cudaMemcpyHostToDevice, c->compute));
+    // Device staging buffers of this call (the distinct ones).
+    std::vector<const void *> bufs{idx_dev};
+    for (int i = 0; i < n; ++i) {
+        bufs.push_back(xs_dev[i]);
+        bufs.push_back(ys_dev[i]);
+    }
+    std::sort(bufs.begin(), bufs.end());
+    bufs.erase(std::unique(bufs.begin(), bufs.end()), bufs.end());
+    // Copies in on the upload stream, each buffer after the last call that used
+    // it: a caller alternating buffer sets overlaps one call's copies in with
+    // the previous call's apply and copies back. Under stream capture, or with
+    // too many distinct buffers to track, everything stays on the compute stream.
+    constexpr size_t kMaxTracked = 64;
+    bool split = !capturing(c->compute);
+    if (split && !c->h2d_done) CUDA_TRY(cudaEventCreateWithFlags(&c->h2d_done, cudaEventDisableTiming));
+    if (split) {
+        size_t fresh = 0;
+        for (const void *b : bufs) {
+            bool known = false;
+            for (auto &be : c->buf_ev) known = known || be.first == b;
+            fresh += known ? 0 : 1;
+        }
+        split = c->buf_ev.size() + fresh <= kMaxTracked;
+    }
+    cudaStream_t in = split ? c->upload : c->compute;
+    if (split)
+        for (auto &be : c->buf_ev)
+            if (std::binary_search(bufs.begin(), bufs.end(), be.first))
+                CUDA_TRY(cudaStreamWaitEvent(c->upload, be.second, 0));
+    CUDA_TRY(cudaMemcpyAsync(idx_dev, idx_host, sizeof(int32_t) * T, cudaMemcpyHostToDevice, in));
     for (int i = 0; i < n; ++i) {
         const lora_layer_desc &L = c->layers[layers[i]];
         bool dup = false;                          // layers sharing one input copy it once
         for (int j = 0; j < i; ++j) dup = dup || (xs_host[j] == xs_host[i] && xs_dev[j] == xs_dev[i]);
         if (!dup)
-            CUDA_TRY(cudaMemcpyAsync(xs_dev[i], xs_host[i], (size_t)T * L.d_in * e,
-                                     cudaMemcpyHostToDevice, c->compute));
-        CUDA_TRY(cudaMemcpyAsync(ys_dev[i], ys_host[i], (size_t)T * L.d_out * e,
-                                 cudaMemcpyHostToDevice, c->compute));
+            CUDA_TRY(cudaMemcpyAsync(xs_dev[i], xs_host[i], (size_t)T * L.d_in * e, cudaMemcpyHostToDevice, in));
+        CUDA_TRY(cudaMemcpyAsync(ys_dev[i], ys_host[i], (size_t)T * L.d_out * e, cudaMemcpyHostToDevice, in));
+    }
+    if (split) {
+        CUDA_TRY(cudaEventRecord(c->h2d_done, c->upload));
+        CUDA_TRY(cudaStreamWaitEvent(c->compute, c->h2d_done, 0));
     }
     int rc = apply_impl(c, n, layers, xs_dev, ys_dev, idx_dev, T);
     if (rc != LORA_OK) return rc;
@@ -614,6 +653,17 @@ int lora_apply_multi_host(lora_ctx *c, int n, const int *layers, const void *con
         CUDA_TRY(cudaMemcpyAsync(ys_host[i], ys_dev[i], (size_t)T * L.d_out * e,
                                  cudaMemcpyDeviceToHost, c->compute));
     }
+    if (split)
+        for (const void *b : bufs) {
+            cudaEvent_t ev = nullptr;
+            for (auto &be : c->buf_ev)
+                if (be.first == b) ev = be.second;
+            if (!ev) {
+                CUDA_TRY(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+                c->buf_ev.emplace_back(b, ev);
+            }
+            CUDA_TRY(cudaEventRecord(ev, c->compute));
+        }
     return LORA_OK;
 }
 

@@ -326,3 +326,54 @@ def test_batched_upload_rejects_bad_arguments():
         assert sl.stats()["uploads"] == 0          # nothing was queued
     finally:
         sl.close()
+
+
+@pytest.mark.parametrize("device_sets", [1, 2])
+def test_host_buffer_path_matches_oracle(device_sets):
+    """lora_apply_multi_host, several calls queued back to back: copies in on
+    the upload stream ordered per device buffer, apply and copies back on the
+    compute stream. With one device buffer set the calls serialise, with two
+    they overlap; every call's result equals the oracle's."""
+    import torch
+    from rank_adapter_apply_gb300 import binding as B
+    from rank_adapter_apply_gb300.harness import to_torch
+    from rank_adapter_apply_gb300.slots import LoraSlots
+    rng = np.random.default_rng(21)
+    S, R, T, d, dv = 4, 16, 96, 512, 384
+    layers = [wl.Layer("q", d, d, "x"), wl.Layer("v", d, dv, "x")]
+    ranks = np.array([16, 8, 16, 12], np.int32)
+    ads = [wl._adapter(rng, layers, int(r), wl.DTYPE_BF16) for r in ranks]
+    sl = LoraSlots([(d, d), (d, dv)], S, R, T, dtype=torch.bfloat16, device="cuda:0")
+    try:
+        for s in range(S):
+            sl.load_slot(s, [to_torch(ads[s][l.name][0], wl.DTYPE_BF16).pin_memory() for l in layers],
+                         [to_torch(ads[s][l.name][1], wl.DTYPE_BF16).pin_memory() for l in layers],
+                         int(ranks[s]), 2.0 * float(ranks[s]))
+        sl.sync_uploads()
+        batches = []
+        for k in range(6):
+            x = wl._mat(rng, (T, d), "normal", 1.0, wl.DTYPE_BF16)
+            ys = {"q": wl._mat(rng, (T, d), "normal", 1.0, wl.DTYPE_BF16),
+                  "v": wl._mat(rng, (T, dv), "normal", 1.0, wl.DTYPE_BF16)}
+            idx = rng.integers(-1, S, size=T).astype(np.int32)
+            hx = to_torch(x, wl.DTYPE_BF16).pin_memory()
+            hy = [to_torch(ys[n], wl.DTYPE_BF16).clone().pin_memory() for n in ("q", "v")]
+            hidx = torch.from_numpy(idx).pin_memory()
+            batches.append((x, ys, idx, hx, hy, hidx))
+        dev_sets = [(torch.empty((T, d), dtype=torch.bfloat16, device="cuda:0"),
+                     [torch.empty((T, d), dtype=torch.bfloat16, device="cuda:0"),
+                      torch.empty((T, dv), dtype=torch.bfloat16, device="cuda:0")],
+                     torch.empty(T, dtype=torch.int32, device="cuda:0")) for _ in range(device_sets)]
+        for k, (_, _, _, hx, hy, hidx) in enumerate(batches):
+            xd, yd, idd = dev_sets[k % device_sets]
+            B.lora_apply_multi_host(sl.ctx, [0, 1], [hx.data_ptr()] * 2, [t.data_ptr() for t in hy],
+                                    hidx.data_ptr(), T, [xd.data_ptr()] * 2, [t.data_ptr() for t in yd],
+                                    idd.data_ptr())
+        sl.compute.synchronize()
+        for x, ys, idx, hx, hy, hidx in batches:
+            w = wl.Workload("custom", wl.DTYPE_BF16, S, R, layers, idx, {"x": x}, ys, ads, ranks,
+                            2.0 * ranks.astype(np.float64))
+            for name, t in zip(("q", "v"), hy):
+                check_layer(w, name, t.view(torch.int16).numpy().view(np.uint16))
+    finally:
+        sl.close()
