@@ -418,7 +418,10 @@ def copy_floor(step_bytes, stream, dev, l2):
     larger than L2 in total: what a single launch of this size reaches on this
     GPU, for comparison with the step's achieved GB/s."""
     import torch
-    n = max(1, int(step_bytes // 4))                     # bf16 elements per buffer (bytes/2 each)
+    # bf16 elements per buffer (bytes/2 each), rounded up to whole 64 KiB: the
+    # driver's copy runs a slower path on sizes that are not (6.82 MB copies
+    # measured 6.05 us against 4.1 us for 6.5 MiB).
+    n = max(1, -(-int(step_bytes // 4) // 32768) * 32768)
     sets = int(max(8, -(-2.5 * l2 // (2 * n * 2))))
     bufs = [(torch.empty(n, dtype=torch.bfloat16, device=dev), torch.empty(n, dtype=torch.bfloat16, device=dev))
             for _ in range(sets)]

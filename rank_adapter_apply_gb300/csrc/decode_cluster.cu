@@ -23,7 +23,10 @@
 //   * after a cluster barrier reads the 8 partials of the tile through
 //     distributed shared memory, adds them in rank order (deterministic),
 //     splits v into bf16 high and low parts and runs the expand MMAs for its
-//     d_out slice, writing y once (fp32 add, one rounding).
+//     d_out slice, writing y once (fp32 add, one rounding). When the slice is
+//     at most two stages (d_out <= 4096) the products B_s v are formed before
+//     the wait on the previous kernel and parked in shared memory; after the
+//     wait only the y rows (prefetched into L2) are loaded, updated and stored.
 // No global flags, no spin loops; every mbarrier wait is bounded and a wait
 // that gives up sets the error word and leaves the rows it guards unchanged.
 // Each CTA also groups the batch itself (slot ids in shared memory, counts,
@@ -122,6 +125,56 @@ __device__ __forceinline__ int bsw(int P, int k, int R) {
     if (R == 32) ch ^= ((P >> 3) & 1) << 1;
     else if (R == 64) ch ^= ((P & 1) | (((P >> 3) & 1) << 1)) << 1;
     return P * R + (ch << 3) + (k & 7);
+}
+
+// Products B_s v for one warp's 64 columns [c0, c0 + 64) of an expand stage:
+// two 32-column groups of four 8-column MMA blocks. Every B fragment is read
+// first; then, for each 16-rank block, the high-part MMAs of all eight column
+// blocks are issued, and after them the low-part ones. Each accumulator still
+// adds high before low, rank block by rank block, so the sums are those of a
+// one-block-at-a-time loop, but eight independent MMAs go out back to back
+// instead of each waiting on its dependent partner and on its own B load.
+template <int KB>
+__device__ __forceinline__ void expand_products(const uint16_t *bs, int c0, int w, int R, int r, int nmb,
+                                                const uint32_t (&ahi)[KB][4], const uint32_t (&alo)[KB][4],
+                                                int gq, int tq, float (&acc)[2][4][4]) {
+    uint2 bfr[2][4][KB];
+#pragma unroll
+    for (int grp = 0; grp < 2; ++grp)
+#pragma unroll
+        for (int jn = 0; jn < 4; ++jn) {
+            const int P = c0 + grp * 32 + 8 * (gq >> 1) + 2 * jn + (gq & 1);
+#pragma unroll
+            for (int kb = 0; kb < KB; ++kb) {
+                const int k = kb * 16 + 4 * tq;
+                uint2 bb = (kb < nmb && P < w && k < R) ? lds64(bs + bsw(P, k, R)) : make_uint2(0, 0);
+                if (k + 4 > r) {               // ranks at or past r contribute nothing
+                    if (k + 0 >= r) bb.x &= 0xffff0000u;
+                    if (k + 1 >= r) bb.x &= 0x0000ffffu;
+                    if (k + 2 >= r) bb.y &= 0xffff0000u;
+                    if (k + 3 >= r) bb.y &= 0x0000ffffu;
+                }
+                bfr[grp][jn][kb] = bb;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[grp][jn][q] = 0.f;
+        }
+#pragma unroll
+    for (int kb = 0; kb < KB; ++kb) {
+        if (kb >= nmb) break;
+#pragma unroll
+        for (int grp = 0; grp < 2; ++grp)
+#pragma unroll
+            for (int jn = 0; jn < 4; ++jn)
+                mma_bf16(acc[grp][jn], ahi[kb][0], ahi[kb][1], ahi[kb][2], ahi[kb][3], bfr[grp][jn][kb].x,
+                         bfr[grp][jn][kb].y);
+#pragma unroll
+        for (int grp = 0; grp < 2; ++grp)
+#pragma unroll
+            for (int jn = 0; jn < 4; ++jn)
+                mma_bf16(acc[grp][jn], alo[kb][0], alo[kb][1], alo[kb][2], alo[kb][3], bfr[grp][jn][kb].x,
+                         bfr[grp][jn][kb].y);
+    }
 }
 
 // Shrink stage j: x rows of the tile and A rows of the slot, columns [ks, ks + w).
@@ -333,9 +386,10 @@ decode_cluster_kernel(const __grid_constant__ FusedArgs fa) {
                     if (m < nmb) {
                         const uint4 a0 = lds128(as + swz(m * 16 + gq, cc));
                         const uint4 a1 = lds128(as + swz(m * 16 + gq + 8, cc));
+                        // the two accumulators alternate, so no MMA waits on the one before it
                         mma_bf16(acc[m][0], a0.x, a1.x, a0.y, a1.y, xa.x, xa.y);
-                        mma_bf16(acc[m][0], a0.z, a1.z, a0.w, a1.w, xa.z, xa.w);
                         mma_bf16(acc[m][1], a0.x, a1.x, a0.y, a1.y, xb.x, xb.y);
+                        mma_bf16(acc[m][0], a0.z, a1.z, a0.w, a1.w, xa.z, xa.w);
                         mma_bf16(acc[m][1], a0.z, a1.z, a0.w, a1.w, xb.z, xb.w);
                     }
                 }
@@ -350,6 +404,13 @@ decode_cluster_kernel(const __grid_constant__ FusedArgs fa) {
     // for it once the partials of v have been exchanged).
     __syncthreads();
     for (int j = 0; j < nes && j < 2; ++j) issue_expand<KB>(L, sm, d, t, R, o0, o1, j, &sm.ebar[j], 1);
+    // The y rows are read right after the wait on the previous kernel. Asking
+    // L2 for them now, behind the shrink's own loads, takes their DRAM latency
+    // out of the chain that follows the wait; the loads after the wait still
+    // see that kernel's writes.
+    if (fa.early && nes >= 1 && nes <= 2 && tid < t.cnt)
+        prefetch_l2_bulk(static_cast<const uint16_t *>(L.y) + (size_t)sm.tok[tid] * L.d_out + o0,
+                         (uint32_t)(o1 - o0) * 2u);
 
     // Cross-warp sum into this CTA's partial v[token][k].
     float *red = d.red;
@@ -438,6 +499,92 @@ decode_cluster_kernel(const __grid_constant__ FusedArgs fa) {
         }
     }
 
+    const float scale = sm.scale;
+    const int tok0 = gq < t.cnt ? sm.tok[gq] : -1;
+    const int tok1 = gq + 8 < t.cnt ? sm.tok[gq + 8] : -1;
+    uint16_t *yg = static_cast<uint16_t *>(L.y);
+    const int d_out = L.d_out;
+
+    // ---- short path: this CTA's d_out slice is at most two stages ----------
+    // The products B_s v do not depend on y, so they are formed here, before
+    // the wait on the previous kernel, and parked as fp32 in region 1 (slots
+    // private to each thread: float4 index (stage * 8 + i) * kCT + tid). After
+    // the wait only the y rows are read, straight into registers, updated with
+    // the same fma and rounding as below, and written back.
+    if (nes <= 2) {
+        cp_async_wait_all();                // this thread's B rows have landed
+        __syncthreads();                    // and everyone else's
+        float4 *dl = reinterpret_cast<float4 *>(d.xs);
+        float4 keep[8];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            if (j >= nes) break;
+            const int w = min(kSW, o1 - (o0 + j * kSW));
+            const uint16_t *bs = d.bs + (size_t)j * kSW * KB * 16;
+            float acc2[2][4][4];
+            expand_products<KB>(bs, warp * 64, w, R, t.r, nmb, ahi, alo, gq, tq, acc2);
+#pragma unroll
+            for (int grp = 0; grp < 2; ++grp) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float(&a)[4][4] = acc2[grp];
+                    const float4 f0 = make_float4(a[0][2 * h], a[0][2 * h + 1], a[1][2 * h], a[1][2 * h + 1]);
+                    const float4 f1 = make_float4(a[2][2 * h], a[2][2 * h + 1], a[3][2 * h], a[3][2 * h + 1]);
+                    const int i = grp * 4 + h * 2;
+                    if (j == 0) {
+                        dl[i * kCT + tid] = f0;
+                        dl[(i + 1) * kCT + tid] = f1;
+                    } else {
+                        keep[i] = f0;
+                        keep[i + 1] = f1;
+                    }
+                }
+            }
+        }
+        __syncthreads();                    // every read of the B rows is done
+        if (nes == 2) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) dl[(8 + i) * kCT + tid] = keep[i];
+        }
+        if (fa.early) grid_dependency_wait();
+        uint4 yv[2][2][2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int grp = 0; grp < 2; ++grp)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int os = o0 + j * kSW, cc = warp * 64 + grp * 32 + 8 * tq;
+                    const int tok = h ? tok1 : tok0;
+                    yv[j][grp][h] = (j < nes && cc < o1 - os && tok >= 0)
+                                        ? __ldcg(reinterpret_cast<const uint4 *>(yg + (size_t)tok * d_out + os + cc))
+                                        : make_uint4(0, 0, 0, 0);
+                }
+        if (ok) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+                for (int grp = 0; grp < 2; ++grp)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int os = o0 + j * kSW, cc = warp * 64 + grp * 32 + 8 * tq;
+                        const int tok = h ? tok1 : tok0;
+                        if (j >= nes || cc >= o1 - os || tok < 0) continue;
+                        const int i = j * 8 + grp * 4 + h * 2;
+                        const float4 f0 = dl[i * kCT + tid], f1 = dl[(i + 1) * kCT + tid];
+                        const float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+                        uint32_t wv[4] = {yv[j][grp][h].x, yv[j][grp][h].y, yv[j][grp][h].z, yv[j][grp][h].w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            wv[q] = pack_bf16(fmaf(scale, f[2 * q], bf_lo(wv[q])), fmaf(scale, f[2 * q + 1], bf_hi(wv[q])));
+                        *reinterpret_cast<uint4 *>(yg + (size_t)tok * d_out + os + cc) =
+                            make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    }
+        }
+        if (!ok && tid == 0) atomicExch(fa.hdr + kHdrError, 1);
+        return;
+    }
+
     // Everything so far depends only on inputs the caller declared ready
     // (fa.early): the partial exchange ran before the wait, so after it only
     // the y rows are fetched, updated and written.
@@ -445,11 +592,6 @@ decode_cluster_kernel(const __grid_constant__ FusedArgs fa) {
     for (int j = 0; j < nes && j < 2; ++j) issue_expand<KB>(L, sm, d, t, R, o0, o1, j, &sm.ebar[j], 2);
 
     // ---- expand over this CTA's d_out slice --------------------------------
-    const float scale = sm.scale;
-    const int tok0 = gq < t.cnt ? sm.tok[gq] : -1;
-    const int tok1 = gq + 8 < t.cnt ? sm.tok[gq + 8] : -1;
-    uint16_t *yg = static_cast<uint16_t *>(L.y);
-    const int d_out = L.d_out;
     for (int j = 0; j < nes; ++j) {
         const int b = j & 1;
         const bool got = mbar_wait_bounded(&sm.ebar[b], (j >> 1) & 1, kWaitLimit);
@@ -457,52 +599,22 @@ decode_cluster_kernel(const __grid_constant__ FusedArgs fa) {
         const int os = o0 + j * kSW, w = min(kSW, o1 - os);
         const uint16_t *ys = d.ys + b * kTileTokens * kSW;
         const uint16_t *bs = d.bs + (size_t)b * kSW * KB * 16;
-        // operands of both 32-column groups first, then the MMAs, then the stores
-        uint2 bfr[2][4][KB];
+        // y fragments first, then the products, then the stores
         uint4 yv[2][2];
 #pragma unroll
         for (int grp = 0; grp < 2; ++grp) {
-            const int c = warp * 64 + grp * 32;
-#pragma unroll
-            for (int jn = 0; jn < 4; ++jn) {
-                const int P = c + 8 * (gq >> 1) + 2 * jn + (gq & 1);
-#pragma unroll
-                for (int kb = 0; kb < KB; ++kb) {
-                    const int k = kb * 16 + 4 * tq;
-                    bfr[grp][jn][kb] = (kb < nmb && P < w && k < R) ? lds64(bs + bsw(P, k, R))
-                                                                     : make_uint2(0, 0);
-                }
-            }
-            const int cc = c + 8 * tq;
+            const int cc = warp * 64 + grp * 32 + 8 * tq;
 #pragma unroll
             for (int h = 0; h < 2; ++h)
                 yv[grp][h] = (cc < w && gq + 8 * h < t.cnt) ? lds128(ys + swz(gq + 8 * h, cc))
                                                              : make_uint4(0, 0, 0, 0);
         }
+        float acc[2][4][4];
+        expand_products<KB>(bs, warp * 64, w, R, t.r, nmb, ahi, alo, gq, tq, acc);
 #pragma unroll
         for (int grp = 0; grp < 2; ++grp) {
             const int c = warp * 64 + grp * 32;          // stage-local first column
-            if (c >= w) continue;
-            float acc2[4][4];
-#pragma unroll
-            for (int jn = 0; jn < 4; ++jn) {
-                acc2[jn][0] = acc2[jn][1] = acc2[jn][2] = acc2[jn][3] = 0.f;
-#pragma unroll
-                for (int kb = 0; kb < KB; ++kb) {
-                    if (kb < nmb) {
-                        const int k = kb * 16 + 4 * tq;
-                        uint2 bb = bfr[grp][jn][kb];
-                        if (k + 4 > t.r) {
-                            if (k + 0 >= t.r) bb.x &= 0xffff0000u;
-                            if (k + 1 >= t.r) bb.x &= 0x0000ffffu;
-                            if (k + 2 >= t.r) bb.y &= 0xffff0000u;
-                            if (k + 3 >= t.r) bb.y &= 0x0000ffffu;
-                        }
-                        mma_bf16(acc2[jn], ahi[kb][0], ahi[kb][1], ahi[kb][2], ahi[kb][3], bb.x, bb.y);
-                        mma_bf16(acc2[jn], alo[kb][0], alo[kb][1], alo[kb][2], alo[kb][3], bb.x, bb.y);
-                    }
-                }
-            }
+            const float(&acc2)[4][4] = acc[grp];
             const int cc = c + 8 * tq;
             if (cc >= w || !ok) continue;
 #pragma unroll

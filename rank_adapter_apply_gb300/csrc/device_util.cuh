@@ -96,6 +96,13 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     return false;
 }
 
+// Hint to bring [src, src + bytes) into L2 (16-byte aligned, size % 16 == 0).
+// It has no effect on what any load observes: L2 is where every SM's stores
+// land, so a line fetched early is updated in place by later writes.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Bulk global -> shared copy completing on an mbarrier (16-byte aligned, size % 16 == 0).
 __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src, uint32_t bytes, uint64_t *bar) {
     asm volatile(
