@@ -449,48 +449,76 @@ def copy_floor(step_bytes, stream, dev, l2):
 
 def run_e2e(args, w, batches, d0, stream, dev, world):
     """Whole-job throughput through lora_apply_multi_host with pinned host
-    buffers: per step host admission of every adapter in the batch (lookup hit,
-    acquire), H2D of x / y / slot ids, apply, D2H of both y, release."""
+    buffers: per step admission of every token's adapter (lora_assign_tokens:
+    lookup hit, acquire, slot id per token), H2D of slot ids / x / y (one packed
+    copy), apply, D2H of both y (one packed copy), release."""
     import torch
     from rank_adapter_apply_gb300 import binding as B
     from rank_adapter_apply_gb300.harness import to_torch
 
     ctx = d0.slots.ctx
     nh = min(16, len(batches))                 # host buffer sets, reused after a sync
-    hx = [to_torch(batches[i][0], w.dtype).pin_memory() for i in range(nh)]
-    hy = [[to_torch(batches[i][1][ly.name], w.dtype).pin_memory() for ly in w.layers] for i in range(nh)]
-    hid = [batches[i][2] for i in range(nh)]                       # adapter id per token (-1: base)
-    hidx = [torch.empty(T_TOKENS, dtype=torch.int32).pin_memory() for _ in range(nh)]
-    # two sets of device staging buffers, alternated: one call's copies in
-    # overlap the previous call's apply and copies back
-    xd = [torch.empty((T_TOKENS, D), dtype=torch.bfloat16, device=dev) for _ in range(2)]
-    yd = [[torch.empty((T_TOKENS, D), dtype=torch.bfloat16, device=dev) for _ in w.layers] for _ in range(2)]
-    idd = [torch.empty(T_TOKENS, dtype=torch.int32, device=dev) for _ in range(2)]
     lib = B.load()
     import ctypes
+    # One pinned block per host set and one device block per staging set, each
+    # laid out idx | x | y_q | y_v, so the library copies each way in one piece.
+    off_x = T_TOKENS * 4
+    off_y = [off_x + T_TOKENS * D * 2 * (1 + li) for li in range(len(w.layers))]
+    blk = off_y[-1] + T_TOKENS * D * 2
+
+    def views(buf):
+        idx = buf[:off_x].view(torch.int32)
+        x = buf[off_x:off_x + T_TOKENS * D * 2].view(torch.bfloat16).view(T_TOKENS, D)
+        ys = [buf[o:o + T_TOKENS * D * 2].view(torch.bfloat16).view(T_TOKENS, D) for o in off_y]
+        return idx, x, ys
+
+    hblk = [torch.empty(blk, dtype=torch.uint8).pin_memory() for _ in range(nh)]
+    hv = [views(hb) for hb in hblk]
+    for i in range(nh):
+        hv[i][1].copy_(to_torch(batches[i][0], w.dtype))
+        for li, ly in enumerate(w.layers):
+            hv[i][2][li].copy_(to_torch(batches[i][1][ly.name], w.dtype))
+    # two device staging sets, alternated: one call's copies in overlap the
+    # previous call's apply and copies back
+    dblk = [torch.empty(blk, dtype=torch.uint8, device=dev) for _ in range(2)]
+    dv = [views(db) for db in dblk]
     lay = (ctypes.c_int * 2)(0, 1)
-    xs_dev = [B._vp_array([xd[k].data_ptr(), xd[k].data_ptr()]) for k in range(2)]
-    ys_dev = [B._vp_array([t.data_ptr() for t in yd[k]]) for k in range(2)]
-    host_x = [B._vp_array([h.data_ptr(), h.data_ptr()]) for h in hx]
-    host_y = [B._vp_array([t.data_ptr() for t in hy[i]]) for i in range(nh)]
-    slot_of = np.full(N_SLOTS, -1, np.int32)
-    distinct = [np.unique(h[h >= 0]) for h in hid]
-    act = [int((h >= 0).sum()) for h in hid]
+    xs_dev = [B._vp_array([dv[k][1].data_ptr()] * 2) for k in range(2)]
+    ys_dev = [B._vp_array([t.data_ptr() for t in dv[k][2]]) for k in range(2)]
+    host_x = [B._vp_array([hv[i][1].data_ptr()] * 2) for i in range(nh)]
+    host_y = [B._vp_array([t.data_ptr() for t in hv[i][2]]) for i in range(nh)]
+    idx_h = [ctypes.cast(hv[i][0].data_ptr(), ctypes.POINTER(ctypes.c_int)) for i in range(nh)]
+    idx_hp = [hv[i][0].data_ptr() for i in range(nh)]
+    idx_dp = [dv[k][0].data_ptr() for k in range(2)]
+    # the adapter of every token (base-only: the no-adapter id) and its rank
+    ids_np = [np.ascontiguousarray(np.where(batches[i][2] >= 0, batches[i][2], -1).astype(np.int64)
+                                   .astype(np.uint64)) for i in range(nh)]
+    ids_p = [a.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)) for a in ids_np]
+    ranks_np = np.full(T_TOKENS, RANK, np.int32)
+    ranks_p = ranks_np.ctypes.data_as(ctypes.POINTER(ctypes.c_int))
+    dids = np.zeros(N_SLOTS, np.uint64)
+    slots = np.zeros(N_SLOTS, np.int32)
+    need = np.zeros(N_SLOTS, np.int32)
+    evi = np.zeros(N_SLOTS, np.uint64)
+    P = ctypes.POINTER
+    dids_p, slots_p = dids.ctypes.data_as(P(ctypes.c_uint64)), slots.ctypes.data_as(P(ctypes.c_int))
+    need_p, evi_p = need.ctypes.data_as(P(ctypes.c_int)), evi.ctypes.data_as(P(ctypes.c_uint64))
+    nd, ndone = ctypes.c_int(0), ctypes.c_int(0)
+    nd_r, ndone_r = ctypes.byref(nd), ctypes.byref(ndone)
+    act = [int((batches[i][2] >= 0).sum()) for i in range(nh)]
 
     def step(i):
         j = i % nh
-        # admission of the batch's adapters in one call (all hits here), then
-        # the slot id of every token from a lookup table
-        rc, done, slots, need, _ = B.lora_assign_batch(ctx, distinct[j], [RANK] * len(distinct[j]))
-        if rc != 0 or need.any():
+        # admission of the batch's adapters and the slot id of every token, in
+        # one call (all hits here), written straight into the pinned idx block
+        rc = lib.lora_assign_tokens(ctx, T_TOKENS, ids_p[j], ranks_p, 1, idx_h[j], N_SLOTS, dids_p, slots_p,
+                                    need_p, evi_p, nd_r, ndone_r)
+        if rc != 0 or need[:nd.value].any():
             raise RuntimeError("adapter unexpectedly not resident")
-        slot_of[distinct[j]] = slots
-        ids = hid[j]
-        hidx[j].numpy()[:] = np.where(ids >= 0, slot_of[np.maximum(ids, 0)], -1)
         b = i & 1
-        B.check(lib.lora_apply_multi_host(ctx, 2, lay, host_x[j], host_y[j], hidx[j].data_ptr(),
-                                          T_TOKENS, xs_dev[b], ys_dev[b], idd[b].data_ptr()))
-        B.check(B.lora_release_batch(ctx, slots))
+        B.check(lib.lora_apply_multi_host(ctx, 2, lay, host_x[j], host_y[j], idx_hp[j], T_TOKENS,
+                                          xs_dev[b], ys_dev[b], idx_dp[b]))
+        B.check(lib.lora_release_batch(ctx, nd.value, slots_p))
         return act[j]
 
     for i in range(max(3, args.warmup)):

@@ -41,6 +41,9 @@ extern "C" {
 
 typedef struct lora_ctx lora_ctx;
 
+/* Adapter id meaning "base model only" in lora_assign_tokens (never bound). */
+#define LORA_NO_ADAPTER UINT64_MAX
+
 enum lora_status {
     LORA_OK = 0,
     LORA_ERR_ARG = -1,      /* bad pointer, size, index or layout */
@@ -156,8 +159,11 @@ int lora_apply_multi(lora_ctx *ctx, int n, const int *layers, const void *const 
  * back of the last call that used it; the apply and the copies back run on the
  * compute stream. A caller that alternates two sets of device buffers thus
  * overlaps one call's copies in with the previous call's work; reusing one set
- * is also correct (the calls then serialise). Under stream capture, or with
- * more than 64 distinct device buffers seen, everything runs on the compute
+ * is also correct (the calls then serialise). Copies that continue one another
+ * in both host and device memory, in the order idx, then per layer x (once per
+ * distinct input) and y, are merged: a caller that packs idx | x | y_0 | y_1 ...
+ * back to back in one pinned block and one device block gets one copy in and
+ * one copy back per call. Under stream capture everything runs on the compute
  * stream. Returns after queuing; synchronise the compute stream before reading
  * ys_host or reusing a host buffer. Host buffers should be pinned.
  */
@@ -194,6 +200,26 @@ int lora_assign(lora_ctx *ctx, uint64_t adapter_id, int rank, int *slot,
  */
 int lora_assign_batch(lora_ctx *ctx, int n, const uint64_t *adapter_ids, const int *ranks, int acquire,
                       int *slots, int *needs_load, uint64_t *evicted_ids, int *n_done);
+
+/*
+ * Admission for one batch given per token: adapter_ids[t] is the adapter of
+ * token t (LORA_NO_ADAPTER: base model only) and ranks[t] its rank (read where
+ * the adapter first appears). The distinct adapters, in order of first
+ * appearance, go through lora_assign_batch exactly (same decisions, same
+ * acquire); their ids, slots, load flags and evicted ids are written to
+ * distinct_ids / slots / needs_load / evicted_ids[max_distinct], and
+ * *n_distinct = their number. token_slot_idx[T] (host memory; may be the
+ * pinned buffer handed to lora_apply_multi_host) receives each token's slot,
+ * -1 for base tokens and for tokens whose adapter was not admitted. More than
+ * max_distinct adapters: LORA_ERR_ARG before any admission (table unchanged).
+ * Otherwise returns the first failed admission's status (LORA_ERR_RANK,
+ * LORA_ERR_NO_SLOT), with *n_done = adapters admitted (their effects stay).
+ * This is the slot lookup of a serving step (touch on hit, bind on miss;
+ * section 核心原理 of the "Multi-LoRA 适配器缓存生产实战" page) done in one call.
+ */
+int lora_assign_tokens(lora_ctx *ctx, int n_tokens, const uint64_t *adapter_ids, const int *ranks,
+                       int acquire, int32_t *token_slot_idx, int max_distinct, uint64_t *distinct_ids,
+                       int *slots, int *needs_load, uint64_t *evicted_ids, int *n_distinct, int *n_done);
 
 /* lora_release on each of slots[n] in order; stops at the first slot not in flight (LORA_ERR_STATE). */
 int lora_release_batch(lora_ctx *ctx, int n, const int *slots);

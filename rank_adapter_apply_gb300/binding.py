@@ -34,7 +34,7 @@ EXPORTED = [
     "lora_last_error", "lora_apply_static_scratch", "lora_pin", "lora_set_min_residency",
     "lora_set_policy", "lora_set_keep_score_weights", "lora_set_adapter_priority",
     "lora_set_slot_tracking", "lora_load_slots", "lora_assign_batch", "lora_release_batch",
-    "lora_selftest_wait_timeout",
+    "lora_selftest_wait_timeout", "lora_assign_tokens",
 ]
 
 
@@ -96,6 +96,8 @@ def load(path: str = LIB_PATH):
         "lora_selftest_wait_timeout": (i32, [vp, P(i32)]),
         "lora_assign_batch": (i32, [vp, i32, P(u64), P(i32), i32, P(i32), P(i32), P(u64), P(i32)]),
         "lora_release_batch": (i32, [vp, i32, P(i32)]),
+        "lora_assign_tokens": (i32, [vp, i32, P(u64), P(i32), i32, P(i32), i32, P(u64), P(i32), P(i32), P(u64),
+                                     P(i32), P(i32)]),
         "lora_load_slots": (i32, [vp, i32, P(i32), P(vp), P(vp), P(i32), P(ctypes.c_float)]),
         "lora_set_min_residency": (i32, [vp, i32]),
         "lora_set_policy": (i32, [vp, i32]),
@@ -220,6 +222,33 @@ def lora_assign_batch(ctx, ids, ranks, acquire=True):
                                   ev.ctypes.data_as(P(ctypes.c_uint64)), ctypes.byref(done))
     evi = np.where(ev == np.uint64(NO_ID), -1, ev.astype(np.int64))
     return rc, done.value, slots, need, evi
+
+
+def lora_assign_tokens(ctx, adapter_ids, ranks, acquire=True, max_distinct=None):
+    """Per-token admission. adapter_ids: int64 per token (-1 = base model only),
+    ranks: per token. Returns (status, token_slot_idx int32[T], distinct ids,
+    slots, needs_load, evicted ids (-1: none), n_done) as numpy arrays."""
+    import numpy as np
+    ids = np.asarray(adapter_ids, dtype=np.int64)
+    T = ids.shape[0]
+    ida = np.ascontiguousarray(np.where(ids < 0, np.uint64(NO_ID), ids.astype(np.uint64)))
+    rka = np.ascontiguousarray(np.asarray(ranks, dtype=np.int32))
+    m = T if max_distinct is None else int(max_distinct)
+    tsi = np.full(T, -1, np.int32)
+    dids = np.zeros(max(m, 1), np.uint64)
+    slots = np.full(max(m, 1), -1, np.int32)
+    need = np.zeros(max(m, 1), np.int32)
+    ev = np.zeros(max(m, 1), np.uint64)
+    nd, done = ctypes.c_int(0), ctypes.c_int(0)
+    P = ctypes.POINTER
+    rc = load().lora_assign_tokens(ctx, T, ida.ctypes.data_as(P(ctypes.c_uint64)), rka.ctypes.data_as(P(ctypes.c_int)),
+                                   1 if acquire else 0, tsi.ctypes.data_as(P(ctypes.c_int)), m,
+                                   dids.ctypes.data_as(P(ctypes.c_uint64)), slots.ctypes.data_as(P(ctypes.c_int)),
+                                   need.ctypes.data_as(P(ctypes.c_int)), ev.ctypes.data_as(P(ctypes.c_uint64)),
+                                   ctypes.byref(nd), ctypes.byref(done))
+    k = nd.value
+    evi = np.where(ev[:k] == np.uint64(NO_ID), -1, ev[:k].astype(np.int64))
+    return rc, tsi, dids[:k].astype(np.int64), slots[:k], need[:k], evi, done.value
 
 
 def lora_release_batch(ctx, slots):

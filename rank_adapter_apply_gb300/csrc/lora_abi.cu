@@ -90,11 +90,17 @@ struct lora_ctx {
     std::vector<cudaEvent_t> ring;
     std::vector<int64_t> slot_gen;
     int64_t n_apply = 0;
-    // Host-buffer path: the last use of each device staging buffer (recorded on
-    // the compute stream after that call's copies back), and this call's
-    // host-to-device copies (on the upload stream).
-    std::vector<std::pair<const void *, cudaEvent_t>> buf_ev;
+    // Host-buffer path: call k records host_ev[k % kHostRing] on the compute
+    // stream after its copies back; buf_use maps each device staging buffer to
+    // the last call that used it; h2d_done marks a call's copies in (upload
+    // stream).
+    std::vector<cudaEvent_t> host_ev;
+    std::vector<std::pair<const void *, int64_t>> buf_use;
+    int64_t n_host = 0, host_forgot = -1;
     cudaEvent_t h2d_done = nullptr;
+    // lora_assign_tokens: open-addressing table adapter id -> distinct index
+    std::vector<uint64_t> tok_key;
+    std::vector<int> tok_val, tok_rank;
 
     lora_ctx(int S_, int R_) : table(S_, R_) {}
 };
@@ -155,6 +161,32 @@ bool capturing(cudaStream_t s) {
     cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(s, &st) != cudaSuccess) return false;
     return st != cudaStreamCaptureStatusNone;
+}
+
+constexpr int kHostRing = 8;
+
+struct Copy {
+    void *dst;
+    const void *src;
+    size_t bytes;
+};
+
+// Joins copies that continue one another in both address spaces (in the
+// order given; the first copy of a run keeps its place).
+std::vector<Copy> merge_copies(const std::vector<Copy> &cs) {
+    std::vector<Copy> out;
+    for (const Copy &c : cs) {
+        if (!out.empty()) {
+            Copy &p = out.back();
+            if (static_cast<const char *>(p.src) + p.bytes == c.src &&
+                static_cast<char *>(p.dst) + p.bytes == c.dst) {
+                p.bytes += c.bytes;
+                continue;
+            }
+        }
+        out.push_back(c);
+    }
+    return out;
 }
 
 }  // namespace
@@ -269,8 +301,8 @@ void lora_destroy(lora_ctx *c) {
         if (c->compute_done) cudaEventDestroy(c->compute_done);
         for (auto ev : c->ring)
             if (ev) cudaEventDestroy(ev);
-        for (auto &be : c->buf_ev)
-            if (be.second) cudaEventDestroy(be.second);
+        for (auto ev : c->host_ev)
+            if (ev) cudaEventDestroy(ev);
         if (c->h2d_done) cudaEventDestroy(c->h2d_done);
     }
     delete c;
@@ -612,58 +644,87 @@ int lora_apply_multi_host(lora_ctx *c, int n, const int *layers, const void *con
     }
     std::sort(bufs.begin(), bufs.end());
     bufs.erase(std::unique(bufs.begin(), bufs.end()), bufs.end());
-    // Copies in on the upload stream, each buffer after the last call that used
-    // it: a caller alternating buffer sets overlaps one call's copies in with
-    // the previous call's apply and copies back. Under stream capture, or with
-    // too many distinct buffers to track, everything stays on the compute stream.
-    constexpr size_t kMaxTracked = 64;
-    bool split = !capturing(c->compute);
-    if (split && !c->h2d_done) CUDA_TRY(cudaEventCreateWithFlags(&c->h2d_done, cudaEventDisableTiming));
-    if (split) {
-        size_t fresh = 0;
-        for (const void *b : bufs) {
-            bool known = false;
-            for (auto &be : c->buf_ev) known = known || be.first == b;
-            fresh += known ? 0 : 1;
-        }
-        split = c->buf_ev.size() + fresh <= kMaxTracked;
-    }
-    cudaStream_t in = split ? c->upload : c->compute;
-    if (split)
-        for (auto &be : c->buf_ev)
-            if (std::binary_search(bufs.begin(), bufs.end(), be.first))
-                CUDA_TRY(cudaStreamWaitEvent(c->upload, be.second, 0));
-    CUDA_TRY(cudaMemcpyAsync(idx_dev, idx_host, sizeof(int32_t) * T, cudaMemcpyHostToDevice, in));
+    // Copies in, then copies back; a copy that continues the previous one in
+    // both host and device memory joins it (a caller that packs its staging
+    // buffers back to back gets one copy each way).
+    std::vector<Copy> in_copies{{idx_dev, idx_host, sizeof(int32_t) * (size_t)T}};
     for (int i = 0; i < n; ++i) {
         const lora_layer_desc &L = c->layers[layers[i]];
         bool dup = false;                          // layers sharing one input copy it once
         for (int j = 0; j < i; ++j) dup = dup || (xs_host[j] == xs_host[i] && xs_dev[j] == xs_dev[i]);
-        if (!dup)
-            CUDA_TRY(cudaMemcpyAsync(xs_dev[i], xs_host[i], (size_t)T * L.d_in * e, cudaMemcpyHostToDevice, in));
-        CUDA_TRY(cudaMemcpyAsync(ys_dev[i], ys_host[i], (size_t)T * L.d_out * e, cudaMemcpyHostToDevice, in));
+        if (!dup) in_copies.push_back({xs_dev[i], xs_host[i], (size_t)T * L.d_in * e});
+        in_copies.push_back({ys_dev[i], ys_host[i], (size_t)T * L.d_out * e});
     }
+    std::vector<Copy> out_copies;
+    for (int i = 0; i < n; ++i) {
+        const lora_layer_desc &L = c->layers[layers[i]];
+        out_copies.push_back({ys_host[i], ys_dev[i], (size_t)T * L.d_out * e});
+    }
+    in_copies = merge_copies(in_copies);
+    out_copies = merge_copies(out_copies);
+    // Copies in run on the upload stream, after the copies back of the last
+    // call that used any of this call's device buffers: a caller alternating
+    // buffer sets overlaps one call's copies in with the previous call's apply
+    // and copies back. Under stream capture everything stays on the compute
+    // stream.
+    const bool split = !capturing(c->compute);
+    if (split && !c->h2d_done) CUDA_TRY(cudaEventCreateWithFlags(&c->h2d_done, cudaEventDisableTiming));
+    if (split && c->host_ev.empty()) {
+        c->host_ev.assign(kHostRing, nullptr);
+        for (auto &ev : c->host_ev) CUDA_TRY(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+    }
+    cudaStream_t in = split ? c->upload : c->compute;
+    if (split) {
+        // Newest earlier use of any of these buffers. A ring event re-recorded
+        // by a later call only lengthens the wait: every call records on the
+        // compute stream, in call order.
+        int64_t last = -1;
+        for (const void *b : bufs) {
+            bool found = false;
+            for (auto &bu : c->buf_use)
+                if (bu.first == b) {
+                    last = std::max(last, bu.second);
+                    found = true;
+                }
+            if (!found) last = std::max(last, c->host_forgot);   // maybe a forgotten buffer
+        }
+        if (last >= 0) CUDA_TRY(cudaStreamWaitEvent(c->upload, c->host_ev[last % kHostRing], 0));
+    }
+    for (const Copy &cp : in_copies)
+        CUDA_TRY(cudaMemcpyAsync(cp.dst, cp.src, cp.bytes, cudaMemcpyHostToDevice, in));
     if (split) {
         CUDA_TRY(cudaEventRecord(c->h2d_done, c->upload));
         CUDA_TRY(cudaStreamWaitEvent(c->compute, c->h2d_done, 0));
     }
     int rc = apply_impl(c, n, layers, xs_dev, ys_dev, idx_dev, T);
     if (rc != LORA_OK) return rc;
-    for (int i = 0; i < n; ++i) {
-        const lora_layer_desc &L = c->layers[layers[i]];
-        CUDA_TRY(cudaMemcpyAsync(ys_host[i], ys_dev[i], (size_t)T * L.d_out * e,
-                                 cudaMemcpyDeviceToHost, c->compute));
-    }
-    if (split)
+    for (const Copy &cp : out_copies)
+        CUDA_TRY(cudaMemcpyAsync(cp.dst, cp.src, cp.bytes, cudaMemcpyDeviceToHost, c->compute));
+    if (split) {
+        const int64_t k = c->n_host++;
+        CUDA_TRY(cudaEventRecord(c->host_ev[k % kHostRing], c->compute));
         for (const void *b : bufs) {
-            cudaEvent_t ev = nullptr;
-            for (auto &be : c->buf_ev)
-                if (be.first == b) ev = be.second;
-            if (!ev) {
-                CUDA_TRY(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
-                c->buf_ev.emplace_back(b, ev);
-            }
-            CUDA_TRY(cudaEventRecord(ev, c->compute));
+            bool found = false;
+            for (auto &bu : c->buf_use)
+                if (bu.first == b) {
+                    bu.second = k;
+                    found = true;
+                }
+            if (!found) c->buf_use.emplace_back(b, k);
         }
+        // Keep the list short: forget buffers not used for a whole ring and
+        // remember the newest call forgotten; a buffer not on the list then
+        // waits for that call (or a later one), which covers its last use.
+        if (c->buf_use.size() > 64) {
+            for (auto &bu : c->buf_use)
+                if (bu.second + kHostRing <= k) c->host_forgot = std::max(c->host_forgot, bu.second);
+            c->buf_use.erase(std::remove_if(c->buf_use.begin(), c->buf_use.end(),
+                                            [&](const std::pair<const void *, int64_t> &bu) {
+                                                return bu.second + kHostRing <= k;
+                                            }),
+                             c->buf_use.end());
+        }
+    }
     return LORA_OK;
 }
 
@@ -704,6 +765,72 @@ int lora_assign_batch(lora_ctx *c, int n, const uint64_t *ids, const int *ranks,
         *n_done = i + 1;
     }
     return LORA_OK;
+}
+
+int lora_assign_tokens(lora_ctx *c, int T, const uint64_t *adapter_ids, const int *ranks, int acquire,
+                       int32_t *token_slot_idx, int max_distinct, uint64_t *distinct_ids, int *slots,
+                       int *needs_load, uint64_t *evicted_ids, int *n_distinct, int *n_done) {
+    if (!c || !n_distinct || !n_done) return fail(LORA_ERR_ARG, "NULL argument");
+    *n_distinct = 0;
+    *n_done = 0;
+    if (T < 0 || max_distinct < 0) return fail(LORA_ERR_ARG, "negative size");
+    if (T == 0) return LORA_OK;
+    if (!adapter_ids || !ranks || !token_slot_idx ||
+        (max_distinct > 0 && (!distinct_ids || !slots || !needs_load || !evicted_ids)))
+        return fail(LORA_ERR_ARG, "NULL argument");
+    // Distinct adapters in order of first appearance (open addressing on the
+    // id); until the slots are known token_slot_idx holds each token's index
+    // among them.
+    size_t cap = 16;
+    while (cap < 2 * (size_t)T) cap <<= 1;
+    if (c->tok_key.size() < cap) {
+        c->tok_key.resize(cap);
+        c->tok_val.resize(cap);
+    }
+    std::fill(c->tok_key.begin(), c->tok_key.begin() + cap, LORA_NO_ADAPTER);
+    const size_t mask = cap - 1;
+    std::vector<int> &first_rank = c->tok_rank;
+    first_rank.clear();
+    for (int t = 0; t < T; ++t) {
+        const uint64_t id = adapter_ids[t];
+        if (id == LORA_NO_ADAPTER) {
+            token_slot_idx[t] = -1;
+            continue;
+        }
+        size_t h = (size_t)((id * 0x9E3779B97F4A7C15ull) >> 17) & mask;
+        while (c->tok_key[h] != LORA_NO_ADAPTER && c->tok_key[h] != id) h = (h + 1) & mask;
+        if (c->tok_key[h] == LORA_NO_ADAPTER) {
+            const int nd = (int)first_rank.size();
+            if (nd == max_distinct) {        // nothing admitted: the table is unchanged
+                for (int u = 0; u < T; ++u) token_slot_idx[u] = -1;
+                return fail(LORA_ERR_ARG, "more than max_distinct (%d) adapters in the batch", max_distinct);
+            }
+            c->tok_key[h] = id;
+            c->tok_val[h] = nd;
+            distinct_ids[nd] = id;
+            first_rank.push_back(ranks[t]);
+        }
+        token_slot_idx[t] = c->tok_val[h];
+    }
+    const int nd = (int)first_rank.size();
+    *n_distinct = nd;
+    for (int i = 0; i < nd; ++i) {
+        slots[i] = -1;
+        needs_load[i] = 0;
+        evicted_ids[i] = LORA_NO_ADAPTER;
+    }
+    int rc = LORA_OK;
+    for (int i = 0; i < nd; ++i) {           // lora_assign_batch over the distinct list
+        rc = lora_assign(c, distinct_ids[i], first_rank[i], &slots[i], &needs_load[i], &evicted_ids[i]);
+        if (rc != LORA_OK) break;
+        if (acquire) c->table.acquire(slots[i]);
+        *n_done = i + 1;
+    }
+    for (int t = 0; t < T; ++t) {
+        const int i = token_slot_idx[t];
+        if (i >= 0) token_slot_idx[t] = i < *n_done ? slots[i] : -1;
+    }
+    return rc;
 }
 
 int lora_release_batch(lora_ctx *c, int n, const int *slots) {

@@ -266,6 +266,61 @@ def test_assign_batch_equals_sequential_calls(lib):
         B.lora_destroy(ctx)
 
 
+def test_assign_tokens_matches_simulator_and_maps_tokens(lib):
+    """lora_assign_tokens admits the batch's distinct adapters in order of first
+    appearance with the simulator's decisions, and maps every token to its
+    adapter's slot (-1 for base-only tokens)."""
+    rng = np.random.default_rng(11)
+    S, R = 6, 16
+    ctx = _host_ctx(S, R)
+    sim = LruSlotSim(S, R)
+    try:
+        for step in range(150):
+            T = int(rng.integers(1, 40))
+            ids = rng.integers(0, 25, size=T).astype(np.int64)
+            ids[rng.random(T) < 0.15] = -1
+            # at most S distinct adapters, so every admission succeeds (all in flight)
+            keep = list(dict.fromkeys(int(a) for a in ids if a >= 0))[:S]
+            ids = np.where(np.isin(ids, keep), ids, -1)
+            rank_of = {a: int(rng.choice([8, 16])) for a in keep}
+            ranks = np.array([rank_of.get(int(a), 0) for a in ids], np.int32)
+            rc, tsi, dids, slots, need, ev, done = B.lora_assign_tokens(ctx, ids, ranks, max_distinct=S)
+            assert rc == 0 and done == len(keep)
+            assert list(dids) == keep
+            for a, s_, n_, e_ in zip(keep, slots, need, ev):
+                assert sim.assign(a, rank_of[a]) == (0, int(s_), int(n_), int(e_))
+                assert sim.acquire(int(s_)) == 0
+            slot_of = dict(zip(keep, (int(x) for x in slots)))
+            expect = np.array([slot_of[int(a)] if a >= 0 else -1 for a in ids], np.int32)
+            assert np.array_equal(tsi, expect)
+            assert B.lora_release_batch(ctx, slots) == 0
+            for s_ in slots:
+                sim.release(int(s_))
+            B.lora_tick(ctx)
+            sim.tick()
+        # a failing admission stops the batch: its tokens and later ones map to -1
+        ids = np.array([2001, -1, 2002, 2001, 2003, 2002], np.int64)
+        ranks = np.array([8, 0, 8, 8, 99, 8], np.int32)
+        rc, tsi, dids, slots, need, ev, done = B.lora_assign_tokens(ctx, ids, ranks)
+        assert rc == B.LORA_ERR_RANK and done == 2 and list(dids) == [2001, 2002, 2003]
+        assert list(tsi) == [slots[0], -1, slots[1], slots[0], -1, slots[1]]
+        assert B.lora_release_batch(ctx, slots[:2]) == 0
+        # more distinct adapters than max_distinct: rejected before any admission
+        before = [B.lora_lookup(ctx, a) for a in (2001, 2002)]
+        rc, tsi, dids, slots, need, ev, done = B.lora_assign_tokens(ctx, [3001, 3002, 3003], [8, 8, 8],
+                                                                     max_distinct=2)
+        assert rc == B.LORA_ERR_ARG and done == 0 and list(tsi) == [-1, -1, -1]
+        assert B.lora_lookup(ctx, 3001) == -1
+        assert [B.lora_lookup(ctx, a) for a in (2001, 2002)] == before
+        # all base-only, and an empty batch
+        rc, tsi, dids, slots, need, ev, done = B.lora_assign_tokens(ctx, [-1, -1], [0, 0])
+        assert rc == 0 and done == 0 and len(dids) == 0 and list(tsi) == [-1, -1]
+        rc, tsi, dids, slots, need, ev, done = B.lora_assign_tokens(ctx, np.zeros(0, np.int64), [])
+        assert rc == 0 and len(tsi) == 0
+    finally:
+        B.lora_destroy(ctx)
+
+
 def test_selftest_needs_a_device_context(lib):
     ctx = _host_ctx(2, 16)
     try:

@@ -328,12 +328,28 @@ def test_batched_upload_rejects_bad_arguments():
         sl.close()
 
 
+def _packed_bytes(T, d, dv):
+    return T * 4 + T * d * 2 * 2 + T * dv * 2
+
+
+def _packed_views(buf, T, d, dv):
+    """idx | x | y_q | y_v back to back in one byte buffer."""
+    import torch
+    o1, o2 = T * 4, T * 4 + T * d * 2
+    o3 = o2 + T * d * 2
+    return (buf[:o1].view(torch.int32), buf[o1:o2].view(torch.bfloat16).view(T, d),
+            [buf[o2:o3].view(torch.bfloat16).view(T, d), buf[o3:o3 + T * dv * 2].view(torch.bfloat16).view(T, dv)])
+
+
+@pytest.mark.parametrize("packed", [False, True])
 @pytest.mark.parametrize("device_sets", [1, 2])
-def test_host_buffer_path_matches_oracle(device_sets):
+def test_host_buffer_path_matches_oracle(device_sets, packed):
     """lora_apply_multi_host, several calls queued back to back: copies in on
     the upload stream ordered per device buffer, apply and copies back on the
     compute stream. With one device buffer set the calls serialise, with two
-    they overlap; every call's result equals the oracle's."""
+    they overlap; with packed buffers (idx | x | y_q | y_v back to back on both
+    sides) the copies each way are merged into one. Every call's result equals
+    the oracle's."""
     import torch
     from rank_adapter_apply_gb300 import binding as B
     from rank_adapter_apply_gb300.harness import to_torch
@@ -356,14 +372,29 @@ def test_host_buffer_path_matches_oracle(device_sets):
             ys = {"q": wl._mat(rng, (T, d), "normal", 1.0, wl.DTYPE_BF16),
                   "v": wl._mat(rng, (T, dv), "normal", 1.0, wl.DTYPE_BF16)}
             idx = rng.integers(-1, S, size=T).astype(np.int32)
-            hx = to_torch(x, wl.DTYPE_BF16).pin_memory()
-            hy = [to_torch(ys[n], wl.DTYPE_BF16).clone().pin_memory() for n in ("q", "v")]
-            hidx = torch.from_numpy(idx).pin_memory()
+            if packed:
+                hidx, hx, hy = _packed_views(torch.empty(_packed_bytes(T, d, dv), dtype=torch.uint8).pin_memory(),
+                                             T, d, dv)
+                hidx.copy_(torch.from_numpy(idx))
+                hx.copy_(to_torch(x, wl.DTYPE_BF16))
+                for t, n in zip(hy, ("q", "v")):
+                    t.copy_(to_torch(ys[n], wl.DTYPE_BF16))
+            else:
+                hx = to_torch(x, wl.DTYPE_BF16).pin_memory()
+                hy = [to_torch(ys[n], wl.DTYPE_BF16).clone().pin_memory() for n in ("q", "v")]
+                hidx = torch.from_numpy(idx).pin_memory()
             batches.append((x, ys, idx, hx, hy, hidx))
-        dev_sets = [(torch.empty((T, d), dtype=torch.bfloat16, device="cuda:0"),
-                     [torch.empty((T, d), dtype=torch.bfloat16, device="cuda:0"),
-                      torch.empty((T, dv), dtype=torch.bfloat16, device="cuda:0")],
-                     torch.empty(T, dtype=torch.int32, device="cuda:0")) for _ in range(device_sets)]
+        if packed:
+            dev_sets = []
+            for _ in range(device_sets):
+                di, dx, dy = _packed_views(torch.empty(_packed_bytes(T, d, dv), dtype=torch.uint8, device="cuda:0"),
+                                           T, d, dv)
+                dev_sets.append((dx, dy, di))
+        else:
+            dev_sets = [(torch.empty((T, d), dtype=torch.bfloat16, device="cuda:0"),
+                         [torch.empty((T, d), dtype=torch.bfloat16, device="cuda:0"),
+                          torch.empty((T, dv), dtype=torch.bfloat16, device="cuda:0")],
+                         torch.empty(T, dtype=torch.int32, device="cuda:0")) for _ in range(device_sets)]
         for k, (_, _, _, hx, hy, hidx) in enumerate(batches):
             xd, yd, idd = dev_sets[k % device_sets]
             B.lora_apply_multi_host(sl.ctx, [0, 1], [hx.data_ptr()] * 2, [t.data_ptr() for t in hy],
