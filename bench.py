@@ -44,6 +44,7 @@ METRIC = "LoRA-delta tokens/s per layer set; achieved HBM GB/s and % roofline (1
 UNIT = "delta-tokens/s"
 WORKLOAD = "decode_qv_4096"
 T_TOKENS, N_SLOTS, RANK, ALPHA, D = 256, 8, 16, 32.0, 4096
+E2E_HOST_SETS, E2E_STAGING_SETS = 32, 3     # e2e: pinned host sets (a sync per cycle), device staging sets
 
 
 def peaks():
@@ -457,7 +458,8 @@ def run_e2e(args, w, batches, d0, stream, dev, world):
     from rank_adapter_apply_gb300.harness import to_torch
 
     ctx = d0.slots.ctx
-    nh = min(16, len(batches))                 # host buffer sets, reused after a sync
+    nh = min(E2E_HOST_SETS, len(batches))      # host buffer sets, reused after a sync
+    nd_sets = E2E_STAGING_SETS
     lib = B.load()
     import ctypes
     # One pinned block per host set and one device block per staging set, each
@@ -478,18 +480,18 @@ def run_e2e(args, w, batches, d0, stream, dev, world):
         hv[i][1].copy_(to_torch(batches[i][0], w.dtype))
         for li, ly in enumerate(w.layers):
             hv[i][2][li].copy_(to_torch(batches[i][1][ly.name], w.dtype))
-    # two device staging sets, alternated: one call's copies in overlap the
+    # device staging sets, rotated: one call's copies in overlap the
     # previous call's apply and copies back
-    dblk = [torch.empty(blk, dtype=torch.uint8, device=dev) for _ in range(2)]
+    dblk = [torch.empty(blk, dtype=torch.uint8, device=dev) for _ in range(nd_sets)]
     dv = [views(db) for db in dblk]
     lay = (ctypes.c_int * 2)(0, 1)
-    xs_dev = [B._vp_array([dv[k][1].data_ptr()] * 2) for k in range(2)]
-    ys_dev = [B._vp_array([t.data_ptr() for t in dv[k][2]]) for k in range(2)]
+    xs_dev = [B._vp_array([dv[k][1].data_ptr()] * 2) for k in range(nd_sets)]
+    ys_dev = [B._vp_array([t.data_ptr() for t in dv[k][2]]) for k in range(nd_sets)]
     host_x = [B._vp_array([hv[i][1].data_ptr()] * 2) for i in range(nh)]
     host_y = [B._vp_array([t.data_ptr() for t in hv[i][2]]) for i in range(nh)]
     idx_h = [ctypes.cast(hv[i][0].data_ptr(), ctypes.POINTER(ctypes.c_int)) for i in range(nh)]
     idx_hp = [hv[i][0].data_ptr() for i in range(nh)]
-    idx_dp = [dv[k][0].data_ptr() for k in range(2)]
+    idx_dp = [dv[k][0].data_ptr() for k in range(nd_sets)]
     # the adapter of every token (base-only: the no-adapter id) and its rank
     ids_np = [np.ascontiguousarray(np.where(batches[i][2] >= 0, batches[i][2], -1).astype(np.int64)
                                    .astype(np.uint64)) for i in range(nh)]
@@ -515,7 +517,7 @@ def run_e2e(args, w, batches, d0, stream, dev, world):
                                     need_p, evi_p, nd_r, ndone_r)
         if rc != 0 or need[:nd.value].any():
             raise RuntimeError("adapter unexpectedly not resident")
-        b = i & 1
+        b = i % nd_sets
         B.check(lib.lora_apply_multi_host(ctx, 2, lay, host_x[j], host_y[j], idx_hp[j], T_TOKENS,
                                           xs_dev[b], ys_dev[b], idx_dp[b]))
         B.check(lib.lora_release_batch(ctx, nd.value, slots_p))
@@ -523,24 +525,59 @@ def run_e2e(args, w, batches, d0, stream, dev, world):
 
     for i in range(max(3, args.warmup)):
         step(i)
-    stream.synchronize()
+    B.check(lib.lora_sync_host(ctx))
     k = min(args.steps, 20000)
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
     toks = 0
     for i in range(k):
         if i % nh == 0 and i > 0:
-            stream.synchronize()          # host buffers of a set are reused every nh steps
+            B.check(lib.lora_sync_host(ctx))   # host buffers of a set are reused every nh steps
         toks += step(i)
-    stream.synchronize()
+    B.check(lib.lora_sync_host(ctx))
     el = time.perf_counter() - t0
     el_ms, job_toks = reduce_over_ranks(el * 1e3, toks, dev)
     el = el_ms * 1e-3
     h2d = T_TOKENS * D * 2 + 2 * T_TOKENS * D * 2 + T_TOKENS * 4
     d2h = 2 * T_TOKENS * D * 2
+    floor = link_floor(hblk, dblk, blk - off_y[0], off_y[0], dev)
     return {"value": job_toks / el, "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": k,
+            "d2h_bytes_per_step": d2h, "steps": k, "us_per_step": el / k * 1e6,
+            "link_floor": floor,
             "timing": "wall clock, host admission + H2D + apply + D2H per step"}
+
+
+def link_floor(hblk, dblk, out_bytes, out_off, dev, reps=200):
+    """Time per step of the host link alone: each step's whole block copied in
+    on one stream while the previous step's y bytes are copied back on another,
+    rotating the same pinned host sets and device staging sets as the e2e loop
+    (no kernels, no admission)."""
+    import torch
+    si, so = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    nh, nd = len(hblk), len(dblk)
+    ev = [torch.cuda.Event() for _ in range(nd)]
+
+    def run(n):
+        for i in range(n):
+            b = i % nd
+            with torch.cuda.stream(si):
+                si.wait_event(ev[b])
+                dblk[b].copy_(hblk[i % nh], non_blocking=True)
+            so.wait_stream(si)
+            with torch.cuda.stream(so):
+                hblk[i % nh][out_off:out_off + out_bytes].copy_(dblk[b][out_off:out_off + out_bytes],
+                                                                non_blocking=True)
+                ev[b].record(so)
+    for e in ev:
+        e.record(so)
+    run(10)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    run(reps)
+    torch.cuda.synchronize(dev)
+    us = (time.perf_counter() - t0) / reps * 1e6
+    return {"us_per_step": us, "note": "the step's bytes copied in and out concurrently on two streams, "
+                                       "same buffer rotation, no kernels"}
 
 
 def run_big(args, name):

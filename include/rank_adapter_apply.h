@@ -23,7 +23,7 @@
  *    CUDA events only.
  *  - Streams are passed as cudaStream_t cast to void*. Kernels run on the
  *    compute stream; slot uploads on the upload stream. No call synchronises
- *    the host except lora_sync_uploads and lora_stats.
+ *    the host except lora_sync_uploads, lora_sync_host and lora_stats.
  *  - Layouts are row-major. A pool of layer l: [max_loras][max_lora_rank][d_in];
  *    B pool: [max_loras][d_out][max_lora_rank]; element type = the context's
  *    dtype. Activations x: [n_tokens][d_in]; outputs y: [n_tokens][d_out].
@@ -156,21 +156,28 @@ int lora_apply_multi(lora_ctx *ctx, int n, const int *layers, const void *const 
  * xs_host once each, ys_host, idx_host) to the caller's device staging buffers
  * xs_dev / ys_dev / idx_dev, applies, and copies every y back to ys_host.
  * The copies in run on the upload stream, each device buffer after the copies
- * back of the last call that used it; the apply and the copies back run on the
- * compute stream. A caller that alternates two sets of device buffers thus
- * overlaps one call's copies in with the previous call's work; reusing one set
- * is also correct (the calls then serialise). Copies that continue one another
+ * back of the last call that used it; the apply runs on the compute stream and
+ * the copies back on a download stream the context creates on first use (it
+ * owns and destroys it). A caller rotating two or more sets of device buffers
+ * thus keeps both directions of the host link and the kernels busy at once;
+ * reusing one set is also correct (the calls then serialise). The staging
+ * buffers belong to this path until lora_sync_host returns: other work on them
+ * must not be queued before that. Copies that continue one another
  * in both host and device memory, in the order idx, then per layer x (once per
  * distinct input) and y, are merged: a caller that packs idx | x | y_0 | y_1 ...
  * back to back in one pinned block and one device block gets one copy in and
  * one copy back per call. Under stream capture everything runs on the compute
- * stream. Returns after queuing; synchronise the compute stream before reading
- * ys_host or reusing a host buffer. Host buffers should be pinned.
+ * stream. Returns after queuing; call lora_sync_host before reading ys_host or
+ * reusing a host buffer. Host buffers should be pinned.
  */
 int lora_apply_multi_host(lora_ctx *ctx, int n, const int *layers,
                           const void *const *xs_host, void *const *ys_host,
                           const int32_t *idx_host, int n_tokens,
                           void *const *xs_dev, void *const *ys_dev, int32_t *idx_dev);
+
+/* Blocks until the copies back of every queued lora_apply_multi_host call have
+ * landed in host memory (LORA_OK at once for a host-only context). */
+int lora_sync_host(lora_ctx *ctx);
 
 /*
  * Host slot table (the LRU of the "Multi-LoRA 适配器缓存生产实战" page, section

@@ -34,7 +34,7 @@ EXPORTED = [
     "lora_last_error", "lora_apply_static_scratch", "lora_pin", "lora_set_min_residency",
     "lora_set_policy", "lora_set_keep_score_weights", "lora_set_adapter_priority",
     "lora_set_slot_tracking", "lora_load_slots", "lora_assign_batch", "lora_release_batch",
-    "lora_selftest_wait_timeout", "lora_assign_tokens",
+    "lora_selftest_wait_timeout", "lora_assign_tokens", "lora_sync_host",
 ]
 
 
@@ -107,6 +107,7 @@ def load(path: str = LIB_PATH):
         "lora_set_small_batch_tokens": (i32, [vp, i32]),
         "lora_set_inputs_ready": (i32, [vp, i32]),
         "lora_sync_uploads": (i32, [vp]),
+        "lora_sync_host": (i32, [vp]),
         "lora_stats": (i32, [vp, P(LoraStats)]),
         "lora_adapter_bytes": (u64, [i32, P(i32), P(i32), i32, i32]),
         "lora_last_error": (ctypes.c_char_p, []),
@@ -326,6 +327,10 @@ def lora_set_small_batch_tokens(ctx, n):
 
 def lora_set_inputs_ready(ctx, on):
     return check(load().lora_set_inputs_ready(ctx, 1 if on else 0))
+
+
+def lora_sync_host(ctx):
+    return check(load().lora_sync_host(ctx))
 
 
 def lora_sync_uploads(ctx):

@@ -97,7 +97,8 @@ struct lora_ctx {
     std::vector<cudaEvent_t> host_ev;
     std::vector<std::pair<const void *, int64_t>> buf_use;
     int64_t n_host = 0, host_forgot = -1;
-    cudaEvent_t h2d_done = nullptr;
+    cudaEvent_t h2d_done = nullptr, apply_done = nullptr;
+    cudaStream_t down = nullptr;    // copies back of the host-buffer path (created on first use)
     // lora_assign_tokens: open-addressing table adapter id -> distinct index
     std::vector<uint64_t> tok_key;
     std::vector<int> tok_val, tok_rank;
@@ -301,9 +302,12 @@ void lora_destroy(lora_ctx *c) {
         if (c->compute_done) cudaEventDestroy(c->compute_done);
         for (auto ev : c->ring)
             if (ev) cudaEventDestroy(ev);
+        if (c->down) cudaStreamSynchronize(c->down);
         for (auto ev : c->host_ev)
             if (ev) cudaEventDestroy(ev);
         if (c->h2d_done) cudaEventDestroy(c->h2d_done);
+        if (c->apply_done) cudaEventDestroy(c->apply_done);
+        if (c->down) cudaStreamDestroy(c->down);
     }
     delete c;
 }
@@ -663,12 +667,15 @@ int lora_apply_multi_host(lora_ctx *c, int n, const int *layers, const void *con
     in_copies = merge_copies(in_copies);
     out_copies = merge_copies(out_copies);
     // Copies in run on the upload stream, after the copies back of the last
-    // call that used any of this call's device buffers: a caller alternating
-    // buffer sets overlaps one call's copies in with the previous call's apply
-    // and copies back. Under stream capture everything stays on the compute
-    // stream.
+    // call that used any of this call's device buffers; the apply on the
+    // compute stream; the copies back on the context's own download stream.
+    // A caller rotating two or more buffer sets thus keeps both directions of
+    // the host link and the GPU busy at once. Under stream capture everything
+    // stays on the compute stream.
     const bool split = !capturing(c->compute);
     if (split && !c->h2d_done) CUDA_TRY(cudaEventCreateWithFlags(&c->h2d_done, cudaEventDisableTiming));
+    if (split && !c->apply_done) CUDA_TRY(cudaEventCreateWithFlags(&c->apply_done, cudaEventDisableTiming));
+    if (split && !c->down) CUDA_TRY(cudaStreamCreateWithFlags(&c->down, cudaStreamNonBlocking));
     if (split && c->host_ev.empty()) {
         c->host_ev.assign(kHostRing, nullptr);
         for (auto &ev : c->host_ev) CUDA_TRY(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
@@ -677,7 +684,7 @@ int lora_apply_multi_host(lora_ctx *c, int n, const int *layers, const void *con
     if (split) {
         // Newest earlier use of any of these buffers. A ring event re-recorded
         // by a later call only lengthens the wait: every call records on the
-        // compute stream, in call order.
+        // download stream, in call order.
         int64_t last = -1;
         for (const void *b : bufs) {
             bool found = false;
@@ -698,11 +705,16 @@ int lora_apply_multi_host(lora_ctx *c, int n, const int *layers, const void *con
     }
     int rc = apply_impl(c, n, layers, xs_dev, ys_dev, idx_dev, T);
     if (rc != LORA_OK) return rc;
+    cudaStream_t out = split ? c->down : c->compute;
+    if (split) {
+        CUDA_TRY(cudaEventRecord(c->apply_done, c->compute));
+        CUDA_TRY(cudaStreamWaitEvent(c->down, c->apply_done, 0));
+    }
     for (const Copy &cp : out_copies)
-        CUDA_TRY(cudaMemcpyAsync(cp.dst, cp.src, cp.bytes, cudaMemcpyDeviceToHost, c->compute));
+        CUDA_TRY(cudaMemcpyAsync(cp.dst, cp.src, cp.bytes, cudaMemcpyDeviceToHost, out));
     if (split) {
         const int64_t k = c->n_host++;
-        CUDA_TRY(cudaEventRecord(c->host_ev[k % kHostRing], c->compute));
+        CUDA_TRY(cudaEventRecord(c->host_ev[k % kHostRing], c->down));
         for (const void *b : bufs) {
             bool found = false;
             for (auto &bu : c->buf_use)
@@ -945,6 +957,13 @@ int lora_set_small_batch_tokens(lora_ctx *c, int n) {
 int lora_set_inputs_ready(lora_ctx *c, int on) {
     if (!c) return fail(LORA_ERR_ARG, "ctx is NULL");
     c->inputs_ready = on ? 1 : 0;
+    return LORA_OK;
+}
+
+int lora_sync_host(lora_ctx *c) {
+    if (!c) return fail(LORA_ERR_ARG, "ctx is NULL");
+    if (!c->device) return LORA_OK;
+    CUDA_TRY(cudaStreamSynchronize(c->down ? c->down : c->compute));
     return LORA_OK;
 }
 

@@ -400,7 +400,7 @@ def test_host_buffer_path_matches_oracle(device_sets, packed):
             B.lora_apply_multi_host(sl.ctx, [0, 1], [hx.data_ptr()] * 2, [t.data_ptr() for t in hy],
                                     hidx.data_ptr(), T, [xd.data_ptr()] * 2, [t.data_ptr() for t in yd],
                                     idd.data_ptr())
-        sl.compute.synchronize()
+        B.lora_sync_host(sl.ctx)
         for x, ys, idx, hx, hy, hidx in batches:
             w = wl.Workload("custom", wl.DTYPE_BF16, S, R, layers, idx, {"x": x}, ys, ads, ranks,
                             2.0 * ranks.astype(np.float64))
