@@ -19,6 +19,8 @@ to compare the eviction policies of the section 为什么纯 LRU 在多租户场
 """
 from __future__ import annotations
 
+import ctypes
+
 import time
 from dataclasses import dataclass, field
 
@@ -147,6 +149,27 @@ class ChurnRunner:
         self.idx_host = torch.empty((self.ring, self.max_groups, tokens), dtype=torch.int32).pin_memory()
         self.idx = torch.empty((self.ring, self.max_groups, tokens), dtype=torch.int32, device=self.dev)
         self.step_done = [None] * self.ring
+        # call arguments built once: host pointers of every adapter's A and B
+        # per layer (adapter-major rows), the layer list and x / y pointers
+        self.A_ptr = np.array([[self.A[l][a].data_ptr() for l in self.layers] for a in range(n_adapters)],
+                              dtype=np.uint64)
+        self.B_ptr = np.array([[self.B[l][a].data_ptr() for l in self.layers] for a in range(n_adapters)],
+                              dtype=np.uint64)
+        self._lay = B._i32_array([0, 1])
+        self._xs = B._vp_array([self.x.data_ptr()] * 2)
+        self._ys = B._vp_array([t.data_ptr() for t in self.y])
+        S = max_loras
+        self._dids = np.zeros(S, np.uint64)
+        self._slots = np.zeros(S, np.int32)
+        self._need = np.zeros(S, np.int32)
+        self._ev = np.zeros(S, np.uint64)
+        P = ctypes.POINTER
+        self._dids_p = self._dids.ctypes.data_as(P(ctypes.c_uint64))
+        self._slots_p = self._slots.ctypes.data_as(P(ctypes.c_int))
+        self._need_p = self._need.ctypes.data_as(P(ctypes.c_int))
+        self._ev_p = self._ev.ctypes.data_as(P(ctypes.c_uint64))
+        self._ranks = np.full(tokens, rank, np.int32)
+        self._ranks_p = self._ranks.ctypes.data_as(P(ctypes.c_int))
 
     def upload(self, slot, adapter):
         a = [self.A[l][adapter] for l in self.layers]
@@ -160,6 +183,7 @@ class ChurnRunner:
         decisions = []
         tokens = 0
         ctx = self.slots.ctx
+        lib = B.load()
         torch.cuda.synchronize(self.dev)
         t0 = time.perf_counter()
         for k, ids in enumerate(trace.steps):
@@ -170,41 +194,58 @@ class ChurnRunner:
                 with torch.cuda.stream(self.slots.compute):
                     for y, y0 in zip(self.y, self.y0):
                         y.copy_(y0)
-            _, first = np.unique(ids, return_index=True)        # distinct, first appearance
-            order = [int(a) for a in ids[np.sort(first)]]
+            uniq, first, inv = np.unique(ids, return_index=True, return_inverse=True)
+            ford = np.argsort(first)                             # distinct, first appearance
+            order = [int(a) for a in uniq[ford]]
+            groups = plan_groups(order, self.pinned, self.S - len(self.pinned))
+            gof = np.empty(len(uniq), np.int32)                  # group of each distinct adapter
+            gof[ford] = np.repeat(np.arange(len(groups), dtype=np.int32), [len(g) for g in groups])
+            tok_group = gof[inv]
+            ids_u = ids.astype(np.uint64)
             slot_tok = np.full(self.T, -1, np.int32)
-            for gi, group in enumerate(plan_groups(order, self.pinned, self.S - len(self.pinned))):
-                # admit the group in one call: assign (hit: touch; miss: free
-                # slot or policy victim) and take an in-flight reference
-                rc, done, slots, need, evicted = B.lora_assign_batch(ctx, group, [self.R] * len(group))
+            for gi, group in enumerate(groups):
+                # admit the group's adapters and map its tokens in one call:
+                # assign (hit: touch; miss: free slot or policy victim), take an
+                # in-flight reference, write every token's slot id (-1: not in
+                # this group) straight into the pinned slot-id buffer
+                gids = np.where(tok_group == gi, ids_u, np.uint64(B.NO_ID))
+                idx_h = self.idx_host[rb, gi].numpy()
+                nd, done = ctypes.c_int(0), ctypes.c_int(0)
+                rc = lib.lora_assign_tokens(ctx, self.T, gids.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)),
+                                            self._ranks_p, 1, idx_h.ctypes.data_as(ctypes.POINTER(ctypes.c_int)),
+                                            self.S, self._dids_p, self._slots_p, self._need_p, self._ev_p,
+                                            ctypes.byref(nd), ctypes.byref(done))
+                n = nd.value
                 if rc != 0:
-                    raise RuntimeError(f"assign failed for adapter {group[done]}: {rc}")
+                    raise RuntimeError(f"assign failed for adapter {group[done.value]}: {rc}")
+                slots, need = self._slots[:n], self._need[:n]
                 if record:
-                    decisions += [(k, a, 0, int(sl), int(nd), int(ev_))
-                                  for a, sl, nd, ev_ in zip(group, slots, need, evicted)]
-                pending = [(int(sl), a) for a, sl, nd in zip(group, slots, need) if nd]
-                for a, sl in zip(group, slots):
-                    if a < self.pin_top and a not in self.pinned:
-                        B.check(B.lora_pin(ctx, int(sl), True))
-                        self.pinned[a] = int(sl)
-                if pending and self.batched_upload:
-                    self.slots.load_slots([sl for sl, _ in pending],
-                                          [([self.A[l][a] for l in self.layers], [self.B[l][a] for l in self.layers])
-                                           for _, a in pending],
-                                          [self.R] * len(pending), [self.alpha] * len(pending))
+                    decisions += [(k, a, 0, int(sl), int(nd_), -1 if ev_ == np.uint64(B.NO_ID) else int(ev_))
+                                  for a, sl, nd_, ev_ in zip(group, slots, need, self._ev[:n])]
+                if self.pin_top:
+                    for a, sl in zip(group, slots):
+                        if a < self.pin_top and a not in self.pinned:
+                            B.check(B.lora_pin(ctx, int(sl), True))
+                            self.pinned[a] = int(sl)
+                miss = np.nonzero(need)[0]
+                if len(miss) and self.batched_upload:
+                    ad = np.asarray(group, dtype=np.int64)[miss]
+                    m = len(miss)
+                    rc = lib.lora_load_slots(ctx, m, B._i32_array(slots[miss].tolist()),
+                                             B._vp_array(self.A_ptr[ad].ravel().tolist()),
+                                             B._vp_array(self.B_ptr[ad].ravel().tolist()),
+                                             B._i32_array([self.R] * m), (ctypes.c_float * m)(*([self.alpha] * m)))
+                    B.check(rc)
                 else:
-                    for sl, a in pending:
-                        self.upload(sl, a)
-                slot_of = np.full(self.n_adapters, -1, np.int32)
-                slot_of[np.asarray(group)] = slots
-                idx = slot_of[ids]
-                sel = idx >= 0
-                slot_tok[sel] = idx[sel]
-                self.idx_host[rb, gi].numpy()[:] = idx
+                    for i in miss:
+                        self.upload(int(slots[i]), group[i])
+                sel = idx_h >= 0
+                slot_tok[sel] = idx_h[sel]
                 with torch.cuda.stream(self.slots.compute):
                     self.idx[rb, gi].copy_(self.idx_host[rb, gi], non_blocking=True)
-                    self.slots.apply_multi([0, 1], [self.x, self.x], self.y, self.idx[rb, gi])
-                B.check(B.lora_release_batch(ctx, slots))
+                B.check(lib.lora_apply_multi(ctx, 2, self._lay, self._xs, self._ys, self.idx[rb, gi].data_ptr(),
+                                             self.T))
+                B.check(lib.lora_release_batch(ctx, n, self._slots_p))
                 tokens += int(sel.sum())
             ev = torch.cuda.Event()
             ev.record(self.slots.compute)
