@@ -92,11 +92,17 @@ __device__ __forceinline__ void shrink_steps(float (&acc)[4][2][4], const uint16
             a0[m] = load8_bf16(As + (size_t)k0 * d_in, cc, d_in, k0 < r, vec);
             a1[m] = load8_bf16(As + (size_t)k1 * d_in, cc, d_in, k1 < r, vec);
         }
+        // first halves of K for every accumulator, then the second halves: each
+        // accumulator adds in the same order, and no MMA waits on the one
+        // issued just before it
 #pragma unroll
         for (int m = 0; m < NMB; ++m) {
             mma_bf16(acc[m][0], a0[m].x, a1[m].x, a0[m].y, a1[m].y, xa.x, xa.y);
-            mma_bf16(acc[m][0], a0[m].z, a1[m].z, a0[m].w, a1[m].w, xa.z, xa.w);
             mma_bf16(acc[m][1], a0[m].x, a1[m].x, a0[m].y, a1[m].y, xb.x, xb.y);
+        }
+#pragma unroll
+        for (int m = 0; m < NMB; ++m) {
+            mma_bf16(acc[m][0], a0[m].z, a1[m].z, a0[m].w, a1[m].w, xa.z, xa.w);
             mma_bf16(acc[m][1], a0[m].z, a1[m].z, a0[m].w, a1[m].w, xb.z, xb.w);
         }
     }
@@ -252,25 +258,37 @@ __device__ __forceinline__ void expand_bf16_tile(const LayerArgs &L, const Group
     for (int grp = 0; grp < 2; ++grp) {
         const int c = dblock * kExpandCols + warp * 64 + grp * 32;
         if (c >= d_out) break;
-        float acc[4][4];
+        // Every B fragment of the group first, then per 16-rank block the
+        // high-part MMAs of the four column blocks and after them the low-part
+        // ones: each accumulator adds in the order of a one-block-at-a-time
+        // loop, while four independent MMAs go out back to back.
+        // (ranks >= r are zero in the pool and in v, so no mask is needed)
+        uint2 bb[4][4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
             const int P = c + 8 * (gq >> 1) + 2 * j + (gq & 1);
 #pragma unroll
             for (int kb = 0; kb < 4; ++kb) {
-                if (kb < nkb) {
-                    const int k = kb * 16 + 4 * tq;
-                    // ranks >= r: zero in the pool and in v, so no mask is needed
-                    uint2 bb = make_uint2(0, 0);
-                    if (P < d_out) {
-                        const int Pl = P - c0;
-                        bb = *reinterpret_cast<const uint2 *>(bs + Pl * 64 + (((k >> 3) ^ bkey(Pl)) << 3) + (k & 7));
-                    }
-                    mma_bf16(acc[j], ahi[kb][0], ahi[kb][1], ahi[kb][2], ahi[kb][3], bb.x, bb.y);
-                    mma_bf16(acc[j], alo[kb][0], alo[kb][1], alo[kb][2], alo[kb][3], bb.x, bb.y);
+                const int k = kb * 16 + 4 * tq;
+                bb[j][kb] = make_uint2(0, 0);
+                if (kb < nkb && P < d_out) {
+                    const int Pl = P - c0;
+                    bb[j][kb] = *reinterpret_cast<const uint2 *>(bs + Pl * 64 + (((k >> 3) ^ bkey(Pl)) << 3) + (k & 7));
                 }
             }
+        }
+        float acc[4][4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb) {
+            if (kb >= nkb) break;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                mma_bf16(acc[j], ahi[kb][0], ahi[kb][1], ahi[kb][2], ahi[kb][3], bb[j][kb].x, bb[j][kb].y);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                mma_bf16(acc[j], alo[kb][0], alo[kb][1], alo[kb][2], alo[kb][3], bb[j][kb].x, bb[j][kb].y);
         }
         // Lane owns columns c + 8tq .. c + 8tq + 7 of rows tok0 (acc[.][0..1]) and tok1 (acc[.][2..3]).
         const int cc = c + 8 * tq;

@@ -381,16 +381,28 @@ decode_cluster_kernel(const __grid_constant__ FusedArgs fa) {
             if (cc < w) {
                 const uint4 xa = lds128(xs + swz(gq, cc));
                 const uint4 xb = lds128(xs + swz(gq + 8, cc));
+                // A fragments of every rank block first; then the first halves
+                // of K for every accumulator and after them the second halves
+                // (each accumulator adds in the same order, and no MMA waits on
+                // the one issued just before it)
+                uint4 a0[KB], a1[KB];
+#pragma unroll
+                for (int m = 0; m < KB; ++m) {
+                    a0[m] = m < nmb ? lds128(as + swz(m * 16 + gq, cc)) : make_uint4(0, 0, 0, 0);
+                    a1[m] = m < nmb ? lds128(as + swz(m * 16 + gq + 8, cc)) : make_uint4(0, 0, 0, 0);
+                }
 #pragma unroll
                 for (int m = 0; m < KB; ++m) {
                     if (m < nmb) {
-                        const uint4 a0 = lds128(as + swz(m * 16 + gq, cc));
-                        const uint4 a1 = lds128(as + swz(m * 16 + gq + 8, cc));
-                        // the two accumulators alternate, so no MMA waits on the one before it
-                        mma_bf16(acc[m][0], a0.x, a1.x, a0.y, a1.y, xa.x, xa.y);
-                        mma_bf16(acc[m][1], a0.x, a1.x, a0.y, a1.y, xb.x, xb.y);
-                        mma_bf16(acc[m][0], a0.z, a1.z, a0.w, a1.w, xa.z, xa.w);
-                        mma_bf16(acc[m][1], a0.z, a1.z, a0.w, a1.w, xb.z, xb.w);
+                        mma_bf16(acc[m][0], a0[m].x, a1[m].x, a0[m].y, a1[m].y, xa.x, xa.y);
+                        mma_bf16(acc[m][1], a0[m].x, a1[m].x, a0[m].y, a1[m].y, xb.x, xb.y);
+                    }
+                }
+#pragma unroll
+                for (int m = 0; m < KB; ++m) {
+                    if (m < nmb) {
+                        mma_bf16(acc[m][0], a0[m].z, a1[m].z, a0[m].w, a1[m].w, xa.z, xa.w);
+                        mma_bf16(acc[m][1], a0[m].z, a1[m].z, a0[m].w, a1[m].w, xb.z, xb.w);
                     }
                 }
             }
