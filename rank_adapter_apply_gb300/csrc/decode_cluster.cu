@@ -377,10 +377,16 @@ decode_cluster_kernel(const __grid_constant__ FusedArgs fa) {
         const uint16_t *as = d.as + b * KB * 16 * kSW;
 #pragma unroll
         for (int step = 0; step < 2; ++step) {
-            const int cc = warp * 64 + step * 32 + 8 * tq;
-            if (cc < w) {
-                const uint4 xa = lds128(xs + swz(gq, cc));
-                const uint4 xb = lds128(xs + swz(gq + 8, cc));
+            // The MMAs are warp-wide, so the test that skips a step is too:
+            // a lane whose 8 columns lie past the slice (its last step can end
+            // inside the 32 columns, w being a multiple of 8 only) takes zeros.
+            const int cb = warp * 64 + step * 32;
+            if (cb < w) {
+                const int cc = cb + 8 * tq;
+                const bool in = cc < w;
+                const uint4 z = make_uint4(0, 0, 0, 0);
+                const uint4 xa = in ? lds128(xs + swz(gq, cc)) : z;
+                const uint4 xb = in ? lds128(xs + swz(gq + 8, cc)) : z;
                 // A fragments of every rank block first; then the first halves
                 // of K for every accumulator and after them the second halves
                 // (each accumulator adds in the same order, and no MMA waits on
@@ -388,8 +394,8 @@ decode_cluster_kernel(const __grid_constant__ FusedArgs fa) {
                 uint4 a0[KB], a1[KB];
 #pragma unroll
                 for (int m = 0; m < KB; ++m) {
-                    a0[m] = m < nmb ? lds128(as + swz(m * 16 + gq, cc)) : make_uint4(0, 0, 0, 0);
-                    a1[m] = m < nmb ? lds128(as + swz(m * 16 + gq + 8, cc)) : make_uint4(0, 0, 0, 0);
+                    a0[m] = (in && m < nmb) ? lds128(as + swz(m * 16 + gq, cc)) : z;
+                    a1[m] = (in && m < nmb) ? lds128(as + swz(m * 16 + gq + 8, cc)) : z;
                 }
 #pragma unroll
                 for (int m = 0; m < KB; ++m) {

@@ -67,6 +67,31 @@ def test_small_and_ragged_token_counts(T):
     check_layer(w, "l0", out["l0"])
 
 
+@pytest.mark.parametrize("d_in,d_out,R,early", [(1032, 1000, 16, True), (1032, 1000, 16, False),
+                                                  (4096, 4104, 16, True), (512, 4096, 32, True),
+                                                  (768, 2056, 64, True)])
+def test_cluster_decode_partial_stages(d_in, d_out, R, early):
+    """Small-batch cluster kernel with column slices that end inside a stage:
+    d_out up to 4096 takes the short path (products before the wait on the
+    previous kernel, y updated from registers), d_out above 4096 the staged
+    path; both with and without inputs declared ready."""
+    from rank_adapter_apply_gb300.harness import DeviceWorkload
+    from rank_adapter_apply_gb300 import binding as B
+    T = 53
+    rng = np.random.default_rng(d_in + d_out + R)
+    S = 5
+    ranks = [R, max(1, R // 2), 8, R, 5]
+    idx = rng.integers(-1, S, size=T)
+    w = _custom(T, d_in, d_out, S, R, ranks, idx, seed=d_out)
+    dw = DeviceWorkload(w)
+    try:
+        B.lora_set_inputs_ready(dw.slots.ctx, early)
+        out = dw.run(None, multi=True)
+    finally:
+        dw.close()
+    check_layer(w, "l0", out["l0"])
+
+
 def test_all_base_only_is_bitwise_noop():
     T = 64
     w = _custom(T, 512, 256, 4, 16, [16] * 4, np.full(T, -1))
