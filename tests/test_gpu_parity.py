@@ -207,6 +207,22 @@ def test_tensor_core_prefill_small(R):
     assert st["device_wait_timeouts"] == 0
 
 
+@pytest.mark.parametrize("R", [32, 64])
+def test_tensor_core_prefill_ragged_dims(R):
+    """d_in not a multiple of the 64-column k-block (the last TMA box of x and A
+    reaches past the row and reads zeros) and d_out a multiple of 64 but not of
+    the 128-column n-block; decode tokens of the same batch take the general
+    path with a d_in chunk that ends inside a 32-column step."""
+    rng = np.random.default_rng(R + 1)
+    runs = [(1, 150), (0, 64), (-1, 9), (2, 70), (3, 5), (0, 200), (1, 3)]
+    idx = np.concatenate([np.full(n, s) for s, n in runs]).astype(np.int32)
+    ranks = [R, 8, R // 2, 5]
+    w = _custom(idx.shape[0], 1032, 448, 4, R, ranks, idx, seed=R + 7)
+    out, st = _run(w, small_batch_tokens=0)
+    check_layer(w, "l0", out["l0"])
+    assert st["device_wait_timeouts"] == 0
+
+
 def test_prefill_small_general_path_matches_oracle():
     w = wl.prefill_5120(1, n_seqs=5, len_range=(60, 300))
     out, st = _run(w, small_batch_tokens=0)
