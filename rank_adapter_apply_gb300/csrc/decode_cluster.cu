@@ -53,7 +53,6 @@ constexpr unsigned kFullMask = 0xffffffffu;
 // prologue (the first cluster barrier).
 struct GroupScratch {
     int cnt[kMaxSlots];
-    int off[kMaxSlots + 1];
     int toff[kMaxSlots + 1];
     int rank[kMaxSlots];
     float scale[kMaxSlots];
@@ -62,6 +61,7 @@ struct GroupScratch {
 
 struct ClusterSmem {
     int tok[kTileTokens];
+    int wcnt[kCW];                         // per-warp counts while collecting the tile's tokens
     uint64_t sbar[2], ebar[2];
     int ntiles, invalid;
     float scale;                           // scale of this tile's slot
@@ -291,59 +291,92 @@ decode_cluster_kernel(const __grid_constant__ FusedArgs fa) {
     }
     if (inv) atomicAdd(&sm.invalid, inv);
     __syncthreads();
-    if (warp == 0) {
-        int carry_o = 0, carry_t = 0;
-        for (int base = 0; base < S; base += 32) {
-            const int s = base + lane;
-            const int c = s < S ? d.g->cnt[s] : 0;
-            const int nt = (c + kTileTokens - 1) / kTileTokens;
-            int ic = c, it = nt;
+    // Tiles per slot, their prefix, and this tile's slot. With at most 32 slots
+    // every warp does this in registers (one lane per slot, no barrier);
+    // beyond that warp 0 scans through shared memory.
+    int ntiles, lo, toff_lo;
+    if (S <= 32) {
+        const int c = lane < S ? d.g->cnt[lane] : 0;
+        const int nt = (c + kTileTokens - 1) / kTileTokens;
+        int it = nt;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int a = __shfl_up_sync(kFullMask, ic, o), bb = __shfl_up_sync(kFullMask, it, o);
-                if (lane >= o) { ic += a; it += bb; }
-            }
-            if (s < S) {
-                d.g->off[s] = carry_o + ic - c;
-                d.g->toff[s] = carry_t + it - nt;
-            }
-            carry_o += __shfl_sync(kFullMask, ic, 31);
-            carry_t += __shfl_sync(kFullMask, it, 31);
+        for (int o = 1; o < 32; o <<= 1) {
+            const int a2 = __shfl_up_sync(kFullMask, it, o);
+            if (lane >= o) it += a2;
         }
-        if (lane == 0) {
-            d.g->off[S] = carry_o;
-            d.g->toff[S] = carry_t;
-            sm.ntiles = carry_t;
+        ntiles = __shfl_sync(kFullMask, it, 31);
+        const int tex = it - nt;            // first tile of slot `lane`
+        // the slot whose tiles hold `tile`: the last one that has tiles and
+        // starts at or before it
+        const unsigned cand = __ballot_sync(kFullMask, nt > 0 && tex <= tile);
+        lo = cand ? 31 - __clz(cand) : 0;
+        toff_lo = __shfl_sync(kFullMask, tex, lo);
+    } else {
+        if (warp == 0) {
+            int carry_t = 0;
+            for (int base = 0; base < S; base += 32) {
+                const int s = base + lane;
+                const int c = s < S ? d.g->cnt[s] : 0;
+                const int nt = (c + kTileTokens - 1) / kTileTokens;
+                int it = nt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int a2 = __shfl_up_sync(kFullMask, it, o);
+                    if (lane >= o) it += a2;
+                }
+                if (s < S) d.g->toff[s] = carry_t + it - nt;
+                carry_t += __shfl_sync(kFullMask, it, 31);
+            }
+            if (lane == 0) {
+                d.g->toff[S] = carry_t;
+                sm.ntiles = carry_t;
+            }
         }
-    }
-    __syncthreads();
-    if (blockIdx.x == 0 && blockIdx.y == 0 && tid == 0 && sm.invalid)
-        atomicAdd(fa.hdr + kHdrInvalid, sm.invalid);
-    if (tile >= sm.ntiles) return;          // the whole cluster leaves together
-
-    // ---- this tile: slot, tokens -----------------------------------------
-    Tile t;
-    {
-        int lo = 0, hi = S - 1;
+        __syncthreads();
+        ntiles = sm.ntiles;
+        lo = 0;
+        int hi = S - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
             if (d.g->toff[mid] <= tile) lo = mid; else hi = mid - 1;
         }
+        toff_lo = d.g->toff[lo];
+    }
+    if (blockIdx.x == 0 && blockIdx.y == 0 && tid == 0 && sm.invalid)
+        atomicAdd(fa.hdr + kHdrInvalid, sm.invalid);
+    if (tile >= ntiles) return;             // the whole cluster leaves together
+
+    // ---- this tile: slot, tokens -----------------------------------------
+    Tile t;
+    {
         t.s = lo;
-        const int first = (tile - d.g->toff[lo]) * kTileTokens;
+        const int first = (tile - toff_lo) * kTileTokens;
         t.cnt = min(kTileTokens, d.g->cnt[lo] - first);
         t.r = d.g->rank[lo];
         if (tid == 0) sm.scale = d.g->scale[lo];
-        if (warp == 0) {                   // the (first + i)-th token on slot s, original order
+        // The (first + i)-th token on slot lo, in original order: every warp
+        // takes 32 tokens of a 128-token block (one ballot each), the warp
+        // counts meet in shared memory, and a running count carries the
+        // blocks before; the loop stops once the tile's tokens are found.
+        {
             const unsigned lt = (1u << lane) - 1u;
-            int seen = 0;
-            for (int base = 0; base < T && seen < first + kTileTokens; base += 32) {
-                const int tk = base + lane;
+            int seen = 0;                   // the same in every thread
+            for (int base = 0; base < T && seen < first + kTileTokens; base += kCT) {
+                const int tk = base + tid;
                 const bool m = tk < T && d.g->eff[tk] == (uint8_t)lo;
                 const unsigned bal = __ballot_sync(kFullMask, m);
-                const int before = seen + __popc(bal & lt);
+                if (lane == 0) sm.wcnt[warp] = __popc(bal);
+                __syncthreads();
+                int before = seen + __popc(bal & lt), total = 0;
+#pragma unroll
+                for (int w2 = 0; w2 < kCW; ++w2) {
+                    const int c = sm.wcnt[w2];
+                    before += w2 < warp ? c : 0;
+                    total += c;
+                }
                 if (m && before >= first && before < first + kTileTokens) sm.tok[before - first] = tk;
-                seen += __popc(bal);
+                seen += total;
+                __syncthreads();            // wcnt is rewritten by the next block
             }
         }
     }
