@@ -402,8 +402,15 @@ def run_ours(args):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quick:
         v, n, cores, el = cpu_oracle_run(w, batches, budget_s=args.cpu_seconds)
+        # the same oracle on one thread, over a shorter sample
+        import oracle
+        oracle.set_threads(1)
+        v1, n1, _, el1 = cpu_oracle_run(w, batches, budget_s=max(1.0, args.cpu_seconds / 3))
+        oracle.set_threads(cores)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": f"{n} whole batches (256 tokens, q_proj+v_proj) in {el:.1f} s"}
+                                "sample": f"{n} whole batches (256 tokens, q_proj+v_proj) in {el:.1f} s",
+                                "single_thread": {"value": v1, "cores": 1,
+                                                  "sample": f"{n1} whole batches in {el1:.1f} s"}}
     if rank == 0:
         print(json.dumps(line), flush=True)
     for d in sets:

@@ -57,6 +57,8 @@ def _load():
                                               vp, vp, vp, vp, vp, vp, vp, i32, vp]
             lib.oracle_lora_apply.restype = i32
             lib.oracle_threads.restype = i32
+            lib.oracle_set_threads.argtypes = [i32]
+            lib.oracle_set_threads.restype = None
             _lib = lib
     return _lib
 
@@ -64,6 +66,11 @@ def _load():
 def threads() -> int:
     """OpenMP threads the oracle runs with."""
     return int(_load().oracle_threads())
+
+
+def set_threads(n: int) -> None:
+    """OpenMP threads for the calls that follow (timing only)."""
+    _load().oracle_set_threads(int(n))
 
 
 def _ptr(a: np.ndarray):

@@ -56,6 +56,17 @@ int oracle_threads(void)
 #endif
 }
 
+/* Thread count for the calls that follow (timing runs only; results do not
+ * depend on it: each token's sums run in one thread in a fixed order). */
+void oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /*
  * y_out is [n_list][d_out], one row per listed token (tokens[n] indexes x,
  * y_in and token_slot_idx). Returns 0, or -1 on bad arguments.
