@@ -147,7 +147,6 @@ class ChurnRunner:
         # ceil(tokens / evictable slots) groups); reused only after the step's sync
         self.max_groups = (tokens + max(1, max_loras - pin_top) - 1) // max(1, max_loras - pin_top)
         self.idx_host = torch.empty((self.ring, self.max_groups, tokens), dtype=torch.int32).pin_memory()
-        self.idx = torch.empty((self.ring, self.max_groups, tokens), dtype=torch.int32, device=self.dev)
         self.step_done = [None] * self.ring
         # call arguments built once: host pointers of every adapter's A and B
         # per layer (adapter-major rows), the layer list and x / y pointers
@@ -170,6 +169,8 @@ class ChurnRunner:
         self._ev_p = self._ev.ctypes.data_as(P(ctypes.c_uint64))
         self._ranks = np.full(tokens, rank, np.int32)
         self._ranks_p = self._ranks.ctypes.data_as(P(ctypes.c_int))
+        self._alphas = np.full(S, alpha, np.float32)
+        self._alphas_p = self._alphas.ctypes.data_as(P(ctypes.c_float))
 
     def upload(self, slot, adapter):
         a = [self.A[l][adapter] for l in self.layers]
@@ -231,19 +232,23 @@ class ChurnRunner:
                 if len(miss) and self.batched_upload:
                     ad = np.asarray(group, dtype=np.int64)[miss]
                     m = len(miss)
-                    rc = lib.lora_load_slots(ctx, m, B._i32_array(slots[miss].tolist()),
-                                             B._vp_array(self.A_ptr[ad].ravel().tolist()),
-                                             B._vp_array(self.B_ptr[ad].ravel().tolist()),
-                                             B._i32_array([self.R] * m), (ctypes.c_float * m)(*([self.alpha] * m)))
+                    sl_m = np.ascontiguousarray(slots[miss])
+                    a_p = np.ascontiguousarray(self.A_ptr[ad].ravel())
+                    b_p = np.ascontiguousarray(self.B_ptr[ad].ravel())
+                    P = ctypes.POINTER
+                    rc = lib.lora_load_slots(ctx, m, sl_m.ctypes.data_as(P(ctypes.c_int)),
+                                             a_p.ctypes.data_as(P(ctypes.c_void_p)),
+                                             b_p.ctypes.data_as(P(ctypes.c_void_p)), self._ranks_p, self._alphas_p)
                     B.check(rc)
                 else:
                     for i in miss:
                         self.upload(int(slots[i]), group[i])
                 sel = idx_h >= 0
                 slot_tok[sel] = idx_h[sel]
-                with torch.cuda.stream(self.slots.compute):
-                    self.idx[rb, gi].copy_(self.idx_host[rb, gi], non_blocking=True)
-                B.check(lib.lora_apply_multi(ctx, 2, self._lay, self._xs, self._ys, self.idx[rb, gi].data_ptr(),
+                # the kernels read the slot ids straight from the pinned buffer
+                # (same address on the device; it is rewritten only after the
+                # step that used it has finished)
+                B.check(lib.lora_apply_multi(ctx, 2, self._lay, self._xs, self._ys, self.idx_host[rb, gi].data_ptr(),
                                              self.T))
                 B.check(lib.lora_release_batch(ctx, n, self._slots_p))
                 tokens += int(sel.sum())

@@ -139,6 +139,40 @@ cudaError_t wait_slot_reads(lora_ctx *c, int slot) {
     return c->compute_recorded ? cudaStreamWaitEvent(c->upload, c->compute_done, 0) : cudaSuccess;
 }
 
+// wait_slot_reads for several slots, each distinct event waited on once.
+cudaError_t wait_slots_reads(lora_ctx *c, const std::vector<int> &slots) {
+    if (!c->track) return slots.empty() ? cudaSuccess : wait_slot_reads(c, slots[0]);
+    std::vector<int> idx;
+    for (int s : slots) {
+        const int64_t g = c->slot_gen[s];
+        if (g >= 0) idx.push_back((int)(g % kRing));
+    }
+    std::sort(idx.begin(), idx.end());
+    idx.erase(std::unique(idx.begin(), idx.end()), idx.end());
+    for (int i : idx) {
+        cudaError_t e = cudaStreamWaitEvent(c->upload, c->ring[i], 0);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+// True when the current device reads host memory through the host's page
+// tables (any host address is valid in a kernel); checked once per device.
+bool host_pages_visible() {
+    static std::atomic<uint64_t> known{0}, yes{0};
+    if (device_bit(known)) return device_bit(yes);
+    int dev = 0, a = 0, b = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&a, cudaDevAttrPageableMemoryAccess, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&b, cudaDevAttrPageableMemoryAccessUsesHostPageTables, dev) != cudaSuccess) {
+        cudaGetLastError();
+        a = b = 0;
+    }
+    if (a == 1 && b == 1) set_device_bit(yes);
+    set_device_bit(known);
+    return a == 1 && b == 1;
+}
+
 // Move finished upload timings into upload_seconds (blocking when `wait`).
 int harvest_timings(lora_ctx *c, bool wait) {
     std::vector<UploadTiming> keep;
@@ -382,21 +416,27 @@ int lora_load_slots(lora_ctx *c, int n, const int *slots, const void *const *A_h
             if (!A_host[(size_t)i * L + l] || !B_host[(size_t)i * L + l])
                 return fail(LORA_ERR_ARG, "adapter %d layer %d weights are NULL", i, l);
     }
-    // Adapters the kernel can read: device-mapped host pointers, 16-byte
-    // aligned rows. The others take the copy-engine path of lora_load_slot.
+    // Adapters the kernel can read: host pointers the GPU reaches at the same
+    // address, 16-byte aligned rows. When the GPU walks the host's page tables
+    // every host address qualifies and no per-pointer lookup is needed;
+    // otherwise each pointer must be device-mapped pinned memory. The others
+    // take the copy-engine path of lora_load_slot.
+    const bool all_host = host_pages_visible();
     std::vector<int> direct, copies;
     for (int i = 0; i < n; ++i) {
         bool ok = ((size_t)ranks[i] * e) % 16 == 0;
         for (int l = 0; l < L && ok; ++l) {
             const void *p[2] = {A_host[(size_t)i * L + l], B_host[(size_t)i * L + l]};
             for (int q = 0; q < 2 && ok; ++q) {
-                void *dp = nullptr;
-                ok = cudaHostGetDevicePointer(&dp, const_cast<void *>(p[q]), 0) == cudaSuccess && dp == p[q] &&
-                     reinterpret_cast<uintptr_t>(p[q]) % 16 == 0;
+                ok = reinterpret_cast<uintptr_t>(p[q]) % 16 == 0;
+                if (ok && !all_host) {
+                    void *dp = nullptr;
+                    ok = cudaHostGetDevicePointer(&dp, const_cast<void *>(p[q]), 0) == cudaSuccess && dp == p[q];
+                }
             }
             ok = ok && ((size_t)c->layers[l].d_in * e) % 16 == 0;
         }
-        cudaGetLastError();                    // clear a lookup failure of an unmapped pointer
+        if (!all_host) cudaGetLastError();     // clear a lookup failure of an unmapped pointer
         (ok ? direct : copies).push_back(i);
     }
     for (int i : copies) {
@@ -413,9 +453,11 @@ int lora_load_slots(lora_ctx *c, int n, const int *slots, const void *const *A_h
         ua.rank_dev = c->rank_dev;
         int units = 0;
         uint64_t bytes = 0;
+        std::vector<int> wslots;
+        for (size_t k = b0; k < b1; ++k) wslots.push_back(slots[direct[k]]);
+        CUDA_TRY(wait_slots_reads(c, wslots));
         for (size_t k = b0; k < b1; ++k) {
             const int i = direct[k], s = slots[i];
-            CUDA_TRY(wait_slot_reads(c, s));
             for (int l = 0; l < L; ++l) {
                 const lora_layer_desc &D = c->layers[l];
                 UploadEntry &u = ua.e[ua.n];

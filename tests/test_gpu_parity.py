@@ -282,9 +282,10 @@ def test_prefill_batch_shorter_than_a_tile(T, run):
 @pytest.mark.parametrize("dtype", [wl.DTYPE_BF16, wl.DTYPE_F32])
 def test_batched_upload_matches_oracle(dtype):
     """lora_load_slots: adapters of several ranks (zero padding up to R) in one
-    call, pinned buffers read by the upload kernel plus one pageable adapter on
-    the copy-engine path; then the delta equals the oracle's, and padding rows
-    of a slot that held a larger rank before are zero again."""
+    call, pinned buffers read by the upload kernel plus one pageable adapter
+    (read by the kernel too where the GPU walks the host's page tables, else
+    taken by the copy-engine path); then the delta equals the oracle's, and
+    padding rows of a slot that held a larger rank before are zero again."""
     import torch
     from rank_adapter_apply_gb300.harness import to_torch, from_torch
     from rank_adapter_apply_gb300.slots import LoraSlots
@@ -310,7 +311,7 @@ def test_batched_upload_matches_oracle(dtype):
         for s in range(S):
             A = to_torch(ads[s]["l0"][0], dtype)
             Bm = to_torch(ads[s]["l0"][1], dtype)
-            if s != 3:                                   # slot 3: pageable, copy-engine path
+            if s != 3:                                   # slot 3: pageable memory
                 A, Bm = A.pin_memory(), Bm.pin_memory()
             host.append(([A], [Bm]))
         sl.load_slots(list(range(S)), host, ranks, [2.0 * r for r in ranks])
