@@ -73,8 +73,12 @@ struct lora_ctx {
     WsLayout lay{};
     cudaStream_t compute = nullptr, upload = nullptr;
     SlotTable table;
-    std::vector<cudaEvent_t> slot_ev;
-    std::vector<char> slot_pending;
+    // Uploads and evictions: call k records up_ev[k % size] on the upload
+    // stream; slot_up[s] = the newest such call that wrote slot s and that no
+    // apply has waited for yet (-1: none).
+    std::vector<cudaEvent_t> up_ev;
+    std::vector<int64_t> slot_up;
+    int64_t n_up = 0;
     cudaEvent_t compute_done = nullptr;
     bool compute_recorded = false;
     std::vector<UploadTiming> timing;
@@ -137,6 +141,16 @@ cudaError_t wait_slot_reads(lora_ctx *c, int slot) {
         return g >= 0 ? cudaStreamWaitEvent(c->upload, c->ring[g % kRing], 0) : cudaSuccess;
     }
     return c->compute_recorded ? cudaStreamWaitEvent(c->upload, c->compute_done, 0) : cudaSuccess;
+}
+
+// After the upload-stream work of one upload or eviction call: one event for
+// every slot it wrote.
+cudaError_t note_upload(lora_ctx *c, const int *slots, int n) {
+    const int64_t k = c->n_up++;
+    cudaError_t e = cudaEventRecord(c->up_ev[k % (int64_t)c->up_ev.size()], c->upload);
+    if (e != cudaSuccess) return e;
+    for (int i = 0; i < n; ++i) c->slot_up[slots[i]] = k;
+    return cudaSuccess;
 }
 
 // wait_slot_reads for several slots, each distinct event waited on once.
@@ -303,13 +317,13 @@ int lora_slots_init(lora_ctx **out, int max_loras, int max_lora_rank, int max_to
     c->ws_bytes = workspace_bytes;
     c->compute = static_cast<cudaStream_t>(compute_stream);
     c->upload = static_cast<cudaStream_t>(upload_stream);
-    c->slot_ev.assign(max_loras, nullptr);
-    c->slot_pending.assign(max_loras, 0);
+    c->up_ev.assign(max_loras, nullptr);
+    c->slot_up.assign(max_loras, -1);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
     for (int s = 0; s < max_loras && e == cudaSuccess; ++s)
-        e = cudaEventCreateWithFlags(&c->slot_ev[s], cudaEventDisableTiming);
+        e = cudaEventCreateWithFlags(&c->up_ev[s], cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->compute_done, cudaEventDisableTiming);
     // Empty table: every slot rank 0; workspace zeroed (arrival counters start at 0).
     if (e == cudaSuccess) e = cudaMemsetAsync(rank_dev, 0, sizeof(int32_t) * max_loras, c->compute);
@@ -331,7 +345,7 @@ void lora_destroy(lora_ctx *c) {
         if (c->upload) cudaStreamSynchronize(c->upload);
         if (c->compute) cudaStreamSynchronize(c->compute);
         harvest_timings(c, true);
-        for (auto ev : c->slot_ev)
+        for (auto ev : c->up_ev)
             if (ev) cudaEventDestroy(ev);
         if (c->compute_done) cudaEventDestroy(c->compute_done);
         for (auto ev : c->ring)
@@ -385,8 +399,7 @@ int lora_load_slot(lora_ctx *c, int slot, const void *const *A_host, const void 
     }
     CUDA_TRY(launch_set_slot(c->scale_dev, c->rank_dev, slot, alpha / (float)rank, rank, c->upload));
     CUDA_TRY(cudaEventRecord(tm.end, c->upload));
-    CUDA_TRY(cudaEventRecord(c->slot_ev[slot], c->upload));
-    c->slot_pending[slot] = 1;
+    CUDA_TRY(note_upload(c, &slot, 1));
     c->timing.push_back(tm);
     c->uploads += 1;
     c->upload_bytes += bytes;
@@ -484,10 +497,7 @@ int lora_load_slots(lora_ctx *c, int n, const int *slots, const void *const *A_h
         CUDA_TRY(cudaEventRecord(tm.start, c->upload));
         CUDA_TRY(launch_upload_slots(ua, units, c->upload));
         CUDA_TRY(cudaEventRecord(tm.end, c->upload));
-        for (int k = 0; k < ua.n_slots; ++k) {
-            CUDA_TRY(cudaEventRecord(c->slot_ev[ua.slots[k]], c->upload));
-            c->slot_pending[ua.slots[k]] = 1;
-        }
+        CUDA_TRY(note_upload(c, ua.slots, ua.n_slots));
         c->timing.push_back(tm);
         c->uploads += (uint64_t)ua.n_slots;
         c->upload_bytes += bytes;
@@ -553,16 +563,20 @@ int apply_impl(lora_ctx *c, int n, const int *layers, const void *const *xs, voi
     if (T == 0) return LORA_OK;
     if (!idx) return fail(LORA_ERR_ARG, "token_slot_idx is NULL");
 
-    // Uploads queued since the last apply must land before any kernel reads a slot.
+    // Uploads queued since the last apply must land before any kernel reads a
+    // slot: one wait on the newest of them covers the older ones (the upload
+    // stream runs in order; a ring event re-recorded since only waits longer).
     if (!capturing(c->compute)) {
-        for (int s = 0; s < c->S; ++s)
-            if (c->slot_pending[s]) {
-                CUDA_TRY(cudaStreamWaitEvent(c->compute, c->slot_ev[s], 0));
-                c->slot_pending[s] = 0;
-            }
+        int64_t newest = -1;
+        for (int s = 0; s < c->S; ++s) {
+            newest = std::max(newest, c->slot_up[s]);
+            c->slot_up[s] = -1;
+        }
+        if (newest >= 0)
+            CUDA_TRY(cudaStreamWaitEvent(c->compute, c->up_ev[newest % (int64_t)c->up_ev.size()], 0));
     } else {
         for (int s = 0; s < c->S; ++s)
-            if (c->slot_pending[s])
+            if (c->slot_up[s] >= 0)
                 return fail(LORA_ERR_STATE, "slot %d upload pending during stream capture; "
                                             "call lora_sync_uploads before capturing", s);
     }
@@ -966,8 +980,7 @@ int lora_evict_lru(lora_ctx *c, int *evicted_slot, uint64_t *evicted_id) {
         // The slot reads as empty for work queued after this call.
         CUDA_TRY(wait_slot_reads(c, *evicted_slot));
         CUDA_TRY(launch_set_slot(c->scale_dev, c->rank_dev, *evicted_slot, 0.f, 0, c->upload));
-        CUDA_TRY(cudaEventRecord(c->slot_ev[*evicted_slot], c->upload));
-        c->slot_pending[*evicted_slot] = 1;
+        CUDA_TRY(note_upload(c, evicted_slot, 1));
     }
     return LORA_OK;
 }
