@@ -4,11 +4,11 @@ namespace lora {
 
 SlotTable::SlotTable(int max_loras, int max_lora_rank)
     : S_(max_loras), R_(max_lora_rank), id_(max_loras, 0), occ_(max_loras, 0), pin_(max_loras, 0),
-      last_use_(max_loras, 0), refs_(max_loras, 0) {}
+      last_use_(max_loras, 0), refs_(max_loras, 0), res_(max_loras, nullptr) {}
 
 void SlotTable::touch(int slot) {
     last_use_[slot] = ++clock_;
-    AdapterResidency &r = rec_[id_[slot]];
+    AdapterResidency &r = *res_[slot];
     r.last_access_epoch = epoch_;
     if (!r.accesses.empty() && r.accesses.back().first == epoch_) ++r.accesses.back().second;
     else r.accesses.emplace_back(epoch_, 1u);
@@ -23,14 +23,14 @@ int SlotTable::lookup(uint64_t id) {
     if (it == where_.end()) return -1;
     touch(it->second);
     ++hits;
-    ++rec_[id].hit_count;
+    ++res_[it->second]->hit_count;
     return it->second;
 }
 
 bool SlotTable::evictable(int s) const {
     if (!occ_[s] || refs_[s] > 0 || pin_[s]) return false;
     if (min_res_ > 0) {
-        const AdapterResidency &r = rec_.at(id_[s]);
+        const AdapterResidency &r = *res_[s];
         if (epoch_ - r.last_access_epoch < min_res_) return false;
     }
     return true;
@@ -38,7 +38,7 @@ bool SlotTable::evictable(int s) const {
 
 // Evaluated in this order in double precision (the simulator does the same).
 double SlotTable::keep_score(int s) const {
-    const AdapterResidency &r = rec_.at(id_[s]);
+    const AdapterResidency &r = *res_[s];
     const double recent = 1.0 / (1.0 + (double)(epoch_ - r.last_access_epoch));
     uint64_t n = 0;
     for (const auto &a : r.accesses)
@@ -79,7 +79,8 @@ uint64_t SlotTable::evict(int slot) {
     refs_[slot] = 0;
     where_.erase(id);
     ++evictions;
-    AdapterResidency &r = rec_[id];
+    AdapterResidency &r = *res_[slot];
+    res_[slot] = nullptr;
     ++r.eviction_count;
     r.last_evict_epoch = epoch_;
     return id;
@@ -111,6 +112,7 @@ AssignResult SlotTable::assign(uint64_t id, int rank, int *slot, uint64_t *evict
         *evicted_id = evict(s);
     }
     AdapterResidency &r = rec_[id];
+    res_[s] = &r;
     if (r.last_evict_epoch >= 0 && epoch_ - r.last_evict_epoch <= window_) ++reloads;
     ++r.load_count;
     r.rank = rank;

@@ -87,6 +87,9 @@ private:
     std::vector<int> refs_;
     std::unordered_map<uint64_t, int> where_;
     std::unordered_map<uint64_t, AdapterResidency> rec_;
+    // The record of each occupied slot's adapter (elements of an unordered_map
+    // keep their address across insertions), so victim scans need no lookup.
+    std::vector<AdapterResidency *> res_;
 };
 
 }  // namespace lora
