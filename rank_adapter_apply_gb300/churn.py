@@ -171,6 +171,23 @@ class ChurnRunner:
         self._ranks_p = self._ranks.ctypes.data_as(P(ctypes.c_int))
         self._alphas = np.full(S, alpha, np.float32)
         self._alphas_p = self._alphas.ctypes.data_as(P(ctypes.c_float))
+        # per-call buffers as ctypes arrays with numpy views over them (filled
+        # through the views, handed to the library as they are)
+        nl = len(self.layers)
+        self._gids_c = (ctypes.c_uint64 * tokens)()
+        self._gids = np.frombuffer(self._gids_c, dtype=np.uint64)
+        self._sl_c = (ctypes.c_int * S)()
+        self._sl = np.frombuffer(self._sl_c, dtype=np.int32)
+        self._ap_c = (ctypes.c_void_p * (S * nl))()
+        self._ap = np.frombuffer(self._ap_c, dtype=np.uint64)
+        self._bp_c = (ctypes.c_void_p * (S * nl))()
+        self._bp = np.frombuffer(self._bp_c, dtype=np.uint64)
+        self._nd, self._done = ctypes.c_int(0), ctypes.c_int(0)
+        self._nd_r, self._done_r = ctypes.byref(self._nd), ctypes.byref(self._done)
+        self._idx_np = [[self.idx_host[rb, gi].numpy() for gi in range(self.max_groups)] for rb in range(self.ring)]
+        self._idx_p = [[ctypes.cast(self.idx_host[rb, gi].data_ptr(), P(ctypes.c_int)) for gi in range(self.max_groups)]
+                       for rb in range(self.ring)]
+        self._idx_addr = [[self.idx_host[rb, gi].data_ptr() for gi in range(self.max_groups)] for rb in range(self.ring)]
 
     def upload(self, slot, adapter):
         a = [self.A[l][adapter] for l in self.layers]
@@ -209,16 +226,14 @@ class ChurnRunner:
                 # assign (hit: touch; miss: free slot or policy victim), take an
                 # in-flight reference, write every token's slot id (-1: not in
                 # this group) straight into the pinned slot-id buffer
-                gids = np.where(tok_group == gi, ids_u, np.uint64(B.NO_ID))
-                idx_h = self.idx_host[rb, gi].numpy()
-                nd, done = ctypes.c_int(0), ctypes.c_int(0)
-                rc = lib.lora_assign_tokens(ctx, self.T, gids.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)),
-                                            self._ranks_p, 1, idx_h.ctypes.data_as(ctypes.POINTER(ctypes.c_int)),
+                np.copyto(self._gids, np.where(tok_group == gi, ids_u, np.uint64(B.NO_ID)))
+                idx_h = self._idx_np[rb][gi]
+                rc = lib.lora_assign_tokens(ctx, self.T, self._gids_c, self._ranks_p, 1, self._idx_p[rb][gi],
                                             self.S, self._dids_p, self._slots_p, self._need_p, self._ev_p,
-                                            ctypes.byref(nd), ctypes.byref(done))
-                n = nd.value
+                                            self._nd_r, self._done_r)
+                n = self._nd.value
                 if rc != 0:
-                    raise RuntimeError(f"assign failed for adapter {group[done.value]}: {rc}")
+                    raise RuntimeError(f"assign failed for adapter {group[self._done.value]}: {rc}")
                 slots, need = self._slots[:n], self._need[:n]
                 if record:
                     decisions += [(k, a, 0, int(sl), int(nd_), -1 if ev_ == np.uint64(B.NO_ID) else int(ev_))
@@ -232,14 +247,12 @@ class ChurnRunner:
                 if len(miss) and self.batched_upload:
                     ad = np.asarray(group, dtype=np.int64)[miss]
                     m = len(miss)
-                    sl_m = np.ascontiguousarray(slots[miss])
-                    a_p = np.ascontiguousarray(self.A_ptr[ad].ravel())
-                    b_p = np.ascontiguousarray(self.B_ptr[ad].ravel())
-                    P = ctypes.POINTER
-                    rc = lib.lora_load_slots(ctx, m, sl_m.ctypes.data_as(P(ctypes.c_int)),
-                                             a_p.ctypes.data_as(P(ctypes.c_void_p)),
-                                             b_p.ctypes.data_as(P(ctypes.c_void_p)), self._ranks_p, self._alphas_p)
-                    B.check(rc)
+                    nl = len(self.layers)
+                    self._sl[:m] = slots[miss]
+                    self._ap[:m * nl] = self.A_ptr[ad].ravel()
+                    self._bp[:m * nl] = self.B_ptr[ad].ravel()
+                    B.check(lib.lora_load_slots(ctx, m, self._sl_c, self._ap_c, self._bp_c, self._ranks_p,
+                                                self._alphas_p))
                 else:
                     for i in miss:
                         self.upload(int(slots[i]), group[i])
@@ -248,8 +261,7 @@ class ChurnRunner:
                 # the kernels read the slot ids straight from the pinned buffer
                 # (same address on the device; it is rewritten only after the
                 # step that used it has finished)
-                B.check(lib.lora_apply_multi(ctx, 2, self._lay, self._xs, self._ys, self.idx_host[rb, gi].data_ptr(),
-                                             self.T))
+                B.check(lib.lora_apply_multi(ctx, 2, self._lay, self._xs, self._ys, self._idx_addr[rb][gi], self.T))
                 B.check(lib.lora_release_batch(ctx, n, self._slots_p))
                 tokens += int(sel.sum())
             ev = torch.cuda.Event()
