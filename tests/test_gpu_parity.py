@@ -92,6 +92,24 @@ def test_cluster_decode_partial_stages(d_in, d_out, R, early):
     check_layer(w, "l0", out["l0"])
 
 
+@pytest.mark.parametrize("T,S,one_slot", [(1024, 40, False), (1025, 40, False), (1024, 8, True)])
+def test_small_batch_limits(T, S, one_slot):
+    """The cluster path at its largest batch (1024 tokens) and one token past it
+    (general path), with more than 32 slots (the tile prefix runs through shared
+    memory) or every token on one slot (64 tiles of one slot)."""
+    rng = np.random.default_rng(T + S)
+    R = 32
+    ranks = [int(rng.choice([8, 16, 24, 32])) for _ in range(S)]
+    if one_slot:
+        idx = np.full(T, 3, np.int32)
+    else:
+        idx = rng.integers(-1, S, size=T).astype(np.int32)
+    w = _custom(T, 512, 256, S, R, ranks, idx, seed=T + 1)
+    out, st = _run(w)
+    check_layer(w, "l0", out["l0"])
+    assert st["device_wait_timeouts"] == 0
+
+
 def test_all_base_only_is_bitwise_noop():
     T = 64
     w = _custom(T, 512, 256, 4, 16, [16] * 4, np.full(T, -1))
