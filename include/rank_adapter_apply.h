@@ -80,6 +80,8 @@ typedef struct {
     int64_t epoch;                  /* current epoch (lora_tick) */
     uint64_t device_wait_timeouts;  /* non-zero: a bounded device-side wait gave up and the
                                        rows it guarded were left unchanged (never expected) */
+    uint64_t cluster_applies;       /* applies served by the single-launch cluster decode kernel */
+    uint64_t grouped_applies;       /* applies served by grouping + prefill / decode kernels */
 } lora_stats_t;
 
 /*
@@ -341,10 +343,12 @@ int lora_set_adapter_priority(lora_ctx *ctx, uint64_t adapter_id, double priorit
 int lora_set_prefill_min_tokens(lora_ctx *ctx, int n);
 
 /*
- * Batches of at most n tokens (0..1024, default 1024) take the single-launch
- * decode kernel (thread-block clusters), which treats every token as a decode
- * token; larger batches take the grouping + tensor-core prefill + decode
- * kernels. 0 always takes the latter.
+ * Batches of at most n tokens (0..1024) take the single-launch decode kernel
+ * (thread-block clusters), which treats every token as a decode token; larger
+ * batches take the grouping + tensor-core prefill + decode kernels. 0 always
+ * takes the latter. Until this is called the limit follows max_lora_rank:
+ * 1024 tokens up to rank 16, 512 up to rank 32, 0 above (where the grouped
+ * kernels are faster at every batch size).
  */
 int lora_set_small_batch_tokens(lora_ctx *ctx, int n);
 

@@ -49,7 +49,8 @@ class LoraStats(ctypes.Structure):
                 ("rejected", ctypes.c_uint64), ("uploads", ctypes.c_uint64),
                 ("upload_bytes", ctypes.c_uint64), ("invalid_token_index", ctypes.c_uint64),
                 ("upload_seconds", ctypes.c_double), ("epoch", ctypes.c_int64),
-                ("device_wait_timeouts", ctypes.c_uint64)]
+                ("device_wait_timeouts", ctypes.c_uint64), ("cluster_applies", ctypes.c_uint64),
+                ("grouped_applies", ctypes.c_uint64)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}

@@ -84,8 +84,9 @@ struct lora_ctx {
     std::vector<UploadTiming> timing;
     double upload_seconds = 0.0;
     uint64_t uploads = 0, upload_bytes = 0, invalid_seen = 0;
+    uint64_t cluster_applies = 0, grouped_applies = 0;   // which path served each apply
     int prefill_min = 0;          // shortest same-slot run sent to the tensor-core prefill kernel
-    int small_batch = kFusedMaxTokens;   // batches up to this size take the cluster decode kernel
+    int small_batch = -1;         // batches up to this size take the cluster decode kernel; -1: by rank
     int inputs_ready = 0;         // caller: x, slot ids, pools not written by the preceding kernel
     int num_sms = 148;
     // Per-slot tracking (lora_set_slot_tracking): apply i records ring[i % kRing];
@@ -549,6 +550,17 @@ int fused_apply(lora_ctx *c, int n, const int *layers, const void *const *xs, vo
     return LORA_OK;
 }
 
+// Largest batch the cluster decode kernel takes. Unless the caller set it,
+// it follows max_lora_rank: the kernel's registers grow with the rank (five
+// CTAs per SM at rank 16, three at rank 32, one at rank 64), and measured on
+// GB300 (q_proj + v_proj 4096 x 4096) it beats the grouped kernels at every
+// batch size up to 1024 tokens at rank 16, up to about 512 at rank 32 (even at
+// 1024), and at none at rank 64 (three times slower at 1024 tokens).
+int small_batch_limit(const lora_ctx *c) {
+    if (c->small_batch >= 0) return c->small_batch;
+    return c->R <= 16 ? kFusedMaxTokens : (c->R <= 32 ? kFusedMaxTokens / 2 : 0);
+}
+
 int apply_impl(lora_ctx *c, int n, const int *layers, const void *const *xs, void *const *ys,
                const int32_t *idx, int T) {
     if (!c) return fail(LORA_ERR_ARG, "ctx is NULL");
@@ -581,10 +593,12 @@ int apply_impl(lora_ctx *c, int n, const int *layers, const void *const *xs, voi
                                             "call lora_sync_uploads before capturing", s);
     }
 
-    if (c->dtype == LORA_DTYPE_BF16 && T <= c->small_batch) {
+    if (c->dtype == LORA_DTYPE_BF16 && T <= small_batch_limit(c)) {
         int rc = fused_apply(c, n, layers, xs, ys, idx, T);
+        if (rc == LORA_OK) ++c->cluster_applies;
         if (rc != 1) return rc;          // 1: shapes not eligible, take the general path
     }
+    ++c->grouped_applies;
 
     // Long same-slot runs go to the tensor-core prefill kernel when every layer allows it.
     bool prefill = c->prefill_min > 0 && c->dtype == LORA_DTYPE_BF16 && prefill_tc_supported(c->R) &&
@@ -1054,6 +1068,8 @@ int lora_stats(lora_ctx *c, lora_stats_t *o) {
         int rc = harvest_timings(c, false);
         if (rc != LORA_OK) return rc;
     }
+    o->cluster_applies = c->cluster_applies;
+    o->grouped_applies = c->grouped_applies;
     o->hits = c->table.hits;
     o->misses = c->table.misses;
     o->evictions = c->table.evictions;

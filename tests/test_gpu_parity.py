@@ -83,7 +83,7 @@ def test_cluster_decode_partial_stages(d_in, d_out, R, early):
     ranks = [R, max(1, R // 2), 8, R, 5]
     idx = rng.integers(-1, S, size=T)
     w = _custom(T, d_in, d_out, S, R, ranks, idx, seed=d_out)
-    dw = DeviceWorkload(w)
+    dw = DeviceWorkload(w, small_batch_tokens=1024)       # the cluster kernel at every rank
     try:
         B.lora_set_inputs_ready(dw.slots.ctx, early)
         out = dw.run(None, multi=True)
@@ -105,9 +105,29 @@ def test_small_batch_limits(T, S, one_slot):
     else:
         idx = rng.integers(-1, S, size=T).astype(np.int32)
     w = _custom(T, 512, 256, S, R, ranks, idx, seed=T + 1)
-    out, st = _run(w)
+    out, st = _run(w, small_batch_tokens=1024)            # rank 32: the cluster kernel up to 1024 tokens
     check_layer(w, "l0", out["l0"])
     assert st["device_wait_timeouts"] == 0
+
+
+def test_small_batch_limit_follows_rank():
+    """Without an explicit limit, rank 64 pools send small batches to the
+    grouped kernels and rank 16 pools to the cluster kernel."""
+    from rank_adapter_apply_gb300 import binding as B
+    from rank_adapter_apply_gb300.harness import DeviceWorkload
+    for R, grouped in ((16, False), (64, True)):
+        rng = np.random.default_rng(R)
+        T = 64
+        idx = rng.integers(0, 4, size=T)
+        w = _custom(T, 512, 256, 4, R, [R] * 4, idx, seed=R)
+        dw = DeviceWorkload(w)
+        try:
+            out = dw.run(None, multi=True)
+            check_layer(w, "l0", out["l0"])
+            st = dw.slots.stats()
+        finally:
+            dw.close()
+        assert (st["grouped_applies"], st["cluster_applies"]) == ((1, 0) if grouped else (0, 1)), (R, st)
 
 
 def test_all_base_only_is_bitwise_noop():
@@ -146,13 +166,16 @@ def test_empty_slot_and_invalid_indices():
     assert st["invalid_token_index"] == 10
 
 
-def test_max_rank_64_mixed():
+@pytest.mark.parametrize("small_batch", [None, 1024])
+def test_max_rank_64_mixed(small_batch):
+    """max_lora_rank 64: the grouped kernels by default, the cluster kernel
+    when the caller asks for it."""
     T = 96
     rng = np.random.default_rng(9)
     ranks = [8, 16, 32, 64, 48, 24]
     idx = rng.integers(0, 6, size=T)
     w = _custom(T, 1024, 512, 6, 64, ranks, idx)
-    out, _ = _run(w)
+    out, _ = _run(w, small_batch_tokens=small_batch)
     check_layer(w, "l0", out["l0"])
 
 
