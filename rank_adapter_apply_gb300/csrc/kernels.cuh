@@ -11,7 +11,8 @@ namespace lora {
 
 constexpr int kTileTokens = 16;      // decode tile: tokens of one slot per CTA row
 constexpr int kPrefillRows = 128;    // prefill tile: rows of one same-slot segment
-constexpr int kMinPrefillRun = 64;   // shortest run routed to the prefill path
+constexpr int kMinPrefillRun = 32;   // shortest run the prefill path may be given (workspace bound)
+constexpr int kDefaultPrefillRun = 64;   // shortest run routed to the prefill path by default
 constexpr int kMaxLayersPerCall = 8;
 constexpr int kMaxChunks = 16;       // split of d_in in the decode shrink
 constexpr int kPartialRowCap = 65536;

@@ -308,7 +308,7 @@ int lora_slots_init(lora_ctx **out, int max_loras, int max_lora_rank, int max_to
     if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
         return reject(LORA_ERR_ARG, "workspace must be 256-byte aligned");
     c->device = true;
-    c->prefill_min = kMinPrefillRun;
+    c->prefill_min = kDefaultPrefillRun;
     c->max_tokens = max_tokens;
     c->max_layers = max_layers_per_call;
     c->layers.assign(layers, layers + n_layers);

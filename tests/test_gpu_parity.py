@@ -264,6 +264,20 @@ def test_tensor_core_prefill_ragged_dims(R):
     assert st["device_wait_timeouts"] == 0
 
 
+@pytest.mark.parametrize("R", [16, 64])
+def test_tensor_core_prefill_short_runs(R):
+    """Threshold 32: runs of 32-63 tokens take the tensor-core prefill path
+    (a single ragged tile each), shorter ones the decode kernels."""
+    rng = np.random.default_rng(R + 3)
+    runs = [(0, 32), (1, 33), (2, 31), (3, 47), (-1, 5), (1, 63), (0, 64), (2, 40), (3, 1), (1, 32)]
+    idx = np.concatenate([np.full(n, s) for s, n in runs]).astype(np.int32)
+    ranks = [R, max(8, R // 2), 8, R]
+    w = _custom(idx.shape[0], 512, 384, 4, R, ranks, idx, seed=R + 5)
+    out, st = _run(w, small_batch_tokens=0, prefill_min_tokens=32)
+    check_layer(w, "l0", out["l0"])
+    assert st["device_wait_timeouts"] == 0
+
+
 def test_prefill_small_general_path_matches_oracle():
     w = wl.prefill_5120(1, n_seqs=5, len_range=(60, 300))
     out, st = _run(w, small_batch_tokens=0)
