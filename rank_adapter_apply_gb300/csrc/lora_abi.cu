@@ -1018,7 +1018,8 @@ int lora_set_prefill_min_tokens(lora_ctx *c, int n) {
 }
 
 int lora_set_small_batch_tokens(lora_ctx *c, int n) {
-    if (!c || n < 0 || n > kFusedMaxTokens) return fail(LORA_ERR_ARG, "n must be in 0..%d", kFusedMaxTokens);
+    if (!c || n < -1 || n > kFusedMaxTokens)
+        return fail(LORA_ERR_ARG, "n must be -1 (by rank) or in 0..%d", kFusedMaxTokens);
     c->small_batch = n;
     return LORA_OK;
 }

@@ -321,6 +321,18 @@ def test_assign_tokens_matches_simulator_and_maps_tokens(lib):
         B.lora_destroy(ctx)
 
 
+def test_small_batch_limit_arguments(lib):
+    """-1 restores the rank-based limit; 0..1024 set it; anything else is refused."""
+    ctx = _host_ctx(4, 16)
+    try:
+        for n in (-1, 0, 512, 1024, -1):
+            assert lib.lora_set_small_batch_tokens(ctx, n) == 0
+        for n in (-2, 1025):
+            assert lib.lora_set_small_batch_tokens(ctx, n) == B.LORA_ERR_ARG
+    finally:
+        B.lora_destroy(ctx)
+
+
 def test_selftest_needs_a_device_context(lib):
     ctx = _host_ctx(2, 16)
     try:
