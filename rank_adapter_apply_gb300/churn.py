@@ -50,6 +50,19 @@ def plan_groups(order, pinned_resident, capacity):
     return groups
 
 
+def plan_step(ids, pinned_resident, capacity):
+    """A step's distinct adapters in first-appearance order, cut into groups by
+    plan_groups, and the group of every token (numpy int32 per token)."""
+    ids = np.asarray(ids)
+    uniq, first, inv = np.unique(ids, return_index=True, return_inverse=True)
+    ford = np.argsort(first)
+    order = [int(a) for a in uniq[ford]]
+    groups = plan_groups(order, pinned_resident, capacity)
+    gof = np.empty(len(uniq), np.int32)                  # group of each distinct adapter
+    gof[ford] = np.repeat(np.arange(len(groups), dtype=np.int32), [len(g) for g in groups])
+    return groups, gof[inv.reshape(-1)]
+
+
 def admission_stats(trace, max_loras=64, rank=16, policy=0, weights=None, pin_top=0,
                     min_residency=0, window=10, record=False):
     """Host-only replay of the churn admission: per step, groups of adapters are
@@ -212,13 +225,7 @@ class ChurnRunner:
                 with torch.cuda.stream(self.slots.compute):
                     for y, y0 in zip(self.y, self.y0):
                         y.copy_(y0)
-            uniq, first, inv = np.unique(ids, return_index=True, return_inverse=True)
-            ford = np.argsort(first)                             # distinct, first appearance
-            order = [int(a) for a in uniq[ford]]
-            groups = plan_groups(order, self.pinned, self.S - len(self.pinned))
-            gof = np.empty(len(uniq), np.int32)                  # group of each distinct adapter
-            gof[ford] = np.repeat(np.arange(len(groups), dtype=np.int32), [len(g) for g in groups])
-            tok_group = gof[inv]
+            groups, tok_group = plan_step(ids, self.pinned, self.S - len(self.pinned))
             ids_u = ids.astype(np.uint64)
             slot_tok = np.full(self.T, -1, np.int32)
             for gi, group in enumerate(groups):

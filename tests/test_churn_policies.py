@@ -69,3 +69,21 @@ def test_policies_beat_pure_lru_on_the_churn_trace():
         assert other["hit_rate"] > lru["hit_rate"]
         assert other["reloads_after_eviction"] < lru["reloads_after_eviction"]
         assert other["thrash_ratio"] < lru["thrash_ratio"]
+
+
+@pytest.mark.parametrize("capacity,pinned", [(64, {}), (5, {}), (5, {3: 0, 7: 1, 11: 2})])
+def test_plan_step_groups_every_token(capacity, pinned):
+    """plan_step: groups hold the step's distinct adapters in first-appearance
+    order with at most `capacity` unpinned ones each, and every token is given
+    the group that holds its adapter (checked with a plain loop)."""
+    import numpy as np
+    trace = wl.churn_trace(3, n_steps=12)
+    for ids in trace.steps:
+        groups, tok_group = churn.plan_step(ids, pinned, capacity)
+        order = [a for g in groups for a in g]
+        assert order == list(dict.fromkeys(int(a) for a in ids))
+        for g in groups:
+            assert sum(1 for a in g if a not in pinned) <= capacity
+        where = {a: gi for gi, g in enumerate(groups) for a in g}
+        assert tok_group.dtype == np.int32 and tok_group.shape == (len(ids),)
+        assert [int(x) for x in tok_group] == [where[int(a)] for a in ids]
