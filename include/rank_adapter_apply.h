@@ -258,13 +258,15 @@ int lora_set_thrash_window(lora_ctx *ctx, int epochs);
  * the TTFT decomposition there). slots[n], ranks[n], alphas[n]; A_host and
  * B_host hold n * n_layers host pointers, adapter-major (entry i * n_layers +
  * l is layer l of adapter i), each laid out as for lora_load_slot. Adapters
- * whose buffers are page-locked and device-mapped (cudaHostAlloc, torch
- * pin_memory) with 16-byte aligned rows (r * bytes_per_param and d_in *
- * bytes_per_param multiples of 16) are copied by one kernel that reads host
- * memory directly and also zero-fills the padding and sets scale = alpha / r
- * and the rank; any other adapter takes the copy-engine path of
- * lora_load_slot. Same ordering, events and statistics as n calls of
- * lora_load_slot. Everything is validated before anything is queued
+ * the GPU can read in place with 16-byte aligned rows (r * bytes_per_param
+ * and d_in * bytes_per_param multiples of 16) are copied by one kernel that
+ * reads host memory directly and also zero-fills the padding and sets scale =
+ * alpha / r and the rank: any host memory where the device walks the host's
+ * page tables (pageable-memory access through host page tables, as on
+ * Grace-based systems), else page-locked device-mapped buffers (cudaHostAlloc,
+ * torch pin_memory). Any other adapter takes the copy-engine path of
+ * lora_load_slot. Same ordering and statistics as n calls of lora_load_slot
+ * (one event covers the whole call). Everything is validated before anything is queued
  * (LORA_ERR_ARG: bad slot, a slot twice, NULL; LORA_ERR_RANK). The host
  * buffers must stay alive and unchanged until lora_sync_uploads returns.
  */
