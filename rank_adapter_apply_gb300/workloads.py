@@ -235,11 +235,13 @@ def churn_trace(seed: int = 0, n_adapters: int = 512, n_steps: int = 200,
                 burst_len: int = 20) -> ChurnTrace:
     """Adapter ids per decode step. Zipf(zipf_s) over n_adapters (id = rank-1).
     At steps k with k % burst_every == 0 and k > 0 the last burst_len tokens take
-    burst_len distinct ids never used so far, taken from the tail (highest id
-    downward)."""
+    burst_len distinct cold ids: ids not used in the burst_every steps before,
+    taken from the tail (highest id downward). (Ids never used at all run out:
+    with Zipf(1.2) over 512 ids one is left before step 100 and none before
+    step 150.)"""
     rng = np.random.default_rng(seed)
     p = zipf_probs(n_adapters, zipf_s)
-    used: set[int] = set()
+    last_use = np.full(n_adapters, -(1 << 30), np.int64)    # step of each id's last use
     steps = []
     for k in range(n_steps):
         ids = rng.choice(n_adapters, size=tokens, p=p).astype(np.int64)
@@ -247,11 +249,11 @@ def churn_trace(seed: int = 0, n_adapters: int = 512, n_steps: int = 200,
             cold = []
             cand = n_adapters - 1
             while len(cold) < burst_len and cand >= 0:
-                if cand not in used:
+                if last_use[cand] < k - burst_every:
                     cold.append(cand)
                 cand -= 1
             ids[tokens - len(cold):] = np.array(cold, dtype=np.int64)
-        used.update(int(i) for i in np.unique(ids))
+        last_use[np.unique(ids)] = k
         steps.append(ids)
     return ChurnTrace(n_adapters, steps)
 
