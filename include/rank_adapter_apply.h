@@ -351,7 +351,7 @@ int lora_set_prefill_min_tokens(lora_ctx *ctx, int n);
  * (thread-block clusters), which treats every token as a decode token; larger
  * batches take the grouping + tensor-core prefill + decode kernels. 0 always
  * takes the latter. By default (and after n = -1) the limit follows
- * max_lora_rank: 1024 tokens up to rank 16, 512 up to rank 32, 0 above (where
+ * max_lora_rank: 1024 tokens up to rank 16, 768 up to rank 32, 0 above (where
  * the grouped kernels are faster at every batch size).
  */
 int lora_set_small_batch_tokens(lora_ctx *ctx, int n);

@@ -554,11 +554,11 @@ int fused_apply(lora_ctx *c, int n, const int *layers, const void *const *xs, vo
 // it follows max_lora_rank: the kernel's registers grow with the rank (five
 // CTAs per SM at rank 16, three at rank 32, one at rank 64), and measured on
 // GB300 (q_proj + v_proj 4096 x 4096) it beats the grouped kernels at every
-// batch size up to 1024 tokens at rank 16, up to about 512 at rank 32 (even at
+// batch size up to 1024 tokens at rank 16, up to 768 at rank 32 (slower at
 // 1024), and at none at rank 64 (three times slower at 1024 tokens).
 int small_batch_limit(const lora_ctx *c) {
     if (c->small_batch >= 0) return c->small_batch;
-    return c->R <= 16 ? kFusedMaxTokens : (c->R <= 32 ? kFusedMaxTokens / 2 : 0);
+    return c->R <= 16 ? kFusedMaxTokens : (c->R <= 32 ? 768 : 0);
 }
 
 int apply_impl(lora_ctx *c, int n, const int *layers, const void *const *xs, void *const *ys,

@@ -105,7 +105,7 @@ def test_small_batch_limits(T, S, one_slot):
     else:
         idx = rng.integers(-1, S, size=T).astype(np.int32)
     w = _custom(T, 512, 256, S, R, ranks, idx, seed=T + 1)
-    out, st = _run(w, small_batch_tokens=1024)            # rank 32: the cluster kernel up to 1024 tokens
+    out, st = _run(w, small_batch_tokens=1024)            # the cluster kernel up to 1024 tokens at rank 32
     check_layer(w, "l0", out["l0"])
     assert st["device_wait_timeouts"] == 0
 
