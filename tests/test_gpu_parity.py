@@ -112,12 +112,11 @@ def test_small_batch_limits(T, S, one_slot):
 
 def test_small_batch_limit_follows_rank():
     """Without an explicit limit, rank 64 pools send small batches to the
-    grouped kernels and rank 16 pools to the cluster kernel."""
-    from rank_adapter_apply_gb300 import binding as B
+    grouped kernels, rank 32 pools batches up to 768 tokens and rank 16 pools
+    batches up to 1024 tokens to the cluster kernel."""
     from rank_adapter_apply_gb300.harness import DeviceWorkload
-    for R, grouped in ((16, False), (64, True)):
-        rng = np.random.default_rng(R)
-        T = 64
+    for R, T, grouped in ((16, 64, False), (64, 64, True), (32, 768, False), (32, 769, True)):
+        rng = np.random.default_rng(R + T)
         idx = rng.integers(0, 4, size=T)
         w = _custom(T, 512, 256, 4, R, [R] * 4, idx, seed=R)
         dw = DeviceWorkload(w)
@@ -127,7 +126,7 @@ def test_small_batch_limit_follows_rank():
             st = dw.slots.stats()
         finally:
             dw.close()
-        assert (st["grouped_applies"], st["cluster_applies"]) == ((1, 0) if grouped else (0, 1)), (R, st)
+        assert (st["grouped_applies"], st["cluster_applies"]) == ((1, 0) if grouped else (0, 1)), (R, T, st)
 
 
 def test_all_base_only_is_bitwise_noop():
