@@ -114,7 +114,7 @@ __device__ __forceinline__ void shrink_bf16_tile(const LayerArgs &L, const Group
     const int r = tile.w;                      // the slot's rank, from the grouping
     const int nmb = (r + 15) >> 4;
     const int R = g.R, d_in = L.d_in;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2;
 
     const int tok0 = gq < cnt ? g.perm[p0 + gq] : -1;
     const int tok1 = gq + 8 < cnt ? g.perm[p0 + 8 + gq] : -1;
