@@ -341,3 +341,29 @@ def test_selftest_needs_a_device_context(lib):
         assert lib.lora_selftest_wait_timeout(ctx, ctypes.byref(g)) == B.LORA_ERR_STATE
     finally:
         B.lora_destroy(ctx)
+
+
+def test_static_scratch_validates_before_touching_the_device(lib):
+    """lora_apply_static_scratch checks its arguments before any CUDA call, so
+    every rejection below (and the empty batch) is decided on the host. The
+    pointer values are never dereferenced: each case returns before a launch."""
+    P = 0x10000                                     # 16-byte aligned stand-in address
+    ok = dict(x=P, y=P, idx=P, T=64, d_in=512, d_out=512, S=4, R=16, dtype=B.LORA_DTYPE_BF16,
+              A=P, B=P, scale=P, rank=P)
+
+    def call(**kw):
+        a = {**ok, **kw}
+        return lib.lora_apply_static_scratch(a["x"], a["y"], a["idx"], a["T"], a["d_in"],
+                                             a["d_out"], a["S"], a["R"], a["dtype"], a["A"],
+                                             a["B"], a["scale"], a["rank"], None)
+
+    assert call(T=0) == B.LORA_OK                      # empty batch: nothing to do
+    assert call(T=0, x=None, A=None) == B.LORA_OK      # not even the pointers are read
+    bad = [dict(dtype=9), dict(S=0), dict(S=257), dict(R=4), dict(R=12), dict(R=72),
+           dict(R=264, dtype=B.LORA_DTYPE_F32), dict(d_in=0), dict(d_out=0), dict(T=-1),
+           dict(x=None), dict(y=None), dict(idx=None), dict(A=None), dict(B=None),
+           dict(scale=None), dict(rank=None), dict(A=P + 8), dict(B=P + 2),
+           dict(T=9000, R=64)]                      # partials of 9000 x 64 fp32 exceed 4 MiB
+    for kw in bad:
+        assert call(**kw) == B.LORA_ERR_ARG, kw
+    assert "static scratch" in B.last_error()
