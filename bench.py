@@ -183,10 +183,21 @@ def make_batches(n_sets: int, seed0: int = 0):
     return w, batches
 
 
-def cpu_oracle_run(w, batches, budget_s: float = 10.0, max_batches=None):
+def cpu_oracle_run(w, batches, budget_s: float = 10.0, max_batches=None, threads=None):
     """Time the fp64 oracle over whole batches (both layers) until the budget
-    is spent. Returns (delta tokens/s, batches done, threads)."""
+    is spent, on `threads` host threads (default: all cores). Returns
+    (delta tokens/s, batches done, threads used, seconds)."""
     import oracle
+    all_cores = oracle.threads()
+    if threads is not None:
+        oracle.set_threads(threads)
+    try:
+        return _time_oracle(oracle, w, batches, budget_s, max_batches)
+    finally:
+        oracle.set_threads(all_cores)
+
+
+def _time_oracle(oracle, w, batches, budget_s, max_batches):
     pools = {ly.name: w.padded_pools(ly.name) for ly in w.layers}
     oracle.lora_apply_ref(batches[0][0][:1], batches[0][1]["q_proj"][:1], *pools["q_proj"],
                           w.ranks, w.alphas, batches[0][2][:1])        # build + load outside timing
@@ -403,10 +414,8 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quick:
         v, n, cores, el = cpu_oracle_run(w, batches, budget_s=args.cpu_seconds)
         # the same oracle on one thread, over a shorter sample
-        import oracle
-        oracle.set_threads(1)
-        v1, n1, _, el1 = cpu_oracle_run(w, batches, budget_s=max(1.0, args.cpu_seconds / 3))
-        oracle.set_threads(cores)
+        v1, n1, _, el1 = cpu_oracle_run(w, batches, budget_s=max(1.0, args.cpu_seconds / 3),
+                                        threads=1)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                                 "sample": f"{n} whole batches (256 tokens, q_proj+v_proj) in {el:.1f} s",
                                 "single_thread": {"value": v1, "cores": 1,
