@@ -367,3 +367,11 @@ def test_static_scratch_validates_before_touching_the_device(lib):
     for kw in bad:
         assert call(**kw) == B.LORA_ERR_ARG, kw
     assert "static scratch" in B.last_error()
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """With the compiled library absent the binding raises; there is no other
+    implementation to fall back on."""
+    monkeypatch.setattr(B, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        B.load(str(tmp_path / "librank_adapter_apply.so"))
