@@ -95,10 +95,10 @@ struct lora_ctx {
     std::vector<cudaEvent_t> ring;
     std::vector<int64_t> slot_gen;
     int64_t n_apply = 0;
-    // Host-buffer path: call k records host_ev[k % kHostRing] on the compute
-    // stream after its copies back; buf_use maps each device staging buffer to
-    // the last call that used it; h2d_done marks a call's copies in (upload
-    // stream).
+    // Host-buffer path: call k records host_ev[k % kHostRing] on the download
+    // stream after its copies back (on the compute stream under capture);
+    // buf_use maps each device staging buffer to the last call that used it;
+    // h2d_done marks a call's copies in (upload stream), apply_done its apply.
     std::vector<cudaEvent_t> host_ev;
     std::vector<std::pair<const void *, int64_t>> buf_use;
     int64_t n_host = 0, host_forgot = -1;
