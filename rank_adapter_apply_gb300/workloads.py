@@ -168,9 +168,12 @@ def decode_batch(rng, T: int, S: int, direct_base: bool, layers=DECODE_LAYERS,
     return x, ys, idx
 
 
-def decode_qv_4096(seed: int = 0, direct_base: bool = False, n_tokens: int = 256) -> Workload:
+def decode_qv_4096(seed: int = 0, direct_base: bool = False, n_tokens: int = 256,
+                   rank: int = 16) -> Workload:
+    """Decode batch on q_proj and v_proj (4096 -> 4096, bf16), 8 slots of one
+    rank (16 by default; max_lora_rank the same), alpha = 2 x rank."""
     rng = np.random.default_rng(seed)
-    S, R, r, alpha, T = 8, 16, 16, 32.0, n_tokens
+    S, R, r, alpha, T = 8, rank, rank, 2.0 * rank, n_tokens
     layers = list(DECODE_LAYERS)
     adapters = [_adapter(rng, layers, r, DTYPE_BF16) for _ in range(S)]
     x, ys, idx = decode_batch(rng, T, S, direct_base, layers)

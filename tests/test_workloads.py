@@ -91,3 +91,13 @@ def test_churn_trace_bursts():
     assert not (set(int(a) for a in t.steps[50][-20:]) & never)
     first = np.concatenate(t.steps[:40])
     assert np.bincount(first, minlength=512)[0] == np.bincount(first, minlength=512).max()
+
+
+def test_decode_recipe_other_ranks():
+    """The decode recipe at another rank: every slot and max_lora_rank take it,
+    alpha = 2 x rank (scale 2), the batch keeps its 256 tokens."""
+    w16, w32 = wl.decode_qv_4096(0, direct_base=True), wl.decode_qv_4096(0, direct_base=True, rank=32)
+    assert w32.max_lora_rank == 32 and np.all(w32.ranks == 32) and np.all(w32.alphas == 64.0)
+    A, B = w32.adapters[5]["v_proj"]
+    assert A.shape == (32, 4096) and B.shape == (4096, 32)
+    assert w16.token_slot_idx.shape == w32.token_slot_idx.shape == (256,)
