@@ -321,6 +321,33 @@ def test_assign_tokens_matches_simulator_and_maps_tokens(lib):
         B.lora_destroy(ctx)
 
 
+def test_assign_tokens_large_batches_and_colliding_ids(lib):
+    """Thousands of tokens over 200 distinct adapters, with ids drawn from the
+    whole 63-bit range and with ids that differ only in their top bits (they
+    all land on one bucket of the call's hash table): the distinct list is in
+    order of first appearance and every token gets its adapter's slot."""
+    rng = np.random.default_rng(5)
+    for kind in ("random", "top_bits"):
+        ctx = _host_ctx(256, 16)
+        try:
+            if kind == "random":
+                pool = rng.integers(0, 2 ** 63 - 1, size=200, dtype=np.int64)
+            else:
+                pool = (np.arange(1, 201, dtype=np.int64) << 47)
+            T = 3000
+            ids = pool[rng.integers(0, len(pool), size=T)]
+            ids[rng.random(T) < 0.1] = -1
+            rc, tsi, dids, slots, need, ev, done = B.lora_assign_tokens(ctx, ids, np.full(T, 8, np.int32))
+            first = list(dict.fromkeys(int(a) for a in ids if a >= 0))
+            assert rc == 0 and done == len(first) and [int(a) for a in dids] == first
+            assert sorted(int(s_) for s_ in slots) == list(range(len(first)))   # lowest free slots
+            slot_of = dict(zip(first, (int(x) for x in slots)))
+            assert np.array_equal(tsi, np.array([slot_of[int(a)] if a >= 0 else -1 for a in ids], np.int32))
+            assert all(B.lora_lookup(ctx, a) == slot_of[a] for a in first[:20])
+        finally:
+            B.lora_destroy(ctx)
+
+
 def test_small_batch_limit_arguments(lib):
     """-1 restores the rank-based limit; 0..1024 set it; anything else is refused."""
     ctx = _host_ctx(4, 16)
