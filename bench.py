@@ -475,7 +475,7 @@ def run_e2e(args, w, batches, d0, stream, dev, world):
 
     ctx = d0.slots.ctx
     nh = min(E2E_HOST_SETS, len(batches))      # host buffer sets, reused after a sync
-    nd_sets = E2E_STAGING_SETS
+    nd_sets = args.e2e_staging_sets
     lib = B.load()
     import ctypes
     # One pinned block per host set and one device block per staging set, each
@@ -559,7 +559,7 @@ def run_e2e(args, w, batches, d0, stream, dev, world):
     floor = link_floor(hblk, dblk, blk - off_y[0], off_y[0], dev)
     return {"value": job_toks / el, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": k, "us_per_step": el / k * 1e6,
-            "link_floor": floor,
+            "link_floor": floor, "host_sets": nh, "staging_sets": nd_sets,
             "timing": "wall clock, host admission + H2D + apply + D2H per step"}
 
 
@@ -714,9 +714,13 @@ def main():
                     help="churn: one upload kernel per group (default) or copy-engine copies per adapter")
     ap.add_argument("--churn-overlap", action="store_true",
                     help="churn: per-slot upload ordering, host runs ahead of the GPU")
+    ap.add_argument("--e2e-staging-sets", type=int, default=E2E_STAGING_SETS,
+                    help="e2e: device staging sets rotated by the host-buffer calls")
     ap.add_argument("--quick", action="store_true",
                     help="profiling runs: no clock settling, no e2e, no CPU baseline")
     args = ap.parse_args()
+    if args.e2e_staging_sets < 1:
+        ap.error("--e2e-staging-sets must be >= 1")
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
