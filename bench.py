@@ -331,13 +331,18 @@ def run_ours(args):
     with torch.cuda.graph(g_all, stream=stream):
         for d in sets:
             step_apply(d)
-    g_one = []
+    g_one, per_step = [], set()
     for d in sets:
+        k0 = d.slots.stats()["kernel_launches"]
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             step_apply(d)
         g_one.append(g)
+        per_step.add(d.slots.stats()["kernel_launches"] - k0)   # kernels in one step, counted by the library
     torch.cuda.synchronize(dev)
+    if len(per_step) != 1:
+        raise RuntimeError(f"steps of different sets queue different kernel counts: {sorted(per_step)}")
+    launches_per_step = per_step.pop()
 
     def run_steps(k):
         full, rem = divmod(k, len(sets))
@@ -408,7 +413,7 @@ def run_ours(args):
                      "algorithmic_bytes_per_step": bytes_ / max(1, args.steps),
                      "tflops": flops / (ms * 1e-3) / 1e12},
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": launches_per_step * args.steps,
         "clocks": ClockSampler.summary(clock_rows),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quick:
@@ -613,9 +618,11 @@ def run_big(args, name):
         for _ in range(max(3, args.warmup)):
             dw.slots.apply_multi(lys, xs, ys, dw.idx)
     st.synchronize()
+    k0 = dw.slots.stats()["kernel_launches"]
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=st):
         dw.slots.apply_multi(lys, xs, ys, dw.idx)
+    per_step = dw.slots.stats()["kernel_launches"] - k0      # kernels in one replay of the step
     with torch.cuda.stream(st):
         for _ in range(3):
             g.replay()
@@ -649,8 +656,9 @@ def run_big(args, name):
                          "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "peak_kind": kind,
                          "traffic": None, "algorithmic_bytes_per_step": bytes_,
                          "tflops": flops * args.steps / (ms * 1e-3) / 1e12},
-            # grouping, prefill shrink, [chunk sums at rank 64], prefill expand, decode shrink + expand
-            "gpu_launches": (6 if name == "mixed_ranks_8b" else 5) * args.steps, "clocks": clocks}
+            # grouping, prefill shrink, [chunk sums at rank 64], prefill expand, decode shrink + expand,
+            # as counted by the library while the step was captured
+            "gpu_launches": per_step * args.steps, "clocks": clocks}
     print(json.dumps(line), flush=True)
     dw.close()
     return 0
@@ -688,7 +696,7 @@ def run_churn(args):
                       "hit_rate": d["hits"] / max(1, d["hits"] + d["misses"]),
                       "h2d_GBps": d["upload_bytes"] / up_s / 1e9 if up_s > 0 else None,
                       "delta_tokens_per_s": res.tokens / res.wall_s},
-            "gpu_launches": None}
+            "gpu_launches": st["kernel_launches"] - base["kernel_launches"]}
     print(json.dumps(line), flush=True)
     r.close()
     return 0

@@ -73,7 +73,7 @@ typedef struct {
     uint64_t evictions;             /* adapters removed from a slot */
     uint64_t reloads_after_eviction;/* misses within thrash_window epochs of that adapter's eviction */
     uint64_t rejected;              /* assigns refused before any eviction (bad rank) */
-    uint64_t uploads;               /* lora_load_slot calls that queued copies */
+    uint64_t uploads;               /* adapters uploaded (lora_load_slot, lora_load_slots) */
     uint64_t upload_bytes;          /* sum of (d_in + d_out) * r * bytes_per_param per upload */
     uint64_t invalid_token_index;   /* tokens with index < -1 or >= max_loras (skipped) */
     double upload_seconds;          /* device time of completed uploads */
@@ -82,6 +82,15 @@ typedef struct {
                                        rows it guarded were left unchanged (never expected) */
     uint64_t cluster_applies;       /* applies served by the single-launch cluster decode kernel */
     uint64_t grouped_applies;       /* applies served by grouping + prefill / decode kernels */
+    uint64_t kernel_launches;       /* kernels queued by this context's calls: 1 per cluster
+                                       apply; 3 per grouped apply (grouping, decode shrink,
+                                       decode expand) plus 2-3 tensor-core prefill kernels when
+                                       the batch has at least the prefill threshold of tokens
+                                       (queued even if no run is that long; they then exit at
+                                       once); 1 per lora_load_slot, per upload kernel of
+                                       lora_load_slots and per device-side eviction. A call
+                                       made during stream capture counts once, when captured,
+                                       however often the graph runs. */
 } lora_stats_t;
 
 /*

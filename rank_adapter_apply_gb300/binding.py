@@ -50,7 +50,7 @@ class LoraStats(ctypes.Structure):
                 ("upload_bytes", ctypes.c_uint64), ("invalid_token_index", ctypes.c_uint64),
                 ("upload_seconds", ctypes.c_double), ("epoch", ctypes.c_int64),
                 ("device_wait_timeouts", ctypes.c_uint64), ("cluster_applies", ctypes.c_uint64),
-                ("grouped_applies", ctypes.c_uint64)]
+                ("grouped_applies", ctypes.c_uint64), ("kernel_launches", ctypes.c_uint64)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}

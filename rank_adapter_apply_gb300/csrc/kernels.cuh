@@ -137,9 +137,10 @@ struct PrefillLayer {
     int d_in, d_out;
 };
 bool prefill_tc_supported(int R);
+// *kernels (if not NULL) is increased by the number of kernels queued (2 or 3).
 cudaError_t launch_prefill_tc(const PrefillLayer *layers, int n, int T, int S, int R, const float *scale,
                               int *hdr, const int4 *ptiles, int grid_tiles, int part_rows, int num_sms,
-                              cudaStream_t st);
+                              cudaStream_t st, int *kernels);
 
 // Batched slot upload (upload.cu): one kernel reads every adapter of a call
 // from page-locked host memory (device-mapped) into its slot rows.

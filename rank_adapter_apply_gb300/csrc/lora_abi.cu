@@ -85,6 +85,7 @@ struct lora_ctx {
     double upload_seconds = 0.0;
     uint64_t uploads = 0, upload_bytes = 0, invalid_seen = 0;
     uint64_t cluster_applies = 0, grouped_applies = 0;   // which path served each apply
+    uint64_t launches = 0;        // kernels queued by this context's calls
     int prefill_min = 0;          // shortest same-slot run sent to the tensor-core prefill kernel
     int small_batch = -1;         // batches up to this size take the cluster decode kernel; -1: by rank
     int inputs_ready = 0;         // caller: x, slot ids, pools not written by the preceding kernel
@@ -399,6 +400,7 @@ int lora_load_slot(lora_ctx *c, int slot, const void *const *A_host, const void 
         bytes += (din + dout) * r * e;
     }
     CUDA_TRY(launch_set_slot(c->scale_dev, c->rank_dev, slot, alpha / (float)rank, rank, c->upload));
+    ++c->launches;
     CUDA_TRY(cudaEventRecord(tm.end, c->upload));
     CUDA_TRY(note_upload(c, &slot, 1));
     c->timing.push_back(tm);
@@ -497,6 +499,7 @@ int lora_load_slots(lora_ctx *c, int n, const int *slots, const void *const *A_h
         CUDA_TRY(cudaEventCreate(&tm.end));
         CUDA_TRY(cudaEventRecord(tm.start, c->upload));
         CUDA_TRY(launch_upload_slots(ua, units, c->upload));
+        ++c->launches;
         CUDA_TRY(cudaEventRecord(tm.end, c->upload));
         CUDA_TRY(note_upload(c, ua.slots, ua.n_slots));
         c->timing.push_back(tm);
@@ -546,6 +549,7 @@ int fused_apply(lora_ctx *c, int n, const int *layers, const void *const *xs, vo
     fa.hdr = reinterpret_cast<int *>(c->ws + c->lay.hdr);
     fa.early = c->inputs_ready;
     CUDA_TRY(launch_cluster_decode(fa, est_tiles, c->compute, true));
+    ++c->launches;
     if (!capturing(c->compute)) CUDA_TRY(note_apply(c));
     return LORA_OK;
 }
@@ -610,6 +614,7 @@ int apply_impl(lora_ctx *c, int n, const int *layers, const void *const *xs, voi
     }
     CUDA_TRY(launch_group_tokens(idx, T, c->rank_dev, c->S, prefill ? c->prefill_min : 0, c->ws, c->lay,
                                  c->compute));
+    ++c->launches;
     if (prefill) {
         // upper bound on prefill tiles: T/128 full tiles plus one ragged tile per run
         int grid_tiles = T / kPrefillRows + T / c->prefill_min + 2;
@@ -625,9 +630,11 @@ int apply_impl(lora_ctx *c, int n, const int *layers, const void *const *xs, voi
             pl[i].d_in = L.d_in;
             pl[i].d_out = L.d_out;
         }
+        int queued = 0;
         cudaError_t e = launch_prefill_tc(pl, n, T, c->S, c->R, c->scale_dev, reinterpret_cast<int *>(c->ws + c->lay.hdr),
                                           reinterpret_cast<const int4 *>(c->ws + c->lay.ptiles), grid_tiles,
-                                          c->lay.part_rows, c->num_sms, c->compute);
+                                          c->lay.part_rows, c->num_sms, c->compute, &queued);
+        c->launches += (uint64_t)queued;
         if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
     }
 
@@ -681,6 +688,7 @@ int apply_impl(lora_ctx *c, int n, const int *layers, const void *const *xs, voi
     gv.T = T;
     int grid_tiles = est_tiles < c->lay.max_tiles ? est_tiles : c->lay.max_tiles;
     CUDA_TRY(launch_decode(ma, gv, c->dtype, grid_tiles, max_chunks, max_dblocks, c->num_sms, c->compute));
+    if (grid_tiles > 0) c->launches += 2;          // shrink and expand
     if (!capturing(c->compute)) CUDA_TRY(note_apply(c));
     return LORA_OK;
 }
@@ -994,6 +1002,7 @@ int lora_evict_lru(lora_ctx *c, int *evicted_slot, uint64_t *evicted_id) {
         // The slot reads as empty for work queued after this call.
         CUDA_TRY(wait_slot_reads(c, *evicted_slot));
         CUDA_TRY(launch_set_slot(c->scale_dev, c->rank_dev, *evicted_slot, 0.f, 0, c->upload));
+        ++c->launches;
         CUDA_TRY(note_upload(c, evicted_slot, 1));
     }
     return LORA_OK;
@@ -1050,6 +1059,7 @@ int lora_selftest_wait_timeout(lora_ctx *c, int *gave_up) {
     *gave_up = 0;
     int *word = reinterpret_cast<int *>(c->ws + c->lay.hdr) + kHdrError;
     CUDA_TRY(launch_selftest_wait(word, 1u << 14, c->compute));
+    ++c->launches;
     CUDA_TRY(cudaStreamSynchronize(c->compute));
     int v = 0;
     CUDA_TRY(cudaMemcpy(&v, word, sizeof v, cudaMemcpyDeviceToHost));
@@ -1071,6 +1081,7 @@ int lora_stats(lora_ctx *c, lora_stats_t *o) {
     }
     o->cluster_applies = c->cluster_applies;
     o->grouped_applies = c->grouped_applies;
+    o->kernel_launches = c->launches;
     o->hits = c->table.hits;
     o->misses = c->table.misses;
     o->evictions = c->table.evictions;

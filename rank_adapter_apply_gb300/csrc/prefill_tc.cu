@@ -642,7 +642,8 @@ size_t expand_smem(int stages) {
 
 template <int R>
 cudaError_t launch_r(const ShrinkArgs &sa, int grid_tiles, int n_jobs, size_t shrink_smem,
-                     const ReduceArgs *ra, const ExpandArgs &ea, int expand_grid, cudaStream_t st) {
+                     const ReduceArgs *ra, const ExpandArgs &ea, int expand_grid, cudaStream_t st,
+                     int *kernels) {
     static std::atomic<uint64_t> attr{0};
     if (!device_bit(attr)) {
         cudaError_t e = cudaFuncSetAttribute(prefill_shrink_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -653,16 +654,22 @@ cudaError_t launch_r(const ShrinkArgs &sa, int grid_tiles, int n_jobs, size_t sh
         if (e != cudaSuccess) return e;
         set_device_bit(attr);
     }
+    int queued = 0;
     prefill_shrink_kernel<R><<<dim3(grid_tiles, n_jobs, 1), kThreads, shrink_smem, st>>>(sa);
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    if (ra) {
+    if (e == cudaSuccess) ++queued;
+    if (e == cudaSuccess && ra) {
         prefill_reduce_kernel<<<dim3(grid_tiles * (kPrefillRows / (256 / (R / 4))), ea.n, 1), 256, 0, st>>>(*ra);
         e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
+        if (e == cudaSuccess) ++queued;
     }
-    prefill_expand_kernel<R><<<expand_grid, kExpandThreads, expand_smem<R>(ea.stages), st>>>(ea);
-    return cudaGetLastError();
+    if (e == cudaSuccess) {
+        prefill_expand_kernel<R><<<expand_grid, kExpandThreads, expand_smem<R>(ea.stages), st>>>(ea);
+        e = cudaGetLastError();
+        if (e == cudaSuccess) ++queued;
+    }
+    if (kernels) *kernels += queued;
+    return e;
 }
 
 }  // namespace
@@ -671,7 +678,7 @@ bool prefill_tc_supported(int R) { return R == 16 || R == 32 || R == 64; }
 
 cudaError_t launch_prefill_tc(const PrefillLayer *L, int n, int T, int S, int R, const float *scale,
                               int *hdr, const int4 *ptiles, int grid_tiles, int part_rows, int num_sms,
-                              cudaStream_t st) {
+                              cudaStream_t st, int *kernels) {
     if (!prefill_tc_supported(R) || n < 1 || n > kMaxLayersPerCall || T < 1) return cudaErrorInvalidValue;
     if (!g_encode) {
         cudaDriverEntryPointQueryResult q;
@@ -815,9 +822,12 @@ cudaError_t launch_prefill_tc(const PrefillLayer *L, int n, int T, int S, int R,
     const int expand_grid = (int)(items < num_sms ? items : num_sms);
 
     switch (R) {
-    case 16: return launch_r<16>(sa, grid_tiles, n_jobs, shrink_smem, reduce_pass ? &ra : nullptr, ea, expand_grid, st);
-    case 32: return launch_r<32>(sa, grid_tiles, n_jobs, shrink_smem, reduce_pass ? &ra : nullptr, ea, expand_grid, st);
-    case 64: return launch_r<64>(sa, grid_tiles, n_jobs, shrink_smem, reduce_pass ? &ra : nullptr, ea, expand_grid, st);
+    case 16: return launch_r<16>(sa, grid_tiles, n_jobs, shrink_smem, reduce_pass ? &ra : nullptr, ea, expand_grid, st,
+                             kernels);
+    case 32: return launch_r<32>(sa, grid_tiles, n_jobs, shrink_smem, reduce_pass ? &ra : nullptr, ea, expand_grid, st,
+                             kernels);
+    case 64: return launch_r<64>(sa, grid_tiles, n_jobs, shrink_smem, reduce_pass ? &ra : nullptr, ea, expand_grid, st,
+                             kernels);
     default: return cudaErrorInvalidValue;
     }
 }

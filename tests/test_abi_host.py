@@ -402,3 +402,25 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(B, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         B.load(str(tmp_path / "librank_adapter_apply.so"))
+
+
+def test_stats_struct_matches_the_header(lib):
+    """lora_stats writes exactly the binding's LoraStats: a buffer with guard
+    bytes after it comes back with every struct byte written and the guard
+    untouched, and a host-only context reports no kernel launches."""
+    import ctypes
+    n = ctypes.sizeof(B.LoraStats)
+    buf = (ctypes.c_ubyte * (n + 64))(*([0xAB] * (n + 64)))
+    ctx = _host_ctx(4, 16)
+    try:
+        assert lib.lora_stats(ctx, ctypes.cast(buf, ctypes.POINTER(B.LoraStats))) == 0
+        assert all(b == 0xAB for b in bytes(buf)[n:])
+        st = B.LoraStats.from_buffer_copy(bytes(buf)[:n])
+        assert all(getattr(st, k) == 0 for k, _ in B.LoraStats._fields_)
+        # the header declares the same fields in the same order
+        src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+        body = re.search(r"typedef struct \{([^}]*)\} lora_stats_t;", src).group(1)
+        names = re.findall(r"\b(\w+)\s*;", body)
+        assert names == [k for k, _ in B.LoraStats._fields_]
+    finally:
+        B.lora_destroy(ctx)

@@ -115,11 +115,12 @@ def test_small_batch_limit_follows_rank():
     grouped kernels, rank 32 pools batches up to 768 tokens and rank 16 pools
     batches up to 1024 tokens to the cluster kernel."""
     from rank_adapter_apply_gb300.harness import DeviceWorkload
-    for R, T, grouped in ((16, 64, False), (64, 64, True), (32, 768, False), (32, 769, True)):
+    for R, T, grouped, prefill_min in ((16, 64, False, None), (64, 64, True, None), (32, 768, False, None),
+                                       (32, 769, True, None), (64, 64, True, 0)):
         rng = np.random.default_rng(R + T)
         idx = rng.integers(0, 4, size=T)
         w = _custom(T, 512, 256, 4, R, [R] * 4, idx, seed=R)
-        dw = DeviceWorkload(w)
+        dw = DeviceWorkload(w, prefill_min_tokens=prefill_min)
         try:
             out = dw.run(None, multi=True)
             check_layer(w, "l0", out["l0"])
@@ -127,6 +128,17 @@ def test_small_batch_limit_follows_rank():
         finally:
             dw.close()
         assert (st["grouped_applies"], st["cluster_applies"]) == ((1, 0) if grouped else (0, 1)), (R, T, st)
+        # four slot uploads (one kernel each), then one cluster kernel, or the
+        # grouping, decode shrink and decode expand kernels plus two or three
+        # prefill kernels when the batch reaches the prefill threshold (64
+        # tokens by default; 0 turns the prefill kernels off)
+        if not grouped:
+            expect = {1}
+        elif prefill_min == 0:
+            expect = {3}
+        else:
+            expect = {5, 6}
+        assert st["kernel_launches"] - 4 in expect, (R, T, prefill_min, st)
 
 
 def test_all_base_only_is_bitwise_noop():
