@@ -324,6 +324,65 @@ def test_inputs_ready_back_to_back():
         dw.close()
 
 
+def test_graph_replay_in_bench_launch_configuration():
+    """The decode step as the benchmark times it: inputs declared ready
+    (programmatic dependent launch), three steps on their own x, y and slot ids
+    captured back to back in one CUDA graph. After a replay every step matches
+    the oracle, and a second replay from the same inputs gives the same bits."""
+    import torch
+    from rank_adapter_apply_gb300 import binding as B
+    from rank_adapter_apply_gb300.harness import DeviceWorkload, from_torch, to_torch
+    w = wl.decode_qv_4096(21, direct_base=True)
+    dw = DeviceWorkload(w)
+    try:
+        B.lora_set_inputs_ready(dw.slots.ctx, True)
+        dev = dw.device
+        steps = []
+        for k in range(3):
+            x, ys, idx = wl.decode_batch(np.random.default_rng(300 + k), w.n_tokens, w.max_loras, True)
+            wk = wl.Workload("decode_qv_4096", w.dtype, w.max_loras, w.max_lora_rank, w.layers, idx,
+                             {"x": x}, ys, w.adapters, w.ranks, w.alphas)
+            steps.append((wk, to_torch(x, w.dtype).to(dev),
+                          {n: to_torch(ys[n], w.dtype).to(dev) for n in ys},
+                          {n: to_torch(ys[n], w.dtype).to(dev) for n in ys},
+                          torch.from_numpy(idx).to(dev)))
+        st = dw.slots.compute
+
+        def apply(step):
+            _, xd, _, yd, idd = step
+            dw.slots.apply_multi([0, 1], [xd, xd], [yd["q_proj"], yd["v_proj"]], idd)
+
+        def reset():
+            for _, _, y0, yd, _ in steps:
+                for n in yd:
+                    yd[n].copy_(y0[n])
+            torch.cuda.synchronize(dev)
+
+        with torch.cuda.stream(st):
+            apply(steps[0])                 # eager call first: uploads are waited for outside the graph
+        st.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            for step in steps:
+                apply(step)
+        outs = []
+        for _ in range(2):
+            reset()
+            with torch.cuda.stream(st):
+                g.replay()
+            st.synchronize()
+            outs.append([{n: from_torch(yd[n]) for n in yd} for _, _, _, yd, _ in steps])
+        for (wk, *_), out in zip(steps, outs[0]):
+            for n, y in out.items():
+                check_layer(wk, n, y)
+        for a, b in zip(outs[0], outs[1]):
+            for n in a:
+                assert np.array_equal(a[n], b[n]), n
+        assert dw.slots.stats()["device_wait_timeouts"] == 0
+    finally:
+        dw.close()
+
+
 def test_mixed_ranks_small_general_path():
     """Five layers reading one input at max_lora_rank 64: the shrink splits
     them into input groups of at most four, each x tile read once per group."""
