@@ -193,6 +193,20 @@ def test_scale_uses_true_rank_and_is_linear_in_alpha():
     np.testing.assert_allclose(d1, ref, rtol=1e-12, atol=1e-14)
 
 
+def test_token_list_matches_whole_batch():
+    """Invariant: the rows computed for a list of tokens (any order, repeats
+    allowed) are the rows of those tokens in the whole-batch result."""
+    rng = np.random.default_rng(7)
+    T, d_in, d_out, S, R = 12, 10, 6, 3, 8
+    x, A, B = _int_case(rng, T, d_in, d_out, S, R, [8, 3, 5])
+    y = rng.integers(-5, 6, size=(T, d_out)).astype(np.float32)
+    idx = np.array([2, 0, -1, 1, 1, 2, 0, -1, 2, 1, 0, 0], np.int32)
+    whole = lora_apply_ref(x, y, A, B, [8, 3, 5], [16.0, 6.0, 5.0], idx, dtype=F32)
+    tok = [9, 3, 3, 0, 11, 2, 6]
+    part = lora_apply_ref(x, y, A, B, [8, 3, 5], [16.0, 6.0, 5.0], idx, tokens=tok, dtype=F32)
+    np.testing.assert_array_equal(part, whole[tok])
+
+
 def test_bf16_decoding_is_exact():
     v = np.array([1.0, -2.5, 3.140625, 1e-3, -0.0, 65504.0], np.float32)
     bits = wl.f32_to_bf16_bits(v)
