@@ -199,6 +199,37 @@ def test_policy_decision_log_matches_simulator(lib, policy, min_res):
         B.lora_destroy(ctx)
 
 
+def test_window_edges_and_priority_match_simulator(lib):
+    """The boundary cases pinned on the simulator, through the library: a
+    reload exactly thrash_window epochs after its eviction, and a priority that
+    decides a keep_score eviction."""
+    from oracle.lru_sim import LruSlotSim, KEEP_SCORE
+    ctx = _host_ctx(1, 16)
+    sim = LruSlotSim(1, 16, thrash_window=2)
+    try:
+        B.lora_set_thrash_window(ctx, 2)
+        _run_script(ctx, sim, [("assign", 1, 8), ("assign", 2, 8), ("tick",), ("tick",), ("assign", 1, 8),
+                               ("tick",), ("tick",), ("tick",), ("assign", 2, 8)])
+        assert sim.reloads == 1
+    finally:
+        B.lora_destroy(ctx)
+    for prio in (True, False):
+        ctx = _host_ctx(2, 16)
+        sim = LruSlotSim(2, 16)
+        try:
+            B.lora_set_policy(ctx, KEEP_SCORE)
+            sim.policy = KEEP_SCORE
+            B.lora_set_keep_score_weights(ctx, (1.0, 1.0, 1.0, 0.0, 0.0))
+            sim.weights = (1.0, 1.0, 1.0, 0.0, 0.0)
+            _run_script(ctx, sim, [("assign", 1, 16), ("assign", 2, 16)])
+            if prio:
+                B.lora_set_adapter_priority(ctx, 1, 5.0)
+                sim.set_priority(1, 5.0)
+            _run_script(ctx, sim, [("assign", 3, 16)])
+        finally:
+            B.lora_destroy(ctx)
+
+
 def test_policy_argument_errors(lib):
     ctx = _host_ctx(2, 16)
     try:

@@ -199,3 +199,51 @@ def test_keep_score_burst_keeps_hot_set():
     hot = [s.assign(a, 16) for a in range(4)]
     assert [h[2] for h in hot] == [1, 0, 0, 0]       # only adapter 0 reloads
     assert s.reloads == 1
+
+
+def test_reload_at_the_window_edge_is_thrash():
+    """A reload exactly `thrash_window` epochs after the eviction still counts
+    (the window is inclusive); one epoch later it does not."""
+    s = LruSlotSim(1, 16, thrash_window=2)
+    s.assign(1, 8)
+    s.assign(2, 8)          # evicts 1 at epoch 0
+    s.tick()
+    s.tick()
+    s.assign(1, 8)          # epoch 2: 2 - 0 <= 2, and evicts 2 at epoch 2
+    assert s.reloads == 1
+    for _ in range(3):
+        s.tick()
+    s.assign(2, 8)          # epoch 5: 5 - 2 > 2
+    assert s.reloads == 1 and s.evictions == 3
+
+
+def test_frequency_counts_an_access_for_window_epochs():
+    """keep_score with only the frequency term, window 3: an access made at
+    epoch 0 counts at epochs 0, 1 and 2 and no longer at epoch 3."""
+    s = LruSlotSim(2, 16, thrash_window=3)
+    s.policy = KEEP_SCORE
+    s.weights = (0.0, 1.0, 0.0, 0.0, 0.0)
+    s.assign(7, 16)
+    seen = []
+    for _ in range(4):
+        seen.append(s.keep_score(0))
+        s.tick()
+    assert seen == [1.0, 1.0, 1.0, 0.0]
+
+
+def test_keep_score_priority_outweighs_recency():
+    """Weights (1, 1, 1, 0, 0), two adapters bound in the same epoch (recency
+    1 and frequency 1 each): with priority 5 on the older one, the newer one
+    scores 2 against 7 and is evicted; without it the scores tie and the
+    least recently used (the older one) goes."""
+    def run(prio):
+        s = LruSlotSim(2, 16)
+        s.policy = KEEP_SCORE
+        s.weights = (1.0, 1.0, 1.0, 0.0, 0.0)
+        s.assign(1, 16)
+        s.assign(2, 16)
+        if prio:
+            s.set_priority(1, 5.0)
+        return s.assign(3, 16)
+    assert run(True) == (OK, 1, 1, 2)
+    assert run(False) == (OK, 0, 1, 1)

@@ -5,7 +5,10 @@ wrong sign, index or slot, a transposed operand, an off-by-one loop bound, a
 rounded intermediate, a wrong scale), builds the copy with the oracle's own
 compiler flags, points the oracle module at it and runs the pins of
 test_oracle_pins.py: at least one pin must fail for every mistake. Every
-planted index stays inside the arrays it reads, so no copy can crash.
+planted index stays inside the arrays it reads, so no copy can crash. The
+second half does the same for the slot-table simulator (recency, victim
+choice, in-flight and pinned slots, rank check, counters, window edges and
+every keep_score term) against the hand-derived scripts of test_lru_sim.py.
 """
 import os
 import subprocess
@@ -106,3 +109,88 @@ def test_planted_mistake_fails_a_pin(name, old, new, nth, tmp_path, use_library)
     assert mutant != text
     use_library(_build(mutant, str(tmp_path)))
     assert _first_failing_pin() is not None, f"no pin catches: {name}"
+
+
+# ---- the slot-table simulator ------------------------------------------------
+
+import importlib.util  # noqa: E402
+import sys  # noqa: E402
+
+from tests import test_lru_sim as lru_pins  # noqa: E402
+
+SIM_SRC = os.path.join(os.path.dirname(oracle.__file__), "lru_sim.py")
+
+SIM_MUTANTS = [
+    ("touch does not refresh recency", "self.last_use[s] = self.clock", "self.last_use[s] = self.last_use[s]", 0),
+    ("most recent evicted", "return min(cands, key=lambda s: self.last_use[s])",
+     "return max(cands, key=lambda s: self.last_use[s])", 0),
+    ("highest free slot first", "s = free[0]", "s = free[-1]", 0),
+    ("in-flight adapters evictable", "if aid is None or self.refs[s] > 0 or self.pinned[s]:",
+     "if aid is None or self.pinned[s]:", 0),
+    ("pinned adapters evictable", "if aid is None or self.refs[s] > 0 or self.pinned[s]:",
+     "if aid is None or self.refs[s] > 0:", 0),
+    ("rank not validated", "if rank < 1 or rank > self.R:", "if rank < 1:", 0),
+    ("hits not counted", "self.hits += 1", "self.hits += 0", 0),
+    ("hit does not touch", "self._touch(s)", "pass", 0),
+    ("reloads never counted", "self.reloads += 1", "self.reloads += 0", 0),
+    ("thrash window one short", "self.epoch - rec.last_evict_epoch <= self.window",
+     "self.epoch - rec.last_evict_epoch < self.window", 0),
+    ("thrash window unbounded", "self.epoch - rec.last_evict_epoch <= self.window", "True", 0),
+    ("cooling window ignored", "if self.min_residency > 0 and", "if False and", 0),
+    ("cooling window one short", "< self.min_residency:", "< self.min_residency - 1:", 0),
+    ("release keeps the reference", "self.refs[s] -= 1", "self.refs[s] -= 0", 0),
+    ("keep_score frequency subtracted", "k += w2 * freq", "k -= w2 * freq", 0),
+    ("keep_score recency inverted", "recent = 1.0 / (1.0 + float(self.epoch - rec.last_access))",
+     "recent = float(self.epoch - rec.last_access)", 0),
+    ("keep_score priority dropped", "k += w3 * rec.priority", "k += 0.0", 0),
+    ("keep_score size added", "k -= w5 * rel", "k += w5 * rel", 0),
+    ("keep_score highest evicted", "return min(cands, key=lambda s: (self.keep_score(s), self.last_use[s]))",
+     "return max(cands, key=lambda s: (self.keep_score(s), self.last_use[s]))", 0),
+    ("keep_score tie to most recent", "return min(cands, key=lambda s: (self.keep_score(s), self.last_use[s]))",
+     "return min(cands, key=lambda s: (self.keep_score(s), -self.last_use[s]))", 0),
+    ("frequency window one short", "if e > self.epoch - self.window)", "if e > self.epoch - self.window + 1)", 0),
+    ("pin of an empty slot accepted", "if self.slot_id[s] is None:\n            return STATE_ERR",
+     "if False:\n            return STATE_ERR", 0),
+]
+
+LRU_PINS = [getattr(lru_pins, n) for n in dir(lru_pins) if n.startswith("test_")]
+
+
+def _load_sim(text, out_dir, tag):
+    path = os.path.join(out_dir, f"lru_sim_{tag}.py")
+    with open(path, "w") as f:
+        f.write(text)
+    name = f"lru_sim_{tag}"
+    spec = importlib.util.spec_from_file_location(name, path)
+    mod = importlib.util.module_from_spec(spec)
+    sys.modules[name] = mod              # dataclasses look their module up while the class is built
+    try:
+        spec.loader.exec_module(mod)
+    finally:
+        del sys.modules[name]
+    return mod
+
+
+def _first_failing_lru_pin(monkeypatch, mod):
+    monkeypatch.setattr(lru_pins, "LruSlotSim", mod.LruSlotSim)
+    for pin in LRU_PINS:
+        try:
+            pin()
+        except (AssertionError, KeyError, IndexError, TypeError, ValueError):
+            return pin.__name__
+    return None
+
+
+def test_unchanged_simulator_passes_every_pin(tmp_path, monkeypatch):
+    assert len(LRU_PINS) >= 14
+    mod = _load_sim(open(SIM_SRC).read(), str(tmp_path), "same")
+    assert _first_failing_lru_pin(monkeypatch, mod) is None
+
+
+@pytest.mark.parametrize("name,old,new,nth", SIM_MUTANTS, ids=[m[0] for m in SIM_MUTANTS])
+def test_planted_simulator_mistake_fails_a_pin(name, old, new, nth, tmp_path, monkeypatch):
+    text = open(SIM_SRC).read()
+    mutant = _replace_nth(text, old, new, nth)
+    assert mutant != text
+    mod = _load_sim(mutant, str(tmp_path), "mut")
+    assert _first_failing_lru_pin(monkeypatch, mod) is not None, f"no pin catches: {name}"
