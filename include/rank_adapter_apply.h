@@ -103,8 +103,10 @@ size_t lora_workspace_bytes(int max_loras, int max_lora_rank, int max_tokens,
                             int max_layers_per_call);
 
 /*
- * Create a context. max_loras: 1..256 slots. max_lora_rank: 8..256, a
- * multiple of 8. dtype: lora_dtype. layers[n_layers]: shapes and pools (d_in,
+ * Create a context: the GPU slot table of the "Multi-LoRA 适配器缓存生产实战"
+ * page (section 核心原理, parameter table: max_loras adapters usable in one
+ * batch, ranks up to max_lora_rank). max_loras: 1..256 slots. max_lora_rank:
+ * 8..256, a multiple of 8. dtype: lora_dtype. layers[n_layers]: shapes and pools (d_in,
  * d_out >= 1). scale_dev / rank_dev: device arrays [max_loras] (fp32 / int32)
  * that the library writes on every upload or eviction. workspace: device,
  * lora_workspace_bytes(...) bytes, 256-byte aligned; it is zeroed here (on the
@@ -123,7 +125,8 @@ int lora_slots_init(lora_ctx **out, int max_loras, int max_lora_rank, int max_to
                     void *workspace, size_t workspace_bytes,
                     void *compute_stream, void *upload_stream);
 
-/* Release events and host state. Waits for work the library queued. NULL ok. */
+/* Release events and host state. Waits for work the library queued. NULL ok.
+ * (Resource handling only; no counterpart on the source pages.) */
 void lora_destroy(lora_ctx *ctx);
 
 /*
@@ -144,7 +147,9 @@ int lora_load_slot(lora_ctx *ctx, int slot, const void *const *A_host,
 
 /*
  * Apply the delta of one layer: y[t] += scale_s * B_s (A_s x[t]) for the
- * n_tokens rows of x / y (device). token_slot_idx: device int32 [n_tokens].
+ * n_tokens rows of x / y (device), scale_s = lora_alpha / r of the adapter in
+ * slot s (the PEFT adapter_config.json on the "vLLM LoRA Resolver 插件详解"
+ * page, section 3.2). token_slot_idx: device int32 [n_tokens].
  * Index -1, an index >= max_loras or < -1 (counted in invalid_token_index), or
  * an empty slot (rank 0) leaves y[t] bit-for-bit unchanged. Stream-ordered on
  * the compute stream; no host synchronisation. 0 <= n_tokens <= max_tokens.
@@ -154,7 +159,10 @@ int lora_apply(lora_ctx *ctx, int layer, const void *x, void *y,
                const int32_t *token_slot_idx, int n_tokens);
 
 /*
- * Apply n layers (a layer set: q/k/v/o, gate/up/down) that share one token
+ * Apply n layers (a layer set: the adapter's target_modules, q_proj and v_proj
+ * in the PEFT config of the "vLLM LoRA Resolver 插件详解" page, section 3.2;
+ * q/k/v/o in the adapter manifest of the "Multi-LoRA 适配器缓存生产实战" page,
+ * section "Adapter 容量不能只按「个数」规划") that share one token
  * batch and one token_slot_idx. xs[i] / ys[i] are the device input / output of
  * layer layers[i]. Layers may share an input pointer (q, k, v read the same
  * hidden state). The grouping of tokens by slot is computed once for the set.
@@ -187,7 +195,8 @@ int lora_apply_multi_host(lora_ctx *ctx, int n, const int *layers,
                           void *const *xs_dev, void *const *ys_dev, int32_t *idx_dev);
 
 /* Blocks until the copies back of every queued lora_apply_multi_host call have
- * landed in host memory (LORA_OK at once for a host-only context). */
+ * landed in host memory (LORA_OK at once for a host-only context).
+ * (Host-buffer plumbing; no counterpart on the source pages.) */
 int lora_sync_host(lora_ctx *ctx);
 
 /*
@@ -239,10 +248,14 @@ int lora_assign_tokens(lora_ctx *ctx, int n_tokens, const uint64_t *adapter_ids,
                        int acquire, int32_t *token_slot_idx, int max_distinct, uint64_t *distinct_ids,
                        int *slots, int *needs_load, uint64_t *evicted_ids, int *n_distinct, int *n_done);
 
-/* lora_release on each of slots[n] in order; stops at the first slot not in flight (LORA_ERR_STATE). */
+/* lora_release on each of slots[n] in order; stops at the first slot not in flight (LORA_ERR_STATE).
+ * The in-flight protection of the "Multi-LoRA 适配器缓存生产实战" page: section 核心原理, last
+ * paragraph, and the inflight_requests field of section 数据面. */
 int lora_release_batch(lora_ctx *ctx, int n, const int *slots);
 
-/* In-flight reference count of an occupied slot (never evicted while > 0). */
+/* In-flight reference count of an occupied slot (never evicted while > 0): the
+ * inflight_requests field of the "Multi-LoRA 适配器缓存生产实战" page, section 数据面.
+ * LORA_ERR_STATE: acquire of an empty slot, release of a slot not in flight. */
 int lora_acquire(lora_ctx *ctx, int slot);
 int lora_release(lora_ctx *ctx, int slot);
 
@@ -255,10 +268,16 @@ int lora_release(lora_ctx *ctx, int slot);
  */
 int lora_evict_lru(lora_ctx *ctx, int *evicted_slot, uint64_t *evicted_id);
 
-/* Advance the epoch used by the thrash window (call once per step). */
+/* Advance the epoch used by the thrash window (call once per step). The window
+ * is the "short time window" of adapter_thrash_ratio on the "Multi-LoRA
+ * 适配器缓存生产实战" page, section 需要重点监控哪些指标; the page leaves its unit
+ * open, and epochs (steps) are this library's reading. */
 int lora_tick(lora_ctx *ctx);
 
-/* Set the thrash window in epochs (default 10). */
+/* Set the thrash window in epochs (default 10): a reload at most this many
+ * epochs after the adapter's eviction counts in reloads_after_eviction (the
+ * numerator of adapter_thrash_ratio, same page and section as lora_tick).
+ * < 0 is LORA_ERR_ARG. */
 int lora_set_thrash_window(lora_ctx *ctx, int epochs);
 
 /*
@@ -345,6 +364,10 @@ int lora_set_keep_score_weights(lora_ctx *ctx, const double *w);
 int lora_set_adapter_priority(lora_ctx *ctx, uint64_t adapter_id, double priority);
 
 /*
+ * (Implementation controls from here to lora_set_inputs_ready: they choose
+ * kernels and launch order, never the result; the source pages have no
+ * counterpart.)
+ *
  * Segment-length threshold for the tensor-core prefill path (bf16 contexts
  * with max_lora_rank 16, 32 or 64; layers with d_out a multiple of 64):
  * contiguous runs of tokens on one slot at least this long use it; shorter
@@ -377,10 +400,15 @@ int lora_set_small_batch_tokens(lora_ctx *ctx, int n);
  */
 int lora_set_inputs_ready(lora_ctx *ctx, int on);
 
-/* Block until every queued upload finished; accumulates upload_seconds. */
+/* Block until every queued upload finished; accumulates upload_seconds (the
+ * adapter_h2d time of the page's TTFT decomposition, section 冷加载延迟). */
 int lora_sync_uploads(lora_ctx *ctx);
 
-/* Counters; synchronises the compute stream to read the device error count. */
+/* Counters; synchronises the compute stream to read the device error count.
+ * hits, misses, evictions and the reload count are the residency counters of
+ * the "Multi-LoRA 适配器缓存生产实战" page (section 数据面: hit_count, load_count,
+ * eviction_count) and the inputs of its thrash ratio and H2D metrics (section
+ * 需要重点监控哪些指标). */
 int lora_stats(lora_ctx *ctx, lora_stats_t *out);
 
 /*
@@ -394,7 +422,9 @@ int lora_stats(lora_ctx *ctx, lora_stats_t *out);
  */
 int lora_selftest_wait_timeout(lora_ctx *ctx, int *gave_up);
 
-/* Bytes one adapter upload moves: sum over layers of (d_in + d_out) * rank * bytes_per_param. */
+/* Bytes one adapter upload moves: sum over layers of (d_in + d_out) * rank * bytes_per_param
+ * (the capacity formula of the "Multi-LoRA 适配器缓存生产实战" page, section
+ * "Adapter 容量不能只按「个数」规划"). 0 for negative or NULL arguments. */
 uint64_t lora_adapter_bytes(int n_layers, const int *d_in, const int *d_out, int rank,
                             int bytes_per_param);
 
@@ -429,7 +459,8 @@ int lora_apply_static_scratch(const void *x, void *y, const int32_t *token_slot_
                               const void *B_pool, const float *scale_dev,
                               const int32_t *rank_dev, void *stream);
 
-/* Message for the last failed call on this thread ("" if none). */
+/* Message for the last failed call on this thread ("" if none; error reporting
+ * only, no counterpart on the source pages). */
 const char *lora_last_error(void);
 
 #ifdef __cplusplus
