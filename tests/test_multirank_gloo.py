@@ -5,7 +5,6 @@ ranks check the reduction the benchmark uses."""
 import os
 import socket
 
-import pytest
 import torch.multiprocessing as mp
 
 
