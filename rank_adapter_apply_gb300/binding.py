@@ -14,7 +14,9 @@ import ctypes
 import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "_build", "librank_adapter_apply.so")
+# RANK_ADAPTER_APPLY_LIB selects another build of the same library (for
+# example the sanitizer build of build.py); the default is the in-tree build.
+LIB_PATH = os.environ.get("RANK_ADAPTER_APPLY_LIB") or os.path.join(HERE, "_build", "librank_adapter_apply.so")
 
 LORA_OK = 0
 LORA_ERR_ARG = -1

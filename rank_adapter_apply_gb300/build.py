@@ -1,6 +1,11 @@
 """Build the C-ABI shared library in-tree with nvcc (sm_103a only).
 
     python -m rank_adapter_apply_gb300.build        # -> rank_adapter_apply_gb300/_build/librank_adapter_apply.so
+    python -m rank_adapter_apply_gb300.build --sanitize
+        # -> _build_sanitize/: host code with AddressSanitizer and UBSan, for
+        #    checking the host paths (run with LD_PRELOAD of libasan and
+        #    libubsan, ASAN_OPTIONS=detect_leaks=0 and RANK_ADAPTER_APPLY_LIB
+        #    pointing at that library)
 
 Translation units compile in parallel; cudart is linked statically so the
 library needs only the NVIDIA driver at run time (loaded lazily on the first
@@ -40,20 +45,26 @@ def _stale(target: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+SANITIZE_FLAGS = ["-Xcompiler", "-fsanitize=address,-fsanitize=undefined,-fno-omit-frame-pointer", "-g"]
+
+
+def build(force: bool = False, verbose: bool = False, sanitize: bool = False) -> str:
+    out_dir = BUILD + "_sanitize" if sanitize else BUILD
+    lib_path = os.path.join(out_dir, os.path.basename(LIB))
+    flags = FLAGS + (SANITIZE_FLAGS if sanitize else [])
+    os.makedirs(out_dir, exist_ok=True)
     nvcc = _nvcc()
     common_deps = [os.path.join(CSRC, h) for h in HEADERS] + [
         os.path.join(ROOT, "include", "rank_adapter_apply.h")]
     objs, jobs = [], []
     for src in SOURCES:
         path = os.path.join(CSRC, src)
-        obj = os.path.join(BUILD, src + ".o")
+        obj = os.path.join(out_dir, src + ".o")
         objs.append(obj)
         if force or _stale(obj, [path] + common_deps):
-            cmd = [nvcc, *ARCH, *FLAGS, "-c", path, "-o", obj]
+            cmd = [nvcc, *ARCH, *flags, "-c", path, "-o", obj]
             if src.endswith(".cpp"):
-                cmd = [nvcc, *FLAGS, "-x", "c++", "-c", path, "-o", obj]
+                cmd = [nvcc, *flags, "-x", "c++", "-c", path, "-o", obj]
             jobs.append(cmd)
 
     def run(cmd):
@@ -68,12 +79,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
         for err in ex.map(run, jobs):
             if verbose and err:
                 print(err, flush=True)
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
-        run([nvcc, *ARCH, "-shared", "-cudart", "static", *objs, "-o", tmp])
-        os.replace(tmp, LIB)
-    return LIB
+    if force or jobs or _stale(lib_path, objs):
+        tmp = lib_path + f".tmp{os.getpid()}"
+        link_extra = ["-Xcompiler", "-fsanitize=address,-fsanitize=undefined"] if sanitize else []
+        run([nvcc, *ARCH, "-shared", "-cudart", "static", *objs, *link_extra, "-o", tmp])
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True))
+    print(build(force="--force" in sys.argv, verbose=True, sanitize="--sanitize" in sys.argv))
