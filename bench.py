@@ -667,13 +667,14 @@ def run_churn(args):
     """Slot churn: 64 GPU slots, 512 rank-16 adapters in pinned host memory,
     Zipf(1.2) adapter ids with a burst of 20 cold adapters every 50 steps."""
     from rank_adapter_apply_gb300 import build as build_mod
-    from rank_adapter_apply_gb300.churn import ChurnRunner
+    from rank_adapter_apply_gb300.churn import KEEP_PIN32, ChurnRunner
     build_mod.build()
     steps = args.steps if args.steps <= 1000 else 200
     trace = wl.churn_trace(0, n_steps=steps)
     warm = wl.churn_trace(99, n_steps=max(3, min(args.warmup, 20)))
     pol = {"lru": {}, "pin16": {"pin_top": 16},
-           "keep": {"policy": 1, "weights": (1.0, 1.0, 0.0, 0.0, 0.0)}}[args.churn_policy]
+           "keep": {"policy": 1, "weights": (1.0, 1.0, 0.0, 0.0, 0.0)},
+           "keep_pin32": dict(KEEP_PIN32)}[args.churn_policy]
     r = ChurnRunner(overlap=args.churn_overlap, batched_upload=args.churn_upload == "batched", **pol)
     r.run(warm)
     base = r.slots.stats()
@@ -715,8 +716,9 @@ def main():
                     help="decode: do not declare inputs independent of the preceding kernel")
     ap.add_argument("--prefill-seqs", type=int, default=32,
                     help="sequences in the prefill workload (32 = the full workload)")
-    ap.add_argument("--churn-policy", choices=["lru", "pin16", "keep"], default="lru",
-                    help="churn: pure LRU, LRU with the 16 most popular adapters pinned, or keep_score")
+    ap.add_argument("--churn-policy", choices=["lru", "pin16", "keep", "keep_pin32"], default="lru",
+                    help="churn: pure LRU, LRU with the 16 most popular adapters pinned, keep_score, "
+                         "or keep_score (40-epoch window) with the 32 most popular pinned")
     ap.add_argument("--churn-upload", choices=["batched", "copy"], default="batched",
                     help="churn: one upload kernel per group (default) or copy-engine copies per adapter")
     ap.add_argument("--churn-overlap", action="store_true",
