@@ -9,6 +9,8 @@ or calls anything here, and nothing here imports the product.
   ``lora_oracle.c``, compiled with gcc, OpenMP over tokens).
 * ``LruSlotSim``      -- an independent simulator of the GPU slot table.
 * ``adapter_bytes``   -- the capacity formula.
+* ``belady``          -- an offline replay that evicts the adapter used
+  farthest in the future: the yardstick for the eviction policies.
 """
 from __future__ import annotations
 
