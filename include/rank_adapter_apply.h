@@ -91,6 +91,7 @@ typedef struct {
                                        lora_load_slots and per device-side eviction. A call
                                        made during stream capture counts once, when captured,
                                        however often the graph runs. */
+    uint64_t aborted_loads;         /* lora_abort_load calls that emptied a slot */
 } lora_stats_t;
 
 /*
@@ -267,6 +268,20 @@ int lora_release(lora_ctx *ctx, int slot);
  * set to 0 on the device, after compute work already queued.
  */
 int lora_evict_lru(lora_ctx *ctx, int *evicted_slot, uint64_t *evicted_id);
+
+/*
+ * The upload into `slot` failed or was abandoned (the "load failed" outcome the
+ * "vLLM LoRA Resolver 插件详解" page gives a dynamic load, section 6.1): the slot
+ * becomes empty, so the adapter lora_assign bound to it is no longer resident
+ * and a later assign of that adapter is a miss that loads it again. The adapter
+ * the assign evicted stays evicted (its slot bytes may already be overwritten).
+ * Counted in aborted_loads, not as an eviction; any in-flight reference and pin
+ * of the slot end. With a device context the slot reads as empty (rank 0) for
+ * work queued after this call, after compute already queued. *unbound_id = the
+ * id that was bound. LORA_ERR_ARG: slot out of range or NULL; LORA_ERR_STATE:
+ * the slot is empty.
+ */
+int lora_abort_load(lora_ctx *ctx, int slot, uint64_t *unbound_id);
 
 /* Advance the epoch used by the thrash window (call once per step). The window
  * is the "short time window" of adapter_thrash_ratio on the "Multi-LoRA

@@ -18,6 +18,10 @@ Semantics, as read from the "Multi-LoRA 适配器缓存生产实战" page:
   window (minimum residency) against short bursts, and a recency + frequency
   keep_score  w1 recent + w2 frequency + w3 priority + w4 reload_cost - w5 size.
 
+A failed upload (the "load failed" outcome of a dynamic load on the "vLLM LoRA
+Resolver 插件详解" page, section 6.1) is undone with ``abort_load``: the slot
+becomes empty; the adapter the assign evicted stays evicted.
+
 Readings where the page is silent: the LRU clock is a counter that advances by
 one on every touch or bind, so no two slots tie; a free slot (lowest index
 first) is used before anything is evicted; the rank is validated before any
@@ -69,6 +73,7 @@ class LruSlotSim:
         self.where: dict[int, int] = {}
         self.records: dict[int, AdapterRecord] = {}
         self.hits = self.misses = self.evictions = self.reloads = self.rejected = 0
+        self.aborted = 0
         self.log: list[tuple] = []
         self.pinned = [False] * max_loras
         self.min_residency = 0
@@ -203,6 +208,22 @@ class LruSlotSim:
         aid = self._evict(s)
         self.log.append(("evict", OK, s, aid))
         return OK, s, aid
+
+    def abort_load(self, s: int):
+        """The upload into slot s failed: the slot becomes empty (not an
+        eviction; refs and pin end). Returns (status, id that was bound or -1)."""
+        if not 0 <= s < self.S:
+            return ARG_ERR, -1
+        aid = self.slot_id[s]
+        if aid is None:
+            return STATE_ERR, -1
+        self.slot_id[s] = None
+        self.pinned[s] = False
+        self.refs[s] = 0
+        del self.where[aid]
+        self.aborted += 1
+        self.log.append(("abort", s, aid))
+        return OK, aid
 
     def tick(self) -> None:
         self.epoch += 1

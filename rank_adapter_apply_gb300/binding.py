@@ -36,7 +36,7 @@ EXPORTED = [
     "lora_last_error", "lora_apply_static_scratch", "lora_pin", "lora_set_min_residency",
     "lora_set_policy", "lora_set_keep_score_weights", "lora_set_adapter_priority",
     "lora_set_slot_tracking", "lora_load_slots", "lora_assign_batch", "lora_release_batch",
-    "lora_selftest_wait_timeout", "lora_assign_tokens", "lora_sync_host",
+    "lora_selftest_wait_timeout", "lora_assign_tokens", "lora_sync_host", "lora_abort_load",
 ]
 
 
@@ -52,7 +52,8 @@ class LoraStats(ctypes.Structure):
                 ("upload_bytes", ctypes.c_uint64), ("invalid_token_index", ctypes.c_uint64),
                 ("upload_seconds", ctypes.c_double), ("epoch", ctypes.c_int64),
                 ("device_wait_timeouts", ctypes.c_uint64), ("cluster_applies", ctypes.c_uint64),
-                ("grouped_applies", ctypes.c_uint64), ("kernel_launches", ctypes.c_uint64)]
+                ("grouped_applies", ctypes.c_uint64), ("kernel_launches", ctypes.c_uint64),
+                ("aborted_loads", ctypes.c_uint64)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -92,6 +93,7 @@ def load(path: str = LIB_PATH):
         "lora_acquire": (i32, [vp, i32]),
         "lora_release": (i32, [vp, i32]),
         "lora_evict_lru": (i32, [vp, P(i32), P(u64)]),
+        "lora_abort_load": (i32, [vp, i32, P(u64)]),
         "lora_tick": (i32, [vp]),
         "lora_set_thrash_window": (i32, [vp, i32]),
         "lora_pin": (i32, [vp, i32, i32]),
@@ -274,6 +276,13 @@ def lora_evict_lru(ctx):
     s, ev = ctypes.c_int(-1), ctypes.c_uint64(NO_ID)
     rc = load().lora_evict_lru(ctx, ctypes.byref(s), ctypes.byref(ev))
     return rc, s.value, (-1 if ev.value == NO_ID else ev.value)
+
+
+def lora_abort_load(ctx, slot):
+    """Returns (status, id that was bound or -1)."""
+    ev = ctypes.c_uint64(NO_ID)
+    rc = load().lora_abort_load(ctx, int(slot), ctypes.byref(ev))
+    return rc, (-1 if ev.value == NO_ID else ev.value)
 
 
 def lora_tick(ctx):

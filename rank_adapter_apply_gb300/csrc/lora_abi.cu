@@ -994,18 +994,37 @@ int lora_set_adapter_priority(lora_ctx *c, uint64_t adapter_id, double priority)
     return LORA_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// A slot emptied in the host table reads as empty (rank 0) for device work
+// queued after the call; compute already queued that may read it finishes first.
+int mark_slot_empty_on_device(lora_ctx *c, int slot) {
+    if (!c->device) return LORA_OK;
+    CUDA_TRY(wait_slot_reads(c, slot));
+    CUDA_TRY(launch_set_slot(c->scale_dev, c->rank_dev, slot, 0.f, 0, c->upload));
+    ++c->launches;
+    CUDA_TRY(note_upload(c, &slot, 1));
+    return LORA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 int lora_evict_lru(lora_ctx *c, int *evicted_slot, uint64_t *evicted_id) {
     if (!c || !evicted_slot || !evicted_id) return fail(LORA_ERR_ARG, "NULL argument");
     if (!c->table.evict_lru(evicted_slot, evicted_id))
         return fail(LORA_ERR_NO_SLOT, "no occupied slot may be evicted (in flight, pinned or cooling)");
-    if (c->device && *evicted_slot >= 0) {
-        // The slot reads as empty for work queued after this call.
-        CUDA_TRY(wait_slot_reads(c, *evicted_slot));
-        CUDA_TRY(launch_set_slot(c->scale_dev, c->rank_dev, *evicted_slot, 0.f, 0, c->upload));
-        ++c->launches;
-        CUDA_TRY(note_upload(c, evicted_slot, 1));
-    }
-    return LORA_OK;
+    return *evicted_slot >= 0 ? mark_slot_empty_on_device(c, *evicted_slot) : LORA_OK;
+}
+
+int lora_abort_load(lora_ctx *c, int slot, uint64_t *unbound_id) {
+    if (!c || !unbound_id) return fail(LORA_ERR_ARG, "NULL argument");
+    if (slot < 0 || slot >= c->S) return fail(LORA_ERR_ARG, "slot %d out of range", slot);
+    if (!c->table.abort_load(slot, unbound_id)) return fail(LORA_ERR_STATE, "slot %d is empty", slot);
+    return mark_slot_empty_on_device(c, slot);
 }
 
 int lora_tick(lora_ctx *c) {
@@ -1082,6 +1101,7 @@ int lora_stats(lora_ctx *c, lora_stats_t *o) {
     o->cluster_applies = c->cluster_applies;
     o->grouped_applies = c->grouped_applies;
     o->kernel_launches = c->launches;
+    o->aborted_loads = c->table.aborted_loads;
     o->hits = c->table.hits;
     o->misses = c->table.misses;
     o->evictions = c->table.evictions;

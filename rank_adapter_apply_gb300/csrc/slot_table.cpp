@@ -145,6 +145,20 @@ bool SlotTable::pin(int slot, bool on) {
     return true;
 }
 
+bool SlotTable::abort_load(int slot, uint64_t *unbound_id) {
+    *unbound_id = UINT64_MAX;
+    if (slot < 0 || slot >= S_ || !occ_[slot]) return false;
+    const uint64_t id = id_[slot];
+    occ_[slot] = 0;
+    pin_[slot] = 0;
+    refs_[slot] = 0;
+    where_.erase(id);
+    res_[slot] = nullptr;
+    ++aborted_loads;
+    *unbound_id = id;
+    return true;
+}
+
 bool SlotTable::evict_lru(int *slot, uint64_t *evicted_id) {
     *slot = -1;
     *evicted_id = UINT64_MAX;

@@ -49,6 +49,10 @@ public:
     bool release(int slot);
     // Returns false when no occupied slot may be evicted. *slot = -1 if empty.
     bool evict_lru(int *slot, uint64_t *evicted_id);
+    // Empty an occupied slot whose upload failed or was abandoned: the bound
+    // adapter is no longer resident (not counted as an eviction). False if the
+    // slot is out of range or empty.
+    bool abort_load(int slot, uint64_t *unbound_id);
 
     bool pin(int slot, bool on);
     void set_min_residency(int epochs) { min_res_ = epochs < 0 ? 0 : epochs; }
@@ -65,7 +69,7 @@ public:
     bool pinned(int slot) const { return pin_[slot]; }
     int refs(int slot) const { return refs_[slot]; }
 
-    uint64_t hits = 0, misses = 0, evictions = 0, reloads = 0, rejected = 0;
+    uint64_t hits = 0, misses = 0, evictions = 0, reloads = 0, rejected = 0, aborted_loads = 0;
     int64_t epoch() const { return epoch_; }
 
 private:

@@ -74,12 +74,15 @@ def _run_script(ctx, sim, ops):
             assert B.lora_release(ctx, op[1]) == sim.release(op[1]), op
         elif kind == "evict":
             assert B.lora_evict_lru(ctx) == sim.evict_lru(), op
+        elif kind == "abort":
+            assert B.lora_abort_load(ctx, op[1]) == sim.abort_load(op[1]), op
         elif kind == "tick":
             B.lora_tick(ctx)
             sim.tick()
     st = B.lora_stats(ctx)
     assert (st["hits"], st["misses"], st["evictions"], st["reloads_after_eviction"],
-            st["rejected"]) == (sim.hits, sim.misses, sim.evictions, sim.reloads, sim.rejected)
+            st["rejected"], st["aborted_loads"]) == (sim.hits, sim.misses, sim.evictions, sim.reloads,
+                                                     sim.rejected, sim.aborted)
 
 
 def test_scripted_decisions_match_simulator(lib):
@@ -453,5 +456,65 @@ def test_stats_struct_matches_the_header(lib):
         body = re.search(r"typedef struct \{([^}]*)\} lora_stats_t;", src).group(1)
         names = re.findall(r"\b(\w+)\s*;", body)
         assert names == [k for k, _ in B.LoraStats._fields_]
+    finally:
+        B.lora_destroy(ctx)
+
+
+def test_failed_load_leaves_the_table_consistent(lib):
+    """A serving step whose upload fails part-way: the adapters whose uploads
+    failed are unbound with lora_abort_load, the others stay resident, nothing
+    else is evicted, and the next step loads the failed ones again; every
+    decision equals the simulator's."""
+    from oracle.lru_sim import LruSlotSim
+    ctx = _host_ctx(4, 16)
+    sim = LruSlotSim(4, 16)
+    try:
+        _run_script(ctx, sim, [("assign", a, 16) for a in (1, 2, 3, 4)] + [("tick",)])
+        # next step: 5 and 6 miss (evicting 1 and 2) and are taken in flight;
+        # the upload of 6 fails
+        got = [B.lora_assign(ctx, a, 16) for a in (5, 6)]
+        assert got == [sim.assign(a, 16) for a in (5, 6)]
+        slot5, slot6 = got[0][1], got[1][1]
+        _run_script(ctx, sim, [("acquire", slot5), ("acquire", slot6), ("abort", slot6),
+                               ("release", slot6),        # the abort ended that reference
+                               ("release", slot5), ("tick",)])
+        assert B.lora_lookup(ctx, 6) == -1 and B.lora_lookup(ctx, 5) == got[0][1]
+        sim.lookup(5)
+        assert [B.lora_lookup(ctx, a) for a in (3, 4)] == [sim.lookup(a) for a in (3, 4)]
+        # the retry is a miss into the emptied slot, evicting nothing
+        assert B.lora_assign(ctx, 6, 16) == sim.assign(6, 16) == (0, slot6, 1, -1)
+        _run_script(ctx, sim, [("abort", 9), ("abort", 0), ("abort", 0), ("assign", 7, 16)])
+        assert B.lora_stats(ctx)["aborted_loads"] == sim.aborted == 2
+    finally:
+        B.lora_destroy(ctx)
+
+
+def test_random_decisions_with_aborted_loads_match_simulator(lib):
+    """Zipf admission with about one upload in ten failing (and aborted), plus
+    in-flight references taken and dropped and explicit evictions: every
+    decision, status and counter equal to the simulator's."""
+    from oracle.lru_sim import LruSlotSim
+    rng = np.random.default_rng(21)
+    S, R = 6, 32
+    ctx = _host_ctx(S, R)
+    sim = LruSlotSim(S, R)
+    try:
+        ops = []
+        for step in range(300):
+            a = int(rng.zipf(1.3)) % 40
+            ops.append(("assign", a, int(rng.choice([8, 16, 32]))))
+            r = rng.random()
+            if r < 0.1:
+                ops.append(("abort", int(rng.integers(0, S))))
+            elif r < 0.15:
+                ops.append(("evict",))
+            elif r < 0.35:
+                ops.append(("acquire", int(rng.integers(0, S))))
+            elif r < 0.55:
+                ops.append(("release", int(rng.integers(0, S))))
+            if step % 7 == 0:
+                ops.append(("tick",))
+        _run_script(ctx, sim, ops)
+        assert sim.aborted > 10
     finally:
         B.lora_destroy(ctx)

@@ -247,3 +247,34 @@ def test_keep_score_priority_outweighs_recency():
         return s.assign(3, 16)
     assert run(True) == (OK, 1, 1, 2)
     assert run(False) == (OK, 0, 1, 1)
+
+
+def test_abort_load_frees_the_slot():
+    """2 slots: 3 evicts 1 from slot 0, then its upload fails. Slot 0 is empty:
+    3 is not resident, 1 stays evicted, the next miss takes slot 0 without an
+    eviction, and a retry of 3 is a miss again."""
+    s = LruSlotSim(2, 16)
+    s.assign(1, 8)
+    s.assign(2, 8)
+    assert s.assign(3, 8) == (OK, 0, 1, 1)
+    assert s.abort_load(0) == (OK, 3)
+    assert s.lookup(3) == -1 and s.lookup(1) == -1
+    assert s.assign(4, 8) == (OK, 0, 1, -1)          # the free slot, nothing evicted
+    assert s.assign(3, 8) == (OK, 1, 1, 2)           # 3 loads again, evicting 2 (LRU)
+    assert (s.evictions, s.aborted, s.misses) == (2, 1, 5)
+    assert s.abort_load(0) == (OK, 4)
+    assert s.abort_load(0) == (STATE_ERR, -1)        # already empty
+    assert s.abort_load(9) == (ARG_ERR, -1)
+
+
+def test_abort_load_ends_reference_and_pin():
+    s = LruSlotSim(2, 16)
+    s.assign(1, 8)
+    s.acquire(0)
+    s.pin(0)
+    assert s.abort_load(0) == (OK, 1)
+    assert s.release(0) == STATE_ERR                 # no reference left
+    assert s.pin(0) == STATE_ERR                     # empty slot
+    s.assign(2, 8)
+    s.assign(3, 8)
+    assert s.assign(4, 8)[3] == 2                    # slot 0 is an ordinary LRU slot again

@@ -151,6 +151,9 @@ SIM_MUTANTS = [
     ("frequency window one short", "if e > self.epoch - self.window)", "if e > self.epoch - self.window + 1)", 0),
     ("pin of an empty slot accepted", "if self.slot_id[s] is None:\n            return STATE_ERR",
      "if False:\n            return STATE_ERR", 0),
+    ("aborted load keeps the id resident", "del self.where[aid]\n        self.aborted += 1",
+     "self.aborted += 1", 0),
+    ("aborted load keeps the reference", "self.refs[s] = 0\n        del self.where[aid]", "del self.where[aid]", 0),
 ]
 
 LRU_PINS = [getattr(lru_pins, n) for n in dir(lru_pins) if n.startswith("test_")]

@@ -47,7 +47,10 @@ MUTANTS = [
     ("keep_score tie to most recent", "(k == best_k && last_use_[s] < last_use_[best])",
      "(k == best_k && last_use_[s] > last_use_[best])"),
     ("release keeps the reference", "    --refs_[slot];\n", "\n"),
-    ("eviction keeps the id resident", "    where_.erase(id);\n", "\n"),
+    ("eviction keeps the id resident", "    where_.erase(id);\n    ++evictions;", "    ++evictions;"),
+    ("aborted load keeps the reference", "    refs_[slot] = 0;\n    where_.erase(id);\n    res_[slot] = nullptr;",
+     "    where_.erase(id);\n    res_[slot] = nullptr;"),
+    ("aborted load not counted", "    ++aborted_loads;\n", "\n"),
 ]
 
 # host-only decision tests (library against the simulator), cheapest first
@@ -61,6 +64,8 @@ CHECKS = [
     lambda lib: abi.test_policy_decision_log_matches_simulator(lib, 1, 0),
     lambda lib: abi.test_policy_decision_log_matches_simulator(lib, 1, 2),
     lambda lib: abi.test_assign_tokens_matches_simulator_and_maps_tokens(lib),
+    lambda lib: abi.test_failed_load_leaves_the_table_consistent(lib),
+    lambda lib: abi.test_random_decisions_with_aborted_loads_match_simulator(lib),
 ]
 
 
