@@ -177,6 +177,39 @@ def test_empty_slot_and_invalid_indices():
     assert st["invalid_token_index"] == 10
 
 
+@pytest.mark.parametrize("how", ["evict", "abort"])
+def test_emptied_slot_reads_as_empty_on_the_device(how):
+    """A slot emptied after its upload -- lora_evict_lru of the least recently
+    used slot, or lora_abort_load of a chosen one -- reads as empty on the
+    device: its tokens come back bit for bit, and the others match the oracle
+    given the same slot as empty."""
+    from rank_adapter_apply_gb300 import binding as B
+    from rank_adapter_apply_gb300.harness import DeviceWorkload
+    T = 40
+    idx = np.array(([0, 1, 2, 3, -1] * 8)[:T])
+    w = _custom(T, 256, 256, 4, 16, [16, 8, 16, 16], idx)
+    dw = DeviceWorkload(w)
+    try:
+        ctx = dw.slots.ctx
+        for a in range(4):                       # bind ids 100..103 to slots 0..3, in that order
+            assert B.lora_assign(ctx, 100 + a, int(w.ranks[a])) == (0, a, 1, -1)
+        if how == "evict":
+            assert B.lora_evict_lru(ctx) == (0, 0, 100)
+            gone = 0
+        else:
+            assert B.lora_abort_load(ctx, 2) == (0, 102)
+            gone = 2
+        out = dw.run(None, multi=True)
+    finally:
+        dw.close()
+    adapters = [None if s == gone else a for s, a in enumerate(w.adapters)]
+    ranks = np.where(np.arange(4) == gone, 0, w.ranks).astype(np.int32)
+    w_gone = wl.Workload("custom", w.dtype, w.max_loras, w.max_lora_rank, w.layers, w.token_slot_idx,
+                         w.xs, w.ys, adapters, ranks, w.alphas)
+    check_layer(w_gone, "l0", out["l0"])
+    assert np.array_equal(out["l0"][idx == gone].view(np.uint8), w.ys["l0"][idx == gone].view(np.uint8))
+
+
 @pytest.mark.parametrize("small_batch", [None, 1024])
 def test_max_rank_64_mixed(small_batch):
     """max_lora_rank 64: the grouped kernels by default, the cluster kernel
