@@ -114,8 +114,10 @@ size_t lora_workspace_bytes(int max_loras, int max_lora_rank, int max_tokens,
  * compute stream). compute_stream / upload_stream: caller-owned cudaStream_t.
  *
  * n_layers == 0 creates a host-only slot table: no CUDA call is made, and only
- * lora_lookup/assign/acquire/release/evict_lru/tick/stats may be used. That is
- * how the slot-table decisions are tested without a GPU.
+ * the slot-table calls (lookup, assign and its batched forms, acquire,
+ * release, evict_lru, abort_load, pin, the policy settings, tick, stats) and
+ * lora_load_slot (bookkeeping only) may be used. That is how the slot-table
+ * decisions are tested without a GPU.
  *
  * On success *out owns host state and CUDA events; free it with lora_destroy.
  */
@@ -141,7 +143,10 @@ void lora_destroy(lora_ctx *ctx);
  * Validation (slot range, 1 <= rank <= max_lora_rank, non-NULL pointers,
  * finite alpha) happens before anything is queued: a rejected call changes
  * nothing. The copies wait for compute work already queued (so a slot being
- * read is never overwritten) and the next apply waits for the copies.
+ * read is never overwritten) and the next apply waits for the copies. On a
+ * host-only context (n_layers == 0) nothing is copied: the call only records
+ * that the slot's adapter has arrived (see lora_abort_load), after the same
+ * validation of slot, rank and alpha.
  */
 int lora_load_slot(lora_ctx *ctx, int slot, const void *const *A_host,
                    const void *const *B_host, int rank, float alpha);
@@ -211,7 +216,8 @@ int lora_lookup(lora_ctx *ctx, uint64_t adapter_id, int *slot);
 
 /*
  * Hit: touch, *slot = its slot, *needs_load = 0. Miss: validate rank first
- * (LORA_ERR_RANK, nothing evicted), then take the lowest free slot, else evict
+ * (LORA_ERR_RANK, nothing evicted), then take the lowest free slot (bound to
+ * no adapter and holding no reference; see lora_abort_load), else evict
  * the slot the eviction policy picks among those not in flight, not pinned and
  * not cooling (least recently used by default; LORA_ERR_NO_SLOT if none);
  * bind the id, *needs_load = 1, *evicted_id = the removed id or UINT64_MAX.
@@ -271,15 +277,21 @@ int lora_evict_lru(lora_ctx *ctx, int *evicted_slot, uint64_t *evicted_id);
 
 /*
  * The upload into `slot` failed or was abandoned (the "load failed" outcome the
- * "vLLM LoRA Resolver 插件详解" page gives a dynamic load, section 6.1): the slot
- * becomes empty, so the adapter lora_assign bound to it is no longer resident
- * and a later assign of that adapter is a miss that loads it again. The adapter
- * the assign evicted stays evicted (its slot bytes may already be overwritten).
- * Counted in aborted_loads, not as an eviction; any in-flight reference and pin
- * of the slot end. With a device context the slot reads as empty (rank 0) for
- * work queued after this call, after compute already queued. *unbound_id = the
- * id that was bound. LORA_ERR_ARG: slot out of range or NULL; LORA_ERR_STATE:
- * the slot is empty.
+ * "vLLM LoRA Resolver 插件详解" page gives a dynamic load, section 6.1). Valid
+ * only while that upload is pending: the slot was bound by a miss of
+ * lora_assign (or a batched admission) and no lora_load_slot / lora_load_slots
+ * into it has been queued since; an adapter whose upload was queued is removed
+ * with eviction instead. The adapter is unbound, so it is no longer resident
+ * and a later assign of it is a miss that loads it again; the adapter the
+ * assign evicted stays evicted (its slot bytes may already be overwritten).
+ * Counted in aborted_loads, not as an eviction; the pin ends. References
+ * already taken on the slot (lora_acquire) stay and are released as usual: the
+ * slot is bound to no adapter meanwhile and becomes free for a new adapter only
+ * once none is left, so a late release can never lower the count of an adapter
+ * bound to the slot later. With a device context the slot reads as empty (rank
+ * 0) for work queued after this call, after compute already queued.
+ * *unbound_id = the id that was bound. LORA_ERR_ARG: slot out of range or
+ * NULL; LORA_ERR_STATE: the slot is empty or its upload was already queued.
  */
 int lora_abort_load(lora_ctx *ctx, int slot, uint64_t *unbound_id);
 
@@ -462,11 +474,15 @@ uint64_t lora_adapter_bytes(int n_layers, const int *d_in, const int *d_out, int
  *
  * Scratch comes from a file-scope device array of 4 MiB that every GPU loading
  * this library holds until the process exits. Calls needing more (large
- * n_tokens at large max_lora_rank) return LORA_ERR_ARG with a message. The
- * first call on each device looks up that array's address while the device is
- * current: make it before any stream capture. All calls share the array:
- * calls whose work overlaps on the GPU race and must be serialised. The call
- * calls no cudaMalloc, cudaFree or other allocating routine.
+ * n_tokens at large max_lora_rank: about 7,970 tokens at max_lora_rank 64)
+ * return LORA_ERR_ARG with a message. Every call looks up that array's address
+ * on the current device (so a device reset or another context on the device
+ * is handled); the first call on a device also loads the library's device
+ * code there: make it before any stream capture. All calls share the array,
+ * which keeps the previous call's contents (what must start at zero is
+ * cleared on `stream` at the start of each call): calls whose work overlaps on
+ * the GPU race and must be serialised. The call calls no cudaMalloc, cudaFree
+ * or other allocating routine.
  */
 int lora_apply_static_scratch(const void *x, void *y, const int32_t *token_slot_idx,
                               int n_tokens, int d_in, int d_out, int max_loras,

@@ -19,8 +19,12 @@ Semantics, as read from the "Multi-LoRA 适配器缓存生产实战" page:
   keep_score  w1 recent + w2 frequency + w3 priority + w4 reload_cost - w5 size.
 
 A failed upload (the "load failed" outcome of a dynamic load on the "vLLM LoRA
-Resolver 插件详解" page, section 6.1) is undone with ``abort_load``: the slot
-becomes empty; the adapter the assign evicted stays evicted.
+Resolver 插件详解" page, section 6.1) is undone with ``abort_load`` while that
+upload is pending (bound by a miss, no upload recorded since with ``loaded``):
+the adapter is unbound; the adapter the assign evicted stays evicted;
+references already taken stay until released, and the slot is free for a new
+adapter only once none is left (so a late release can never lower the count
+of an adapter bound there later).
 
 Readings where the page is silent: the LRU clock is a counter that advances by
 one on every touch or bind, so no two slots tie; a free slot (lowest index
@@ -76,6 +80,7 @@ class LruSlotSim:
         self.aborted = 0
         self.log: list[tuple] = []
         self.pinned = [False] * max_loras
+        self.pending = [False] * max_loras      # bound by a miss, upload not recorded yet
         self.min_residency = 0
         self.policy = LRU
         self.weights = (1.0, 1.0, 1.0, 0.0, 0.0)
@@ -134,6 +139,7 @@ class LruSlotSim:
         aid = self.slot_id[s]
         self.slot_id[s] = None
         self.pinned[s] = False
+        self.pending[s] = False
         del self.where[aid]
         self.evictions += 1
         rec = self.records[aid]
@@ -160,7 +166,7 @@ class LruSlotSim:
             self.rejected += 1
             self.log.append(("assign", aid, RANK_ERR, -1, 0, -1))
             return RANK_ERR, -1, 0, -1
-        free = [s for s in range(self.S) if self.slot_id[s] is None]
+        free = [s for s in range(self.S) if self.slot_id[s] is None and self.refs[s] == 0]
         evicted = -1
         if free:
             s = free[0]
@@ -179,6 +185,7 @@ class LruSlotSim:
         self.where[aid] = s
         self.refs[s] = 0
         self.pinned[s] = False
+        self.pending[s] = True
         self._touch(s)
         self.misses += 1
         self.log.append(("assign", aid, OK, s, 1, evicted))
@@ -209,17 +216,25 @@ class LruSlotSim:
         self.log.append(("evict", OK, s, aid))
         return OK, s, aid
 
+    def loaded(self, s: int) -> int:
+        """An upload into slot s was queued: its adapter is no longer pending."""
+        if not 0 <= s < self.S:
+            return ARG_ERR
+        self.pending[s] = False
+        return OK
+
     def abort_load(self, s: int):
-        """The upload into slot s failed: the slot becomes empty (not an
-        eviction; refs and pin end). Returns (status, id that was bound or -1)."""
+        """The pending upload into slot s failed: the adapter is unbound (not
+        an eviction; the pin ends, references stay until released). Returns
+        (status, id that was bound or -1)."""
         if not 0 <= s < self.S:
             return ARG_ERR, -1
         aid = self.slot_id[s]
-        if aid is None:
+        if aid is None or not self.pending[s]:
             return STATE_ERR, -1
         self.slot_id[s] = None
         self.pinned[s] = False
-        self.refs[s] = 0
+        self.pending[s] = False
         del self.where[aid]
         self.aborted += 1
         self.log.append(("abort", s, aid))

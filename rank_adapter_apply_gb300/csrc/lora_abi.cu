@@ -365,11 +365,15 @@ void lora_destroy(lora_ctx *c) {
 int lora_load_slot(lora_ctx *c, int slot, const void *const *A_host, const void *const *B_host,
                    int rank, float alpha) {
     if (!c) return fail(LORA_ERR_ARG, "ctx is NULL");
-    if (!c->device) return fail(LORA_ERR_STATE, "host-only context has no slot pools");
     if (slot < 0 || slot >= c->S) return fail(LORA_ERR_ARG, "slot %d out of range", slot);
     if (rank < 1 || rank > c->R)
         return fail(LORA_ERR_RANK, "LoRA rank %d exceeds maximum %d (or is < 1)", rank, c->R);
     if (!std::isfinite(alpha)) return fail(LORA_ERR_ARG, "alpha is not finite");
+    if (!c->device) {                 // host-only table: the upload is only recorded
+        c->table.mark_loaded(slot);
+        c->uploads += 1;
+        return LORA_OK;
+    }
     if (!A_host || !B_host) return fail(LORA_ERR_ARG, "A_host / B_host is NULL");
     for (int l = 0; l < c->n_layers; ++l)
         if (!A_host[l] || !B_host[l]) return fail(LORA_ERR_ARG, "layer %d weights are NULL", l);
@@ -406,6 +410,7 @@ int lora_load_slot(lora_ctx *c, int slot, const void *const *A_host, const void 
     c->timing.push_back(tm);
     c->uploads += 1;
     c->upload_bytes += bytes;
+    c->table.mark_loaded(slot);
     if (c->timing.size() > 256) harvest_timings(c, false);
     return LORA_OK;
 }
@@ -505,6 +510,7 @@ int lora_load_slots(lora_ctx *c, int n, const int *slots, const void *const *A_h
         c->timing.push_back(tm);
         c->uploads += (uint64_t)ua.n_slots;
         c->upload_bytes += bytes;
+        for (int k = 0; k < ua.n_slots; ++k) c->table.mark_loaded(ua.slots[k]);
     }
     if (c->timing.size() > 256) harvest_timings(c, false);
     return LORA_OK;
@@ -1023,7 +1029,8 @@ int lora_evict_lru(lora_ctx *c, int *evicted_slot, uint64_t *evicted_id) {
 int lora_abort_load(lora_ctx *c, int slot, uint64_t *unbound_id) {
     if (!c || !unbound_id) return fail(LORA_ERR_ARG, "NULL argument");
     if (slot < 0 || slot >= c->S) return fail(LORA_ERR_ARG, "slot %d out of range", slot);
-    if (!c->table.abort_load(slot, unbound_id)) return fail(LORA_ERR_STATE, "slot %d is empty", slot);
+    if (!c->table.abort_load(slot, unbound_id))
+        return fail(LORA_ERR_STATE, "slot %d is empty or its upload was already queued", slot);
     return mark_slot_empty_on_device(c, slot);
 }
 

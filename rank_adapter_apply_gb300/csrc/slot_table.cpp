@@ -4,7 +4,7 @@ namespace lora {
 
 SlotTable::SlotTable(int max_loras, int max_lora_rank)
     : S_(max_loras), R_(max_lora_rank), id_(max_loras, 0), occ_(max_loras, 0), pin_(max_loras, 0),
-      last_use_(max_loras, 0), refs_(max_loras, 0), res_(max_loras, nullptr) {}
+      pending_(max_loras, 0), last_use_(max_loras, 0), refs_(max_loras, 0), res_(max_loras, nullptr) {}
 
 void SlotTable::touch(int slot) {
     last_use_[slot] = ++clock_;
@@ -76,6 +76,7 @@ uint64_t SlotTable::evict(int slot) {
     uint64_t id = id_[slot];
     occ_[slot] = 0;
     pin_[slot] = 0;
+    pending_[slot] = 0;
     refs_[slot] = 0;
     where_.erase(id);
     ++evictions;
@@ -100,9 +101,11 @@ AssignResult SlotTable::assign(uint64_t id, int rank, int *slot, uint64_t *evict
         *slot = -1;
         return AssignResult::BadRank;
     }
+    // A free slot: unbound and unreferenced (a slot whose load was aborted
+    // stays taken until its references are released).
     int s = -1;
     for (int i = 0; i < S_; ++i)
-        if (!occ_[i]) { s = i; break; }
+        if (!occ_[i] && refs_[i] == 0) { s = i; break; }
     if (s < 0) {
         s = victim();
         if (s < 0) {
@@ -119,6 +122,7 @@ AssignResult SlotTable::assign(uint64_t id, int rank, int *slot, uint64_t *evict
     id_[s] = id;
     occ_[s] = 1;
     pin_[s] = 0;
+    pending_[s] = 1;
     refs_[s] = 0;
     where_[id] = s;
     touch(s);
@@ -147,11 +151,11 @@ bool SlotTable::pin(int slot, bool on) {
 
 bool SlotTable::abort_load(int slot, uint64_t *unbound_id) {
     *unbound_id = UINT64_MAX;
-    if (slot < 0 || slot >= S_ || !occ_[slot]) return false;
+    if (slot < 0 || slot >= S_ || !occ_[slot] || !pending_[slot]) return false;
     const uint64_t id = id_[slot];
     occ_[slot] = 0;
     pin_[slot] = 0;
-    refs_[slot] = 0;
+    pending_[slot] = 0;
     where_.erase(id);
     res_[slot] = nullptr;
     ++aborted_loads;

@@ -49,10 +49,16 @@ public:
     bool release(int slot);
     // Returns false when no occupied slot may be evicted. *slot = -1 if empty.
     bool evict_lru(int *slot, uint64_t *evicted_id);
-    // Empty an occupied slot whose upload failed or was abandoned: the bound
-    // adapter is no longer resident (not counted as an eviction). False if the
-    // slot is out of range or empty.
+    // Unbind the adapter of a slot whose upload failed or was abandoned: only
+    // while that upload is pending (bound by assign, no upload queued since).
+    // The adapter is no longer resident (not counted as an eviction) and the
+    // pin ends; references already taken stay until released, and the slot
+    // is free again once none is left. False if the slot is out of range,
+    // empty or not pending.
     bool abort_load(int slot, uint64_t *unbound_id);
+    // An upload into the slot was queued: its adapter is no longer pending.
+    void mark_loaded(int slot) { pending_[slot] = 0; }
+    bool pending(int slot) const { return pending_[slot]; }
 
     bool pin(int slot, bool on);
     void set_min_residency(int epochs) { min_res_ = epochs < 0 ? 0 : epochs; }
@@ -86,7 +92,7 @@ private:
     uint64_t clock_ = 0;
     int64_t epoch_ = 0;
     std::vector<uint64_t> id_;
-    std::vector<char> occ_, pin_;
+    std::vector<char> occ_, pin_, pending_;
     std::vector<uint64_t> last_use_;
     std::vector<int> refs_;
     std::unordered_map<uint64_t, int> where_;

@@ -13,9 +13,11 @@
 // Properties callers must know:
 //  * g_scratch is kStaticScratchBytes (4 MiB) of device memory that every GPU
 //    which loads this library holds until the process exits.
-//  * The first call on each device looks up the array's device address with
-//    cudaGetSymbolAddress while that device is current; make that first call
-//    before any stream capture.
+//  * Every call looks up the array's device address on the current device
+//    with cudaGetSymbolAddress (which allocates nothing), so the address is
+//    right after a device reset or in another context of the same device. The
+//    first call on a device also loads the library's device code there: make
+//    that first call before any stream capture.
 //  * All calls share the one array and it keeps the previous call's contents.
 //    The arrival counters that must start at zero are cleared on the caller's
 //    stream at the start of every call. Two calls whose work overlaps on the
@@ -28,7 +30,6 @@
 #include <cuda_runtime.h>
 
 #include <cstdio>
-#include <mutex>
 #include <string>
 
 namespace lora {
@@ -37,11 +38,6 @@ namespace {
 constexpr size_t kStaticScratchBytes = 4u << 20;
 
 static __device__ __align__(256) unsigned char g_scratch[kStaticScratchBytes];
-
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void *g_scratch_ptr[kMaxDevices] = {};
-int g_num_sms[kMaxDevices] = {};
 
 int fail_static(int code, const char *msg) { return set_last_error(code, msg); }
 
@@ -92,29 +88,21 @@ extern "C" int lora_apply_static_scratch(const void *x, void *y, const int32_t *
         return fail_static(LORA_ERR_ARG, buf);
     }
 
+    // The array's address on the current device, looked up on every call (a
+    // cached address would go stale after a device reset or in another
+    // context). In host code the name g_scratch is only a host-side stand-in.
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices)
-        return fail_static(LORA_ERR_CUDA, "cudaGetDevice failed");
-    char *scratch = nullptr;
+    if (e != cudaSuccess) return fail_static(LORA_ERR_CUDA, "cudaGetDevice failed");
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_scratch);
+    if (e != cudaSuccess)
+        return fail_static(LORA_ERR_CUDA,
+                           (std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e)).c_str());
+    char *scratch = static_cast<char *>(p);
     int num_sms = 0;
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        if (!g_scratch_ptr[dev]) {
-            void *p = nullptr;
-            e = cudaGetSymbolAddress(&p, g_scratch);
-            if (e != cudaSuccess)
-                return fail_static(LORA_ERR_CUDA, (std::string("cudaGetSymbolAddress: ") +
-                                                   cudaGetErrorString(e)).c_str());
-            int sms = 0;
-            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-            if (e != cudaSuccess) return fail_static(LORA_ERR_CUDA, "cudaDeviceGetAttribute failed");
-            g_scratch_ptr[dev] = p;
-            g_num_sms[dev] = sms;
-        }
-        scratch = static_cast<char *>(g_scratch_ptr[dev]);
-        num_sms = g_num_sms[dev];
-    }
+    e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail_static(LORA_ERR_CUDA, "cudaDeviceGetAttribute failed");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     // Arrival counters of the split reduction and the header start at zero.

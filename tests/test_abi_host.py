@@ -59,13 +59,24 @@ def _host_ctx(S, R):
     return B.lora_slots_init(S, R, 0, 1, B.LORA_DTYPE_BF16, [], None, None, None, 0, None, None)
 
 
+def _host_load(ctx, slot, rank=8):
+    """lora_load_slot on a host-only context: records the upload, copies nothing."""
+    try:
+        B.lora_load_slot(ctx, slot, [], [], rank, 16.0)
+        return 0
+    except B.LoraError as e:
+        return e.code
+
+
 def _run_script(ctx, sim, ops):
+    last_bound = [None]
     for op in ops:
         kind = op[0]
         if kind == "assign":
             got = B.lora_assign(ctx, op[1], op[2])
             exp = sim.assign(op[1], op[2])
             assert got == exp, (op, got, exp)
+            last_bound[0] = got[1] if got[0] == 0 and got[2] == 1 else None
         elif kind == "lookup":
             assert B.lora_lookup(ctx, op[1]) == sim.lookup(op[1]), op
         elif kind == "acquire":
@@ -76,6 +87,15 @@ def _run_script(ctx, sim, ops):
             assert B.lora_evict_lru(ctx) == sim.evict_lru(), op
         elif kind == "abort":
             assert B.lora_abort_load(ctx, op[1]) == sim.abort_load(op[1]), op
+        elif kind == "abort_last":         # the upload of the last assign that bound a slot failed
+            if last_bound[0] is not None:
+                assert B.lora_abort_load(ctx, last_bound[0]) == sim.abort_load(last_bound[0]), op
+        elif kind == "loaded_last":        # the upload of the last assign that bound a slot
+            if last_bound[0] is not None:
+                assert _host_load(ctx, last_bound[0]) == sim.loaded(last_bound[0]) == 0
+        elif kind == "loaded":             # an upload queued into the slot (host-only: recorded)
+            rc = _host_load(ctx, op[1])
+            assert rc == sim.loaded(op[1]), op
         elif kind == "tick":
             B.lora_tick(ctx)
             sim.tick()
@@ -475,16 +495,39 @@ def test_failed_load_leaves_the_table_consistent(lib):
         got = [B.lora_assign(ctx, a, 16) for a in (5, 6)]
         assert got == [sim.assign(a, 16) for a in (5, 6)]
         slot5, slot6 = got[0][1], got[1][1]
-        _run_script(ctx, sim, [("acquire", slot5), ("acquire", slot6), ("abort", slot6),
-                               ("release", slot6),        # the abort ended that reference
+        _run_script(ctx, sim, [("loaded", slot5), ("acquire", slot5), ("acquire", slot6), ("abort", slot6),
+                               ("abort", slot5),          # its upload was queued: refused
+                               ("release", slot6),        # the reference outlives the abort
+                               ("release", slot6),        # ... once
                                ("release", slot5), ("tick",)])
         assert B.lora_lookup(ctx, 6) == -1 and B.lora_lookup(ctx, 5) == got[0][1]
         sim.lookup(5)
         assert [B.lora_lookup(ctx, a) for a in (3, 4)] == [sim.lookup(a) for a in (3, 4)]
         # the retry is a miss into the emptied slot, evicting nothing
         assert B.lora_assign(ctx, 6, 16) == sim.assign(6, 16) == (0, slot6, 1, -1)
-        _run_script(ctx, sim, [("abort", 9), ("abort", 0), ("abort", 0), ("assign", 7, 16)])
+        # out of range; the retried load of 6 fails again; then the slot is empty
+        _run_script(ctx, sim, [("abort", 9), ("abort", slot6), ("abort", slot6), ("abort", slot5),
+                               ("assign", 7, 16)])
         assert B.lora_stats(ctx)["aborted_loads"] == sim.aborted == 2
+    finally:
+        B.lora_destroy(ctx)
+
+
+def test_late_release_after_abort_matches_simulator(lib):
+    """Holder A's adapter is bound and referenced, its upload fails and is
+    aborted; holder B's adapter is bound while A's reference stays (it cannot
+    take A's slot), A releases late, and B's adapter stays protected from
+    eviction while in flight. Every status and decision equals the simulator's."""
+    from oracle.lru_sim import LruSlotSim
+    ctx = _host_ctx(2, 16)
+    sim = LruSlotSim(2, 16)
+    try:
+        _run_script(ctx, sim, [("assign", 10, 8), ("acquire", 0), ("abort", 0), ("acquire", 0),
+                               ("assign", 20, 8), ("loaded", 1), ("acquire", 1), ("release", 0),
+                               ("release", 0), ("assign", 30, 8), ("loaded", 0), ("evict",), ("evict",),
+                               ("abort", 1), ("release", 1), ("evict",)])
+        assert B.lora_lookup(ctx, 20) == sim.lookup(20) == -1
+        assert sim.log[-1] == ("lookup", 20, -1)
     finally:
         B.lora_destroy(ctx)
 
@@ -503,9 +546,16 @@ def test_random_decisions_with_aborted_loads_match_simulator(lib):
         for step in range(300):
             a = int(rng.zipf(1.3)) % 40
             ops.append(("assign", a, int(rng.choice([8, 16, 32]))))
+            u = rng.random()
+            if u < 0.12:                                 # the upload fails
+                ops.append(("abort_last",))
+            elif u < 0.8:                                # the upload is queued
+                ops.append(("loaded_last",))
             r = rng.random()
             if r < 0.1:
                 ops.append(("abort", int(rng.integers(0, S))))
+            elif r < 0.12:
+                ops.append(("loaded", int(rng.integers(-1, S + 1))))
             elif r < 0.15:
                 ops.append(("evict",))
             elif r < 0.35:

@@ -267,14 +267,49 @@ def test_abort_load_frees_the_slot():
     assert s.abort_load(9) == (ARG_ERR, -1)
 
 
-def test_abort_load_ends_reference_and_pin():
+def test_abort_load_ends_pin_and_keeps_references():
+    """The pin ends with the abort; a reference taken before it stays until it
+    is released, and the slot is not reused meanwhile."""
     s = LruSlotSim(2, 16)
     s.assign(1, 8)
     s.acquire(0)
     s.pin(0)
     assert s.abort_load(0) == (OK, 1)
-    assert s.release(0) == STATE_ERR                 # no reference left
-    assert s.pin(0) == STATE_ERR                     # empty slot
+    assert s.pin(0) == STATE_ERR                     # bound to nothing
+    assert s.acquire(0) == STATE_ERR                 # no new reference on an unbound slot
+    assert s.assign(2, 8) == (OK, 1, 1, -1)          # slot 0 still referenced: slot 1 is the free one
+    assert s.release(0) == OK                        # the reference taken before the abort
+    assert s.release(0) == STATE_ERR                 # none left
+    assert s.assign(3, 8) == (OK, 0, 1, -1)          # slot 0 is free again
+    assert s.assign(4, 8) == (OK, 1, 1, 2)           # an ordinary LRU table again: 2 is the oldest
+
+
+def test_abort_only_while_the_upload_is_pending():
+    """An adapter whose upload was recorded cannot be aborted (it is removed by
+    eviction instead); a new bind of the slot makes it pending again."""
+    s = LruSlotSim(2, 16)
+    s.assign(1, 8)
+    assert s.loaded(0) == OK
+    assert s.abort_load(0) == (STATE_ERR, -1)
+    assert s.lookup(1) == 0                          # still resident
     s.assign(2, 8)
-    s.assign(3, 8)
-    assert s.assign(4, 8)[3] == 2                    # slot 0 is an ordinary LRU slot again
+    assert s.assign(3, 8) == (OK, 0, 1, 1)           # evicts 1; 3 is pending in slot 0
+    assert s.abort_load(0) == (OK, 3)
+    assert s.loaded(7) == ARG_ERR
+
+
+def test_late_release_after_abort_cannot_touch_a_later_adapter():
+    """Holder A takes a reference on its adapter's slot, the upload fails and is
+    aborted; holder B's adapter cannot be bound to that slot while A's
+    reference stays, so A's release (however late) lowers no count of B's."""
+    s = LruSlotSim(2, 16)
+    assert s.assign(10, 8) == (OK, 0, 1, -1)
+    s.acquire(0)                                     # holder A
+    assert s.abort_load(0) == (OK, 10)
+    assert s.assign(20, 8) == (OK, 1, 1, -1)         # holder B: slot 1, not the referenced slot 0
+    s.loaded(1)
+    s.acquire(1)
+    assert s.release(0) == OK                        # A's release hits its own slot
+    assert s.assign(30, 8) == (OK, 0, 1, -1)         # slot 0 free now; B's adapter untouched
+    assert s.evict_lru() == (OK, 0, 30)              # B's slot is in flight: never the victim
+    assert s.refs == [0, 1]

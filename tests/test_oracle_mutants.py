@@ -153,7 +153,12 @@ SIM_MUTANTS = [
      "if False:\n            return STATE_ERR", 0),
     ("aborted load keeps the id resident", "del self.where[aid]\n        self.aborted += 1",
      "self.aborted += 1", 0),
-    ("aborted load keeps the reference", "self.refs[s] = 0\n        del self.where[aid]", "del self.where[aid]", 0),
+    ("aborted load drops the references", "del self.where[aid]\n        self.aborted += 1",
+     "self.refs[s] = 0\n        del self.where[aid]\n        self.aborted += 1", 0),
+    ("abort allowed after the upload", "if aid is None or not self.pending[s]:", "if aid is None:", 0),
+    ("aborted slot reused while referenced", "if self.slot_id[s] is None and self.refs[s] == 0]",
+     "if self.slot_id[s] is None]", 0),
+    ("upload does not clear pending", "self.pending[s] = False\n        return OK", "return OK", 0),
 ]
 
 LRU_PINS = [getattr(lru_pins, n) for n in dir(lru_pins) if n.startswith("test_")]

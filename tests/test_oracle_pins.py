@@ -234,3 +234,25 @@ def test_adapter_bytes_formula(layers, rank, bpp, expected):
     assert oracle.adapter_bytes(layers, rank, bpp) == expected
     # the same count as the element count of A [r, d_in] plus B [d_out, r]
     assert expected == sum(rank * di * bpp + do * rank * bpp for di, do in layers)
+
+
+def test_delta_bound_of_the_parity_helper():
+    """The delta-only comparison accepts the oracle's own delta rounded once to
+    bf16 (the one rounding the bound allows) and rejects a delta 1 % off, a
+    delta of the wrong sign, and a changed base-only row."""
+    from tests.parity_util import check_delta, zero_base
+    w = zero_base(wl.decode_qv_4096(0, n_tokens=24))
+    for ly in w.layers:
+        A, B = w.padded_pools(ly.name)
+        ref = oracle.lora_apply_ref(w.xs["x"], w.ys[ly.name], A, B, w.ranks, w.alphas, w.token_slot_idx)
+        good = wl.f32_to_bf16_bits(ref.astype(np.float32))
+        assert check_delta(w, ly.name, good)["worst_ratio"] <= 1.0
+        for bad in (wl.f32_to_bf16_bits((ref * 1.01).astype(np.float32)),
+                    wl.f32_to_bf16_bits((-ref).astype(np.float32))):
+            with pytest.raises(AssertionError):
+                check_delta(w, ly.name, bad)
+        off = np.nonzero(w.token_slot_idx < 0)[0]
+        changed = good.copy()
+        changed[off[0], 0] = 0x3F80
+        with pytest.raises(AssertionError):
+            check_delta(w, ly.name, changed)

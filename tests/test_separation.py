@@ -58,7 +58,7 @@ def test_bench_uses_the_oracle_only_for_cpu_timing():
     host (the cpu_baseline leg and the reference arm) and nowhere else."""
     path = os.path.join(ROOT, "bench.py")
     tree = ast.parse(open(path).read(), path)
-    allowed = {"cpu_oracle_run", "run_reference"}
+    allowed = {"oracle_tokens_per_s", "run_reference"}
     owners = set()
     for f in ast.walk(tree):
         if isinstance(f, ast.FunctionDef):

@@ -25,7 +25,12 @@ MUTANTS = [
     ("touch does not refresh recency", "last_use_[slot] = ++clock_;", "++clock_;"),
     ("most recent evicted", "if (best < 0 || last_use_[s] < last_use_[best]) best = s;",
      "if (best < 0 || last_use_[s] > last_use_[best]) best = s;"),
-    ("highest free slot first", "if (!occ_[i]) { s = i; break; }", "if (!occ_[i]) { s = i; }"),
+    ("highest free slot first", "if (!occ_[i] && refs_[i] == 0) { s = i; break; }",
+     "if (!occ_[i] && refs_[i] == 0) { s = i; }"),
+    ("aborted slot reused while referenced", "if (!occ_[i] && refs_[i] == 0) { s = i; break; }",
+     "if (!occ_[i]) { s = i; break; }"),
+    ("abort allowed after the upload", "|| !occ_[slot] || !pending_[slot]) return false;",
+     "|| !occ_[slot]) return false;"),
     ("in-flight slots evictable", "if (!occ_[s] || refs_[s] > 0 || pin_[s]) return false;",
      "if (!occ_[s] || pin_[s]) return false;"),
     ("pinned slots evictable", "if (!occ_[s] || refs_[s] > 0 || pin_[s]) return false;",
@@ -48,8 +53,8 @@ MUTANTS = [
      "(k == best_k && last_use_[s] > last_use_[best])"),
     ("release keeps the reference", "    --refs_[slot];\n", "\n"),
     ("eviction keeps the id resident", "    where_.erase(id);\n    ++evictions;", "    ++evictions;"),
-    ("aborted load keeps the reference", "    refs_[slot] = 0;\n    where_.erase(id);\n    res_[slot] = nullptr;",
-     "    where_.erase(id);\n    res_[slot] = nullptr;"),
+    ("aborted load drops the references", "    pending_[slot] = 0;\n    where_.erase(id);\n    res_[slot] = nullptr;",
+     "    pending_[slot] = 0;\n    refs_[slot] = 0;\n    where_.erase(id);\n    res_[slot] = nullptr;"),
     ("aborted load not counted", "    ++aborted_loads;\n", "\n"),
 ]
 
@@ -65,6 +70,7 @@ CHECKS = [
     lambda lib: abi.test_policy_decision_log_matches_simulator(lib, 1, 2),
     lambda lib: abi.test_assign_tokens_matches_simulator_and_maps_tokens(lib),
     lambda lib: abi.test_failed_load_leaves_the_table_consistent(lib),
+    lambda lib: abi.test_late_release_after_abort_matches_simulator(lib),
     lambda lib: abi.test_random_decisions_with_aborted_loads_match_simulator(lib),
 ]
 
