@@ -316,9 +316,11 @@ def run_reference(args):
     return 0
 
 
-def load_workload(name):
+def load_workload(name, prefill_seqs=32):
     if name == DECODE:
         return wl.decode_qv_4096(0)
+    if name == HEADLINE and prefill_seqs != 32:
+        return wl.prefill_5120(0, n_seqs=prefill_seqs)      # smaller case for profiler captures
     return wl.BY_NAME[name](0)
 
 
@@ -390,7 +392,7 @@ def run_big(args, ctx, name, headline):
     import torch
     from rank_adapter_apply_gb300.harness import DeviceWorkload
     dev, world, rank = ctx["dev"], ctx["world"], ctx["rank"]
-    w = load_workload(name)
+    w = load_workload(name, args.prefill_seqs if headline else 32)
     dw = DeviceWorkload(w, device=dev, max_tokens=w.n_tokens)
     lys = list(range(len(w.layers)))
     xs = [dw.xs[ly.x_key] for ly in w.layers]
@@ -954,6 +956,9 @@ def main():
                     help="churn: per-slot upload ordering, host runs ahead of the GPU")
     ap.add_argument("--e2e-staging-sets", type=int, default=E2E_STAGING_SETS,
                     help="decode e2e: device staging sets rotated by the host-buffer calls")
+    ap.add_argument("--prefill-seqs", type=int, default=32,
+                    help="sequences of the prefill workload (32 = the full workload; fewer only for "
+                         "profiler captures)")
     ap.add_argument("--quick", action="store_true",
                     help="profiling runs: no e2e, no CPU baseline, no sub-records, short decode graphs")
     args = ap.parse_args()

@@ -112,6 +112,8 @@ size_t lora_workspace_bytes(int max_loras, int max_lora_rank, int max_tokens,
  * that the library writes on every upload or eviction. workspace: device,
  * lora_workspace_bytes(...) bytes, 256-byte aligned; it is zeroed here (on the
  * compute stream). compute_stream / upload_stream: caller-owned cudaStream_t.
+ * max_tokens: at most 16,384 x the GPU's SM count (2,490,368 tokens on a
+ * 152-SM GB300), else LORA_ERR_ARG.
  *
  * n_layers == 0 creates a host-only slot table: no CUDA call is made, and only
  * the slot-table calls (lookup, assign and its batched forms, acquire,
@@ -474,7 +476,7 @@ uint64_t lora_adapter_bytes(int n_layers, const int *d_in, const int *d_out, int
  *
  * Scratch comes from a file-scope device array of 4 MiB that every GPU loading
  * this library holds until the process exits. Calls needing more (large
- * n_tokens at large max_lora_rank: about 7,970 tokens at max_lora_rank 64)
+ * n_tokens at large max_lora_rank: more than 8,090 tokens at max_lora_rank 64)
  * return LORA_ERR_ARG with a message. Every call looks up that array's address
  * on the current device (so a device reset or another context on the device
  * is handled); the first call on a device also loads the library's device

@@ -388,6 +388,8 @@ __device__ __forceinline__ void expand_f32_tile(const LayerArgs &L, const GroupV
 // count and items past the count cost nothing.
 __global__ void __launch_bounds__(kThreads)
 shrink_bf16_kernel(MultiArgs ma, GroupView g, int max_chunks) {
+    grid_dependency_wait();            // launched early: the kernel before has to finish first
+    grid_launch_dependents();
     const int per_tile = max_chunks * ma.n;
     const int items = g.hdr[kHdrTiles] * per_tile;
     for (int w = blockIdx.x; w < items; w += gridDim.x) {
@@ -401,6 +403,8 @@ shrink_bf16_kernel(MultiArgs ma, GroupView g, int max_chunks) {
 
 __global__ void __launch_bounds__(kThreads)
 expand_bf16_kernel(MultiArgs ma, GroupView g, int max_dblocks) {
+    grid_dependency_wait();            // launched early: the kernel before has to finish first
+    grid_launch_dependents();
     const int per_tile = max_dblocks * ma.n;
     const int items = g.hdr[kHdrTiles] * per_tile;
     for (int w = blockIdx.x; w < items; w += gridDim.x) {
@@ -414,6 +418,8 @@ expand_bf16_kernel(MultiArgs ma, GroupView g, int max_dblocks) {
 
 __global__ void __launch_bounds__(kThreads)
 shrink_f32_kernel(MultiArgs ma, GroupView g, int max_chunks) {
+    grid_dependency_wait();            // launched early: the kernel before has to finish first
+    grid_launch_dependents();
     const int per_tile = max_chunks * ma.n;
     const int items = g.hdr[kHdrTiles] * per_tile;
     for (int w = blockIdx.x; w < items; w += gridDim.x) {
@@ -427,6 +433,8 @@ shrink_f32_kernel(MultiArgs ma, GroupView g, int max_chunks) {
 
 __global__ void __launch_bounds__(kThreads)
 expand_f32_kernel(MultiArgs ma, GroupView g, int max_dblocks) {
+    grid_dependency_wait();            // launched early: the kernel before has to finish first
+    grid_launch_dependents();
     const int per_tile = max_dblocks * ma.n;
     const int items = g.hdr[kHdrTiles] * per_tile;
     for (int w = blockIdx.x; w < items; w += gridDim.x) {
@@ -467,15 +475,18 @@ cudaError_t launch_decode(const MultiArgs &ma, const GroupView &gv, int dtype, i
         long long items = (long long)grid_tiles * per_tile * ma.n;
         return (int)(items < cap ? items : cap);
     };
+    cudaError_t e;
     if (dtype == 1) {
-        shrink_bf16_kernel<<<grid(max_chunks), kThreads, 0, st>>>(ma, gv, max_chunks);
-        expand_bf16_kernel<<<grid(max_dblocks), kThreads, 0, st>>>(ma, gv, max_dblocks);
+        e = launch_pdl(shrink_bf16_kernel, dim3(grid(max_chunks)), dim3(kThreads), 0, st, ma, gv, max_chunks);
+        if (e == cudaSuccess)
+            e = launch_pdl(expand_bf16_kernel, dim3(grid(max_dblocks)), dim3(kThreads), 0, st, ma, gv, max_dblocks);
     } else {
-        shrink_f32_kernel<<<grid(max_chunks), kThreads, 0, st>>>(ma, gv, max_chunks);
+        e = launch_pdl(shrink_f32_kernel, dim3(grid(max_chunks)), dim3(kThreads), 0, st, ma, gv, max_chunks);
         size_t smem = (size_t)kTileTokens * gv.R * sizeof(float);
-        expand_f32_kernel<<<grid(max_dblocks), kThreads, smem, st>>>(ma, gv, max_dblocks);
+        if (e == cudaSuccess)
+            e = launch_pdl(expand_f32_kernel, dim3(grid(max_dblocks)), dim3(kThreads), smem, st, ma, gv, max_dblocks);
     }
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_selftest_wait(int *err_word, uint32_t limit, cudaStream_t st) {

@@ -22,15 +22,45 @@ constexpr int kMaxSlots = 256;
 enum HdrWord {
     kHdrTiles = 0, kHdrPrefillTiles = 1, kHdrInvalid = 2, kHdrDecodeTokens = 3,
     kHdrError = 6,      // non-zero: a bounded wait gave up (the affected rows were skipped)
+    // grouping kernel's grid barrier, finished-CTA count and failure flag (zero between calls)
+    kHdrGroupBar = 8, kHdrGroupDone = 9, kHdrGroupFail = 10,
 };
 constexpr int kFusedMaxTokens = 1024;   // batches up to this size take the cluster decode kernel
 
 struct WsLayout {
-    size_t hdr, perm, run_start, run_of, tiles, ptiles, counters, v, part, total;
+    size_t hdr, perm, gx, tiles, ptiles, counters, v, part, total;
+    size_t gx_ints;     // ints of the grouping kernel's exchange area
     int max_tiles, max_ptiles, part_rows, max_tokens, R, max_layers;
 };
 
+// Grouping kernel (group.cu): CTAs for a batch of T tokens, and the largest
+// batch it takes on a GPU with num_sms SMs.
+int group_ctas(int T);
+int group_max_tokens(int num_sms);
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the kernel before it in the stream still runs (its launch and ramp-up
+// overlap that kernel's tail). Every kernel launched this way calls
+// grid_dependency_wait() before it touches memory that an earlier kernel of
+// the stream may read or write; once the wait returns, every earlier kernel
+// has completed (each of them waited on its own predecessor in turn).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 
 // Kernel attributes (e.g. the dynamic shared-memory limit) are per device:
 // one bit per device (ids 0..63) records that the current device has them.
@@ -59,8 +89,9 @@ inline WsLayout ws_layout(int S, int R, int max_tokens, int max_layers) {
     auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
     w.hdr = take(64 * sizeof(int));
     w.perm = take((size_t)T * sizeof(int));
-    w.run_start = take((size_t)(T + 1) * sizeof(int));
-    w.run_of = take((size_t)T * sizeof(int));
+    const int G = group_ctas(T);
+    w.gx_ints = G > 1 ? (size_t)G * (3 + S) : 1;
+    w.gx = take(w.gx_ints * sizeof(int));
     w.tiles = take((size_t)w.max_tiles * sizeof(int4));
     w.ptiles = take((size_t)w.max_ptiles * sizeof(int4));
     w.counters = take((size_t)max_layers * w.max_tiles * sizeof(int));
@@ -102,7 +133,7 @@ struct GroupView {
 };
 
 cudaError_t launch_group_tokens(const int32_t *idx, int T, const int *rank_dev, int S,
-                                int min_run, char *ws, const WsLayout &lay, cudaStream_t st);
+                                int min_run, char *ws, const WsLayout &lay, int num_sms, cudaStream_t st);
 cudaError_t launch_decode(const MultiArgs &ma, const GroupView &gv, int dtype, int grid_tiles,
                           int max_chunks, int max_dblocks, int num_sms, cudaStream_t st);
 // Single-launch decode step on 8-CTA clusters, batches of at most

@@ -324,6 +324,11 @@ int lora_slots_init(lora_ctx **out, int max_loras, int max_lora_rank, int max_to
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess && max_tokens > group_max_tokens(c->num_sms)) {
+        delete c;
+        return fail(LORA_ERR_ARG, "max_tokens %d above the %d tokens one apply may take on this GPU", max_tokens,
+                    group_max_tokens(c->num_sms));
+    }
     for (int s = 0; s < max_loras && e == cudaSuccess; ++s)
         e = cudaEventCreateWithFlags(&c->up_ev[s], cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->compute_done, cudaEventDisableTiming);
@@ -619,7 +624,7 @@ int apply_impl(lora_ctx *c, int n, const int *layers, const void *const *xs, voi
                   reinterpret_cast<uintptr_t>(ys[i]) % 16 == 0;
     }
     CUDA_TRY(launch_group_tokens(idx, T, c->rank_dev, c->S, prefill ? c->prefill_min : 0, c->ws, c->lay,
-                                 c->compute));
+                                 c->num_sms, c->compute));
     ++c->launches;
     if (prefill) {
         // upper bound on prefill tiles: T/128 full tiles plus one ragged tile per run

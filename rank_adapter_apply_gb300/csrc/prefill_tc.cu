@@ -135,6 +135,8 @@ struct ReduceArgs {
 
 __global__ void __launch_bounds__(256)
 prefill_reduce_kernel(const __grid_constant__ ReduceArgs a) {
+    grid_dependency_wait();                 // the shrink's partials
+    grid_launch_dependents();
     const int R4 = a.R / 4, rows_per_cta = 256 / R4, blocks = kPrefillRows / rows_per_cta;
     const int p = blockIdx.x / blocks, rb = blockIdx.x % blocks, l = blockIdx.y;
     if (p >= a.hdr[kHdrPrefillTiles] || a.nch[l] < 2) return;
@@ -179,6 +181,8 @@ prefill_shrink_kernel(const __grid_constant__ ShrinkArgs a) {
     __shared__ int error;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    grid_dependency_wait();                 // the tile list of the grouping kernel
+    grid_launch_dependents();
     if ((int)blockIdx.x >= a.hdr[kHdrPrefillTiles]) return;
     const int4 pt = a.ptiles[blockIdx.x];
     const int s = pt.x, row0 = pt.y, rows = pt.z;
@@ -340,6 +344,8 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
     uint8_t *vbuf = base + (size_t)stages * kStage;            // [2][hi, lo]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    grid_dependency_wait();                 // the partials of V (shrink, chunk sums)
+    grid_launch_dependents();
     const int np = a.hdr[kHdrPrefillTiles];
     const long long total = (long long)np * a.sum_ncb;
     const int k0 = (int)(total * blockIdx.x / gridDim.x);
@@ -655,17 +661,17 @@ cudaError_t launch_r(const ShrinkArgs &sa, int grid_tiles, int n_jobs, size_t sh
         set_device_bit(attr);
     }
     int queued = 0;
-    prefill_shrink_kernel<R><<<dim3(grid_tiles, n_jobs, 1), kThreads, shrink_smem, st>>>(sa);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(prefill_shrink_kernel<R>, dim3(grid_tiles, n_jobs, 1), dim3(kThreads), shrink_smem,
+                               st, sa);
     if (e == cudaSuccess) ++queued;
     if (e == cudaSuccess && ra) {
-        prefill_reduce_kernel<<<dim3(grid_tiles * (kPrefillRows / (256 / (R / 4))), ea.n, 1), 256, 0, st>>>(*ra);
-        e = cudaGetLastError();
+        e = launch_pdl(prefill_reduce_kernel, dim3(grid_tiles * (kPrefillRows / (256 / (R / 4))), ea.n, 1),
+                       dim3(256), 0, st, *ra);
         if (e == cudaSuccess) ++queued;
     }
     if (e == cudaSuccess) {
-        prefill_expand_kernel<R><<<expand_grid, kExpandThreads, expand_smem<R>(ea.stages), st>>>(ea);
-        e = cudaGetLastError();
+        e = launch_pdl(prefill_expand_kernel<R>, dim3(expand_grid), dim3(kExpandThreads), expand_smem<R>(ea.stages),
+                       st, ea);
         if (e == cudaSuccess) ++queued;
     }
     if (kernels) *kernels += queued;

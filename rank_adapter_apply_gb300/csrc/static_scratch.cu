@@ -109,7 +109,7 @@ extern "C" int lora_apply_static_scratch(const void *x, void *y, const int32_t *
     e = cudaMemsetAsync(scratch + lay.counters, 0, (size_t)lay.max_tiles * sizeof(int), st);
     if (e == cudaSuccess) e = cudaMemsetAsync(scratch + lay.hdr, 0, 64 * sizeof(int), st);
     if (e == cudaSuccess)
-        e = launch_group_tokens(token_slot_idx, n_tokens, rank_dev, max_loras, 0, scratch, lay, st);
+        e = launch_group_tokens(token_slot_idx, n_tokens, rank_dev, max_loras, 0, scratch, lay, num_sms, st);
     if (e != cudaSuccess)
         return fail_static(LORA_ERR_CUDA, (std::string("launch: ") + cudaGetErrorString(e)).c_str());
 

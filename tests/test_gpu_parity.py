@@ -608,3 +608,41 @@ def test_host_buffer_path_matches_oracle(device_sets, packed):
                 check_layer(w, name, t.view(torch.int16).numpy().view(np.uint16))
     finally:
         sl.close()
+
+
+@pytest.mark.parametrize("prefill_min", [None, 0])
+def test_grouping_across_blocks(prefill_min):
+    """40,000 tokens: the grouping kernel splits the batch into three blocks of
+    one CTA each. Long runs that cross the block edges (tensor-core prefill
+    tiles, or decode tiles when the prefill path is off), short decode runs,
+    base-only tokens and out-of-range indices next to the edges; sampled tokens
+    (every edge among them) against the oracle, base-only and invalid rows bit
+    for bit, the invalid count exact."""
+    rng = np.random.default_rng(40)
+    T = 40000
+    edges = [T // 3, 2 * T // 3]
+    parts, n = [], 0
+    while n < T:
+        kind = rng.random()
+        if kind < 0.3:
+            ln, s = int(rng.integers(100, 3000)), int(rng.integers(0, 12))
+        elif kind < 0.9:
+            ln, s = int(rng.integers(1, 40)), int(rng.integers(-1, 12))
+        else:
+            ln, s = int(rng.integers(1, 5)), int(rng.choice([12, 99, -7]))
+        parts.append(np.full(ln, s))
+        n += ln
+    idx = np.concatenate(parts)[:T].astype(np.int32)
+    # one run straight across each edge, with an invalid index and a base-only
+    # token right after the first edge
+    for e in edges:
+        idx[e - 700:e + 900] = 5
+    idx[edges[0] + 901] = 99
+    idx[edges[0] + 902] = -1
+    w = _custom(T, 256, 192, 12, 16, [16, 8, 16, 12, 16, 16, 8, 16, 16, 4, 16, 16], idx, seed=41)
+    out, st = _run(w, prefill_min_tokens=prefill_min)
+    near = np.concatenate([np.arange(e - 3, e + 4) for e in edges] + [[0, T - 1, edges[0] + 901, edges[0] + 902]])
+    tok = np.unique(np.concatenate([_sample(w, 600, seed=3), near]))
+    check_layer(w, "l0", out["l0"], tokens=tok)
+    assert st["invalid_token_index"] == int(((idx < -1) | (idx >= 12)).sum())
+    assert st["device_wait_timeouts"] == 0
