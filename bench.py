@@ -376,6 +376,7 @@ def subrecords(args, ctx):
     jobs = [(DECODE, lambda: run_decode(args, ctx, sub=True)),
             ("mixed_ranks_8b", lambda: run_big(args, ctx, "mixed_ranks_8b", headline=False)),
             ("churn_4096 lru", lambda: run_churn(args, ctx, "lru", False, sub=True)),
+            ("churn_4096 lru overlap", lambda: run_churn(args, ctx, "lru", True, sub=True)),
             ("churn_4096 keep_pin32 overlap", lambda: run_churn(args, ctx, "keep_pin32", True, sub=True))]
     for name, job in jobs:
         try:
@@ -909,11 +910,11 @@ def run_churn(args, ctx, policy, overlap, sub=False):
     pol = {"lru": {}, "pin16": {"pin_top": 16},
            "keep": {"policy": 1, "weights": (1.0, 1.0, 0.0, 0.0, 0.0)},
            "keep_pin32": dict(KEEP_PIN32)}[policy]
-    r = ChurnRunner(overlap=overlap, batched_upload=args.churn_upload == "batched", device=ctx["dev"], **pol)
+    r = ChurnRunner(overlap=overlap, device=ctx["dev"], **pol)
     try:
-        r.run(warm)
+        r.run(warm, reset_y=False)
         base = r.slots.stats()
-        res = r.run(trace)
+        res = r.run(trace, reset_y=False)
         st = res.stats
     finally:
         r.close()
@@ -926,7 +927,8 @@ def run_churn(args, ctx, policy, overlap, sub=False):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded Zipf(1.2) adapter ids over 512 with cold bursts)",
             "config": {"workload": "churn_4096", "max_loras": 64, "host_adapters": 512, "rank": 16,
-                       "eviction_policy": policy, "upload_overlap": overlap, "upload": args.churn_upload,
+                       "eviction_policy": policy, "upload_overlap": overlap,
+                       "host_calls_per_step": "one lora_serve_step",
                        "tokens_per_step": 256, "timing": "wall clock over every step of the trace, "
                                                          "host bookkeeping included"},
             "churn": {**d, "thrash_ratio": (d["reloads_after_eviction"] / d["evictions"]) if d["evictions"] else 0.0,
@@ -950,8 +952,6 @@ def main():
     ap.add_argument("--churn-policy", choices=["lru", "pin16", "keep", "keep_pin32"], default="lru",
                     help="churn: pure LRU, LRU with the 16 most popular adapters pinned, keep_score, "
                          "or keep_score (40-epoch window) with the 32 most popular pinned")
-    ap.add_argument("--churn-upload", choices=["batched", "copy"], default="batched",
-                    help="churn: one upload kernel per group (default) or copy-engine copies per adapter")
     ap.add_argument("--churn-overlap", action="store_true",
                     help="churn: per-slot upload ordering, host runs ahead of the GPU")
     ap.add_argument("--e2e-staging-sets", type=int, default=E2E_STAGING_SETS,

@@ -257,6 +257,68 @@ int lora_assign_tokens(lora_ctx *ctx, int n_tokens, const uint64_t *adapter_ids,
                        int acquire, int32_t *token_slot_idx, int max_distinct, uint64_t *distinct_ids,
                        int *slots, int *needs_load, uint64_t *evicted_ids, int *n_distinct, int *n_done);
 
+/*
+ * The host adapter store of lora_serve_step: the CPU-resident adapters that a
+ * miss uploads (tier L1 of the "Multi-LoRA 适配器缓存生产实战" page, section
+ * 冷加载延迟). Entry i: id ids[i] (distinct, not LORA_NO_ADAPTER), rank
+ * ranks[i] (1..max_lora_rank, else LORA_ERR_RANK), lora_alpha alphas[i], and
+ * per layer l the host pointers A_host[i * n_layers + l] ([rank][d_in]) and
+ * B_host[i * n_layers + l] ([d_out][rank]) laid out as for lora_load_slot (NULL
+ * allowed on a host-only context). The library copies the table, not the
+ * weights: the caller keeps that memory alive and unchanged while it stays
+ * registered. A new call replaces the whole store; a rejected call changes
+ * nothing.
+ */
+int lora_register_host_adapters(lora_ctx *ctx, int n, const uint64_t *ids, const int *ranks,
+                                const float *alphas, const void *const *A_host, const void *const *B_host);
+
+/*
+ * The warm set of lora_serve_step: adapters pinned (lora_pin) when a step binds
+ * them or finds them resident unpinned, so the eviction policy never removes
+ * them (the warm set / pin of the "Multi-LoRA 适配器缓存生产实战" page, section
+ * 为什么纯 LRU 在多租户场景下容易失效). Replaces the previous set; removing an id
+ * does not unpin a slot already pinned.
+ */
+int lora_set_warm_set(lora_ctx *ctx, int n, const uint64_t *ids);
+
+/*
+ * One serving step in one call: the batch's tokens name their adapters
+ * (adapter_ids[t], LORA_NO_ADAPTER for base-model tokens), every adapter
+ * registered with lora_register_host_adapters. The distinct adapters, in order
+ * of first appearance, are cut into groups that fit the slots (max_loras
+ * adapters per batch, section 核心原理 of the "Multi-LoRA 适配器缓存生产实战"
+ * page): each adapter needs a slot except one already resident in a pinned
+ * slot, and a group takes at most max_loras minus the slots pinned when the
+ * step starts. Group after group:
+ *   1. each adapter is admitted as by lora_assign (hit: touch; miss: lowest
+ *      free slot or the policy's victim among slots not in flight, pinned or
+ *      cooling) and taken in flight (lora_acquire); warm-set adapters are
+ *      pinned;
+ *   2. the misses are uploaded from the store (lora_load_slots);
+ *   3. idx_bufs[g * n_tokens + t] receives token t's slot if its adapter is in
+ *      group g, else -1, and the delta of the n layers is applied to those
+ *      tokens (lora_apply_multi with xs / ys, reading that buffer);
+ *   4. the group's references are released.
+ * Then the epoch advances (lora_tick). idx_bufs (max_groups * n_tokens int32)
+ * is written by the host and read by the kernels: host memory the GPU can read
+ * (page-locked, or any host memory on a GPU that walks the host's page
+ * tables), which the caller does not rewrite until the step's kernels have run
+ * (the compute stream). Outputs, per distinct adapter in order (when
+ * max_distinct > 0): its id, slot, whether it was uploaded, and the id it
+ * evicted (LORA_NO_ADAPTER if none); *n_distinct and *n_groups.
+ * Errors before any admission leave the table unchanged: an unregistered id,
+ * more than max_distinct adapters, more than max_groups groups (device
+ * contexts), bad arguments. A failed admission (LORA_ERR_NO_SLOT) or upload
+ * returns its status after releasing the references of its group; the groups
+ * before it were applied and released, and the epoch does not advance.
+ * On a host-only context only the admission runs (uploads are recorded as by
+ * lora_load_slot there; layers, xs, ys and idx_bufs may be NULL).
+ */
+int lora_serve_step(lora_ctx *ctx, int n_tokens, const uint64_t *adapter_ids, int n, const int *layers,
+                    const void *const *xs, void *const *ys, int32_t *idx_bufs, int max_groups, int max_distinct,
+                    uint64_t *out_ids, int *out_slots, int *out_needs_load, uint64_t *out_evicted,
+                    int *n_distinct, int *n_groups);
+
 /* lora_release on each of slots[n] in order; stops at the first slot not in flight (LORA_ERR_STATE).
  * The in-flight protection of the "Multi-LoRA 适配器缓存生产实战" page: section 核心原理, last
  * paragraph, and the inflight_requests field of section 数据面. */
@@ -443,11 +505,14 @@ int lora_stats(lora_ctx *ctx, lora_stats_t *out);
 /*
  * Failure-path self test (no counterpart on the source pages): launches, on
  * the compute stream, a one-CTA kernel that waits on a barrier nothing
- * completes, with the same bounded wait every kernel of the library uses. The
- * wait gives up after 2^14 probes, the kernel sets the device error word and
- * returns; *gave_up = 1 once it has. The word stays set, as after a real
- * timeout, and lora_stats reports it (device_wait_timeouts). Nothing faults
- * or hangs and the context stays usable. Synchronises the compute stream.
+ * completes, with the same bounded wait every kernel of the library uses, and
+ * a two-CTA cluster kernel whose CTAs wait on their partial-exchange barriers
+ * with the cluster decode kernel's bounded cluster-scope wait while no peer
+ * arrives. Each wait gives up after 2^14 probes, the kernel sets the device
+ * error word and returns; *gave_up = 1 once all three have. The word stays
+ * set, as after a real timeout, and lora_stats reports it
+ * (device_wait_timeouts). Nothing faults or hangs and the context stays
+ * usable. Synchronises the compute stream.
  */
 int lora_selftest_wait_timeout(lora_ctx *ctx, int *gave_up);
 

@@ -37,6 +37,7 @@ EXPORTED = [
     "lora_set_policy", "lora_set_keep_score_weights", "lora_set_adapter_priority",
     "lora_set_slot_tracking", "lora_load_slots", "lora_assign_batch", "lora_release_batch",
     "lora_selftest_wait_timeout", "lora_assign_tokens", "lora_sync_host", "lora_abort_load",
+    "lora_register_host_adapters", "lora_set_warm_set", "lora_serve_step",
 ]
 
 
@@ -118,6 +119,10 @@ def load(path: str = LIB_PATH):
         "lora_last_error": (ctypes.c_char_p, []),
         "lora_apply_static_scratch": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp,
                                             vp]),
+        "lora_register_host_adapters": (i32, [vp, i32, P(u64), P(i32), P(ctypes.c_float), P(vp), P(vp)]),
+        "lora_set_warm_set": (i32, [vp, i32, P(u64)]),
+        "lora_serve_step": (i32, [vp, i32, P(u64), i32, P(i32), P(vp), P(vp), vp, i32, i32, P(u64), P(i32),
+                                  P(i32), P(u64), P(i32), P(i32)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -367,3 +372,19 @@ def lora_apply_static_scratch(x_ptr, y_ptr, idx_ptr, n_tokens, d_in, d_out, max_
     return check(load().lora_apply_static_scratch(x_ptr, y_ptr, idx_ptr, n_tokens, d_in, d_out,
                                                   max_loras, max_lora_rank, dtype, A_pool, B_pool,
                                                   scale_dev, rank_dev, stream))
+
+
+def lora_register_host_adapters(ctx, ids, ranks, alphas, A_ptrs=None, B_ptrs=None):
+    """ids / ranks / alphas per adapter; A_ptrs / B_ptrs: n * n_layers host
+    pointers, adapter-major (None on a host-only context)."""
+    n = len(ids)
+    A = _vp_array(A_ptrs) if A_ptrs is not None else None
+    Bp = _vp_array(B_ptrs) if B_ptrs is not None else None
+    return check(load().lora_register_host_adapters(
+        ctx, n, (ctypes.c_uint64 * n)(*[int(i) for i in ids]), _i32_array(list(ranks)),
+        (ctypes.c_float * n)(*[float(a) for a in alphas]), A, Bp))
+
+
+def lora_set_warm_set(ctx, ids):
+    n = len(ids)
+    return check(load().lora_set_warm_set(ctx, n, (ctypes.c_uint64 * n)(*[int(i) for i in ids])))

@@ -27,8 +27,13 @@
 //     at most two stages (d_out <= 4096) the products B_s v are formed before
 //     the wait on the previous kernel and parked in shared memory; after the
 //     wait only the y rows (prefetched into L2) are loaded, updated and stored.
-// No global flags, no spin loops; every mbarrier wait is bounded and a wait
-// that gives up sets the error word and leaves the rows it guards unchanged.
+// No global flags; every wait for data is a bounded mbarrier wait (stage
+// loads, and the exchange: each CTA arrives remotely on every peer's exchange
+// barrier after pushing its partial), and a wait that gives up sets the error
+// word and leaves the rows it guards unchanged. The two cluster barriers that
+// remain only make sure that every CTA has started before a peer writes into
+// it and has stopped writing into a peer before that peer exits; each CTA
+// reaches both on every path, whatever its loads do.
 // Each CTA also groups the batch itself (slot ids in shared memory, counts,
 // prefix sums, warp ballots), so the step is a single launch; with
 // programmatic dependent launch the next launch's CTAs are already resident
@@ -63,6 +68,7 @@ struct ClusterSmem {
     int tok[kTileTokens];
     int wcnt[kCW];                         // per-warp counts while collecting the tile's tokens
     uint64_t sbar[2], ebar[2];
+    uint64_t xbar;                         // one remote arrival per CTA of the cluster once its partial is here
     int ntiles, invalid;
     float scale;                           // scale of this tile's slot
     uint32_t bad[kCl];                     // per source rank: its shrink data never arrived
@@ -271,6 +277,7 @@ decode_cluster_kernel(const __grid_constant__ FusedArgs fa) {
         mbar_init(&sm.sbar[1], kCT);
         mbar_init(&sm.ebar[0], kCT);
         mbar_init(&sm.ebar[1], kCT);
+        mbar_init(&sm.xbar, kCl);
         fence_mbar_init();
     }
     __syncthreads();
@@ -392,6 +399,19 @@ decode_cluster_kernel(const __grid_constant__ FusedArgs fa) {
 
     // ---- issue everything that fits in the stage rings --------------------
     for (int j = 0; j < nks && j < 2; ++j) issue_shrink<KB>(L, sm, d, t, R, k0, k1, j, &sm.sbar[j]);
+    // The slot's B rows of this slice and the tile's y rows are read only
+    // after the shrink and the exchange: asking L2 for them now, behind the
+    // shrink's loads, takes their DRAM latency out of the chain that follows.
+    // A prefetch changes nothing a load observes (L2 is where every SM's
+    // stores land), so y may still be written by the kernel before this one.
+    if (nes > 0) {
+        if (tid < t.cnt)
+            prefetch_l2_bulk(static_cast<const uint16_t *>(L.y) + (size_t)sm.tok[tid] * L.d_out + o0,
+                             (uint32_t)(o1 - o0) * 2u);
+        if (tid == kCT - 1)
+            prefetch_l2_bulk(static_cast<const uint16_t *>(L.B) + ((size_t)t.s * L.d_out + o0) * R,
+                             (uint32_t)(o1 - o0) * (uint32_t)R * 2u);
+    }
     bool ok = true;
 
     // ---- shrink over this CTA's d_in slice ---------------------------------
@@ -455,13 +475,6 @@ decode_cluster_kernel(const __grid_constant__ FusedArgs fa) {
     // for it once the partials of v have been exchanged).
     __syncthreads();
     for (int j = 0; j < nes && j < 2; ++j) issue_expand<KB>(L, sm, d, t, R, o0, o1, j, &sm.ebar[j], 1);
-    // The y rows are read right after the wait on the previous kernel. Asking
-    // L2 for them now, behind the shrink's own loads, takes their DRAM latency
-    // out of the chain that follows the wait; the loads after the wait still
-    // see that kernel's writes.
-    if (fa.early && nes >= 1 && nes <= 2 && tid < t.cnt)
-        prefetch_l2_bulk(static_cast<const uint16_t *>(L.y) + (size_t)sm.tok[tid] * L.d_out + o0,
-                         (uint32_t)(o1 - o0) * 2u);
 
     // Cross-warp sum into this CTA's partial v[token][k].
     float *red = d.red;
@@ -500,7 +513,16 @@ decode_cluster_kernel(const __grid_constant__ FusedArgs fa) {
         }
         if (tid < kCl) *cluster.map_shared_rank(&sm.bad[crank], (unsigned)tid) = ok ? 0u : 1u;
     }
-    cluster_sync_all();                     // every partial of the tile has arrived here
+    // Every thread's stores into the peers are done; thread p then arrives on
+    // peer p's exchange barrier (release at cluster scope), and each CTA waits
+    // on its own barrier for the 8 arrivals with the usual iteration limit.
+    // The cluster barrier arrived on here is waited on only before exit, so
+    // that no CTA leaves while a peer may still write into it; it waits for
+    // peers to reach this point, never for data.
+    __syncthreads();
+    if (tid < kCl) mbar_arrive_remote(map_peer(smem_u32(&sm.xbar), (uint32_t)tid));
+    cluster_arrive_release();
+    if (!mbar_wait_bounded_cluster(&sm.xbar, 0, kWaitLimit)) ok = false;
 
     // ---- v = sum of the 8 partials in rank order (deterministic) -----------
     for (int e = tid; e < kTileTokens * KB * 16; e += kCT) {
@@ -633,6 +655,7 @@ decode_cluster_kernel(const __grid_constant__ FusedArgs fa) {
                     }
         }
         if (!ok && tid == 0) atomicExch(fa.hdr + kHdrError, 1);
+        cluster_wait_acquire();             // no peer writes into this CTA any more
         return;
     }
 
@@ -685,9 +708,38 @@ decode_cluster_kernel(const __grid_constant__ FusedArgs fa) {
         if (j + 2 < nes) issue_expand<KB>(L, sm, d, t, R, o0, o1, j + 2, &sm.ebar[b]);
     }
     if (!ok && tid == 0) atomicExch(fa.hdr + kHdrError, 1);
+    cluster_wait_acquire();                 // no peer writes into this CTA any more
+}
+
+// The exchange wait of decode_cluster_kernel on a barrier that nothing
+// arrives on: the same barrier setup, remote-arrival count, cluster-scope
+// bounded wait and exit barrier, in a two-CTA cluster. Each CTA that gives up
+// adds one to `gave_up` and sets the error word, then leaves normally.
+__global__ void __cluster_dims__(2, 1, 1) selftest_cluster_wait_kernel(int *err_word, int *gave_up,
+                                                                       uint32_t limit) {
+    __shared__ uint64_t xbar;
+    if (threadIdx.x == 0) {
+        mbar_init(&xbar, kCl);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    cluster_arrive_relaxed();
+    cluster_wait_acquire();
+    cluster_arrive_release();
+    const bool done = mbar_wait_bounded_cluster(&xbar, 0, limit);
+    if (!done && threadIdx.x == 0) {
+        atomicAdd(gave_up, 1);
+        atomicExch(err_word, 1);
+    }
+    cluster_wait_acquire();
 }
 
 }  // namespace
+
+cudaError_t launch_selftest_cluster_wait(int *err_word, int *gave_up, uint32_t limit, cudaStream_t st) {
+    selftest_cluster_wait_kernel<<<2, 32, 0, st>>>(err_word, gave_up, limit);
+    return cudaGetLastError();
+}
 
 int cluster_decode_kb(int R) { return R <= 16 ? 1 : (R <= 32 ? 2 : 4); }
 

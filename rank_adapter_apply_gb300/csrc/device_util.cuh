@@ -96,6 +96,34 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     return false;
 }
 
+// Arrive on the mbarrier at `cluster_addr` (a shared::cluster address, e.g. a
+// peer CTA's barrier from map_peer), releasing at cluster scope: the writes of
+// this thread, and those ordered before it by a CTA barrier, are visible to a
+// thread that observes the phase with an acquire at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// One probe of phase `parity` acquiring at cluster scope (for barriers that
+// peers of the cluster arrive on remotely).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_bounded_cluster(uint64_t *bar, uint32_t parity, uint32_t limit) {
+    for (uint32_t i = 0; i < limit; ++i)
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+    return false;
+}
+
 // Hint to bring [src, src + bytes) into L2 (16-byte aligned, size % 16 == 0).
 // It has no effect on what any load observes: L2 is where every SM's stores
 // land, so a line fetched early is updated in place by later writes.

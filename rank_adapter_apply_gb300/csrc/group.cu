@@ -10,18 +10,22 @@
 // Multiple slots per batch come from the "Multi-LoRA 适配器缓存生产实战" page,
 // section 核心原理 (max_loras: adapters usable in one batch).
 //
-// Work split: every token is handled on its own. A CTA of 1024 threads owns a
-// block of up to kGBlock tokens (16 contiguous tokens per thread) held in
-// shared memory: a block-wide max scan gives each token the start of its run,
-// a min scan the start of the next run, so each token knows its run's length
-// and slot without walking it. Batches of up to kGBlock tokens take one CTA;
-// larger ones one CTA per block, which exchange per-block figures (first and
-// last run start, prefill tile heads, decode tokens per slot) through the
-// workspace at two grid barriers. The grid never exceeds what fits on the
+// Work split: a CTA of 256 threads owns a block of up to kGBlock = 4096
+// tokens, 16 contiguous tokens per thread, held in shared memory. Each thread
+// marks the run starts among its tokens in a 16-bit mask; a suffix min scan
+// gives it the first run start after its tokens, so every run's length is
+// known to the thread holding its start, which classifies it (prefill tiles
+// or decode tokens) and emits its prefill tiles; a max scan hands the class
+// of the run entering each thread's tokens to that thread. Scans are warp
+// shuffles plus one exchange of warp totals through shared memory. Batches of
+// up to kGBlock tokens take one CTA; larger ones one CTA per block, which
+// exchange per-block figures (first and last run start, prefill tiles,
+// decode tokens per slot) through the workspace at two grid barriers. The grid never exceeds what fits on the
 // GPU at once, every barrier wait is bounded, and a wait that gives up sets
 // the error word and leaves the batch with no tiles at all (every row of y
 // unchanged). The position of a decode token inside its slot's list comes
-// from shared-memory atomics, so the order of tokens of one slot is not fixed;
+// from shared-memory atomics (one per stretch of same-slot tokens of a
+// thread), so the order of tokens of one slot is not fixed;
 // every token's result is computed from its own row only, so no output
 // depends on it.
 #include "kernels.cuh"
@@ -30,13 +34,14 @@
 namespace lora {
 namespace {
 
-constexpr int kGT = 1024;                  // threads per CTA
+constexpr int kGT = 256;                   // threads per CTA
 constexpr int kGPer = 16;                  // contiguous tokens per thread
 constexpr int kGBlock = kGT * kGPer;       // tokens per CTA
 constexpr int kGW = kGT / 32;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr uint32_t kBarrierLimit = 1u << 22;
 constexpr int kNoStart = 0x7fffffff;
+static_assert(kMaxSlots <= kGT, "one thread per slot in the per-slot scans");
 
 struct GroupArgs {
     const int32_t *idx;
@@ -52,49 +57,56 @@ struct GroupSmem {
     int rank[kMaxSlots];
     int cnt[kMaxSlots];             // decode tokens of this block per slot, then the fill counters
     int base[kMaxSlots];            // where this block's decode tokens of each slot start in perm
-    int wpart[kGW];
-    int red;
+    int w0[3][kGW], w1[3][kGW];     // warp totals of the three scan passes
     int invalid;
     int prev_eff;                   // effective slot of the token before the block (-2: none)
     int fail;
+    int blk_last;                   // the block's last run start (block position, -1: none)
     int n_tiles, n_ptiles, n_dec;
-    int up[kGT], from[kGT];         // per-thread last / first run start (block positions)
 };
 
-// Block-wide scans over one value per thread (all threads call). `op` 0: sum,
-// exclusive (returns the sum of lower threads, *total = the sum of all);
-// 1: max, inclusive; 2: min over this and higher threads (inclusive suffix).
-template <int OP>
-__device__ int block_scan(int v, GroupSmem &sm, int *total = nullptr) {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    auto f = [](int a, int b) { return OP == 0 ? a + b : (OP == 1 ? max(a, b) : min(a, b)); };
-    const int ident = OP == 0 ? 0 : (OP == 1 ? -1 : kNoStart);
-    int x = v;
+// Warp-level inclusive scans.
+__device__ __forceinline__ int warp_sum(int x, int lane) {
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const int y = OP == 2 ? __shfl_down_sync(kFull, x, o) : __shfl_up_sync(kFull, x, o);
-        if (OP == 2 ? lane + o < 32 : lane >= o) x = f(x, y);
+        const int y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += y;
     }
-    if (OP == 2 ? lane == 0 : lane == 31) sm.wpart[w] = x;
-    __syncthreads();
-    if (w == 0) {
-        int s = sm.wpart[lane];
+    return x;
+}
+__device__ __forceinline__ int warp_max(int x, int lane) {
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = OP == 2 ? __shfl_down_sync(kFull, s, o) : __shfl_up_sync(kFull, s, o);
-            if (OP == 2 ? lane + o < 32 : lane >= o) s = f(s, y);
-        }
-        sm.wpart[lane] = s;         // inclusive over warps (prefix, or suffix for OP 2)
-        if (lane == (OP == 2 ? 0 : 31)) sm.red = s;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x = max(x, y);
     }
-    __syncthreads();
-    int res;
-    if (OP == 0) res = x - v + (w > 0 ? sm.wpart[w - 1] : 0);
-    else if (OP == 1) res = f(x, w > 0 ? sm.wpart[w - 1] : ident);
-    else res = f(x, w < kGW - 1 ? sm.wpart[w + 1] : ident);
-    if (total) *total = sm.red;
-    __syncthreads();
-    return res;
+    return x;
+}
+__device__ __forceinline__ int warp_suffix_min(int x, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_down_sync(kFull, x, o);
+        if (lane + o < 32) x = min(x, y);
+    }
+    return x;
+}
+
+// Reduce a[q * stride] over q < G (op 0: sum, 1: max, 2: sum over q < lim
+// only), eight loads in flight at a time.
+template <int OP>
+__device__ __forceinline__ int gx_reduce(const int *a, int stride, int G, int lim = 0) {
+    int acc = OP == 1 ? -1 : 0;
+    for (int q0 = 0; q0 < G; q0 += 8) {
+        int v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = q0 + i < G ? a[(size_t)(q0 + i) * stride] : (OP == 1 ? -1 : 0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (OP == 1) acc = max(acc, v[i]);
+            else if (OP == 0 || q0 + i < lim) acc += v[i];
+        }
+    }
+    return acc;
 }
 
 __device__ __forceinline__ int eff_of(int raw, const int *rank_s, int S) {
@@ -114,7 +126,7 @@ __device__ bool grid_barrier(int *ctr, int k, int G) {
         do {
             asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
             if (v >= k * G) break;
-            __nanosleep(64);
+            __nanosleep(32);
         } while (++n < kBarrierLimit);
         __threadfence();
         ok = v >= k * G;
@@ -127,124 +139,211 @@ __global__ void __launch_bounds__(kGT, 1) group_tokens_kernel(const __grid_const
     extern __shared__ __align__(16) unsigned char smem_raw[];
     GroupSmem &sm = *reinterpret_cast<GroupSmem *>(smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    const int c = blockIdx.x, G = a.G, S = a.S;
+    const int c = blockIdx.x, G = a.G, S = a.S, T = a.T;
     // Launched early (programmatic dependent launch): the slot ids and ranks
     // may come from the kernel before, and the previous apply's kernels still
     // read the lists rewritten here, so everything waits for it.
     grid_dependency_wait();
     grid_launch_dependents();
-    const int b0 = (int)((long long)a.T * c / G), b1 = (int)((long long)a.T * (c + 1) / G);
+    const int b0 = (int)((long long)T * c / G), b1 = (int)((long long)T * (c + 1) / G);
     const int n = b1 - b0;
 
     // ---- phase 1: slot ids of the block into shared memory ---------------
+    // every load issued before any is used (one memory round trip)
+    int raw[kGPer];
+#pragma unroll
+    for (int j = 0; j < kGPer; ++j) {
+        const int i = j * kGT + tid;
+        raw[j] = -1;
+        if (i < n) raw[j] = a.idx[b0 + i];
+    }
+    const int raw_prev = (tid == 0 && b0 > 0) ? a.idx[b0 - 1] : -1;
+    const int my_rank = tid < S ? a.rank[tid] : 0;
     if (tid == 0) {
         sm.invalid = 0;
         sm.fail = 0;
         sm.n_tiles = sm.n_ptiles = sm.n_dec = 0;
+        sm.blk_last = -1;
     }
-    for (int s = tid; s < S; s += kGT) {
-        sm.rank[s] = a.rank[s];
-        sm.cnt[s] = 0;
+    if (tid < S) {
+        sm.rank[tid] = my_rank;
+        sm.cnt[tid] = 0;
     }
     int inval = 0;
 #pragma unroll
     for (int j = 0; j < kGPer; ++j) {
-        const int i = j * kGT + tid;
-        const int raw = i < n ? a.idx[b0 + i] : -1;
-        inval += (i < n) && (raw < -1 || raw >= S);
-        sm.eff[i] = raw;
+        inval += raw[j] < -1 || raw[j] >= S;
+        sm.eff[j * kGT + tid] = raw[j];
     }
-    const int raw_prev = (tid == 0 && b0 > 0) ? a.idx[b0 - 1] : -1;
     __syncthreads();
     if (tid == 0) sm.prev_eff = b0 > 0 ? eff_of(raw_prev, sm.rank, S) : -2;
-    const int p0 = tid * kGPer;                 // this thread's tokens: block positions [p0, p0 + 16)
-    int e[kGPer];
-#pragma unroll
-    for (int j = 0; j < kGPer; ++j) e[j] = p0 + j < n ? eff_of(sm.eff[p0 + j], sm.rank, S) : -1;
     if (inval) atomicAdd(&sm.invalid, inval);
-    __syncthreads();
+    // this thread's tokens: block positions [p0, p0 + kGPer), read 16 bytes at a time
+    const int p0 = tid * kGPer;
+    int e[kGPer];
+    {
+        const int4 *src = reinterpret_cast<const int4 *>(sm.eff + p0);
 #pragma unroll
-    for (int j = 0; j < kGPer; ++j) sm.eff[p0 + j] = e[j];
+        for (int q = 0; q < kGPer / 4; ++q) {
+            const int4 v = src[q];
+            e[4 * q] = v.x;
+            e[4 * q + 1] = v.y;
+            e[4 * q + 2] = v.z;
+            e[4 * q + 3] = v.w;
+        }
+#pragma unroll
+        for (int j = 0; j < kGPer; ++j) e[j] = p0 + j < n ? eff_of(e[j], sm.rank, S) : -1;
+    }
+    __syncthreads();
+    {
+        int4 *dst = reinterpret_cast<int4 *>(sm.eff + p0);
+#pragma unroll
+        for (int q = 0; q < kGPer / 4; ++q) dst[q] = make_int4(e[4 * q], e[4 * q + 1], e[4 * q + 2], e[4 * q + 3]);
+    }
     __syncthreads();
 
-    // ---- phase 2: each token's run [start, end) ---------------------------
-    // Run starts (block positions); the last one at or before each token by a
-    // max scan, the first one after each token by a suffix min scan.
-    int last_start = -1, first_start = kNoStart;
+    // ---- phase 2: runs ----------------------------------------------------
+    // Bit j of smask: token p0 + j starts a run (its slot differs from the
+    // token before).
+    unsigned smask = 0;
+    {
+        int prev = tid == 0 ? sm.prev_eff : sm.eff[p0 - 1];
 #pragma unroll
-    for (int j = 0; j < kGPer; ++j) {
-        const int p = p0 + j;
-        const bool st = p < n && e[j] != (p == 0 ? sm.prev_eff : sm.eff[p - 1]);
-        if (st) {
-            last_start = p;
-            if (first_start == kNoStart) first_start = p;
+        for (int j = 0; j < kGPer; ++j) {
+            if (p0 + j < n && e[j] != prev) smask |= 1u << j;
+            prev = e[j];
         }
     }
-    const int upto = block_scan<1>(last_start, sm);      // last start at or before my last token
-    const int from = block_scan<2>(first_start, sm);     // first start at or after my first token
+    // First run start after this thread's tokens (block position): suffix min
+    // over higher lanes, then over higher warps.
+    int hi_start, blk_first;
+    {
+        const int first_start = smask ? p0 + __ffs(smask) - 1 : kNoStart;
+        const int inc = warp_suffix_min(first_start, lane);
+        int exc = __shfl_down_sync(kFull, inc, 1);
+        if (lane == 31) exc = kNoStart;
+        if (lane == 0) sm.w0[0][w] = inc;
+        if (smask) atomicMax(&sm.blk_last, p0 + 31 - __clz(smask));
+        __syncthreads();
+        int higher = kNoStart, all = kNoStart;
+#pragma unroll
+        for (int q = 0; q < kGW; ++q) {
+            const int v = sm.w0[0][q];
+            if (q > w) higher = min(higher, v);
+            all = min(all, v);
+        }
+        hi_start = min(exc, higher);
+        blk_first = all;
+    }
     bool good = true;
     if (G > 1) {
-        // the block's first and last run start, for the neighbouring blocks
-        if (tid == 0) a.gx[c] = from == kNoStart ? kNoStart : b0 + from;
-        if (tid == kGT - 1) a.gx[G + c] = upto < 0 ? -1 : b0 + upto;
+        if (tid == 0) {
+            a.gx[c] = blk_first == kNoStart ? kNoStart : b0 + blk_first;
+            a.gx[G + c] = sm.blk_last < 0 ? -1 : b0 + sm.blk_last;
+        }
         good = grid_barrier(a.hdr + kHdrGroupBar, 1, G);
     }
-    // Runs that cross the block's edges: the last start before the block and
-    // the first start after it (global positions; block 0 starts a run at 0).
-    int before = 0, after = a.T;
+    // The last start before the block and the first one after it (global
+    // positions; block 0 starts a run at token 0).
+    int before = 0, after = T;
     if (G > 1 && good) {
-        for (int q = 0; q < c; ++q) before = max(before, a.gx[G + q]);
-        for (int q = G - 1; q > c; --q) after = a.gx[q] != kNoStart ? a.gx[q] : after;
+        if (c > 0) before = max(0, gx_reduce<1>(a.gx + G, 1, c));
+        for (int q0 = c + 1; q0 < G; q0 += 8) {     // the nearest later block with a start
+            int v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = q0 + i < G ? a.gx[q0 + i] : kNoStart;
+            int f = kNoStart;
+#pragma unroll
+            for (int i = 7; i >= 0; --i) f = v[i] != kNoStart ? v[i] : f;
+            if (f != kNoStart) {
+                after = f;
+                break;
+            }
+        }
     }
-    // The last start among lower threads and the first among higher threads
-    // bound the runs of this thread's first and last tokens; the tokens in
-    // between are walked.
-    sm.up[tid] = upto;
-    sm.from[tid] = from;
-    __syncthreads();
-    const int lo_start = tid > 0 ? sm.up[tid - 1] : -1;
-    const int hi_start = tid < kGT - 1 ? sm.from[tid + 1] : kNoStart;
-
-    int heads = 0;
-    int run_s[kGPer], run_e[kGPer];
+    // Class of a run: 0 none (base-only slot), 1 prefill tiles, 2 decode tokens.
+    auto run_class = [&](int slot, int len) {
+        return slot < 0 ? 0 : ((a.min_run > 0 && len >= a.min_run) ? 1 : 2);
+    };
+    // Runs starting in this thread's tokens: their prefill tiles, the class of
+    // the last one (for the tokens of higher threads), 2 bits of class per start.
+    int heads = 0, last_key = -1;
+    uint32_t cls_bits = 0;
     {
-        int cur = lo_start >= 0 ? b0 + lo_start : before;
-        for (int j = 0; j < kGPer; ++j) {
-            const int p = p0 + j;
-            if (p < n && e[j] != (p == 0 ? sm.prev_eff : sm.eff[p - 1])) cur = b0 + p;
-            run_s[j] = cur;
-        }
-        int nxt = hi_start != kNoStart ? b0 + hi_start : after;
-        for (int j = kGPer - 1; j >= 0; --j) {
-            const int p = p0 + j;
-            run_e[j] = nxt;
-            if (p < n && e[j] != (p == 0 ? sm.prev_eff : sm.eff[p - 1])) nxt = b0 + p;
+        unsigned m = smask;
+        while (m) {
+            const int j = __ffs(m) - 1;
+            m &= m - 1;
+            const int s0 = b0 + p0 + j;
+            const int end = m ? b0 + p0 + __ffs(m) - 1 : (hi_start != kNoStart ? b0 + hi_start : after);
+            const int cls = run_class(sm.eff[p0 + j], end - s0);
+            if (cls == 1) heads += (end - s0 + kPrefillRows - 1) / kPrefillRows;
+            cls_bits |= (uint32_t)cls << (2 * j);
+            last_key = (p0 + j + 1) * 4 + cls;
         }
     }
-    // Classify: prefill tile heads and decode tokens (per-slot counts).
+    // One pass: the last run key of lower threads (max) and the prefill tiles
+    // of lower threads (sum).
+    int key_lower, head_pos, n_heads_blk;
+    {
+        const int km = warp_max(last_key, lane), hs = warp_sum(heads, lane);
+        int km_exc = __shfl_up_sync(kFull, km, 1), hs_exc = hs - heads;
+        if (lane == 0) km_exc = -1;
+        if (lane == 31) {
+            sm.w0[1][w] = km;
+            sm.w1[1][w] = hs;
+        }
+        __syncthreads();
+        int kl = -1, hl = 0, ht = 0;
+#pragma unroll
+        for (int q = 0; q < kGW; ++q) {
+            const int kv = sm.w0[1][q], hv = sm.w1[1][q];
+            if (q < w) {
+                kl = max(kl, kv);
+                hl += hv;
+            }
+            ht += hv;
+        }
+        key_lower = max(km_exc, kl);
+        head_pos = hs_exc + hl;
+        n_heads_blk = ht;
+    }
+    // The class of the run entering this thread's tokens.
+    int cls_cur;
+    if (key_lower >= 0) {
+        cls_cur = key_lower & 3;
+    } else if (c == 0) {
+        cls_cur = 0;                              // token 0 starts a run
+    } else {
+        const int end = blk_first != kNoStart ? b0 + blk_first : after;
+        cls_cur = run_class(sm.prev_eff, end - before);
+    }
     unsigned dec_mask = 0;
 #pragma unroll
     for (int j = 0; j < kGPer; ++j) {
-        const int p = p0 + j;
-        if (p >= n || e[j] < 0) continue;
-        const int len = run_e[j] - run_s[j];
-        if (a.min_run > 0 && len >= a.min_run) {
-            heads += ((b0 + p - run_s[j]) % kPrefillRows) == 0;
-        } else {
-            dec_mask |= 1u << j;
-        }
+        if ((smask >> j) & 1u) cls_cur = (cls_bits >> (2 * j)) & 3u;
+        if (p0 + j < n && e[j] >= 0 && cls_cur == 2) dec_mask |= 1u << j;
     }
+    // decode tokens per slot: one shared atomic per stretch of same-slot
+    // decode tokens among this thread's tokens
+    {
+        int cs = -1, cl = 0;
 #pragma unroll
-    for (int j = 0; j < kGPer; ++j) {
-        const int s = (dec_mask >> j) & 1u ? e[j] : -1 - lane;
-        const unsigned peers = __match_any_sync(kFull, s);
-        if (s >= 0 && lane == __ffs(peers) - 1) atomicAdd(&sm.cnt[s], __popc(peers));
+        for (int j = 0; j < kGPer; ++j) {
+            const int s = (dec_mask >> j) & 1u ? e[j] : -1;
+            if (s != cs) {
+                if (cs >= 0) atomicAdd(&sm.cnt[cs], cl);
+                cs = s;
+                cl = 0;
+            }
+            cl += s >= 0;
+        }
+        if (cs >= 0) atomicAdd(&sm.cnt[cs], cl);
     }
-    int n_heads_blk;
-    const int head_pos = block_scan<0>(heads, sm, &n_heads_blk);
+    __syncthreads();
     if (G > 1) {
         if (tid == 0) a.gx[2 * G + c] = n_heads_blk;
-        for (int s = tid; s < S; s += kGT) a.gx[3 * G + c * S + s] = sm.cnt[s];
+        if (tid < S) a.gx[3 * G + c * S + tid] = sm.cnt[tid];
         good = grid_barrier(a.hdr + kHdrGroupBar, 2, G) && good;
     }
     if (!good) {
@@ -255,70 +354,96 @@ __global__ void __launch_bounds__(kGT, 1) group_tokens_kernel(const __grid_const
 
     // ---- phase 3: offsets, then every list ---------------------------------
     {
-    int head0 = 0, n_ptiles = n_heads_blk;
-    if (G > 1) {
-        n_ptiles = 0;
-        for (int q = 0; q < G; ++q) {
-            const int h = a.gx[2 * G + q];
-            head0 += q < c ? h : 0;
-            n_ptiles += h;
-        }
-    }
-    // decode tokens per slot over the batch, and this block's share before it
-    int tot = 0, mine_before = 0;
-    if (tid < S) {
+        int head0 = 0, n_ptiles = n_heads_blk;
         if (G > 1) {
-            for (int q = 0; q < G; ++q) {
-                const int v = a.gx[3 * G + q * S + tid];
-                tot += v;
-                mine_before += q < c ? v : 0;
-            }
-        } else {
-            tot = sm.cnt[tid];
+            head0 = gx_reduce<2>(a.gx + 2 * G, 1, G, c);
+            n_ptiles = gx_reduce<0>(a.gx + 2 * G, 1, G);
         }
-    }
-    int n_dec;
-    const int slot_off = block_scan<0>(tid < S ? tot : 0, sm, &n_dec);
-    const int nt = (tot + kTileTokens - 1) / kTileTokens;
-    int n_tiles;
-    const int tile_off = block_scan<0>(tid < S ? nt : 0, sm, &n_tiles);
-    if (tid < S) {
-        sm.base[tid] = slot_off + mine_before;
-        sm.cnt[tid] = 0;                        // now the fill counter of this block
-        if (c == 0)
-            for (int i = 0; i < nt; ++i) {
-                const int k = tot - i * kTileTokens;
-                a.tiles[tile_off + i] = make_int4(tid, slot_off + i * kTileTokens, k < kTileTokens ? k : kTileTokens,
-                                                  sm.rank[tid]);
+        // decode tokens per slot over the batch (thread = slot), and the
+        // blocks' share before this one
+        int tot = 0, mine_before = 0;
+        if (tid < S) {
+            if (G > 1) {
+                tot = gx_reduce<0>(a.gx + 3 * G + tid, S, G);
+                mine_before = gx_reduce<2>(a.gx + 3 * G + tid, S, G, c);
+            } else {
+                tot = sm.cnt[tid];
             }
-    }
-    __syncthreads();
-    // prefill tiles, in token order
-    int hp = head0 + head_pos;
+        }
+        // One pass: each slot's first place in perm and first decode tile.
+        const int nt = (tot + kTileTokens - 1) / kTileTokens;
+        int slot_off, tile_off, n_dec, n_tiles;
+        {
+            const int ds = warp_sum(tot, lane), ts = warp_sum(nt, lane);
+            if (lane == 31) {
+                sm.w0[2][w] = ds;
+                sm.w1[2][w] = ts;
+            }
+            __syncthreads();
+            int dl = 0, tl = 0, dt = 0, tt = 0;
 #pragma unroll
-    for (int j = 0; j < kGPer; ++j) {
-        const int p = p0 + j;
-        if (p >= n || e[j] < 0 || ((dec_mask >> j) & 1u)) continue;
-        if (((b0 + p - run_s[j]) % kPrefillRows) != 0) continue;
-        const int rows = run_e[j] - (b0 + p);
-        a.ptiles[hp++] = make_int4(e[j], b0 + p, rows < kPrefillRows ? rows : kPrefillRows, 0);
-    }
-    // decode tokens: a place in their slot's list
+            for (int q = 0; q < kGW; ++q) {
+                const int dv = sm.w0[2][q], tv = sm.w1[2][q];
+                if (q < w) {
+                    dl += dv;
+                    tl += tv;
+                }
+                dt += dv;
+                tt += tv;
+            }
+            slot_off = ds - tot + dl;
+            tile_off = ts - nt + tl;
+            n_dec = dt;
+            n_tiles = tt;
+        }
+        if (tid < S) {
+            sm.base[tid] = slot_off + mine_before;
+            sm.cnt[tid] = 0;                        // from here the fill counter of this block
+            if (c == 0)
+                for (int i = 0; i < nt; ++i) {
+                    const int k = tot - i * kTileTokens;
+                    a.tiles[tile_off + i] = make_int4(tid, slot_off + i * kTileTokens,
+                                                      k < kTileTokens ? k : kTileTokens, sm.rank[tid]);
+                }
+        }
+        __syncthreads();
+        // prefill tiles of the runs starting here, in token order
+        int hp = head0 + head_pos;
+        unsigned m = smask;
+        while (m) {
+            const int j = __ffs(m) - 1;
+            m &= m - 1;
+            if (((cls_bits >> (2 * j)) & 3u) != 1u) continue;
+            const int s0 = b0 + p0 + j;
+            const int end = m ? b0 + p0 + __ffs(m) - 1 : (hi_start != kNoStart ? b0 + hi_start : after);
+            const int slot = sm.eff[p0 + j];
+            for (int r = s0; r < end; r += kPrefillRows)
+                a.ptiles[hp++] = make_int4(slot, r, end - r < kPrefillRows ? end - r : kPrefillRows, 0);
+        }
+        // decode tokens: each stretch of same-slot decode tokens of this
+        // thread claims a place in its slot's list with one shared atomic
+        {
+            int cs = -1, cl = 0, cj = 0;
 #pragma unroll
-    for (int j = 0; j < kGPer; ++j) {
-        const int s = (dec_mask >> j) & 1u ? e[j] : -1 - lane;
-        const unsigned peers = __match_any_sync(kFull, s);
-        const int leader = __ffs(peers) - 1;
-        int at = 0;
-        if (s >= 0 && lane == leader) at = atomicAdd(&sm.cnt[s], __popc(peers));
-        at = __shfl_sync(kFull, at, leader);
-        if (s >= 0) a.perm[sm.base[s] + at + __popc(peers & ((1u << lane) - 1u))] = b0 + p0 + j;
-    }
-    if (tid == 0) {
-        sm.n_tiles = n_tiles;
-        sm.n_ptiles = n_ptiles;
-        sm.n_dec = n_dec;
-    }
+            for (int j = 0; j <= kGPer; ++j) {
+                const int s = j < kGPer && ((dec_mask >> j) & 1u) ? e[j] : -1;
+                if (s != cs || j == kGPer) {
+                    if (cs >= 0) {
+                        const int at = sm.base[cs] + atomicAdd(&sm.cnt[cs], cl);
+                        for (int k = 0; k < cl; ++k) a.perm[at + k] = b0 + p0 + cj + k;
+                    }
+                    cs = s;
+                    cl = 0;
+                    cj = j;
+                }
+                cl += s >= 0;
+            }
+        }
+        if (tid == 0) {
+            sm.n_tiles = n_tiles;
+            sm.n_ptiles = n_ptiles;
+            sm.n_dec = n_dec;
+        }
     }
 
     // ---- the header: written by the last CTA to finish ---------------------
@@ -330,11 +455,12 @@ header:
         if (sm.fail) {
             atomicExch(a.hdr + kHdrError, 1);
             atomicExch(a.hdr + kHdrGroupFail, 1);
+            __threadfence();                    // the flag before the count
         }
-        __threadfence();
+        // (the lists need no fence: the kernels that read them start after
+        // this one has completed)
         const int done = G > 1 ? atomicAdd(a.hdr + kHdrGroupDone, 1) : 0;
         if (done == G - 1) {
-            __threadfence();
             const bool failed = sm.fail || (G > 1 && atomicAdd(a.hdr + kHdrGroupFail, 0) != 0);
             // A failed barrier leaves the lists incomplete: no tiles at all.
             a.hdr[kHdrTiles] = failed ? 0 : n_tiles;

@@ -24,6 +24,7 @@ enum HdrWord {
     kHdrError = 6,      // non-zero: a bounded wait gave up (the affected rows were skipped)
     // grouping kernel's grid barrier, finished-CTA count and failure flag (zero between calls)
     kHdrGroupBar = 8, kHdrGroupDone = 9, kHdrGroupFail = 10,
+    kHdrSelftest = 11,  // CTAs of the cluster self-test that gave up
 };
 constexpr int kFusedMaxTokens = 1024;   // batches up to this size take the cluster decode kernel
 
@@ -203,5 +204,8 @@ int set_last_error(int code, const char *msg);
 cudaError_t launch_set_slot(float *scale_dev, int *rank_dev, int slot, float scale, int rank,
                             cudaStream_t st);
 cudaError_t launch_selftest_wait(int *err_word, uint32_t limit, cudaStream_t st);
+// The cluster decode kernel's exchange wait on a barrier nothing arrives on
+// (two-CTA cluster); *gave_up += 1 for each CTA that gave up.
+cudaError_t launch_selftest_cluster_wait(int *err_word, int *gave_up, uint32_t limit, cudaStream_t st);
 
 }  // namespace lora

@@ -12,6 +12,8 @@
 #include <cstdio>
 #include <cstring>
 #include <string>
+#include <unordered_map>
+#include <unordered_set>
 #include <vector>
 
 using namespace lora;
@@ -108,6 +110,15 @@ struct lora_ctx {
     // lora_assign_tokens: open-addressing table adapter id -> distinct index
     std::vector<uint64_t> tok_key;
     std::vector<int> tok_val, tok_rank;
+    // lora_serve_step: the registered host adapter store (id -> index; per
+    // adapter rank, alpha and per-layer host pointers), the warm set, scratch
+    std::unordered_map<uint64_t, int> store;
+    std::vector<int> store_rank;
+    std::vector<float> store_alpha;
+    std::vector<const void *> store_A, store_B;
+    std::unordered_set<uint64_t> warm;
+    std::vector<int> step_tok, step_group, step_slot, step_need;
+    std::vector<uint64_t> step_id, step_ev;
 
     lora_ctx(int S_, int R_) : table(S_, R_) {}
 };
@@ -934,6 +945,189 @@ int lora_assign_tokens(lora_ctx *c, int T, const uint64_t *adapter_ids, const in
     return rc;
 }
 
+int lora_register_host_adapters(lora_ctx *c, int n, const uint64_t *ids, const int *ranks,
+                                const float *alphas, const void *const *A_host, const void *const *B_host) {
+    if (!c) return fail(LORA_ERR_ARG, "ctx is NULL");
+    if (n < 0) return fail(LORA_ERR_ARG, "n must be >= 0");
+    const int L = c->n_layers;
+    if (n > 0 && (!ids || !ranks || !alphas || (L > 0 && (!A_host || !B_host))))
+        return fail(LORA_ERR_ARG, "NULL argument");
+    std::unordered_map<uint64_t, int> m;
+    m.reserve((size_t)n * 2);
+    for (int i = 0; i < n; ++i) {
+        if (ids[i] == LORA_NO_ADAPTER) return fail(LORA_ERR_ARG, "adapter %d has the no-adapter id", i);
+        if (!m.emplace(ids[i], i).second) return fail(LORA_ERR_ARG, "adapter id of entry %d appears twice", i);
+        if (ranks[i] < 1 || ranks[i] > c->R)
+            return fail(LORA_ERR_RANK, "LoRA rank %d exceeds maximum %d (or is < 1)", ranks[i], c->R);
+        if (!std::isfinite(alphas[i])) return fail(LORA_ERR_ARG, "alpha %d is not finite", i);
+        for (int l = 0; l < L; ++l)
+            if (!A_host[(size_t)i * L + l] || !B_host[(size_t)i * L + l])
+                return fail(LORA_ERR_ARG, "adapter %d layer %d weights are NULL", i, l);
+    }
+    c->store.swap(m);
+    c->store_rank.assign(ranks, ranks + n);
+    c->store_alpha.assign(alphas, alphas + n);
+    c->store_A.assign(A_host, A_host + (size_t)n * L);
+    c->store_B.assign(B_host, B_host + (size_t)n * L);
+    return LORA_OK;
+}
+
+int lora_set_warm_set(lora_ctx *c, int n, const uint64_t *ids) {
+    if (!c) return fail(LORA_ERR_ARG, "ctx is NULL");
+    if (n < 0 || (n > 0 && !ids)) return fail(LORA_ERR_ARG, "bad arguments");
+    c->warm.clear();
+    c->warm.insert(ids, ids + n);
+    return LORA_OK;
+}
+
+int lora_serve_step(lora_ctx *c, int T, const uint64_t *adapter_ids, int n, const int *layers,
+                    const void *const *xs, void *const *ys, int32_t *idx_bufs, int max_groups, int max_distinct,
+                    uint64_t *out_ids, int *out_slots, int *out_needs_load, uint64_t *out_evicted,
+                    int *n_distinct, int *n_groups) {
+    if (!c || !n_distinct || !n_groups) return fail(LORA_ERR_ARG, "NULL argument");
+    *n_distinct = 0;
+    *n_groups = 0;
+    if (T < 0 || max_groups < 0 || max_distinct < 0) return fail(LORA_ERR_ARG, "negative size");
+    if (T > 0 && !adapter_ids) return fail(LORA_ERR_ARG, "adapter_ids is NULL");
+    if (max_distinct > 0 && (!out_ids || !out_slots || !out_needs_load || !out_evicted))
+        return fail(LORA_ERR_ARG, "NULL output array");
+    if (c->device && T > 0) {
+        if (T > c->max_tokens) return fail(LORA_ERR_ARG, "n_tokens %d above max_tokens %d", T, c->max_tokens);
+        if (n < 1 || n > c->max_layers || !layers || !xs || !ys || !idx_bufs)
+            return fail(LORA_ERR_ARG, "layers, xs, ys and idx_bufs are required (n in 1..%d)", c->max_layers);
+        for (int i = 0; i < n; ++i)
+            if (layers[i] < 0 || layers[i] >= c->n_layers || !xs[i] || !ys[i])
+                return fail(LORA_ERR_ARG, "bad layer entry %d", i);
+    }
+    // Distinct adapters in order of first appearance; each token's index among them.
+    size_t cap = 16;
+    while (cap < 2 * (size_t)T) cap <<= 1;
+    if (c->tok_key.size() < cap) {
+        c->tok_key.resize(cap);
+        c->tok_val.resize(cap);
+    }
+    std::fill(c->tok_key.begin(), c->tok_key.begin() + cap, LORA_NO_ADAPTER);
+    const size_t mask = cap - 1;
+    std::vector<uint64_t> &dist = c->step_id;
+    std::vector<int> &tok = c->step_tok;
+    dist.clear();
+    tok.resize((size_t)T);
+    for (int t = 0; t < T; ++t) {
+        const uint64_t id = adapter_ids[t];
+        if (id == LORA_NO_ADAPTER) {
+            tok[t] = -1;
+            continue;
+        }
+        size_t h = (size_t)((id * 0x9E3779B97F4A7C15ull) >> 17) & mask;
+        while (c->tok_key[h] != LORA_NO_ADAPTER && c->tok_key[h] != id) h = (h + 1) & mask;
+        if (c->tok_key[h] == LORA_NO_ADAPTER) {
+            if (!c->store.count(id)) return fail(LORA_ERR_ARG, "adapter id %llu is not registered",
+                                                 (unsigned long long)id);
+            c->tok_key[h] = id;
+            c->tok_val[h] = (int)dist.size();
+            dist.push_back(id);
+        }
+        tok[t] = c->tok_val[h];
+    }
+    const int nd = (int)dist.size();
+    if (max_distinct > 0 && nd > max_distinct)
+        return fail(LORA_ERR_ARG, "more than max_distinct (%d) adapters in the batch", max_distinct);
+    // Groups: at most max_loras minus the pinned slots need a slot each; an
+    // adapter resident in a pinned slot needs none.
+    int pinned = 0;
+    for (int s = 0; s < c->S; ++s) pinned += c->table.pinned(s) ? 1 : 0;
+    const int capacity = c->S - pinned;
+    std::vector<int> &grp = c->step_group;
+    grp.resize((size_t)nd);
+    int ng = 0, cost = 0, in_cur = 0;
+    for (int i = 0; i < nd; ++i) {
+        const int s = c->table.find(dist[i]);
+        const int k = (s >= 0 && c->table.pinned(s)) ? 0 : 1;
+        if (in_cur > 0 && cost + k > capacity) {
+            ++ng;
+            cost = 0;
+            in_cur = 0;
+        }
+        grp[i] = ng;
+        cost += k;
+        ++in_cur;
+    }
+    if (nd > 0) ++ng;
+    if (c->device && ng > max_groups)
+        return fail(LORA_ERR_ARG, "the batch needs %d adapter groups, idx_bufs holds %d", ng, max_groups);
+    std::vector<int> &slot = c->step_slot, &need = c->step_need;
+    std::vector<uint64_t> &ev = c->step_ev;
+    slot.assign((size_t)nd, -1);
+    need.assign((size_t)nd, 0);
+    ev.assign((size_t)nd, LORA_NO_ADAPTER);
+    const int L = c->n_layers;
+    std::vector<int> up_slots, up_ranks;
+    std::vector<float> up_alphas;
+    std::vector<const void *> up_A, up_B;
+    int i0 = 0;
+    for (int g = 0; g < ng; ++g) {
+        int i1 = i0;
+        while (i1 < nd && grp[i1] == g) ++i1;
+        // admission of the group's adapters, in order: hit (touch) or bind, and
+        // an in-flight reference on each
+        up_slots.clear();
+        up_ranks.clear();
+        up_alphas.clear();
+        up_A.clear();
+        up_B.clear();
+        for (int i = i0; i < i1; ++i) {
+            const int si = c->store.at(dist[i]);
+            int rc = lora_assign(c, dist[i], c->store_rank[si], &slot[i], &need[i], &ev[i]);
+            if (rc != LORA_OK) {
+                for (int q = i0; q < i; ++q) c->table.release(slot[q]);
+                return rc;
+            }
+            c->table.acquire(slot[i]);
+            if (c->warm.count(dist[i]) && !c->table.pinned(slot[i])) c->table.pin(slot[i], true);
+            if (need[i]) {
+                up_slots.push_back(slot[i]);
+                up_ranks.push_back(c->store_rank[si]);
+                up_alphas.push_back(c->store_alpha[si]);
+                for (int l = 0; l < L; ++l) {
+                    up_A.push_back(c->store_A[(size_t)si * L + l]);
+                    up_B.push_back(c->store_B[(size_t)si * L + l]);
+                }
+            }
+        }
+        int rc = LORA_OK;
+        if (!up_slots.empty()) {
+            if (c->device) {
+                rc = lora_load_slots(c, (int)up_slots.size(), up_slots.data(), up_A.data(), up_B.data(),
+                                     up_ranks.data(), up_alphas.data());
+            } else {
+                for (int s : up_slots) c->table.mark_loaded(s);
+                c->uploads += up_slots.size();
+            }
+        }
+        if (rc == LORA_OK && c->device && T > 0) {
+            int32_t *idx = idx_bufs + (size_t)g * T;
+            for (int t = 0; t < T; ++t) {
+                const int i = tok[t];
+                idx[t] = (i >= i0 && i < i1) ? slot[i] : -1;
+            }
+            rc = apply_impl(c, n, layers, xs, ys, idx, T);
+        }
+        for (int i = i0; i < i1; ++i) c->table.release(slot[i]);
+        if (rc != LORA_OK) return rc;
+        i0 = i1;
+    }
+    c->table.tick();
+    for (int i = 0; i < nd && i < max_distinct; ++i) {
+        out_ids[i] = dist[i];
+        out_slots[i] = slot[i];
+        out_needs_load[i] = need[i];
+        out_evicted[i] = ev[i];
+    }
+    *n_distinct = nd;
+    *n_groups = ng;
+    return LORA_OK;
+}
+
 int lora_release_batch(lora_ctx *c, int n, const int *slots) {
     if (!c) return fail(LORA_ERR_ARG, "ctx is NULL");
     if (n < 0 || (n > 0 && !slots)) return fail(LORA_ERR_ARG, "bad arguments");
@@ -1088,13 +1282,16 @@ int lora_selftest_wait_timeout(lora_ctx *c, int *gave_up) {
     if (!c || !gave_up) return fail(LORA_ERR_ARG, "NULL argument");
     if (!c->device) return fail(LORA_ERR_STATE, "host-only context has no device");
     *gave_up = 0;
-    int *word = reinterpret_cast<int *>(c->ws + c->lay.hdr) + kHdrError;
-    CUDA_TRY(launch_selftest_wait(word, 1u << 14, c->compute));
-    ++c->launches;
+    int *hdr = reinterpret_cast<int *>(c->ws + c->lay.hdr);
+    CUDA_TRY(cudaMemsetAsync(hdr + kHdrSelftest, 0, sizeof(int), c->compute));
+    CUDA_TRY(launch_selftest_wait(hdr + kHdrError, 1u << 14, c->compute));
+    CUDA_TRY(launch_selftest_cluster_wait(hdr + kHdrError, hdr + kHdrSelftest, 1u << 14, c->compute));
+    c->launches += 2;
     CUDA_TRY(cudaStreamSynchronize(c->compute));
-    int v = 0;
-    CUDA_TRY(cudaMemcpy(&v, word, sizeof v, cudaMemcpyDeviceToHost));
-    *gave_up = v != 0;
+    int v[2] = {0, 0};
+    CUDA_TRY(cudaMemcpy(&v[0], hdr + kHdrError, sizeof(int), cudaMemcpyDeviceToHost));
+    CUDA_TRY(cudaMemcpy(&v[1], hdr + kHdrSelftest, sizeof(int), cudaMemcpyDeviceToHost));
+    *gave_up = v[0] != 0 && v[1] == 2;
     return LORA_OK;
 }
 

@@ -43,6 +43,11 @@ public:
 
     // Hit: touch, return slot. Miss: -1, no state change.
     int lookup(uint64_t id);
+    // The slot holding the adapter, or -1; no state change (no touch).
+    int find(uint64_t id) const {
+        auto it = where_.find(id);
+        return it == where_.end() ? -1 : it->second;
+    }
     // See lora_assign in the public header.
     AssignResult assign(uint64_t id, int rank, int *slot, uint64_t *evicted_id);
     bool acquire(int slot);
