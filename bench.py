@@ -70,20 +70,19 @@ def peaks():
         return 6800.0, "fallback"
 
 
-def kernel_traffic(record: str, kernel_file: str):
-    """DRAM bytes per step from a committed ncu summary, if that summary was
-    taken on the current kernel source (else None)."""
+def kernel_traffic(record: str):
+    """DRAM bytes per launch (or per step) from a committed ncu summary, if
+    that summary was taken on the current sources of its kernels (else None)."""
     import hashlib
-    src = os.path.join(ROOT, "rank_adapter_apply_gb300", "csrc", kernel_file)
-    summ = os.path.join(ROOT, "profiles", record)
     try:
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-        rec = json.load(open(summ))
-        if rec.get("kernel_source_sha256") == sha:
-            return float(rec["dram_bytes_per_launch"])
+        rec = json.load(open(os.path.join(ROOT, "profiles", record)))
+        for f, want in rec["kernel_sources"].items():
+            src = os.path.join(ROOT, "rank_adapter_apply_gb300", "csrc", f)
+            if hashlib.sha256(open(src, "rb").read()).hexdigest() != want:
+                return None
+        return float(rec["dram_bytes_per_launch"])
     except Exception:
-        pass
-    return None
+        return None
 
 
 def algorithmic_bytes(idx: np.ndarray, ranks, layers, e=2) -> int:
@@ -433,7 +432,7 @@ def run_big(args, ctx, name, headline):
                       "[prefill_reduce], prefill_expand, decode shrink + expand; every layer of the set)",
             "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "peak_kind": kind,
             "frac_of_8TBps": ach / 8000.0,
-            "traffic": kernel_traffic(f"{name}_traffic.json", "prefill_tc.cu"),
+            "traffic": kernel_traffic(f"{name}_traffic.json"),
             "algorithmic_bytes_per_step": bytes_,
             "tflops": flops * n_steps / (ms * 1e-3) / 1e12}
     line = {"metric": METRIC, "value": job_tokens / (ms_job * 1e-3), "unit": UNIT, "n_gpus": world,
@@ -712,7 +711,7 @@ def run_decode(args, ctx, sub=False):
             "roofline": {**out["overlapped"]["roofline"],
                          "kernel": "decode_cluster_kernel (one launch per step: grouping, shrink and "
                                    "expand of q_proj and v_proj)",
-                         "traffic": kernel_traffic("decode_cluster_qv4096_traffic.json", "decode_cluster.cu"),
+                         "traffic": kernel_traffic("decode_cluster_qv4096_traffic.json"),
                          "copy_floor": floor, "algorithmic_bytes_per_step": bytes_ / n_steps},
             "e2e": e2e, "gpu_launches": out["overlapped"]["gpu_launches"], "clocks": clocks}
     if not sub and rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quick:

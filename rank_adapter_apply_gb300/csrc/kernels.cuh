@@ -29,7 +29,7 @@ enum HdrWord {
 constexpr int kFusedMaxTokens = 1024;   // batches up to this size take the cluster decode kernel
 
 struct WsLayout {
-    size_t hdr, perm, gx, tiles, ptiles, counters, v, part, total;
+    size_t hdr, perm, gx, tiles, ptiles, counters, v, part, dpart, total;
     size_t gx_ints;     // ints of the grouping kernel's exchange area
     int max_tiles, max_ptiles, part_rows, max_tokens, R, max_layers;
 };
@@ -98,6 +98,9 @@ inline WsLayout ws_layout(int S, int R, int max_tokens, int max_layers) {
     w.counters = take((size_t)max_layers * w.max_tiles * sizeof(int));
     w.v = take((size_t)max_layers * T * R * sizeof(float));
     w.part = take((size_t)max_layers * w.part_rows * R * sizeof(float));
+    // The decode kernels' own partials: they run beside the prefill kernels
+    // (which use `part`) on a second stream.
+    w.dpart = take((size_t)max_layers * w.part_rows * R * sizeof(float));
     w.total = o;
     return w;
 }

@@ -107,6 +107,10 @@ struct lora_ctx {
     int64_t n_host = 0, host_forgot = -1;
     cudaEvent_t h2d_done = nullptr, apply_done = nullptr;
     cudaStream_t down = nullptr;    // copies back of the host-buffer path (created on first use)
+    // The decode kernels of a grouped apply run on `side`, beside the prefill
+    // kernels on the compute stream: fork after the grouping, join at the end.
+    cudaStream_t side = nullptr;
+    cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
     // lora_assign_tokens: open-addressing table adapter id -> distinct index
     std::vector<uint64_t> tok_key;
     std::vector<int> tok_val, tok_rank;
@@ -343,6 +347,9 @@ int lora_slots_init(lora_ctx **out, int max_loras, int max_lora_rank, int max_to
     for (int s = 0; s < max_loras && e == cudaSuccess; ++s)
         e = cudaEventCreateWithFlags(&c->up_ev[s], cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->compute_done, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->fork_ev, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->join_ev, cudaEventDisableTiming);
     // Empty table: every slot rank 0; workspace zeroed (arrival counters start at 0).
     if (e == cudaSuccess) e = cudaMemsetAsync(rank_dev, 0, sizeof(int32_t) * max_loras, c->compute);
     if (e == cudaSuccess) e = cudaMemsetAsync(scale_dev, 0, sizeof(float) * max_loras, c->compute);
@@ -369,6 +376,10 @@ void lora_destroy(lora_ctx *c) {
         for (auto ev : c->ring)
             if (ev) cudaEventDestroy(ev);
         if (c->down) cudaStreamSynchronize(c->down);
+        if (c->side) cudaStreamSynchronize(c->side);
+        if (c->fork_ev) cudaEventDestroy(c->fork_ev);
+        if (c->join_ev) cudaEventDestroy(c->join_ev);
+        if (c->side) cudaStreamDestroy(c->side);
         for (auto ev : c->host_ev)
             if (ev) cudaEventDestroy(ev);
         if (c->h2d_done) cudaEventDestroy(c->h2d_done);
@@ -637,6 +648,13 @@ int apply_impl(lora_ctx *c, int n, const int *layers, const void *const *xs, voi
     CUDA_TRY(launch_group_tokens(idx, T, c->rank_dev, c->S, prefill ? c->prefill_min : 0, c->ws, c->lay,
                                  c->num_sms, c->compute));
     ++c->launches;
+    // The decode kernels read only the grouping's lists and write other rows
+    // of y and their own partials: they run on the side stream while the
+    // prefill kernels run on the compute stream, which waits for both at the
+    // end. (Under stream capture the side stream joins the capture through
+    // the event and leaves it through the join.)
+    CUDA_TRY(cudaEventRecord(c->fork_ev, c->compute));
+    CUDA_TRY(cudaStreamWaitEvent(c->side, c->fork_ev, 0));
     if (prefill) {
         // upper bound on prefill tiles: T/128 full tiles plus one ragged tile per run
         int grid_tiles = T / kPrefillRows + T / c->prefill_min + 2;
@@ -675,7 +693,7 @@ int apply_impl(lora_ctx *c, int n, const int *layers, const void *const *xs, voi
         a.d_in = L.d_in;
         a.d_out = L.d_out;
         a.v = reinterpret_cast<float *>(c->ws + c->lay.v) + (size_t)i * c->lay.max_tokens * c->R;
-        a.part = reinterpret_cast<float *>(c->ws + c->lay.part) + (size_t)i * c->lay.part_rows * c->R;
+        a.part = reinterpret_cast<float *>(c->ws + c->lay.dpart) + (size_t)i * c->lay.part_rows * c->R;
         a.counters = reinterpret_cast<int *>(c->ws + c->lay.counters) + (size_t)i * c->lay.max_tiles;
         // Split d_in into chunks of ~256 columns so that a tile's shrink is
         // spread over many CTAs (the host cannot tell how many decode tiles a
@@ -709,8 +727,10 @@ int apply_impl(lora_ctx *c, int n, const int *layers, const void *const *xs, voi
     gv.R = c->R;
     gv.T = T;
     int grid_tiles = est_tiles < c->lay.max_tiles ? est_tiles : c->lay.max_tiles;
-    CUDA_TRY(launch_decode(ma, gv, c->dtype, grid_tiles, max_chunks, max_dblocks, c->num_sms, c->compute));
+    CUDA_TRY(launch_decode(ma, gv, c->dtype, grid_tiles, max_chunks, max_dblocks, c->num_sms, c->side));
     if (grid_tiles > 0) c->launches += 2;          // shrink and expand
+    CUDA_TRY(cudaEventRecord(c->join_ev, c->side));
+    CUDA_TRY(cudaStreamWaitEvent(c->compute, c->join_ev, 0));
     if (!capturing(c->compute)) CUDA_TRY(note_apply(c));
     return LORA_OK;
 }
