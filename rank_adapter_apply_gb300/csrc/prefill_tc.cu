@@ -113,6 +113,7 @@ struct ShrinkJob {
 
 struct ShrinkArgs {
     CUtensorMap mx[kMaxLayersPerCall];        // per group: x [T][d_in], box 64 x 128
+    CUtensorMap mx32[kMaxLayersPerCall];      // the same x, box 64 x 32 (ragged tiles)
     CUtensorMap ma[kMaxLayersPerCall];        // per member (group order): A pool [S*R][d_in], box 64 x R
     float *part[kMaxLayersPerCall];           // per member
     int g_first[kMaxLayersPerCall], g_count[kMaxLayersPerCall];
@@ -201,6 +202,7 @@ prefill_shrink_kernel(const __grid_constant__ ShrinkArgs a) {
         error = 0;
         fence_mbar_init();
         tc::prefetch_tensormap(&a.mx[g]);
+        tc::prefetch_tensormap(&a.mx32[g]);
         for (int l = 0; l < nl; ++l) tc::prefetch_tensormap(&a.ma[m0 + l]);
     }
     if (warp == 1) {
@@ -217,14 +219,21 @@ prefill_shrink_kernel(const __grid_constant__ ShrinkArgs a) {
     if (warp == 0) {
         if (lane == 0) {
             // ---------------- producer ----------------
+            // A ragged tile (the last of a run) reads only the 32-row boxes
+            // that hold its rows; the MMA rows past them are never stored.
+            const int nx = rows >= kPrefillRows ? 0 : (rows + 31) >> 5;
+            const uint32_t xbytes = nx ? (uint32_t)nx * 4096u : (uint32_t)kTileBytes;
             int issued = 0;
             for (int j = 0; j < nkb; ++j) {
                 const int st = j % stages;
                 if (!wait_ok(&empty[st], ((uint32_t)(j / stages) & 1u) ^ 1u, err)) break;
                 uint8_t *tile = base + (size_t)st * stage_bytes;
                 const int col = (job.kb0 + j) * 64;
-                mbar_arrive_expect_tx(&full[st], stage_bytes);
-                tc::tma_load_2d(tile, &a.mx[g], col, row0, &full[st]);
+                mbar_arrive_expect_tx(&full[st], stage_bytes - kTileBytes + xbytes);
+                if (nx)
+                    for (int q = 0; q < nx; ++q) tc::tma_load_2d(tile + q * 4096, &a.mx32[g], col, row0 + 32 * q, &full[st]);
+                else
+                    tc::tma_load_2d(tile, &a.mx[g], col, row0, &full[st]);
                 for (int l = 0; l < nl; ++l)
                     tc::tma_load_2d(tile + kTileBytes + l * R * 128, &a.ma[m0 + l], col, s * R, &full[st]);
                 issued = j + 1;
@@ -393,14 +402,25 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
                 const Item it = item_at(a, k, np);
                 const int4 pt = a.ptiles[it.p];
                 const int nb = n_blocks(a, it), d_out = a.d_out[it.l];
+                // a ragged tile reads only the 32-row boxes of y that hold its rows
+                const int ny = pt.z >= kPrefillRows ? 0 : (pt.z + 31) >> 5;
+                const uint32_t ybytes = ny ? 2u * (uint32_t)ny * 4096u : 2u * (uint32_t)kTileBytes;
                 for (int b = 0; b < nb; ++b) {
                     const int st = j % stages;
                     if (!wait_ok(&empty[st], ((uint32_t)(j / stages) & 1u) ^ 1u, err)) break;
                     uint8_t *tile = ring + (size_t)st * kStage;
                     const int col = it.cb * kColBlock + b * kNB;
-                    mbar_arrive_expect_tx(&full[st], kStage);
-                    tc::tma_load_2d(tile, &a.my[it.l], col, pt.y, &full[st]);
-                    tc::tma_load_2d(tile + kTileBytes, &a.my[it.l], col + 64, pt.y, &full[st]);
+                    mbar_arrive_expect_tx(&full[st], kStage - 2u * kTileBytes + ybytes);
+                    if (ny) {
+                        for (int q = 0; q < ny; ++q) {
+                            tc::tma_load_2d(tile + q * 4096, &a.ms[it.l], col, pt.y + 32 * q, &full[st]);
+                            tc::tma_load_2d(tile + kTileBytes + q * 4096, &a.ms[it.l], col + 64, pt.y + 32 * q,
+                                            &full[st]);
+                        }
+                    } else {
+                        tc::tma_load_2d(tile, &a.my[it.l], col, pt.y, &full[st]);
+                        tc::tma_load_2d(tile + kTileBytes, &a.my[it.l], col + 64, pt.y, &full[st]);
+                    }
                     tc::tma_load_2d(tile + 2 * kTileBytes, &a.mb[it.l], 0, pt.x * d_out + col, &full[st]);
                     ++j;
                 }
@@ -718,7 +738,8 @@ cudaError_t launch_prefill_tc(const PrefillLayer *L, int n, int T, int S, int R,
         sa.g_first[g] = m;
         sa.g_count[g] = gcount[g];
         const PrefillLayer &x = L[glead[g]];
-        if (!encode_2d(&sa.mx[g], x.x, (uint64_t)x.d_in, (uint64_t)T, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+        if (!encode_2d(&sa.mx[g], x.x, (uint64_t)x.d_in, (uint64_t)T, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_2d(&sa.mx32[g], x.x, (uint64_t)x.d_in, (uint64_t)T, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
         for (int i = 0; i < n; ++i) {
             if (grp[i] != g) continue;
