@@ -388,3 +388,30 @@ def lora_register_host_adapters(ctx, ids, ranks, alphas, A_ptrs=None, B_ptrs=Non
 def lora_set_warm_set(ctx, ids):
     n = len(ids)
     return check(load().lora_set_warm_set(ctx, n, (ctypes.c_uint64 * n)(*[int(i) for i in ids])))
+
+
+def lora_serve_step(ctx, adapter_ids, layers=(), x_ptrs=(), y_ptrs=(), idx_bufs=0, max_groups=0):
+    """One serving step (lora_serve_step). adapter_ids: one adapter id per token
+    (NO_ID for base-model tokens); layers / x_ptrs / y_ptrs: the layer indices
+    and device pointers of the call; idx_bufs: address of max_groups x
+    n_tokens int32 that the host writes and the GPU reads (pinned memory).
+    Returns (decisions, n_groups), decisions = per distinct adapter in order
+    (id, slot, uploaded, evicted id or -1)."""
+    import numpy as np
+    ids = np.ascontiguousarray(adapter_ids, dtype=np.uint64)
+    T = int(ids.shape[0])
+    n = len(layers)
+    md = max(1, T)
+    o_ids = (ctypes.c_uint64 * md)()
+    o_sl = (ctypes.c_int * md)()
+    o_nd = (ctypes.c_int * md)()
+    o_ev = (ctypes.c_uint64 * md)()
+    nd, ng = ctypes.c_int(0), ctypes.c_int(0)
+    check(load().lora_serve_step(
+        ctx, T, ids.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)), n,
+        _i32_array(list(layers)) if n else None, _vp_array(x_ptrs) if n else None,
+        _vp_array(y_ptrs) if n else None, idx_bufs or None, int(max_groups), md, o_ids, o_sl, o_nd, o_ev,
+        ctypes.byref(nd), ctypes.byref(ng)))
+    dec = [(int(o_ids[i]), int(o_sl[i]), int(o_nd[i]), -1 if o_ev[i] == NO_ID else int(o_ev[i]))
+           for i in range(nd.value)]
+    return dec, ng.value

@@ -568,3 +568,106 @@ def test_random_decisions_with_aborted_loads_match_simulator(lib):
         assert sim.aborted > 10
     finally:
         B.lora_destroy(ctx)
+
+
+def _serve(ctx, ids, max_distinct=None):
+    """lora_serve_step on a host-only context: (status, decisions, n_groups)."""
+    import ctypes
+    lib = B.load()
+    T = len(ids)
+    md = T if max_distinct is None else max_distinct
+    arr = (ctypes.c_uint64 * max(1, T))(*[int(a) for a in ids])
+    o_ids = (ctypes.c_uint64 * max(1, md))()
+    o_sl = (ctypes.c_int * max(1, md))()
+    o_nd = (ctypes.c_int * max(1, md))()
+    o_ev = (ctypes.c_uint64 * max(1, md))()
+    nd, ng = ctypes.c_int(0), ctypes.c_int(0)
+    rc = lib.lora_serve_step(ctx, T, arr, 0, None, None, None, None, 0, md, o_ids, o_sl, o_nd, o_ev,
+                             ctypes.byref(nd), ctypes.byref(ng))
+    dec = [(int(o_ids[i]), int(o_sl[i]), int(o_nd[i]), -1 if o_ev[i] == B.NO_ID else int(o_ev[i]))
+           for i in range(nd.value)]
+    return rc, dec, ng.value
+
+
+def test_serve_step_groups_and_decisions_match_simulator(lib):
+    """A step with more distinct adapters than slots is cut into groups in
+    first-appearance order (a warm-set adapter resident in a pinned slot needs
+    no slot); each adapter's admission, in order, equals the simulator's; the
+    epoch advances once per step; base-model tokens are skipped."""
+    from oracle.lru_sim import LruSlotSim
+    from rank_adapter_apply_gb300 import churn
+    S, R = 4, 16
+    ctx = _host_ctx(S, R)
+    sim = LruSlotSim(S, R)
+    try:
+        B.lora_register_host_adapters(ctx, list(range(20)), [8] * 20, [16.0] * 20)
+        B.lora_set_warm_set(ctx, [0])
+        pinned = {}
+        steps = [[0, 1, 2, B.NO_ID, 1, 3], [4, 5, 0, 6, 7, 8, 5, 9, 10], [0, 11, 12, 13, 14, 15, 16, 17, 0]]
+        for k, ids in enumerate(steps):
+            rc, dec, ng = _serve(ctx, ids)
+            assert rc == 0, B.last_error()
+            order = list(dict.fromkeys(a for a in ids if a != B.NO_ID))
+            groups = churn.plan_groups(order, pinned, S - len(pinned))
+            exp = []
+            for group in groups:
+                held = []
+                for a in group:
+                    st, slot, need, ev = sim.assign(a, 8)
+                    assert st == 0
+                    exp.append((a, slot, need, ev))
+                    if a == 0 and a not in pinned:
+                        sim.pin(slot)
+                        pinned[a] = slot
+                    sim.acquire(slot)
+                    held.append(slot)
+                for s_ in held:
+                    sim.release(s_)
+            sim.tick()
+            assert dec == exp and ng == len(groups), (k, dec, exp)
+        st = B.lora_stats(ctx)
+        assert (st["hits"], st["misses"], st["evictions"], st["epoch"]) == (sim.hits, sim.misses, sim.evictions, 3)
+        assert st["uploads"] == sim.misses                  # host-only: uploads are recorded
+    finally:
+        B.lora_destroy(ctx)
+
+
+def test_serve_step_rejects_before_any_admission(lib):
+    """An unregistered adapter id, more adapters than max_distinct, a bad
+    registration: the call fails and the table is unchanged."""
+    ctx = _host_ctx(4, 16)
+    try:
+        with pytest.raises(B.LoraError) as ei:                       # rank above max_lora_rank
+            B.lora_register_host_adapters(ctx, [1, 2], [8, 32], [16.0, 16.0])
+        assert ei.value.code == B.LORA_ERR_RANK
+        with pytest.raises(B.LoraError):                             # an id twice
+            B.lora_register_host_adapters(ctx, [1, 1], [8, 8], [16.0, 16.0])
+        B.lora_register_host_adapters(ctx, [1, 2, 3], [8, 8, 8], [16.0, 16.0, 16.0])
+        rc, dec, ng = _serve(ctx, [1, 7, 2])                          # 7 was never registered
+        assert rc == B.LORA_ERR_ARG and "not registered" in B.last_error()
+        rc, dec, ng = _serve(ctx, [1, 2, 3], max_distinct=2)
+        assert rc == B.LORA_ERR_ARG
+        st = B.lora_stats(ctx)
+        assert (st["hits"], st["misses"], st["epoch"]) == (0, 0, 0)
+        rc, dec, ng = _serve(ctx, [])                                 # an empty step only ticks
+        assert rc == 0 and dec == [] and ng == 0 and B.lora_stats(ctx)["epoch"] == 1
+    finally:
+        B.lora_destroy(ctx)
+
+
+def test_serve_step_no_slot_releases_its_group(lib):
+    """Every slot in flight elsewhere: the first admission of the step fails
+    with NO_SLOT, the step's own references are released, the epoch stays."""
+    ctx = _host_ctx(2, 16)
+    try:
+        B.lora_register_host_adapters(ctx, [1, 2, 3], [8, 8, 8], [16.0] * 3)
+        for a in (1, 2):
+            st, slot, need, ev = B.lora_assign(ctx, a, 8)
+            B.lora_acquire(ctx, slot)                                 # held by another request
+        rc, dec, ng = _serve(ctx, [1, 3])
+        assert rc == B.LORA_ERR_NO_SLOT
+        assert B.lora_release(ctx, 0) == 0 and B.lora_release(ctx, 1) == 0
+        assert B.lora_release(ctx, 0) == B.LORA_ERR_STATE            # no reference left behind
+        assert B.lora_stats(ctx)["epoch"] == 0
+    finally:
+        B.lora_destroy(ctx)

@@ -71,6 +71,7 @@ CHECKS = [
     lambda lib: abi.test_assign_tokens_matches_simulator_and_maps_tokens(lib),
     lambda lib: abi.test_failed_load_leaves_the_table_consistent(lib),
     lambda lib: abi.test_late_release_after_abort_matches_simulator(lib),
+    lambda lib: abi.test_serve_step_groups_and_decisions_match_simulator(lib),
     lambda lib: abi.test_random_decisions_with_aborted_loads_match_simulator(lib),
 ]
 
