@@ -120,7 +120,7 @@ struct ShrinkArgs {
     ShrinkJob jobs[kMaxJobs];
     const int4 *ptiles;
     int *hdr;
-    int T, stages, tmem_cols;
+    int T, ring_bytes, tmem_cols;             // ring_bytes: this launch's shared ring (every group fits two stages)
 };
 
 // Sum of the d_in chunks of V, in chunk order, left in chunk 0: one CTA per
@@ -189,8 +189,11 @@ prefill_shrink_kernel(const __grid_constant__ ShrinkArgs a) {
     const int s = pt.x, row0 = pt.y, rows = pt.z;
     const ShrinkJob job = a.jobs[blockIdx.y];
     const int g = job.group, nl = a.g_count[g], m0 = a.g_first[g];
-    const int stages = a.stages;
     const uint32_t stage_bytes = kTileBytes + (uint32_t)nl * R * 128;
+    // As many stages as this group's stage size fits in the ring (a group with
+    // fewer layers has smaller stages and keeps more loads in flight).
+    int stages = (int)((uint32_t)a.ring_bytes / stage_bytes);
+    stages = stages > kMaxStages ? kMaxStages : stages;
 
     if (tid == 0) {
         for (int i = 0; i < stages; ++i) {
@@ -792,11 +795,11 @@ cudaError_t launch_prefill_tc(const PrefillLayer *L, int n, int T, int S, int R,
             ++jb;
         }
     }
-    // One ring depth for the launch: the deepest that the largest stage fits.
-    sa.stages = (int)(kShrinkRingBudget / max_stage);
-    if (sa.stages > kMaxStages) sa.stages = kMaxStages;
-    if (sa.stages < 2) return cudaErrorInvalidValue;
-    const size_t shrink_smem = 1024 + (size_t)sa.stages * max_stage;
+    // One ring for the launch; each CTA cuts it into as many stages of its
+    // group's size as fit (at least two for the largest stage).
+    if (kShrinkRingBudget / max_stage < 2) return cudaErrorInvalidValue;
+    sa.ring_bytes = (int)kShrinkRingBudget;
+    const size_t shrink_smem = 1024 + kShrinkRingBudget;
     int max_cols = 0;
     for (int g = 0; g < ng; ++g)
         if (gcount[g] * R > max_cols) max_cols = gcount[g] * R;
