@@ -112,7 +112,7 @@ size_t lora_workspace_bytes(int max_loras, int max_lora_rank, int max_tokens,
  * that the library writes on every upload or eviction. workspace: device,
  * lora_workspace_bytes(...) bytes, 256-byte aligned; it is zeroed here (on the
  * compute stream). compute_stream / upload_stream: caller-owned cudaStream_t.
- * max_tokens: at most 16,384 x the GPU's SM count (2,490,368 tokens on a
+ * max_tokens: at most 4,096 x the GPU's SM count (622,592 tokens on a
  * 152-SM GB300), else LORA_ERR_ARG.
  *
  * n_layers == 0 creates a host-only slot table: no CUDA call is made, and only

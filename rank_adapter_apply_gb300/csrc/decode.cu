@@ -161,50 +161,66 @@ __device__ __forceinline__ void shrink_bf16_tile(const LayerArgs &L, const Group
 }
 
 // ---------------------------------------------------------------------------
-// bf16 expand-add. CTA = (256-column block of d_out, tile, layer); each warp
-// owns 64 columns (two 32-column groups). Per group: 4 MMAs with M = 16 tokens,
-// N = 8 columns, K = 16 ranks, columns permuted so that each lane ends with 8
-// consecutive outputs of two token rows (one 128-bit y access per row).
+// bf16 expand-add. CTA = (256-column block of d_out, slot, layer): the block's
+// B rows of the slot cross HBM once and serve every tile of that slot (the
+// tiles of one slot are consecutive in the tile list). Each warp owns 64
+// columns (two 32-column groups). Per group and tile: 4 MMAs with M = 16
+// tokens, N = 8 columns, K = 16 ranks, columns permuted so that each lane ends
+// with 8 consecutive outputs of two token rows (one 128-bit y access per row).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int bkey(int P) { return (((P >> 3) & 3) << 1) | (P & 1); }
 
-__device__ __forceinline__ void expand_bf16_tile(const LayerArgs &L, const GroupView &g, int dblock, int tile_i) {
+__device__ __forceinline__ void expand_bf16_run(const LayerArgs &L, const GroupView &g, int dblock, int t0,
+                                                int n_tiles) {
     const int d_out = L.d_out;
-    const int4 tile = g.tiles[tile_i];
-    const int s = tile.x, p0 = tile.y, cnt = tile.z;
-    const int r = tile.w;                      // the slot's rank, from the grouping
+    const int4 head = g.tiles[t0];
+    const int s = head.x;
+    const int r = head.w;                      // the slot's rank, from the grouping
     const int nkb = (r + 15) >> 4;
     const float scale = g.scale[s];
     const int R = g.R;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
 
-    const int tok0 = gq < cnt ? g.perm[p0 + gq] : -1;
-    const int tok1 = gq + 8 < cnt ? g.perm[p0 + 8 + gq] : -1;
-
     // This block's B rows (the slot's first 16 * nkb ranks) go to shared memory
     // in one burst of 16-byte cp.async: row P of the block at bs + 64 P, chunk
     // c of the row at chunk c ^ key(P). One fragment read touches rows
     // P0 + 8a + b (a < 4, b < 2), so the key takes bits 3..4 and 0 of P and
-    // those eight rows land in distinct bank groups.
+    // those eight rows land in distinct bank groups. Thread i copies chunk
+    // i % 8 of rows i / 8, i / 8 + 16, ...
     __shared__ __align__(16) uint16_t bs[kExpandCols * 64];
     const uint16_t *Bs = static_cast<const uint16_t *>(L.B) + (size_t)s * d_out * R;
     const int c0 = dblock * kExpandCols;
     {
-        const int cpr = 2 * nkb;
-        for (int i = threadIdx.x; i < kExpandCols * cpr; i += kThreads) {
-            const int P = i / cpr, ch = i - P * cpr;
-            if (c0 + P < d_out) cp_async16(bs + P * 64 + ((ch ^ bkey(P)) << 3), Bs + (size_t)(c0 + P) * R + ch * 8);
+        const int ch = threadIdx.x & 7;
+        if (ch < 2 * nkb) {
+            const int rows = min(kExpandCols, d_out - c0);
+            for (int P = threadIdx.x >> 3; P < rows; P += kThreads / 8)
+                cp_async16(bs + P * 64 + ((ch ^ bkey(P)) << 3), Bs + (size_t)(c0 + P) * R + ch * 8);
         }
         cp_async_commit();
     }
 
-    // A fragments of V (rows = tokens gq, gq+8; k = 4tq..4tq+3 of each 16-rank block).
-    uint32_t ahi[4][4], alo[4][4];
+    uint16_t *y = static_cast<uint16_t *>(L.y);
+    const int vec = L.vec;
+    bool staged = false;
+    for (int t = t0; t < n_tiles; ++t) {
+        int4 tile = head;
+        if (t != t0) {
+            tile = g.tiles[t];
+            if (tile.x != s) break;              // the next slot's tiles
+        }
+        const int p0 = tile.y, cnt = tile.z;
+        const int tok0 = gq < cnt ? g.perm[p0 + gq] : -1;
+        const int tok1 = gq + 8 < cnt ? g.perm[p0 + 8 + gq] : -1;
+
+        // A fragments of V (rows = tokens gq, gq+8; k = 4tq..4tq+3 of each
+        // 16-rank block), split into bf16 high and low parts.
+        uint32_t ahi[4][4], alo[4][4];
 #pragma unroll
-    for (int kb = 0; kb < 4; ++kb) {
-        float f0[4] = {0.f, 0.f, 0.f, 0.f}, f1[4] = {0.f, 0.f, 0.f, 0.f};
-        const int kq = kb * 16 + 4 * tq;                 // ranks kq .. kq + 3, one 16-byte load per row
-        if (kb < nkb) {
+        for (int kb = 0; kb < 4; ++kb) {
+            if (kb >= nkb) break;
+            float f0[4] = {0.f, 0.f, 0.f, 0.f}, f1[4] = {0.f, 0.f, 0.f, 0.f};
+            const int kq = kb * 16 + 4 * tq;             // ranks kq .. kq + 3, one 16-byte load per row
             if (gq < cnt) {
                 const float4 q = *reinterpret_cast<const float4 *>(L.v + (size_t)(p0 + gq) * R + kq);
                 f0[0] = q.x; f0[1] = q.y; f0[2] = q.z; f0[3] = q.w;
@@ -216,108 +232,109 @@ __device__ __forceinline__ void expand_bf16_tile(const LayerArgs &L, const Group
 #pragma unroll
             for (int i = 0; i < 4; ++i)
                 if (kq + i >= r) f0[i] = f1[i] = 0.f;
+            float h0[4], h1[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                h0[i] = __bfloat162float(__float2bfloat16_rn(f0[i]));
+                h1[i] = __bfloat162float(__float2bfloat16_rn(f1[i]));
+            }
+            ahi[kb][0] = pack_bf16(h0[0], h0[1]);
+            ahi[kb][1] = pack_bf16(h1[0], h1[1]);
+            ahi[kb][2] = pack_bf16(h0[2], h0[3]);
+            ahi[kb][3] = pack_bf16(h1[2], h1[3]);
+            alo[kb][0] = pack_bf16(f0[0] - h0[0], f0[1] - h0[1]);
+            alo[kb][1] = pack_bf16(f1[0] - h1[0], f1[1] - h1[1]);
+            alo[kb][2] = pack_bf16(f0[2] - h0[2], f0[3] - h0[3]);
+            alo[kb][3] = pack_bf16(f1[2] - h1[2], f1[3] - h1[3]);
         }
-        float h0[4], h1[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            h0[i] = __bfloat162float(__float2bfloat16_rn(f0[i]));
-            h1[i] = __bfloat162float(__float2bfloat16_rn(f1[i]));
-        }
-        ahi[kb][0] = pack_bf16(h0[0], h0[1]);
-        ahi[kb][1] = pack_bf16(h1[0], h1[1]);
-        ahi[kb][2] = pack_bf16(h0[2], h0[3]);
-        ahi[kb][3] = pack_bf16(h1[2], h1[3]);
-        alo[kb][0] = pack_bf16(f0[0] - h0[0], f0[1] - h0[1]);
-        alo[kb][1] = pack_bf16(f1[0] - h1[0], f1[1] - h1[1]);
-        alo[kb][2] = pack_bf16(f0[2] - h0[2], f0[3] - h0[3]);
-        alo[kb][3] = pack_bf16(f1[2] - h1[2], f1[3] - h1[3]);
-    }
 
-    uint16_t *y = static_cast<uint16_t *>(L.y);
-    const int vec = L.vec;
-
-    // y of both column groups and both token rows, fetched before the MMAs so
-    // that their latency overlaps the B loads.
-    uint4 ypre[2][2];
+        // y of both column groups and both token rows, fetched before the
+        // MMAs so that their latency overlaps the B loads.
+        uint4 ypre[2][2];
 #pragma unroll
-    for (int grp = 0; grp < 2; ++grp) {
-        const int cc = dblock * kExpandCols + warp * 64 + grp * 32 + 8 * tq;
+        for (int grp = 0; grp < 2; ++grp) {
+            const int cc = c0 + warp * 64 + grp * 32 + 8 * tq;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int tok = h ? tok1 : tok0;
-            ypre[grp][h] = (vec && tok >= 0 && cc + 8 <= d_out)
-                               ? *reinterpret_cast<const uint4 *>(y + (size_t)tok * d_out + cc)
-                               : make_uint4(0, 0, 0, 0);
-        }
-    }
-
-    cp_async_wait_all();                 // this thread's B chunks have landed
-    __syncthreads();                     // and every other thread's
-
-#pragma unroll
-    for (int grp = 0; grp < 2; ++grp) {
-        const int c = dblock * kExpandCols + warp * 64 + grp * 32;
-        if (c >= d_out) break;
-        // Every B fragment of the group first, then per 16-rank block the
-        // high-part MMAs of the four column blocks and after them the low-part
-        // ones: each accumulator adds in the order of a one-block-at-a-time
-        // loop, while four independent MMAs go out back to back.
-        // (ranks >= r are zero in the pool and in v, so no mask is needed)
-        uint2 bb[4][4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int P = c + 8 * (gq >> 1) + 2 * j + (gq & 1);
-#pragma unroll
-            for (int kb = 0; kb < 4; ++kb) {
-                const int k = kb * 16 + 4 * tq;
-                bb[j][kb] = make_uint2(0, 0);
-                if (kb < nkb && P < d_out) {
-                    const int Pl = P - c0;
-                    bb[j][kb] = *reinterpret_cast<const uint2 *>(bs + Pl * 64 + (((k >> 3) ^ bkey(Pl)) << 3) + (k & 7));
-                }
+            for (int h = 0; h < 2; ++h) {
+                const int tok = h ? tok1 : tok0;
+                ypre[grp][h] = (vec && tok >= 0 && cc + 8 <= d_out)
+                                   ? *reinterpret_cast<const uint4 *>(y + (size_t)tok * d_out + cc)
+                                   : make_uint4(0, 0, 0, 0);
             }
         }
-        float acc[4][4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-#pragma unroll
-        for (int kb = 0; kb < 4; ++kb) {
-            if (kb >= nkb) break;
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                mma_bf16(acc[j], ahi[kb][0], ahi[kb][1], ahi[kb][2], ahi[kb][3], bb[j][kb].x, bb[j][kb].y);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                mma_bf16(acc[j], alo[kb][0], alo[kb][1], alo[kb][2], alo[kb][3], bb[j][kb].x, bb[j][kb].y);
+
+        if (!staged) {                           // (the same for every thread of the CTA)
+            cp_async_wait_all();                 // this thread's B chunks have landed
+            __syncthreads();                     // and every other thread's
+            staged = true;
         }
-        // Lane owns columns c + 8tq .. c + 8tq + 7 of rows tok0 (acc[.][0..1]) and tok1 (acc[.][2..3]).
-        const int cc = c + 8 * tq;
+
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int tok = h ? tok1 : tok0;
-            if (tok < 0) continue;
-            uint16_t *row = y + (size_t)tok * d_out;
-            float dlt[8];
+        for (int grp = 0; grp < 2; ++grp) {
+            const int c = c0 + warp * 64 + grp * 32;
+            if (c >= d_out) break;
+            // Every B fragment of the group first, then per 16-rank block the
+            // high-part MMAs of the four column blocks and after them the
+            // low-part ones: each accumulator adds in the order of a
+            // one-block-at-a-time loop, while four independent MMAs go out
+            // back to back. (ranks >= r are zero in the pool and in v, so no
+            // mask is needed)
+            uint2 bb[4][4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                dlt[2 * j] = acc[j][2 * h];
-                dlt[2 * j + 1] = acc[j][2 * h + 1];
+                const int P = c + 8 * (gq >> 1) + 2 * j + (gq & 1);
+#pragma unroll
+                for (int kb = 0; kb < 4; ++kb) {
+                    const int k = kb * 16 + 4 * tq;
+                    bb[j][kb] = make_uint2(0, 0);
+                    if (kb < nkb && P < d_out) {
+                        const int Pl = P - c0;
+                        bb[j][kb] = *reinterpret_cast<const uint2 *>(bs + Pl * 64 + (((k >> 3) ^ bkey(Pl)) << 3) + (k & 7));
+                    }
+                }
             }
-            if (vec && cc + 8 <= d_out) {
-                const uint4 yv = ypre[grp][h];
-                uint32_t w[4] = {yv.x, yv.y, yv.z, yv.w};
+            float acc[4][4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    w[q] = pack_bf16(fmaf(scale, dlt[2 * q], bf_lo(w[q])),
-                                     fmaf(scale, dlt[2 * q + 1], bf_hi(w[q])));
-                *reinterpret_cast<uint4 *>(row + cc) = make_uint4(w[0], w[1], w[2], w[3]);
-            } else {
+            for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    if (cc + i < d_out) {
-                        float yo = __uint_as_float((uint32_t)row[cc + i] << 16);
-                        __nv_bfloat16 o = __float2bfloat16_rn(fmaf(scale, dlt[i], yo));
-                        row[cc + i] = *reinterpret_cast<uint16_t *>(&o);
+            for (int kb = 0; kb < 4; ++kb) {
+                if (kb >= nkb) break;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    mma_bf16(acc[j], ahi[kb][0], ahi[kb][1], ahi[kb][2], ahi[kb][3], bb[j][kb].x, bb[j][kb].y);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    mma_bf16(acc[j], alo[kb][0], alo[kb][1], alo[kb][2], alo[kb][3], bb[j][kb].x, bb[j][kb].y);
+            }
+            // Lane owns columns c + 8tq .. c + 8tq + 7 of rows tok0 (acc[.][0..1]) and tok1 (acc[.][2..3]).
+            const int cc = c + 8 * tq;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int tok = h ? tok1 : tok0;
+                if (tok < 0) continue;
+                uint16_t *row = y + (size_t)tok * d_out;
+                float dlt[8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    dlt[2 * j] = acc[j][2 * h];
+                    dlt[2 * j + 1] = acc[j][2 * h + 1];
+                }
+                if (vec && cc + 8 <= d_out) {
+                    const uint4 yv = ypre[grp][h];
+                    uint32_t w[4] = {yv.x, yv.y, yv.z, yv.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        w[q] = pack_bf16(fmaf(scale, dlt[2 * q], bf_lo(w[q])),
+                                         fmaf(scale, dlt[2 * q + 1], bf_hi(w[q])));
+                    *reinterpret_cast<uint4 *>(row + cc) = make_uint4(w[0], w[1], w[2], w[3]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        if (cc + i < d_out) {
+                            float yo = __uint_as_float((uint32_t)row[cc + i] << 16);
+                            __nv_bfloat16 o = __float2bfloat16_rn(fmaf(scale, dlt[i], yo));
+                            row[cc + i] = *reinterpret_cast<uint16_t *>(&o);
+                        }
                     }
                 }
             }
@@ -401,17 +418,20 @@ shrink_bf16_kernel(MultiArgs ma, GroupView g, int max_chunks) {
     }
 }
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
 expand_bf16_kernel(MultiArgs ma, GroupView g, int max_dblocks) {
     grid_dependency_wait();            // launched early: the kernel before has to finish first
     grid_launch_dependents();
     const int per_tile = max_dblocks * ma.n;
-    const int items = g.hdr[kHdrTiles] * per_tile;
+    const int n_tiles = g.hdr[kHdrTiles];
+    const int items = n_tiles * per_tile;
     for (int w = blockIdx.x; w < items; w += gridDim.x) {
         const int db = w % max_dblocks, l = (w / max_dblocks) % ma.n, t = w / per_tile;
         const LayerArgs &L = ma.l[l];
         if (db * kExpandCols >= L.d_out) continue;
-        expand_bf16_tile(L, g, db, t);
+        // Items of a slot's first tile cover all of that slot's tiles.
+        if (t > 0 && g.tiles[t - 1].x == g.tiles[t].x) continue;
+        expand_bf16_run(L, g, db, t, n_tiles);
         __syncthreads();                     // the staged B rows are free for the next item
     }
 }
