@@ -20,16 +20,22 @@
 // shuffles plus one exchange of warp totals through shared memory. Batches of
 // up to kGBlock tokens take one CTA; larger ones one CTA per block, which
 // exchange per-block figures (first and last run start, prefill tiles,
-// decode tokens per slot) through the workspace at two grid barriers. The grid never exceeds what fits on the
-// GPU at once, every barrier wait is bounded, and a wait that gives up sets
-// the error word and leaves the batch with no tiles at all (every row of y
-// unchanged). The position of a decode token inside its slot's list comes
-// from shared-memory atomics (one per stretch of same-slot tokens of a
-// thread), so the order of tokens of one slot is not fixed;
-// every token's result is computed from its own row only, so no output
-// depends on it.
+// decode tokens per slot) at two barriers. Up to kGCluster blocks form one
+// thread-block cluster: the figures go to CTA 0's shared memory and the
+// barriers are the cluster's hardware barriers (every CTA of a cluster is
+// resident at once and reaches each of them on every path). Larger batches
+// exchange through the workspace at two grid barriers; that grid never
+// exceeds what fits on the GPU at once, every barrier wait is bounded, and a
+// wait that gives up sets the error word and leaves the batch with no tiles
+// at all (every row of y unchanged). The position of a decode token inside
+// its slot's list comes from one shared-memory atomic per stretch of
+// same-slot tokens of a thread (which also counts them), so the order of
+// tokens of one slot is not fixed; every token's result is computed from its
+// own row only, so no output depends on it.
 #include "kernels.cuh"
 #include "device_util.cuh"
+
+#include <cooperative_groups.h>
 
 namespace lora {
 namespace {
@@ -41,7 +47,9 @@ constexpr int kGW = kGT / 32;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr uint32_t kBarrierLimit = 1u << 22;
 constexpr int kNoStart = 0x7fffffff;
+constexpr int kGCluster = 8;               // blocks that exchange through a cluster's shared memory
 static_assert(kMaxSlots <= kGT, "one thread per slot in the per-slot scans");
+static_assert(kPrefillRows == 128, "prefill tile count by shift");
 
 struct GroupArgs {
     const int32_t *idx;
@@ -55,8 +63,11 @@ struct GroupArgs {
 struct GroupSmem {
     int eff[kGBlock];               // effective slot of each token of the block (-1: none)
     int rank[kMaxSlots];
-    int cnt[kMaxSlots];             // decode tokens of this block per slot, then the fill counters
+    int cnt[kMaxSlots];             // decode tokens of this block per slot
     int base[kMaxSlots];            // where this block's decode tokens of each slot start in perm
+    int toff[kMaxSlots + 1];        // first decode tile of each slot; [S]: all decode tiles
+    int soff[kMaxSlots + 1];        // first place of each slot in perm; [S]: all decode tokens
+    int gx[kGCluster * (3 + kMaxSlots)];   // a cluster's exchange area (CTA 0's copy is used)
     int w0[3][kGW], w1[3][kGW];     // warp totals of the three scan passes
     int invalid;
     int prev_eff;                   // effective slot of the token before the block (-2: none)
@@ -135,11 +146,32 @@ __device__ bool grid_barrier(int *ctr, int k, int G) {
     return ok;
 }
 
+// The two exchanges between the blocks of a batch: with a cluster, the
+// cluster's barrier (release the figures written into CTA 0, acquire every
+// block's); otherwise the bounded grid barrier.
+template <bool kCl>
+__device__ __forceinline__ bool exchange(int *hdr, int k, int G) {
+    if constexpr (kCl) {
+        cluster_arrive_release();
+        cluster_wait_acquire();
+        return true;
+    } else {
+        return grid_barrier(hdr + kHdrGroupBar, k, G);
+    }
+}
+
+template <bool kCl>
 __global__ void __launch_bounds__(kGT, 1) group_tokens_kernel(const __grid_constant__ GroupArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     GroupSmem &sm = *reinterpret_cast<GroupSmem *>(smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int c = blockIdx.x, G = a.G, S = a.S, T = a.T;
+    // Exchange area: CTA 0's shared copy in a cluster, else the workspace's.
+    int *gx = a.gx;
+    if constexpr (kCl) {
+        cluster_arrive_relaxed();             // this CTA has started: peers may write into it
+        gx = cooperative_groups::this_cluster().map_shared_rank(sm.gx, 0);
+    }
     // Launched early (programmatic dependent launch): the slot ids and ranks
     // may come from the kernel before, and the previous apply's kernels still
     // read the lists rewritten here, so everything waits for it.
@@ -237,21 +269,22 @@ __global__ void __launch_bounds__(kGT, 1) group_tokens_kernel(const __grid_const
     }
     bool good = true;
     if (G > 1) {
+        if constexpr (kCl) cluster_wait_acquire();   // every CTA of the cluster has started
         if (tid == 0) {
-            a.gx[c] = blk_first == kNoStart ? kNoStart : b0 + blk_first;
-            a.gx[G + c] = sm.blk_last < 0 ? -1 : b0 + sm.blk_last;
+            gx[c] = blk_first == kNoStart ? kNoStart : b0 + blk_first;
+            gx[G + c] = sm.blk_last < 0 ? -1 : b0 + sm.blk_last;
         }
-        good = grid_barrier(a.hdr + kHdrGroupBar, 1, G);
+        good = exchange<kCl>(a.hdr, 1, G);
     }
     // The last start before the block and the first one after it (global
     // positions; block 0 starts a run at token 0).
     int before = 0, after = T;
     if (G > 1 && good) {
-        if (c > 0) before = max(0, gx_reduce<1>(a.gx + G, 1, c));
+        if (c > 0) before = max(0, gx_reduce<1>(gx + G, 1, c));
         for (int q0 = c + 1; q0 < G; q0 += 8) {     // the nearest later block with a start
             int v[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = q0 + i < G ? a.gx[q0 + i] : kNoStart;
+            for (int i = 0; i < 8; ++i) v[i] = q0 + i < G ? gx[q0 + i] : kNoStart;
             int f = kNoStart;
 #pragma unroll
             for (int i = 7; i >= 0; --i) f = v[i] != kNoStart ? v[i] : f;
@@ -267,19 +300,21 @@ __global__ void __launch_bounds__(kGT, 1) group_tokens_kernel(const __grid_const
     };
     // Runs starting in this thread's tokens: their prefill tiles, the class of
     // the last one (for the tokens of higher threads), 2 bits of class per start.
+    // (last start first: each run ends where the next one starts)
     int heads = 0, last_key = -1;
     uint32_t cls_bits = 0;
     {
-        unsigned m = smask;
-        while (m) {
-            const int j = __ffs(m) - 1;
-            m &= m - 1;
-            const int s0 = b0 + p0 + j;
-            const int end = m ? b0 + p0 + __ffs(m) - 1 : (hi_start != kNoStart ? b0 + hi_start : after);
-            const int cls = run_class(sm.eff[p0 + j], end - s0);
-            if (cls == 1) heads += (end - s0 + kPrefillRows - 1) / kPrefillRows;
-            cls_bits |= (uint32_t)cls << (2 * j);
-            last_key = (p0 + j + 1) * 4 + cls;
+        int end = hi_start != kNoStart ? b0 + hi_start : after;
+#pragma unroll
+        for (int j = kGPer - 1; j >= 0; --j) {
+            if ((smask >> j) & 1u) {
+                const int s0 = b0 + p0 + j;
+                const int cls = run_class(e[j], end - s0);
+                if (cls == 1) heads += (end - s0 + kPrefillRows - 1) >> 7;
+                cls_bits |= (uint32_t)cls << (2 * j);
+                if (last_key < 0) last_key = (p0 + j + 1) * 4 + cls;
+                end = s0;
+            }
         }
     }
     // One pass: the last run key of lower threads (max) and the prefill tiles
@@ -324,27 +359,35 @@ __global__ void __launch_bounds__(kGT, 1) group_tokens_kernel(const __grid_const
         if ((smask >> j) & 1u) cls_cur = (cls_bits >> (2 * j)) & 3u;
         if (p0 + j < n && e[j] >= 0 && cls_cur == 2) dec_mask |= 1u << j;
     }
-    // decode tokens per slot: one shared atomic per stretch of same-slot
-    // decode tokens among this thread's tokens
+    // Decode tokens per slot, and each token's place among this block's
+    // tokens of its slot: one shared atomic per stretch of same-slot decode
+    // tokens of this thread claims the whole stretch (its length from a
+    // backward pass).
+    int off[kGPer];
     {
-        int cs = -1, cl = 0;
+        int len[kGPer];
+        int n_len = 0, n_slot = -1;
+#pragma unroll
+        for (int j = kGPer - 1; j >= 0; --j) {
+            const int s = (dec_mask >> j) & 1u ? e[j] : -1;
+            n_len = (s >= 0 && s == n_slot) ? n_len + 1 : 1;
+            len[j] = n_len;
+            n_slot = s;
+        }
+        int ps = -1, o = 0;
 #pragma unroll
         for (int j = 0; j < kGPer; ++j) {
             const int s = (dec_mask >> j) & 1u ? e[j] : -1;
-            if (s != cs) {
-                if (cs >= 0) atomicAdd(&sm.cnt[cs], cl);
-                cs = s;
-                cl = 0;
-            }
-            cl += s >= 0;
+            if (s >= 0) o = s == ps ? o + 1 : atomicAdd(&sm.cnt[s], len[j]);
+            off[j] = o;
+            ps = s;
         }
-        if (cs >= 0) atomicAdd(&sm.cnt[cs], cl);
     }
     __syncthreads();
     if (G > 1) {
-        if (tid == 0) a.gx[2 * G + c] = n_heads_blk;
-        if (tid < S) a.gx[3 * G + c * S + tid] = sm.cnt[tid];
-        good = grid_barrier(a.hdr + kHdrGroupBar, 2, G) && good;
+        if (tid == 0) gx[2 * G + c] = n_heads_blk;
+        if (tid < S) gx[3 * G + c * S + tid] = sm.cnt[tid];
+        good = exchange<kCl>(a.hdr, 2, G) && good;
     }
     if (!good) {
         // A barrier gave up: this CTA writes no list (the header will hold no tiles).
@@ -356,16 +399,16 @@ __global__ void __launch_bounds__(kGT, 1) group_tokens_kernel(const __grid_const
     {
         int head0 = 0, n_ptiles = n_heads_blk;
         if (G > 1) {
-            head0 = gx_reduce<2>(a.gx + 2 * G, 1, G, c);
-            n_ptiles = gx_reduce<0>(a.gx + 2 * G, 1, G);
+            head0 = gx_reduce<2>(gx + 2 * G, 1, G, c);
+            n_ptiles = gx_reduce<0>(gx + 2 * G, 1, G);
         }
         // decode tokens per slot over the batch (thread = slot), and the
         // blocks' share before this one
         int tot = 0, mine_before = 0;
         if (tid < S) {
             if (G > 1) {
-                tot = gx_reduce<0>(a.gx + 3 * G + tid, S, G);
-                mine_before = gx_reduce<2>(a.gx + 3 * G + tid, S, G, c);
+                tot = gx_reduce<0>(gx + 3 * G + tid, S, G);
+                mine_before = gx_reduce<2>(gx + 3 * G + tid, S, G, c);
             } else {
                 tot = sm.cnt[tid];
             }
@@ -398,15 +441,28 @@ __global__ void __launch_bounds__(kGT, 1) group_tokens_kernel(const __grid_const
         }
         if (tid < S) {
             sm.base[tid] = slot_off + mine_before;
-            sm.cnt[tid] = 0;                        // from here the fill counter of this block
-            if (c == 0)
-                for (int i = 0; i < nt; ++i) {
-                    const int k = tot - i * kTileTokens;
-                    a.tiles[tile_off + i] = make_int4(tid, slot_off + i * kTileTokens,
-                                                      k < kTileTokens ? k : kTileTokens, sm.rank[tid]);
-                }
+            sm.toff[tid] = tile_off;
+            sm.soff[tid] = slot_off;
+        }
+        if (tid == 0) {
+            sm.toff[S] = n_tiles;
+            sm.soff[S] = n_dec;
         }
         __syncthreads();
+        // decode tiles, spread over every thread of the grid: tile i belongs
+        // to the slot s with toff[s] <= i < toff[s + 1]
+        for (int i = c * kGT + tid; i < n_tiles; i += G * kGT) {
+            int lo = 0, hi = S;
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (sm.toff[mid] <= i) lo = mid;
+                else hi = mid;
+            }
+            const int k = i - sm.toff[lo];
+            const int left = sm.soff[lo + 1] - sm.soff[lo] - k * kTileTokens;
+            a.tiles[i] = make_int4(lo, sm.soff[lo] + k * kTileTokens, left < kTileTokens ? left : kTileTokens,
+                                   sm.rank[lo]);
+        }
         // prefill tiles of the runs starting here, in token order
         int hp = head0 + head_pos;
         unsigned m = smask;
@@ -420,25 +476,10 @@ __global__ void __launch_bounds__(kGT, 1) group_tokens_kernel(const __grid_const
             for (int r = s0; r < end; r += kPrefillRows)
                 a.ptiles[hp++] = make_int4(slot, r, end - r < kPrefillRows ? end - r : kPrefillRows, 0);
         }
-        // decode tokens: each stretch of same-slot decode tokens of this
-        // thread claims a place in its slot's list with one shared atomic
-        {
-            int cs = -1, cl = 0, cj = 0;
+        // decode tokens at the places claimed above
 #pragma unroll
-            for (int j = 0; j <= kGPer; ++j) {
-                const int s = j < kGPer && ((dec_mask >> j) & 1u) ? e[j] : -1;
-                if (s != cs || j == kGPer) {
-                    if (cs >= 0) {
-                        const int at = sm.base[cs] + atomicAdd(&sm.cnt[cs], cl);
-                        for (int k = 0; k < cl; ++k) a.perm[at + k] = b0 + p0 + cj + k;
-                    }
-                    cs = s;
-                    cl = 0;
-                    cj = j;
-                }
-                cl += s >= 0;
-            }
-        }
+        for (int j = 0; j < kGPer; ++j)
+            if ((dec_mask >> j) & 1u) a.perm[sm.base[e[j]] + off[j]] = b0 + p0 + j;
         if (tid == 0) {
             sm.n_tiles = n_tiles;
             sm.n_ptiles = n_ptiles;
@@ -449,6 +490,13 @@ __global__ void __launch_bounds__(kGT, 1) group_tokens_kernel(const __grid_const
     // ---- the header: written by the last CTA to finish ---------------------
 header:
     __syncthreads();
+    if constexpr (kCl) {
+        // CTA 0 keeps its shared memory until every peer has read it
+        if (G > 1) {
+            cluster_arrive_release();
+            cluster_wait_acquire();
+        }
+    }
     if (tid == 0) {
         const int n_tiles = sm.n_tiles, n_ptiles = sm.n_ptiles, n_dec = sm.n_dec;
         if (sm.invalid) atomicAdd(a.hdr + kHdrInvalid, sm.invalid);
@@ -459,14 +507,14 @@ header:
         }
         // (the lists need no fence: the kernels that read them start after
         // this one has completed)
-        const int done = G > 1 ? atomicAdd(a.hdr + kHdrGroupDone, 1) : 0;
+        const int done = kCl ? (c == 0 ? G - 1 : -1) : (G > 1 ? atomicAdd(a.hdr + kHdrGroupDone, 1) : 0);
         if (done == G - 1) {
             const bool failed = sm.fail || (G > 1 && atomicAdd(a.hdr + kHdrGroupFail, 0) != 0);
             // A failed barrier leaves the lists incomplete: no tiles at all.
             a.hdr[kHdrTiles] = failed ? 0 : n_tiles;
             a.hdr[kHdrPrefillTiles] = failed ? 0 : n_ptiles;
             a.hdr[kHdrDecodeTokens] = failed ? 0 : n_dec;
-            if (G > 1) {
+            if (!kCl && G > 1) {
                 a.hdr[kHdrGroupBar] = 0;
                 a.hdr[kHdrGroupDone] = 0;
                 a.hdr[kHdrGroupFail] = 0;
@@ -489,8 +537,11 @@ cudaError_t launch_group_tokens(const int32_t *idx, int T, const int *rank_dev, 
     static std::atomic<uint64_t> attr_set{0};
     const size_t smem = sizeof(GroupSmem);
     if (!device_bit(attr_set)) {
-        cudaError_t e = cudaFuncSetAttribute(group_tokens_kernel,
+        cudaError_t e = cudaFuncSetAttribute(group_tokens_kernel<false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(group_tokens_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem);
         if (e != cudaSuccess) return e;
         set_device_bit(attr_set);
     }
@@ -509,7 +560,24 @@ cudaError_t launch_group_tokens(const int32_t *idx, int T, const int *rank_dev, 
     a.tiles = reinterpret_cast<int4 *>(ws + lay.tiles);
     a.ptiles = reinterpret_cast<int4 *>(ws + lay.ptiles);
     a.gx = reinterpret_cast<int *>(ws + lay.gx);
-    return launch_pdl(group_tokens_kernel, dim3(a.G), dim3(kGT), smem, st, a);
+    if (a.G == 1 || a.G > kGCluster)
+        return launch_pdl(group_tokens_kernel<false>, dim3(a.G), dim3(kGT), smem, st, a);
+    // 2..kGCluster blocks: one cluster of G CTAs
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(a.G);
+    cfg.blockDim = dim3(kGT);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = a.G;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, group_tokens_kernel<true>, a);
 }
 
 }  // namespace lora

@@ -610,17 +610,20 @@ def test_host_buffer_path_matches_oracle(device_sets, packed):
         sl.close()
 
 
-@pytest.mark.parametrize("prefill_min", [None, 0])
-def test_grouping_across_blocks(prefill_min):
-    """40,000 tokens: the grouping kernel splits the batch into three blocks of
-    one CTA each. Long runs that cross the block edges (tensor-core prefill
-    tiles, or decode tiles when the prefill path is off), short decode runs,
-    base-only tokens and out-of-range indices next to the edges; sampled tokens
-    (every edge among them) against the oracle, base-only and invalid rows bit
-    for bit, the invalid count exact."""
+@pytest.mark.parametrize("T,prefill_min", [(40000, None), (40000, 0), (18000, None), (18000, 0), (8193, None)])
+def test_grouping_across_blocks(T, prefill_min):
+    """The grouping kernel splits a batch into G = ceil(T / 4096) blocks of one
+    CTA each (block c from token T*c/G), exchanging per-block figures through a
+    cluster's shared memory for G <= 8 (8,193 and 18,000 tokens) and through
+    the workspace at grid barriers beyond (40,000 tokens). Long runs that cross
+    the block edges (tensor-core prefill tiles, or decode tiles when the
+    prefill path is off), short decode runs, base-only tokens and out-of-range
+    indices next to the edges; sampled tokens (every edge among them) against
+    the oracle, base-only and invalid rows bit for bit, the invalid count
+    exact."""
     rng = np.random.default_rng(40)
-    T = 40000
-    edges = [T // 3, 2 * T // 3]
+    G = (T + 4095) // 4096
+    edges = [T * c // G for c in range(1, G)]
     parts, n = [], 0
     while n < T:
         kind = rng.random()
