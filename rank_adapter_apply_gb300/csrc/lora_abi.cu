@@ -84,6 +84,7 @@ struct lora_ctx {
     cudaEvent_t compute_done = nullptr;
     bool compute_recorded = false;
     std::vector<UploadTiming> timing;
+    std::vector<UploadTiming> timing_free;   // timing events of harvested uploads, reused
     double upload_seconds = 0.0;
     uint64_t uploads = 0, upload_bytes = 0, invalid_seen = 0;
     uint64_t cluster_applies = 0, grouped_applies = 0;   // which path served each apply
@@ -123,6 +124,9 @@ struct lora_ctx {
     std::unordered_set<uint64_t> warm;
     std::vector<int> step_tok, step_group, step_slot, step_need;
     std::vector<uint64_t> step_id, step_ev;
+    std::vector<int> up_slots, up_ranks;     // uploads of one serving-step group
+    std::vector<float> up_alphas;
+    std::vector<const void *> up_A, up_B;
 
     lora_ctx(int S_, int R_) : table(S_, R_) {}
 };
@@ -216,11 +220,25 @@ int harvest_timings(lora_ctx *c, bool wait) {
         if (q != cudaSuccess) return fail(LORA_ERR_CUDA, "upload event: %s", cudaGetErrorString(q));
         float ms = 0.f;
         if (cudaEventElapsedTime(&ms, t.start, t.end) == cudaSuccess) c->upload_seconds += ms * 1e-3;
-        cudaEventDestroy(t.start);
-        cudaEventDestroy(t.end);
+        c->timing_free.push_back(t);
     }
     c->timing.swap(keep);
     return LORA_OK;
+}
+
+// A pair of timing events for one upload call: a harvested pair if there is
+// one (creating events costs a driver call each), else a new pair.
+cudaError_t take_timing(lora_ctx *c, UploadTiming *t) {
+    if (!c->timing_free.empty()) {
+        *t = c->timing_free.back();
+        c->timing_free.pop_back();
+        return cudaSuccess;
+    }
+    cudaError_t e = cudaEventCreate(&t->start);
+    if (e != cudaSuccess) return e;
+    e = cudaEventCreate(&t->end);
+    if (e != cudaSuccess) cudaEventDestroy(t->start);
+    return e;
 }
 
 bool capturing(cudaStream_t s) {
@@ -370,6 +388,14 @@ void lora_destroy(lora_ctx *c) {
         if (c->upload) cudaStreamSynchronize(c->upload);
         if (c->compute) cudaStreamSynchronize(c->compute);
         harvest_timings(c, true);
+        for (auto &t : c->timing) {                // (only if a harvest failed)
+            cudaEventDestroy(t.start);
+            cudaEventDestroy(t.end);
+        }
+        for (auto &t : c->timing_free) {
+            cudaEventDestroy(t.start);
+            cudaEventDestroy(t.end);
+        }
         for (auto ev : c->up_ev)
             if (ev) cudaEventDestroy(ev);
         if (c->compute_done) cudaEventDestroy(c->compute_done);
@@ -408,8 +434,7 @@ int lora_load_slot(lora_ctx *c, int slot, const void *const *A_host, const void 
     const size_t e = elem_bytes(c->dtype);
     const size_t R = c->R, r = rank;
     UploadTiming tm{};
-    CUDA_TRY(cudaEventCreate(&tm.start));
-    CUDA_TRY(cudaEventCreate(&tm.end));
+    CUDA_TRY(take_timing(c, &tm));
     // Never overwrite a slot that queued compute work may still read.
     CUDA_TRY(wait_slot_reads(c, slot));
     CUDA_TRY(cudaEventRecord(tm.start, c->upload));
@@ -527,8 +552,7 @@ int lora_load_slots(lora_ctx *c, int n, const int *slots, const void *const *A_h
             ++ua.n_slots;
         }
         UploadTiming tm{};
-        CUDA_TRY(cudaEventCreate(&tm.start));
-        CUDA_TRY(cudaEventCreate(&tm.end));
+        CUDA_TRY(take_timing(c, &tm));
         CUDA_TRY(cudaEventRecord(tm.start, c->upload));
         CUDA_TRY(launch_upload_slots(ua, units, c->upload));
         ++c->launches;
@@ -1081,9 +1105,9 @@ int lora_serve_step(lora_ctx *c, int T, const uint64_t *adapter_ids, int n, cons
     need.assign((size_t)nd, 0);
     ev.assign((size_t)nd, LORA_NO_ADAPTER);
     const int L = c->n_layers;
-    std::vector<int> up_slots, up_ranks;
-    std::vector<float> up_alphas;
-    std::vector<const void *> up_A, up_B;
+    std::vector<int> &up_slots = c->up_slots, &up_ranks = c->up_ranks;
+    std::vector<float> &up_alphas = c->up_alphas;
+    std::vector<const void *> &up_A = c->up_A, &up_B = c->up_B;
     int i0 = 0;
     for (int g = 0; g < ng; ++g) {
         int i1 = i0;

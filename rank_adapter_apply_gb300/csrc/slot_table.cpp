@@ -56,6 +56,19 @@ double SlotTable::keep_score(int s) const {
 // The evictable slot chosen by the policy; -1 if none.
 int SlotTable::victim() const {
     int best = -1;
+    if (policy_ == EvictPolicy::Lru && min_res_ == 0) {
+        // the first evictable slot with the smallest LRU clock, in one pass
+        // over the flat arrays
+        uint64_t best_t = UINT64_MAX;
+        for (int s = 0; s < S_; ++s) {
+            const bool ok = occ_[s] && refs_[s] == 0 && !pin_[s];
+            if (ok && last_use_[s] < best_t) {
+                best_t = last_use_[s];
+                best = s;
+            }
+        }
+        return best;
+    }
     double best_k = 0.0;
     for (int s = 0; s < S_; ++s) {
         if (!evictable(s)) continue;
@@ -75,6 +88,7 @@ int SlotTable::victim() const {
 uint64_t SlotTable::evict(int slot) {
     uint64_t id = id_[slot];
     occ_[slot] = 0;
+    --n_occ_;
     pin_[slot] = 0;
     pending_[slot] = 0;
     refs_[slot] = 0;
@@ -104,8 +118,9 @@ AssignResult SlotTable::assign(uint64_t id, int rank, int *slot, uint64_t *evict
     // A free slot: unbound and unreferenced (a slot whose load was aborted
     // stays taken until its references are released).
     int s = -1;
-    for (int i = 0; i < S_; ++i)
-        if (!occ_[i] && refs_[i] == 0) { s = i; break; }
+    if (n_occ_ < S_)
+        for (int i = 0; i < S_; ++i)
+            if (!occ_[i] && refs_[i] == 0) { s = i; break; }
     if (s < 0) {
         s = victim();
         if (s < 0) {
@@ -121,6 +136,7 @@ AssignResult SlotTable::assign(uint64_t id, int rank, int *slot, uint64_t *evict
     r.rank = rank;
     id_[s] = id;
     occ_[s] = 1;
+    ++n_occ_;
     pin_[s] = 0;
     pending_[s] = 1;
     refs_[s] = 0;
@@ -154,6 +170,7 @@ bool SlotTable::abort_load(int slot, uint64_t *unbound_id) {
     if (slot < 0 || slot >= S_ || !occ_[slot] || !pending_[slot]) return false;
     const uint64_t id = id_[slot];
     occ_[slot] = 0;
+    --n_occ_;
     pin_[slot] = 0;
     pending_[slot] = 0;
     where_.erase(id);

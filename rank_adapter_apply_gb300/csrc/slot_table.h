@@ -96,6 +96,7 @@ private:
     double w_[5] = {1.0, 1.0, 1.0, 0.0, 0.0};
     uint64_t clock_ = 0;
     int64_t epoch_ = 0;
+    int n_occ_ = 0;                     // occupied slots (no free slot is searched for when all are)
     std::vector<uint64_t> id_;
     std::vector<char> occ_, pin_, pending_;
     std::vector<uint64_t> last_use_;
