@@ -585,19 +585,33 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
                     tc::fence_before_sync();
                     tc::mbar_arrive(&acc_empty[ac]);
                     if (live) {
+                        // four 16-byte chunks of the row at a time: their loads
+                        // go out together, then the arithmetic, then the
+                        // stores (a store may not pass a later load of the same
+                        // buffer, so one chunk at a time would chain them)
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            uint4 *p = reinterpret_cast<uint4 *>(yt + ((c ^ (i & 7)) * 16));
-                            const uint4 yv = *p;
-                            uint32_t w[4] = {yv.x, yv.y, yv.z, yv.w};
+                        for (int c0 = 0; c0 < 8; c0 += 4) {
+                            uint4 yv[4];
 #pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                w[e] = pack_bf16(fmaf(scale, __uint_as_float(d[8 * c + 2 * e]), bf_lo(w[e])),
-                                                 fmaf(scale, __uint_as_float(d[8 * c + 2 * e + 1]), bf_hi(w[e])));
-                            const uint4 o = make_uint4(w[0], w[1], w[2], w[3]);
-                            *p = o;
-                            if (rows < 128 && i < rows)
-                                reinterpret_cast<uint4 *>(a.y[it.l] + (size_t)(row0 + i) * d_out + col)[c] = o;
+                            for (int q = 0; q < 4; ++q)
+                                yv[q] = *reinterpret_cast<const uint4 *>(yt + (((c0 + q) ^ (i & 7)) * 16));
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const int c = c0 + q;
+                                uint32_t w[4] = {yv[q].x, yv[q].y, yv[q].z, yv[q].w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e)
+                                    w[e] = pack_bf16(fmaf(scale, __uint_as_float(d[8 * c + 2 * e]), bf_lo(w[e])),
+                                                     fmaf(scale, __uint_as_float(d[8 * c + 2 * e + 1]), bf_hi(w[e])));
+                                yv[q] = make_uint4(w[0], w[1], w[2], w[3]);
+                            }
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const int c = c0 + q;
+                                *reinterpret_cast<uint4 *>(yt + ((c ^ (i & 7)) * 16)) = yv[q];
+                                if (rows < 128 && i < rows)
+                                    reinterpret_cast<uint4 *>(a.y[it.l] + (size_t)(row0 + i) * d_out + col)[c] = yv[q];
+                            }
                         }
                     }
                 }
