@@ -24,11 +24,13 @@
 //
 // prefill_expand_kernel  persistent, one CTA per SM. The work items are
 //   (layer, tile, 256-column block of d_out), split into contiguous ranges.
-//   The epilogue warps sum the partials of V in a fixed order, split V into
-//   bf16 high + low parts in swizzled shared memory (double-buffered across
-//   tiles), the producer streams y and B_s n-blocks (64 columns) through the
-//   ring, one thread issues the expand MMAs (M 128, N 64, K R, twice: high
-//   and low parts) into rotating TMEM accumulators, and the epilogue computes
+//   The V-loader warps sum the partials of V in a fixed order and write V as
+//   bf16 high + low parts (double-buffered across tiles) into swizzled
+//   shared memory, or at rank 64 into tensor memory (which leaves the shared
+//   memory for one more ring stage), the producer streams y and B_s n-blocks
+//   through the ring, one thread issues the expand MMAs (M 128, N 128, K R,
+//   twice: high and low parts) into rotating TMEM accumulators, and the
+//   epilogue computes
 //   y = round(y + scale * D) in place in the ring and stores full tiles back
 //   with a TMA store (ragged tiles with plain row stores, so that no row of a
 //   neighbouring run is touched).
@@ -74,6 +76,14 @@ __host__ __device__ inline uint32_t tmem_cols_for(int cols) {
     while ((int)c < cols) c <<= 1;
     return c;
 }
+
+// Where the expand keeps V. In tensor memory its 32 KB of shared memory at
+// rank 64 become a fourth ring stage (3 -> 4: mixed-rank step 316 -> 300 us);
+// at rank 32 the fifth stage that it would allow was measured slower than
+// four (346 against 335 us per prefill step) and an MMA reading A from tensor
+// memory slightly slower than one reading shared memory (337 us at four
+// stages), so lower ranks keep V in shared memory.
+__host__ __device__ constexpr bool expand_v_in_tmem(int R) { return R == 64; }
 
 // Row i of a K-major operand of R bf16 per row, in the swizzle the TMA and
 // the MMA descriptors use for that row width: 16-byte chunk c of the row goes
@@ -351,9 +361,14 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
     constexpr uint32_t kSwzRank = R == 64 ? tc::kSwz128 : (R == 32 ? tc::kSwz64 : tc::kSwz32);
     constexpr uint32_t kStage = 2 * kTileBytes + kNB * W;       // y boxes [2][128][64], B [128][R]
     constexpr uint32_t kVBytes = 128 * W;
+    // V in tensor memory (rank 64): after the kAcc accumulators of kNB
+    // columns, [2 buffers][hi, lo] of R / 2 columns each (two bf16 per column)
+    constexpr bool kVTmem = expand_v_in_tmem(R);
+    constexpr uint32_t kVCol = kNB * kAcc, kTmemCols = kVTmem ? 512 : kNB * kAcc;
+    static_assert(!kVTmem || kVCol + 2 * R <= kTmemCols, "V fits in the allocation");
     const int stages = a.stages;
     uint8_t *ring = base;
-    uint8_t *vbuf = base + (size_t)stages * kStage;            // [2][hi, lo]
+    uint8_t *vbuf = base + (size_t)stages * kStage;            // [2][hi, lo] (V in shared memory)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     grid_dependency_wait();                 // the partials of V (shrink, chunk sums)
@@ -388,7 +403,7 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
     }
     for (int x = tid; x < a.S; x += kExpandThreads) sscale[x] = a.scale[x];
     if (warp == 1) {
-        tc::tmem_alloc(&tmem_base, kNB * kAcc);
+        tc::tmem_alloc(&tmem_base, kTmemCols);
         tc::tmem_relinquish();
     }
     tc::fence_before_sync();
@@ -445,8 +460,10 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
                     if (!wait_ok(&v_full[gen & 1], (uint32_t)(gen >> 1) & 1u, err)) break;
                     tc::fence_after_sync();
                 }
-                const uint32_t vh = smem_u32(vbuf + (size_t)(gen & 1) * 2 * kVBytes);
-                const uint32_t vl = vh + kVBytes;
+                // V: tensor-memory columns, or shared-memory addresses
+                const uint32_t vh = kVTmem ? tmem + kVCol + (uint32_t)(gen & 1) * R
+                                           : smem_u32(vbuf + (size_t)(gen & 1) * 2 * kVBytes);
+                const uint32_t vl = kVTmem ? vh + R / 2 : vh + kVBytes;
                 const int nb = n_blocks(a, it);
                 for (int b = 0; b < nb; ++b) {
                     const int st = j % stages, ac = j % kAcc;
@@ -455,14 +472,24 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
                     tc::fence_after_sync();
                     const uint32_t ba = smem_u32(ring + (size_t)st * kStage + 2 * kTileBytes);
                     const uint32_t d = tmem + (uint32_t)kNB * ac;
+                    if constexpr (kVTmem) {
 #pragma unroll
-                    for (int kk = 0; kk < R / 16; ++kk)
-                        tc::mma_bf16(d, tc::smem_desc(vh + kk * 32, W, kSwzRank),
-                                     tc::smem_desc(ba + kk * 32, W, kSwzRank), idesc, kk != 0);
+                        for (int kk = 0; kk < R / 16; ++kk)
+                            tc::mma_bf16_tmem_a(d, vh + kk * 8, tc::smem_desc(ba + kk * 32, W, kSwzRank), idesc,
+                                                kk != 0);
 #pragma unroll
-                    for (int kk = 0; kk < R / 16; ++kk)
-                        tc::mma_bf16(d, tc::smem_desc(vl + kk * 32, W, kSwzRank),
-                                     tc::smem_desc(ba + kk * 32, W, kSwzRank), idesc, 1);
+                        for (int kk = 0; kk < R / 16; ++kk)
+                            tc::mma_bf16_tmem_a(d, vl + kk * 8, tc::smem_desc(ba + kk * 32, W, kSwzRank), idesc, 1);
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < R / 16; ++kk)
+                            tc::mma_bf16(d, tc::smem_desc(vh + kk * 32, W, kSwzRank),
+                                         tc::smem_desc(ba + kk * 32, W, kSwzRank), idesc, kk != 0);
+#pragma unroll
+                        for (int kk = 0; kk < R / 16; ++kk)
+                            tc::mma_bf16(d, tc::smem_desc(vl + kk * 32, W, kSwzRank),
+                                         tc::smem_desc(ba + kk * 32, W, kSwzRank), idesc, 1);
+                    }
                     tc::mma_commit(&acc_full[ac]);
                     ++j;
                 }
@@ -478,7 +505,10 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
         }
     } else if (warp < 6) {
         // ---------------- V loaders: row i of the tile ----------------
-        const int i = tid - 64;
+        // (V in tensor memory: a warp reaches the lanes 32 (warp % 4) ..
+        // 32 (warp % 4) + 31)
+        const int i = kVTmem ? (warp & 3) * 32 + lane : tid - 64;
+        const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
         int gen = -1, pl = -1, pp = -1;
         for (int k = k0; k < k1; ++k) {
             const Item it = item_at(a, k, np);
@@ -487,8 +517,15 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
             pl = it.l;
             pp = it.p;
             const int vb = gen & 1;
-            if (!wait_ok(&v_empty[vb], ((uint32_t)(gen >> 1) & 1u) ^ 1u, err)) break;
+            if constexpr (kVTmem) {
+                // (warp-uniform: the TMEM stores below are issued by whole warps)
+                if (!__all_sync(0xffffffffu, wait_ok(&v_empty[vb], ((uint32_t)(gen >> 1) & 1u) ^ 1u, err))) break;
+                tc::fence_after_sync();
+            } else {
+                if (!wait_ok(&v_empty[vb], ((uint32_t)(gen >> 1) & 1u) ^ 1u, err)) break;
+            }
             const int4 pt = a.ptiles[it.p];
+            const uint32_t vth = tmem + lane_addr + kVCol + (uint32_t)vb * R, vtl = vth + R / 2;
             uint8_t *vh = vbuf + (size_t)vb * 2 * kVBytes;
             uint8_t *vl = vh + kVBytes;
             float v[R];
@@ -529,21 +566,41 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
                     }
                 }
             }
+            if constexpr (kVTmem) {
+                // 16 ranks (eight tensor-memory columns) of each part at a time
 #pragma unroll
-            for (int c = 0; c < R / 8; ++c) {
-                uint32_t hw[4], lw[4];
+                for (int c = 0; c < R / 16; ++c) {
+                    uint32_t hw[8], lw[8];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float x0 = v[8 * c + 2 * e], x1 = v[8 * c + 2 * e + 1];
-                    const float h0 = round_bf16(x0), h1 = round_bf16(x1);
-                    hw[e] = pack_bf16(h0, h1);
-                    lw[e] = pack_bf16(x0 - h0, x1 - h1);
+                    for (int e = 0; e < 8; ++e) {
+                        const float x0 = v[16 * c + 2 * e], x1 = v[16 * c + 2 * e + 1];
+                        const float h0 = round_bf16(x0), h1 = round_bf16(x1);
+                        hw[e] = pack_bf16(h0, h1);
+                        lw[e] = pack_bf16(x0 - h0, x1 - h1);
+                    }
+                    tc::tmem_st8(vth + 8 * c, hw);
+                    tc::tmem_st8(vtl + 8 * c, lw);
                 }
-                const int pc = swz_chunk<R>(c, i);
-                *reinterpret_cast<uint4 *>(vh + i * W + pc * 16) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4 *>(vl + i * W + pc * 16) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                tc::tmem_st_wait();
+                tc::fence_before_sync();
+            } else {
+                // one swizzled 16-byte chunk (8 ranks) of each part at a time
+#pragma unroll
+                for (int c = 0; c < R / 8; ++c) {
+                    uint32_t hw[4], lw[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float x0 = v[8 * c + 2 * e], x1 = v[8 * c + 2 * e + 1];
+                        const float h0 = round_bf16(x0), h1 = round_bf16(x1);
+                        hw[e] = pack_bf16(h0, h1);
+                        lw[e] = pack_bf16(x0 - h0, x1 - h1);
+                    }
+                    const int pc = swz_chunk<R>(c, i);
+                    *reinterpret_cast<uint4 *>(vh + i * W + pc * 16) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    *reinterpret_cast<uint4 *>(vl + i * W + pc * 16) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                }
+                tc::fence_proxy_async_smem();
             }
-            tc::fence_proxy_async_smem();
             tc::mbar_arrive(&v_full[vb]);
         }
     } else {
@@ -653,7 +710,7 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
     if (warp == 1) {
         __syncwarp();
         tc::fence_after_sync();
-        tc::tmem_dealloc(tmem, kNB * kAcc);
+        tc::tmem_dealloc(tmem, kTmemCols);
     }
 }
 
@@ -680,7 +737,8 @@ bool encode_2d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, ui
 
 template <int R>
 size_t expand_smem(int stages) {
-    return 1024 + (size_t)stages * (2 * kTileBytes + kNB * R * 2) + 4 * (size_t)128 * R * 2;
+    return 1024 + (size_t)stages * (2 * kTileBytes + kNB * R * 2) +
+           (expand_v_in_tmem(R) ? 0 : 4 * (size_t)128 * R * 2);
 }
 
 template <int R>
@@ -854,7 +912,8 @@ cudaError_t launch_prefill_tc(const PrefillLayer *L, int n, int T, int S, int R,
         ra.nch[i] = nch[grp[i]];
         ea.sum_ncb += ea.ncb[i];
     }
-    const size_t vbytes = 4 * (size_t)128 * R * 2, stage = 2 * kTileBytes + kNB * (size_t)R * 2;
+    const size_t vbytes = expand_v_in_tmem(R) ? 0 : 4 * (size_t)128 * R * 2;
+    const size_t stage = 2 * kTileBytes + kNB * (size_t)R * 2;
     ea.stages = (int)((kExpandSmemBudget - 1024 - vbytes) / stage);
     if (ea.stages > kMaxStages) ea.stages = kMaxStages;
     ea.ptiles = ptiles;
