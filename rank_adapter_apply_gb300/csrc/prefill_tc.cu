@@ -826,8 +826,11 @@ cudaError_t launch_prefill_tc(const PrefillLayer *L, int n, int T, int S, int R,
         }
     }
 
-    // d_in chunks: about two waves of shrink CTAs (two per SM), each group's
-    // share proportional to its d_in; partial rows bound the chunk count.
+    // d_in chunks: about one and a half waves of shrink CTAs (two per SM),
+    // each group's share proportional to its d_in; partial rows bound the
+    // chunk count. (Measured: a target of 3 x SMs CTAs equals 4 x on the
+    // rank-32 prefill step and beats it by 2 us on the rank-64 mixed step;
+    // 2 x and 6-12 x are slower.)
     int max_ch = part_rows / T;
     if (max_ch > 16) max_ch = 16;
     if (max_ch < 1) return cudaErrorInvalidValue;
@@ -837,7 +840,7 @@ cudaError_t launch_prefill_tc(const PrefillLayer *L, int n, int T, int S, int R,
         kb[g] = (L[glead[g]].d_in + 63) / 64;
         kb_total += kb[g];
     }
-    const int want = (4 * num_sms + est_tiles - 1) / est_tiles;    // jobs per tile
+    const int want = (3 * num_sms + est_tiles - 1) / est_tiles;    // jobs per tile
     int n_jobs = 0;
     for (int g = 0; g < ng; ++g) {
         int c = (int)(((long long)want * kb[g] + kb_total - 1) / kb_total);
