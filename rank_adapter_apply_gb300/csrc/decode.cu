@@ -33,11 +33,27 @@ constexpr int kThreads = 128;
 constexpr int kWarps = kThreads / 32;
 constexpr int kExpandCols = 256;          // output columns per expand CTA (bf16 and fp32)
 
-// Sum the chunk partials of one tile in chunk order and write v (last CTA only).
-// Loads of eight chunks are issued before they are added (the sum keeps the
-// chunk order), so a 14-way split costs two L2 round trips, not fourteen.
+// v of the bf16 path, kept in the order the expand's MMA fragments read it:
+// row `pos` of R x 4 bytes holds, for every four ranks k0 .. k0 + 3 (k0 a
+// multiple of 4), one 16-byte group: the bf16 high parts of the four ranks,
+// then their bf16 low parts (value - high part), lower rank first. The
+// expand then loads a fragment with one 16-byte load per row instead of
+// splitting fp32 values for every 256-column block it covers.
+__device__ __forceinline__ void store_vfrag(float *v, int R, int pos, int k, float s) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(s);
+    const __nv_bfloat16 l = __float2bfloat16_rn(s - __bfloat162float(h));
+    __nv_bfloat16 *grp = reinterpret_cast<__nv_bfloat16 *>(v + (size_t)pos * R) + (k >> 2) * 8;
+    grp[k & 3] = h;
+    grp[4 + (k & 3)] = l;
+}
+
+// Sum the chunk partials of one tile in chunk order and write v (last CTA
+// only): ranks below `kr` of each row, as fp32 or (frag) in the bf16
+// fragment order. Loads of eight chunks are issued before they are added
+// (the sum keeps the chunk order), so a 14-way split costs two L2 round
+// trips, not fourteen.
 __device__ void finish_split(const LayerArgs &L, const GroupView &g, int tile_i, int p0, int cnt,
-                             int r) {
+                             int kr, bool frag) {
     __shared__ int last;
     __threadfence();
     __syncthreads();
@@ -50,8 +66,8 @@ __device__ void finish_split(const LayerArgs &L, const GroupView &g, int tile_i,
     __threadfence();
     const int R = g.R, T = g.T;
     const size_t cs = (size_t)T * R;
-    for (int e = threadIdx.x; e < cnt * r; e += kThreads) {
-        const int pos = p0 + e / r, k = e % r;
+    for (int e = threadIdx.x; e < cnt * kr; e += kThreads) {
+        const int pos = p0 + e / kr, k = e % kr;
         const float *src = L.part + (size_t)pos * R + k;
         float s = 0.f;
         int ch = 0;
@@ -63,7 +79,8 @@ __device__ void finish_split(const LayerArgs &L, const GroupView &g, int tile_i,
             for (int u = 0; u < 8; ++u) s += a[u];
         }
         for (; ch < L.n_chunks; ++ch) s += __ldcg(src + (size_t)ch * cs);
-        L.v[(size_t)pos * R + k] = s;
+        if (frag) store_vfrag(L.v, R, pos, k, s);
+        else L.v[(size_t)pos * R + k] = s;
     }
     if (threadIdx.x == 0) L.counters[tile_i] = 0;
 }
@@ -148,16 +165,22 @@ __device__ __forceinline__ void shrink_bf16_tile(const LayerArgs &L, const Group
 #pragma unroll
             for (int j = 0; j < 4; ++j) red[warp][(m * 2 + n) * 4 + j][lane] = acc[m][n][j];
     __syncthreads();
-    float *dst_base = L.n_chunks == 1 ? L.v : L.part + (size_t)chunk * g.T * R;
+    // ranks r .. 16 nmb - 1 come out as exact zeros (their A rows are
+    // masked) and are written too: the expand reads whole 16-rank blocks
+    const bool split = L.n_chunks > 1;
+    float *part = L.part + (size_t)chunk * g.T * R;
     for (int e = threadIdx.x; e < nmb * 256; e += kThreads) {
         const int ln = e & 31, slot_j = e >> 5;          // slot_j = (m*2+n)*4 + j
         const int j = slot_j & 3, n = (slot_j >> 2) & 1, m = slot_j >> 3;
         float v = red[0][slot_j][ln] + red[1][slot_j][ln] + red[2][slot_j][ln] + red[3][slot_j][ln];
         const int k = m * 16 + (ln >> 2) + ((j & 2) ? 8 : 0);
         const int tk = n * 8 + 2 * (ln & 3) + (j & 1);
-        if (tk < cnt && k < r) dst_base[(size_t)(p0 + tk) * R + k] = v;
+        if (tk < cnt) {
+            if (split) part[(size_t)(p0 + tk) * R + k] = v;
+            else store_vfrag(L.v, R, p0 + tk, k, v);
+        }
     }
-    if (L.n_chunks > 1) finish_split(L, g, tile_i, p0, cnt, r);
+    if (split) finish_split(L, g, tile_i, p0, cnt, 16 * nmb, true);
 }
 
 // ---------------------------------------------------------------------------
@@ -214,38 +237,24 @@ __device__ __forceinline__ void expand_bf16_run(const LayerArgs &L, const GroupV
         const int tok1 = gq + 8 < cnt ? g.perm[p0 + 8 + gq] : -1;
 
         // A fragments of V (rows = tokens gq, gq+8; k = 4tq..4tq+3 of each
-        // 16-rank block), split into bf16 high and low parts.
+        // 16-rank block): one 16-byte load per row and block of the high and
+        // low parts the shrink stored in fragment order.
         uint32_t ahi[4][4], alo[4][4];
 #pragma unroll
         for (int kb = 0; kb < 4; ++kb) {
             if (kb >= nkb) break;
-            float f0[4] = {0.f, 0.f, 0.f, 0.f}, f1[4] = {0.f, 0.f, 0.f, 0.f};
-            const int kq = kb * 16 + 4 * tq;             // ranks kq .. kq + 3, one 16-byte load per row
-            if (gq < cnt) {
-                const float4 q = *reinterpret_cast<const float4 *>(L.v + (size_t)(p0 + gq) * R + kq);
-                f0[0] = q.x; f0[1] = q.y; f0[2] = q.z; f0[3] = q.w;
-            }
-            if (gq + 8 < cnt) {
-                const float4 q = *reinterpret_cast<const float4 *>(L.v + (size_t)(p0 + gq + 8) * R + kq);
-                f1[0] = q.x; f1[1] = q.y; f1[2] = q.z; f1[3] = q.w;
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                if (kq + i >= r) f0[i] = f1[i] = 0.f;
-            float h0[4], h1[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                h0[i] = __bfloat162float(__float2bfloat16_rn(f0[i]));
-                h1[i] = __bfloat162float(__float2bfloat16_rn(f1[i]));
-            }
-            ahi[kb][0] = pack_bf16(h0[0], h0[1]);
-            ahi[kb][1] = pack_bf16(h1[0], h1[1]);
-            ahi[kb][2] = pack_bf16(h0[2], h0[3]);
-            ahi[kb][3] = pack_bf16(h1[2], h1[3]);
-            alo[kb][0] = pack_bf16(f0[0] - h0[0], f0[1] - h0[1]);
-            alo[kb][1] = pack_bf16(f1[0] - h1[0], f1[1] - h1[1]);
-            alo[kb][2] = pack_bf16(f0[2] - h0[2], f0[3] - h0[3]);
-            alo[kb][3] = pack_bf16(f1[2] - h1[2], f1[3] - h1[3]);
+            const int grp = kb * 4 + tq;                 // ranks 4 grp .. 4 grp + 3
+            uint4 q0 = make_uint4(0, 0, 0, 0), q1 = make_uint4(0, 0, 0, 0);
+            if (gq < cnt) q0 = *reinterpret_cast<const uint4 *>(L.v + (size_t)(p0 + gq) * R + grp * 4);
+            if (gq + 8 < cnt) q1 = *reinterpret_cast<const uint4 *>(L.v + (size_t)(p0 + gq + 8) * R + grp * 4);
+            ahi[kb][0] = q0.x;
+            ahi[kb][1] = q1.x;
+            ahi[kb][2] = q0.y;
+            ahi[kb][3] = q1.y;
+            alo[kb][0] = q0.z;
+            alo[kb][1] = q1.z;
+            alo[kb][2] = q0.w;
+            alo[kb][3] = q1.w;
         }
 
         // y of both column groups and both token rows, fetched before the
@@ -368,7 +377,7 @@ __device__ __forceinline__ void shrink_f32_tile(const LayerArgs &L, const GroupV
             if (lane == 0) dst_base[(size_t)(p0 + i) * R + k] = a;
         }
     }
-    if (L.n_chunks > 1) finish_split(L, g, tile_i, p0, cnt, r);
+    if (L.n_chunks > 1) finish_split(L, g, tile_i, p0, cnt, r, false);
 }
 
 // fp32 expand-add: each thread owns two columns of the 256-column block.
