@@ -288,18 +288,20 @@ __device__ __forceinline__ void expand_bf16_run(const LayerArgs &L, const GroupV
             // one-block-at-a-time loop, while four independent MMAs go out
             // back to back. (ranks >= r are zero in the pool and in v, so no
             // mask is needed)
+            // The rows this lane reads, P = c + 8 (gq >> 1) + 2 j + (gq & 1),
+            // all have key(P - c0) = gq (c - c0 is a multiple of 32), so the
+            // swizzled chunk of rank block kb is (2 kb + tq / 2) ^ gq.
             uint2 bb[4][4];
+            const uint16_t *brow = bs + (c - c0 + 8 * (gq >> 1) + (gq & 1)) * 64 + 4 * (tq & 1);
+            const bool full_grp = c + 32 <= d_out;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int P = c + 8 * (gq >> 1) + 2 * j + (gq & 1);
 #pragma unroll
                 for (int kb = 0; kb < 4; ++kb) {
-                    const int k = kb * 16 + 4 * tq;
                     bb[j][kb] = make_uint2(0, 0);
-                    if (kb < nkb && P < d_out) {
-                        const int Pl = P - c0;
-                        bb[j][kb] = *reinterpret_cast<const uint2 *>(bs + Pl * 64 + (((k >> 3) ^ bkey(Pl)) << 3) + (k & 7));
-                    }
+                    if (kb < nkb && (full_grp || P < d_out))
+                        bb[j][kb] = *reinterpret_cast<const uint2 *>(brow + 2 * j * 64 + (((2 * kb + (tq >> 1)) ^ gq) << 3));
                 }
             }
             float acc[4][4];
