@@ -125,6 +125,48 @@ __device__ __forceinline__ void shrink_steps(float (&acc)[4][2][4], const uint16
     }
 }
 
+// The same loop when every row is 16-byte aligned and the chunk is a whole
+// number of 32-column steps (d_in % 32 == 0): plain 16-byte loads, predicated
+// only on the token existing and the rank being below the slot's rank.
+template <int NMB, int UNROLL>
+__device__ __forceinline__ void shrink_steps_fast(float (&acc)[4][2][4], const uint16_t *xr0, const uint16_t *xr1,
+                                                  const uint16_t *As, bool ok0, bool ok1, int r, int d_in, int c0,
+                                                  int c1) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    const uint16_t *ar0[NMB], *ar1[NMB];
+    bool ak0[NMB], ak1[NMB];
+#pragma unroll
+    for (int m = 0; m < NMB; ++m) {
+        const int k0 = m * 16 + gq, k1 = k0 + 8;
+        ar0[m] = As + (size_t)k0 * d_in;
+        ar1[m] = As + (size_t)k1 * d_in;
+        ak0[m] = k0 < r;
+        ak1[m] = k1 < r;
+    }
+#pragma unroll UNROLL
+    for (int cc = c0 + warp * 32 + 8 * tq; cc < c1; cc += kWarps * 32) {
+        const uint4 xa = ok0 ? __ldg(reinterpret_cast<const uint4 *>(xr0 + cc)) : zero;
+        const uint4 xb = ok1 ? __ldg(reinterpret_cast<const uint4 *>(xr1 + cc)) : zero;
+        uint4 a0[NMB], a1[NMB];
+#pragma unroll
+        for (int m = 0; m < NMB; ++m) {
+            a0[m] = ak0[m] ? __ldg(reinterpret_cast<const uint4 *>(ar0[m] + cc)) : zero;
+            a1[m] = ak1[m] ? __ldg(reinterpret_cast<const uint4 *>(ar1[m] + cc)) : zero;
+        }
+#pragma unroll
+        for (int m = 0; m < NMB; ++m) {
+            mma_bf16(acc[m][0], a0[m].x, a1[m].x, a0[m].y, a1[m].y, xa.x, xa.y);
+            mma_bf16(acc[m][1], a0[m].x, a1[m].x, a0[m].y, a1[m].y, xb.x, xb.y);
+        }
+#pragma unroll
+        for (int m = 0; m < NMB; ++m) {
+            mma_bf16(acc[m][0], a0[m].z, a1[m].z, a0[m].w, a1[m].w, xa.z, xa.w);
+            mma_bf16(acc[m][1], a0[m].z, a1[m].z, a0[m].w, a1[m].w, xb.z, xb.w);
+        }
+    }
+}
+
 __device__ __forceinline__ void shrink_bf16_tile(const LayerArgs &L, const GroupView &g, int chunk, int tile_i) {
     const int4 tile = g.tiles[tile_i];
     const int s = tile.x, p0 = tile.y, cnt = tile.z;
@@ -152,9 +194,15 @@ __device__ __forceinline__ void shrink_bf16_tile(const LayerArgs &L, const Group
     const int c1 = min(d_in, c0 + L.chunk_cols);
     // The rank-block count is a template argument of the loop, so that no
     // runtime condition stands between the loads of several steps.
-    if (nmb <= 1) shrink_steps<1, 4>(acc, xr0, xr1, As, tok0, tok1, r, d_in, c0, c1, L.vec);
-    else if (nmb == 2) shrink_steps<2, 2>(acc, xr0, xr1, As, tok0, tok1, r, d_in, c0, c1, L.vec);
-    else shrink_steps<4, 2>(acc, xr0, xr1, As, tok0, tok1, r, d_in, c0, c1, L.vec);
+    if (L.vec && (d_in & 31) == 0) {
+        if (nmb <= 1) shrink_steps_fast<1, 4>(acc, xr0, xr1, As, tok0 >= 0, tok1 >= 0, r, d_in, c0, c1);
+        else if (nmb == 2) shrink_steps_fast<2, 2>(acc, xr0, xr1, As, tok0 >= 0, tok1 >= 0, r, d_in, c0, c1);
+        else shrink_steps_fast<4, 2>(acc, xr0, xr1, As, tok0 >= 0, tok1 >= 0, r, d_in, c0, c1);
+    } else {
+        if (nmb <= 1) shrink_steps<1, 4>(acc, xr0, xr1, As, tok0, tok1, r, d_in, c0, c1, L.vec);
+        else if (nmb == 2) shrink_steps<2, 2>(acc, xr0, xr1, As, tok0, tok1, r, d_in, c0, c1, L.vec);
+        else shrink_steps<4, 2>(acc, xr0, xr1, As, tok0, tok1, r, d_in, c0, c1, L.vec);
+    }
 
     // Cross-warp sum through shared memory.
     __shared__ float red[kWarps][4 * 2 * 4][32];
