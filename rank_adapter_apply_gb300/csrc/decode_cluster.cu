@@ -195,12 +195,19 @@ __device__ void issue_shrink(const LayerArgs &L, const ClusterSmem &sm, Dyn<KB> 
     uint16_t *xs = d.xs + b * kTileTokens * kSW;
     uint16_t *as = d.as + b * KB * 16 * kSW;
     const int total = (t.cnt + t.r) * cpr;
-    for (int e = threadIdx.x; e < total; e += kCT) {
-        const int row = e / cpr, col = (e - row * cpr) * 8;
+    auto issue = [&](int row, int col) {
         if (row < t.cnt)
             cp_async16(xs + swz(row, col), x + (size_t)sm.tok[row] * L.d_in + ks + col);
         else
             cp_async16(as + swz(row - t.cnt, col), A + (size_t)(row - t.cnt) * L.d_in + ks + col);
+    };
+    if (cpr == kSW / 8) {                   // a full stage: row and column by shifts
+        for (int e = threadIdx.x; e < total; e += kCT) issue(e >> 5, (e & 31) << 3);
+    } else {
+        for (int e = threadIdx.x; e < total; e += kCT) {
+            const int row = e / cpr;
+            issue(row, (e - row * cpr) * 8);
+        }
     }
     cp_async_arrive_noinc(bar);
 }
@@ -219,16 +226,26 @@ __device__ void issue_expand(const LayerArgs &L, const ClusterSmem &sm, Dyn<KB> 
     uint16_t *ys = d.ys + b * kTileTokens * kSW;
     uint16_t *bs = d.bs + (size_t)b * kSW * KB * 16;
     if (parts & 1) {
+        // chunk e of the contiguous block: element q = 8 e, row q / R (R a
+        // power of two in 16..64 takes a shift)
+        const int rs = R == 16 ? 4 : (R == 32 ? 5 : (R == 64 ? 6 : 0));
         for (int e = threadIdx.x; e < (w * R) >> 3; e += kCT) {
-            const int q = e * 8;                  // element offset in the contiguous block
-            const int P = q / R;
+            const int q = e * 8;
+            const int P = rs ? q >> rs : q / R;
             cp_async16(bs + bsw(P, q - P * R, R), B + q);
         }
     }
     if (parts & 2) {
-        for (int e = threadIdx.x; e < t.cnt * cpr; e += kCT) {
-            const int row = e / cpr, col = (e - row * cpr) * 8;
-            cp_async16(ys + swz(row, col), y + (size_t)sm.tok[row] * L.d_out + os + col);
+        if (cpr == kSW / 8) {
+            for (int e = threadIdx.x; e < t.cnt * cpr; e += kCT) {
+                const int row = e >> 5, col = (e & 31) << 3;
+                cp_async16(ys + swz(row, col), y + (size_t)sm.tok[row] * L.d_out + os + col);
+            }
+        } else {
+            for (int e = threadIdx.x; e < t.cnt * cpr; e += kCT) {
+                const int row = e / cpr, col = (e - row * cpr) * 8;
+                cp_async16(ys + swz(row, col), y + (size_t)sm.tok[row] * L.d_out + os + col);
+            }
         }
         cp_async_arrive_noinc(bar);
     }
