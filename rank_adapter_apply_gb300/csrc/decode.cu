@@ -55,15 +55,19 @@ __device__ __forceinline__ void store_vfrag(float *v, int R, int pos, int k, flo
 __device__ void finish_split(const LayerArgs &L, const GroupView &g, int tile_i, int p0, int cnt,
                              int kr, bool frag) {
     __shared__ int last;
-    __threadfence();
+    // The CTA's partial stores are ordered before thread 0's count by the
+    // barrier, and published at GPU scope by the count's release; the last
+    // CTA's acquire (the same atomic) and the barrier after it order every
+    // thread's reads of the other chunks' partials after their counts.
     __syncthreads();
     if (threadIdx.x == 0) {
-        int prev = atomicAdd(&L.counters[tile_i], 1);
+        int prev;
+        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                     : "=r"(prev) : "l"(L.counters + tile_i) : "memory");
         last = (prev == L.n_chunks - 1);
     }
     __syncthreads();
     if (!last) return;
-    __threadfence();
     const int R = g.R, T = g.T;
     const size_t cs = (size_t)T * R;
     for (int e = threadIdx.x; e < cnt * kr; e += kThreads) {
