@@ -461,6 +461,37 @@ __device__ __forceinline__ void expand_f32_tile(const LayerArgs &L, const GroupV
     }
 }
 
+// Work item w = (t * n + l) * inner + i (tile t, layer l, chunk or column
+// block i), walked with a stride of gridDim.x from blockIdx.x: the indices
+// are carried from one item to the next, so a CTA divides once, not three
+// times per item (most items of a mixed batch are skipped, so this is most of
+// what a skipped item costs).
+struct ItemWalk {
+    int i, l, t, si, sl, st, inner, n;
+    __device__ ItemWalk(int inner_, int n_) : inner(inner_), n(n_) {
+        const int w = (int)blockIdx.x, g = (int)gridDim.x;
+        i = w % inner;
+        l = (w / inner) % n;
+        t = w / (inner * n);
+        si = g % inner;
+        sl = (g / inner) % n;
+        st = g / (inner * n);
+    }
+    __device__ void next() {
+        i += si;
+        l += sl;
+        t += st;
+        if (i >= inner) {
+            i -= inner;
+            ++l;
+        }
+        if (l >= n) {
+            l -= n;
+            ++t;
+        }
+    }
+};
+
 // The kernels are persistent: work items are (tile, layer, chunk) for the
 // shrink and (tile, layer, 256-column block) for the expand, taken with a
 // stride of gridDim.x. The tile count is known on the device only (a prefill
@@ -470,10 +501,9 @@ __global__ void __launch_bounds__(kThreads)
 shrink_bf16_kernel(MultiArgs ma, GroupView g, int max_chunks) {
     grid_dependency_wait();            // launched early: the kernel before has to finish first
     grid_launch_dependents();
-    const int per_tile = max_chunks * ma.n;
-    const int items = g.hdr[kHdrTiles] * per_tile;
-    for (int w = blockIdx.x; w < items; w += gridDim.x) {
-        const int chunk = w % max_chunks, l = (w / max_chunks) % ma.n, t = w / per_tile;
+    const int n_tiles = g.hdr[kHdrTiles];
+    for (ItemWalk it(max_chunks, ma.n); it.t < n_tiles; it.next()) {
+        const int chunk = it.i, l = it.l, t = it.t;
         const LayerArgs &L = ma.l[l];
         if (chunk >= L.n_chunks) continue;
         shrink_bf16_tile(L, g, chunk, t);
@@ -485,11 +515,9 @@ __global__ void __launch_bounds__(kThreads, 4)
 expand_bf16_kernel(MultiArgs ma, GroupView g, int max_dblocks) {
     grid_dependency_wait();            // launched early: the kernel before has to finish first
     grid_launch_dependents();
-    const int per_tile = max_dblocks * ma.n;
     const int n_tiles = g.hdr[kHdrTiles];
-    const int items = n_tiles * per_tile;
-    for (int w = blockIdx.x; w < items; w += gridDim.x) {
-        const int db = w % max_dblocks, l = (w / max_dblocks) % ma.n, t = w / per_tile;
+    for (ItemWalk it(max_dblocks, ma.n); it.t < n_tiles; it.next()) {
+        const int db = it.i, l = it.l, t = it.t;
         const LayerArgs &L = ma.l[l];
         if (db * kExpandCols >= L.d_out) continue;
         // Items of a slot's first tile cover all of that slot's tiles.
@@ -503,10 +531,9 @@ __global__ void __launch_bounds__(kThreads)
 shrink_f32_kernel(MultiArgs ma, GroupView g, int max_chunks) {
     grid_dependency_wait();            // launched early: the kernel before has to finish first
     grid_launch_dependents();
-    const int per_tile = max_chunks * ma.n;
-    const int items = g.hdr[kHdrTiles] * per_tile;
-    for (int w = blockIdx.x; w < items; w += gridDim.x) {
-        const int chunk = w % max_chunks, l = (w / max_chunks) % ma.n, t = w / per_tile;
+    const int n_tiles = g.hdr[kHdrTiles];
+    for (ItemWalk it(max_chunks, ma.n); it.t < n_tiles; it.next()) {
+        const int chunk = it.i, l = it.l, t = it.t;
         const LayerArgs &L = ma.l[l];
         if (chunk >= L.n_chunks) continue;
         shrink_f32_tile(L, g, chunk, t);
@@ -518,10 +545,9 @@ __global__ void __launch_bounds__(kThreads)
 expand_f32_kernel(MultiArgs ma, GroupView g, int max_dblocks) {
     grid_dependency_wait();            // launched early: the kernel before has to finish first
     grid_launch_dependents();
-    const int per_tile = max_dblocks * ma.n;
-    const int items = g.hdr[kHdrTiles] * per_tile;
-    for (int w = blockIdx.x; w < items; w += gridDim.x) {
-        const int db = w % max_dblocks, l = (w / max_dblocks) % ma.n, t = w / per_tile;
+    const int n_tiles = g.hdr[kHdrTiles];
+    for (ItemWalk it(max_dblocks, ma.n); it.t < n_tiles; it.next()) {
+        const int db = it.i, l = it.l, t = it.t;
         const LayerArgs &L = ma.l[l];
         if (db * kExpandCols >= L.d_out) continue;
         expand_f32_tile(L, g, db, t);
