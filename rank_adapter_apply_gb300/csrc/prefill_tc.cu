@@ -183,7 +183,7 @@ prefill_reduce_kernel(const __grid_constant__ ReduceArgs a) {
 }
 
 template <int R>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 3)
 prefill_shrink_kernel(const __grid_constant__ ShrinkArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -718,7 +718,11 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
 // Host side
 // ============================================================================
 
-constexpr size_t kShrinkRingBudget = 108 * 1024;   // two shrink CTAs per SM
+// Shrink ring per CTA: three CTAs per SM below rank 64 (70 KB each: the q/k/v
+// group keeps two stages, a single-layer group three; measured 335.6 ->
+// 328.9 us per rank-32 prefill step against two CTAs of 108 KB), two at rank
+// 64, whose four-layer groups need 48 KB stages and 256 TMEM columns.
+constexpr size_t shrink_ring_budget(int R) { return R == 64 ? 108 * 1024 : 70 * 1024; }
 constexpr size_t kExpandSmemBudget = 216 * 1024;   // one expand CTA per SM
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -748,7 +752,7 @@ cudaError_t launch_r(const ShrinkArgs &sa, int grid_tiles, int n_jobs, size_t sh
     static std::atomic<uint64_t> attr{0};
     if (!device_bit(attr)) {
         cudaError_t e = cudaFuncSetAttribute(prefill_shrink_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)(1024 + kShrinkRingBudget));
+                                             (int)(1024 + shrink_ring_budget(R)));
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(prefill_expand_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kExpandSmemBudget);
@@ -826,7 +830,7 @@ cudaError_t launch_prefill_tc(const PrefillLayer *L, int n, int T, int S, int R,
         }
     }
 
-    // d_in chunks: about one and a half waves of shrink CTAs (two per SM),
+    // d_in chunks: about one and a half waves of two shrink CTAs per SM,
     // each group's share proportional to its d_in; partial rows bound the
     // chunk count. (Measured: a target of 3 x SMs CTAs equals 4 x on the
     // rank-32 prefill step and beats it by 2 us on the rank-64 mixed step;
@@ -872,9 +876,10 @@ cudaError_t launch_prefill_tc(const PrefillLayer *L, int n, int T, int S, int R,
     }
     // One ring for the launch; each CTA cuts it into as many stages of its
     // group's size as fit (at least two for the largest stage).
-    if (kShrinkRingBudget / max_stage < 2) return cudaErrorInvalidValue;
-    sa.ring_bytes = (int)kShrinkRingBudget;
-    const size_t shrink_smem = 1024 + kShrinkRingBudget;
+    const size_t ring_budget = shrink_ring_budget(R);
+    if (ring_budget / max_stage < 2) return cudaErrorInvalidValue;
+    sa.ring_bytes = (int)ring_budget;
+    const size_t shrink_smem = 1024 + ring_budget;
     int max_cols = 0;
     for (int g = 0; g < ng; ++g)
         if (gcount[g] * R > max_cols) max_cols = gcount[g] * R;
