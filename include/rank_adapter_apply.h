@@ -24,9 +24,19 @@
  *  - Streams are passed as cudaStream_t cast to void*. Kernels run on the
  *    compute stream; slot uploads on the upload stream. No call synchronises
  *    the host except lora_sync_uploads, lora_sync_host and lora_stats.
- *  - Layouts are row-major. A pool of layer l: [max_loras][max_lora_rank][d_in];
- *    B pool: [max_loras][d_out][max_lora_rank]; element type = the context's
- *    dtype. Activations x: [n_tokens][d_in]; outputs y: [n_tokens][d_out].
+ *  - Layouts are row-major. A pool of layer l: [max_loras][max_lora_rank][d_in].
+ *    B pool: [max_loras][max_lora_rank / kb][d_out][kb] with kb = 32 when
+ *    max_lora_rank is a multiple of 32, else 16 when it is a multiple of 16,
+ *    else 8 (so [max_loras][d_out][max_lora_rank] up to rank 32): slot s's
+ *    B_s (d_out x rank)
+ *    in blocks of kb consecutive ranks, element (i, k) of slot s at
+ *    s * d_out * max_lora_rank + (k / kb) * d_out * kb + i * kb + k % kb, so a
+ *    slot of rank r occupies ceil(r / kb) contiguous runs of d_out * kb
+ *    elements and kernels read no padding past them. Ranks at or past r are
+ *    zero in both pools. Element type = the context's dtype. Activations x:
+ *    [n_tokens][d_in]; outputs y: [n_tokens][d_out]. The upload calls write
+ *    this layout from host adapters in the PEFT layout (A [r][d_in], B
+ *    [d_out][r]).
  *  - A context is not thread-safe: one host thread at a time.
  */
 #ifndef RANK_ADAPTER_APPLY_H
@@ -64,7 +74,7 @@ typedef struct {
     int d_in;
     int d_out;
     void *A_pool;           /* device, [max_loras][max_lora_rank][d_in] */
-    void *B_pool;           /* device, [max_loras][d_out][max_lora_rank] */
+    void *B_pool;           /* device, max_loras x d_out x max_lora_rank elements, blocked by rank (see above) */
 } lora_layer_desc;
 
 typedef struct {
@@ -534,9 +544,10 @@ uint64_t lora_adapter_bytes(int n_layers, const int *d_in, const int *d_out, int
  * decode kernels; every token, long segments included, takes that path). The
  * caller passes inputs and outputs exactly as described for lora_apply and
  * lora_slots_init: x [n_tokens][d_in], y [n_tokens][d_out] updated in place,
- * device token_slot_idx, the layer's slot pools A_pool [max_loras]
- * [max_lora_rank][d_in] and B_pool [max_loras][d_out][max_lora_rank] (16-byte
- * aligned), scale_dev / rank_dev [max_loras] as lora_load_slot fills them,
+ * device token_slot_idx, the layer's slot pools in the layouts given at the
+ * top of this file (A_pool [max_loras][max_lora_rank][d_in], B_pool blocked by
+ * rank; 16-byte aligned), scale_dev / rank_dev [max_loras] as lora_load_slot
+ * fills them,
  * and the stream the work is queued on (cudaStream_t as void*).
  *
  * Scratch comes from a file-scope device array of 4 MiB that every GPU loading

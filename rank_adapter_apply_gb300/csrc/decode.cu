@@ -261,16 +261,18 @@ __device__ __forceinline__ void expand_bf16_run(const LayerArgs &L, const GroupV
     // c of the row at chunk c ^ key(P). One fragment read touches rows
     // P0 + 8a + b (a < 4, b < 2), so the key takes bits 3..4 and 0 of P and
     // those eight rows land in distinct bank groups. Thread i copies chunk
-    // i % 8 of rows i / 8, i / 8 + 16, ...
+    // i % 8 of rows i / 8, i / 8 + 16, ...; in the rank-blocked pool chunk
+    // ch of row P lies in block ch * 8 / kb, at P * kb + ch * 8 % kb there.
     __shared__ __align__(16) uint16_t bs[kExpandCols * 64];
     const uint16_t *Bs = static_cast<const uint16_t *>(L.B) + (size_t)s * d_out * R;
     const int c0 = dblock * kExpandCols;
     {
         const int ch = threadIdx.x & 7;
-        if (ch < 2 * nkb) {
-            const int rows = min(kExpandCols, d_out - c0);
+        if (ch < 2 * nkb && ch * 8 < R) {
+            const int kb = b_block(R), rows = min(kExpandCols, d_out - c0);
+            const uint16_t *src = Bs + ((size_t)((ch * 8) / kb) * d_out + c0) * kb + (ch * 8) % kb;
             for (int P = threadIdx.x >> 3; P < rows; P += kThreads / 8)
-                cp_async16(bs + P * 64 + ((ch ^ bkey(P)) << 3), Bs + (size_t)(c0 + P) * R + ch * 8);
+                cp_async16(bs + P * 64 + ((ch ^ bkey(P)) << 3), src + (size_t)P * kb);
         }
         cp_async_commit();
     }
@@ -451,10 +453,12 @@ __device__ __forceinline__ void expand_f32_tile(const LayerArgs &L, const GroupV
     for (int h = 0; h < 2; ++h) {
         const int col = dblock * kExpandCols + h * kThreads + threadIdx.x;
         if (col >= d_out) continue;
-        const float *br = Bs + (size_t)col * R;
+        const int kb = b_block(R), kbs = kb == 32 ? 5 : (kb == 16 ? 4 : 3);
+        const float *br = Bs + (size_t)col * kb;         // rank k at br[(k / kb) * d_out * kb + k % kb]
         for (int i = 0; i < cnt; ++i) {
             float a = 0.f;
-            for (int k = 0; k < r; ++k) a = fmaf(br[k], sv[i * r + k], a);
+            for (int k = 0; k < r; ++k)
+                a = fmaf(br[(size_t)(k >> kbs) * d_out * kb + (k & (kb - 1))], sv[i * r + k], a);
             float *yp = y + (size_t)g.perm[p0 + i] * d_out + col;
             *yp = fmaf(scale, a, *yp);
         }

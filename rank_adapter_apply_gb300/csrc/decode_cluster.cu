@@ -222,17 +222,20 @@ __device__ void issue_expand(const LayerArgs &L, const ClusterSmem &sm, Dyn<KB> 
     const int os = o0 + j * kSW, w = min(kSW, o1 - os);
     const int cpr = w >> 3;
     const uint16_t *y = static_cast<const uint16_t *>(L.y);
-    const uint16_t *B = static_cast<const uint16_t *>(L.B) + ((size_t)t.s * L.d_out + os) * R;
+    const uint16_t *B = static_cast<const uint16_t *>(L.B) + (size_t)t.s * L.d_out * R;   // the slot's B
     uint16_t *ys = d.ys + b * kTileTokens * kSW;
     uint16_t *bs = d.bs + (size_t)b * kSW * KB * 16;
     if (parts & 1) {
-        // chunk e of the contiguous block: element q = 8 e, row q / R (R a
-        // power of two in 16..64 takes a shift)
-        const int rs = R == 16 ? 4 : (R == 32 ? 5 : (R == 64 ? 6 : 0));
-        for (int e = threadIdx.x; e < (w * R) >> 3; e += kCT) {
-            const int q = e * 8;
-            const int P = rs ? q >> rs : q / R;
-            cp_async16(bs + bsw(P, q - P * R, R), B + q);
+        // rows os .. os + w - 1 of every rank block (blocks of kb ranks, each
+        // [d_out][kb] contiguous): chunk e of a block is row e / (kb / 8),
+        // ranks blk * kb + 8 (e % (kb / 8)) ..
+        const int kb = b_block(R), cpr = kb >> 3, cs = kb == 32 ? 2 : (kb == 16 ? 1 : 0);
+        for (int blk = 0; blk * kb < t.r; ++blk) {           // the slot's blocks (ranks past r: masked)
+            const uint16_t *src = B + ((size_t)blk * L.d_out + os) * kb;
+            for (int e = threadIdx.x; e < w * cpr; e += kCT) {
+                const int P = e >> cs, k = blk * kb + ((e & (cpr - 1)) << 3);
+                cp_async16(bs + bsw(P, k, R), src + (size_t)e * 8);
+            }
         }
     }
     if (parts & 2) {
@@ -425,9 +428,12 @@ decode_cluster_kernel(const __grid_constant__ FusedArgs fa) {
         if (tid < t.cnt)
             prefetch_l2_bulk(static_cast<const uint16_t *>(L.y) + (size_t)sm.tok[tid] * L.d_out + o0,
                              (uint32_t)(o1 - o0) * 2u);
-        if (tid == kCT - 1)
-            prefetch_l2_bulk(static_cast<const uint16_t *>(L.B) + ((size_t)t.s * L.d_out + o0) * R,
-                             (uint32_t)(o1 - o0) * (uint32_t)R * 2u);
+        // rows o0 .. o1 - 1 of each of the slot's rank blocks
+        const int kb = b_block(R), pb = kCT - 1 - tid;
+        if (pb * kb < t.r)
+            prefetch_l2_bulk(static_cast<const uint16_t *>(L.B) + ((size_t)t.s * L.d_out * R +
+                                                                   ((size_t)pb * L.d_out + o0) * kb),
+                             (uint32_t)(o1 - o0) * (uint32_t)kb * 2u);
     }
     bool ok = true;
 

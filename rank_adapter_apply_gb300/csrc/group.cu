@@ -1,7 +1,7 @@
 // Token grouping: turns token_slot_idx into
 //  * prefill tiles: runs (maximal stretches of consecutive tokens with the
 //    same effective slot) of >= min_run tokens, cut into tiles of
-//    kPrefillRows rows (slot, first row, rows), in token order;
+//    kPrefillRows rows (slot, first row, rows, the slot's rank), in token order;
 //  * decode tiles: every other adapter token, grouped by slot (a counting
 //    sort into `perm`), cut into tiles of kTileTokens (slot, perm offset,
 //    count, the slot's rank), slots in increasing order.
@@ -474,7 +474,7 @@ __global__ void __launch_bounds__(kGT, 1) group_tokens_kernel(const __grid_const
             const int end = m ? b0 + p0 + __ffs(m) - 1 : (hi_start != kNoStart ? b0 + hi_start : after);
             const int slot = sm.eff[p0 + j];
             for (int r = s0; r < end; r += kPrefillRows)
-                a.ptiles[hp++] = make_int4(slot, r, end - r < kPrefillRows ? end - r : kPrefillRows, 0);
+                a.ptiles[hp++] = make_int4(slot, r, end - r < kPrefillRows ? end - r : kPrefillRows, sm.rank[slot]);
         }
         // decode tokens at the places claimed above
 #pragma unroll

@@ -41,6 +41,14 @@ int group_max_tokens(int num_sms);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// B pool layout: slot s holds B_s in blocks of kb = b_block(R) consecutive
+// ranks, each block [d_out][kb] contiguous; element (i, k) of slot s at
+// s * d_out * R + (k / kb) * d_out * kb + i * kb + k % kb. A slot of rank r
+// occupies ceil(r / kb) contiguous runs, so reading it touches no padding
+// past them. kb = 32 where max_lora_rank allows it (at rank 32 and below the
+// layout is the plain [d_out][R] one), else 16, else 8.
+__host__ __device__ constexpr int b_block(int R) { return R % 32 == 0 ? 32 : (R % 16 == 0 ? 16 : 8); }
+
 // Launch with programmatic stream serialization: the kernel may be scheduled
 // while the kernel before it in the stream still runs (its launch and ramp-up
 // overlap that kernel's tail). Every kernel launched this way calls

@@ -446,12 +446,15 @@ int lora_load_slot(lora_ctx *c, int slot, const void *const *A_host, const void 
         char *B = static_cast<char *>(L.B_pool) + (size_t)slot * dout * R * e;
         CUDA_TRY(cudaMemcpyAsync(A, A_host[l], r * din * e, cudaMemcpyHostToDevice, c->upload));
         if (r < R) CUDA_TRY(cudaMemsetAsync(A + r * din * e, 0, (R - r) * din * e, c->upload));
-        if (r == R) {
-            CUDA_TRY(cudaMemcpyAsync(B, B_host[l], dout * R * e, cudaMemcpyHostToDevice, c->upload));
-        } else {
-            CUDA_TRY(cudaMemcpy2DAsync(B, R * e, B_host[l], r * e, r * e, dout,
-                                       cudaMemcpyHostToDevice, c->upload));
-            CUDA_TRY(cudaMemset2DAsync(B + r * e, R * e, 0, (R - r) * e, dout, c->upload));
+        // B into the rank-blocked pool layout: one 2D copy per block of
+        // kb ranks (rows of kb elements, the host rows r elements apart);
+        // ranks past r zero
+        const size_t kb = (size_t)b_block(c->R);
+        if (r < R) CUDA_TRY(cudaMemsetAsync(B, 0, dout * R * e, c->upload));
+        for (size_t k0 = 0; k0 < r; k0 += kb) {
+            const size_t w = std::min(kb, r - k0);
+            CUDA_TRY(cudaMemcpy2DAsync(B + k0 * dout * e, kb * e, static_cast<const char *>(B_host[l]) + k0 * e,
+                                       r * e, w * e, dout, cudaMemcpyHostToDevice, c->upload));
         }
         bytes += (din + dout) * r * e;
     }

@@ -85,6 +85,17 @@ __host__ __device__ inline uint32_t tmem_cols_for(int cols) {
 // stages), so lower ranks keep V in shared memory.
 __host__ __device__ constexpr bool expand_v_in_tmem(int R) { return R == 64; }
 
+// Shared-memory descriptor of the B operand for 16-rank K step kk of a stage
+// whose B part (at ba) holds the pool's rank blocks of kBK ranks, each a box
+// of 128 rows x kBK bf16 with the swizzle of its row width.
+template <int R>
+__device__ __forceinline__ uint64_t bdesc(uint32_t ba, int kk) {
+    constexpr int kBK = b_block(R);
+    constexpr uint32_t kBBox = 128 * kBK * 2;
+    constexpr uint32_t kSwzB = kBK == 32 ? tc::kSwz64 : tc::kSwz32;
+    return tc::smem_desc(ba + (uint32_t)(kk / (kBK / 16)) * kBBox + (uint32_t)(kk % (kBK / 16)) * 32, 2 * kBK, kSwzB);
+}
+
 // Row i of a K-major operand of R bf16 per row, in the swizzle the TMA and
 // the MMA descriptors use for that row width: 16-byte chunk c of the row goes
 // to chunk c ^ f(i).
@@ -316,7 +327,7 @@ prefill_shrink_kernel(const __grid_constant__ ShrinkArgs a) {
 struct ExpandArgs {
     CUtensorMap my[kMaxLayersPerCall];        // y [T][d_out], box 64 x 128, 128-byte swizzle (loads)
     CUtensorMap ms[kMaxLayersPerCall];        // the same y, box 64 x 32 (one row quarter's store)
-    CUtensorMap mb[kMaxLayersPerCall];        // B pool [S*d_out][R], box R x 128, rank swizzle
+    CUtensorMap mb[kMaxLayersPerCall];        // B pool as [S*(R/kb)*d_out][kb] (rank blocks), box kb x 128
     const float *part[kMaxLayersPerCall];
     uint16_t *y[kMaxLayersPerCall];
     int d_out[kMaxLayersPerCall], ncb[kMaxLayersPerCall], nch[kMaxLayersPerCall];
@@ -359,7 +370,9 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
 
     constexpr int W = R * 2;                                   // bytes per V / B row
     constexpr uint32_t kSwzRank = R == 64 ? tc::kSwz128 : (R == 32 ? tc::kSwz64 : tc::kSwz32);
-    constexpr uint32_t kStage = 2 * kTileBytes + kNB * W;       // y boxes [2][128][64], B [128][R]
+    constexpr uint32_t kStage = 2 * kTileBytes + kNB * W;       // y boxes [2][128][64], B [R / kBK][128][kBK]
+    constexpr int kBK = b_block(R);                             // ranks per B block of the pool
+    constexpr uint32_t kBBox = kNB * kBK * 2;                   // one block's box: 128 rows
     constexpr uint32_t kVBytes = 128 * W;
     // V in tensor memory (rank 64): after the kAcc accumulators of kNB
     // columns, [2 buffers][hi, lo] of R / 2 columns each (two bf16 per column)
@@ -428,7 +441,10 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
                     if (!wait_ok(&empty[st], ((uint32_t)(j / stages) & 1u) ^ 1u, err)) break;
                     uint8_t *tile = ring + (size_t)st * kStage;
                     const int col = it.cb * kColBlock + b * kNB;
-                    mbar_arrive_expect_tx(&full[st], kStage - 2u * kTileBytes + ybytes);
+                    // B: the rank blocks the tile's slot has (the pool holds B in
+                    // blocks of kBK ranks, each [d_out][kBK])
+                    const int nblk = kBK == R ? 1 : (pt.w + kBK - 1) / kBK;
+                    mbar_arrive_expect_tx(&full[st], (uint32_t)nblk * kBBox + ybytes);
                     if (ny) {
                         for (int q = 0; q < ny; ++q) {
                             tc::tma_load_2d(tile + q * 4096, &a.ms[it.l], col, pt.y + 32 * q, &full[st]);
@@ -439,7 +455,9 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
                         tc::tma_load_2d(tile, &a.my[it.l], col, pt.y, &full[st]);
                         tc::tma_load_2d(tile + kTileBytes, &a.my[it.l], col + 64, pt.y, &full[st]);
                     }
-                    tc::tma_load_2d(tile + 2 * kTileBytes, &a.mb[it.l], 0, pt.x * d_out + col, &full[st]);
+                    for (int kb = 0; kb < nblk; ++kb)
+                        tc::tma_load_2d(tile + 2 * kTileBytes + kb * kBBox, &a.mb[it.l], 0,
+                                        (pt.x * (R / kBK) + kb) * d_out + col, &full[st]);
                     ++j;
                 }
             }
@@ -450,12 +468,16 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
         if (lane == 0) {
             // ---------------- MMA issuer ----------------
             constexpr uint32_t idesc = tc::idesc_bf16(128, kNB);
-            int j = 0, gen = -1, pl = -1, pp = -1;
+            int j = 0, gen = -1, pl = -1, pp = -1, nkb = R / 16;
             for (int k = k0; k < k1 && !*err; ++k) {
                 const Item it = item_at(a, k, np);
                 if (it.l != pl || it.p != pp) {
                     ++gen;
                     pl = it.l;
+                    // the slot's 16-rank MMA steps (its rank from the tile
+                    // list, loaded while the wait for this tile's V runs)
+                    // (up to rank 32 the pool's one block holds every rank: all steps)
+                    if (kBK < R && it.p != pp) nkb = (a.ptiles[it.p].w + 15) >> 4;
                     pp = it.p;
                     if (!wait_ok(&v_full[gen & 1], (uint32_t)(gen >> 1) & 1u, err)) break;
                     tc::fence_after_sync();
@@ -472,23 +494,32 @@ prefill_expand_kernel(const __grid_constant__ ExpandArgs a) {
                     tc::fence_after_sync();
                     const uint32_t ba = smem_u32(ring + (size_t)st * kStage + 2 * kTileBytes);
                     const uint32_t d = tmem + (uint32_t)kNB * ac;
+                    // B for K step kk: block kk / (kBK / 16) of [128 rows][kBK ranks]
+                    // (rows of 2 kBK bytes, swizzled across them), 32 bytes in; V
+                    // columns past the slot's rank are zero, so steps past nkb
+                    // (their blocks possibly not loaded) are skipped
                     if constexpr (kVTmem) {
 #pragma unroll
                         for (int kk = 0; kk < R / 16; ++kk)
-                            tc::mma_bf16_tmem_a(d, vh + kk * 8, tc::smem_desc(ba + kk * 32, W, kSwzRank), idesc,
-                                                kk != 0);
+                            if (kk < nkb)
+                                tc::mma_bf16_tmem_a(d, vh + kk * 8, bdesc<R>(ba, kk),
+                                                    idesc, kk != 0);
 #pragma unroll
                         for (int kk = 0; kk < R / 16; ++kk)
-                            tc::mma_bf16_tmem_a(d, vl + kk * 8, tc::smem_desc(ba + kk * 32, W, kSwzRank), idesc, 1);
+                            if (kk < nkb)
+                                tc::mma_bf16_tmem_a(d, vl + kk * 8, bdesc<R>(ba, kk),
+                                                    idesc, 1);
                     } else {
 #pragma unroll
                         for (int kk = 0; kk < R / 16; ++kk)
-                            tc::mma_bf16(d, tc::smem_desc(vh + kk * 32, W, kSwzRank),
-                                         tc::smem_desc(ba + kk * 32, W, kSwzRank), idesc, kk != 0);
+                            if (kk < nkb)
+                                tc::mma_bf16(d, tc::smem_desc(vh + kk * 32, W, kSwzRank),
+                                             bdesc<R>(ba, kk), idesc, kk != 0);
 #pragma unroll
                         for (int kk = 0; kk < R / 16; ++kk)
-                            tc::mma_bf16(d, tc::smem_desc(vl + kk * 32, W, kSwzRank),
-                                         tc::smem_desc(ba + kk * 32, W, kSwzRank), idesc, 1);
+                            if (kk < nkb)
+                                tc::mma_bf16(d, tc::smem_desc(vl + kk * 32, W, kSwzRank),
+                                             bdesc<R>(ba, kk), idesc, 1);
                     }
                     tc::mma_commit(&acc_full[ac]);
                     ++j;
@@ -901,15 +932,15 @@ cudaError_t launch_prefill_tc(const PrefillLayer *L, int n, int T, int S, int R,
     ra.T = T;
     ra.R = R;
 
-    const CUtensorMapSwizzle swz_rank = R == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
-                                      : (R == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
     ea.n = n;
     ea.sum_ncb = 0;
     for (int i = 0; i < n; ++i) {
         if (L[i].d_out % 64 != 0) return cudaErrorInvalidValue;
         if (!encode_2d(&ea.my[i], L[i].y, (uint64_t)L[i].d_out, (uint64_t)T, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
             !encode_2d(&ea.ms[i], L[i].y, (uint64_t)L[i].d_out, (uint64_t)T, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_2d(&ea.mb[i], L[i].B, (uint64_t)R, (uint64_t)S * L[i].d_out, (uint32_t)R, kNB, swz_rank))
+            !encode_2d(&ea.mb[i], L[i].B, (uint64_t)b_block(R), (uint64_t)S * (R / b_block(R)) * L[i].d_out,
+                       (uint32_t)b_block(R), kNB,
+                       b_block(R) == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B))
             return cudaErrorInvalidValue;
         ea.part[i] = L[i].part;
         ea.y[i] = static_cast<uint16_t *>(L[i].y);

@@ -11,8 +11,9 @@
 //
 // Work units (host-computed prefix sums): per entry, 16 KB chunks of the
 // A region [R][d_in] (source rows r x d_in contiguous, the rest zero) and
-// blocks of 64 rows of the B region [d_out][R] (source rows of r elements,
-// the rest of each row zero).
+// blocks of 64 rows of B (source rows of r elements, [d_out][r]) written
+// into the pool's rank-blocked layout (blocks of b_block(R) ranks, each
+// [d_out][b_block(R)]; ranks past r zero).
 #include "kernels.cuh"
 
 #include <cuda_runtime.h>
@@ -63,6 +64,7 @@ upload_slots_kernel(const __grid_constant__ UploadArgs a) {
         const int p1 = p0 + kBRows < e.d_out ? p0 + kBRows : e.d_out;
         const int row_chunks = (int)((size_t)a.R * es / 16);     // 16-byte chunks per slot row
         const int src_chunks = (int)((size_t)e.r * es / 16);
+        const int bchunks = (int)((size_t)b_block(a.R) * es / 16); // 16-byte chunks per block row
         const char *src = static_cast<const char *>(e.B_src);
         char *dst = static_cast<char *>(e.B_dst);
         const int total = (p1 - p0) * row_chunks;
@@ -70,7 +72,9 @@ upload_slots_kernel(const __grid_constant__ UploadArgs a) {
         for (int i = threadIdx.x; i < total; i += kThreads) {
             const int p = p0 + i / row_chunks, c = i % row_chunks;
             const uint4 v = c < src_chunks ? ld_host16(src + ((size_t)p * src_chunks + c) * 16) : zero;
-            *reinterpret_cast<uint4 *>(dst + ((size_t)p * row_chunks + c) * 16) = v;
+            // chunk c of row p: rank block c / bchunks, chunk c % bchunks of its row there
+            const int blk = c / bchunks, w = c - blk * bchunks;
+            *reinterpret_cast<uint4 *>(dst + (((size_t)blk * e.d_out + p) * bchunks + w) * 16) = v;
         }
     }
     // The scale and rank of every slot of the call, once.

@@ -442,8 +442,9 @@ def test_batched_upload_matches_oracle(dtype):
     """lora_load_slots: adapters of several ranks (zero padding up to R) in one
     call, pinned buffers read by the upload kernel plus one pageable adapter
     (read by the kernel too where the GPU walks the host's page tables, else
-    taken by the copy-engine path); then the delta equals the oracle's, and
-    padding rows of a slot that held a larger rank before are zero again."""
+    taken by the copy-engine path); then the delta equals the oracle's,
+    padding rows of a slot that held a larger rank before are zero again, and
+    every slot's B sits in the pool's rank-blocked layout bit for bit."""
     import torch
     from rank_adapter_apply_gb300.harness import to_torch, from_torch
     from rank_adapter_apply_gb300.slots import LoraSlots
@@ -485,7 +486,14 @@ def test_batched_upload_matches_oracle(dtype):
         A_pool = from_torch(sl.A[0])
         B_pool = from_torch(sl.B[0])
         assert not A_pool[1, 8:].any()                   # rank 8 now: rows 8..31 zero again
-        assert not B_pool[1, :, 8:].any()
+        # B pool of a slot: blocks of kb ranks, each [d_out][kb] (kb = 32 at
+        # max_lora_rank 32: the plain [d_out][R] layout)
+        kb = 32 if R % 32 == 0 else (16 if R % 16 == 0 else 8)
+        for s in range(S):
+            Bs = B_pool[s].reshape(R // kb, d_out, kb).transpose(1, 0, 2).reshape(d_out, R)
+            r = ranks[s]
+            assert np.array_equal(Bs[:, :r].view(np.uint8), np.ascontiguousarray(ads[s]["l0"][1]).view(np.uint8))
+            assert not Bs[:, r:].any()
     finally:
         sl.close()
 
