@@ -34,15 +34,15 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kExpandCols = 256;          // output columns per expand CTA (bf16 and fp32)
 
 // v of the bf16 path, kept in the order the expand's MMA fragments read it:
-// row `pos` of R x 4 bytes holds, for every four ranks k0 .. k0 + 3 (k0 a
+// row `pos` of VS = v_stride(R) floats holds, for every four ranks k0 .. k0 + 3 (k0 a
 // multiple of 4), one 16-byte group: the bf16 high parts of the four ranks,
 // then their bf16 low parts (value - high part), lower rank first. The
 // expand then loads a fragment with one 16-byte load per row instead of
 // splitting fp32 values for every 256-column block it covers.
-__device__ __forceinline__ void store_vfrag(float *v, int R, int pos, int k, float s) {
+__device__ __forceinline__ void store_vfrag(float *v, int VS, int pos, int k, float s) {
     const __nv_bfloat16 h = __float2bfloat16_rn(s);
     const __nv_bfloat16 l = __float2bfloat16_rn(s - __bfloat162float(h));
-    __nv_bfloat16 *grp = reinterpret_cast<__nv_bfloat16 *>(v + (size_t)pos * R) + (k >> 2) * 8;
+    __nv_bfloat16 *grp = reinterpret_cast<__nv_bfloat16 *>(v + (size_t)pos * VS) + (k >> 2) * 8;
     grp[k & 3] = h;
     grp[4 + (k & 3)] = l;
 }
@@ -83,7 +83,7 @@ __device__ void finish_split(const LayerArgs &L, const GroupView &g, int tile_i,
             for (int u = 0; u < 8; ++u) s += a[u];
         }
         for (; ch < L.n_chunks; ++ch) s += __ldcg(src + (size_t)ch * cs);
-        if (frag) store_vfrag(L.v, R, pos, k, s);
+        if (frag) store_vfrag(L.v, v_stride(R), pos, k, s);
         else L.v[(size_t)pos * R + k] = s;
     }
     if (threadIdx.x == 0) L.counters[tile_i] = 0;
@@ -229,7 +229,7 @@ __device__ __forceinline__ void shrink_bf16_tile(const LayerArgs &L, const Group
         const int tk = n * 8 + 2 * (ln & 3) + (j & 1);
         if (tk < cnt) {
             if (split) part[(size_t)(p0 + tk) * R + k] = v;
-            else store_vfrag(L.v, R, p0 + tk, k, v);
+            else store_vfrag(L.v, v_stride(R), p0 + tk, k, v);
         }
     }
     if (split) finish_split(L, g, tile_i, p0, cnt, 16 * nmb, true);
@@ -253,7 +253,7 @@ __device__ __forceinline__ void expand_bf16_run(const LayerArgs &L, const GroupV
     const int r = head.w;                      // the slot's rank, from the grouping
     const int nkb = (r + 15) >> 4;
     const float scale = g.scale[s];
-    const int R = g.R;
+    const int R = g.R, VS = v_stride(R);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
 
     // This block's B rows (the slot's first 16 * nkb ranks) go to shared memory
@@ -268,11 +268,17 @@ __device__ __forceinline__ void expand_bf16_run(const LayerArgs &L, const GroupV
     const int c0 = dblock * kExpandCols;
     {
         const int ch = threadIdx.x & 7;
+        const int rows = min(kExpandCols, d_out - c0);
         if (ch < 2 * nkb && ch * 8 < R) {
-            const int kb = b_block(R), rows = min(kExpandCols, d_out - c0);
+            const int kb = b_block(R);
             const uint16_t *src = Bs + ((size_t)((ch * 8) / kb) * d_out + c0) * kb + (ch * 8) % kb;
             for (int P = threadIdx.x >> 3; P < rows; P += kThreads / 8)
                 cp_async16(bs + P * 64 + ((ch ^ bkey(P)) << 3), src + (size_t)P * kb);
+        } else if (ch < 2 * nkb) {
+            // ranks past max_lora_rank inside the last 16-rank block: zeros
+            // (the MMA multiplies them with v's zero ranks)
+            for (int P = threadIdx.x >> 3; P < rows; P += kThreads / 8)
+                *reinterpret_cast<uint4 *>(bs + P * 64 + ((ch ^ bkey(P)) << 3)) = make_uint4(0, 0, 0, 0);
         }
         cp_async_commit();
     }
@@ -299,8 +305,8 @@ __device__ __forceinline__ void expand_bf16_run(const LayerArgs &L, const GroupV
             if (kb >= nkb) break;
             const int grp = kb * 4 + tq;                 // ranks 4 grp .. 4 grp + 3
             uint4 q0 = make_uint4(0, 0, 0, 0), q1 = make_uint4(0, 0, 0, 0);
-            if (gq < cnt) q0 = *reinterpret_cast<const uint4 *>(L.v + (size_t)(p0 + gq) * R + grp * 4);
-            if (gq + 8 < cnt) q1 = *reinterpret_cast<const uint4 *>(L.v + (size_t)(p0 + gq + 8) * R + grp * 4);
+            if (gq < cnt) q0 = *reinterpret_cast<const uint4 *>(L.v + (size_t)(p0 + gq) * VS + grp * 4);
+            if (gq + 8 < cnt) q1 = *reinterpret_cast<const uint4 *>(L.v + (size_t)(p0 + gq + 8) * VS + grp * 4);
             ahi[kb][0] = q0.x;
             ahi[kb][1] = q1.x;
             ahi[kb][2] = q0.y;

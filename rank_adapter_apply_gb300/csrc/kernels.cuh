@@ -49,6 +49,10 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // layout is the plain [d_out][R] one), else 16, else 8.
 __host__ __device__ constexpr int b_block(int R) { return R % 32 == 0 ? 32 : (R % 16 == 0 ? 16 : 8); }
 
+// Row stride (floats) of the decode path's v: whole 16-rank blocks, which the
+// bf16 path stores in MMA fragment order (the fp32 path uses the first R).
+__host__ __device__ constexpr int v_stride(int R) { return (R + 15) / 16 * 16; }
+
 // Launch with programmatic stream serialization: the kernel may be scheduled
 // while the kernel before it in the stream still runs (its launch and ramp-up
 // overlap that kernel's tail). Every kernel launched this way calls
@@ -104,7 +108,7 @@ inline WsLayout ws_layout(int S, int R, int max_tokens, int max_layers) {
     w.tiles = take((size_t)w.max_tiles * sizeof(int4));
     w.ptiles = take((size_t)w.max_ptiles * sizeof(int4));
     w.counters = take((size_t)max_layers * w.max_tiles * sizeof(int));
-    w.v = take((size_t)max_layers * T * R * sizeof(float));
+    w.v = take((size_t)max_layers * T * v_stride(R) * sizeof(float));
     w.part = take((size_t)max_layers * w.part_rows * R * sizeof(float));
     // The decode kernels' own partials: they run beside the prefill kernels
     // (which use `part`) on a second stream.

@@ -719,7 +719,7 @@ int apply_impl(lora_ctx *c, int n, const int *layers, const void *const *xs, voi
         a.B = L.B_pool;
         a.d_in = L.d_in;
         a.d_out = L.d_out;
-        a.v = reinterpret_cast<float *>(c->ws + c->lay.v) + (size_t)i * c->lay.max_tokens * c->R;
+        a.v = reinterpret_cast<float *>(c->ws + c->lay.v) + (size_t)i * c->lay.max_tokens * v_stride(c->R);
         a.part = reinterpret_cast<float *>(c->ws + c->lay.dpart) + (size_t)i * c->lay.part_rows * c->R;
         a.counters = reinterpret_cast<int *>(c->ws + c->lay.counters) + (size_t)i * c->lay.max_tiles;
         // Split d_in into chunks of ~256 columns so that a tile's shrink is

@@ -69,7 +69,7 @@ def test_small_and_ragged_token_counts(T):
 
 @pytest.mark.parametrize("d_in,d_out,R,early", [(1032, 1000, 16, True), (1032, 1000, 16, False),
                                                   (4096, 4104, 16, True), (512, 4096, 32, True),
-                                                  (768, 2056, 64, True)])
+                                                  (768, 2056, 64, True), (768, 2056, 48, False)])
 def test_cluster_decode_partial_stages(d_in, d_out, R, early):
     """Small-batch cluster kernel with column slices that end inside a stage:
     d_out up to 4096 takes the short path (products before the wait on the
@@ -219,6 +219,20 @@ def test_max_rank_64_mixed(small_batch):
     ranks = [8, 16, 32, 64, 48, 24]
     idx = rng.integers(0, 6, size=T)
     w = _custom(T, 1024, 512, 6, 64, ranks, idx)
+    out, _ = _run(w, small_batch_tokens=small_batch)
+    check_layer(w, "l0", out["l0"])
+
+
+@pytest.mark.parametrize("R,small_batch", [(48, 0), (48, 1024), (40, 0)])
+def test_rank_blocked_pools_of_16_and_8(R, small_batch):
+    """max_lora_rank 48 keeps B in three blocks of 16 ranks and 40 in five blocks
+    of 8: the grouped kernels (small_batch 0) and the cluster kernel read only
+    the blocks a slot's rank covers, ranks of every size inside them."""
+    T = 80
+    rng = np.random.default_rng(R)
+    ranks = [R, 20, 8, 33, 16, 1]
+    idx = rng.integers(-1, 6, size=T)
+    w = _custom(T, 640, 384, 6, R, ranks, idx, seed=R + 3)
     out, _ = _run(w, small_batch_tokens=small_batch)
     check_layer(w, "l0", out["l0"])
 
