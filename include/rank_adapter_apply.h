@@ -298,8 +298,9 @@ int lora_set_warm_set(lora_ctx *ctx, int n, const uint64_t *ids);
  * of first appearance, are cut into groups that fit the slots (max_loras
  * adapters per batch, section 核心原理 of the "Multi-LoRA 适配器缓存生产实战"
  * page): each adapter needs a slot except one already resident in a pinned
- * slot, and a group takes at most max_loras minus the slots pinned when the
- * step starts. Group after group:
+ * slot, and the first group takes at most max_loras minus the slots pinned
+ * when the step starts; each later group takes that many minus the warm-set
+ * adapters pinned by the groups before it (step 1). Group after group:
  *   1. each adapter is admitted as by lora_assign (hit: touch; miss: lowest
  *      free slot or the policy's victim among slots not in flight, pinned or
  *      cooling) and taken in flight (lora_acquire); warm-set adapters are

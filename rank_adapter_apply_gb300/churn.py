@@ -42,30 +42,36 @@ from .slots import LoraSlots
 KEEP_PIN32 = {"policy": 1, "weights": (1.0, 1.0, 0.0, 0.0, 0.0), "pin_top": 32, "window": 40}
 
 
-def plan_groups(order, pinned_resident, capacity):
+def plan_groups(order, pinned_resident, capacity, warm=()):
     """Split a step's distinct adapters (first-appearance order) into groups:
     every adapter not already resident in a pinned slot needs one of
-    `capacity` evictable slots (max_loras minus the pinned ones)."""
-    groups, cur, cost = [], [], 0
+    `capacity` evictable slots (max_loras minus the pinned ones). A warm-set
+    adapter outside the pinned slots pins its slot when its group is
+    admitted, which leaves one evictable slot fewer to every later group."""
+    groups, cur, cost, new_pins = [], [], 0, 0
     for a in order:
         c = 0 if a in pinned_resident else 1
         if cur and cost + c > capacity:
             groups.append(cur)
             cur, cost = [], 0
+            capacity -= new_pins
+            new_pins = 0
         cur.append(a)
         cost += c
+        if c and a in warm:
+            new_pins += 1
     if cur:
         groups.append(cur)
     return groups
 
 
-def plan_step(ids, pinned_resident, capacity):
+def plan_step(ids, pinned_resident, capacity, warm=()):
     """A step's distinct adapters in first-appearance order, cut into groups by
     plan_groups, and the group of every token (numpy int32 per token). Plain
     dict passes over the few hundred tokens of a step: cheaper than sorting
     them with numpy."""
     ids_l = np.asarray(ids).tolist()
-    groups = plan_groups(list(dict.fromkeys(ids_l)), pinned_resident, capacity)
+    groups = plan_groups(list(dict.fromkeys(ids_l)), pinned_resident, capacity, warm)
     group_of = {a: gi for gi, g in enumerate(groups) for a in g}
     return groups, np.fromiter(map(group_of.__getitem__, ids_l), dtype=np.int32, count=len(ids_l))
 

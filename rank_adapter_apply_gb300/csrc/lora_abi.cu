@@ -1080,13 +1080,15 @@ int lora_serve_step(lora_ctx *c, int T, const uint64_t *adapter_ids, int n, cons
     if (max_distinct > 0 && nd > max_distinct)
         return fail(LORA_ERR_ARG, "more than max_distinct (%d) adapters in the batch", max_distinct);
     // Groups: at most max_loras minus the pinned slots need a slot each; an
-    // adapter resident in a pinned slot needs none.
+    // adapter resident in a pinned slot needs none. A warm-set adapter not in
+    // a pinned slot pins its slot when its group is admitted, so every later
+    // group has one evictable slot fewer.
     int pinned = 0;
     for (int s = 0; s < c->S; ++s) pinned += c->table.pinned(s) ? 1 : 0;
-    const int capacity = c->S - pinned;
+    int capacity = c->S - pinned;
     std::vector<int> &grp = c->step_group;
     grp.resize((size_t)nd);
-    int ng = 0, cost = 0, in_cur = 0;
+    int ng = 0, cost = 0, in_cur = 0, new_pins = 0;
     for (int i = 0; i < nd; ++i) {
         const int s = c->table.find(dist[i]);
         const int k = (s >= 0 && c->table.pinned(s)) ? 0 : 1;
@@ -1094,10 +1096,13 @@ int lora_serve_step(lora_ctx *c, int T, const uint64_t *adapter_ids, int n, cons
             ++ng;
             cost = 0;
             in_cur = 0;
+            capacity -= new_pins;
+            new_pins = 0;
         }
         grp[i] = ng;
         cost += k;
         ++in_cur;
+        if (k && c->warm.count(dist[i])) ++new_pins;
     }
     if (nd > 0) ++ng;
     if (c->device && ng > max_groups)

@@ -589,26 +589,26 @@ def _serve(ctx, ids, max_distinct=None):
     return rc, dec, ng.value
 
 
-def test_serve_step_groups_and_decisions_match_simulator(lib):
-    """A step with more distinct adapters than slots is cut into groups in
-    first-appearance order (a warm-set adapter resident in a pinned slot needs
-    no slot); each adapter's admission, in order, equals the simulator's; the
-    epoch advances once per step; base-model tokens are skipped."""
+def _serve_against_simulator(S, warm, steps):
+    """Serve `steps` on a host-only context with warm set `warm` and replay
+    them on the simulator, group by group as churn.plan_groups cuts them;
+    every step must succeed with the simulator's decisions. Returns the
+    number of groups of each step."""
     from oracle.lru_sim import LruSlotSim
     from rank_adapter_apply_gb300 import churn
-    S, R = 4, 16
+    R = 16
     ctx = _host_ctx(S, R)
     sim = LruSlotSim(S, R)
+    n_groups = []
     try:
         B.lora_register_host_adapters(ctx, list(range(20)), [8] * 20, [16.0] * 20)
-        B.lora_set_warm_set(ctx, [0])
+        B.lora_set_warm_set(ctx, list(warm))
         pinned = {}
-        steps = [[0, 1, 2, B.NO_ID, 1, 3], [4, 5, 0, 6, 7, 8, 5, 9, 10], [0, 11, 12, 13, 14, 15, 16, 17, 0]]
         for k, ids in enumerate(steps):
             rc, dec, ng = _serve(ctx, ids)
-            assert rc == 0, B.last_error()
+            assert rc == 0, (k, B.last_error())
             order = list(dict.fromkeys(a for a in ids if a != B.NO_ID))
-            groups = churn.plan_groups(order, pinned, S - len(pinned))
+            groups = churn.plan_groups(order, pinned, S - len(pinned), set(warm))
             exp = []
             for group in groups:
                 held = []
@@ -616,7 +616,7 @@ def test_serve_step_groups_and_decisions_match_simulator(lib):
                     st, slot, need, ev = sim.assign(a, 8)
                     assert st == 0
                     exp.append((a, slot, need, ev))
-                    if a == 0 and a not in pinned:
+                    if a in warm and a not in pinned:
                         sim.pin(slot)
                         pinned[a] = slot
                     sim.acquire(slot)
@@ -625,11 +625,33 @@ def test_serve_step_groups_and_decisions_match_simulator(lib):
                     sim.release(s_)
             sim.tick()
             assert dec == exp and ng == len(groups), (k, dec, exp)
+            n_groups.append(ng)
         st = B.lora_stats(ctx)
-        assert (st["hits"], st["misses"], st["evictions"], st["epoch"]) == (sim.hits, sim.misses, sim.evictions, 3)
+        assert (st["hits"], st["misses"], st["evictions"], st["epoch"]) == \
+            (sim.hits, sim.misses, sim.evictions, len(steps))
         assert st["uploads"] == sim.misses                  # host-only: uploads are recorded
     finally:
         B.lora_destroy(ctx)
+    return n_groups
+
+
+def test_serve_step_groups_and_decisions_match_simulator(lib):
+    """A step with more distinct adapters than slots is cut into groups in
+    first-appearance order (a warm-set adapter resident in a pinned slot needs
+    no slot); each adapter's admission, in order, equals the simulator's; the
+    epoch advances once per step; base-model tokens are skipped."""
+    steps = [[0, 1, 2, B.NO_ID, 1, 3], [4, 5, 0, 6, 7, 8, 5, 9, 10], [0, 11, 12, 13, 14, 15, 16, 17, 0]]
+    _serve_against_simulator(4, [0], steps)
+
+
+def test_serve_step_warm_pins_leave_later_groups_fewer_slots(lib):
+    """Warm-set adapters bound by a step's first group pin their slots, so the
+    next group has that many evictable slots fewer: 4 slots, warm set {0, 1},
+    seven new adapters in one step are served in groups of 4, 2 and 1 (cut
+    at the start-of-step count, 4 and 3, the second group would find only two
+    evictable slots and fail); later steps keep the two pinned slots."""
+    steps = [[0, 1, 2, 3, 4, 5, 6], [7, 0, 8, 9, 1, 10], [11, 12, 13, 14, 15]]
+    assert _serve_against_simulator(4, [0, 1], steps) == [3, 2, 3]
 
 
 def test_serve_step_rejects_before_any_admission(lib):

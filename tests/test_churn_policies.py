@@ -26,7 +26,7 @@ def _sim_replay(trace, S, R, policy, weights, pin_top, window=10):
     pinned, log = {}, []
     for k, ids in enumerate(trace.steps):
         order = list(dict.fromkeys(int(a) for a in ids))
-        for group in churn.plan_groups(order, pinned, S - len(pinned)):
+        for group in churn.plan_groups(order, pinned, S - len(pinned), set(range(pin_top))):
             held = []
             for a in group:
                 st, slot, need, ev = sim.assign(a, R)
@@ -61,6 +61,9 @@ def test_plan_groups_respects_pinned_slots():
     assert churn.plan_groups(order, {}, 4) == [[0, 1, 2, 3], [4, 5, 6, 7], [8, 9]]
     # 0 and 1 sit in pinned slots: they cost nothing, capacity counts the rest
     assert churn.plan_groups(order, {0: 0, 1: 1}, 3) == [[0, 1, 2, 3, 4], [5, 6, 7], [8, 9]]
+    # 2 and 5 are warm and not yet pinned: each takes one evictable slot from
+    # every group after its own
+    assert churn.plan_groups(order, {}, 4, {2, 5}) == [[0, 1, 2, 3], [4, 5, 6], [7, 8], [9]]
 
 
 def test_policies_beat_pure_lru_on_the_churn_trace():
