@@ -223,6 +223,46 @@ def test_max_rank_64_mixed(small_batch):
     check_layer(w, "l0", out["l0"])
 
 
+@pytest.mark.parametrize("R", [256, 200])
+def test_fp32_largest_ranks(R):
+    """fp32 takes max_lora_rank up to 256: the grouped kernels at 256 (B in
+    blocks of 32 ranks) and at 200 (blocks of 8), slot ranks from 1 to R,
+    d_in split into several chunks, ragged tails of tokens and columns."""
+    T = 70
+    rng = np.random.default_rng(R + 1)
+    ranks = [R, 1, 130, 17, 64]
+    idx = rng.integers(-1, 5, size=T)
+    w = _custom(T, 1100, 300, 5, R, ranks, idx, dtype=wl.DTYPE_F32, seed=R)
+    out, _ = _run(w)
+    check_layer(w, "l0", out["l0"])
+
+
+def _runs_over_slots(rng, T, S, long_p):
+    """Slot ids as runs: with probability long_p a run of 64-200 tokens, else
+    1-8 tokens; slots uniform over S, one in ten runs base-only."""
+    idx = []
+    while len(idx) < T:
+        n = int(rng.integers(64, 201)) if rng.random() < long_p else int(rng.integers(1, 9))
+        s = -1 if rng.random() < 0.1 else int(rng.integers(0, S))
+        idx += [s] * n
+    return np.array(idx[:T], np.int32)
+
+
+@pytest.mark.parametrize("T,long_p", [(600, 0.0), (5000, 0.05)])
+def test_max_loras_256(T, long_p):
+    """max_loras at its limit (256 slots, every one bound): the cluster decode
+    kernel takes at most 255 slots, so even a small batch takes the grouped
+    kernels; a batch of two grouping blocks adds tensor-core prefill runs."""
+    S = 256
+    rng = np.random.default_rng(T)
+    ranks = rng.integers(1, 17, size=S)
+    idx = _runs_over_slots(rng, T, S, long_p)
+    w = _custom(T, 256, 192, S, 16, ranks, idx, seed=5)
+    out, st = _run(w)
+    check_layer(w, "l0", out["l0"])
+    assert st["cluster_applies"] == 0 and st["grouped_applies"] >= 1
+
+
 @pytest.mark.parametrize("R,small_batch", [(48, 0), (48, 1024), (40, 0)])
 def test_rank_blocked_pools_of_16_and_8(R, small_batch):
     """max_lora_rank 48 keeps B in three blocks of 16 ranks and 40 in five blocks
