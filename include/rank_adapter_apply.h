@@ -320,8 +320,10 @@ int lora_set_warm_set(lora_ctx *ctx, int n, const uint64_t *ids);
  * Errors before any admission leave the table unchanged: an unregistered id,
  * more than max_distinct adapters, more than max_groups groups (device
  * contexts), bad arguments. A failed admission (LORA_ERR_NO_SLOT) or upload
- * returns its status after releasing the references of its group; the groups
- * before it were applied and released, and the epoch does not advance.
+ * returns its status after releasing the references of its group (the misses
+ * the group bound before a failed admission are still uploaded, so no slot is
+ * left bound without its weights); the groups before it were applied and
+ * released, and the epoch does not advance.
  * On a host-only context only the admission runs (uploads are recorded as by
  * lora_load_slot there; layers, xs, ys and idx_bufs may be NULL).
  */

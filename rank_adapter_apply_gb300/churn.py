@@ -196,47 +196,57 @@ class ChurnRunner:
         # kernels read; a ring slot is reused only after its step has finished
         self.max_groups = (tokens + max(1, max_loras - pin_top) - 1) // max(1, max_loras - pin_top)
         self.idx_host = torch.empty((self.ring, self.max_groups, tokens), dtype=torch.int32).pin_memory()
-        self.step_done = [None] * self.ring
+        self.step_done = [False] * self.ring     # ring slot's event recorded and not yet waited for
         self._lay = B._i32_array([0, 1])
         self._xs = B._vp_array([self.x.data_ptr()] * 2)
         self._ys = B._vp_array([t.data_ptr() for t in self.y])
         self._out = _serve_outputs(tokens)
+        # per ring slot: the step's adapter ids as the ABI takes them, the
+        # address of its slot-id buffers, and an event marking its kernels
+        self._ids = [(ctypes.c_uint64 * tokens)() for _ in range(self.ring)]
+        self._ids_np = [np.frombuffer(b, dtype=np.uint64) for b in self._ids]
+        self._idx_ptr = [self.idx_host[rb].data_ptr() for rb in range(self.ring)]
+        self._events = [torch.cuda.Event() for _ in range(self.ring)]
 
     def run(self, trace: wl.ChurnTrace, record=False, reset_y=True, check_step=None):
         """Run every step of the trace; returns ChurnResult. With check_step=k
         the outputs of step k (y after that step, starting from the base
         outputs) are kept in self.checked = (ids, slot_of_token, y_q, y_v)."""
         decisions = []
-        tokens = 0
         ctx = self.slots.ctx
-        lib = B.load()
+        serve = B.load().lora_serve_step
         out = self._out
-        u64p = ctypes.POINTER(ctypes.c_uint64)
+        n_dist, n_grp = ctypes.byref(out[4]), ctypes.byref(out[5])
+        compute = self.slots.compute
+        # adapter tokens of the trace (the metric's count, not work of a step)
+        no_id = np.uint64(B.NO_ID)
+        tokens = sum(int(np.count_nonzero(np.asarray(ids, dtype=np.uint64) != no_id)) for ids in trace.steps)
         torch.cuda.synchronize(self.dev)
         t0 = time.perf_counter()
         for k, ids in enumerate(trace.steps):
             rb = k % self.ring
-            if self.step_done[rb] is not None:
-                self.step_done[rb].synchronize()          # this step's slot-id buffers are free
+            if self.step_done[rb]:
+                self._events[rb].synchronize()          # this step's slot-id buffers are free
+                self.step_done[rb] = False
             if reset_y or k == check_step:
-                with torch.cuda.stream(self.slots.compute):
+                with torch.cuda.stream(compute):
                     for y, y0 in zip(self.y, self.y0):
                         y.copy_(y0)
-            ids_u = np.ascontiguousarray(ids, dtype=np.uint64)
-            rc = lib.lora_serve_step(ctx, len(ids_u), ids_u.ctypes.data_as(u64p), 2, self._lay, self._xs,
-                                     self._ys, self.idx_host[rb].data_ptr(), self.max_groups, self.T,
-                                     out[0], out[1], out[2], out[3], ctypes.byref(out[4]), ctypes.byref(out[5]))
+            n_ids = len(ids)
+            self._ids_np[rb][:n_ids] = ids
+            rc = serve(ctx, n_ids, self._ids[rb], 2, self._lay, self._xs, self._ys, self._idx_ptr[rb],
+                       self.max_groups, self.T, out[0], out[1], out[2], out[3], n_dist, n_grp)
             if rc != 0:
                 raise RuntimeError(f"step {k}: {B.last_error()}")
             n = out[4].value
             if record:
                 decisions += _decisions(k, out, n)
-            tokens += int((ids_u != np.uint64(B.NO_ID)).sum())
-            ev = torch.cuda.Event()
-            ev.record(self.slots.compute)
-            self.step_done[rb] = ev
+            ev = self._events[rb]
+            ev.record(compute)
             if not self.overlap or k == check_step:
                 ev.synchronize()                    # slot-id buffers are reused next step
+            else:
+                self.step_done[rb] = True
             if k == check_step:
                 slot_of = {int(out[0][i]): int(out[1][i]) for i in range(n)}
                 slot_tok = np.array([slot_of.get(int(a), -1) for a in ids], np.int32)

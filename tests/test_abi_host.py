@@ -677,6 +677,32 @@ def test_serve_step_rejects_before_any_admission(lib):
         B.lora_destroy(ctx)
 
 
+def test_serve_step_failed_admission_uploads_the_bound_misses(lib):
+    """A group whose second admission fails: the miss bound before it is still
+    uploaded (its slot is loaded, so lora_abort_load refuses it and a later
+    step finds it resident with its weights), every reference of the step is
+    released, the epoch stays."""
+    ctx = _host_ctx(2, 16)
+    try:
+        B.lora_register_host_adapters(ctx, [1, 2, 3], [8, 8, 8], [16.0] * 3)
+        st, held, need, ev = B.lora_assign(ctx, 1, 8)
+        B.lora_acquire(ctx, held)                                     # slot of 1 in flight elsewhere
+        up0 = B.lora_stats(ctx)["uploads"]
+        rc, dec, ng = _serve(ctx, [2, 3])                             # 2 binds the free slot, 3 finds none
+        assert rc == B.LORA_ERR_NO_SLOT
+        slot2 = B.lora_lookup(ctx, 2)
+        assert slot2 >= 0 and slot2 != held and B.lora_lookup(ctx, 3) == -1
+        assert B.lora_stats(ctx)["uploads"] == up0 + 1
+        assert B.lora_abort_load(ctx, slot2)[0] == B.LORA_ERR_STATE    # loaded, not pending
+        assert B.lora_release(ctx, slot2) == B.LORA_ERR_STATE          # the step's reference is gone
+        assert B.lora_stats(ctx)["epoch"] == 0
+        assert B.lora_release(ctx, held) == 0
+        rc, dec, ng = _serve(ctx, [2, 3])                             # now both fit
+        assert rc == 0 and [d[2] for d in dec] == [0, 1]              # 2 resident (hit), 3 uploaded
+    finally:
+        B.lora_destroy(ctx)
+
+
 def test_serve_step_no_slot_releases_its_group(lib):
     """Every slot in flight elsewhere: the first admission of the step fails
     with NO_SLOT, the step's own references are released, the epoch stays."""
