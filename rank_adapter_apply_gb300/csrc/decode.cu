@@ -49,9 +49,10 @@ __device__ __forceinline__ void store_vfrag(float *v, int VS, int pos, int k, fl
 
 // Sum the chunk partials of one tile in chunk order and write v (last CTA
 // only): ranks below `kr` of each row, as fp32 or (frag) in the bf16
-// fragment order. Loads of eight chunks are issued before they are added
-// (the sum keeps the chunk order), so a 14-way split costs two L2 round
-// trips, not fourteen.
+// fragment order. Partial rows hold R ranks; ranks from R up to kr (the rest
+// of the last 16-rank block, frag only) are written as zeros. Loads of eight
+// chunks are issued before they are added (the sum keeps the chunk order), so
+// a 14-way split costs two L2 round trips, not fourteen.
 __device__ void finish_split(const LayerArgs &L, const GroupView &g, int tile_i, int p0, int cnt,
                              int kr, bool frag) {
     __shared__ int last;
@@ -74,7 +75,7 @@ __device__ void finish_split(const LayerArgs &L, const GroupView &g, int tile_i,
         const int pos = p0 + e / kr, k = e % kr;
         const float *src = L.part + (size_t)pos * R + k;
         float s = 0.f;
-        int ch = 0;
+        int ch = k < R ? 0 : L.n_chunks;
         for (; ch + 8 <= L.n_chunks; ch += 8) {
             float a[8];
 #pragma unroll
@@ -219,6 +220,8 @@ __device__ __forceinline__ void shrink_bf16_tile(const LayerArgs &L, const Group
     __syncthreads();
     // ranks r .. 16 nmb - 1 come out as exact zeros (their A rows are
     // masked) and are written too: the expand reads whole 16-rank blocks
+    // (v rows hold whole blocks; a partial row holds R ranks, so ranks past
+    // R are left to finish_split)
     const bool split = L.n_chunks > 1;
     float *part = L.part + (size_t)chunk * g.T * R;
     for (int e = threadIdx.x; e < nmb * 256; e += kThreads) {
@@ -228,8 +231,8 @@ __device__ __forceinline__ void shrink_bf16_tile(const LayerArgs &L, const Group
         const int k = m * 16 + (ln >> 2) + ((j & 2) ? 8 : 0);
         const int tk = n * 8 + 2 * (ln & 3) + (j & 1);
         if (tk < cnt) {
-            if (split) part[(size_t)(p0 + tk) * R + k] = v;
-            else store_vfrag(L.v, v_stride(R), p0 + tk, k, v);
+            if (!split) store_vfrag(L.v, v_stride(R), p0 + tk, k, v);
+            else if (k < R) part[(size_t)(p0 + tk) * R + k] = v;
         }
     }
     if (split) finish_split(L, g, tile_i, p0, cnt, 16 * nmb, true);

@@ -223,6 +223,29 @@ def test_max_rank_64_mixed(small_batch):
     check_layer(w, "l0", out["l0"])
 
 
+@pytest.mark.parametrize("small_batch", [0, 1024])
+@pytest.mark.parametrize("R", [8, 24, 56])
+def test_bf16_max_ranks_between_block_sizes(R, small_batch):
+    """bf16 max_lora_rank 8, 24 and 56: B pools in blocks of 8 ranks, decode
+    rows padded to whole 16-rank blocks, and (cluster kernel) MMA rank blocks
+    of 16, 32 and 64 that reach past max_lora_rank; slot ranks from 1 to R on
+    the grouped kernels (small_batch 0, d_in split into 5-9 chunks whose
+    partial rows hold R ranks) and on the cluster kernel. d_in 2048 takes the
+    grouped shrink's loop for whole 32-column steps, 2056 the other one."""
+    T = 75
+    rng = np.random.default_rng(R * 7 + small_batch)
+    ranks = [R, max(1, R // 2), 1, max(1, R - 3), 5]
+    idx = rng.integers(-1, 5, size=T)
+    d_in = {8: 2056, 24: 2048, 56: 2056}[R]
+    w = _custom(T, d_in, 392, 5, R, ranks, idx, seed=R + 11)
+    out, st = _run(w, small_batch_tokens=small_batch)
+    check_layer(w, "l0", out["l0"])
+    if small_batch:
+        assert st["cluster_applies"] >= 1 and st["grouped_applies"] == 0
+    else:
+        assert st["cluster_applies"] == 0 and st["grouped_applies"] >= 1
+
+
 @pytest.mark.parametrize("R", [256, 200])
 def test_fp32_largest_ranks(R):
     """fp32 takes max_lora_rank up to 256: the grouped kernels at 256 (B in
