@@ -49,10 +49,10 @@ __device__ __forceinline__ void store_vfrag(float *v, int VS, int pos, int k, fl
 
 // Sum the chunk partials of one tile in chunk order and write v (last CTA
 // only): ranks below `kr` of each row, as fp32 or (frag) in the bf16
-// fragment order. Partial rows hold R ranks; ranks from R up to kr (the rest
-// of the last 16-rank block, frag only) are written as zeros. Loads of eight
-// chunks are issued before they are added (the sum keeps the chunk order), so
-// a 14-way split costs two L2 round trips, not fourteen.
+// fragment order. A partial row is v_stride(R) floats long (whole 16-rank
+// blocks, like the rows of v). Loads of eight chunks are issued before they
+// are added (the sum keeps the chunk order), so a 14-way split costs two L2
+// round trips, not fourteen.
 __device__ void finish_split(const LayerArgs &L, const GroupView &g, int tile_i, int p0, int cnt,
                              int kr, bool frag) {
     __shared__ int last;
@@ -69,13 +69,13 @@ __device__ void finish_split(const LayerArgs &L, const GroupView &g, int tile_i,
     }
     __syncthreads();
     if (!last) return;
-    const int R = g.R, T = g.T;
-    const size_t cs = (size_t)T * R;
+    const int R = g.R, T = g.T, PS = v_stride(R);
+    const size_t cs = (size_t)T * PS;
     for (int e = threadIdx.x; e < cnt * kr; e += kThreads) {
         const int pos = p0 + e / kr, k = e % kr;
-        const float *src = L.part + (size_t)pos * R + k;
+        const float *src = L.part + (size_t)pos * PS + k;
         float s = 0.f;
-        int ch = k < R ? 0 : L.n_chunks;
+        int ch = 0;
         for (; ch + 8 <= L.n_chunks; ch += 8) {
             float a[8];
 #pragma unroll
@@ -220,10 +220,10 @@ __device__ __forceinline__ void shrink_bf16_tile(const LayerArgs &L, const Group
     __syncthreads();
     // ranks r .. 16 nmb - 1 come out as exact zeros (their A rows are
     // masked) and are written too: the expand reads whole 16-rank blocks
-    // (v rows hold whole blocks; a partial row holds R ranks, so ranks past
-    // R are left to finish_split)
+    // (rows of v and of the partials hold whole blocks)
     const bool split = L.n_chunks > 1;
-    float *part = L.part + (size_t)chunk * g.T * R;
+    const int PS = v_stride(R);
+    float *part = L.part + (size_t)chunk * g.T * PS;
     for (int e = threadIdx.x; e < nmb * 256; e += kThreads) {
         const int ln = e & 31, slot_j = e >> 5;          // slot_j = (m*2+n)*4 + j
         const int j = slot_j & 3, n = (slot_j >> 2) & 1, m = slot_j >> 3;
@@ -231,8 +231,8 @@ __device__ __forceinline__ void shrink_bf16_tile(const LayerArgs &L, const Group
         const int k = m * 16 + (ln >> 2) + ((j & 2) ? 8 : 0);
         const int tk = n * 8 + 2 * (ln & 3) + (j & 1);
         if (tk < cnt) {
-            if (!split) store_vfrag(L.v, v_stride(R), p0 + tk, k, v);
-            else if (k < R) part[(size_t)(p0 + tk) * R + k] = v;
+            if (split) part[(size_t)(p0 + tk) * PS + k] = v;
+            else store_vfrag(L.v, v_stride(R), p0 + tk, k, v);
         }
     }
     if (split) finish_split(L, g, tile_i, p0, cnt, 16 * nmb, true);
@@ -430,7 +430,9 @@ __device__ __forceinline__ void shrink_f32_tile(const LayerArgs &L, const GroupV
     const float *As = static_cast<const float *>(L.A) + (size_t)s * R * d_in;
     const int c0 = chunk * L.chunk_cols;
     const int c1 = min(d_in, c0 + L.chunk_cols);
-    float *dst_base = L.n_chunks == 1 ? L.v : L.part + (size_t)chunk * g.T * R;
+    // v rows hold R floats, partial rows v_stride(R)
+    const int ds = L.n_chunks == 1 ? R : v_stride(R);
+    float *dst_base = L.n_chunks == 1 ? L.v : L.part + (size_t)chunk * g.T * ds;
     for (int i = warp; i < cnt; i += kWarps) {
         const float *xr = x + (size_t)g.perm[p0 + i] * d_in;
         for (int k = 0; k < r; ++k) {
@@ -439,7 +441,7 @@ __device__ __forceinline__ void shrink_f32_tile(const LayerArgs &L, const GroupV
             for (int c = c0 + lane; c < c1; c += 32) a = fmaf(ar[c], xr[c], a);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-            if (lane == 0) dst_base[(size_t)(p0 + i) * R + k] = a;
+            if (lane == 0) dst_base[(size_t)(p0 + i) * ds + k] = a;
         }
     }
     if (L.n_chunks > 1) finish_split(L, g, tile_i, p0, cnt, r, false);

@@ -124,7 +124,7 @@ struct LayerArgs {
     const void *A;       // pool base [S][R][d_in]
     const void *B;       // pool base [S][d_out][R]
     float *v;            // [T][R] fp32 rank-r intermediates, by grouped position
-    float *part;         // [n_chunks * T][R] split partials
+    float *part;         // split partials: chunk c, row t at (c * T + t) * v_stride(R)
     int *counters;       // [max_tiles] arrival counters (self-resetting)
     int d_in, d_out;
     int n_chunks, chunk_cols;

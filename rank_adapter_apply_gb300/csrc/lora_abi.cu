@@ -730,7 +730,10 @@ int apply_impl(lora_ctx *c, int n, const int *layers, const void *const *xs, voi
         const int by_bytes = (int)((size_t)(kTileTokens + c->R) * L.d_in * e / (8 * 2 * kTileTokens * 4 * (size_t)c->R));
         if (chunks > by_bytes) chunks = by_bytes;
         if (chunks > kMaxChunks) chunks = kMaxChunks;
-        if (chunks > c->lay.part_rows / T) chunks = c->lay.part_rows / T;
+        // a layer's partials hold part_rows rows of R floats; the decode
+        // kernels' partial rows are v_stride(R) floats
+        const long long max_split = (long long)c->lay.part_rows * c->R / ((long long)T * v_stride(c->R));
+        if (chunks > max_split) chunks = (int)max_split;
         if (chunks < 1) chunks = 1;
         int cols = (L.d_in + chunks - 1) / chunks;
         cols = (cols + 127) / 128 * 128;

@@ -130,7 +130,9 @@ extern "C" int lora_apply_static_scratch(const void *x, void *y, const int32_t *
     a.counters = reinterpret_cast<int *>(scratch + lay.counters);
     int chunks = (2 * num_sms + est_tiles - 1) / est_tiles;
     if (chunks > kMaxChunks) chunks = kMaxChunks;
-    if (chunks > lay.part_rows / T) chunks = lay.part_rows / T;
+    // partial rows of v_stride(R) floats in part_rows rows of R floats
+    const long long max_split = (long long)lay.part_rows * max_lora_rank / ((long long)T * v_stride(max_lora_rank));
+    if (chunks > max_split) chunks = (int)max_split;
     if (chunks < 1) chunks = 1;
     int cols = ((d_in + chunks - 1) / chunks + 127) / 128 * 128;
     a.chunk_cols = cols;
