@@ -677,6 +677,62 @@ def test_serve_step_rejects_before_any_admission(lib):
         B.lora_destroy(ctx)
 
 
+@pytest.mark.parametrize("seed", range(8))
+def test_serve_step_random_steps_match_simulator(lib, seed):
+    """Random serving steps on 2-8 slots: ids from a small pool with base-model
+    tokens mixed in, often more distinct adapters than slots (several groups
+    per step), a warm set of up to max_loras - 1 adapters, LRU or keep_score.
+    Every step succeeds, and every admission equals the simulator's replay of
+    the groups that churn.plan_groups cuts (the warm adapters pinned as they
+    are bound)."""
+    from oracle.lru_sim import KEEP_SCORE, LRU
+    from rank_adapter_apply_gb300 import churn
+    rng = np.random.default_rng(1000 + seed)
+    S, R = int(rng.integers(2, 9)), 16
+    n_ad = int(rng.integers(S + 2, 4 * S + 3))
+    ranks = [int(r) for r in rng.integers(1, R + 1, size=n_ad)]
+    warm = set(int(a) for a in rng.choice(n_ad, size=int(rng.integers(0, S)), replace=False))
+    policy = LRU if seed % 2 == 0 else KEEP_SCORE
+    weights = (1.0, 1.0, 0.5, 0.25, 0.75)
+    ctx = _host_ctx(S, R)
+    sim = LruSlotSim(S, R)
+    sim.policy = policy
+    sim.weights = weights
+    try:
+        B.lora_set_policy(ctx, policy)
+        B.lora_set_keep_score_weights(ctx, weights)
+        B.lora_register_host_adapters(ctx, list(range(n_ad)), ranks, [2.0 * r for r in ranks])
+        B.lora_set_warm_set(ctx, sorted(warm))
+        pinned = {}
+        for k in range(25):
+            T = int(rng.integers(1, 3 * S + 4))
+            ids = [B.NO_ID if rng.random() < 0.15 else int(rng.integers(0, n_ad)) for _ in range(T)]
+            rc, dec, ng = _serve(ctx, ids)
+            assert rc == 0, (seed, k, B.last_error())
+            order = list(dict.fromkeys(a for a in ids if a != B.NO_ID))
+            groups = churn.plan_groups(order, pinned, S - len(pinned), warm)
+            exp = []
+            for group in groups:
+                held = []
+                for a in group:
+                    st, slot, need, ev = sim.assign(a, ranks[a])
+                    assert st == 0, (seed, k, a)
+                    exp.append((a, slot, need, ev))
+                    if a in warm and a not in pinned:
+                        sim.pin(slot)
+                        pinned[a] = slot
+                    sim.acquire(slot)
+                    held.append(slot)
+                for s_ in held:
+                    sim.release(s_)
+            sim.tick()
+            assert dec == exp and ng == len(groups), (seed, k, dec, exp)
+        st = B.lora_stats(ctx)
+        assert (st["hits"], st["misses"], st["evictions"]) == (sim.hits, sim.misses, sim.evictions)
+    finally:
+        B.lora_destroy(ctx)
+
+
 def test_serve_step_failed_admission_uploads_the_bound_misses(lib):
     """A group whose second admission fails: the miss bound before it is still
     uploaded (its slot is loaded, so lora_abort_load refuses it and a later
