@@ -158,3 +158,19 @@ def test_static_scratch_near_its_limit():
     with pytest.raises(B.LoraError) as ei:
         _static_only(_near_limit(8100), "l0", calls=1)
     assert ei.value.code == B.LORA_ERR_ARG
+
+
+@pytest.mark.parametrize("dtype,R,d_in", [(wl.DTYPE_BF16, 24, 2048), (wl.DTYPE_BF16, 8, 2056),
+                                          (wl.DTYPE_F32, 40, 1100)])
+def test_static_scratch_ranks_between_block_sizes(dtype, R, d_in):
+    """max_lora_rank not a multiple of 16 with d_in split into chunks: the
+    static array's partial rows are whole 16-rank blocks long, so the split is
+    capped at what its rows of R floats hold; sampled against the oracle."""
+    from tests.test_gpu_parity import _custom
+    T = 75
+    rng = np.random.default_rng(R + d_in)
+    ranks = [R, max(1, R // 2), 1, max(1, R - 3), 5]
+    idx = rng.integers(-1, 5, size=T)
+    w = _custom(T, d_in, 392, 5, R, ranks, idx, dtype=dtype, seed=R)
+    for got in _static_only(w, "l0"):
+        check_layer(w, "l0", got)
